@@ -19,7 +19,8 @@
  * Readings where the pages are silent (all listed in the design notes):
  *  - quantizer arithmetic is fp32 after widening the fp16 inputs;
  *  - scale is stored as fp32, zero as fp16 (lossless: zero is an fp16 input);
- *  - a zero of -0.0 is stored as +0.0;
+ *  - min and max of -0.0 are taken as +0.0, so the stored zero and scale
+ *    never carry a negative sign whatever order equal values are met in;
  *  - max == min gives scale 0, every code 0, recon == min;
  *  - codes are packed along D inside each token row, low bits first;
  *  - the decode reads store tokens as their fp32 reconstruction.
@@ -138,7 +139,8 @@ void orc_quantize_group(const float* v, int n, int bits,
         if (v[i] < mn) mn = v[i];
         if (v[i] > mx) mx = v[i];
     }
-    mn = mn + 0.0f;                          /* -0.0 -> +0.0 */
+    mn = mn + 0.0f;                          /* -0.0 -> +0.0: canonical zero */
+    mx = mx + 0.0f;                          /* and canonical range sign */
     float levels = (float)((1 << bits) - 1); /* 2^bits - 1 */
     float range = mx - mn;
     float s = range / levels;

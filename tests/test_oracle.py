@@ -70,6 +70,7 @@ def test_golden_group(line):
     assert c.tolist() == [int(v) for v in codes.split()], name
     assert s == np.float32(float(scale)) and z == np.float32(float(zero)), name
     assert np.signbit(z) == np.signbit(np.float32(float(zero))), name
+    assert np.signbit(s) == np.signbit(np.float32(float(scale))), name
     # the recon of the same group through the key store path
     G = x.size
     store = oracle.Store(0, 1, G, 4 if bits == 2 else 2, G, bits)
@@ -228,6 +229,7 @@ def torch_eight_ops(x16: np.ndarray, G: int, bits: int, axis: int):
         mn = xg.amin(dim=3, keepdim=True)
         mx = xg.amax(dim=3, keepdim=True)
     mn = mn + 0.0
+    mx = mx + 0.0
     s = (mx - mn) / L
     q = torch.round((xg - mn) / s).clamp(0, L)
     q = torch.where(s == 0, torch.zeros_like(q), q)

@@ -24,6 +24,7 @@ MUTANTS = {
                     "float prod = 0.0f; (void)prod;\n    float out = fmaf((float)q, s, z);"),
     "zero_padding": ("buf[i] = real[n_real - 1];", "buf[i] = 0.0f;"),
     "no_signed_zero_fix": ("mn = mn + 0.0f;", ";"),
+    "no_signed_zero_fix_max": ("mx = mx + 0.0f;", ";"),
     "reciprocal_multiply": ("float t = a / s;", "float t = a * (1.0f / s);"),
     "pack_high_bits_first": ("(bit % 8)", "(8 - bits - bit % 8)"),
     "key_meta_ignores_s_off": ("((long)bh * ng_cap + (s_off / G + g)) * D + d",
