@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""KIVI hot-path benchmark on GB300.
+
+One step = one pass of the whole hot path over one batch of the Qwen3-8B-like
+single-layer workload (B=1, H_kv=8, 32 query heads, D=128, 2238-token prompt,
+4-bit, G=32, residual_length=128):
+  1. flush the oldest 2080 tokens of K and V into the packed store (one launch),
+  2. append the 158-token fp16 tail to the K and V residual windows,
+  3. dequantize the packed K and V stores back to fp16,
+  4. fused dequantize-and-attend decode of one query token per head (split over
+     the cached tokens + log-sum-exp combine).
+value = algorithmic HBM bytes of the step / device time per step (GB/s).
+
+Inputs rotate through a pool of independent instances whose total size is
+several times the L2 cache, so no step finds its inputs in L2. Each instance's
+step is captured once in a CUDA graph (timing events between the ops), and the
+timed region replays K graphs back to back between two CUDA events.
+
+--impl reference times the plain CPU oracle on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KIVI flush/dequant/decode-attend HBM GB/s (% of peak); decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--workload", default="qwen8b", choices=["tiny", "qwen8b", "long2bit"])
+    p.add_argument("--pool", type=int, default=0, help="instances in the rotating pool (0 = auto)")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workload accounting
+# ---------------------------------------------------------------------------
+
+def op_bytes(w, n_flush: int, n_res: int) -> dict:
+    """Algorithmic HBM bytes per step, per op (each tensor read or written once)."""
+    el = w.BH * n_flush * w.D                     # flushed elements per tensor
+    packed = w.bits / 8 + 6 / w.G                 # code bits + 4 B scale + 2 B zero per group
+    flush = 2 * el * (2 + packed)                 # K and V: read fp16, write codes + metadata
+    dequant = 2 * el * (packed + 2)               # read codes + metadata, write fp16
+    append = 2 * 2 * w.BH * n_res * w.D * 2       # K and V tail rows: read + write
+    # decode: per (kv head, store token) K+V codes + key metadata (6 B per channel
+    # per 32 tokens) + value metadata (6 B per 32-channel group)
+    per_tok = 2 * w.D * w.bits / 8 + w.D * 6 / w.G + (w.D // w.G) * 6
+    decode = (w.BH * n_flush * per_tok + w.BH * n_res * w.D * 2 * 2
+              + w.B * w.Hq * w.D * 2 + w.B * w.Hq * w.D * 4)
+    return {"flush_kv": flush, "residual_append": append, "dequant_kv": dequant, "decode_attend": decode}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def read_traffic(kernel_file: str, op: str):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel source
+    is unchanged since (profiles/traffic.txt lines: op sha256 bytes)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "kivi_kv_cache_gb300", "csrc", kernel_file)
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for ln in open(path):
+            parts = ln.split()
+            if len(parts) >= 3 and not ln.startswith("#") and parts[0] == op and parts[1] == sha:
+                return float(parts[2])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", self.gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GB300 arm
+# ---------------------------------------------------------------------------
+
+class Instance:
+    """Device buffers of one independent copy of the workload."""
+
+    def __init__(self, w, seed, device, kv, synth):
+        import torch
+        self.kv = kv
+        self.w = w
+        self.k, self.v, self.q = synth.prefill_inputs_torch(w, seed, device)
+        self.n_flush = kv.kivi_flush_count(w.S, w.R, w.G)
+        self.n_res = w.S - self.n_flush
+        self.res_cap = w.R + w.G
+        self.kst = kv.KiviStore(0, w.BH, self.n_flush, w.D, w.G, w.bits, device=device)
+        self.vst = kv.KiviStore(1, w.BH, self.n_flush, w.D, w.G, w.bits, device=device)
+        self.kres = torch.zeros((w.BH, self.res_cap, w.D), dtype=torch.float16, device=device)
+        self.vres = torch.zeros_like(self.kres)
+        self.kdq = torch.empty((w.BH, self.n_flush, w.D), dtype=torch.float16, device=device)
+        self.vdq = torch.empty_like(self.kdq)
+        self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=device)
+        need = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, self.n_flush, self.n_res, w.D)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+
+    def step(self, ev=None):
+        kv, w = self.kv, self.w
+        if ev is not None:
+            ev[0].record()
+        kv.kivi_flush_kv(self.k, self.v, w.R, self.kst, self.vst)
+        if ev is not None:
+            ev[1].record()
+        kv.kivi_residual_append(self.k[:, self.n_flush:], self.kres, 0, self.n_res)
+        kv.kivi_residual_append(self.v[:, self.n_flush:], self.vres, 0, self.n_res)
+        if ev is not None:
+            ev[2].record()
+        kv.kivi_dequant(self.kst, self.n_flush, out=self.kdq)
+        kv.kivi_dequant(self.vst, self.n_flush, out=self.vdq)
+        if ev is not None:
+            ev[3].record()
+        kv.kivi_decode_attend(self.q, self.kst, self.vst, self.n_flush, self.kres, self.vres, self.n_res,
+                              w.Hkv, w.sm_scale, out=self.out, workspace=self.ws)
+        if ev is not None:
+            ev[4].record()
+
+    def nbytes(self):
+        ts = [self.k, self.v, self.q, self.kres, self.vres, self.kdq, self.vdq, self.out, self.ws,
+              self.kst.codes, self.kst.scale, self.kst.zero, self.vst.codes, self.vst.scale, self.vst.zero]
+        return sum(t.numel() * t.element_size() for t in ts)
+
+
+OPS = ["flush_kv", "residual_append", "dequant_kv", "decode_attend"]
+OP_KERNEL_FILE = {"flush_kv": "flush.cu", "residual_append": "residual.cu", "dequant_kv": "dequant.cu",
+                  "decode_attend": "decode.cu"}
+LAUNCHES = {"flush_kv": 1, "residual_append": 2, "dequant_kv": 2}
+
+
+def run_gb300(args, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import kivi_kv_cache_gb300 as kv
+    from kivi_kv_cache_gb300 import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+
+    probe = Instance(w, 1000 * rank + 0, dev, kv, synth)
+    inst_bytes = probe.nbytes()
+    pool = args.pool or int(min(64, max(2, math.ceil(4 * l2 / inst_bytes))))
+    insts = [probe] + [Instance(w, 1000 * rank + i, dev, kv, synth) for i in range(1, pool)]
+    n_split = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, probe.n_flush, probe.n_res, w.D)
+    decode_launches = 2 if n_split > 0 else 1
+    launches_per_step = sum(LAUNCHES.values()) + decode_launches
+
+    # eager warm-up, then one graph per instance with timing events between ops
+    for i in range(max(1, args.warmup)):
+        insts[i % pool].step()
+    torch.cuda.synchronize()
+    use_events = True
+    graphs, events = [], []
+    try:
+        for inst in insts:
+            ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                inst.step(ev)
+            graphs.append(g)
+            events.append(ev)
+    except Exception:
+        use_events = False
+        graphs, events = [], []
+        for inst in insts:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                inst.step()
+            graphs.append(g)
+    for i in range(args.warmup):
+        graphs[i % pool].replay()
+    torch.cuda.synchronize()
+
+    gpu_id = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local_rank)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(args.steps):
+        graphs[i % pool].replay()
+    end.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock = clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # per-op durations: the events of each graph hold its last replay in the timed region
+    op_ms = {}
+    if use_events and args.steps >= pool:
+        for j, op in enumerate(OPS):
+            op_ms[op] = statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in events)
+    else:
+        for j, op in enumerate(OPS):  # eager fallback: time each op alone, same rotation
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(pool)]
+            for i in range(pool):
+                insts[i].step(ev[i])
+            torch.cuda.synchronize()
+            op_ms[op] = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
+
+    ob = op_bytes(w, probe.n_flush, probe.n_res)
+    step_bytes = sum(ob.values())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    ops = {}
+    for op in OPS:
+        gbs = ob[op] / (op_ms[op] * 1e-3) / 1e9
+        ops[op] = {"us": round(op_ms[op] * 1e3, 3), "bytes": int(ob[op]), "GB/s": round(gbs, 1),
+                   "frac_of_peak": round(gbs / peak, 4)}
+    dom = max(OPS, key=lambda o: op_ms[o])
+    achieved = ob[dom] / (op_ms[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": peak_kind + " hbm_gbs (copy, burst)", "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": read_traffic(OP_KERNEL_FILE[dom], dom)}
+
+    # end to end: host inputs (pinned) -> device, the step, result -> host
+    e2e = None
+    if args.e2e_steps > 0:
+        hk = [insts[i].k.cpu().pin_memory() for i in range(min(pool, 4))]
+        hv = [insts[i].v.cpu().pin_memory() for i in range(min(pool, 4))]
+        hq = [insts[i].q.cpu().pin_memory() for i in range(min(pool, 4))]
+        hout = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32).pin_memory()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for i in range(args.e2e_steps):
+            inst = insts[i % pool]
+            h = i % len(hk)
+            inst.k.copy_(hk[h], non_blocking=True)
+            inst.v.copy_(hv[h], non_blocking=True)
+            inst.q.copy_(hq[h], non_blocking=True)
+            inst.step()
+            hout.copy_(inst.out, non_blocking=True)
+        s1.record()
+        torch.cuda.synchronize()
+        e2e_ms = s0.elapsed_time(s1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(t.numel() * t.element_size() for t in (hk[0], hv[0], hq[0]))
+        e2e = {"value": round(world * step_bytes * args.e2e_steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 4),
+               "ms_per_step": round(e2e_ms / args.e2e_steps, 5)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle(w, args.cpu_seconds)
+
+    decode_s = op_ms["decode_attend"] * 1e-3
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "%s: single-layer prefill flush + residual append + dequant + decode "
+                               "(B=%d, H_kv=%d, Hq=%d, D=%d, S=%d, bits=%d, G=%d, residual_length=%d)"
+                               % (w.name, w.B, w.Hkv, w.Hq, w.D, w.S, w.bits, w.G, w.R),
+                   "n_flush": probe.n_flush, "n_res": probe.n_res,
+                   "l2": "rotating pool of %d independent instances, %.0f MB total (L2 %d MB)"
+                         % (pool, pool * inst_bytes / 2 ** 20, l2 >> 20),
+                   "timing": "CUDA graph per instance, K replays between CUDA events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "ops": ops,
+        "decode_tokens_per_s": round(w.B / decode_s, 1),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clock,
+        "peak_hbm_gbs": peak,
+        "per_op_timing": "graph events (last replay of each instance)" if use_events else "eager events",
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def cpu_oracle_step(w, k, v, q, threads):
+    """One step of the workload on the CPU oracle, one KV head per thread."""
+    import numpy as np
+
+    import oracle
+    n = oracle.flush_count(w.S, w.R, w.G)
+    n_res = w.S - n
+    gq = w.Hq // w.Hkv
+
+    def head(bh):
+        b, hk = divmod(bh, w.Hkv)
+        ks = oracle.Store(0, 1, n, w.D, w.G, w.bits)
+        vs = oracle.Store(1, 1, n, w.D, w.G, w.bits)
+        oracle.flush(0, k[bh:bh + 1], n, ks)
+        oracle.flush(1, v[bh:bh + 1], n, vs)
+        kres = np.zeros((1, w.R + w.G, w.D), np.float16)
+        vres = np.zeros_like(kres)
+        oracle.residual_append(kres, 0, np.ascontiguousarray(k[bh:bh + 1, n:]), n_res)
+        oracle.residual_append(vres, 0, np.ascontiguousarray(v[bh:bh + 1, n:]), n_res)
+        oracle.dequant(ks, n)
+        oracle.dequant(vs, n)
+        qh = np.ascontiguousarray(q[b:b + 1, hk * gq:(hk + 1) * gq])
+        return oracle.decode_attend(qh, ks, vs, n, kres, vres, n_res, 1, w.sm_scale)
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(head, range(w.BH)))
+
+
+def cpu_oracle(w, seconds, steps=None):
+    """Time the oracle on host cores: whole steps until `seconds` (or `steps`)."""
+    from kivi_kv_cache_gb300 import synth
+    import oracle
+    oracle.build()
+    k, v, q = synth.prefill_inputs(w)
+    threads = max(1, min(os.cpu_count() or 1, w.BH))
+    cpu_oracle_step(w, k, v, q, threads)  # warm (page in, build)
+    n = oracle.flush_count(w.S, w.R, w.G)
+    step_bytes = sum(op_bytes(w, n, w.S - n).values())
+    done, t0 = 0, time.perf_counter()
+    times = []
+    while True:
+        t = time.perf_counter()
+        cpu_oracle_step(w, k, v, q, threads)
+        times.append(time.perf_counter() - t)
+        done += 1
+        if (steps is not None and done >= steps) or (steps is None and time.perf_counter() - t0 >= seconds):
+            break
+    total = sum(times)
+    return {"value": round(step_bytes * done / total / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d whole steps of the %s workload (C oracle, one KV head per thread), %.1f s"
+                      % (done, w.name, total),
+            "ms_per_step": round(1e3 * total / done, 3)}
+
+
+def run_reference(args, rank, world):
+    from kivi_kv_cache_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    import oracle
+    oracle.build()
+    k, v, q = synth.prefill_inputs(w)
+    threads = max(1, min(os.cpu_count() or 1, w.BH))
+    for _ in range(max(0, args.warmup)):
+        cpu_oracle_step(w, k, v, q, threads)
+    steps = max(1, args.steps)
+    # keep the reference arm to a bounded number of whole steps
+    t = time.perf_counter()
+    cpu_oracle_step(w, k, v, q, threads)
+    one = time.perf_counter() - t
+    steps = max(1, min(steps, int(120.0 / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        cpu_oracle_step(w, k, v, q, threads)
+    el = time.perf_counter() - t0
+    n = oracle.flush_count(w.S, w.R, w.G)
+    step_bytes = sum(op_bytes(w, n, w.S - n).values())
+    value = step_bytes * steps / el / 1e9
+    sample = "%d whole steps of the %s workload (C oracle, one KV head per thread)" % (steps, w.name)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * el / steps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "note": "plain C CPU oracle as the reference arm"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl")
+    line = run_gb300(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * kivi.h -- C ABI of the GB300 (sm_103a) KIVI KV-cache library, libkivi_gb300.so.
+ *
+ * KIVI keeps a KV cache as asymmetric min/max 2- or 4-bit codes: keys are
+ * quantized per channel (each group runs along the token axis), values per
+ * token (each group runs along head_dim), and the newest residual_length
+ * tokens stay in fp16. This library implements, as hand-written CUDA kernels:
+ *   - the flush (quantize + bit-pack) of keys and of values,
+ *   - the dequantize of the packed store back to fp16,
+ *   - the fp16 residual window's append / compact,
+ *   - a fused dequantize-and-attend single-token decode over the packed store
+ *     plus the residual window (split over the cached tokens, then a
+ *     log-sum-exp combine pass).
+ *
+ * Sources (page title, section):
+ *   [F] VeloxQuant-MLX blog, "A 5.65x Metal Kernel That Made My LLM Exactly 0%
+ *       Faster" -- the fused KIVI post.
+ *   [Q] VeloxQuant-MLX blog, "A Kernel That Wasn't There" (Qwen3-8B on M4).
+ *   [R] VeloxQuant-MLX benchmarks page, "KV-Cache Kernel Roofline".
+ *
+ * Conventions shared by every entry point
+ *   - Ownership: the caller owns every buffer. The library never allocates
+ *     device memory and keeps no state between calls (it caches the device's
+ *     SM count per device for the split heuristic).
+ *   - Pointers: device pointers (CUDA global memory), 16-byte aligned, unless
+ *     stated otherwise. Scalars and *_out arguments are host values/pointers.
+ *   - Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL
+ *     is the legacy default stream). Results are ready when the stream is.
+ *   - Errors: argument checks happen on the host before any launch; a failed
+ *     check returns its status and launches nothing. A launch failure returns
+ *     KIVI_ERR_CUDA (from cudaGetLastError). No call aborts, throws, traps or
+ *     spins on the device.
+ *   - Numbers: fp16 is IEEE binary16 passed as raw 16-bit words. Inputs must
+ *     be finite; NaN/Inf inputs give unspecified codes but every access stays
+ *     in bounds.
+ *   - Supported shapes: head_dim D = 128, group_size G = 32, bits in {2, 4}.
+ *     Other values return KIVI_ERR_UNSUPPORTED.
+ *
+ * Store layout (one store per tensor, keys and values separately):
+ *   codes  uint8   [BH, s_cap, D*bits/8]  codes packed along D inside each
+ *                                          token row, element i at bit offset
+ *                                          i*bits, low bits first
+ *   keys:   scale float32 [BH, s_cap/G, D]  zero fp16 [BH, s_cap/G, D]
+ *   values: scale float32 [BH, s_cap, D/G]  zero fp16 [BH, s_cap, D/G]
+ * with s_cap (the store's token capacity) a multiple of G. zero is the group
+ * minimum (an fp16 input, so fp16 storage is lossless); scale is the fp32
+ * value the codes were computed with.
+ */
+#ifndef KIVI_GB300_H
+#define KIVI_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* kivi_stream_t;
+
+typedef enum {
+    KIVI_OK = 0,
+    KIVI_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad offset/capacity */
+    KIVI_ERR_UNSUPPORTED = 2,  /* D, G, bits or Hq/Hkv outside the compiled set */
+    KIVI_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    KIVI_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    KIVI_ERR_ALIGNMENT = 5     /* a pointer is not 16-byte aligned */
+} kivi_status;
+
+typedef enum { KIVI_AXIS_KEYS = 0, KIVI_AXIS_VALUES = 1 } kivi_axis;
+
+/* Human-readable name of a status. Never NULL; host only. */
+const char* kivi_status_string(kivi_status status);
+
+/* Library ABI version (major*100 + minor). */
+int kivi_version(void);
+
+/*
+ * Flush plan ([F] "What we're actually optimizing": the newest
+ * residual_length tokens stay fp16 and fresh tokens are quantized in a batch
+ * once enough accumulate). Given a residual window holding n_res tokens,
+ * returns how many of its oldest tokens to flush:
+ *   residual_length == 0  -> n_res (quantize everything, ragged tail allowed)
+ *   n_res - R <  G        -> 0
+ *   otherwise             -> floor((n_res - R) / G) * G
+ * so that afterwards R <= n_res < R + G. This reproduces the flush counts
+ * printed in [F] "The full end-to-end record" (559 -> 512, 2059 -> 2016,
+ * 8209 -> 8160 at R = G = 32 with 2048-token prefill chunks). Host only;
+ * returns -1 for negative n_res, negative R or G <= 0.
+ */
+int kivi_flush_count(int n_res, int residual_length, int group_size);
+
+/*
+ * Key flush ([F] "The layout problem that shapes everything", "Kernel A",
+ * "Three ways to be off by one bit"). x is fp16 [BH, S, D] row-major with
+ * x_bh_stride tokens between consecutive heads (x_bh_stride >= S; pass S for a
+ * dense tensor, or the capacity of a larger cache to flush a view of it).
+ * n_flush = kivi_flush_count(S, residual_length, group_size) of the oldest
+ * tokens [0, n_flush) are quantized per channel in groups of G consecutive
+ * tokens (a ragged last group, possible only when residual_length == 0, uses
+ * min/max over its real tokens):
+ *     zero = min, scale = RN32(RN32(max - min) / (2^bits - 1)),
+ *     q = clamp(rint(RN32(RN32(x - zero) / scale)), 0, 2^bits - 1)
+ * (IEEE fp32 division, round half to even; scale == 0 gives q = 0), and
+ * written at store token offset s_off (a multiple of G) of a key store of
+ * capacity s_cap: codes[BH, s_cap, D*bits/8], scale f32 / zero fp16
+ * [BH, s_cap/G, D]. Bit-exact with the CPU oracle.
+ * *n_flushed (host pointer, may be NULL) receives n_flush.
+ * Errors: INVALID_ARG if S < 0, BH <= 0, x_bh_stride < S, s_cap % G != 0,
+ * s_off % G != 0 or s_off + n_flush > s_cap; ALIGNMENT if a pointer is not
+ * 16-byte aligned. n_flush == 0 returns KIVI_OK without a launch.
+ */
+kivi_status kivi_flush_keys(const void* x_f16, int BH, int S, int x_bh_stride, int D,
+                            int group_size, int bits, int residual_length,
+                            void* codes_u8, float* scale, void* zero_f16,
+                            int s_off, int s_cap, int* n_flushed, kivi_stream_t stream);
+
+/*
+ * Value flush ([F] "The layout problem", "Kernel B"): as kivi_flush_keys,
+ * but each group is G consecutive channels of one token; scale f32 and zero
+ * fp16 are [BH, s_cap, D/G]. s_off need not be a multiple of G here, but must
+ * satisfy s_off + n_flush <= s_cap.
+ */
+kivi_status kivi_flush_values(const void* x_f16, int BH, int S, int x_bh_stride, int D,
+                              int group_size, int bits, int residual_length,
+                              void* codes_u8, float* scale, void* zero_f16,
+                              int s_off, int s_cap, int* n_flushed, kivi_stream_t stream);
+
+/*
+ * Key and value flush of the same tokens in one launch (both as above, same
+ * n_flush). k and v share x_bh_stride. Bit-exact with the two calls above.
+ */
+kivi_status kivi_flush_kv(const void* k_f16, const void* v_f16, int BH, int S, int x_bh_stride,
+                          int D, int group_size, int bits, int residual_length,
+                          void* kcodes_u8, float* kscale, void* kzero_f16,
+                          void* vcodes_u8, float* vscale, void* vzero_f16,
+                          int s_off, int s_cap, int* n_flushed, kivi_stream_t stream);
+
+/*
+ * Dequantize ([F] "What we're actually optimizing" recon = q*scale + zero;
+ * "Three ways to be off by one bit" #1: a multiply then a separate add, two
+ * roundings, no FMA): tokens [0, S) of a store of capacity s_cap to fp16
+ * out[BH, S, D]:  out = fp16_rn(RN32(RN32(q * scale) + zero)).
+ * axis selects the key or value metadata layout. Bit-exact with the oracle.
+ * Errors: INVALID_ARG if S < 0, S > s_cap or s_cap % G != 0.
+ */
+kivi_status kivi_dequant(kivi_axis axis, const void* codes_u8, const float* scale,
+                         const void* zero_f16, int BH, int S, int D, int group_size, int bits,
+                         int s_cap, void* out_f16, kivi_stream_t stream);
+
+/*
+ * fp16 residual window res[BH, res_cap, D] ([F] "What we're actually
+ * optimizing": the newest tokens stay fp16).
+ * append:  copies src[bh, t, :] (src_bh_stride tokens between heads) for
+ *          t < n_new to res[bh, n_res + t, :]. INVALID_ARG if
+ *          n_res + n_new > res_cap or src_bh_stride < n_new.
+ * compact: drops the oldest n_drop of n_res tokens and moves the other
+ *          n_res - n_drop to the front (overlap-safe). INVALID_ARG if
+ *          n_drop > n_res or n_res > res_cap.
+ */
+kivi_status kivi_residual_append(const void* src_f16, int src_bh_stride, int n_new,
+                                 void* res_f16, int BH, int res_cap, int D, int n_res,
+                                 kivi_stream_t stream);
+kivi_status kivi_residual_compact(void* res_f16, int BH, int res_cap, int D, int n_res,
+                                  int n_drop, kivi_stream_t stream);
+
+/*
+ * Bytes of device workspace kivi_decode_attend needs for these sizes on the
+ * current device (the split count depends on the device's SM count). Returns
+ * 0 for invalid sizes. Host only (reads the device's SM count once).
+ */
+size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D);
+
+/*
+ * Fused dequantize-and-attend single-token decode ([F] "So why does the kernel
+ * ship?": attention reads the packed codes and expands them in registers;
+ * [R] "KV-Cache Kernel Roofline": one query token per head). For each batch
+ * b and query head h, with KV head hk = h / (Hq / Hkv) (grouped-query
+ * attention, query heads of a group contiguous -- [Q] "Picking a model"):
+ *     K_t = fp32 recon of store token t (t < S_q), else k_res[t - S_q]
+ *     score_t = sm_scale * sum_d q[b,h,d] * K_t[d]
+ *     out[b,h,:] = sum_t softmax(score)_t * V_t[:]
+ * over all S_q + n_res tokens (no mask). Stores are those of
+ * kivi_flush_keys / kivi_flush_values with BH = B*Hkv and capacity s_cap;
+ * residuals are fp16 [B*Hkv, res_cap, D]. q fp16 [B, Hq, D]; out f32
+ * [B, Hq, D]. Accumulation is fp32; max-abs error against the float64 oracle
+ * is well below 2e-3 for inputs of unit scale.
+ * workspace: device memory of at least kivi_decode_workspace_size(...) bytes
+ * (split partials; contents on entry are ignored).
+ * Errors: INVALID_ARG if S_q + n_res == 0, S_q > s_cap, n_res > res_cap or
+ * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv is not 1, 2, 4 or 8; WORKSPACE if the
+ * workspace is NULL or too small.
+ */
+kivi_status kivi_decode_attend(const void* q_f16,
+                               const void* kcodes_u8, const float* kscale, const void* kzero_f16,
+                               const void* vcodes_u8, const float* vscale, const void* vzero_f16,
+                               int S_q, int s_cap,
+                               const void* k_res_f16, const void* v_res_f16, int n_res, int res_cap,
+                               int B, int Hq, int Hkv, int D, int group_size, int bits,
+                               float sm_scale, float* out_f32,
+                               void* workspace, size_t workspace_bytes, kivi_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KIVI_GB300_H */

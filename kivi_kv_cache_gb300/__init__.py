@@ -1,0 +1,230 @@
+"""KIVI KV-cache compression on GB300 (sm_103a): Python binding.
+
+Thin ctypes binding of ``libkivi_gb300.so`` (C ABI in ``include/kivi.h``).
+Each ``kivi_*`` function here has the name of the C entry point it calls and
+only marshals arguments: it passes the device pointers of torch CUDA tensors
+and the current CUDA stream, and raises :class:`KiviError` on a non-OK status.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback. If the library has not been built, the first call
+raises ``ImportError`` (build it with ``python -m kivi_kv_cache_gb300.build``).
+
+PyTorch supplies device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "KiviError", "KiviStore", "lib", "library_path",
+    "kivi_status_string", "kivi_version", "kivi_flush_count",
+    "kivi_flush_keys", "kivi_flush_values", "kivi_flush_kv", "kivi_dequant",
+    "kivi_residual_append", "kivi_residual_compact",
+    "kivi_decode_workspace_size", "kivi_decode_attend",
+]
+
+library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkivi_gb300.so")
+
+KIVI_AXIS_KEYS = 0
+KIVI_AXIS_VALUES = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KiviError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__("%s failed: %s" % (fn, kivi_status_string(status)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises ImportError if it was never built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(library_path):
+            raise ImportError("libkivi_gb300.so is not built (run `python -m kivi_kv_cache_gb300.build`); "
+                              "there is no fallback path")
+        L = ctypes.CDLL(library_path)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        IP = ctypes.POINTER(ctypes.c_int)
+        sig = {
+            "kivi_status_string": ([I], ctypes.c_char_p),
+            "kivi_version": ([], I),
+            "kivi_flush_count": ([I, I, I], I),
+            "kivi_flush_keys": ([P, I, I, I, I, I, I, I, P, P, P, I, I, IP, P], I),
+            "kivi_flush_values": ([P, I, I, I, I, I, I, I, P, P, P, I, I, IP, P], I),
+            "kivi_flush_kv": ([P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, I, I, IP, P], I),
+            "kivi_dequant": ([I, P, P, P, I, I, I, I, I, I, P, P], I),
+            "kivi_residual_append": ([P, I, I, P, I, I, I, I, P], I),
+            "kivi_residual_compact": ([P, I, I, I, I, I, P], I),
+            "kivi_decode_workspace_size": ([I, I, I, I, I, I], Z),
+            "kivi_decode_attend": ([P, P, P, P, P, P, P, I, I, P, P, I, I, I, I, I, I, I, I, F, P, P, Z, P], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _stream(stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise KiviError(fn, status)
+
+
+def _rows(x, D: int):
+    """Head stride (in tokens) of a [BH, S, D] fp16 view with dense token rows."""
+    assert x.dim() == 3 and x.shape[2] == D, tuple(x.shape)
+    assert x.stride(2) == 1 and x.stride(1) == D and x.stride(0) % D == 0, x.stride()
+    return x.stride(0) // D
+
+
+def kivi_status_string(status: int) -> str:
+    return lib().kivi_status_string(int(status)).decode()
+
+
+def kivi_version() -> int:
+    return lib().kivi_version()
+
+
+def kivi_flush_count(n_res: int, residual_length: int, group_size: int = 32) -> int:
+    return lib().kivi_flush_count(n_res, residual_length, group_size)
+
+
+class KiviStore:
+    """Device buffers of one packed store (keys or values), allocated by torch.
+
+    codes uint8 [BH, s_cap, D*bits/8]; keys: scale f32 / zero f16
+    [BH, s_cap/G, D]; values: scale f32 / zero f16 [BH, s_cap, D/G].
+    """
+
+    def __init__(self, axis: int, BH: int, s_cap: int, D: int = 128, group_size: int = 32,
+                 bits: int = 4, device="cuda"):
+        import torch
+        assert s_cap % group_size == 0
+        self.axis, self.BH, self.s_cap, self.D, self.G, self.bits = axis, BH, s_cap, D, group_size, bits
+        self.codes = torch.zeros((BH, s_cap, D * bits // 8), dtype=torch.uint8, device=device)
+        meta = (BH, s_cap // group_size, D) if axis == KIVI_AXIS_KEYS else (BH, s_cap, D // group_size)
+        self.scale = torch.zeros(meta, dtype=torch.float32, device=device)
+        self.zero = torch.zeros(meta, dtype=torch.float16, device=device)
+
+    def nbytes_per_token(self) -> float:
+        return (self.codes[0, 0].numel() + (self.scale.numel() * 4 + self.zero.numel() * 2)
+                / (self.BH * self.s_cap))
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def _flush(name: str, x, residual_length: int, store: KiviStore, s_off: int, n_tokens, stream):
+    S = x.shape[1] if n_tokens is None else n_tokens
+    n = ctypes.c_int(0)
+    st = getattr(lib(), name)(_ptr(x), x.shape[0], S, _rows(x, store.D), store.D, store.G, store.bits,
+                              residual_length, _ptr(store.codes), _ptr(store.scale), _ptr(store.zero),
+                              s_off, store.s_cap, ctypes.byref(n), _stream(stream))
+    _check(name, st)
+    return n.value
+
+
+def kivi_flush_keys(x, residual_length: int, store: KiviStore, s_off: int = 0, n_tokens=None,
+                    stream=None) -> int:
+    """Quantize the oldest kivi_flush_count(S, R, G) tokens of x [BH, S, D] fp16
+    into the key store at token offset s_off; returns the number flushed."""
+    return _flush("kivi_flush_keys", x, residual_length, store, s_off, n_tokens, stream)
+
+
+def kivi_flush_values(x, residual_length: int, store: KiviStore, s_off: int = 0, n_tokens=None,
+                      stream=None) -> int:
+    return _flush("kivi_flush_values", x, residual_length, store, s_off, n_tokens, stream)
+
+
+def kivi_flush_kv(k, v, residual_length: int, kstore: KiviStore, vstore: KiviStore, s_off: int = 0,
+                  n_tokens=None, stream=None) -> int:
+    """Key and value flush of the same tokens in one launch."""
+    S = k.shape[1] if n_tokens is None else n_tokens
+    stride = _rows(k, kstore.D)
+    assert _rows(v, vstore.D) == stride and v.shape[0] == k.shape[0]
+    n = ctypes.c_int(0)
+    st = lib().kivi_flush_kv(_ptr(k), _ptr(v), k.shape[0], S, stride, kstore.D, kstore.G, kstore.bits,
+                             residual_length, _ptr(kstore.codes), _ptr(kstore.scale), _ptr(kstore.zero),
+                             _ptr(vstore.codes), _ptr(vstore.scale), _ptr(vstore.zero), s_off,
+                             kstore.s_cap, ctypes.byref(n), _stream(stream))
+    _check("kivi_flush_kv", st)
+    return n.value
+
+
+def kivi_dequant(store: KiviStore, S: int, out=None, stream=None):
+    """fp16 [BH, S, D] reconstruction of tokens [0, S) of a store."""
+    import torch
+    if out is None:
+        out = torch.empty((store.BH, S, store.D), dtype=torch.float16, device=store.codes.device)
+    st = lib().kivi_dequant(store.axis, _ptr(store.codes), _ptr(store.scale), _ptr(store.zero), store.BH,
+                            S, store.D, store.G, store.bits, store.s_cap, _ptr(out), _stream(stream))
+    _check("kivi_dequant", st)
+    return out
+
+
+def kivi_residual_append(src, res, n_res: int, n_new=None, stream=None):
+    """Copy n_new token rows of src [BH, *, D] behind the n_res live rows of res."""
+    n = src.shape[1] if n_new is None else n_new
+    st = lib().kivi_residual_append(_ptr(src), _rows(src, res.shape[2]), n, _ptr(res), res.shape[0],
+                                    res.shape[1], res.shape[2], n_res, _stream(stream))
+    _check("kivi_residual_append", st)
+    return n_res + n
+
+
+def kivi_residual_compact(res, n_res: int, n_drop: int, stream=None):
+    st = lib().kivi_residual_compact(_ptr(res), res.shape[0], res.shape[1], res.shape[2], n_res, n_drop,
+                                     _stream(stream))
+    _check("kivi_residual_compact", st)
+    return n_res - n_drop
+
+
+def kivi_decode_workspace_size(B: int, Hq: int, Hkv: int, S_q: int, n_res: int, D: int = 128) -> int:
+    return lib().kivi_decode_workspace_size(B, Hq, Hkv, S_q, n_res, D)
+
+
+def kivi_decode_attend(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res, v_res, n_res: int,
+                       Hkv: int, sm_scale: float, out=None, workspace=None, stream=None):
+    """Single-token decode: q [B, Hq, D] fp16 -> out [B, Hq, D] fp32."""
+    import torch
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    need = kivi_decode_workspace_size(B, Hq, Hkv, S_q, n_res, D)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    res_cap = 0
+    if k_res is not None:
+        res_cap = _rows(k_res, D)  # head stride in tokens: a view into a larger cache works
+        assert _rows(v_res, D) == res_cap
+    st = lib().kivi_decode_attend(
+        _ptr(q), _ptr(kstore.codes), _ptr(kstore.scale), _ptr(kstore.zero),
+        _ptr(vstore.codes), _ptr(vstore.scale), _ptr(vstore.zero), S_q, kstore.s_cap,
+        _ptr(k_res), _ptr(v_res), n_res, res_cap, B, Hq, Hkv, D, kstore.G, kstore.bits,
+        float(sm_scale), _ptr(out), _ptr(workspace), wbytes, _stream(stream))
+    _check("kivi_decode_attend", st)
+    return out

@@ -1,0 +1,291 @@
+// kivi_api.cu -- the extern "C" boundary of libkivi_gb300.so (declared in
+// include/kivi.h). Every entry point validates its arguments on the host,
+// returns a status without launching when a check fails, and otherwise
+// launches the CUDA kernels on the caller's stream. No allocation, no state
+// beyond a per-device cache of the SM count.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/kivi.h"
+#include "kivi_launch.h"
+
+using namespace kivi;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 152;  // GB300; only used for sizing when no device is visible
+    }
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            return 152;
+        }
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kivi_status shape_check(int D, int G, int bits) {
+    if (D != kD || G != kG || (bits != 2 && bits != 4)) return KIVI_ERR_UNSUPPORTED;
+    return KIVI_OK;
+}
+
+kivi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ERR_CUDA; }
+
+// Split plan for the decode: enough CTAs for about two per SM, whole 32-token
+// tiles per CTA, no empty split.
+DecodePlan make_plan(int B, int Hkv, int S_q, int n_res) {
+    DecodePlan p;
+    p.n_store_tiles = (S_q + kG - 1) / kG;
+    p.n_tiles = p.n_store_tiles + (n_res + kG - 1) / kG;
+    const long long heads = (long long)B * Hkv;
+    const long long target = 2LL * sm_count();
+    long long per_head = (target + heads - 1) / heads;
+    if (per_head < 1) per_head = 1;
+    if (per_head > p.n_tiles) per_head = p.n_tiles;
+    p.tiles_per_split = (int)((p.n_tiles + per_head - 1) / per_head);
+    p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    return p;
+}
+
+size_t workspace_bytes(int B, int Hq, const DecodePlan& p) {
+    if (p.n_split <= 1) return 0;
+    const size_t o = (size_t)B * Hq * p.n_split * kD * sizeof(float);
+    const size_t ml = (size_t)B * Hq * p.n_split * 2 * sizeof(float);
+    return ((o + 255) & ~(size_t)255) + ml;
+}
+
+kivi_status flush_check(const void* x, int BH, int S, int x_bh_stride, int D, int G, int bits,
+                        int R, const void* codes, const void* scale, const void* zero,
+                        int s_off, int s_cap, bool keys, int* n_flush) {
+    kivi_status st = shape_check(D, G, bits);
+    if (st != KIVI_OK) return st;
+    if (BH <= 0 || S < 0 || x_bh_stride < S || R < 0 || s_cap <= 0 || s_cap % G != 0 || s_off < 0)
+        return KIVI_ERR_INVALID_ARG;
+    if (keys && s_off % G != 0) return KIVI_ERR_INVALID_ARG;
+    const int n = kivi_flush_count(S, R, G);
+    if (n < 0 || (long long)s_off + n > s_cap) return KIVI_ERR_INVALID_ARG;
+    if (n > 0 && (!x || !codes || !scale || !zero)) return KIVI_ERR_INVALID_ARG;
+    if (n > 0 && (!aligned16(x) || !aligned16(codes) || !aligned16(scale) || !aligned16(zero)))
+        return KIVI_ERR_ALIGNMENT;
+    *n_flush = n;
+    return KIVI_OK;
+}
+
+FlushArgs flush_args(const void* x, int BH, int x_bh_stride, int n, void* codes, float* scale,
+                     void* zero, int s_off, int s_cap) {
+    FlushArgs a;
+    a.x = static_cast<const __half*>(x);
+    a.x_bh_stride = x_bh_stride;
+    a.BH = BH;
+    a.n_flush = n;
+    a.codes = static_cast<uint8_t*>(codes);
+    a.scale = scale;
+    a.zero = static_cast<__half*>(zero);
+    a.s_off = s_off;
+    a.s_cap = s_cap;
+    return a;
+}
+
+kivi_status flush_one(int axis, const void* x, int BH, int S, int x_bh_stride, int D, int G,
+                      int bits, int R, void* codes, float* scale, void* zero, int s_off,
+                      int s_cap, int* n_flushed, kivi_stream_t stream) {
+    int n = 0;
+    kivi_status st = flush_check(x, BH, S, x_bh_stride, D, G, bits, R, codes, scale, zero, s_off,
+                                 s_cap, axis == 0, &n);
+    if (st != KIVI_OK) return st;
+    if (n_flushed) *n_flushed = n;
+    if (n == 0) return KIVI_OK;
+    return from_cuda(launch_flush(axis, flush_args(x, BH, x_bh_stride, n, codes, scale, zero, s_off, s_cap),
+                                  bits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kivi_status_string(kivi_status s) {
+    switch (s) {
+        case KIVI_OK: return "KIVI_OK";
+        case KIVI_ERR_INVALID_ARG: return "KIVI_ERR_INVALID_ARG";
+        case KIVI_ERR_UNSUPPORTED: return "KIVI_ERR_UNSUPPORTED";
+        case KIVI_ERR_WORKSPACE: return "KIVI_ERR_WORKSPACE";
+        case KIVI_ERR_CUDA: return "KIVI_ERR_CUDA";
+        case KIVI_ERR_ALIGNMENT: return "KIVI_ERR_ALIGNMENT";
+    }
+    return "KIVI_ERR_UNKNOWN";
+}
+
+int kivi_version(void) { return 100; }
+
+int kivi_flush_count(int n_res, int residual_length, int group_size) {
+    if (n_res < 0 || residual_length < 0 || group_size <= 0) return -1;
+    if (n_res == 0) return 0;
+    if (residual_length == 0) return n_res;
+    const int over = n_res - residual_length;
+    if (over < group_size) return 0;
+    return (over / group_size) * group_size;
+}
+
+kivi_status kivi_flush_keys(const void* x_f16, int BH, int S, int x_bh_stride, int D,
+                            int group_size, int bits, int residual_length, void* codes_u8,
+                            float* scale, void* zero_f16, int s_off, int s_cap, int* n_flushed,
+                            kivi_stream_t stream) {
+    return flush_one(0, x_f16, BH, S, x_bh_stride, D, group_size, bits, residual_length, codes_u8,
+                     scale, zero_f16, s_off, s_cap, n_flushed, stream);
+}
+
+kivi_status kivi_flush_values(const void* x_f16, int BH, int S, int x_bh_stride, int D,
+                              int group_size, int bits, int residual_length, void* codes_u8,
+                              float* scale, void* zero_f16, int s_off, int s_cap, int* n_flushed,
+                              kivi_stream_t stream) {
+    return flush_one(1, x_f16, BH, S, x_bh_stride, D, group_size, bits, residual_length, codes_u8,
+                     scale, zero_f16, s_off, s_cap, n_flushed, stream);
+}
+
+kivi_status kivi_flush_kv(const void* k_f16, const void* v_f16, int BH, int S, int x_bh_stride,
+                          int D, int group_size, int bits, int residual_length, void* kcodes_u8,
+                          float* kscale, void* kzero_f16, void* vcodes_u8, float* vscale,
+                          void* vzero_f16, int s_off, int s_cap, int* n_flushed,
+                          kivi_stream_t stream) {
+    int nk = 0, nv = 0;
+    kivi_status st = flush_check(k_f16, BH, S, x_bh_stride, D, group_size, bits, residual_length,
+                                 kcodes_u8, kscale, kzero_f16, s_off, s_cap, true, &nk);
+    if (st != KIVI_OK) return st;
+    st = flush_check(v_f16, BH, S, x_bh_stride, D, group_size, bits, residual_length, vcodes_u8,
+                     vscale, vzero_f16, s_off, s_cap, false, &nv);
+    if (st != KIVI_OK) return st;
+    if (n_flushed) *n_flushed = nk;
+    if (nk == 0) return KIVI_OK;
+    return from_cuda(launch_flush_kv(
+        flush_args(k_f16, BH, x_bh_stride, nk, kcodes_u8, kscale, kzero_f16, s_off, s_cap),
+        flush_args(v_f16, BH, x_bh_stride, nv, vcodes_u8, vscale, vzero_f16, s_off, s_cap), bits,
+        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kivi_status kivi_dequant(kivi_axis axis, const void* codes_u8, const float* scale,
+                         const void* zero_f16, int BH, int S, int D, int group_size, int bits,
+                         int s_cap, void* out_f16, kivi_stream_t stream) {
+    kivi_status st = shape_check(D, group_size, bits);
+    if (st != KIVI_OK) return st;
+    if ((axis != KIVI_AXIS_KEYS && axis != KIVI_AXIS_VALUES) || BH <= 0 || S < 0 || s_cap <= 0 ||
+        s_cap % group_size != 0 || S > s_cap)
+        return KIVI_ERR_INVALID_ARG;
+    if (S == 0) return KIVI_OK;
+    if (!codes_u8 || !scale || !zero_f16 || !out_f16) return KIVI_ERR_INVALID_ARG;
+    if (!aligned16(codes_u8) || !aligned16(scale) || !aligned16(zero_f16) || !aligned16(out_f16))
+        return KIVI_ERR_ALIGNMENT;
+    DequantArgs a;
+    a.codes = static_cast<const uint8_t*>(codes_u8);
+    a.scale = scale;
+    a.zero = static_cast<const __half*>(zero_f16);
+    a.BH = BH;
+    a.S = S;
+    a.s_cap = s_cap;
+    a.out = static_cast<__half*>(out_f16);
+    return from_cuda(launch_dequant((int)axis, a, bits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kivi_status kivi_residual_append(const void* src_f16, int src_bh_stride, int n_new, void* res_f16,
+                                 int BH, int res_cap, int D, int n_res, kivi_stream_t stream) {
+    if (D != kD) return KIVI_ERR_UNSUPPORTED;
+    if (BH <= 0 || n_new < 0 || n_res < 0 || res_cap <= 0 || src_bh_stride < n_new ||
+        (long long)n_res + n_new > res_cap)
+        return KIVI_ERR_INVALID_ARG;
+    if (n_new == 0) return KIVI_OK;
+    if (!src_f16 || !res_f16) return KIVI_ERR_INVALID_ARG;
+    if (!aligned16(src_f16) || !aligned16(res_f16)) return KIVI_ERR_ALIGNMENT;
+    return from_cuda(launch_residual_append(static_cast<const __half*>(src_f16), src_bh_stride, n_new,
+                                            static_cast<__half*>(res_f16), BH, res_cap, n_res,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kivi_status kivi_residual_compact(void* res_f16, int BH, int res_cap, int D, int n_res, int n_drop,
+                                  kivi_stream_t stream) {
+    if (D != kD) return KIVI_ERR_UNSUPPORTED;
+    if (BH <= 0 || res_cap <= 0 || n_res < 0 || n_res > res_cap || n_drop < 0 || n_drop > n_res)
+        return KIVI_ERR_INVALID_ARG;
+    if (n_drop == 0 || n_drop == n_res) return KIVI_OK;
+    if (!res_f16) return KIVI_ERR_INVALID_ARG;
+    if (!aligned16(res_f16)) return KIVI_ERR_ALIGNMENT;
+    return from_cuda(launch_residual_compact(static_cast<__half*>(res_f16), BH, res_cap, n_res, n_drop,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S_q < 0 || n_res < 0 || D != kD || S_q + n_res == 0)
+        return 0;
+    return workspace_bytes(B, Hq, make_plan(B, Hkv, S_q, n_res));
+}
+
+kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const float* kscale,
+                               const void* kzero_f16, const void* vcodes_u8, const float* vscale,
+                               const void* vzero_f16, int S_q, int s_cap, const void* k_res_f16,
+                               const void* v_res_f16, int n_res, int res_cap, int B, int Hq, int Hkv,
+                               int D, int group_size, int bits, float sm_scale, float* out_f32,
+                               void* workspace, size_t workspace_bytes_, kivi_stream_t stream) {
+    kivi_status st = shape_check(D, group_size, bits);
+    if (st != KIVI_OK) return st;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S_q < 0 || n_res < 0 ||
+        S_q + n_res == 0 || S_q > s_cap || n_res > res_cap || s_cap < 0 || res_cap < 0 ||
+        (S_q > 0 && s_cap % group_size != 0) || !std::isfinite(sm_scale))
+        return KIVI_ERR_INVALID_ARG;
+    const int gq = Hq / Hkv;
+    if (gq != 1 && gq != 2 && gq != 4 && gq != 8) return KIVI_ERR_UNSUPPORTED;
+    if (!q_f16 || !out_f32) return KIVI_ERR_INVALID_ARG;
+    if (S_q > 0 && (!kcodes_u8 || !kscale || !kzero_f16 || !vcodes_u8 || !vscale || !vzero_f16))
+        return KIVI_ERR_INVALID_ARG;
+    if (n_res > 0 && (!k_res_f16 || !v_res_f16)) return KIVI_ERR_INVALID_ARG;
+    if (!aligned16(q_f16) || !aligned16(out_f32) || !aligned16(kcodes_u8) || !aligned16(kscale) ||
+        !aligned16(kzero_f16) || !aligned16(vcodes_u8) || !aligned16(vscale) ||
+        !aligned16(vzero_f16) || !aligned16(k_res_f16) || !aligned16(v_res_f16) ||
+        !aligned16(workspace))
+        return KIVI_ERR_ALIGNMENT;
+    const DecodePlan p = make_plan(B, Hkv, S_q, n_res);
+    const size_t need = workspace_bytes(B, Hq, p);
+    if (need > 0 && (!workspace || workspace_bytes_ < need)) return KIVI_ERR_WORKSPACE;
+
+    DecodeArgs a;
+    a.q = static_cast<const __half*>(q_f16);
+    a.kcodes = static_cast<const uint8_t*>(kcodes_u8);
+    a.kscale = kscale;
+    a.kzero = static_cast<const __half*>(kzero_f16);
+    a.vcodes = static_cast<const uint8_t*>(vcodes_u8);
+    a.vscale = vscale;
+    a.vzero = static_cast<const __half*>(vzero_f16);
+    a.S_q = S_q;
+    a.s_cap = s_cap;
+    a.k_res = static_cast<const __half*>(k_res_f16);
+    a.v_res = static_cast<const __half*>(v_res_f16);
+    a.n_res = n_res;
+    a.res_cap = res_cap;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.score_scale = sm_scale * 1.4426950408889634f;
+    a.n_split = p.n_split;
+    a.tiles_per_split = p.tiles_per_split;
+    a.n_store_tiles = p.n_store_tiles;
+    a.n_tiles = p.n_tiles;
+    float* ws = static_cast<float*>(workspace);
+    a.part_o = ws;
+    a.part_ml = need > 0 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                    (((size_t)B * Hq * p.n_split * kD * sizeof(float) + 255) &
+                                                     ~(size_t)255))
+                         : nullptr;
+    a.out = out_f32;
+    return from_cuda(launch_decode(a, bits, gq, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

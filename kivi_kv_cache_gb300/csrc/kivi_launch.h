@@ -1,0 +1,80 @@
+// kivi_launch.h -- internal launch interface between the C ABI (kivi_api.cu)
+// and the kernels. Arguments are validated by the caller; launchers only
+// pick a grid and launch on the given stream.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kivi {
+
+constexpr int kD = 128;  // head_dim compiled in
+constexpr int kG = 32;   // group_size compiled in
+
+struct FlushArgs {
+    const __half* x;      // [BH, x_bh_stride, D], tokens [0, n_flush) used
+    long long x_bh_stride;
+    int BH;
+    int n_flush;
+    uint8_t* codes;       // [BH, s_cap, D*bits/8]
+    float* scale;         // keys [BH, s_cap/G, D]; values [BH, s_cap, D/G]
+    __half* zero;
+    int s_off;
+    int s_cap;
+};
+
+struct DequantArgs {
+    const uint8_t* codes;
+    const float* scale;
+    const __half* zero;
+    int BH;
+    int S;
+    int s_cap;
+    __half* out;          // [BH, S, D]
+};
+
+struct DecodeArgs {
+    const __half* q;      // [B, Hq, D]
+    const uint8_t* kcodes;
+    const float* kscale;
+    const __half* kzero;
+    const uint8_t* vcodes;
+    const float* vscale;
+    const __half* vzero;
+    int S_q;
+    int s_cap;
+    const __half* k_res;  // [B*Hkv, res_cap, D]
+    const __half* v_res;
+    int n_res;
+    int res_cap;
+    int B;
+    int Hq;
+    int Hkv;
+    float score_scale;    // sm_scale * log2(e): scores live in the exp2 domain
+    int n_split;
+    int tiles_per_split;
+    int n_store_tiles;
+    int n_tiles;
+    float* part_o;        // [B, Hq, n_split, D]
+    float* part_ml;       // [B, Hq, n_split, 2]  (running max, running sum)
+    float* out;           // [B, Hq, D]
+};
+
+struct DecodePlan {
+    int n_split;
+    int tiles_per_split;
+    int n_store_tiles;
+    int n_tiles;
+};
+
+cudaError_t launch_flush(int axis, const FlushArgs& a, int bits, cudaStream_t stream);
+cudaError_t launch_flush_kv(const FlushArgs& k, const FlushArgs& v, int bits, cudaStream_t stream);
+cudaError_t launch_dequant(int axis, const DequantArgs& a, int bits, cudaStream_t stream);
+cudaError_t launch_residual_append(const __half* src, long long src_bh_stride, int n_new,
+                                   __half* res, int BH, int res_cap, int n_res, cudaStream_t stream);
+cudaError_t launch_residual_compact(__half* res, int BH, int res_cap, int n_res, int n_drop,
+                                    cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
+
+}  // namespace kivi

@@ -108,3 +108,19 @@ def step_tokens(rng: np.random.Generator, w: Workload, n: int = 1):
     v = normal(rng, (w.BH, n, w.D))
     q = normal(rng, (w.B, w.Hq, w.D))
     return k, v, q
+
+
+def prefill_inputs_torch(w: Workload, seed: int, device, S: int | None = None):
+    """Device-side draw with the same distributions as prefill_inputs (for
+    large input pools; seeded with torch's generator, so the values differ
+    from the numpy draw of the same seed)."""
+    import torch
+    S = w.S if S is None else S
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    ch = torch.as_tensor(outlier_channels(w), device=device)
+    k = torch.randn((w.BH, S, w.D), generator=g, device=device, dtype=torch.float32)
+    k[..., ch] *= w.outlier_scale
+    v = torch.randn((w.BH, S, w.D), generator=g, device=device, dtype=torch.float32)
+    q = torch.randn((w.B, w.Hq, w.D), generator=g, device=device, dtype=torch.float32)
+    return k.half(), v.half(), q.half()

@@ -1,0 +1,151 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/kivi.h declares, computes the flush plan like the
+oracle, and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import kivi_kv_cache_gb300 as kv
+import oracle
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "kivi.h")
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA, ALIGN = range(6)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(kivi_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    return kv.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 11, names
+    raw = ctypes.CDLL(kv.library_path)
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(L):
+    for s, name in enumerate(["KIVI_OK", "KIVI_ERR_INVALID_ARG", "KIVI_ERR_UNSUPPORTED",
+                              "KIVI_ERR_WORKSPACE", "KIVI_ERR_CUDA", "KIVI_ERR_ALIGNMENT"]):
+        assert kv.kivi_status_string(s) == name
+    assert kv.kivi_status_string(99) == "KIVI_ERR_UNKNOWN"
+    assert kv.kivi_version() >= 100
+
+
+def test_flush_count_matches_oracle(L):
+    for n_res in range(0, 300):
+        for r in (0, 1, 32, 128):
+            for g in (32, 64):
+                assert kv.kivi_flush_count(n_res, r, g) == oracle.flush_count(n_res, r, g)
+    assert kv.kivi_flush_count(-1, 32, 32) == -1
+    assert kv.kivi_flush_count(5, 32, 0) == -1
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
+
+# Every call below with FAKE pointers must be rejected by the host-side checks.
+# They run only where no GPU is visible, so that a bug in those checks can
+# never launch a kernel on a bogus address.
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(),
+                            reason="fake-pointer validation tests run only without a GPU")
+
+
+def flush(L, name="kivi_flush_keys", x=FAKE, BH=8, S=256, stride=256, D=128, G=32, bits=4, R=128,
+          codes=FAKE, scale=FAKE, zero=FAKE, s_off=0, s_cap=256):
+    n = ctypes.c_int(-7)
+    st = getattr(L, name)(x, BH, S, stride, D, G, bits, R, codes, scale, zero, s_off, s_cap,
+                          ctypes.byref(n), None)
+    return st, n.value
+
+
+@no_gpu
+@pytest.mark.parametrize("name", ["kivi_flush_keys", "kivi_flush_values"])
+def test_flush_rejects_bad_arguments_without_launching(L, name):
+    assert flush(L, name, bits=3)[0] == UNSUPPORTED
+    assert flush(L, name, D=64)[0] == UNSUPPORTED
+    assert flush(L, name, G=64)[0] == UNSUPPORTED
+    assert flush(L, name, BH=0)[0] == INVALID
+    assert flush(L, name, S=-1)[0] == INVALID
+    assert flush(L, name, stride=100)[0] == INVALID          # head stride < S
+    assert flush(L, name, s_cap=100)[0] == INVALID           # not a multiple of G
+    assert flush(L, name, s_off=160)[0] == INVALID           # 160 + 128 > 256
+    assert flush(L, name, x=None)[0] == INVALID
+    assert flush(L, name, codes=FAKE + 4)[0] == ALIGN
+    assert flush(L, name, zero=FAKE + 2)[0] == ALIGN
+    # nothing to flush: OK, n_flushed = 0, no launch and no pointer needed
+    assert flush(L, name, S=100, x=None, codes=None, scale=None, zero=None) == (OK, 0)
+
+
+@no_gpu
+def test_key_flush_needs_group_aligned_offset(L):
+    assert flush(L, "kivi_flush_keys", s_off=16, s_cap=512)[0] == INVALID
+
+
+@no_gpu
+def test_dequant_rejects_bad_arguments(L):
+    f = L.kivi_dequant
+    assert f(0, FAKE, FAKE, FAKE, 8, 300, 128, 32, 4, 256, FAKE, None) == INVALID  # S > s_cap
+    assert f(2, FAKE, FAKE, FAKE, 8, 64, 128, 32, 4, 256, FAKE, None) == INVALID   # bad axis
+    assert f(0, FAKE, FAKE, FAKE, 8, 64, 128, 32, 5, 256, FAKE, None) == UNSUPPORTED
+    assert f(0, FAKE, FAKE, FAKE + 8, 8, 64, 128, 32, 4, 256, FAKE, None) == ALIGN
+    assert f(1, None, FAKE, FAKE, 8, 64, 128, 32, 4, 256, FAKE, None) == INVALID
+    assert f(1, None, None, None, 8, 0, 128, 32, 4, 256, None, None) == OK         # empty
+
+
+@no_gpu
+def test_residual_rejects_bad_arguments(L):
+    assert L.kivi_residual_append(FAKE, 4, 4, FAKE, 8, 160, 128, 158, None) == INVALID  # overflow
+    assert L.kivi_residual_append(FAKE, 2, 4, FAKE, 8, 160, 128, 0, None) == INVALID    # stride < n_new
+    assert L.kivi_residual_append(FAKE, 4, 4, FAKE, 8, 160, 64, 0, None) == UNSUPPORTED
+    assert L.kivi_residual_append(FAKE + 2, 4, 4, FAKE, 8, 160, 128, 0, None) == ALIGN
+    assert L.kivi_residual_append(None, 4, 0, None, 8, 160, 128, 0, None) == OK
+    assert L.kivi_residual_compact(FAKE, 8, 160, 128, 100, 101, None) == INVALID
+    assert L.kivi_residual_compact(FAKE, 8, 160, 128, 161, 1, None) == INVALID
+    assert L.kivi_residual_compact(FAKE, 8, 160, 128, 100, 0, None) == OK
+    assert L.kivi_residual_compact(FAKE, 8, 160, 128, 100, 100, None) == OK
+
+
+def decode(L, q=FAKE, S_q=2080, s_cap=2080, n_res=158, res_cap=160, B=1, Hq=32, Hkv=8, D=128,
+           G=32, bits=4, ws=FAKE, wbytes=1 << 30, sm=0.088, out=FAKE):
+    return L.kivi_decode_attend(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, S_q, s_cap, FAKE, FAKE, n_res,
+                                res_cap, B, Hq, Hkv, D, G, bits, sm, out, ws, wbytes, None)
+
+
+@no_gpu
+def test_decode_rejects_bad_arguments(L):
+    assert decode(L, Hq=12) == INVALID               # 12 / 8 is not an integer
+    assert decode(L, Hq=24) == UNSUPPORTED           # 3 query heads per KV head
+    assert decode(L, Hq=128) == UNSUPPORTED          # 16 query heads per KV head
+    assert decode(L, S_q=0, n_res=0) == INVALID
+    assert decode(L, S_q=3000) == INVALID            # S_q > s_cap
+    assert decode(L, n_res=200) == INVALID           # n_res > res_cap
+    assert decode(L, q=None) == INVALID
+    assert decode(L, out=FAKE + 4) == ALIGN
+    assert decode(L, sm=float("inf")) == INVALID
+    assert decode(L, ws=None) == WORKSPACE
+    need = L.kivi_decode_workspace_size(1, 32, 8, 2080, 158, 128)
+    assert need > 0
+    assert decode(L, wbytes=need - 1) == WORKSPACE
+
+
+def test_workspace_size(L):
+    assert L.kivi_decode_workspace_size(1, 32, 8, 0, 0, 128) == 0
+    assert L.kivi_decode_workspace_size(1, 32, 8, 64, 0, 64) == 0
+    small = L.kivi_decode_workspace_size(1, 32, 8, 2080, 158, 128)
+    big = L.kivi_decode_workspace_size(1, 32, 8, 32640, 128, 128)
+    assert 0 < small <= big
+    # a single 32-token tile needs no split and no workspace
+    assert L.kivi_decode_workspace_size(1, 32, 8, 32, 0, 128) == 0

@@ -1,0 +1,297 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bar: packed codes, scales and zeros bit-exact; dequantized fp16 bit-exact;
+decode-attend max-abs error <= 2e-3 against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kivi_kv_cache_gb300 as kv
+import oracle
+from kivi_kv_cache_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def assert_store_equal(gpu: kv.KiviStore, ref: oracle.Store, what=""):
+    assert np.array_equal(host(gpu.codes), ref.codes), "packed codes differ " + what
+    assert np.array_equal(host(gpu.scale).view(np.uint32), ref.scale.view(np.uint32)), "scales differ " + what
+    assert np.array_equal(host(gpu.zero).view(np.uint16), ref.zero.view(np.uint16)), "zeros differ " + what
+
+
+def flush_both(axis, x, R, G=32, bits=4, s_cap=None, fused_with=None):
+    """GPU flush (single-axis call) and oracle flush of x [BH, S, D]."""
+    BH, S, D = x.shape
+    n = kv.kivi_flush_count(S, R, G)
+    s_cap = s_cap or max(G, -(-n // G) * G)
+    gs = kv.KiviStore(axis, BH, s_cap, D, G, bits, device=DEV)
+    fn = kv.kivi_flush_keys if axis == 0 else kv.kivi_flush_values
+    assert fn(dev(x), R, gs) == n
+    rs = oracle.Store(axis, BH, s_cap, D, G, bits)
+    if n:
+        oracle.flush(axis, x, n, rs)
+    return n, gs, rs
+
+
+# ---------------------------------------------------------------------------
+# flush + dequant on the workloads
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "qwen8b", "long2bit"])
+def test_flush_and_dequant_workloads(name):
+    w = synth.WORKLOADS[name]
+    k, v, _ = synth.prefill_inputs(w)
+    for axis, x in ((0, k), (1, v)):
+        n, gs, rs = flush_both(axis, x, w.R, w.G, w.bits)
+        assert n == oracle.flush_count(w.S, w.R, w.G)
+        assert_store_equal(gs, rs, "%s axis %d" % (name, axis))
+        d = host(kv.kivi_dequant(gs, n))
+        assert np.array_equal(d.view(np.uint16), oracle.dequant(rs, n).view(np.uint16))
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen8b", "long2bit"])
+def test_fused_kv_flush_equals_separate(name):
+    w = synth.WORKLOADS[name]
+    k, v, _ = synth.prefill_inputs(w)
+    n = kv.kivi_flush_count(w.S, w.R, w.G)
+    ks = kv.KiviStore(0, w.BH, n, w.D, w.G, w.bits, device=DEV)
+    vs = kv.KiviStore(1, w.BH, n, w.D, w.G, w.bits, device=DEV)
+    assert kv.kivi_flush_kv(dev(k), dev(v), w.R, ks, vs) == n
+    assert_store_equal(ks, oracle.flush(0, k, n, oracle.Store(0, w.BH, n, w.D, w.G, w.bits)))
+    assert_store_equal(vs, oracle.flush(1, v, n, oracle.Store(1, w.BH, n, w.D, w.G, w.bits)))
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("axis", [0, 1])
+def test_flush_ragged_sweep(bits, axis):
+    """residual_length 0 flushes every token, so S gives ragged last key groups."""
+    rng = np.random.default_rng(40 + bits + axis)
+    ch = np.array([3, 64, 65, 127])
+    for S in [1, 2, 31, 32, 33, 63, 95, 100, 129, 255, 300]:
+        BH = int(rng.integers(1, 6))
+        x = synth.keys(rng, (BH, S), 128, ch, 10.0) if axis == 0 else synth.normal(rng, (BH, S, 128))
+        n, gs, rs = flush_both(axis, x, 0, 32, bits)
+        assert n == S
+        assert_store_equal(gs, rs, "S=%d" % S)
+        d = host(kv.kivi_dequant(gs, S))
+        assert np.array_equal(d.view(np.uint16), oracle.dequant(rs, S).view(np.uint16)), S
+
+
+def adversarial(rng, BH, S):
+    x = synth.normal(rng, (BH, S, 128))
+    x[0, :, 0] = np.float16(3.0)                          # max == min key group
+    x[0, 5, :] = np.float16(-2.0)                         # max == min value row
+    x[0, :32, 1] = (np.arange(32) % 16 * 0.5).astype(np.float16)   # exact grid, ties at .5 steps
+    x[0, 6, :] = (np.arange(128) % 4 * 0.25).astype(np.float16)
+    x[0, 7, :32] = np.float16(0.0)
+    x[0, 7, 0] = np.float16(-0.0)                         # -0 minimum
+    x[1 % BH, :, 2] = np.float16(65504.0)
+    x[1 % BH, ::2, 2] = np.float16(-65504.0)              # full fp16 range
+    x[1 % BH, 9, :] = np.float16(6e-8)                    # subnormals
+    x[1 % BH, 9, ::3] = np.float16(-6e-8)
+    x[1 % BH, 10, :] = (rng.integers(-2, 3, 128) * 2.0 ** -24).astype(np.float16)
+    x[0, 40:72, 3] = (np.arange(32) * 1.5 - 3).astype(np.float16)
+    return x
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("axis", [0, 1])
+def test_flush_adversarial(bits, axis):
+    rng = np.random.default_rng(77)
+    x = adversarial(rng, 3, 96)
+    n, gs, rs = flush_both(axis, x, 0, 32, bits)
+    assert_store_equal(gs, rs)
+    assert np.array_equal(host(kv.kivi_dequant(gs, n)).view(np.uint16), oracle.dequant(rs, n).view(np.uint16))
+
+
+@pytest.mark.parametrize("axis", [0, 1])
+def test_flush_into_offset_of_larger_cache(axis):
+    """Flush a strided view (head stride 300 tokens) at store offset 64."""
+    rng = np.random.default_rng(5)
+    big = synth.normal(rng, (4, 300, 128))
+    x = dev(big)[:, 40:, :]  # view: tokens 40.., head stride 300
+    gs = kv.KiviStore(axis, 4, 256, device=DEV)
+    fn = kv.kivi_flush_keys if axis == 0 else kv.kivi_flush_values
+    n = fn(x, 32, gs, s_off=64, n_tokens=200)  # flush_count(200, 32, 32) = 160
+    assert n == 160
+    rs = oracle.Store(axis, 4, 256, 128, 32, 4)
+    oracle.flush(axis, big, 160, rs, s_off=64, t0=40)
+    assert_store_equal(gs, rs)
+
+
+# ---------------------------------------------------------------------------
+# residual window
+# ---------------------------------------------------------------------------
+
+def test_residual_append_and_compact():
+    rng = np.random.default_rng(8)
+    res = synth.normal(rng, (6, 160, 128))
+    src = synth.normal(rng, (6, 50, 128))
+    g_res = dev(res)
+    ref = res.copy()
+    assert kv.kivi_residual_append(dev(src), g_res, 100, n_new=37) == 137
+    oracle.residual_append(ref, 100, src, 37)
+    assert np.array_equal(host(g_res), ref)
+    for n_res, n_drop in ((137, 32), (105, 100), (5, 2), (160, 1)):
+        g = dev(ref)
+        kv.kivi_residual_compact(g, n_res, n_drop)
+        r2 = ref.copy()
+        oracle.residual_compact(r2, n_res, n_drop)
+        assert np.array_equal(host(g), r2), (n_res, n_drop)
+
+
+# ---------------------------------------------------------------------------
+# decode-attend
+# ---------------------------------------------------------------------------
+
+def decode_case(w, S_q, n_res, k, v, q, res_k=None, res_v=None):
+    BH = w.BH
+    s_cap = max(w.G, -(-S_q // w.G) * w.G)
+    gk = kv.KiviStore(0, BH, s_cap, w.D, w.G, w.bits, device=DEV)
+    gv = kv.KiviStore(1, BH, s_cap, w.D, w.G, w.bits, device=DEV)
+    rk = oracle.Store(0, BH, s_cap, w.D, w.G, w.bits)
+    rv = oracle.Store(1, BH, s_cap, w.D, w.G, w.bits)
+    if S_q:
+        kv.kivi_flush_kv(dev(k), dev(v), 0, gk, gv, n_tokens=S_q)
+        oracle.flush(0, k, S_q, rk)
+        oracle.flush(1, v, S_q, rv)
+    kr = res_k if res_k is not None else k[:, S_q:S_q + n_res]
+    vr = res_v if res_v is not None else v[:, S_q:S_q + n_res]
+    kr = np.ascontiguousarray(kr)
+    vr = np.ascontiguousarray(vr)
+    out = kv.kivi_decode_attend(dev(q), gk, gv, S_q, dev(kr), dev(vr), n_res, w.Hkv, w.sm_scale)
+    ref = oracle.decode_attend(q, rk, rv, S_q, kr, vr, n_res, w.Hkv, w.sm_scale)
+    return host(out).astype(np.float64), ref
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen8b", "long2bit"])
+def test_decode_prefill_workloads(name):
+    w = synth.WORKLOADS[name]
+    k, v, q = synth.prefill_inputs(w)
+    n = kv.kivi_flush_count(w.S, w.R, w.G)
+    out, ref = decode_case(w, n, w.S - n, k, v, q)
+    err = np.max(np.abs(out - ref))
+    assert err <= TOL, err
+
+
+def test_decode_batched_workload_sampled():
+    """Batched decode (32 sequences x 4096 cached tokens); the oracle checks a
+    sample of 4 sequences, the GPU runs the full batch and is sliced."""
+    w = synth.WORKLOADS["batched"]
+    rng = np.random.default_rng(w.seed)
+    ch = synth.outlier_channels(w)
+    k = synth.keys(rng, (w.BH, w.S_q + w.n_res), w.D, ch, w.outlier_scale)
+    v = synth.normal(rng, (w.BH, w.S_q + w.n_res, w.D))
+    q = synth.normal(rng, (w.B, w.Hq, w.D))
+    s_cap = w.S_q
+    gk = kv.KiviStore(0, w.BH, s_cap, device=DEV)
+    gv = kv.KiviStore(1, w.BH, s_cap, device=DEV)
+    kv.kivi_flush_kv(dev(k), dev(v), 0, gk, gv, n_tokens=w.S_q)
+    kr = np.ascontiguousarray(k[:, w.S_q:])
+    vr = np.ascontiguousarray(v[:, w.S_q:])
+    out = host(kv.kivi_decode_attend(dev(q), gk, gv, w.S_q, dev(kr), dev(vr), w.n_res, w.Hkv, w.sm_scale))
+    for b in (0, 7, 19, 31):
+        sl = slice(b * w.Hkv, (b + 1) * w.Hkv)
+        rk = oracle.flush(0, k[sl].copy(), w.S_q, oracle.Store(0, w.Hkv, s_cap, 128, 32, 4))
+        rv = oracle.flush(1, v[sl].copy(), w.S_q, oracle.Store(1, w.Hkv, s_cap, 128, 32, 4))
+        ref = oracle.decode_attend(q[b:b + 1], rk, rv, w.S_q, kr[sl].copy(), vr[sl].copy(), w.n_res,
+                                   w.Hkv, w.sm_scale)
+        err = np.max(np.abs(out[b:b + 1] - ref))
+        assert err <= TOL, (b, err)
+
+
+@pytest.mark.parametrize("S_q,n_res", [(0, 1), (0, 37), (32, 0), (33, 0), (64, 5), (77, 31),
+                                       (1000, 200), (4096, 0), (96, 128)])
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (32, 8), (16, 2)])
+def test_decode_edge_shapes(S_q, n_res, bits, hq, hkv):
+    B = 2
+    w = synth.Workload("edge", B=B, Hkv=hkv, Hq=hq, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
+                       n_outlier=4, outlier_scale=8.0, seed=S_q * 7 + n_res)
+    rng = np.random.default_rng(w.seed)
+    k = synth.keys(rng, (w.BH, S_q + n_res), 128, synth.outlier_channels(w), 8.0)
+    v = synth.normal(rng, (w.BH, S_q + n_res, 128))
+    q = synth.normal(rng, (B, hq, 128))
+    out, ref = decode_case(w, S_q, n_res, k, v, q)
+    err = np.max(np.abs(out - ref))
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("S_kv", [128, 512, 2048, 8192, 16384])
+def test_decode_stream_sweep_sampled(S_kv):
+    """The streaming workload's decode sweep at B=16 (cache of S_kv tokens with
+    a 128-token residual window); the oracle checks sequences 0 and 15."""
+    w = synth.WORKLOADS["stream"]
+    rng = np.random.default_rng(1000 + S_kv)
+    n_res = min(w.R, S_kv)
+    S_q = S_kv - n_res
+    ch = synth.outlier_channels(w)
+    k = synth.keys(rng, (w.BH, S_kv), w.D, ch, w.outlier_scale)
+    v = synth.normal(rng, (w.BH, S_kv, w.D))
+    q = synth.normal(rng, (w.B, w.Hq, w.D))
+    s_cap = max(32, S_q)
+    gk = kv.KiviStore(0, w.BH, s_cap, device=DEV)
+    gv = kv.KiviStore(1, w.BH, s_cap, device=DEV)
+    if S_q:
+        kv.kivi_flush_kv(dev(k), dev(v), 0, gk, gv, n_tokens=S_q)
+    kr = np.ascontiguousarray(k[:, S_q:])
+    vr = np.ascontiguousarray(v[:, S_q:])
+    out = host(kv.kivi_decode_attend(dev(q), gk, gv, S_q, dev(kr), dev(vr), n_res, w.Hkv, w.sm_scale))
+    for b in (0, 15):
+        sl = slice(b * w.Hkv, (b + 1) * w.Hkv)
+        rk = oracle.Store(0, w.Hkv, s_cap, 128, 32, 4)
+        rv = oracle.Store(1, w.Hkv, s_cap, 128, 32, 4)
+        if S_q:
+            oracle.flush(0, k[sl].copy(), S_q, rk)
+            oracle.flush(1, v[sl].copy(), S_q, rv)
+        ref = oracle.decode_attend(q[b:b + 1], rk, rv, S_q, kr[sl].copy(), vr[sl].copy(), n_res,
+                                   w.Hkv, w.sm_scale)
+        assert np.max(np.abs(out[b:b + 1] - ref)) <= TOL
+
+
+def test_decode_workspace_too_small_is_rejected():
+    w = synth.WORKLOADS["qwen8b"]
+    q = torch.zeros((1, 32, 128), dtype=torch.float16, device=DEV)
+    gk = kv.KiviStore(0, 8, 2080, device=DEV)
+    gv = kv.KiviStore(1, 8, 2080, device=DEV)
+    kr = torch.zeros((8, 160, 128), dtype=torch.float16, device=DEV)
+    need = kv.kivi_decode_workspace_size(1, 32, 8, 2080, 158)
+    assert need > 0
+    ws = torch.zeros(need - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(kv.KiviError) as e:
+        kv.kivi_decode_attend(q, gk, gv, 2080, kr, kr, 158, 8, w.sm_scale, workspace=ws)
+    assert e.value.status == 3
+
+
+def test_many_sequence_lengths_one_build():
+    """55 sequence lengths through flush and decode with no per-length
+    specialisation (sequence length is a runtime argument, never compiled in)."""
+    rng = np.random.default_rng(55)
+    w = synth.Workload("len", B=1, Hkv=2, Hq=8, D=128, S=0, bits=4, G=32, R=32, n_outlier=4,
+                       outlier_scale=8.0, seed=1)
+    for i, S in enumerate(range(33, 33 + 55 * 7, 7)):
+        k = synth.keys(rng, (2, S), 128, np.array([1, 2, 3, 4]), 8.0)
+        v = synth.normal(rng, (2, S, 128))
+        q = synth.normal(rng, (1, 8, 128))
+        n = kv.kivi_flush_count(S, 32, 32)
+        out, ref = decode_case(w, n, S - n, k, v, q)
+        assert np.max(np.abs(out - ref)) <= TOL, S
