@@ -200,6 +200,42 @@ kivi_status kivi_decode_attend(const void* q_f16,
                                float sm_scale, float* out_f32,
                                void* workspace, size_t workspace_bytes, kivi_stream_t stream);
 
+/*
+ * kivi_decode_attend_noalloc -- the same decode as kivi_decode_attend, for
+ * callers that cannot allocate device memory when they decode: serving
+ * runtimes that hand out all of HBM to weights and KV-cache pages at start-up
+ * and forbid later allocations (a late cudaMalloc may fail, or synchronise the
+ * whole device), and C callers that only receive device pointers from a
+ * framework owning the memory pool. The pages have no counterpart; this is an
+ * interface addition of this library.
+ *
+ * Instead of a workspace argument it uses one library-owned device array of
+ * KIVI_NOALLOC_SCRATCH_BYTES (2 MiB) per device, reserved when the library's
+ * device code is loaded and kept until the process exits. It allocates
+ * nothing itself.
+ *   - Size limit: if kivi_decode_workspace_size(...) for these sizes exceeds
+ *     KIVI_NOALLOC_SCRATCH_BYTES, it returns KIVI_ERR_WORKSPACE and launches
+ *     nothing.
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's contents. Calls whose kernels overlap on the GPU (two
+ *     unordered streams) race and give wrong results; order them.
+ *   - First call per device: it looks up the array's device address with
+ *     cudaGetSymbolAddress (the current device must be the one the pointers
+ *     belong to) and caches it; this may load the library's device code, so
+ *     make the first call before capturing any stream. KIVI_ERR_CUDA if the
+ *     lookup fails.
+ * Every other argument, check, status and result is that of
+ * kivi_decode_attend.
+ */
+#define KIVI_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
+kivi_status kivi_decode_attend_noalloc(const void* q_f16,
+                                       const void* kcodes_u8, const float* kscale, const void* kzero_f16,
+                                       const void* vcodes_u8, const float* vscale, const void* vzero_f16,
+                                       int S_q, int s_cap,
+                                       const void* k_res_f16, const void* v_res_f16, int n_res, int res_cap,
+                                       int B, int Hq, int Hkv, int D, int group_size, int bits,
+                                       float sm_scale, float* out_f32, kivi_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

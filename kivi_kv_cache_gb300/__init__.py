@@ -21,7 +21,7 @@ __all__ = [
     "kivi_status_string", "kivi_version", "kivi_flush_count",
     "kivi_flush_keys", "kivi_flush_values", "kivi_flush_kv", "kivi_dequant",
     "kivi_residual_append", "kivi_residual_compact",
-    "kivi_decode_workspace_size", "kivi_decode_attend",
+    "kivi_decode_workspace_size", "kivi_decode_attend", "kivi_decode_attend_noalloc",
 ]
 
 library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkivi_gb300.so")
@@ -227,4 +227,38 @@ def kivi_decode_attend(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res,
         _ptr(k_res), _ptr(v_res), n_res, res_cap, B, Hq, Hkv, D, kstore.G, kstore.bits,
         float(sm_scale), _ptr(out), _ptr(workspace), wbytes, _stream(stream))
     _check("kivi_decode_attend", st)
+    return out
+
+
+_noalloc_fn = None
+
+
+def kivi_decode_attend_noalloc(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res, v_res, n_res: int,
+                               Hkv: int, sm_scale: float, out=None, stream=None):
+    """The decode of kivi_decode_attend without a workspace argument: the split
+    scratch lives in a library-owned 2 MiB device array (for callers that may
+    not allocate device memory when they decode). Calls that overlap on the GPU
+    race on that array; make the first call on a device before any stream
+    capture."""
+    global _noalloc_fn
+    import torch
+    if _noalloc_fn is None:
+        fn = lib().kivi_decode_attend_noalloc
+        P, I = ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [P, P, P, P, P, P, P, I, I, P, P, I, I, I, I, I, I, I, I, ctypes.c_float, P, P]
+        fn.restype = I
+        _noalloc_fn = fn
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    res_cap = 0
+    if k_res is not None:
+        res_cap = _rows(k_res, D)
+        assert _rows(v_res, D) == res_cap
+    st = _noalloc_fn(
+        _ptr(q), _ptr(kstore.codes), _ptr(kstore.scale), _ptr(kstore.zero),
+        _ptr(vstore.codes), _ptr(vstore.scale), _ptr(vstore.zero), S_q, kstore.s_cap,
+        _ptr(k_res), _ptr(v_res), n_res, res_cap, B, Hq, Hkv, D, kstore.G, kstore.bits,
+        float(sm_scale), _ptr(out), _stream(stream))
+    _check("kivi_decode_attend_noalloc", st)
     return out
