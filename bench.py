@@ -5,8 +5,8 @@ One step = one pass of the whole hot path over one batch of the Qwen3-8B-like
 single-layer workload (B=1, H_kv=8, 32 query heads, D=128, 2238-token prompt,
 4-bit, G=32, residual_length=128):
   1. flush the oldest 2080 tokens of K and V into the packed store (one launch),
-  2. append the 158-token fp16 tail to the K and V residual windows,
-  3. dequantize the packed K and V stores back to fp16,
+  2. append the 158-token fp16 tail to the K and V residual windows (one launch),
+  3. dequantize the packed K and V stores back to fp16 (one launch),
   4. fused dequantize-and-attend decode of one query token per head (split over
      the cached tokens + log-sum-exp combine).
 value = algorithmic HBM bytes of the step / device time per step (GB/s).
@@ -189,12 +189,11 @@ class Instance:
         kv.kivi_flush_kv(self.k, self.v, w.R, self.kst, self.vst)
         if ev is not None:
             ev[1].record()
-        kv.kivi_residual_append(self.k[:, self.n_flush:], self.kres, 0, self.n_res)
-        kv.kivi_residual_append(self.v[:, self.n_flush:], self.vres, 0, self.n_res)
+        kv.kivi_residual_append_kv(self.k[:, self.n_flush:], self.v[:, self.n_flush:], self.kres, self.vres,
+                                   0, self.n_res)
         if ev is not None:
             ev[2].record()
-        kv.kivi_dequant(self.kst, self.n_flush, out=self.kdq)
-        kv.kivi_dequant(self.vst, self.n_flush, out=self.vdq)
+        kv.kivi_dequant_kv(self.kst, self.vst, self.n_flush, kout=self.kdq, vout=self.vdq)
         if ev is not None:
             ev[3].record()
         kv.kivi_decode_attend(self.q, self.kst, self.vst, self.n_flush, self.kres, self.vres, self.n_res,
@@ -211,7 +210,7 @@ class Instance:
 OPS = ["flush_kv", "residual_append", "dequant_kv", "decode_attend"]
 OP_KERNEL_FILE = {"flush_kv": "flush.cu", "residual_append": "residual.cu", "dequant_kv": "dequant.cu",
                   "decode_attend": "decode.cu"}
-LAUNCHES = {"flush_kv": 1, "residual_append": 2, "dequant_kv": 2}
+LAUNCHES = {"flush_kv": 1, "residual_append": 1, "dequant_kv": 1}
 
 
 def run_gb300(args, rank, world, local_rank):

@@ -149,6 +149,16 @@ kivi_status kivi_dequant(kivi_axis axis, const void* codes_u8, const float* scal
                          int s_cap, void* out_f16, kivi_stream_t stream);
 
 /*
+ * Key and value dequantize in one launch (both as kivi_dequant, same S and
+ * s_cap): kout from the key store, vout from the value store. Bit-exact with
+ * two kivi_dequant calls.
+ */
+kivi_status kivi_dequant_kv(const void* kcodes_u8, const float* kscale, const void* kzero_f16,
+                            const void* vcodes_u8, const float* vscale, const void* vzero_f16,
+                            int BH, int S, int D, int group_size, int bits, int s_cap,
+                            void* kout_f16, void* vout_f16, kivi_stream_t stream);
+
+/*
  * fp16 residual window res[BH, res_cap, D] ([F] "What we're actually
  * optimizing": the newest tokens stay fp16).
  * append:  copies src[bh, t, :] (src_bh_stride tokens between heads) for
@@ -163,6 +173,14 @@ kivi_status kivi_residual_append(const void* src_f16, int src_bh_stride, int n_n
                                  kivi_stream_t stream);
 kivi_status kivi_residual_compact(void* res_f16, int BH, int res_cap, int D, int n_res,
                                   int n_drop, kivi_stream_t stream);
+
+/* The same two operations on a key window and a value window of equal
+ * geometry, in one launch each. */
+kivi_status kivi_residual_append_kv(const void* k_src_f16, const void* v_src_f16, int src_bh_stride,
+                                    int n_new, void* k_res_f16, void* v_res_f16, int BH, int res_cap,
+                                    int D, int n_res, kivi_stream_t stream);
+kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, int res_cap, int D,
+                                     int n_res, int n_drop, kivi_stream_t stream);
 
 /*
  * Bytes of device workspace kivi_decode_attend needs for these sizes on the

@@ -19,8 +19,8 @@ import threading
 __all__ = [
     "KiviError", "KiviStore", "lib", "library_path",
     "kivi_status_string", "kivi_version", "kivi_flush_count",
-    "kivi_flush_keys", "kivi_flush_values", "kivi_flush_kv", "kivi_dequant",
-    "kivi_residual_append", "kivi_residual_compact",
+    "kivi_flush_keys", "kivi_flush_values", "kivi_flush_kv", "kivi_dequant", "kivi_dequant_kv",
+    "kivi_residual_append", "kivi_residual_compact", "kivi_residual_append_kv", "kivi_residual_compact_kv",
     "kivi_decode_workspace_size", "kivi_decode_attend", "kivi_decode_attend_noalloc",
 ]
 
@@ -61,6 +61,9 @@ def lib() -> ctypes.CDLL:
             "kivi_flush_values": ([P, I, I, I, I, I, I, I, P, P, P, I, I, IP, P], I),
             "kivi_flush_kv": ([P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, I, I, IP, P], I),
             "kivi_dequant": ([I, P, P, P, I, I, I, I, I, I, P, P], I),
+            "kivi_dequant_kv": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, P], I),
+            "kivi_residual_append_kv": ([P, P, I, I, P, P, I, I, I, I, P], I),
+            "kivi_residual_compact_kv": ([P, P, I, I, I, I, I, P], I),
             "kivi_residual_append": ([P, I, I, P, I, I, I, I, P], I),
             "kivi_residual_compact": ([P, I, I, I, I, I, P], I),
             "kivi_decode_workspace_size": ([I, I, I, I, I, I], Z),
@@ -184,6 +187,39 @@ def kivi_dequant(store: KiviStore, S: int, out=None, stream=None):
                             S, store.D, store.G, store.bits, store.s_cap, _ptr(out), _stream(stream))
     _check("kivi_dequant", st)
     return out
+
+
+def kivi_dequant_kv(kstore: KiviStore, vstore: KiviStore, S: int, kout=None, vout=None, stream=None):
+    """Key and value fp16 reconstructions of tokens [0, S) in one launch."""
+    import torch
+    if kout is None:
+        kout = torch.empty((kstore.BH, S, kstore.D), dtype=torch.float16, device=kstore.codes.device)
+    if vout is None:
+        vout = torch.empty((vstore.BH, S, vstore.D), dtype=torch.float16, device=vstore.codes.device)
+    st = lib().kivi_dequant_kv(_ptr(kstore.codes), _ptr(kstore.scale), _ptr(kstore.zero), _ptr(vstore.codes),
+                               _ptr(vstore.scale), _ptr(vstore.zero), kstore.BH, S, kstore.D, kstore.G,
+                               kstore.bits, kstore.s_cap, _ptr(kout), _ptr(vout), _stream(stream))
+    _check("kivi_dequant_kv", st)
+    return kout, vout
+
+
+def kivi_residual_append_kv(ksrc, vsrc, kres, vres, n_res: int, n_new=None, stream=None):
+    """Append n_new token rows of K and V behind the n_res live rows of their windows."""
+    n = ksrc.shape[1] if n_new is None else n_new
+    stride = _rows(ksrc, kres.shape[2])
+    assert _rows(vsrc, vres.shape[2]) == stride and kres.shape == vres.shape
+    st = lib().kivi_residual_append_kv(_ptr(ksrc), _ptr(vsrc), stride, n, _ptr(kres), _ptr(vres), kres.shape[0],
+                                       kres.shape[1], kres.shape[2], n_res, _stream(stream))
+    _check("kivi_residual_append_kv", st)
+    return n_res + n
+
+
+def kivi_residual_compact_kv(kres, vres, n_res: int, n_drop: int, stream=None):
+    assert kres.shape == vres.shape
+    st = lib().kivi_residual_compact_kv(_ptr(kres), _ptr(vres), kres.shape[0], kres.shape[1], kres.shape[2],
+                                        n_res, n_drop, _stream(stream))
+    _check("kivi_residual_compact_kv", st)
+    return n_res - n_drop
 
 
 def kivi_residual_append(src, res, n_res: int, n_new=None, stream=None):

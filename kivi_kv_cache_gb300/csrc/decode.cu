@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
     const int bh = b * a.Hkv + hk;
     const int h0 = hk * GQ;  // first query head of this KV group
 
+    pdl_wait();
     for (int h = 0; h < GQ; ++h)
         sm.q[h][tid] = __half2float(a.q[((long long)b * a.Hq + h0 + h) * kD + tid]) * a.score_scale;
 
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
     }
 
     // ---- partials (or the final output when there is a single split) ----
+    pdl_trigger();
     __syncthreads();
     if (warp == 0 && lane == 0) {
 #pragma unroll
@@ -279,28 +281,59 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
     }
 }
 
-// out[b, h, :] = sum_i o_i * 2^(m_i - M) / sum_i l_i * 2^(m_i - M)
+// out[b, h, :] = sum_i o_i * 2^(m_i - M) / sum_i l_i * 2^(m_i - M).
+// The split weights are computed once into shared memory (all loads issued
+// in parallel), then each thread sums its channel with independent loads.
+constexpr int kMaxSplitSmem = 1024;
+
 __global__ void __launch_bounds__(kThreads) decode_combine_kernel(DecodeArgs a) {
+    __shared__ float wsm[kMaxSplitSmem];
+    __shared__ float red[kThreads / 32];
+    pdl_wait();
     const long long bq = blockIdx.x;
-    const float* ml = a.part_ml + bq * a.n_split * 2;
+    const int n = a.n_split;
+    const float* ml = a.part_ml + bq * n * 2;
     float M = -INFINITY;
-    for (int i = 0; i < a.n_split; ++i) M = fmaxf(M, ml[2 * i]);
-    float L = 0.f, acc = 0.f;
-    for (int i = 0; i < a.n_split; ++i) {
+    for (int i = threadIdx.x; i < n; i += kThreads) M = fmaxf(M, ml[2 * i]);
+    M = warp_max(M);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
+    float L = 0.f;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
         const float w = exp2f(ml[2 * i] - M);
+        if (i < kMaxSplitSmem) wsm[i] = w;
         L = fmaf(ml[2 * i + 1], w, L);
-        acc = fmaf(a.part_o[(bq * a.n_split + i) * kD + threadIdx.x], w, acc);
     }
-    a.out[bq * kD + threadIdx.x] = acc / L;
+    L = warp_sum(L);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = L;
+    __syncthreads();
+    L = red[0] + red[1] + red[2] + red[3];
+    const float* po = a.part_o + bq * n * kD + threadIdx.x;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    int i = 0;
+    for (; i + 4 <= n; i += 4) {
+        const float w0 = i < kMaxSplitSmem ? wsm[i] : exp2f(ml[2 * i] - M);
+        const float w1 = i + 1 < kMaxSplitSmem ? wsm[i + 1] : exp2f(ml[2 * i + 2] - M);
+        const float w2 = i + 2 < kMaxSplitSmem ? wsm[i + 2] : exp2f(ml[2 * i + 4] - M);
+        const float w3 = i + 3 < kMaxSplitSmem ? wsm[i + 3] : exp2f(ml[2 * i + 6] - M);
+        acc0 = fmaf(po[(long long)i * kD], w0, acc0);
+        acc1 = fmaf(po[(long long)(i + 1) * kD], w1, acc1);
+        acc2 = fmaf(po[(long long)(i + 2) * kD], w2, acc2);
+        acc3 = fmaf(po[(long long)(i + 3) * kD], w3, acc3);
+    }
+    for (; i < n; ++i) acc0 = fmaf(po[(long long)i * kD], i < kMaxSplitSmem ? wsm[i] : exp2f(ml[2 * i] - M), acc0);
+    a.out[bq * kD + threadIdx.x] = ((acc0 + acc1) + (acc2 + acc3)) / L;
 }
 
 template <int BITS, int GQ>
 cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
     dim3 grid(a.n_split, a.Hkv, a.B);
-    decode_split_kernel<BITS, GQ><<<grid, kThreads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(decode_split_kernel<BITS, GQ>, grid, kThreads, 0, stream, a);
     if (e != cudaSuccess || a.n_split == 1) return e;
-    decode_combine_kernel<<<a.B * a.Hq, kThreads, 0, stream>>>(a);
+    e = launch_pdl(decode_combine_kernel, dim3(a.B * a.Hq), kThreads, 0, stream, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

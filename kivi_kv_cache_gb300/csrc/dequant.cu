@@ -3,11 +3,19 @@
 // recon = fp16_rn(RN(RN(q * scale) + zero)): VeloxQuant-MLX blog, "A 5.65x
 // Metal Kernel That Made My LLM Exactly 0% Faster", "What we're actually
 // optimizing" (recon = q*scale + zero) and "Three ways to be off by one bit"
-// #1 (multiply, then a separate add: two roundings, never an FMA).
+// #1 (multiply, then a separate add: two roundings, never one fused op for
+// the reconstruction).
+//
+// Arithmetic: a byte permute turns each code q into the fp32 pattern of
+// 2^23 + q. Then fma(2^23 + q, s, -2^23 * s) is the exact value q * s rounded
+// once, i.e. RN(q * s) (-2^23 * s is exact: a power-of-two scaling). The add
+// of zero is a separate round-to-nearest add, as the method requires. Both
+// run as packed fp32x2 operations.
 //
 // Memory pattern: each thread owns 8 channels (one 16-byte fp16 store per
-// token row); code words are 4 bytes (4-bit) or 2 bytes (2-bit) per thread
-// per row, so a warp's loads and stores cover whole contiguous row segments.
+// token row); a warp's loads and stores cover whole contiguous row segments.
+// Keys and values can run in one launch (blocks [0, kbx) of each grid row
+// dequantize keys, the rest values); blockIdx.y is the head.
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
@@ -17,18 +25,47 @@ namespace {
 
 constexpr int kThreads = 128;
 
+// fp32 patterns 2^23 + q of the 8 codes of one row segment (element i at bit
+// offset i*BITS): qm[k] for element k.
 template <int BITS>
-__device__ __forceinline__ uint4 recon8(uint32_t w, const float* s, const float* z) {
-    constexpr uint32_t M = Levels<BITS>::value;
-    float r[8];
+__device__ __forceinline__ void codes_to_magic(uint32_t w, uint32_t (&qm)[8]) {
+    const uint32_t C = 0x4B000000u;  // byte 3 = 0x4B, bytes 0..2 = 0
+    if (BITS == 4) {
+        const uint32_t e = w & 0x0f0f0f0fu;         // elements 0,2,4,6
+        const uint32_t o = (w >> 4) & 0x0f0f0f0fu;  // elements 1,3,5,7
+        qm[0] = __byte_perm(e, C, 0x7440);
+        qm[2] = __byte_perm(e, C, 0x7441);
+        qm[4] = __byte_perm(e, C, 0x7442);
+        qm[6] = __byte_perm(e, C, 0x7443);
+        qm[1] = __byte_perm(o, C, 0x7440);
+        qm[3] = __byte_perm(o, C, 0x7441);
+        qm[5] = __byte_perm(o, C, 0x7442);
+        qm[7] = __byte_perm(o, C, 0x7443);
+    } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) r[k] = recon((w >> (k * BITS)) & M, s[k], z[k]);
-    uint4 o;
-    o.x = h2_as_u32(__floats2half2_rn(r[0], r[1]));
-    o.y = h2_as_u32(__floats2half2_rn(r[2], r[3]));
-    o.z = h2_as_u32(__floats2half2_rn(r[4], r[5]));
-    o.w = h2_as_u32(__floats2half2_rn(r[6], r[7]));
-    return o;
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t p = (w >> (2 * k)) & 0x0303u;  // elements k, k+4
+            qm[k] = __byte_perm(p, C, 0x7440);
+            qm[k + 4] = __byte_perm(p, C, 0x7441);
+        }
+    }
+}
+
+// 8 reconstructions -> 8 fp16 (one 16-byte vector). s2/ns2/z2: per element
+// scale, -2^23*scale and zero, as fp32x2 pairs.
+template <int BITS>
+__device__ __forceinline__ uint4 recon8(uint32_t w, const f32x2 (&s2)[4], const f32x2 (&ns2)[4],
+                                        const f32x2 (&z2)[4]) {
+    uint32_t qm[8];
+    codes_to_magic<BITS>(w, qm);
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const f32x2 q2 = pk(__uint_as_float(qm[2 * k]), __uint_as_float(qm[2 * k + 1]));
+        const float2 r = upk(add2(fma2(q2, s2[k], ns2[k]), z2[k]));
+        h[k] = h2_as_u32(__floats2half2_rn(r.x, r.y));
+    }
+    return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 template <int BITS>
@@ -37,71 +74,62 @@ __device__ __forceinline__ uint32_t load_word(const uint8_t* p) {
     return __ldg(reinterpret_cast<const uint16_t*>(p));
 }
 
-// keys: one warp per (head, key group, 64-channel half); lane = part*8 + octet,
+// keys: one warp per (head, key group, 64-channel half); lane = part*8 + oc,
 // part owns 8 tokens of the group. Scale and zero are per (group, channel).
 template <int BITS>
-__global__ void __launch_bounds__(kThreads) dequant_keys_kernel(DequantArgs a) {
+__device__ __forceinline__ void dequant_keys_warp(const DequantArgs& a, int warp_id, int bh) {
     constexpr int ROWB = kD * BITS / 8;
-    const long long warp_id = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int octet = (int)(warp_id & 1) * 8 + (lane & 7);
+    const int octet = (warp_id & 1) * 8 + (lane & 7);
     const int part = lane >> 3;
-    const long long grp = warp_id >> 1;
-    const int ng = (a.S + kG - 1) / kG;
-    if (grp >= (long long)a.BH * ng) return;
-    const int bh = (int)(grp / ng);
-    const int g = (int)(grp - (long long)bh * ng);
+    const int g = warp_id >> 1;
+    if (g >= (a.S + kG - 1) / kG) return;
     const int t0 = g * kG + part * 8;
 
-    const long long m = ((long long)bh * (a.s_cap / kG) + g) * kD + octet * 8;
-    const float4 s0 = __ldg(reinterpret_cast<const float4*>(a.scale + m));
-    const float4 s1 = __ldg(reinterpret_cast<const float4*>(a.scale + m) + 1);
-    const uint4 zw = __ldg(reinterpret_cast<const uint4*>(a.zero + m));
-    const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    float z[8];
-    {
-        const uint32_t zz[4] = {zw.x, zw.y, zw.z, zw.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(u32_as_h2(zz[k]));
-            z[2 * k] = f.x;
-            z[2 * k + 1] = f.y;
-        }
-    }
     const uint8_t* crow = a.codes + ((long long)bh * a.s_cap + t0) * ROWB + octet * BITS;
     uint32_t w[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = (t0 + i < a.S) ? load_word<BITS>(crow + (long long)i * ROWB) : 0u;
+    for (int i = 0; i < 8; ++i) w[i] = (t0 + i < a.S) ? load_word<BITS>(crow + i * ROWB) : 0u;
+    const long long m = ((long long)bh * (a.s_cap / kG) + g) * kD + octet * 8;
+    const float4 sa = __ldg(reinterpret_cast<const float4*>(a.scale + m));
+    const float4 sb = __ldg(reinterpret_cast<const float4*>(a.scale + m) + 1);
+    const uint4 zw = __ldg(reinterpret_cast<const uint4*>(a.zero + m));
+    pdl_trigger();
+    const float s[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+    const uint32_t zz[4] = {zw.x, zw.y, zw.z, zw.w};
+    f32x2 s2[4], ns2[4], z2[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        s2[k] = pk(s[2 * k], s[2 * k + 1]);
+        ns2[k] = pk(-kMagic * s[2 * k], -kMagic * s[2 * k + 1]);
+        const float2 f = __half22float2(u32_as_h2(zz[k]));
+        z2[k] = pk(f.x, f.y);
+    }
     uint4* orow = reinterpret_cast<uint4*>(a.out) + ((long long)bh * a.S + t0) * (kD / 8) + octet;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        if (t0 + i < a.S) orow[(long long)i * (kD / 8)] = recon8<BITS>(w[i], s, z);
+        if (t0 + i < a.S) orow[i * (kD / 8)] = recon8<BITS>(w[i], s2, ns2, z2);
 }
 
-// values: one warp per 8 consecutive (head, token) rows; lane = sub*16 + octet,
-// iteration i handles row 2*i + sub. Scale and zero are per (token, group).
+// values: one warp per 8 consecutive tokens of one head; lane = sub*16 +
+// octet, iteration i handles token 2*i + sub. Scale and zero are per (token,
+// 32-channel group).
 template <int BITS>
-__global__ void __launch_bounds__(kThreads) dequant_values_kernel(DequantArgs a) {
+__device__ __forceinline__ void dequant_values_warp(const DequantArgs& a, int warp_id, int bh) {
     constexpr int ROWB = kD * BITS / 8;
     constexpr int RPT = 4;
-    const long long warp_id = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int octet = lane & 15;
     const int sub = lane >> 4;
-    const long long rows = (long long)a.BH * a.S;
-    const long long r0 = warp_id * (2 * RPT);
-    if (r0 >= rows) return;
+    const int tw = warp_id * (2 * RPT);
+    if (tw >= a.S) return;
+    const long long row0 = (long long)bh * a.s_cap + tw + sub;
     uint32_t w[RPT];
     float s[RPT], z[RPT];
-    long long orow[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        const long long r = r0 + 2 * i + sub;
-        const int bh = (int)(r / a.S);
-        const int t = (int)(r - (long long)bh * a.S);
-        const long long row = (long long)bh * a.s_cap + t;
-        orow[i] = r;
-        if (r < rows) {
+        const long long row = row0 + 2 * i;
+        if (tw + 2 * i + sub < a.S) {
             w[i] = load_word<BITS>(a.codes + row * ROWB + octet * BITS);
             s[i] = __ldg(a.scale + row * (kD / kG) + (octet >> 2));
             z[i] = __half2float(a.zero[row * (kD / kG) + (octet >> 2)]);
@@ -111,31 +139,84 @@ __global__ void __launch_bounds__(kThreads) dequant_values_kernel(DequantArgs a)
             z[i] = 0.f;
         }
     }
+    pdl_trigger();
+    uint4* orow = reinterpret_cast<uint4*>(a.out) + ((long long)bh * a.S + tw + sub) * (kD / 8) + octet;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        if (orow[i] < rows) {
-            const float sv[8] = {s[i], s[i], s[i], s[i], s[i], s[i], s[i], s[i]};
-            const float zv[8] = {z[i], z[i], z[i], z[i], z[i], z[i], z[i], z[i]};
-            reinterpret_cast<uint4*>(a.out)[orow[i] * (kD / 8) + octet] = recon8<BITS>(w[i], sv, zv);
+        if (tw + 2 * i + sub < a.S) {
+            const f32x2 s1 = pk(s[i], s[i]), n1 = pk(-kMagic * s[i], -kMagic * s[i]), z1 = pk(z[i], z[i]);
+            const f32x2 s2[4] = {s1, s1, s1, s1}, ns2[4] = {n1, n1, n1, n1}, z2[4] = {z1, z1, z1, z1};
+            orow[2 * i * (kD / 8)] = recon8<BITS>(w[i], s2, ns2, z2);
         }
     }
+}
+
+int key_blocks_x(int S) { return ((S + kG - 1) / kG * 2 + 3) / 4; }
+int value_blocks_x(int S) { return (S + 31) / 32; }
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) dequant_keys_kernel(DequantArgs a) {
+    pdl_wait();
+    dequant_keys_warp<BITS>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) dequant_values_kernel(DequantArgs a) {
+    pdl_wait();
+    dequant_values_warp<BITS>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) dequant_kv_kernel(DequantArgs k, DequantArgs v, int kbx) {
+    pdl_wait();
+    if ((int)blockIdx.x < kbx)
+        dequant_keys_warp<BITS>(k, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+    else
+        dequant_values_warp<BITS>(v, (blockIdx.x - kbx) * 4 + (threadIdx.x >> 5), blockIdx.y);
+}
+
+DequantArgs head_slice(const DequantArgs& a, int h0, int nh, int bits, int axis) {
+    DequantArgs s = a;
+    s.BH = nh;
+    s.codes += (long long)h0 * a.s_cap * (kD * bits / 8);
+    const long long meta = axis == 0 ? (long long)(a.s_cap / kG) * kD : (long long)a.s_cap * (kD / kG);
+    s.scale += h0 * meta;
+    s.zero += h0 * meta;
+    s.out += (long long)h0 * a.S * kD;
+    return s;
 }
 
 }  // namespace
 
 cudaError_t launch_dequant(int axis, const DequantArgs& a, int bits, cudaStream_t stream) {
-    long long warps;
-    if (axis == 0) warps = (long long)a.BH * ((a.S + kG - 1) / kG) * 2;
-    else warps = ((long long)a.BH * a.S + 7) / 8;
-    const long long blocks = (warps * 32 + kThreads - 1) / kThreads;
-    if (blocks <= 0) return cudaSuccess;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (axis == 0) {
-        if (bits == 4) dequant_keys_kernel<4><<<(unsigned)blocks, kThreads, 0, stream>>>(a);
-        else dequant_keys_kernel<2><<<(unsigned)blocks, kThreads, 0, stream>>>(a);
-    } else {
-        if (bits == 4) dequant_values_kernel<4><<<(unsigned)blocks, kThreads, 0, stream>>>(a);
-        else dequant_values_kernel<2><<<(unsigned)blocks, kThreads, 0, stream>>>(a);
+    if (a.S <= 0 || a.BH <= 0) return cudaSuccess;
+    const int bx = axis == 0 ? key_blocks_x(a.S) : value_blocks_x(a.S);
+    for (int h0 = 0; h0 < a.BH; h0 += 65535) {
+        const int nh = a.BH - h0 < 65535 ? a.BH - h0 : 65535;
+        const DequantArgs s = head_slice(a, h0, nh, bits, axis);
+        const dim3 grid(bx, nh);
+        cudaError_t e;
+        if (axis == 0)
+            e = bits == 4 ? launch_pdl(dequant_keys_kernel<4>, grid, kThreads, 0, stream, s)
+                          : launch_pdl(dequant_keys_kernel<2>, grid, kThreads, 0, stream, s);
+        else
+            e = bits == 4 ? launch_pdl(dequant_values_kernel<4>, grid, kThreads, 0, stream, s)
+                          : launch_pdl(dequant_values_kernel<2>, grid, kThreads, 0, stream, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_kv(const DequantArgs& k, const DequantArgs& v, int bits, cudaStream_t stream) {
+    if (k.S <= 0 || k.BH <= 0) return cudaSuccess;
+    const int kbx = key_blocks_x(k.S), vbx = value_blocks_x(v.S);
+    for (int h0 = 0; h0 < k.BH; h0 += 65535) {
+        const int nh = k.BH - h0 < 65535 ? k.BH - h0 : 65535;
+        const DequantArgs ks = head_slice(k, h0, nh, bits, 0), vs = head_slice(v, h0, nh, bits, 1);
+        const dim3 grid(kbx + vbx, nh);
+        cudaError_t e = bits == 4 ? launch_pdl(dequant_kv_kernel<4>, grid, kThreads, 0, stream, ks, vs, kbx)
+                                  : launch_pdl(dequant_kv_kernel<2>, grid, kThreads, 0, stream, ks, vs, kbx);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

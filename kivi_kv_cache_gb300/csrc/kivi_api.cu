@@ -197,6 +197,34 @@ kivi_status kivi_dequant(kivi_axis axis, const void* codes_u8, const float* scal
     return from_cuda(launch_dequant((int)axis, a, bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kivi_status kivi_dequant_kv(const void* kcodes_u8, const float* kscale, const void* kzero_f16,
+                            const void* vcodes_u8, const float* vscale, const void* vzero_f16, int BH, int S,
+                            int D, int group_size, int bits, int s_cap, void* kout_f16, void* vout_f16,
+                            kivi_stream_t stream) {
+    kivi_status st = shape_check(D, group_size, bits);
+    if (st != KIVI_OK) return st;
+    if (BH <= 0 || S < 0 || s_cap <= 0 || s_cap % group_size != 0 || S > s_cap) return KIVI_ERR_INVALID_ARG;
+    if (S == 0) return KIVI_OK;
+    if (!kcodes_u8 || !kscale || !kzero_f16 || !vcodes_u8 || !vscale || !vzero_f16 || !kout_f16 || !vout_f16)
+        return KIVI_ERR_INVALID_ARG;
+    if (!aligned16(kcodes_u8) || !aligned16(kscale) || !aligned16(kzero_f16) || !aligned16(vcodes_u8) ||
+        !aligned16(vscale) || !aligned16(vzero_f16) || !aligned16(kout_f16) || !aligned16(vout_f16))
+        return KIVI_ERR_ALIGNMENT;
+    DequantArgs k, v;
+    k.codes = static_cast<const uint8_t*>(kcodes_u8);
+    k.scale = kscale;
+    k.zero = static_cast<const __half*>(kzero_f16);
+    k.out = static_cast<__half*>(kout_f16);
+    v.codes = static_cast<const uint8_t*>(vcodes_u8);
+    v.scale = vscale;
+    v.zero = static_cast<const __half*>(vzero_f16);
+    v.out = static_cast<__half*>(vout_f16);
+    k.BH = v.BH = BH;
+    k.S = v.S = S;
+    k.s_cap = v.s_cap = s_cap;
+    return from_cuda(launch_dequant_kv(k, v, bits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kivi_status kivi_residual_append(const void* src_f16, int src_bh_stride, int n_new, void* res_f16,
                                  int BH, int res_cap, int D, int n_res, kivi_stream_t stream) {
     if (D != kD) return KIVI_ERR_UNSUPPORTED;
@@ -206,8 +234,8 @@ kivi_status kivi_residual_append(const void* src_f16, int src_bh_stride, int n_n
     if (n_new == 0) return KIVI_OK;
     if (!src_f16 || !res_f16) return KIVI_ERR_INVALID_ARG;
     if (!aligned16(src_f16) || !aligned16(res_f16)) return KIVI_ERR_ALIGNMENT;
-    return from_cuda(launch_residual_append(static_cast<const __half*>(src_f16), src_bh_stride, n_new,
-                                            static_cast<__half*>(res_f16), BH, res_cap, n_res,
+    return from_cuda(launch_residual_append(static_cast<const __half*>(src_f16), nullptr, src_bh_stride, n_new,
+                                            static_cast<__half*>(res_f16), nullptr, BH, res_cap, n_res,
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -219,8 +247,37 @@ kivi_status kivi_residual_compact(void* res_f16, int BH, int res_cap, int D, int
     if (n_drop == 0 || n_drop == n_res) return KIVI_OK;
     if (!res_f16) return KIVI_ERR_INVALID_ARG;
     if (!aligned16(res_f16)) return KIVI_ERR_ALIGNMENT;
-    return from_cuda(launch_residual_compact(static_cast<__half*>(res_f16), BH, res_cap, n_res, n_drop,
+    return from_cuda(launch_residual_compact(static_cast<__half*>(res_f16), nullptr, BH, res_cap, n_res, n_drop,
                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kivi_status kivi_residual_append_kv(const void* k_src_f16, const void* v_src_f16, int src_bh_stride, int n_new,
+                                    void* k_res_f16, void* v_res_f16, int BH, int res_cap, int D, int n_res,
+                                    kivi_stream_t stream) {
+    if (D != kD) return KIVI_ERR_UNSUPPORTED;
+    if (BH <= 0 || n_new < 0 || n_res < 0 || res_cap <= 0 || src_bh_stride < n_new ||
+        (long long)n_res + n_new > res_cap)
+        return KIVI_ERR_INVALID_ARG;
+    if (n_new == 0) return KIVI_OK;
+    if (!k_src_f16 || !v_src_f16 || !k_res_f16 || !v_res_f16) return KIVI_ERR_INVALID_ARG;
+    if (!aligned16(k_src_f16) || !aligned16(v_src_f16) || !aligned16(k_res_f16) || !aligned16(v_res_f16))
+        return KIVI_ERR_ALIGNMENT;
+    return from_cuda(launch_residual_append(static_cast<const __half*>(k_src_f16),
+                                            static_cast<const __half*>(v_src_f16), src_bh_stride, n_new,
+                                            static_cast<__half*>(k_res_f16), static_cast<__half*>(v_res_f16), BH,
+                                            res_cap, n_res, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, int res_cap, int D, int n_res,
+                                     int n_drop, kivi_stream_t stream) {
+    if (D != kD) return KIVI_ERR_UNSUPPORTED;
+    if (BH <= 0 || res_cap <= 0 || n_res < 0 || n_res > res_cap || n_drop < 0 || n_drop > n_res)
+        return KIVI_ERR_INVALID_ARG;
+    if (n_drop == 0 || n_drop == n_res) return KIVI_OK;
+    if (!k_res_f16 || !v_res_f16) return KIVI_ERR_INVALID_ARG;
+    if (!aligned16(k_res_f16) || !aligned16(v_res_f16)) return KIVI_ERR_ALIGNMENT;
+    return from_cuda(launch_residual_compact(static_cast<__half*>(k_res_f16), static_cast<__half*>(v_res_f16), BH,
+                                             res_cap, n_res, n_drop, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D) {

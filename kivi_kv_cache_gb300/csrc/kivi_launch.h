@@ -68,12 +68,34 @@ struct DecodePlan {
     int n_tiles;
 };
 
+// Launch with programmatic stream serialization allowed: the kernel may start
+// while the previous kernel on the stream finishes; it must (and every kernel
+// of this library does) execute griddepcontrol.wait before touching memory.
+template <typename... Exp, typename... Act>
+inline cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Act&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+}
+
 cudaError_t launch_flush(int axis, const FlushArgs& a, int bits, cudaStream_t stream);
 cudaError_t launch_flush_kv(const FlushArgs& k, const FlushArgs& v, int bits, cudaStream_t stream);
 cudaError_t launch_dequant(int axis, const DequantArgs& a, int bits, cudaStream_t stream);
-cudaError_t launch_residual_append(const __half* src, long long src_bh_stride, int n_new,
-                                   __half* res, int BH, int res_cap, int n_res, cudaStream_t stream);
-cudaError_t launch_residual_compact(__half* res, int BH, int res_cap, int n_res, int n_drop,
+cudaError_t launch_dequant_kv(const DequantArgs& k, const DequantArgs& v, int bits, cudaStream_t stream);
+// src1/res1 may be null (one tensor); otherwise both pairs are handled in one launch
+cudaError_t launch_residual_append(const __half* src0, const __half* src1, long long src_bh_stride,
+                                   int n_new, __half* res0, __half* res1, int BH, int res_cap, int n_res,
+                                   cudaStream_t stream);
+cudaError_t launch_residual_compact(__half* res0, __half* res1, int BH, int res_cap, int n_res, int n_drop,
                                     cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 

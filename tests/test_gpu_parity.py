@@ -295,3 +295,39 @@ def test_many_sequence_lengths_one_build():
         n = kv.kivi_flush_count(S, 32, 32)
         out, ref = decode_case(w, n, S - n, k, v, q)
         assert np.max(np.abs(out - ref)) <= TOL, S
+
+
+@pytest.mark.parametrize("name", ["qwen8b", "long2bit"])
+def test_dequant_kv_equals_oracle(name):
+    w = synth.WORKLOADS[name]
+    k, v, _ = synth.prefill_inputs(w)
+    n = kv.kivi_flush_count(w.S, w.R, w.G)
+    ks = kv.KiviStore(0, w.BH, n, w.D, w.G, w.bits, device=DEV)
+    vs = kv.KiviStore(1, w.BH, n, w.D, w.G, w.bits, device=DEV)
+    kv.kivi_flush_kv(dev(k), dev(v), w.R, ks, vs)
+    kd, vd = kv.kivi_dequant_kv(ks, vs, n)
+    rk = oracle.flush(0, k, n, oracle.Store(0, w.BH, n, w.D, w.G, w.bits))
+    rv = oracle.flush(1, v, n, oracle.Store(1, w.BH, n, w.D, w.G, w.bits))
+    assert np.array_equal(host(kd).view(np.uint16), oracle.dequant(rk, n).view(np.uint16))
+    assert np.array_equal(host(vd).view(np.uint16), oracle.dequant(rv, n).view(np.uint16))
+    # ragged S through the fused call
+    kd2, vd2 = kv.kivi_dequant_kv(ks, vs, n - 13)
+    assert np.array_equal(host(kd2).view(np.uint16), oracle.dequant(rk, n - 13).view(np.uint16))
+    assert np.array_equal(host(vd2).view(np.uint16), oracle.dequant(rv, n - 13).view(np.uint16))
+
+
+def test_residual_kv_append_and_compact():
+    rng = np.random.default_rng(18)
+    kres = synth.normal(rng, (5, 160, 128))
+    vres = synth.normal(rng, (5, 160, 128))
+    ksrc = synth.normal(rng, (5, 70, 128))
+    vsrc = synth.normal(rng, (5, 70, 128))
+    gk, gv = dev(kres), dev(vres)
+    assert kv.kivi_residual_append_kv(dev(ksrc), dev(vsrc), gk, gv, 90, n_new=70) == 160
+    oracle.residual_append(kres, 90, ksrc, 70)
+    oracle.residual_append(vres, 90, vsrc, 70)
+    assert np.array_equal(host(gk), kres) and np.array_equal(host(gv), vres)
+    assert kv.kivi_residual_compact_kv(gk, gv, 160, 32) == 128
+    oracle.residual_compact(kres, 160, 32)
+    oracle.residual_compact(vres, 160, 32)
+    assert np.array_equal(host(gk), kres) and np.array_equal(host(gv), vres)
