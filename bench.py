@@ -12,9 +12,11 @@ single-layer workload (B=1, H_kv=8, 32 query heads, D=128, 2238-token prompt,
 value = algorithmic HBM bytes of the step / device time per step (GB/s).
 
 Inputs rotate through a pool of independent instances whose total size is
-several times the L2 cache, so no step finds its inputs in L2. Each instance's
-step is captured once in a CUDA graph (timing events between the ops), and the
-timed region replays K graphs back to back between two CUDA events.
+several times the L2 cache, so no step finds its inputs in L2. Steps are
+captured in CUDA graphs of 8 consecutive steps on 8 distinct instances; the
+timed region replays them (K steps in all) between two CUDA events. Each op's
+average launch duration is timed the same way on graphs of 8 launches of that
+op alone.
 
 --impl reference times the plain CPU oracle on the same workload and metric.
 """
@@ -208,6 +210,7 @@ class Instance:
 
 
 OPS = ["flush_kv", "residual_append", "dequant_kv", "decode_attend"]
+GRAPH_STEPS = 8
 OP_KERNEL_FILE = {"flush_kv": "flush.cu", "residual_append": "residual.cu", "dequant_kv": "dequant.cu",
                   "decode_attend": "decode.cu"}
 LAUNCHES = {"flush_kv": 1, "residual_append": 1, "dequant_kv": 1}
@@ -229,36 +232,33 @@ def run_gb300(args, rank, world, local_rank):
 
     probe = Instance(w, 1000 * rank + 0, dev, kv, synth)
     inst_bytes = probe.nbytes()
+    # pool: a multiple of GRAPH_STEPS independent instances, >= 4x L2 in total
     pool = args.pool or int(min(64, max(2, math.ceil(4 * l2 / inst_bytes))))
+    pool = max(GRAPH_STEPS, (pool + GRAPH_STEPS - 1) // GRAPH_STEPS * GRAPH_STEPS)
     insts = [probe] + [Instance(w, 1000 * rank + i, dev, kv, synth) for i in range(1, pool)]
     n_split = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, probe.n_flush, probe.n_res, w.D)
     decode_launches = 2 if n_split > 0 else 1
     launches_per_step = sum(LAUNCHES.values()) + decode_launches
 
-    # eager warm-up, then one graph per instance with timing events between ops
+    # eager warm-up; then CUDA graphs of GRAPH_STEPS consecutive steps, each on
+    # its own instance (a graph launch costs microseconds; steps inside a graph
+    # follow each other with programmatic dependent launch), plus one-step
+    # graphs for a remainder of K that is not a multiple of GRAPH_STEPS
     for i in range(max(1, args.warmup)):
         insts[i % pool].step()
     torch.cuda.synchronize()
-    use_events = True
-    graphs, events = [], []
-    try:
-        for inst in insts:
-            ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                inst.step(ev)
-            graphs.append(g)
-            events.append(ev)
-    except Exception:
-        use_events = False
-        graphs, events = [], []
-        for inst in insts:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                inst.step()
-            graphs.append(g)
-    for i in range(args.warmup):
-        graphs[i % pool].replay()
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    multi = [capture(lambda j=j: [insts[j * GRAPH_STEPS + t].step() for t in range(GRAPH_STEPS)])
+             for j in range(pool // GRAPH_STEPS)]
+    single = [capture(lambda I=I: I.step()) for I in insts]
+    for i in range(max(1, args.warmup // GRAPH_STEPS)):
+        multi[i % len(multi)].replay()
     torch.cuda.synchronize()
 
     gpu_id = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local_rank)
@@ -270,9 +270,12 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    n_multi, n_rest = divmod(args.steps, GRAPH_STEPS)
     start.record()
-    for i in range(args.steps):
-        graphs[i % pool].replay()
+    for i in range(n_multi):
+        multi[i % len(multi)].replay()
+    for i in range(n_rest):
+        single[i % pool].replay()
     end.record()
     torch.cuda.synchronize()
     if world > 1:
@@ -284,18 +287,34 @@ def run_gb300(args, rank, world, local_rank):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
-    # per-op durations: the events of each graph hold its last replay in the timed region
+    # per-op average launch duration: CUDA events on the launching stream
+    # around replays of a graph of GRAPH_STEPS launches of that op alone, on
+    # consecutive instances of the same rotating pool and with the step's
+    # launch configuration
+    op_fns = {
+        "flush_kv": lambda I: kv.kivi_flush_kv(I.k, I.v, w.R, I.kst, I.vst),
+        "residual_append": lambda I: kv.kivi_residual_append_kv(I.k[:, I.n_flush:], I.v[:, I.n_flush:], I.kres,
+                                                                 I.vres, 0, I.n_res),
+        "dequant_kv": lambda I: kv.kivi_dequant_kv(I.kst, I.vst, I.n_flush, kout=I.kdq, vout=I.vdq),
+        "decode_attend": lambda I: kv.kivi_decode_attend(I.q, I.kst, I.vst, I.n_flush, I.kres, I.vres, I.n_res,
+                                                         w.Hkv, w.sm_scale, out=I.out, workspace=I.ws),
+    }
     op_ms = {}
-    if use_events and args.steps >= pool:
-        for j, op in enumerate(OPS):
-            op_ms[op] = statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in events)
-    else:
-        for j, op in enumerate(OPS):  # eager fallback: time each op alone, same rotation
-            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(pool)]
-            for i in range(pool):
-                insts[i].step(ev[i])
-            torch.cuda.synchronize()
-            op_ms[op] = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
+    reps = max(4, min(200, args.steps // GRAPH_STEPS))
+    for op, fn in op_fns.items():
+        gs = [capture(lambda j=j, fn=fn: [fn(insts[j * GRAPH_STEPS + t]) for t in range(GRAPH_STEPS)])
+              for j in range(pool // GRAPH_STEPS)]
+        for g in gs:
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(reps):
+            gs[i % len(gs)].replay()
+        e1.record()
+        torch.cuda.synchronize()
+        op_ms[op] = e0.elapsed_time(e1) / (reps * GRAPH_STEPS)
+        del gs
 
     ob = op_bytes(w, probe.n_flush, probe.n_res)
     step_bytes = sum(ob.values())
@@ -362,7 +381,7 @@ def run_gb300(args, rank, world, local_rank):
                    "n_flush": probe.n_flush, "n_res": probe.n_res,
                    "l2": "rotating pool of %d independent instances, %.0f MB total (L2 %d MB)"
                          % (pool, pool * inst_bytes / 2 ** 20, l2 >> 20),
-                   "timing": "CUDA graph per instance, K replays between CUDA events",
+                   "timing": "graphs of %d steps on distinct instances, K steps between CUDA events" % GRAPH_STEPS,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "ops": ops,
         "decode_tokens_per_s": round(w.B / decode_s, 1),
@@ -372,7 +391,7 @@ def run_gb300(args, rank, world, local_rank):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clock,
         "peak_hbm_gbs": peak,
-        "per_op_timing": "graph events (last replay of each instance)" if use_events else "eager events",
+        "per_op_timing": "CUDA events around graphs of %d back-to-back launches of the op" % GRAPH_STEPS,
     }
     return line
 

@@ -350,6 +350,13 @@ cudaError_t launch_bits(const DecodeArgs& a, int gq, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.n_split == 1) return cudaSuccess;
+    cudaError_t e = launch_pdl(decode_combine_kernel, dim3(a.B * a.Hq), kThreads, 0, stream, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, int bits, int gq, cudaStream_t stream) {
     return bits == 4 ? launch_bits<4>(a, gq, stream) : launch_bits<2>(a, gq, stream);
 }

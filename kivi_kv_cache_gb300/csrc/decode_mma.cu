@@ -1,0 +1,671 @@
+// decode_mma.cu -- fused dequantize-and-attend single-token decode on the
+// tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation), for
+// grouped-query groups of up to 4 query heads per KV head.
+//
+// Method: VeloxQuant-MLX blog, "A 5.65x Metal Kernel That Made My LLM Exactly
+// 0% Faster", "So why does the kernel ship?" (attention reads the packed
+// codes and expands them in registers), and the VeloxQuant-MLX benchmarks
+// page, "KV-Cache Kernel Roofline" (one query token per head; too few
+// threadgroups per (batch, head) leave the GPU idle, so the cached tokens
+// are split across CTAs and merged by a log-sum-exp combine).
+//
+// Why tensor cores: with 4 query heads per KV head every packed byte feeds
+// ~6 multiply-adds (1024 per token of K and V at 4-bit, 176 bytes), more
+// than the fp32 pipes sustain at HBM rate. The dequant is folded out of the
+// contraction (a key group shares s_d, z_d per channel; a value row shares
+// s_j, z_j per 32-channel group):
+//     q . khat_t  = sum_d (q_d s_d) c_td + sum_d q_d z_d
+//     sum_t p_t vhat_td = sum_t (p_t s_tj) c_td + sum_t p_t z_tj
+// so the codes c are one MMA operand, exactly representable in fp16, and the
+// fp32 products q_d s_d / p_t s_tj the other. Exactness of the operands:
+//   * a code nibble (or 2-bit crumb) alone in a byte, read as fp8 e4m3, is
+//     c * 2^-9 exactly (subnormal for c < 8, normal 2^-6 (1 + (c-8)/8) for
+//     c >= 8), so cvt.rn.f16x2.e4m3x2 turns two codes into fp16 in one step;
+//   * each fp32 operand is split into fp16 hi + lo (hi = fp16(x), lo =
+//     fp16(x - hi)), carried as two MMA columns per query head: n = 2h + part.
+//     The sum keeps ~22 significant bits, far below the 2e-3 output budget;
+//   * a per-tile power-of-two factor keeps every hi below 2^14 (no fp16
+//     overflow for any finite input); it is divided out exactly afterwards.
+//
+// Work split: grid (n_split, Hkv, B), 4 warps per CTA; each warp owns a
+// contiguous run of 32-token tiles of its split and keeps its own online
+// softmax; the warps merge in shared memory, the CTA writes one partial (or
+// the output when n_split == 1). Tiles are staged per warp with cp.async,
+// double buffered: packed K/V codes, key scale/zero of the group, value
+// scale/zero of the 32 rows (5.5 KB at 4-bit); residual tiles stage 32 fp16
+// K and V rows (zero-filled past n_res).
+// MMA layouts (m16n8k16, row.col): lane = 4 g + c; A regs hold (row g,
+// k 2c..2c+1), (row g+8, same k), (row g, k 2c+8..9), (row g+8, k 2c+8..9);
+// B regs (k 2c..2c+1, n g), (k 2c+8..9, n g); C regs (row g, n 2c..2c+1),
+// (row g+8, n 2c..2c+1).
+#include <math.h>
+
+#include "kivi_device.cuh"
+#include "kivi_launch.h"
+
+namespace kivi {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kStage = 8192;                       // bytes per stage
+constexpr int kWarpSmem = 2 * kStage;              // two stages per warp
+constexpr int kPbufOff = kWarps * kWarpSmem;       // per-warp p buffers [32][4] f32
+constexpr int kQOff = kPbufOff + kWarps * 512;     // q * score_scale [4][128] f32
+constexpr int kMiscOff = kQOff + 4 * kD * 4;       // qmax, merge m/l
+constexpr int kSmemBytes = kMiscOff + 256;
+// store-tile layout inside a stage
+constexpr int kKC = 0, kVC = 2048, kKS = 4096, kKZ = 4608, kVS = 4864, kVZ = 5376;
+
+// ---------------------------------------------------------------------------
+// small PTX helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool fill) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(fill ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// two e4m3 bytes (low 16 bits / high 16 bits of w) -> f16x2, exact for codes
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// fp16 hi (lo == false) or lo (lo == true) part of the pair (x, y)
+__device__ __forceinline__ uint32_t split_pair(float x, float y, bool lo) {
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(__fsub_rn(x, hf.x), __fsub_rn(y, hf.y));
+    return lo ? h2_as_u32(l) : h2_as_u32(h);
+}
+
+// 2^e as fp32 for e in [-126, 127]
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// exponent E with m * 2^E < 2^14 (m >= 0); 0 for m == 0, clamped
+__device__ __forceinline__ int safe_exp(float m) {
+    if (!(m > 0.f)) return 0;
+    const int ex = ((__float_as_int(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
+    int e = 13 - ex;
+    return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
+// ---------------------------------------------------------------------------
+// tile staging
+// ---------------------------------------------------------------------------
+
+template <int BITS>
+__device__ __forceinline__ void fetch_store_tile(const DecodeArgs& a, int bh, int tile, uint8_t* st, int lane) {
+    constexpr int ROWB = kD * BITS / 8;      // 64 or 32
+    constexpr int CPR = ROWB / 16;           // 16-byte chunks per code row: 4 or 2
+    const int tok0 = tile * 32;
+    const uint8_t* kc = a.kcodes + ((long long)bh * a.s_cap + tok0) * ROWB;
+    const uint8_t* vc = a.vcodes + ((long long)bh * a.s_cap + tok0) * ROWB;
+#pragma unroll
+    for (int i = lane; i < 32 * CPR; i += 32) {
+        const int row = i / CPR, col = i % CPR;
+        cp_async16(st + kKC + i * 16, kc + i * 16, true);
+        const int sw = BITS == 4 ? (col ^ ((row >> 1) & 3)) : (col ^ ((row >> 2) & 1));
+        cp_async16(st + kVC + row * ROWB + sw * 16, vc + i * 16, true);
+    }
+    const float* ks = a.kscale + ((long long)bh * (a.s_cap / kG) + tile) * kD;
+    const __half* kz = a.kzero + ((long long)bh * (a.s_cap / kG) + tile) * kD;
+    cp_async16(st + kKS + lane * 16, ks + lane * 4, true);
+    if (lane < 16) cp_async16(st + kKZ + lane * 16, kz + lane * 8, true);
+    const float* vs = a.vscale + ((long long)bh * a.s_cap + tok0) * (kD / kG);
+    const __half* vz = a.vzero + ((long long)bh * a.s_cap + tok0) * (kD / kG);
+    cp_async16(st + kVS + lane * 16, vs + lane * 4, true);
+    if (lane < 16) cp_async16(st + kVZ + lane * 16, vz + lane * 8, true);
+}
+
+// 32 fp16 rows of K into st0 and of V into st1, 16-byte chunk c of row r at
+// position c ^ (r & 7); rows past nvalid are zero-filled (nothing is read).
+__device__ __forceinline__ void fetch_res_tile(const DecodeArgs& a, int bh, int rtile, int nvalid, uint8_t* st0,
+                                               uint8_t* st1, int lane) {
+    const int tok0 = rtile * 32;
+    const __half* kr = a.k_res + ((long long)bh * a.res_cap + tok0) * kD;
+    const __half* vr = a.v_res + ((long long)bh * a.res_cap + tok0) * kD;
+#pragma unroll 4
+    for (int i = lane; i < 32 * 16; i += 32) {
+        const int row = i >> 4, col = i & 15;
+        const bool ok = row < nvalid;
+        const int off = row * 256 + ((col ^ (row & 7)) << 4);
+        cp_async16(st0 + off, ok ? (const void*)(kr + row * kD + col * 8) : (const void*)kr, ok);
+        cp_async16(st1 + off, ok ? (const void*)(vr + row * kD + col * 8) : (const void*)vr, ok);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int BITS, int GQ>
+__global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int bh = b * a.Hkv + hk, h0 = hk * GQ;
+    uint8_t* st[2] = {smem + warp * kWarpSmem, smem + warp * kWarpSmem + kStage};
+    float* pbuf = reinterpret_cast<float*>(smem + kPbufOff + warp * 512);  // [token][head]
+    float* q_s = reinterpret_cast<float*>(smem + kQOff);                   // [head][channel]
+    float* misc = reinterpret_cast<float*>(smem + kMiscOff);
+
+    pdl_wait();
+    // q * score_scale for the GQ heads of this KV head (heads >= GQ are zero)
+    float qm = 0.f;
+#pragma unroll
+    for (int i = tid; i < 4 * kD; i += kThreads) {
+        const int h = i / kD, d = i % kD;
+        const float v = h < GQ ? __half2float(a.q[((long long)b * a.Hq + h0 + h) * kD + d]) * a.score_scale : 0.f;
+        q_s[i] = v;
+        qm = fmaxf(qm, fabsf(v));
+    }
+    qm = warp_max(qm);
+    if (lane == 0) misc[warp] = qm;
+    __syncthreads();
+    const float qmax = fmaxf(fmaxf(misc[0], misc[1]), fmaxf(misc[2], misc[3]));
+
+    // this warp's tiles
+    const int tile_begin = split * a.tiles_per_split;
+    const int split_end = min(tile_begin + a.tiles_per_split, a.n_tiles);
+    const int w0 = min(tile_begin + warp * a.tiles_per_warp, split_end);
+    const int w1 = min(w0 + a.tiles_per_warp, split_end);
+    const int s_end = min(w1, a.n_store_tiles);           // store tiles [w0, s_end)
+    const int r_begin = max(w0, a.n_store_tiles);         // residual tiles [r_begin, w1)
+
+    const int hh = g >> 1;          // head of this lane's B column n = g
+    const bool lo_part = g & 1;     // hi (0) or lo (1) part of that column
+    const float* qrow = q_s + hh * kD;
+
+    float m_run = -INFINITY, l_run = 0.f;  // online softmax of head c
+    float o[8][4];                         // P.V of head c, store-tile channel layout
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    // ---------------------------- store tiles ----------------------------
+    const int ns = s_end - w0;
+    if (ns > 0) fetch_store_tile<BITS>(a, bh, w0, st[0], lane);
+    cp_async_commit();
+    if (ns > 1) fetch_store_tile<BITS>(a, bh, w0 + 1, st[1], lane);
+    cp_async_commit();
+    for (int it = 0; it < ns; ++it) {
+        const int tile = w0 + it;
+        uint8_t* S = st[it & 1];
+        cp_async_wait<1>();
+        __syncwarp();
+        const int nvalid = min(32, a.S_q - tile * 32);
+        if (nvalid < 32) {  // zero the value metadata of rows past S_q
+            float* vsz = reinterpret_cast<float*>(S + kVS);
+            uint32_t* vzz = reinterpret_cast<uint32_t*>(S + kVZ);
+            if (lane >= nvalid) {
+                vsz[lane * 4 + 0] = vsz[lane * 4 + 1] = vsz[lane * 4 + 2] = vsz[lane * 4 + 3] = 0.f;
+                vzz[lane * 2 + 0] = vzz[lane * 2 + 1] = 0u;
+            }
+            __syncwarp();
+        }
+        const float* KS = reinterpret_cast<const float*>(S + kKS);
+        const __half* KZ = reinterpret_cast<const __half*>(S + kKZ);
+        const float* VS = reinterpret_cast<const float*>(S + kVS);
+        const __half* VZ = reinterpret_cast<const __half*>(S + kVZ);
+
+        // ---- QK operand B: (q s) for this lane's 32 channels, hi or lo ----
+        float qs[32];
+        float smax = 0.f, qz = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 s4 = *reinterpret_cast<const float4*>(KS + 32 * c + 4 * i);
+            const float4 q4 = *reinterpret_cast<const float4*>(qrow + 32 * c + 4 * i);
+            qs[4 * i + 0] = q4.x * s4.x;
+            qs[4 * i + 1] = q4.y * s4.y;
+            qs[4 * i + 2] = q4.z * s4.z;
+            qs[4 * i + 3] = q4.w * s4.w;
+            smax = fmaxf(smax, fmaxf(fmaxf(fabsf(s4.x), fabsf(s4.y)), fmaxf(fabsf(s4.z), fabsf(s4.w))));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 z8 = *reinterpret_cast<const uint4*>(KZ + 32 * c + 8 * i);
+            const uint32_t zw[4] = {z8.x, z8.y, z8.z, z8.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 zf = __half22float2(u32_as_h2(zw[k]));
+                qz = fmaf(qrow[32 * c + 8 * i + 2 * k], zf.x, qz);
+                qz = fmaf(qrow[32 * c + 8 * i + 2 * k + 1], zf.y, qz);
+            }
+        }
+        smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
+        smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
+        qz += __shfl_xor_sync(0xffffffffu, qz, 1);
+        qz += __shfl_xor_sync(0xffffffffu, qz, 2);
+        const int E = safe_exp(qmax * smax);
+        const float fB = pow2i(E);           // B = q s 2^E
+        const float fC = pow2i(9 - E);       // score = C 2^(9-E) (codes are c 2^-9)
+        uint32_t bq[8][2];
+        if (BITS == 4) {
+            // word m of this lane's 16-byte chunk: channels 32c + 8m + {0..7};
+            // K-step 2m pairs channels (0,2),(4,6), K-step 2m+1 pairs (1,3),(5,7)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float* v = qs + 8 * m + e;
+                    bq[2 * m + e][0] = split_pair(v[0] * fB, v[2] * fB, lo_part);
+                    bq[2 * m + e][1] = split_pair(v[4] * fB, v[6] * fB, lo_part);
+                }
+            }
+        } else {
+            // word m (4 bytes) of this lane's 8 bytes: channels 32c + 16m + {0..15};
+            // K-step 4m + k pairs channels (k, k+4), (k+8, k+12)
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float* v = qs + 16 * m + k;
+                    bq[4 * m + k][0] = split_pair(v[0] * fB, v[4] * fB, lo_part);
+                    bq[4 * m + k][1] = split_pair(v[8] * fB, v[12] * fB, lo_part);
+                }
+            }
+        }
+        const float qz_c = __shfl_sync(0xffffffffu, qz, 8 * c);  // sum q z of head c
+
+        // ---- scores: 2 M-tiles of 16 tokens ----
+        float sc[4];  // tokens g, g+8, g+16, g+24 for head c
+        const uint8_t* KC = S + kKC;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const int r0 = mt * 16 + g, r1 = r0 + 8;
+            if (BITS == 4) {
+                const uint4 x0 = *reinterpret_cast<const uint4*>(KC + r0 * 64 + 16 * c);
+                const uint4 x1 = *reinterpret_cast<const uint4*>(KC + r1 * 64 + 16 * c);
+                const uint32_t w0v[4] = {x0.x, x0.y, x0.z, x0.w}, w1v[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t e0l, e0h, e1l, e1h, o0l, o0h, o1l, o1h;
+                    e4m3x4_to_f16(w0v[m] & 0x0f0f0f0fu, e0l, e0h);
+                    e4m3x4_to_f16(w1v[m] & 0x0f0f0f0fu, e1l, e1h);
+                    e4m3x4_to_f16((w0v[m] >> 4) & 0x0f0f0f0fu, o0l, o0h);
+                    e4m3x4_to_f16((w1v[m] >> 4) & 0x0f0f0f0fu, o1l, o1h);
+                    mma16816(acc, e0l, e1l, e0h, e1h, bq[2 * m][0], bq[2 * m][1]);
+                    mma16816(acc, o0l, o1l, o0h, o1h, bq[2 * m + 1][0], bq[2 * m + 1][1]);
+                }
+            } else {
+                const uint2 x0 = *reinterpret_cast<const uint2*>(KC + r0 * 32 + 8 * c);
+                const uint2 x1 = *reinterpret_cast<const uint2*>(KC + r1 * 32 + 8 * c);
+                const uint32_t w0v[2] = {x0.x, x0.y}, w1v[2] = {x1.x, x1.y};
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t p0l, p0h, p1l, p1h;
+                        e4m3x4_to_f16((w0v[m] >> (2 * k)) & 0x03030303u, p0l, p0h);
+                        e4m3x4_to_f16((w1v[m] >> (2 * k)) & 0x03030303u, p1l, p1h);
+                        mma16816(acc, p0l, p1l, p0h, p1h, bq[4 * m + k][0], bq[4 * m + k][1]);
+                    }
+                }
+            }
+            const int t0 = mt * 16 + g;
+            const float s0 = fmaf(acc[0] + acc[1], fC, qz_c);
+            const float s1 = fmaf(acc[2] + acc[3], fC, qz_c);
+            sc[2 * mt] = t0 < nvalid ? s0 : -INFINITY;
+            sc[2 * mt + 1] = t0 + 8 < nvalid ? s1 : -INFINITY;
+        }
+
+        // ---- online softmax (head c; lanes with equal c share it) ----
+        float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        const float m_new = fmaxf(m_run, tmax);
+        const float corr = exp2f(m_run - m_new);
+        float p[4], ps = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            p[i] = exp2f(sc[i] - m_new);
+            ps += p[i];
+        }
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l_run = fmaf(l_run, corr, ps);
+        m_run = m_new;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            o[i][0] *= corr;
+            o[i][1] *= corr;
+            o[i][2] *= corr;
+            o[i][3] *= corr;
+        }
+        // p of tokens g, g+8, g+16, g+24 (head c) -> pbuf; p.vzero partials
+        pbuf[(g) * 4 + c] = p[0];
+        pbuf[(g + 8) * 4 + c] = p[1];
+        pbuf[(g + 16) * 4 + c] = p[2];
+        pbuf[(g + 24) * 4 + c] = p[3];
+        float pz[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = g + 8 * i;
+            const uint2 z4 = *reinterpret_cast<const uint2*>(VZ + t * 4);
+            const float2 za = __half22float2(u32_as_h2(z4.x)), zb = __half22float2(u32_as_h2(z4.y));
+            pz[0] = fmaf(p[i], za.x, pz[0]);
+            pz[1] = fmaf(p[i], za.y, pz[1]);
+            pz[2] = fmaf(p[i], zb.x, pz[2]);
+            pz[3] = fmaf(p[i], zb.y, pz[3]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            pz[j] += __shfl_xor_sync(0xffffffffu, pz[j], 4);
+            pz[j] += __shfl_xor_sync(0xffffffffu, pz[j], 8);
+            pz[j] += __shfl_xor_sync(0xffffffffu, pz[j], 16);
+        }
+        __syncwarp();
+
+        // ---- PV operand B: p_t s_tj of head hh, tokens of this lane's k slots ----
+        uint32_t bp[4][2][2];  // [group j][K-step][b0/b1]
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const int ta = 16 * ks + 2 * c, tb = ta + 8;
+            const float pa0 = pbuf[ta * 4 + hh], pa1 = pbuf[(ta + 1) * 4 + hh];
+            const float pb0 = pbuf[tb * 4 + hh], pb1 = pbuf[(tb + 1) * 4 + hh];
+            const float4 va0 = *reinterpret_cast<const float4*>(VS + ta * 4);
+            const float4 va1 = *reinterpret_cast<const float4*>(VS + (ta + 1) * 4);
+            const float4 vb0 = *reinterpret_cast<const float4*>(VS + tb * 4);
+            const float4 vb1 = *reinterpret_cast<const float4*>(VS + (tb + 1) * 4);
+            const float sa0[4] = {va0.x, va0.y, va0.z, va0.w}, sa1[4] = {va1.x, va1.y, va1.z, va1.w};
+            const float sb0[4] = {vb0.x, vb0.y, vb0.z, vb0.w}, sb1[4] = {vb1.x, vb1.y, vb1.z, vb1.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                bp[j][ks][0] = split_pair(pa0 * sa0[j], pa1 * sa1[j], lo_part);
+                bp[j][ks][1] = split_pair(pb0 * sb0[j], pb1 * sb1[j], lo_part);
+            }
+        }
+
+        // ---- P.V on the tensor cores ----
+        const uint8_t* VC = S + kVC;
+        if (BITS == 4) {
+            // o[2j + u]: rows g -> channel 32j + 4g + u, g+8 -> 32j + 4g + 2 + u
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int row = 8 * (lane >> 3) + (lane & 7);  // token block lane>>3, row lane&7
+                uint32_t W[4];
+                ldsm_x4_t(W, VC + row * 64 + 16 * (j ^ ((row >> 1) & 3)));
+                uint32_t xl[2][4], xh[2][4];  // [u][token block] -> (row g, row g+8) halves
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t E = __byte_perm(W[q] & 0x0f0f0f0fu, 0, 0x3120);
+                    const uint32_t O = __byte_perm((W[q] >> 4) & 0x0f0f0f0fu, 0, 0x3120);
+                    e4m3x4_to_f16(E, xl[0][q], xh[0][q]);
+                    e4m3x4_to_f16(O, xl[1][q], xh[1][q]);
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+                        mma16816(o[2 * j + u], xl[u][2 * ks], xh[u][2 * ks], xl[u][2 * ks + 1], xh[u][2 * ks + 1],
+                                 bp[j][ks][0], bp[j][ks][1]);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    o[2 * j + u][0] += pz[j] * (1.0f / 512.f);  // o is kept in units of 2^-9 (codes)
+                    o[2 * j + u][2] += pz[j] * (1.0f / 512.f);
+                }
+        } else {
+            // o[4h + k]: rows g -> channel 64h + 8g + k, g+8 -> 64h + 8g + 4 + k;
+            // rows of lanes g < 4 lie in group 2h, of lanes g >= 4 in group 2h+1
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                const int row = 8 * (lane >> 3) + (lane & 7);
+                uint32_t W[4];
+                ldsm_x4_t(W, VC + row * 32 + 16 * (hc ^ ((row >> 2) & 1)));
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t xl[4], xh[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        e4m3x4_to_f16(__byte_perm((W[q] >> (2 * k)) & 0x03030303u, 0, 0x3120), xl[q], xh[q]);
+                    const bool first = g < 4;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const uint32_t a0 = xl[2 * ks], a1 = xh[2 * ks], a2 = xl[2 * ks + 1], a3 = xh[2 * ks + 1];
+                        mma16816(o[4 * hc + k], first ? a0 : 0u, first ? a1 : 0u, first ? a2 : 0u,
+                                 first ? a3 : 0u, bp[2 * hc][ks][0], bp[2 * hc][ks][1]);
+                        mma16816(o[4 * hc + k], first ? 0u : a0, first ? 0u : a1, first ? 0u : a2,
+                                 first ? 0u : a3, bp[2 * hc + 1][ks][0], bp[2 * hc + 1][ks][1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                const float pzj = g < 4 ? pz[2 * hc] : pz[2 * hc + 1];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o[4 * hc + k][0] += pzj * (1.0f / 512.f);
+                    o[4 * hc + k][2] += pzj * (1.0f / 512.f);
+                }
+            }
+        }
+        __syncwarp();
+        if (it + 2 < ns) fetch_store_tile<BITS>(a, bh, tile + 2, S, lane);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+
+    // ---------------------------- residual tiles ----------------------------
+    float orr[8][4];  // P.V of head c from residual tiles, rows g / g+8 -> channel 16 mb + g / + 8
+#pragma unroll
+    for (int i = 0; i < 8; ++i) orr[i][0] = orr[i][1] = orr[i][2] = orr[i][3] = 0.f;
+    if (r_begin < w1) {
+        const int Er = safe_exp(qmax);
+        const float fBr = pow2i(Er), fCr = pow2i(-Er);
+        uint32_t br[8][2];  // K-step s: channels 16s + 2c.., 16s + 8 + 2c..
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const float2 qa = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * c);
+            const float2 qb = *reinterpret_cast<const float2*>(qrow + 16 * s + 8 + 2 * c);
+            br[s][0] = split_pair(qa.x * fBr, qa.y * fBr, lo_part);
+            br[s][1] = split_pair(qb.x * fBr, qb.y * fBr, lo_part);
+        }
+        for (int rt = r_begin; rt < w1; ++rt) {
+            const int rtile = rt - a.n_store_tiles;
+            const int nvalid = min(32, a.n_res - rtile * 32);
+            fetch_res_tile(a, bh, rtile, nvalid, st[0], st[1], lane);
+            cp_async_commit();
+            cp_async_wait<0>();
+            __syncwarp();
+            const uint8_t* KR = st[0];
+            const uint8_t* VR = st[1];
+            float sc[4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const int q = lane >> 3, r = lane & 7;
+                    const int row = mt * 16 + (q & 1) * 8 + r, chunk = 2 * s + (q >> 1);
+                    uint32_t A[4];
+                    ldsm_x4(A, KR + row * 256 + ((chunk ^ (row & 7)) << 4));
+                    mma16816(acc, A[0], A[1], A[2], A[3], br[s][0], br[s][1]);
+                }
+                const int t0 = mt * 16 + g;
+                sc[2 * mt] = t0 < nvalid ? (acc[0] + acc[1]) * fCr : -INFINITY;
+                sc[2 * mt + 1] = t0 + 8 < nvalid ? (acc[2] + acc[3]) * fCr : -INFINITY;
+            }
+            float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+            const float m_new = fmaxf(m_run, tmax);
+            const float corr = exp2f(m_run - m_new);
+            float p[4], ps = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                p[i] = exp2f(sc[i] - m_new);
+                ps += p[i];
+            }
+            ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+            l_run = fmaf(l_run, corr, ps);
+            m_run = m_new;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o[i][k] *= corr;
+                    orr[i][k] *= corr;
+                }
+            }
+            pbuf[(g) * 4 + c] = p[0];
+            pbuf[(g + 8) * 4 + c] = p[1];
+            pbuf[(g + 16) * 4 + c] = p[2];
+            pbuf[(g + 24) * 4 + c] = p[3];
+            __syncwarp();
+            uint32_t bpr[2][2];
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int ta = 16 * ks + 2 * c, tb = ta + 8;
+                bpr[ks][0] = split_pair(pbuf[ta * 4 + hh], pbuf[(ta + 1) * 4 + hh], lo_part);
+                bpr[ks][1] = split_pair(pbuf[tb * 4 + hh], pbuf[(tb + 1) * 4 + hh], lo_part);
+            }
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int q = lane >> 3, r = lane & 7;
+                    const int row = 16 * ks + (q >> 1) * 8 + r, chunk = 2 * mb + (q & 1);
+                    uint32_t A[4];
+                    ldsm_x4_t(A, VR + row * 256 + ((chunk ^ (row & 7)) << 4));
+                    mma16816(orr[mb], A[0], A[1], A[2], A[3], bpr[ks][0], bpr[ks][1]);
+                }
+            }
+            __syncwarp();
+        }
+    }
+
+    // ---------------------------- merge the 4 warps ----------------------------
+    __syncthreads();  // every warp is done with its stages
+    float* Ow = reinterpret_cast<float*>(st[0]);          // [4 heads][128] of this warp
+    float* ml = misc + 8;                                  // [warp][head][2]
+    {
+        const float sc9 = 512.f;  // o holds sum p s c 2^-9 + pz 2^-9
+        if (BITS == 4) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    Ow[c * kD + 32 * j + 4 * g + u] = (o[2 * j + u][0] + o[2 * j + u][1]) * sc9;
+                    Ow[c * kD + 32 * j + 4 * g + 2 + u] = (o[2 * j + u][2] + o[2 * j + u][3]) * sc9;
+                }
+        } else {
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    Ow[c * kD + 64 * hc + 8 * g + k] = (o[4 * hc + k][0] + o[4 * hc + k][1]) * sc9;
+                    Ow[c * kD + 64 * hc + 8 * g + 4 + k] = (o[4 * hc + k][2] + o[4 * hc + k][3]) * sc9;
+                }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+            Ow[c * kD + 16 * mb + g] += orr[mb][0] + orr[mb][1];
+            Ow[c * kD + 16 * mb + 8 + g] += orr[mb][2] + orr[mb][3];
+        }
+        if (g == 0) {
+            ml[(warp * 4 + c) * 2 + 0] = m_run;
+            ml[(warp * 4 + c) * 2 + 1] = l_run;
+        }
+    }
+    pdl_trigger();
+    __syncthreads();
+    const int d = tid;
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 4 + h) * 2]);
+        float L = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = ml[(w * 4 + h) * 2];
+            if (mw == -INFINITY) continue;  // a warp without tiles
+            const float f = exp2f(mw - M);
+            L = fmaf(ml[(w * 4 + h) * 2 + 1], f, L);
+            acc = fmaf(reinterpret_cast<const float*>(smem + w * kWarpSmem)[h * kD + d], f, acc);
+        }
+        const long long bq = (long long)b * a.Hq + h0 + h;
+        if (a.n_split == 1) {
+            a.out[bq * kD + d] = acc / L;
+        } else {
+            a.part_o[(bq * a.n_split + split) * kD + d] = acc;
+            if (d == 0) {
+                a.part_ml[(bq * a.n_split + split) * 2 + 0] = M;
+                a.part_ml[(bq * a.n_split + split) * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+template <int BITS, int GQ>
+cudaError_t launch_mma_typed(const DecodeArgs& a, cudaStream_t stream) {
+    static bool configured = false;  // benign race: every caller sets the same value
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_pdl(decode_mma_kernel<BITS, GQ>, dim3(a.n_split, a.Hkv, a.B), kThreads, kSmemBytes, stream, a);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, int bits, int gq, cudaStream_t stream) {
+    if (bits == 4) {
+        if (gq == 1) return launch_mma_typed<4, 1>(a, stream);
+        if (gq == 2) return launch_mma_typed<4, 2>(a, stream);
+        if (gq == 4) return launch_mma_typed<4, 4>(a, stream);
+    } else {
+        if (gq == 1) return launch_mma_typed<2, 1>(a, stream);
+        if (gq == 2) return launch_mma_typed<2, 2>(a, stream);
+        if (gq == 4) return launch_mma_typed<2, 4>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kivi

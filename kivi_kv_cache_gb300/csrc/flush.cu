@@ -291,7 +291,7 @@ int key_blocks_x(int n_flush) { return ((n_flush + kG - 1) / kG * 2 + 3) / 4; } 
 int value_blocks_x(int n_flush) { return (n_flush + 31) / 32; }                    // 32 tokens per block
 
 template <int BITS>
-__global__ void __launch_bounds__(kThreads) flush_keys_kernel(FlushArgs a) {
+__global__ void __launch_bounds__(kThreads, 6) flush_keys_kernel(FlushArgs a) {
     pdl_wait();
     flush_keys_warp<BITS>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) flush_values_kernel(FlushArgs a) {
 // Keys and values of the same tokens in one launch: blocks [0, kbx) of each
 // grid row (blockIdx.y = head) run the key flush, the rest the value flush.
 template <int BITS>
-__global__ void __launch_bounds__(kThreads) flush_kv_kernel(FlushArgs k, FlushArgs v, int kbx) {
+__global__ void __launch_bounds__(kThreads, 6) flush_kv_kernel(FlushArgs k, FlushArgs v, int kbx) {
     pdl_wait();
     if ((int)blockIdx.x < kbx)
         flush_keys_warp<BITS>(k, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);

@@ -43,18 +43,30 @@ kivi_status shape_check(int D, int G, int bits) {
 
 kivi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ERR_CUDA; }
 
-// Split plan for the decode: enough CTAs for about two per SM, whole 32-token
-// tiles per CTA, no empty split.
-DecodePlan make_plan(int B, int Hkv, int S_q, int n_res) {
+// Split plan for the decode. The tensor-core kernel (<= 4 query heads per KV
+// head) gives each of its 4 warps a run of tiles_per_warp 32-token tiles,
+// sized for about 8 warps (2 CTAs) per SM over the whole batch; the fp32 kernel (8
+// query heads per KV head) targets two CTAs per SM. Whole tiles per split,
+// no empty split.
+DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res) {
     DecodePlan p;
     p.n_store_tiles = (S_q + kG - 1) / kG;
     p.n_tiles = p.n_store_tiles + (n_res + kG - 1) / kG;
     const long long heads = (long long)B * Hkv;
-    const long long target = 2LL * sm_count();
-    long long per_head = (target + heads - 1) / heads;
-    if (per_head < 1) per_head = 1;
-    if (per_head > p.n_tiles) per_head = p.n_tiles;
-    p.tiles_per_split = (int)((p.n_tiles + per_head - 1) / per_head);
+    if (Hkv > 0 && Hq / Hkv <= 4) {
+        const long long target = 8LL * sm_count();
+        long long tpw = (heads * p.n_tiles + target - 1) / target;
+        if (tpw < 1) tpw = 1;
+        p.tiles_per_warp = (int)tpw;
+        p.tiles_per_split = 4 * p.tiles_per_warp;
+    } else {
+        const long long target = 2LL * sm_count();
+        long long per_head = (target + heads - 1) / heads;
+        if (per_head < 1) per_head = 1;
+        if (per_head > p.n_tiles) per_head = p.n_tiles;
+        p.tiles_per_split = (int)((p.n_tiles + per_head - 1) / per_head);
+        p.tiles_per_warp = p.tiles_per_split;
+    }
     p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
     return p;
 }
@@ -283,7 +295,7 @@ kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, i
 size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || S_q < 0 || n_res < 0 || D != kD || S_q + n_res == 0)
         return 0;
-    return workspace_bytes(B, Hq, make_plan(B, Hkv, S_q, n_res));
+    return workspace_bytes(B, Hq, make_plan(B, Hkv, Hq, S_q, n_res));
 }
 
 kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const float* kscale,
@@ -309,7 +321,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
         !aligned16(vzero_f16) || !aligned16(k_res_f16) || !aligned16(v_res_f16) ||
         !aligned16(workspace))
         return KIVI_ERR_ALIGNMENT;
-    const DecodePlan p = make_plan(B, Hkv, S_q, n_res);
+    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res);
     const size_t need = workspace_bytes(B, Hq, p);
     if (need > 0 && (!workspace || workspace_bytes_ < need)) return KIVI_ERR_WORKSPACE;
 
@@ -333,6 +345,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
     a.score_scale = sm_scale * 1.4426950408889634f;
     a.n_split = p.n_split;
     a.tiles_per_split = p.tiles_per_split;
+    a.tiles_per_warp = p.tiles_per_warp;
     a.n_store_tiles = p.n_store_tiles;
     a.n_tiles = p.n_tiles;
     float* ws = static_cast<float*>(workspace);
@@ -342,7 +355,13 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
                                                      ~(size_t)255))
                          : nullptr;
     a.out = out_f32;
-    return from_cuda(launch_decode(a, bits, gq, reinterpret_cast<cudaStream_t>(stream)));
+    const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+    if (gq <= 4) {
+        cudaError_t e = launch_decode_mma(a, bits, gq, strm);
+        if (e == cudaSuccess) e = launch_decode_combine(a, strm);
+        return from_cuda(e);
+    }
+    return from_cuda(launch_decode(a, bits, gq, strm));
 }
 
 }  // extern "C"

@@ -54,6 +54,7 @@ struct DecodeArgs {
     float score_scale;    // sm_scale * log2(e): scores live in the exp2 domain
     int n_split;
     int tiles_per_split;
+    int tiles_per_warp;   // tensor-core kernel: contiguous tiles per warp (4 warps)
     int n_store_tiles;
     int n_tiles;
     float* part_o;        // [B, Hq, n_split, D]
@@ -64,6 +65,7 @@ struct DecodeArgs {
 struct DecodePlan {
     int n_split;
     int tiles_per_split;
+    int tiles_per_warp;
     int n_store_tiles;
     int n_tiles;
 };
@@ -98,5 +100,8 @@ cudaError_t launch_residual_append(const __half* src0, const __half* src1, long 
 cudaError_t launch_residual_compact(__half* res0, __half* res1, int BH, int res_cap, int n_res, int n_drop,
                                     cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
+// tensor-core decode for gq in {1, 2, 4}; the combine pass is shared
+cudaError_t launch_decode_mma(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace kivi
