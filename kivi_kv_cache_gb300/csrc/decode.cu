@@ -281,50 +281,41 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
     }
 }
 
-// out[b, h, :] = sum_i o_i * 2^(m_i - M) / sum_i l_i * 2^(m_i - M).
-// The split weights are computed once into shared memory (all loads issued
-// in parallel), then each thread sums its channel with independent loads.
-constexpr int kMaxSplitSmem = 1024;
-
+// out[b, h, :] = sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M), M = max_i m_i.
+// One pass with a running maximum; the loads of 8 splits are issued together
+// so a merge of n splits waits on about n/8 memory round trips.
 __global__ void __launch_bounds__(kThreads) decode_combine_kernel(DecodeArgs a) {
-    __shared__ float wsm[kMaxSplitSmem];
-    __shared__ float red[kThreads / 32];
     pdl_wait();
     const long long bq = blockIdx.x;
     const int n = a.n_split;
     const float* ml = a.part_ml + bq * n * 2;
-    float M = -INFINITY;
-    for (int i = threadIdx.x; i < n; i += kThreads) M = fmaxf(M, ml[2 * i]);
-    M = warp_max(M);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = M;
-    __syncthreads();
-    M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    __syncthreads();
-    float L = 0.f;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-        const float w = exp2f(ml[2 * i] - M);
-        if (i < kMaxSplitSmem) wsm[i] = w;
-        L = fmaf(ml[2 * i + 1], w, L);
-    }
-    L = warp_sum(L);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = L;
-    __syncthreads();
-    L = red[0] + red[1] + red[2] + red[3];
     const float* po = a.part_o + bq * n * kD + threadIdx.x;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-    int i = 0;
-    for (; i + 4 <= n; i += 4) {
-        const float w0 = i < kMaxSplitSmem ? wsm[i] : exp2f(ml[2 * i] - M);
-        const float w1 = i + 1 < kMaxSplitSmem ? wsm[i + 1] : exp2f(ml[2 * i + 2] - M);
-        const float w2 = i + 2 < kMaxSplitSmem ? wsm[i + 2] : exp2f(ml[2 * i + 4] - M);
-        const float w3 = i + 3 < kMaxSplitSmem ? wsm[i + 3] : exp2f(ml[2 * i + 6] - M);
-        acc0 = fmaf(po[(long long)i * kD], w0, acc0);
-        acc1 = fmaf(po[(long long)(i + 1) * kD], w1, acc1);
-        acc2 = fmaf(po[(long long)(i + 2) * kD], w2, acc2);
-        acc3 = fmaf(po[(long long)(i + 3) * kD], w3, acc3);
+    float M = -INFINITY, L = 0.f, acc = 0.f;
+    for (int i0 = 0; i0 < n; i0 += 8) {
+        float m[8], l[8], o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const bool ok = i0 + k < n;
+            m[k] = ok ? ml[2 * (i0 + k)] : -INFINITY;
+            l[k] = ok ? ml[2 * (i0 + k) + 1] : 0.f;
+            o[k] = ok ? po[(long long)(i0 + k) * kD] : 0.f;
+        }
+        float mc = m[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) mc = fmaxf(mc, m[k]);
+        const float Mn = fmaxf(M, mc);
+        const float r = Mn == -INFINITY ? 0.f : exp2f(M - Mn);
+        L *= r;
+        acc *= r;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float w = m[k] == -INFINITY ? 0.f : exp2f(m[k] - Mn);
+            L = fmaf(l[k], w, L);
+            acc = fmaf(o[k], w, acc);
+        }
+        M = Mn;
     }
-    for (; i < n; ++i) acc0 = fmaf(po[(long long)i * kD], i < kMaxSplitSmem ? wsm[i] : exp2f(ml[2 * i] - M), acc0);
-    a.out[bq * kD + threadIdx.x] = ((acc0 + acc1) + (acc2 + acc3)) / L;
+    a.out[bq * kD + threadIdx.x] = acc / L;
 }
 
 template <int BITS, int GQ>

@@ -183,7 +183,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
     float* q_s = reinterpret_cast<float*>(smem + kQOff);                   // [head][channel]
     float* misc = reinterpret_cast<float*>(smem + kMiscOff);
 
+    // this warp's tiles
+    const int tile_begin = split * a.tiles_per_split;
+    const int split_end = min(tile_begin + a.tiles_per_split, a.n_tiles);
+    const int w0 = min(tile_begin + warp * a.tiles_per_warp, split_end);
+    const int w1 = min(w0 + a.tiles_per_warp, split_end);
+    const int s_end = min(w1, a.n_store_tiles);           // store tiles [w0, s_end)
+    const int r_begin = max(w0, a.n_store_tiles);         // residual tiles [r_begin, w1)
+    const int ns = s_end - w0;
+
     pdl_wait();
+    // start the first two store tiles' copies, then stage q while they fly
+    if (ns > 0) fetch_store_tile<BITS>(a, bh, w0, st[0], lane);
+    cp_async_commit();
+    if (ns > 1) fetch_store_tile<BITS>(a, bh, w0 + 1, st[1], lane);
+    cp_async_commit();
+
     // q * score_scale for the GQ heads of this KV head (heads >= GQ are zero)
     float qm = 0.f;
 #pragma unroll
@@ -198,14 +213,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
     __syncthreads();
     const float qmax = fmaxf(fmaxf(misc[0], misc[1]), fmaxf(misc[2], misc[3]));
 
-    // this warp's tiles
-    const int tile_begin = split * a.tiles_per_split;
-    const int split_end = min(tile_begin + a.tiles_per_split, a.n_tiles);
-    const int w0 = min(tile_begin + warp * a.tiles_per_warp, split_end);
-    const int w1 = min(w0 + a.tiles_per_warp, split_end);
-    const int s_end = min(w1, a.n_store_tiles);           // store tiles [w0, s_end)
-    const int r_begin = max(w0, a.n_store_tiles);         // residual tiles [r_begin, w1)
-
     const int hh = g >> 1;          // head of this lane's B column n = g
     const bool lo_part = g & 1;     // hi (0) or lo (1) part of that column
     const float* qrow = q_s + hh * kD;
@@ -216,11 +223,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
     // ---------------------------- store tiles ----------------------------
-    const int ns = s_end - w0;
-    if (ns > 0) fetch_store_tile<BITS>(a, bh, w0, st[0], lane);
-    cp_async_commit();
-    if (ns > 1) fetch_store_tile<BITS>(a, bh, w0 + 1, st[1], lane);
-    cp_async_commit();
     for (int it = 0; it < ns; ++it) {
         const int tile = w0 + it;
         uint8_t* S = st[it & 1];

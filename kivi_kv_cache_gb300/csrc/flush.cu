@@ -27,7 +27,11 @@
 //    sends the rare near-tie element to an exact IEEE division (out of line).
 //    RN(y + 2^23) rounds half to even and leaves the code in the low byte;
 //    byte permutes pack 8 codes per 32-bit word.
-//  * 2-D grids (y = head) keep all index arithmetic in 32 bits.
+//  * work is cut into 4 KB items (a key group's 32 tokens x 64 channels, or
+//    16 value rows); each warp walks the items with a grid stride, staging
+//    two at a time in shared memory with cp.async, so the copy of the next
+//    item overlaps the quantization of the current one, and the quantize
+//    loop is one copy of the code per path (small instruction footprint).
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
@@ -105,40 +109,81 @@ __device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4],
 __device__ __forceinline__ float canon(float v) { return __fadd_rn(v, 0.0f); }
 
 // ---------------------------------------------------------------------------
-// keys
+// work items, staged per warp through shared memory
 // ---------------------------------------------------------------------------
+//
+// A key item is (head, key group, 64-channel half): 32 tokens x 128 bytes. A
+// value item is (head, 16 consecutive tokens): 16 rows x 256 bytes. Both are
+// 4 KB. Each warp walks the item list with a grid stride and keeps two items
+// in flight (cp.async, double buffered), so copies of the next item overlap
+// the quantization of the current one. Rows past n_flush are zero-filled and
+// never read from global memory.
 
-// One warp covers (head, group, 64 channels): lane = part * 8 + oc, part in
-// [0, 4) owns tokens [8*part, 8*part + 8) of the group, oc owns 8 channels.
-// Two warps cover the 128 channels of a group.
-template <int BITS>
-__device__ __forceinline__ void flush_keys_warp(const FlushArgs& a, int warp_id, int bh) {
-    constexpr int TPT = 8;
-    const int lane = threadIdx.x & 31;
-    const int oc = lane & 7;
-    const int part = lane >> 3;
-    const int octet = (warp_id & 1) * 8 + oc;
-    const int g = warp_id >> 1;
-    const int ng = (a.n_flush + kG - 1) / kG;
-    if (g >= ng) return;  // warp-uniform
-    const int t0 = g * kG + part * TPT;
+constexpr int kItemBytes = 4096;
+constexpr int kWarpSmem = 2 * kItemBytes + 1024;  // two stages + value-row constants
+constexpr int kBlocksPerSm = 4;
 
-    const uint4* xrow = reinterpret_cast<const uint4*>(a.x) +
-                        ((long long)bh * a.x_bh_stride + t0) * (kD / 8) + octet;
-    uint4 v[TPT];
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool fill) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(fill ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+struct Items {
+    int key_items;   // BH * ng * 2
+    int val_items;   // BH * ceil(n_flush / 16)
+    int ng;          // key groups per head
+    int nv;          // value items per head
+};
+
+__device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& v, const Items& it, int item,
+                                           uint8_t* st, int lane) {
+    if (item < it.key_items) {
+        const int half = item & 1, g = (item >> 1) % it.ng, bh = (item >> 1) / it.ng;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(k.x) + ((long long)bh * k.x_bh_stride + g * kG) * 256 + half * 128;
 #pragma unroll
-    for (int i = 0; i < TPT; ++i)
-        v[i] = (t0 + i < a.n_flush) ? __ldg(xrow + i * (kD / 8)) : make_uint4(0, 0, 0, 0);
-    pdl_trigger();
+        for (int i = lane; i < 256; i += 32) {  // 32 rows x 8 chunks
+            const int row = i >> 3, col = i & 7;
+            const bool ok = g * kG + row < k.n_flush;
+            cp_async16(st + i * 16, ok ? (const void*)(src + row * 256 + col * 16) : (const void*)src, ok);
+        }
+    } else {
+        const int vi = item - it.key_items;
+        const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(v.x) + ((long long)bh * v.x_bh_stride + t0) * 256;
+#pragma unroll
+        for (int i = lane; i < 256; i += 32) {  // 16 rows x 16 chunks
+            const bool ok = t0 + (i >> 4) < v.n_flush;
+            cp_async16(st + i * 16, ok ? (const void*)(src + i * 16) : (const void*)src, ok);
+        }
+    }
+}
+
+// keys: lane = part * 8 + oc; part owns tokens [8 part, 8 part + 8) of the
+// group, oc owns 8 channels of this 64-channel half.
+template <int BITS>
+__device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st, int lane) {
+    const int half = item & 1, g = (item >> 1) % it.ng, bh = (item >> 1) / it.ng;
+    const int oc = lane & 7, part = lane >> 3;
+    const int octet = half * 8 + oc;
+    const int t0 = g * kG + part * 8;
+    const int nv = min(8, a.n_flush - t0);  // may be <= 0 in a ragged last group
+    const uint4* xs = reinterpret_cast<const uint4*>(st) + (part * 8) * 8 + oc;  // row stride 8 vectors
 
     const __half2 pinf = __half2half2(__ushort_as_half(0x7c00));
     const __half2 ninf = __half2half2(__ushort_as_half(0xfc00));
     __half2 mn[4] = {pinf, pinf, pinf, pinf};
     __half2 mx[4] = {ninf, ninf, ninf, ninf};
 #pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-        if (t0 + i < a.n_flush) {
-            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    for (int i = 0; i < 8; ++i) {
+        if (i < nv) {
+            const uint4 x = xs[i * 8];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 mn[k] = __hmin2(mn[k], u32_as_h2(w[k]));
@@ -154,7 +199,6 @@ __device__ __forceinline__ void flush_keys_warp(const FlushArgs& a, int warp_id,
             mx[k] = __hmax2(mx[k], u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(mx[k]), o)));
         }
     }
-    // zero of all 8 channels; this part's 2 channels' scale and reciprocal
     float z[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -191,7 +235,6 @@ __device__ __forceinline__ void flush_keys_warp(const FlushArgs& a, int warp_id,
         z2[k] = pk(z[2 * k], z[2 * k + 1]);
         r2[k] = pk(r[2 * k], r[2 * k + 1]);
     }
-
     if (part == 0) {
         const long long m = ((long long)bh * (a.s_cap / kG) + a.s_off / kG + g) * kD + octet * 8;
         float4* sp = reinterpret_cast<float4*>(a.scale + m);
@@ -204,48 +247,31 @@ __device__ __forceinline__ void flush_keys_warp(const FlushArgs& a, int warp_id,
         zp.w = h2_as_u32(__floats2half2_rn(z[6], z[7]));
         *reinterpret_cast<uint4*>(a.zero + m) = zp;
     }
-
     constexpr int ROWB = kD * BITS / 8;
     uint8_t* crow = a.codes + ((long long)bh * a.s_cap + a.s_off + t0) * ROWB + octet * BITS;
-#pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-        if (t0 + i < a.n_flush) {
-            const uint32_t packed = quant8<BITS>(v[i], z2, r2, s);
-            if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
-            else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
-        }
+#pragma unroll 1
+    for (int i = 0; i < nv; ++i) {
+        const uint32_t packed = quant8<BITS>(xs[i * 8], z2, r2, s);
+        if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
+        else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
     }
 }
 
-// ---------------------------------------------------------------------------
-// values
-// ---------------------------------------------------------------------------
-
-// One warp covers 8 consecutive tokens of one head: lane = sub * 16 + octet;
-// iteration i handles token 2*i + sub, so each warp load reads 512 contiguous
-// bytes. Lanes 4j..4j+3 of a half-warp form value group j.
+// values: lane = sub * 16 + octet; row 2i + sub of the item for i in [0, 8);
+// lanes 4j..4j+3 of a half-warp form value group j.
 template <int BITS>
-__device__ __forceinline__ void flush_values_warp(const FlushArgs& a, int warp_id, int bh) {
-    constexpr int RPT = 4;
-    const int lane = threadIdx.x & 31;
-    const int octet = lane & 15;
-    const int sub = lane >> 4;
-    const int tw = warp_id * (2 * RPT);  // first token of this warp
-    if (tw >= a.n_flush) return;         // warp-uniform
-    constexpr int ROWB = kD * BITS / 8;
+__device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
+                                           float* rowc, int lane) {
+    const int vi = item - it.key_items;
+    const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
+    const int octet = lane & 15, sub = lane >> 4, j = octet >> 2;
     const float L = (float)Levels<BITS>::value;
-
-    const uint4* xrow = reinterpret_cast<const uint4*>(a.x) + ((long long)bh * a.x_bh_stride + tw + sub) * (kD / 8) + octet;
-    uint4 v[RPT];
+    const uint4* xs = reinterpret_cast<const uint4*>(st) + sub * 16 + octet;  // row stride 16 vectors
+    // pass 1: (zero, range) of every row's group -> rowc[row][j][0..1]
 #pragma unroll
-    for (int i = 0; i < RPT; ++i)
-        v[i] = (tw + 2 * i + sub < a.n_flush) ? __ldg(xrow + 2 * i * (kD / 8)) : make_uint4(0, 0, 0, 0);
-    pdl_trigger();
-
-    float z[RPT], range[RPT];
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    for (int i = 0; i < 8; ++i) {
+        const uint4 x = xs[i * 32];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         const __half2 m2 = __hmin2(__hmin2(u32_as_h2(w[0]), u32_as_h2(w[1])), __hmin2(u32_as_h2(w[2]), u32_as_h2(w[3])));
         const __half2 x2 = __hmax2(__hmax2(u32_as_h2(w[0]), u32_as_h2(w[1])), __hmax2(u32_as_h2(w[2]), u32_as_h2(w[3])));
         __half2 mm = __halves2half2(__hmin(__low2half(m2), __high2half(m2)), __hmax(__low2half(x2), __high2half(x2)));
@@ -254,66 +280,100 @@ __device__ __forceinline__ void flush_values_warp(const FlushArgs& a, int warp_i
             const __half2 other = u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(mm), o));
             mm = __halves2half2(__hmin(__low2half(mm), __low2half(other)), __hmax(__high2half(mm), __high2half(other)));
         }
-        z[i] = canon(__low2float(mm));
-        range[i] = __fsub_rn(canon(__high2float(mm)), z[i]);
+        if ((octet & 3) == 0) {
+            const float z = canon(__low2float(mm));
+            float* rc = rowc + ((2 * i + sub) * 4 + j) * 4;
+            rc[0] = z;
+            rc[1] = __fsub_rn(canon(__high2float(mm)), z);
+        }
     }
-    // lane (octet & 3) == i computes row i's scale, then all 4 lanes share it
-    const int mine = octet & 3;
-    float rg = range[0];
+    __syncwarp();
+    // pass 2: each lane computes the scale of 2 of the 32 (row, group) pairs
 #pragma unroll
-    for (int i = 1; i < RPT; ++i)
-        if (mine == i) rg = range[i];
-    const float my_s = __fdiv_rn(rg, L);
-    const float my_r = my_s == 0.0f ? 0.0f : __frcp_rn(my_s);
-
-    uint8_t* cbase = a.codes + ((long long)bh * a.s_cap + a.s_off + tw + sub) * ROWB + octet * BITS;
-    const long long mbase = ((long long)bh * a.s_cap + a.s_off + tw + sub) * (kD / kG) + (octet >> 2);
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-        const float s = __shfl_sync(0xffffffffu, my_s, (lane & ~3) | i);
-        const float rc = __shfl_sync(0xffffffffu, my_r, (lane & ~3) | i);
-        if (tw + 2 * i + sub >= a.n_flush) continue;
-        const f32x2 z2[4] = {pk(z[i], z[i]), pk(z[i], z[i]), pk(z[i], z[i]), pk(z[i], z[i])};
-        const f32x2 r2[4] = {pk(rc, rc), pk(rc, rc), pk(rc, rc), pk(rc, rc)};
-        const float sv[8] = {s, s, s, s, s, s, s, s};
-        const uint32_t packed = quant8<BITS>(v[i], z2, r2, sv);
-        uint8_t* c = cbase + 2 * i * ROWB;
+    for (int e = 0; e < 2; ++e) {
+        float* rc = rowc + (e * 32 + lane) * 4;
+        const float sc = __fdiv_rn(rc[1], L);
+        rc[2] = sc;
+        rc[3] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
+    }
+    __syncwarp();
+    // pass 3: quantize
+    constexpr int ROWB = kD * BITS / 8;
+    const int nrows = min(16, a.n_flush - t0);
+    const long long row0 = (long long)bh * a.s_cap + a.s_off + t0;
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+        const int row = 2 * i + sub;
+        if (row >= nrows) break;
+        const float4 c4 = *reinterpret_cast<const float4*>(rowc + (row * 4 + j) * 4);  // z, range, s, r
+        const f32x2 z2[4] = {pk(c4.x, c4.x), pk(c4.x, c4.x), pk(c4.x, c4.x), pk(c4.x, c4.x)};
+        const f32x2 r2[4] = {pk(c4.w, c4.w), pk(c4.w, c4.w), pk(c4.w, c4.w), pk(c4.w, c4.w)};
+        const float sv[8] = {c4.z, c4.z, c4.z, c4.z, c4.z, c4.z, c4.z, c4.z};
+        const uint32_t packed = quant8<BITS>(xs[i * 32], z2, r2, sv);
+        uint8_t* c = a.codes + (row0 + row) * ROWB + octet * BITS;
         if (BITS == 4) *reinterpret_cast<uint32_t*>(c) = packed;
         else *reinterpret_cast<uint16_t*>(c) = (uint16_t)packed;
         if ((octet & 3) == 0) {
-            a.scale[mbase + 2 * i * (kD / kG)] = s;
-            a.zero[mbase + 2 * i * (kD / kG)] = __float2half_rn(z[i]);
+            const long long m = (row0 + row) * (kD / kG) + j;
+            a.scale[m] = c4.z;
+            a.zero[m] = __float2half_rn(c4.x);
         }
+    }
+    __syncwarp();
+}
+
+// Keys, values, or both: warp w of the grid handles items w, w + W, ... of the
+// list [key items | value items] (W = total warps).
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t* base = smem + warp * kWarpSmem;
+    uint8_t* st[2] = {base, base + kItemBytes};
+    float* rowc = reinterpret_cast<float*>(base + 2 * kItemBytes);
+    const int total = it.key_items + it.val_items;
+    const int stride = gridDim.x * (kThreads / 32);
+    int item = blockIdx.x * (kThreads / 32) + warp;
+    pdl_wait();
+    if (item < total) fetch_item(k, v, it, item, st[0], lane);
+    cp_async_commit();
+    if (item + stride < total) fetch_item(k, v, it, item + stride, st[1], lane);
+    cp_async_commit();
+    pdl_trigger();
+    for (int n = 0; item < total; item += stride, ++n) {
+        uint8_t* S = st[n & 1];
+        cp_async_wait1();
+        __syncwarp();
+        if (item < it.key_items) key_item<BITS>(k, it, item, S, lane);
+        else value_item<BITS>(v, it, item, S, rowc, lane);
+        __syncwarp();
+        if (item + 2 * stride < total) fetch_item(k, v, it, item + 2 * stride, S, lane);
+        cp_async_commit();
     }
 }
 
-int key_blocks_x(int n_flush) { return ((n_flush + kG - 1) / kG * 2 + 3) / 4; }   // 4 warps per block
-int value_blocks_x(int n_flush) { return (n_flush + 31) / 32; }                    // 32 tokens per block
-
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 6) flush_keys_kernel(FlushArgs a) {
-    pdl_wait();
-    flush_keys_warp<BITS>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
+    static int grid_cap = 0;
+    static bool configured = false;
+    const int smem = (kThreads / 32) * kWarpSmem;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = 152;
+        grid_cap = sms * kBlocksPerSm;
+        configured = true;
+    }
+    const long long total = (long long)it.key_items + it.val_items;
+    if (total <= 0) return cudaSuccess;
+    long long blocks = (total + 3) / 4;
+    if (blocks > grid_cap) blocks = grid_cap;
+    return launch_pdl(flush_kernel<BITS>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(kThreads) flush_values_kernel(FlushArgs a) {
-    pdl_wait();
-    flush_values_warp<BITS>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
-}
-
-// Keys and values of the same tokens in one launch: blocks [0, kbx) of each
-// grid row (blockIdx.y = head) run the key flush, the rest the value flush.
-template <int BITS>
-__global__ void __launch_bounds__(kThreads, 6) flush_kv_kernel(FlushArgs k, FlushArgs v, int kbx) {
-    pdl_wait();
-    if ((int)blockIdx.x < kbx)
-        flush_keys_warp<BITS>(k, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
-    else
-        flush_values_warp<BITS>(v, (blockIdx.x - kbx) * 4 + (threadIdx.x >> 5), blockIdx.y);
-}
-
-// Heads are split into launches of at most 65535 (the grid's y limit).
+// Pointers of heads [h0, h0 + nh) of a flush.
 FlushArgs head_slice(const FlushArgs& a, int h0, int nh, int bits, int axis) {
     FlushArgs s = a;
     s.BH = nh;
@@ -327,37 +387,36 @@ FlushArgs head_slice(const FlushArgs& a, int h0, int nh, int bits, int axis) {
 
 }  // namespace
 
-cudaError_t launch_flush(int axis, const FlushArgs& a, int bits, cudaStream_t stream) {
+// Item counts must fit in an int; inputs beyond that are split by heads.
+cudaError_t launch_flush_impl(const FlushArgs& k, const FlushArgs& v, bool do_k, bool do_v, int bits,
+                              cudaStream_t stream) {
+    const FlushArgs& a = do_k ? k : v;
     if (a.n_flush <= 0 || a.BH <= 0) return cudaSuccess;
-    const int bx = axis == 0 ? key_blocks_x(a.n_flush) : value_blocks_x(a.n_flush);
-    for (int h0 = 0; h0 < a.BH; h0 += 65535) {
-        const int nh = a.BH - h0 < 65535 ? a.BH - h0 : 65535;
-        const FlushArgs s = head_slice(a, h0, nh, bits, axis);
-        const dim3 grid(bx, nh);
-        cudaError_t e;
-        if (axis == 0)
-            e = bits == 4 ? launch_pdl(flush_keys_kernel<4>, grid, kThreads, 0, stream, s)
-                          : launch_pdl(flush_keys_kernel<2>, grid, kThreads, 0, stream, s);
-        else
-            e = bits == 4 ? launch_pdl(flush_values_kernel<4>, grid, kThreads, 0, stream, s)
-                          : launch_pdl(flush_values_kernel<2>, grid, kThreads, 0, stream, s);
+    const int ng = (a.n_flush + kG - 1) / kG, nv = (a.n_flush + 15) / 16;
+    const int per_head = (do_k ? 2 * ng : 0) + (do_v ? nv : 0);
+    const int max_heads = (int)(0x3fffffff / per_head) > 0 ? (int)(0x3fffffff / per_head) : 1;
+    for (int h0 = 0; h0 < a.BH; h0 += max_heads) {
+        const int nh = a.BH - h0 < max_heads ? a.BH - h0 : max_heads;
+        FlushArgs ks = k, vs = v;
+        if (do_k) ks = head_slice(k, h0, nh, bits, 0);
+        if (do_v) vs = head_slice(v, h0, nh, bits, 1);
+        Items it;
+        it.ng = ng;
+        it.nv = nv;
+        it.key_items = do_k ? nh * 2 * ng : 0;
+        it.val_items = do_v ? nh * nv : 0;
+        cudaError_t e = bits == 4 ? launch_items<4>(ks, vs, it, stream) : launch_items<2>(ks, vs, it, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
 
+cudaError_t launch_flush(int axis, const FlushArgs& a, int bits, cudaStream_t stream) {
+    return launch_flush_impl(a, a, axis == 0, axis == 1, bits, stream);
+}
+
 cudaError_t launch_flush_kv(const FlushArgs& k, const FlushArgs& v, int bits, cudaStream_t stream) {
-    if (k.n_flush <= 0 || k.BH <= 0) return cudaSuccess;
-    const int kbx = key_blocks_x(k.n_flush), vbx = value_blocks_x(v.n_flush);
-    for (int h0 = 0; h0 < k.BH; h0 += 65535) {
-        const int nh = k.BH - h0 < 65535 ? k.BH - h0 : 65535;
-        const FlushArgs ks = head_slice(k, h0, nh, bits, 0), vs = head_slice(v, h0, nh, bits, 1);
-        const dim3 grid(kbx + vbx, nh);
-        cudaError_t e = bits == 4 ? launch_pdl(flush_kv_kernel<4>, grid, kThreads, 0, stream, ks, vs, kbx)
-                                  : launch_pdl(flush_kv_kernel<2>, grid, kThreads, 0, stream, ks, vs, kbx);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaGetLastError();
+    return launch_flush_impl(k, v, true, true, bits, stream);
 }
 
 }  // namespace kivi
