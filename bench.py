@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="instead of the step line: per-op GB/s at larger sizes and a decode S_kv sweep")
     return p.parse_args()
 
 
@@ -488,8 +490,110 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_sweep(args):
+    """Per-op throughput at larger sizes (one JSON line per measurement).
+
+    Each measurement: a rotating pool of independent inputs totalling more than
+    4x L2, CUDA graphs of 8 launches of the op on distinct pool entries, CUDA
+    events around R graph replays; GB/s = algorithmic bytes / mean duration."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import kivi_kv_cache_gb300 as kv
+    from kivi_kv_cache_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20)
+    peak, kind = measured_peaks()
+
+    def timed(fns, nbytes, label, extra):
+        gs = []
+        for j in range(len(fns) // 8):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for f in fns[8 * j:8 * j + 8]:
+                    f()
+            gs.append(g)
+        for g in gs:
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(8, 400 // len(gs))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(reps):
+            gs[i % len(gs)].replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * 8)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        line = {"op": label, "us": round(us, 3), "bytes": int(nbytes), "GB/s": round(gbs, 1),
+                "frac_of_peak": round(gbs / peak, 4), "peak": peak, "peak_kind": kind}
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    def pool_count(bytes_each):
+        return max(8, min(64, int(math.ceil(4 * l2 / max(bytes_each, 1) / 8)) * 8))
+
+    # flush / dequant at the long-context 2-bit and qwen8b sizes
+    for name in ("qwen8b", "long2bit"):
+        w = synth.WORKLOADS[name]
+        n = kv.kivi_flush_count(w.S, w.R, w.G)
+        per = w.BH * w.S * w.D * 2 * 2 + 2 * w.BH * n * (w.D * w.bits // 8 + w.D * 6 // w.G) + w.BH * n * w.D * 4
+        P = pool_count(per)
+        ks, vs, kd, vd, xs = [], [], [], [], []
+        for i in range(P):
+            k, v, _ = synth.prefill_inputs_torch(w, 7000 + i, dev)
+            xs.append((k, v))
+            ks.append(kv.KiviStore(0, w.BH, n, w.D, w.G, w.bits, device=dev))
+            vs.append(kv.KiviStore(1, w.BH, n, w.D, w.G, w.bits, device=dev))
+            kd.append(torch.empty((w.BH, n, w.D), dtype=torch.float16, device=dev))
+            vd.append(torch.empty_like(kd[-1]))
+        ob = op_bytes(w, n, w.S - n)
+        timed([lambda i=i: kv.kivi_flush_kv(xs[i][0], xs[i][1], w.R, ks[i], vs[i]) for i in range(P)],
+              ob["flush_kv"], "flush_kv", {"workload": name, "tokens": n, "bits": w.bits, "pool": P})
+        timed([lambda i=i: kv.kivi_dequant_kv(ks[i], vs[i], n, kout=kd[i], vout=vd[i]) for i in range(P)],
+              ob["dequant_kv"], "dequant_kv", {"workload": name, "tokens": n, "bits": w.bits, "pool": P})
+        del ks, vs, kd, vd, xs
+        torch.cuda.empty_cache()
+
+    # decode over a packed store + fp16 residual
+    cases = [(1, 4096 - 128, 128, 4), (1, 8192 - 128, 128, 4), (1, 16384 - 128, 128, 4),
+             (1, 32768 - 128, 128, 2), (32, 4032, 64, 4), (16, 2048 - 128, 128, 4), (16, 16384 - 128, 128, 4)]
+    for B, S_q, n_res, bits in cases:
+        w = synth.Workload("decode", B=B, Hkv=8, Hq=32, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
+                           n_outlier=4, outlier_scale=8.0, seed=11)
+        per_tok = 2 * w.D * bits / 8 + w.D * 6 / w.G + (w.D // w.G) * 6
+        nbytes = w.BH * S_q * per_tok + w.BH * n_res * w.D * 4 + B * w.Hq * w.D * 6
+        P = pool_count(nbytes)
+        entries = []
+        for i in range(P):
+            k, v, q = synth.prefill_inputs_torch(w, 9000 + i, dev)
+            gk = kv.KiviStore(0, w.BH, S_q, w.D, w.G, bits, device=dev)
+            gv = kv.KiviStore(1, w.BH, S_q, w.D, w.G, bits, device=dev)
+            kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
+            kr = k[:, S_q:].contiguous()
+            vr = v[:, S_q:].contiguous()
+            out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device=dev)
+            need = kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, S_q, n_res, w.D)
+            ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            entries.append((q, gk, gv, kr, vr, out, ws))
+            del k, v
+        torch.cuda.synchronize()
+        fns = [lambda e=e: kv.kivi_decode_attend(e[0], e[1], e[2], S_q, e[3], e[4], n_res, w.Hkv, w.sm_scale,
+                                                 out=e[5], workspace=e[6]) for e in entries]
+        timed(fns, nbytes, "decode_attend", {"B": B, "Hkv": 8, "Hq": 32, "S_kv": S_q + n_res, "bits": bits,
+                                             "pool": P, "tokens_per_s": None})
+        del entries, fns
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

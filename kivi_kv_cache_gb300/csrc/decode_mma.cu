@@ -52,11 +52,14 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kStage = 8192;                       // bytes per stage
 constexpr int kWarpSmem = 2 * kStage;              // two stages per warp
 constexpr int kPbufOff = kWarps * kWarpSmem;       // per-warp p buffers [32][4] f32
-constexpr int kQOff = kPbufOff + kWarps * 512;     // q * score_scale [4][128] f32
-constexpr int kMiscOff = kQOff + 4 * kD * 4;       // qmax, merge m/l
+constexpr int kQRow = kD + 16;                      // padded row: channel ch at ch + (ch >> 5) * 4
+constexpr int kQOff = kPbufOff + kWarps * 512;     // q * score_scale [4][kQRow] f32
+constexpr int kMiscOff = kQOff + 4 * kQRow * 4;    // qmax, merge m/l
 constexpr int kSmemBytes = kMiscOff + 256;
-// store-tile layout inside a stage
-constexpr int kKC = 0, kVC = 2048, kKS = 4096, kKZ = 4608, kVS = 4864, kVZ = 5376;
+// store-tile layout inside a stage (KS padded like q: channel ch at ch + (ch >> 5) * 4)
+constexpr int kKC = 0, kVC = 2048, kKS = 4096, kKZ = 4672, kVS = 4928, kVZ = 5440;
+
+__device__ __forceinline__ int padc(int ch) { return ch + ((ch >> 5) << 2); }
 
 // ---------------------------------------------------------------------------
 // small PTX helpers
@@ -142,7 +145,7 @@ __device__ __forceinline__ void fetch_store_tile(const DecodeArgs& a, int bh, in
     }
     const float* ks = a.kscale + ((long long)bh * (a.s_cap / kG) + tile) * kD;
     const __half* kz = a.kzero + ((long long)bh * (a.s_cap / kG) + tile) * kD;
-    cp_async16(st + kKS + lane * 16, ks + lane * 4, true);
+    cp_async16(st + kKS + padc(lane * 4) * 4, ks + lane * 4, true);
     if (lane < 16) cp_async16(st + kKZ + lane * 16, kz + lane * 8, true);
     const float* vs = a.vscale + ((long long)bh * a.s_cap + tok0) * (kD / kG);
     const __half* vz = a.vzero + ((long long)bh * a.s_cap + tok0) * (kD / kG);
@@ -172,7 +175,7 @@ __device__ __forceinline__ void fetch_res_tile(const DecodeArgs& a, int bh, int 
 // ---------------------------------------------------------------------------
 
 template <int BITS, int GQ>
-__global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
     for (int i = tid; i < 4 * kD; i += kThreads) {
         const int h = i / kD, d = i % kD;
         const float v = h < GQ ? __half2float(a.q[((long long)b * a.Hq + h0 + h) * kD + d]) * a.score_scale : 0.f;
-        q_s[i] = v;
+        q_s[h * kQRow + padc(d)] = v;
         qm = fmaxf(qm, fabsf(v));
     }
     qm = warp_max(qm);
@@ -215,7 +218,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
 
     const int hh = g >> 1;          // head of this lane's B column n = g
     const bool lo_part = g & 1;     // hi (0) or lo (1) part of that column
-    const float* qrow = q_s + hh * kD;
+    const float* qrow = q_s + hh * kQRow;
+
+    // q (this lane's head, hi or lo) in natural channel order, scaled by 2^Er:
+    // the B operand of the residual-tile QK and of sum_d q_d z_d on store tiles
+    const int Er = safe_exp(qmax);
+    const float fBr = pow2i(Er), fCr = pow2i(-Er);
+    uint32_t br[8][2];  // K-step s: channels 16s + 2c.., 16s + 8 + 2c..
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const float2 qa = *reinterpret_cast<const float2*>(qrow + padc(16 * s + 2 * c));
+        const float2 qb = *reinterpret_cast<const float2*>(qrow + padc(16 * s + 8 + 2 * c));
+        br[s][0] = split_pair(qa.x * fBr, qa.y * fBr, lo_part);
+        br[s][1] = split_pair(qb.x * fBr, qb.y * fBr, lo_part);
+    }
 
     float m_run = -INFINITY, l_run = 0.f;  // online softmax of head c
     float o[8][4];                         // P.V of head c, store-tile channel layout
@@ -243,64 +259,71 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
         const float* VS = reinterpret_cast<const float*>(S + kVS);
         const __half* VZ = reinterpret_cast<const __half*>(S + kVZ);
 
-        // ---- QK operand B: (q s) for this lane's 32 channels, hi or lo ----
-        float qs[32];
-        float smax = 0.f, qz = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 s4 = *reinterpret_cast<const float4*>(KS + 32 * c + 4 * i);
-            const float4 q4 = *reinterpret_cast<const float4*>(qrow + 32 * c + 4 * i);
-            qs[4 * i + 0] = q4.x * s4.x;
-            qs[4 * i + 1] = q4.y * s4.y;
-            qs[4 * i + 2] = q4.z * s4.z;
-            qs[4 * i + 3] = q4.w * s4.w;
-            smax = fmaxf(smax, fmaxf(fmaxf(fabsf(s4.x), fabsf(s4.y)), fmaxf(fabsf(s4.z), fabsf(s4.w))));
+        // ---- QK operand B: q s 2^E for this lane's 32 channels, hi or lo ----
+        float smax;
+        {
+            const float4 s4 = *reinterpret_cast<const float4*>(KS + padc(4 * lane));  // scales are >= 0
+            smax = warp_max(fmaxf(fmaxf(s4.x, s4.y), fmaxf(s4.z, s4.w)));
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 z8 = *reinterpret_cast<const uint4*>(KZ + 32 * c + 8 * i);
-            const uint32_t zw[4] = {z8.x, z8.y, z8.z, z8.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 zf = __half22float2(u32_as_h2(zw[k]));
-                qz = fmaf(qrow[32 * c + 8 * i + 2 * k], zf.x, qz);
-                qz = fmaf(qrow[32 * c + 8 * i + 2 * k + 1], zf.y, qz);
-            }
-        }
-        smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
-        smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
-        qz += __shfl_xor_sync(0xffffffffu, qz, 1);
-        qz += __shfl_xor_sync(0xffffffffu, qz, 2);
         const int E = safe_exp(qmax * smax);
         const float fB = pow2i(E);           // B = q s 2^E
         const float fC = pow2i(9 - E);       // score = C 2^(9-E) (codes are c 2^-9)
+        const f32x2 fB2 = pk(fB, fB);
         uint32_t bq[8][2];
         if (BITS == 4) {
             // word m of this lane's 16-byte chunk: channels 32c + 8m + {0..7};
             // K-step 2m pairs channels (0,2),(4,6), K-step 2m+1 pairs (1,3),(5,7)
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float* v = qs + 8 * m + e;
-                    bq[2 * m + e][0] = split_pair(v[0] * fB, v[2] * fB, lo_part);
-                    bq[2 * m + e][1] = split_pair(v[4] * fB, v[6] * fB, lo_part);
-                }
+                const float4 sa = *reinterpret_cast<const float4*>(KS + padc(32 * c + 8 * m));
+                const float4 sb = *reinterpret_cast<const float4*>(KS + padc(32 * c + 8 * m + 4));
+                const float4 qa = *reinterpret_cast<const float4*>(qrow + padc(32 * c + 8 * m));
+                const float4 qb = *reinterpret_cast<const float4*>(qrow + padc(32 * c + 8 * m + 4));
+                const float2 v01 = upk(mul2(mul2(pk(qa.x, qa.y), pk(sa.x, sa.y)), fB2));
+                const float2 v23 = upk(mul2(mul2(pk(qa.z, qa.w), pk(sa.z, sa.w)), fB2));
+                const float2 v45 = upk(mul2(mul2(pk(qb.x, qb.y), pk(sb.x, sb.y)), fB2));
+                const float2 v67 = upk(mul2(mul2(pk(qb.z, qb.w), pk(sb.z, sb.w)), fB2));
+                bq[2 * m][0] = split_pair(v01.x, v23.x, lo_part);
+                bq[2 * m][1] = split_pair(v45.x, v67.x, lo_part);
+                bq[2 * m + 1][0] = split_pair(v01.y, v23.y, lo_part);
+                bq[2 * m + 1][1] = split_pair(v45.y, v67.y, lo_part);
             }
         } else {
             // word m (4 bytes) of this lane's 8 bytes: channels 32c + 16m + {0..15};
             // K-step 4m + k pairs channels (k, k+4), (k+8, k+12)
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 s4 = *reinterpret_cast<const float4*>(KS + padc(32 * c + 16 * m + 4 * i));
+                    const float4 q4 = *reinterpret_cast<const float4*>(qrow + padc(32 * c + 16 * m + 4 * i));
+                    const float2 lo2 = upk(mul2(mul2(pk(q4.x, q4.y), pk(s4.x, s4.y)), fB2));
+                    const float2 hi2 = upk(mul2(mul2(pk(q4.z, q4.w), pk(s4.z, s4.w)), fB2));
+                    v[4 * i] = lo2.x;
+                    v[4 * i + 1] = lo2.y;
+                    v[4 * i + 2] = hi2.x;
+                    v[4 * i + 3] = hi2.y;
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float* v = qs + 16 * m + k;
-                    bq[4 * m + k][0] = split_pair(v[0] * fB, v[4] * fB, lo_part);
-                    bq[4 * m + k][1] = split_pair(v[8] * fB, v[12] * fB, lo_part);
+                    bq[4 * m + k][0] = split_pair(v[k], v[k + 4], lo_part);
+                    bq[4 * m + k][1] = split_pair(v[k + 8], v[k + 12], lo_part);
                 }
             }
         }
-        const float qz_c = __shfl_sync(0xffffffffu, qz, 8 * c);  // sum q z of head c
+        // ---- sum_d q_d z_d of head c on the tensor cores: A = key zeros in every row ----
+        float qz_c;
+        {
+            float zacc[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t* kz32 = reinterpret_cast<const uint32_t*>(KZ);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t za = kz32[8 * s + c], zb = kz32[8 * s + 4 + c];  // channels 16s+2c.., 16s+8+2c..
+                mma16816(zacc, za, za, zb, zb, br[s][0], br[s][1]);
+            }
+            qz_c = (zacc[0] + zacc[1]) * fCr;
+        }
 
         // ---- scores: 2 M-tiles of 16 tokens ----
         float sc[4];  // tokens g, g+8, g+16, g+24 for head c
@@ -363,12 +386,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
         ps += __shfl_xor_sync(0xffffffffu, ps, 16);
         l_run = fmaf(l_run, corr, ps);
         m_run = m_new;
+        {
+            const f32x2 c2 = pk(corr, corr);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            o[i][0] *= corr;
-            o[i][1] *= corr;
-            o[i][2] *= corr;
-            o[i][3] *= corr;
+            for (int i = 0; i < 8; ++i) {
+                const float2 lo = upk(mul2(pk(o[i][0], o[i][1]), c2)), hi = upk(mul2(pk(o[i][2], o[i][3]), c2));
+                o[i][0] = lo.x;
+                o[i][1] = lo.y;
+                o[i][2] = hi.x;
+                o[i][3] = hi.y;
+            }
         }
         // p of tokens g, g+8, g+16, g+24 (head c) -> pbuf; p.vzero partials
         pbuf[(g) * 4 + c] = p[0];
@@ -409,8 +436,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
             const float sb0[4] = {vb0.x, vb0.y, vb0.z, vb0.w}, sb1[4] = {vb1.x, vb1.y, vb1.z, vb1.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                bp[j][ks][0] = split_pair(pa0 * sa0[j], pa1 * sa1[j], lo_part);
-                bp[j][ks][1] = split_pair(pb0 * sb0[j], pb1 * sb1[j], lo_part);
+                const float2 a2 = upk(mul2(pk(pa0, pa1), pk(sa0[j], sa1[j])));
+                const float2 b2 = upk(mul2(pk(pb0, pb1), pk(sb0[j], sb1[j])));
+                bp[j][ks][0] = split_pair(a2.x, a2.y, lo_part);
+                bp[j][ks][1] = split_pair(b2.x, b2.y, lo_part);
             }
         }
 
@@ -492,16 +521,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) orr[i][0] = orr[i][1] = orr[i][2] = orr[i][3] = 0.f;
     if (r_begin < w1) {
-        const int Er = safe_exp(qmax);
-        const float fBr = pow2i(Er), fCr = pow2i(-Er);
-        uint32_t br[8][2];  // K-step s: channels 16s + 2c.., 16s + 8 + 2c..
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const float2 qa = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * c);
-            const float2 qb = *reinterpret_cast<const float2*>(qrow + 16 * s + 8 + 2 * c);
-            br[s][0] = split_pair(qa.x * fBr, qa.y * fBr, lo_part);
-            br[s][1] = split_pair(qb.x * fBr, qb.y * fBr, lo_part);
-        }
         for (int rt = r_begin; rt < w1; ++rt) {
             const int rtile = rt - a.n_store_tiles;
             const int nvalid = min(32, a.n_res - rtile * 32);

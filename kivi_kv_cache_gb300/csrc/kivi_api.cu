@@ -45,7 +45,7 @@ kivi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_
 
 // Split plan for the decode. The tensor-core kernel (<= 4 query heads per KV
 // head) gives each of its 4 warps a run of tiles_per_warp 32-token tiles,
-// sized for about 8 warps (2 CTAs) per SM over the whole batch; the fp32 kernel (8
+// sized for about 12 warps (3 CTAs) per SM over the whole batch; the fp32 kernel (8
 // query heads per KV head) targets two CTAs per SM. Whole tiles per split,
 // no empty split.
 DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res) {
@@ -54,7 +54,7 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res) {
     p.n_tiles = p.n_store_tiles + (n_res + kG - 1) / kG;
     const long long heads = (long long)B * Hkv;
     if (Hkv > 0 && Hq / Hkv <= 4) {
-        const long long target = 8LL * sm_count();
+        const long long target = 12LL * sm_count();
         long long tpw = (heads * p.n_tiles + target - 1) / target;
         if (tpw < 1) tpw = 1;
         p.tiles_per_warp = (int)tpw;
