@@ -9,6 +9,7 @@ single-layer workload (B=1, H_kv=8, 32 query heads, D=128, 2238-token prompt,
   3. dequantize the packed K and V stores back to fp16 (one launch),
   4. fused dequantize-and-attend decode of one query token per head (split over
      the cached tokens + log-sum-exp combine).
+Steps 2 and 4 run on a side stream (4 after the flush), beside step 3.
 value = algorithmic HBM bytes of the step / device time per step (GB/s).
 
 Inputs rotate through a pool of independent instances whose total size is
@@ -52,6 +53,7 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--hashes", action="store_true", help="print the source hash of each op and exit")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step line: per-op GB/s at larger sizes and a decode S_kv sweep")
     return p.parse_args()
@@ -86,15 +88,22 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def read_traffic(kernel_file: str, op: str):
-    """DRAM bytes per launch recorded from an ncu capture, if the kernel source
-    is unchanged since (profiles/traffic.txt lines: op sha256 bytes)."""
+def source_hash(files) -> str:
+    """First 16 hex digits of the sha256 of the op's CUDA sources."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic.txt")
-    src = os.path.join(ROOT, "kivi_kv_cache_gb300", "csrc", kernel_file)
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "kivi_kv_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(files, op: str):
+    """DRAM bytes per launch of an op from an ncu capture (profiles/traffic.txt
+    lines 'op sha bytes'), or None if the op's sources changed since."""
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        for ln in open(path):
+        sha = source_hash(files)
+        for ln in open(os.path.join(ROOT, "profiles", "traffic.txt")):
             parts = ln.split()
             if len(parts) >= 3 and not ln.startswith("#") and parts[0] == op and parts[1] == sha:
                 return float(parts[2])
@@ -185,25 +194,31 @@ class Instance:
         self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=device)
         need = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, self.n_flush, self.n_res, w.D)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        self.side = torch.cuda.Stream(device=device)
+        self.flushed = torch.cuda.Event()
 
-    def step(self, ev=None):
+    def step(self, join=True):
+        """One pass of the hot path. The flush and the dequant run on the
+        current stream; the residual append and the decode (which needs the
+        flushed store) run on a side stream beside the dequant; the side
+        stream joins the current one at the end (or, with join=False, when the
+        caller joins it, so independent steps may overlap)."""
+        import torch
         kv, w = self.kv, self.w
-        if ev is not None:
-            ev[0].record()
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            kv.kivi_residual_append_kv(self.k[:, self.n_flush:], self.v[:, self.n_flush:], self.kres, self.vres,
+                                       0, self.n_res)
         kv.kivi_flush_kv(self.k, self.v, w.R, self.kst, self.vst)
-        if ev is not None:
-            ev[1].record()
-        kv.kivi_residual_append_kv(self.k[:, self.n_flush:], self.v[:, self.n_flush:], self.kres, self.vres,
-                                   0, self.n_res)
-        if ev is not None:
-            ev[2].record()
+        self.flushed.record(main)
         kv.kivi_dequant_kv(self.kst, self.vst, self.n_flush, kout=self.kdq, vout=self.vdq)
-        if ev is not None:
-            ev[3].record()
-        kv.kivi_decode_attend(self.q, self.kst, self.vst, self.n_flush, self.kres, self.vres, self.n_res,
-                              w.Hkv, w.sm_scale, out=self.out, workspace=self.ws)
-        if ev is not None:
-            ev[4].record()
+        with torch.cuda.stream(self.side):
+            self.side.wait_event(self.flushed)
+            kv.kivi_decode_attend(self.q, self.kst, self.vst, self.n_flush, self.kres, self.vres, self.n_res,
+                                  w.Hkv, w.sm_scale, out=self.out, workspace=self.ws)
+        if join:
+            main.wait_stream(self.side)
 
     def nbytes(self):
         ts = [self.k, self.v, self.q, self.kres, self.vres, self.kdq, self.vdq, self.out, self.ws,
@@ -213,8 +228,8 @@ class Instance:
 
 OPS = ["flush_kv", "residual_append", "dequant_kv", "decode_attend"]
 GRAPH_STEPS = 8
-OP_KERNEL_FILE = {"flush_kv": "flush.cu", "residual_append": "residual.cu", "dequant_kv": "dequant.cu",
-                  "decode_attend": "decode.cu"}
+OP_KERNEL_FILES = {"flush_kv": ["flush.cu"], "residual_append": ["residual.cu"], "dequant_kv": ["dequant.cu"],
+                   "decode_attend": ["decode_mma.cu", "decode.cu"]}
 LAUNCHES = {"flush_kv": 1, "residual_append": 1, "dequant_kv": 1}
 
 
@@ -256,8 +271,14 @@ def run_gb300(args, rank, world, local_rank):
             fn()
         return g
 
-    multi = [capture(lambda j=j: [insts[j * GRAPH_STEPS + t].step() for t in range(GRAPH_STEPS)])
-             for j in range(pool // GRAPH_STEPS)]
+    def steps(j):
+        group = insts[j * GRAPH_STEPS:(j + 1) * GRAPH_STEPS]
+        for inst in group:
+            inst.step(join=False)
+        for inst in group:
+            torch.cuda.current_stream().wait_stream(inst.side)
+
+    multi = [capture(lambda j=j: steps(j)) for j in range(pool // GRAPH_STEPS)]
     single = [capture(lambda I=I: I.step()) for I in insts]
     for i in range(max(1, args.warmup // GRAPH_STEPS)):
         multi[i % len(multi)].replay()
@@ -332,7 +353,7 @@ def run_gb300(args, rank, world, local_rank):
     achieved = ob[dom] / (op_ms[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                 "peak_kind": peak_kind + " hbm_gbs (copy, burst)", "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": read_traffic(OP_KERNEL_FILE[dom], dom)}
+                "frac": round(achieved / peak, 4), "traffic": read_traffic(OP_KERNEL_FILES[dom], dom)}
 
     # end to end: host inputs (pinned) -> device, the step, result -> host
     e2e = None
@@ -591,6 +612,10 @@ def run_sweep(args):
 
 def main():
     args = parse_args()
+    if args.hashes:
+        for op, files in OP_KERNEL_FILES.items():
+            print(op, source_hash(files))
+        return
     if args.sweep:
         run_sweep(args)
         return

@@ -17,9 +17,9 @@
 //    combine min/max with two shuffles; each of the four computes the scale
 //    of two channels and shares it; every thread then quantizes its own 8
 //    tokens from registers (x is read from HBM exactly once).
-//  * values: 4 lanes (4 x 8 channels) form one 32-channel group; min/max is a
-//    2-step __shfl_xor butterfly on packed (min, max) halves; each of the 4
-//    lanes computes the scale of one of its 4 rows and shares it.
+//  * values: one lane owns whole 32-channel groups of a row (min/max, scale
+//    and the 16-byte code word of a group in one lane, no shuffles); shared
+//    memory chunks are swizzled by row so a warp's reads are conflict-free.
 //  * min/max run on packed fp16 (exact). The quantizer runs on packed fp32x2
 //    IEEE operations. The quotient: y = RN(a * RN(1/s)) lies within 2^-18 of
 //    RN(a/s) for quotients below 16, so rint(y) == rint(RN(a/s)) whenever y is
@@ -120,7 +120,7 @@ __device__ __forceinline__ float canon(float v) { return __fadd_rn(v, 0.0f); }
 // never read from global memory.
 
 constexpr int kItemBytes = 4096;
-constexpr int kWarpSmem = 2 * kItemBytes + 1024;  // two stages + value-row constants
+constexpr int kWarpSmem = 2 * kItemBytes;  // two stages
 constexpr int kBlocksPerSm = 4;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -157,9 +157,10 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
         const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
         const uint8_t* src = reinterpret_cast<const uint8_t*>(v.x) + ((long long)bh * v.x_bh_stride + t0) * 256;
 #pragma unroll
-        for (int i = lane; i < 256; i += 32) {  // 16 rows x 16 chunks
-            const bool ok = t0 + (i >> 4) < v.n_flush;
-            cp_async16(st + i * 16, ok ? (const void*)(src + i * 16) : (const void*)src, ok);
+        for (int i = lane; i < 256; i += 32) {  // 16 rows x 16 chunks, chunk c of row r at c ^ (r & 7)
+            const int row = i >> 4, col = i & 15;
+            const bool ok = t0 + row < v.n_flush;
+            cp_async16(st + row * 256 + ((col ^ (row & 7)) << 4), ok ? (const void*)(src + i * 16) : (const void*)src, ok);
         }
     }
 }
@@ -257,69 +258,54 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     }
 }
 
-// values: lane = sub * 16 + octet; row 2i + sub of the item for i in [0, 8);
-// lanes 4j..4j+3 of a half-warp form value group j.
+// values: lane = 16 jp + row; the lane quantizes the groups j = 2 jp and
+// 2 jp + 1 (32 channels each) of row `row` of the item: min/max, scale and
+// codes of a whole group in one lane, no shuffles, one 16-byte code store
+// (4-bit) per group.
 template <int BITS>
 __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
-                                           float* rowc, int lane) {
+                                           int lane) {
     const int vi = item - it.key_items;
     const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
-    const int octet = lane & 15, sub = lane >> 4, j = octet >> 2;
+    const int row = lane & 15, jp = lane >> 4;
+    if (t0 + row >= a.n_flush) return;
     const float L = (float)Levels<BITS>::value;
-    const uint4* xs = reinterpret_cast<const uint4*>(st) + sub * 16 + octet;  // row stride 16 vectors
-    // pass 1: (zero, range) of every row's group -> rowc[row][j][0..1]
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint4 x = xs[i * 32];
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        const __half2 m2 = __hmin2(__hmin2(u32_as_h2(w[0]), u32_as_h2(w[1])), __hmin2(u32_as_h2(w[2]), u32_as_h2(w[3])));
-        const __half2 x2 = __hmax2(__hmax2(u32_as_h2(w[0]), u32_as_h2(w[1])), __hmax2(u32_as_h2(w[2]), u32_as_h2(w[3])));
-        __half2 mm = __halves2half2(__hmin(__low2half(m2), __high2half(m2)), __hmax(__low2half(x2), __high2half(x2)));
-#pragma unroll
-        for (int o = 1; o < 4; o <<= 1) {
-            const __half2 other = u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(mm), o));
-            mm = __halves2half2(__hmin(__low2half(mm), __low2half(other)), __hmax(__high2half(mm), __high2half(other)));
-        }
-        if ((octet & 3) == 0) {
-            const float z = canon(__low2float(mm));
-            float* rc = rowc + ((2 * i + sub) * 4 + j) * 4;
-            rc[0] = z;
-            rc[1] = __fsub_rn(canon(__high2float(mm)), z);
-        }
-    }
-    __syncwarp();
-    // pass 2: each lane computes the scale of 2 of the 32 (row, group) pairs
+    const uint4* xs = reinterpret_cast<const uint4*>(st + row * 256);
+    const long long grow = (long long)bh * a.s_cap + a.s_off + t0 + row;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-        float* rc = rowc + (e * 32 + lane) * 4;
-        const float sc = __fdiv_rn(rc[1], L);
-        rc[2] = sc;
-        rc[3] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
-    }
-    __syncwarp();
-    // pass 3: quantize
-    constexpr int ROWB = kD * BITS / 8;
-    const int nrows = min(16, a.n_flush - t0);
-    const long long row0 = (long long)bh * a.s_cap + a.s_off + t0;
-#pragma unroll 1
-    for (int i = 0; i < 8; ++i) {
-        const int row = 2 * i + sub;
-        if (row >= nrows) break;
-        const float4 c4 = *reinterpret_cast<const float4*>(rowc + (row * 4 + j) * 4);  // z, range, s, r
-        const f32x2 z2[4] = {pk(c4.x, c4.x), pk(c4.x, c4.x), pk(c4.x, c4.x), pk(c4.x, c4.x)};
-        const f32x2 r2[4] = {pk(c4.w, c4.w), pk(c4.w, c4.w), pk(c4.w, c4.w), pk(c4.w, c4.w)};
-        const float sv[8] = {c4.z, c4.z, c4.z, c4.z, c4.z, c4.z, c4.z, c4.z};
-        const uint32_t packed = quant8<BITS>(xs[i * 32], z2, r2, sv);
-        uint8_t* c = a.codes + (row0 + row) * ROWB + octet * BITS;
-        if (BITS == 4) *reinterpret_cast<uint32_t*>(c) = packed;
-        else *reinterpret_cast<uint16_t*>(c) = (uint16_t)packed;
-        if ((octet & 3) == 0) {
-            const long long m = (row0 + row) * (kD / kG) + j;
-            a.scale[m] = c4.z;
-            a.zero[m] = __float2half_rn(c4.x);
+        const int j = 2 * jp + e;
+        uint4 x[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = xs[(4 * j + k) ^ (row & 7)];
+        __half2 m2 = u32_as_h2(x[0].x), x2 = m2;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                m2 = __hmin2(m2, u32_as_h2(w[i]));
+                x2 = __hmax2(x2, u32_as_h2(w[i]));
+            }
         }
+        const float z = canon(__half2float(__hmin(__low2half(m2), __high2half(m2))));
+        const float sc = __fdiv_rn(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z), L);
+        const float rc = sc == 0.0f ? 0.0f : __frcp_rn(sc);
+        const f32x2 z1 = pk(z, z), r1 = pk(rc, rc);
+        const f32x2 z2[4] = {z1, z1, z1, z1}, r2[4] = {r1, r1, r1, r1};
+        const float sv[8] = {sc, sc, sc, sc, sc, sc, sc, sc};
+        uint32_t pq[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS>(x[k], z2, r2, sv);
+        if (BITS == 4) {
+            *reinterpret_cast<uint4*>(a.codes + grow * 64 + 16 * j) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
+        } else {
+            *reinterpret_cast<uint2*>(a.codes + grow * 32 + 8 * j) =
+                make_uint2(pq[0] | (pq[1] << 16), pq[2] | (pq[3] << 16));
+        }
+        a.scale[grow * (kD / kG) + j] = sc;
+        a.zero[grow * (kD / kG) + j] = __float2half_rn(z);
     }
-    __syncwarp();
 }
 
 // Keys, values, or both: warp w of the grid handles items w, w + W, ... of the
@@ -330,7 +316,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t* base = smem + warp * kWarpSmem;
     uint8_t* st[2] = {base, base + kItemBytes};
-    float* rowc = reinterpret_cast<float*>(base + 2 * kItemBytes);
     const int total = it.key_items + it.val_items;
     const int stride = gridDim.x * (kThreads / 32);
     int item = blockIdx.x * (kThreads / 32) + warp;
@@ -345,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs
         cp_async_wait1();
         __syncwarp();
         if (item < it.key_items) key_item<BITS>(k, it, item, S, lane);
-        else value_item<BITS>(v, it, item, S, rowc, lane);
+        else value_item<BITS>(v, it, item, S, lane);
         __syncwarp();
         if (item + 2 * stride < total) fetch_item(k, v, it, item + 2 * stride, S, lane);
         cp_async_commit();
