@@ -8,7 +8,7 @@ single-layer workload (B=1, H_kv=8, 32 query heads, D=128, 2238-token prompt,
   2. append the 158-token fp16 tail to the K and V residual windows (one launch),
   3. dequantize the packed K and V stores back to fp16 (one launch),
   4. fused dequantize-and-attend decode of one query token per head (split over
-     the cached tokens + log-sum-exp combine).
+     the cached tokens; the last CTA of each head merges the splits).
 Steps 2 and 4 run on a side stream (4 after the flush), beside step 3.
 value = algorithmic HBM bytes of the step / device time per step (GB/s).
 
@@ -42,6 +42,14 @@ METRIC = "KIVI flush/dequant/decode-attend HBM GB/s (% of peak); decode tokens/s
 FALLBACK_HBM_GBS = 6800.0
 
 
+# --profile-case NAME: (op kind, B, S_q, n_res, bits); flush cases use the named workload
+PROFILE_CASES = {
+    "flush_long2bit": ("flush", 0, 0, 0, 2),
+    "decode_b1_16k": ("decode", 1, 16384 - 128, 128, 4),
+    "decode_b32_4k": ("decode", 32, 4032, 64, 4),
+}
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -54,8 +62,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--hashes", action="store_true", help="print the source hash of each op and exit")
-    p.add_argument("--sweep", action="store_true",
-                   help="instead of the step line: per-op GB/s at larger sizes and a decode S_kv sweep")
+    p.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
+                   help="run one op on one case a few times, untimed (a target for ncu captures)")
+    p.add_argument("--sweep", nargs="?", const="all", choices=["all", "decode"],
+                   help="instead of the step line: per-op GB/s at larger sizes and a decode S_kv sweep "
+                        "('decode': the decode cases only)")
     return p.parse_args()
 
 
@@ -193,7 +204,7 @@ class Instance:
         self.vdq = torch.empty_like(self.kdq)
         self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=device)
         need = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, self.n_flush, self.n_res, w.D)
-        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        self.ws = kv.kivi_decode_workspace(need, device)
         self.side = torch.cuda.Stream(device=device)
         self.flushed = torch.cuda.Event()
 
@@ -229,8 +240,8 @@ class Instance:
 OPS = ["flush_kv", "residual_append", "dequant_kv", "decode_attend"]
 GRAPH_STEPS = 8
 OP_KERNEL_FILES = {"flush_kv": ["flush.cu"], "residual_append": ["residual.cu"], "dequant_kv": ["dequant.cu"],
-                   "decode_attend": ["decode_mma.cu", "decode.cu"]}
-LAUNCHES = {"flush_kv": 1, "residual_append": 1, "dequant_kv": 1}
+                   "decode_attend": ["decode_attend.cu"]}
+LAUNCHES = {"flush_kv": 1, "residual_append": 1, "dequant_kv": 1, "decode_attend": 1}
 
 
 def run_gb300(args, rank, world, local_rank):
@@ -253,9 +264,7 @@ def run_gb300(args, rank, world, local_rank):
     pool = args.pool or int(min(64, max(2, math.ceil(4 * l2 / inst_bytes))))
     pool = max(GRAPH_STEPS, (pool + GRAPH_STEPS - 1) // GRAPH_STEPS * GRAPH_STEPS)
     insts = [probe] + [Instance(w, 1000 * rank + i, dev, kv, synth) for i in range(1, pool)]
-    n_split = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, probe.n_flush, probe.n_res, w.D)
-    decode_launches = 2 if n_split > 0 else 1
-    launches_per_step = sum(LAUNCHES.values()) + decode_launches
+    launches_per_step = sum(LAUNCHES.values())
 
     # eager warm-up; then CUDA graphs of GRAPH_STEPS consecutive steps, each on
     # its own instance (a graph launch costs microseconds; steps inside a graph
@@ -558,7 +567,7 @@ def run_sweep(args):
         return max(8, min(64, int(math.ceil(4 * l2 / max(bytes_each, 1) / 8)) * 8))
 
     # flush / dequant at the long-context 2-bit and qwen8b sizes
-    for name in ("qwen8b", "long2bit"):
+    for name in (("qwen8b", "long2bit") if args.sweep == "all" else ()):
         w = synth.WORKLOADS[name]
         n = kv.kivi_flush_count(w.S, w.R, w.G)
         per = w.BH * w.S * w.D * 2 * 2 + 2 * w.BH * n * (w.D * w.bits // 8 + w.D * 6 // w.G) + w.BH * n * w.D * 4
@@ -580,7 +589,7 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
     # decode over a packed store + fp16 residual
-    cases = [(1, 4096 - 128, 128, 4), (1, 8192 - 128, 128, 4), (1, 16384 - 128, 128, 4),
+    cases = [(1, 2080, 158, 4), (1, 4096 - 128, 128, 4), (1, 8192 - 128, 128, 4), (1, 16384 - 128, 128, 4),
              (1, 32768 - 128, 128, 2), (32, 4032, 64, 4), (16, 2048 - 128, 128, 4), (16, 16384 - 128, 128, 4)]
     for B, S_q, n_res, bits in cases:
         w = synth.Workload("decode", B=B, Hkv=8, Hq=32, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
@@ -598,7 +607,7 @@ def run_sweep(args):
             vr = v[:, S_q:].contiguous()
             out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device=dev)
             need = kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, S_q, n_res, w.D)
-            ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            ws = kv.kivi_decode_workspace(need, dev)
             entries.append((q, gk, gv, kr, vr, out, ws))
             del k, v
         torch.cuda.synchronize()
@@ -610,8 +619,49 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_profile_case(name: str, reps: int = 3):
+    """A few untimed launches of one op, for profiler captures of a size the
+    step bench does not run."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import kivi_kv_cache_gb300 as kv
+    from kivi_kv_cache_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kind, B, S_q, n_res, bits = PROFILE_CASES[name]
+    if kind == "flush":
+        w = synth.WORKLOADS[name.split("_")[1]]
+        n = kv.kivi_flush_count(w.S, w.R, w.G)
+        k, v, _ = synth.prefill_inputs_torch(w, 1, dev)
+        ks = kv.KiviStore(0, w.BH, n, w.D, w.G, w.bits, device=dev)
+        vs = kv.KiviStore(1, w.BH, n, w.D, w.G, w.bits, device=dev)
+        for _ in range(reps):
+            kv.kivi_flush_kv(k, v, w.R, ks, vs)
+    else:
+        w = synth.Workload("decode", B=B, Hkv=8, Hq=32, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
+                           n_outlier=4, outlier_scale=8.0, seed=4)
+        k, v, q = synth.prefill_inputs_torch(w, 2, dev)
+        gk = kv.KiviStore(0, w.BH, S_q, w.D, w.G, bits, device=dev)
+        gv = kv.KiviStore(1, w.BH, S_q, w.D, w.G, bits, device=dev)
+        kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
+        kr = k[:, S_q:].contiguous()
+        vr = v[:, S_q:].contiguous()
+        del k, v
+        ws = kv.kivi_decode_workspace(kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, S_q, n_res, w.D), dev)
+        for _ in range(reps):
+            kv.kivi_decode_attend(q, gk, gv, S_q, kr, vr, n_res, w.Hkv, w.sm_scale, workspace=ws)
+    torch.cuda.synchronize()
+    print("ok", name)
+
+
 def main():
     args = parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     if args.hashes:
         for op, files in OP_KERNEL_FILES.items():
             print(op, source_hash(files))

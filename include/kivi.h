@@ -185,9 +185,28 @@ kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, i
 /*
  * Bytes of device workspace kivi_decode_attend needs for these sizes on the
  * current device (the split count depends on the device's SM count). Returns
- * 0 for invalid sizes. Host only (reads the device's SM count once).
+ * 0 when the decode runs as a single split per (batch, KV head) and needs no
+ * workspace, and 0 for invalid sizes. Host only (reads the device's SM count
+ * once).
+ *
+ * Workspace layout: the first KIVI_DECODE_COUNTER_BYTES bytes hold the merge
+ * counters of the split decode, one per (batch, KV head); the split partials
+ * follow. The counters must be zero before a workspace's first use
+ * (kivi_decode_workspace_init, or any zero fill), and every completed call
+ * leaves them zero again, whatever its sizes. The rest of the workspace is
+ * scratch whose contents on entry are ignored. One workspace serves one call
+ * at a time: calls whose kernels may overlap need distinct workspaces.
  */
+#define KIVI_DECODE_COUNTER_BYTES 32768u
 size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D);
+
+/*
+ * Zero the merge counters of a fresh decode workspace: the first
+ * min(workspace_bytes, KIVI_DECODE_COUNTER_BYTES) bytes, by an asynchronous
+ * memset on `stream`. Needed once per workspace, before its first decode.
+ * INVALID_ARG if workspace is NULL and workspace_bytes > 0.
+ */
+kivi_status kivi_decode_workspace_init(void* workspace, size_t workspace_bytes, kivi_stream_t stream);
 
 /*
  * Fused dequantize-and-attend single-token decode ([F] "So why does the kernel
@@ -203,11 +222,12 @@ size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, in
  * residuals are fp16 [B*Hkv, res_cap, D]. q fp16 [B, Hq, D]; out f32
  * [B, Hq, D]. Accumulation is fp32; max-abs error against the float64 oracle
  * is well below 2e-3 for inputs of unit scale.
- * workspace: device memory of at least kivi_decode_workspace_size(...) bytes
- * (split partials; contents on entry are ignored).
+ * workspace: device memory of at least kivi_decode_workspace_size(...) bytes,
+ * laid out and initialised as described there (may be NULL when that size is
+ * 0).
  * Errors: INVALID_ARG if S_q + n_res == 0, S_q > s_cap, n_res > res_cap or
- * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv is not 1, 2, 4 or 8; WORKSPACE if the
- * workspace is NULL or too small.
+ * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv > 8; WORKSPACE if the workspace is
+ * NULL or too small.
  */
 kivi_status kivi_decode_attend(const void* q_f16,
                                const void* kcodes_u8, const float* kscale, const void* kzero_f16,
@@ -228,7 +248,7 @@ kivi_status kivi_decode_attend(const void* q_f16,
  * interface addition of this library.
  *
  * Instead of a workspace argument it uses one library-owned device array of
- * KIVI_NOALLOC_SCRATCH_BYTES (2 MiB) per device, reserved when the library's
+ * KIVI_NOALLOC_SCRATCH_BYTES (4 MiB) per device, reserved when the library's
  * device code is loaded and kept until the process exits. It allocates
  * nothing itself.
  *   - Size limit: if kivi_decode_workspace_size(...) for these sizes exceeds
@@ -237,6 +257,8 @@ kivi_status kivi_decode_attend(const void* q_f16,
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's contents. Calls whose kernels overlap on the GPU (two
  *     unordered streams) race and give wrong results; order them.
+ *   - Its merge counters start at zero (the array is zero-initialised when
+ *     the device code loads) and every completed call leaves them zero.
  *   - First call per device: it looks up the array's device address with
  *     cudaGetSymbolAddress (the current device must be the one the pointers
  *     belong to) and caches it; this may load the library's device code, so
@@ -245,7 +267,7 @@ kivi_status kivi_decode_attend(const void* q_f16,
  * Every other argument, check, status and result is that of
  * kivi_decode_attend.
  */
-#define KIVI_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
+#define KIVI_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
 kivi_status kivi_decode_attend_noalloc(const void* q_f16,
                                        const void* kcodes_u8, const float* kscale, const void* kzero_f16,
                                        const void* vcodes_u8, const float* vscale, const void* vzero_f16,

@@ -21,10 +21,14 @@ __all__ = [
     "kivi_status_string", "kivi_version", "kivi_flush_count",
     "kivi_flush_keys", "kivi_flush_values", "kivi_flush_kv", "kivi_dequant", "kivi_dequant_kv",
     "kivi_residual_append", "kivi_residual_compact", "kivi_residual_append_kv", "kivi_residual_compact_kv",
-    "kivi_decode_workspace_size", "kivi_decode_attend", "kivi_decode_attend_noalloc",
+    "kivi_decode_workspace_size", "kivi_decode_workspace", "kivi_decode_workspace_init",
+    "kivi_decode_attend", "kivi_decode_attend_noalloc",
 ]
 
-library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkivi_gb300.so")
+# KIVI_GB300_LIB: load the library from another path (e.g. a build with other
+# compile-time tuning); the default is the in-tree build.
+library_path = os.environ.get("KIVI_GB300_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                                 "libkivi_gb300.so")
 
 KIVI_AXIS_KEYS = 0
 KIVI_AXIS_VALUES = 1
@@ -67,6 +71,7 @@ def lib() -> ctypes.CDLL:
             "kivi_residual_append": ([P, I, I, P, I, I, I, I, P], I),
             "kivi_residual_compact": ([P, I, I, I, I, I, P], I),
             "kivi_decode_workspace_size": ([I, I, I, I, I, I], Z),
+            "kivi_decode_workspace_init": ([P, Z, P], I),
             "kivi_decode_attend": ([P, P, P, P, P, P, P, I, I, P, P, I, I, I, I, I, I, I, I, F, P, P, Z, P], I),
         }
         for name, (args, res) in sig.items():
@@ -242,6 +247,20 @@ def kivi_decode_workspace_size(B: int, Hq: int, Hkv: int, S_q: int, n_res: int, 
     return lib().kivi_decode_workspace_size(B, Hq, Hkv, S_q, n_res, D)
 
 
+def kivi_decode_workspace_init(workspace, stream=None) -> None:
+    """Zero the merge counters of a fresh workspace (once, before its first decode)."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("kivi_decode_workspace_init", lib().kivi_decode_workspace_init(_ptr(workspace), nbytes, _stream(stream)))
+
+
+def kivi_decode_workspace(nbytes: int, device):
+    """A decode workspace of nbytes (at least 16), ready for its first call."""
+    import torch
+    ws = torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+    kivi_decode_workspace_init(ws)
+    return ws
+
+
 def kivi_decode_attend(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res, v_res, n_res: int,
                        Hkv: int, sm_scale: float, out=None, workspace=None, stream=None):
     """Single-token decode: q [B, Hq, D] fp16 -> out [B, Hq, D] fp32."""
@@ -251,7 +270,7 @@ def kivi_decode_attend(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res,
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     need = kivi_decode_workspace_size(B, Hq, Hkv, S_q, n_res, D)
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = kivi_decode_workspace(need, q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     res_cap = 0
     if k_res is not None:
@@ -272,7 +291,7 @@ _noalloc_fn = None
 def kivi_decode_attend_noalloc(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res, v_res, n_res: int,
                                Hkv: int, sm_scale: float, out=None, stream=None):
     """The decode of kivi_decode_attend without a workspace argument: the split
-    scratch lives in a library-owned 2 MiB device array (for callers that may
+    scratch lives in a library-owned 4 MiB device array (for callers that may
     not allocate device memory when they decode). Calls that overlap on the GPU
     race on that array; make the first call on a device before any stream
     capture."""

@@ -1,0 +1,154 @@
+// decode_merge.cuh -- the split merge shared by the decode kernels.
+//
+// The cached tokens of one (batch, KV head) are split over n_split CTAs
+// (VeloxQuant-MLX benchmarks page, "KV-Cache Kernel Roofline": one CTA per
+// head leaves the GPU idle). Each CTA leaves a partial (o, m, l) in the
+// workspace and takes a ticket from the head's counter. The CTA with the last
+// ticket sets the counter back to zero, so the workspace is ready for the
+// next call, and merges the partials:
+//     M = max_s m_s,  out = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
+// The merge runs inside the decode launch, so no second kernel is needed.
+#pragma once
+
+#include <math.h>
+
+#include "kivi_device.cuh"
+#include "kivi_launch.h"
+
+namespace kivi {
+
+// Called by all threads of the CTA after its partials are written. Returns
+// true in the CTA that must merge; *flag is a shared-memory int.
+__device__ __forceinline__ bool take_last_ticket(const DecodeArgs& a, int bh, int* flag) {
+    __syncthreads();  // every thread's partial stores precede thread 0's fence
+    if (threadIdx.x == 0) {
+        __threadfence();  // cumulative: the CTA's partials are visible before the ticket
+        const unsigned ticket = atomicAdd(a.counters + bh, 1u);
+        const bool last = ticket == (unsigned)(a.n_split - 1);
+        if (last) atomicExch(a.counters + bh, 0u);  // ready for the next call
+        *flag = last;
+    }
+    __syncthreads();
+    const bool last = *flag != 0;
+    if (last) __threadfence();  // every other CTA's partials are visible
+    return last;
+}
+
+// Log-sum-exp sum of the partials lo .. hi-1 of one query head: *M = their
+// largest running max, *L = sum_s l_s 2^(m_s - M), and the returned float4 =
+// sum_s o_s 2^(m_s - M) for this lane's 4 channels (M = -inf, L = 0, 0 for an
+// empty range). Partials are read through L2 (ld.global.cg): other CTAs of
+// this launch wrote them. The first CHUNK partial rows are requested together
+// with the (m, l) pairs, so up to CHUNK splits cost one L2 round trip.
+template <int CHUNK>
+__device__ __forceinline__ float4 merge_range(const float2* ml, const float4* po, int lo, int hi, int lane,
+                                              float* M_out, float* L_out) {
+    static_assert(CHUNK == 8 || CHUNK == 16, "chunk of partial rows");
+    const int n = hi - lo;
+    ml += lo;
+    po += (long long)lo * (kD / 4);
+    float4 v[CHUNK];
+#pragma unroll
+    for (int k = 0; k < CHUNK; ++k)
+        v[k] = k < n ? __ldcg(po + (long long)k * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float2 x0 = lane < n ? __ldcg(&ml[lane]) : make_float2(-INFINITY, 0.f);
+    float M = x0.x;
+    for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, __ldcg(&ml[s]).x);
+    M = warp_max(M);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < n; s0 += 32) {
+        float2 x = x0;
+        if (s0 > 0) x = s0 + lane < n ? __ldcg(&ml[s0 + lane]) : make_float2(-INFINITY, 0.f);
+        const float wt = x.x == -INFINITY ? 0.f : exp2f(x.x - M);
+        L = fmaf(x.y, wt, L);
+        for (int k0 = 0; k0 < 32 && s0 + k0 < n; k0 += CHUNK) {
+            if (s0 + k0 > 0) {
+#pragma unroll
+                for (int k = 0; k < CHUNK; ++k)
+                    v[k] = s0 + k0 + k < n ? __ldcg(po + (long long)(s0 + k0 + k) * (kD / 4))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < CHUNK; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, wt, k0 + k);  // 0 past the last split
+                acc.x = fmaf(v[k].x, wk, acc.x);
+                acc.y = fmaf(v[k].y, wk, acc.y);
+                acc.z = fmaf(v[k].z, wk, acc.z);
+                acc.w = fmaf(v[k].w, wk, acc.w);
+            }
+        }
+    }
+    *M_out = M;
+    *L_out = warp_sum(L);
+    return acc;
+}
+
+constexpr int kScratchRow = kD + 4;  // o[kD], m, l; a multiple of 4 floats keeps float4 rows aligned
+
+// Merge of the partials of query heads bq0 .. bq0 + nheads - 1 (nheads <= 4)
+// by a CTA of nwarps (4 or 8) warps: warp w takes head w % 4 and the w / 4-th
+// of the splits, so 8 warps halve the L2 round trips; the halves meet in
+// `scratch` (16-byte aligned shared memory, 2 * 4 * kScratchRow floats).
+// Every thread of the CTA must call it (it holds a CTA barrier when nwarps == 8).
+
+template <int CHUNK>
+__device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0, int nheads, int warp,
+                                             int nwarps, int lane, float* scratch) {
+    const int n = a.n_split;
+    const int h = warp & 3, sub = warp >> 2, nsub = nwarps >> 2;
+    const int per = (n + nsub - 1) / nsub;
+    const int lo = min(n, sub * per), hi = min(n, lo + per);
+    const long long bq = bq0 + h;
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (h < nheads)
+        acc = merge_range<CHUNK>(reinterpret_cast<const float2*>(a.part_ml) + bq * n,
+                                 reinterpret_cast<const float4*>(a.part_o + bq * n * kD) + lane, lo, hi, lane, &M,
+                                 &L);
+    if (nsub > 1) {
+        float* mine = scratch + (sub * 4 + h) * kScratchRow;
+        if (sub > 0 && h < nheads) {
+            reinterpret_cast<float4*>(mine)[lane] = acc;
+            if (lane == 0) {
+                mine[kD] = M;
+                mine[kD + 1] = L;
+            }
+        }
+        __syncthreads();
+        if (sub > 0 || h >= nheads) return;
+        for (int t = 1; t < nsub; ++t) {
+            const float* other = scratch + (t * 4 + h) * kScratchRow;
+            const float Mo = other[kD];
+            if (Mo == -INFINITY) continue;  // an empty share of the splits
+            const float Mn = fmaxf(M, Mo);
+            const float fa = M == -INFINITY ? 0.f : exp2f(M - Mn), fb = exp2f(Mo - Mn);
+            const float4 ob = reinterpret_cast<const float4*>(other)[lane];
+            acc = make_float4(fmaf(acc.x, fa, ob.x * fb), fmaf(acc.y, fa, ob.y * fb), fmaf(acc.z, fa, ob.z * fb),
+                              fmaf(acc.w, fa, ob.w * fb));
+            L = fmaf(L, fa, other[kD + 1] * fb);
+            M = Mn;
+        }
+    }
+    if (h < nheads)
+        reinterpret_cast<float4*>(a.out + bq * kD)[lane] = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+}
+
+// The same merge for the channel-split kernel: 4 warps, query heads warp,
+// warp + 4 (up to 8 heads), no barrier.
+template <int CHUNK>
+__device__ __forceinline__ void merge_splits_by_head(const DecodeArgs& a, long long bq0, int nheads, int warp,
+                                                     int lane) {
+    for (int h = warp; h < nheads; h += 4) {
+        const long long bq = bq0 + h;
+        float M, L;
+        const float4 acc = merge_range<CHUNK>(reinterpret_cast<const float2*>(a.part_ml) + bq * a.n_split,
+                                              reinterpret_cast<const float4*>(a.part_o + bq * a.n_split * kD) +
+                                                  lane,
+                                              0, a.n_split, lane, &M, &L);
+        reinterpret_cast<float4*>(a.out + bq * kD)[lane] =
+            make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+    }
+}
+
+}  // namespace kivi

@@ -27,19 +27,24 @@
 //   * a per-tile power-of-two factor keeps every hi below 2^14 (no fp16
 //     overflow for any finite input); it is divided out exactly afterwards.
 //
-// Work split: grid (n_split, Hkv, B), 4 warps per CTA; each warp owns a
-// contiguous run of 32-token tiles of its split and keeps its own online
-// softmax; the warps merge in shared memory, the CTA writes one partial (or
-// the output when n_split == 1). Tiles are staged per warp with cp.async,
-// double buffered: packed K/V codes, key scale/zero of the group, value
-// scale/zero of the 32 rows (5.5 KB at 4-bit); residual tiles stage 32 fp16
-// K and V rows (zero-filled past n_res).
+// Work split: grid (n_split, Hkv, B), 4 or 8 warps per CTA; each warp owns a
+// contiguous run of tiles of its split (32-token store tiles, then 16-token
+// residual tiles) and keeps its own online softmax; the warps merge in shared
+// memory and the CTA writes one partial (or the output when n_split == 1; the
+// last CTA of a (batch, KV head) merges the partials, see decode_merge.cuh).
+// Tiles are staged per warp with cp.async, double buffered: packed K/V codes,
+// key scale/zero of the group, value scale/zero of the 32 rows (5.6 KB at
+// 4-bit); residual tiles stage 16 fp16 K and V rows (zero-filled past n_res).
+// 128 registers; 50 KB (4 warps) or 97 KB (8 warps) of shared memory per
+// CTA: 16 warps per SM either way. 8-warp CTAs halve the partials a merge
+// reads; the plan takes them when 4-warp CTAs would leave more than 16 splits.
 // MMA layouts (m16n8k16, row.col): lane = 4 g + c; A regs hold (row g,
 // k 2c..2c+1), (row g+8, same k), (row g, k 2c+8..9), (row g+8, k 2c+8..9);
 // B regs (k 2c..2c+1, n g), (k 2c+8..9, n g); C regs (row g, n 2c..2c+1),
 // (row g+8, n 2c..2c+1).
 #include <math.h>
 
+#include "decode_merge.cuh"
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
@@ -47,17 +52,23 @@ namespace kivi {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kStage = 8192;                       // bytes per stage
+constexpr int kStage = 5760;                       // bytes per stage (a 4-bit store tile: 5696)
 constexpr int kWarpSmem = 2 * kStage;              // two stages per warp
-constexpr int kPbufOff = kWarps * kWarpSmem;       // per-warp p buffers [32][4] f32
 constexpr int kQRow = kD + 16;                      // padded row: channel ch at ch + (ch >> 5) * 4
-constexpr int kQOff = kPbufOff + kWarps * 512;     // q * score_scale [4][kQRow] f32
-constexpr int kMiscOff = kQOff + 4 * kQRow * 4;    // qmax, merge m/l
-constexpr int kSmemBytes = kMiscOff + 256;
+
+// Shared memory of a CTA of NW warps: each warp's two stages, per-warp p
+// buffers [32][4] f32, q * score_scale [4][kQRow] f32, then misc: qmax per
+// warp [8], the warps' (m, l) [NW][4][2] at 16, the merge flag at 96.
+template <int NW>
+struct Layout {
+    static constexpr int kPbufOff = NW * kWarpSmem;
+    static constexpr int kQOff = kPbufOff + NW * 512;
+    static constexpr int kMiscOff = kQOff + 4 * kQRow * 4;
+    static constexpr int kSmemBytes = kMiscOff + 512;
+};
 // store-tile layout inside a stage (KS padded like q: channel ch at ch + (ch >> 5) * 4)
 constexpr int kKC = 0, kVC = 2048, kKS = 4096, kKZ = 4672, kVS = 4928, kVZ = 5440;
+constexpr int kResTok = kResTileTokensMma;  // residual tile: 16 K rows in stage 0, 16 V rows in stage 1
 
 __device__ __forceinline__ int padc(int ch) { return ch + ((ch >> 5) << 2); }
 
@@ -153,15 +164,15 @@ __device__ __forceinline__ void fetch_store_tile(const DecodeArgs& a, int bh, in
     if (lane < 16) cp_async16(st + kVZ + lane * 16, vz + lane * 8, true);
 }
 
-// 32 fp16 rows of K into st0 and of V into st1, 16-byte chunk c of row r at
-// position c ^ (r & 7); rows past nvalid are zero-filled (nothing is read).
+// kResTok fp16 rows of K into st0 and of V into st1, 16-byte chunk c of row r
+// at position c ^ (r & 7); rows past nvalid are zero-filled (nothing is read).
 __device__ __forceinline__ void fetch_res_tile(const DecodeArgs& a, int bh, int rtile, int nvalid, uint8_t* st0,
                                                uint8_t* st1, int lane) {
-    const int tok0 = rtile * 32;
+    const int tok0 = rtile * kResTok;
     const __half* kr = a.k_res + ((long long)bh * a.res_cap + tok0) * kD;
     const __half* vr = a.v_res + ((long long)bh * a.res_cap + tok0) * kD;
 #pragma unroll 4
-    for (int i = lane; i < 32 * 16; i += 32) {
+    for (int i = lane; i < kResTok * 16; i += 32) {
         const int row = i >> 4, col = i & 15;
         const bool ok = row < nvalid;
         const int off = row * 256 + ((col ^ (row & 7)) << 4);
@@ -174,17 +185,21 @@ __device__ __forceinline__ void fetch_res_tile(const DecodeArgs& a, int bh, int 
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int BITS, int GQ>
-__global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
+// NW warps per CTA (4 or 8): 16 warps per SM either way, at 128 registers.
+template <int BITS, int GQ, int NW>
+__global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs a) {
+    constexpr int kWarps = NW;
+    constexpr int kThreads = 32 * NW;
+    using LY = Layout<NW>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c = lane & 3;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int bh = b * a.Hkv + hk, h0 = hk * GQ;
     uint8_t* st[2] = {smem + warp * kWarpSmem, smem + warp * kWarpSmem + kStage};
-    float* pbuf = reinterpret_cast<float*>(smem + kPbufOff + warp * 512);  // [token][head]
-    float* q_s = reinterpret_cast<float*>(smem + kQOff);                   // [head][channel]
-    float* misc = reinterpret_cast<float*>(smem + kMiscOff);
+    float* pbuf = reinterpret_cast<float*>(smem + LY::kPbufOff + warp * 512);  // [token][head]
+    float* q_s = reinterpret_cast<float*>(smem + LY::kQOff);                   // [head][channel]
+    float* misc = reinterpret_cast<float*>(smem + LY::kMiscOff);
 
     // this warp's tiles
     const int tile_begin = split * a.tiles_per_split;
@@ -214,24 +229,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
     qm = warp_max(qm);
     if (lane == 0) misc[warp] = qm;
     __syncthreads();
-    const float qmax = fmaxf(fmaxf(misc[0], misc[1]), fmaxf(misc[2], misc[3]));
+    float qmax = misc[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) qmax = fmaxf(qmax, misc[w]);
 
     const int hh = g >> 1;          // head of this lane's B column n = g
     const bool lo_part = g & 1;     // hi (0) or lo (1) part of that column
     const float* qrow = q_s + hh * kQRow;
 
-    // q (this lane's head, hi or lo) in natural channel order, scaled by 2^Er:
-    // the B operand of the residual-tile QK and of sum_d q_d z_d on store tiles
+    // residual tiles take q 2^Er (hi or lo) in natural channel order as their B operand
     const int Er = safe_exp(qmax);
     const float fBr = pow2i(Er), fCr = pow2i(-Er);
-    uint32_t br[8][2];  // K-step s: channels 16s + 2c.., 16s + 8 + 2c..
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-        const float2 qa = *reinterpret_cast<const float2*>(qrow + padc(16 * s + 2 * c));
-        const float2 qb = *reinterpret_cast<const float2*>(qrow + padc(16 * s + 8 + 2 * c));
-        br[s][0] = split_pair(qa.x * fBr, qa.y * fBr, lo_part);
-        br[s][1] = split_pair(qb.x * fBr, qb.y * fBr, lo_part);
-    }
 
     float m_run = -INFINITY, l_run = 0.f;  // online softmax of head c
     float o[8][4];                         // P.V of head c, store-tile channel layout
@@ -312,17 +320,29 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
                 }
             }
         }
-        // ---- sum_d q_d z_d of head c on the tensor cores: A = key zeros in every row ----
+        // ---- sum_d q_d z_d of head c: this lane sums 16 channels of head hh ----
         float qz_c;
         {
-            float zacc[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint32_t* kz32 = reinterpret_cast<const uint32_t*>(KZ);
+            const int cb = 16 * (4 * (g & 1) + c);
+            const uint4 za = *reinterpret_cast<const uint4*>(KZ + cb);
+            const uint4 zb = *reinterpret_cast<const uint4*>(KZ + cb + 8);
+            const uint32_t zw[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
+            const float* qz = qrow + padc(cb);  // 16 contiguous floats
+            float t = 0.f;
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t za = kz32[8 * s + c], zb = kz32[8 * s + 4 + c];  // channels 16s+2c.., 16s+8+2c..
-                mma16816(zacc, za, za, zb, zb, br[s][0], br[s][1]);
+            for (int k = 0; k < 4; ++k) {
+                const float4 q4 = *reinterpret_cast<const float4*>(qz + 4 * k);
+                const float2 z01 = __half22float2(u32_as_h2(zw[2 * k]));
+                const float2 z23 = __half22float2(u32_as_h2(zw[2 * k + 1]));
+                t = fmaf(q4.x, z01.x, t);
+                t = fmaf(q4.y, z01.y, t);
+                t = fmaf(q4.z, z23.x, t);
+                t = fmaf(q4.w, z23.y, t);
             }
-            qz_c = (zacc[0] + zacc[1]) * fCr;
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            t += __shfl_xor_sync(0xffffffffu, t, 4);
+            qz_c = __shfl_sync(0xffffffffu, t, 8 * c);  // lane 8c has g = 2c: head c
         }
 
         // ---- scores: 2 M-tiles of 16 tokens ----
@@ -517,91 +537,115 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
     __syncwarp();
 
     // ---------------------------- residual tiles ----------------------------
-    float orr[8][4];  // P.V of head c from residual tiles, rows g / g+8 -> channel 16 mb + g / + 8
+    // kResTok fp16 K and V rows per tile. Their P.V is accumulated in fp32 per
+    // 16-channel block and added into o (store-tile channel layout, units of 2^-9).
+    for (int rt = r_begin; rt < w1; ++rt) {
+        const int rtile = rt - a.n_store_tiles;
+        const int nvalid = min(kResTok, a.n_res - rtile * kResTok);
+        fetch_res_tile(a, bh, rtile, nvalid, st[0], st[1], lane);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncwarp();
+        const uint8_t* KR = st[0];
+        const uint8_t* VR = st[1];
+        float sc[4];
+        {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const int q = lane >> 3, r = lane & 7;
+            const int row = (q & 1) * 8 + r;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) orr[i][0] = orr[i][1] = orr[i][2] = orr[i][3] = 0.f;
-    if (r_begin < w1) {
-        for (int rt = r_begin; rt < w1; ++rt) {
-            const int rtile = rt - a.n_store_tiles;
-            const int nvalid = min(32, a.n_res - rtile * 32);
-            fetch_res_tile(a, bh, rtile, nvalid, st[0], st[1], lane);
-            cp_async_commit();
-            cp_async_wait<0>();
-            __syncwarp();
-            const uint8_t* KR = st[0];
-            const uint8_t* VR = st[1];
-            float sc[4];
+            for (int s = 0; s < 8; ++s) {
+                // B: q 2^Er of this lane's head (hi or lo), channels 16s + {2c, 2c+1 | 2c+8, 2c+9}
+                const float2 qa = *reinterpret_cast<const float2*>(qrow + padc(16 * s + 2 * c));
+                const float2 qb = *reinterpret_cast<const float2*>(qrow + padc(16 * s + 8 + 2 * c));
+                const uint32_t b0 = split_pair(qa.x * fBr, qa.y * fBr, lo_part);
+                const uint32_t b1 = split_pair(qb.x * fBr, qb.y * fBr, lo_part);
+                const int chunk = 2 * s + (q >> 1);
+                uint32_t A[4];
+                ldsm_x4(A, KR + row * 256 + ((chunk ^ (row & 7)) << 4));
+                mma16816(acc, A[0], A[1], A[2], A[3], b0, b1);
+            }
+            sc[0] = g < nvalid ? (acc[0] + acc[1]) * fCr : -INFINITY;
+            sc[1] = g + 8 < nvalid ? (acc[2] + acc[3]) * fCr : -INFINITY;
+            sc[2] = sc[3] = -INFINITY;
+        }
+        float tmax = fmaxf(sc[0], sc[1]);
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        const float m_new = fmaxf(m_run, tmax);
+        const float corr = exp2f(m_run - m_new);
+        const float p0 = exp2f(sc[0] - m_new), p1 = exp2f(sc[1] - m_new);
+        float ps = p0 + p1;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l_run = fmaf(l_run, corr, ps);
+        m_run = m_new;
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const int q = lane >> 3, r = lane & 7;
-                    const int row = mt * 16 + (q & 1) * 8 + r, chunk = 2 * s + (q >> 1);
-                    uint32_t A[4];
-                    ldsm_x4(A, KR + row * 256 + ((chunk ^ (row & 7)) << 4));
-                    mma16816(acc, A[0], A[1], A[2], A[3], br[s][0], br[s][1]);
+            for (int k = 0; k < 4; ++k) o[i][k] *= corr;
+        pbuf[g * 4 + c] = p0;
+        pbuf[(g + 8) * 4 + c] = p1;
+        __syncwarp();
+        // B: p of head hh (hi or lo), tokens {2c, 2c+1 | 2c+8, 2c+9}
+        const uint32_t bp0 = split_pair(pbuf[(2 * c) * 4 + hh], pbuf[(2 * c + 1) * 4 + hh], lo_part);
+        const uint32_t bp1 = split_pair(pbuf[(2 * c + 8) * 4 + hh], pbuf[(2 * c + 9) * 4 + hh], lo_part);
+        if (BITS == 4) {
+            // o[2j + u]: rows g -> channel 32j + 4g + u, g+8 -> 32j + 4g + 2 + u
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint2 rv[4];  // tokens 2c, 2c+1, 2c+8, 2c+9: channels 32j + 4g .. 32j + 4g + 3
+#pragma unroll
+                for (int ti = 0; ti < 4; ++ti) {
+                    const int t = 2 * c + (ti & 1) + 8 * (ti >> 1);
+                    rv[ti] = *reinterpret_cast<const uint2*>(VR + t * 256 + (((4 * j + (g >> 1)) ^ (t & 7)) << 4) +
+                                                             (g & 1) * 8);
                 }
-                const int t0 = mt * 16 + g;
-                sc[2 * mt] = t0 < nvalid ? (acc[0] + acc[1]) * fCr : -INFINITY;
-                sc[2 * mt + 1] = t0 + 8 < nvalid ? (acc[2] + acc[3]) * fCr : -INFINITY;
-            }
-            float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-            const float m_new = fmaxf(m_run, tmax);
-            const float corr = exp2f(m_run - m_new);
-            float p[4], ps = 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                p[i] = exp2f(sc[i] - m_new);
-                ps += p[i];
-            }
-            ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-            l_run = fmaf(l_run, corr, ps);
-            m_run = m_new;
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t sel = u ? 0x7632u : 0x5410u;  // half u of each word
+                    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma16816(tmp, __byte_perm(rv[0].x, rv[1].x, sel), __byte_perm(rv[0].y, rv[1].y, sel),
+                             __byte_perm(rv[2].x, rv[3].x, sel), __byte_perm(rv[2].y, rv[3].y, sel), bp0, bp1);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+                    for (int k = 0; k < 4; ++k) o[2 * j + u][k] = fmaf(tmp[k], 1.0f / 512.f, o[2 * j + u][k]);
+                }
+            }
+        } else {
+            // o[4hc + k]: rows g -> channel 64hc + 8g + k, g+8 -> 64hc + 8g + 4 + k
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                uint32_t rv[4][4];  // tokens 2c, 2c+1, 2c+8, 2c+9: channels 64hc + 8g .. + 7
+#pragma unroll
+                for (int ti = 0; ti < 4; ++ti) {
+                    const int t = 2 * c + (ti & 1) + 8 * (ti >> 1);
+                    const uint4 v4 = *reinterpret_cast<const uint4*>(VR + t * 256 + (((8 * hc + g) ^ (t & 7)) << 4));
+                    rv[ti][0] = v4.x;
+                    rv[ti][1] = v4.y;
+                    rv[ti][2] = v4.z;
+                    rv[ti][3] = v4.w;
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    o[i][k] *= corr;
-                    orr[i][k] *= corr;
+                    const uint32_t sel = (k & 1) ? 0x7632u : 0x5410u;
+                    const int wa = k >> 1, wb = 2 + (k >> 1);  // words of channels k and 4 + k
+                    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma16816(tmp, __byte_perm(rv[0][wa], rv[1][wa], sel), __byte_perm(rv[0][wb], rv[1][wb], sel),
+                             __byte_perm(rv[2][wa], rv[3][wa], sel), __byte_perm(rv[2][wb], rv[3][wb], sel), bp0, bp1);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[4 * hc + k][e] = fmaf(tmp[e], 1.0f / 512.f, o[4 * hc + k][e]);
                 }
             }
-            pbuf[(g) * 4 + c] = p[0];
-            pbuf[(g + 8) * 4 + c] = p[1];
-            pbuf[(g + 16) * 4 + c] = p[2];
-            pbuf[(g + 24) * 4 + c] = p[3];
-            __syncwarp();
-            uint32_t bpr[2][2];
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int ta = 16 * ks + 2 * c, tb = ta + 8;
-                bpr[ks][0] = split_pair(pbuf[ta * 4 + hh], pbuf[(ta + 1) * 4 + hh], lo_part);
-                bpr[ks][1] = split_pair(pbuf[tb * 4 + hh], pbuf[(tb + 1) * 4 + hh], lo_part);
-            }
-#pragma unroll
-            for (int mb = 0; mb < 8; ++mb) {
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    const int q = lane >> 3, r = lane & 7;
-                    const int row = 16 * ks + (q >> 1) * 8 + r, chunk = 2 * mb + (q & 1);
-                    uint32_t A[4];
-                    ldsm_x4_t(A, VR + row * 256 + ((chunk ^ (row & 7)) << 4));
-                    mma16816(orr[mb], A[0], A[1], A[2], A[3], bpr[ks][0], bpr[ks][1]);
-                }
-            }
-            __syncwarp();
         }
+        __syncwarp();
     }
 
-    // ---------------------------- merge the 4 warps ----------------------------
+    // ---------------------------- merge the warps ----------------------------
     __syncthreads();  // every warp is done with its stages
     float* Ow = reinterpret_cast<float*>(st[0]);          // [4 heads][128] of this warp
-    float* ml = misc + 8;                                  // [warp][head][2]
+    float* ml = misc + 16;                                 // [warp][head][2]
     {
         const float sc9 = 512.f;  // o holds sum p s c 2^-9 + pz 2^-9
         if (BITS == 4) {
@@ -621,12 +665,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
                     Ow[c * kD + 64 * hc + 8 * g + 4 + k] = (o[4 * hc + k][2] + o[4 * hc + k][3]) * sc9;
                 }
         }
-        __syncwarp();
-#pragma unroll
-        for (int mb = 0; mb < 8; ++mb) {
-            Ow[c * kD + 16 * mb + g] += orr[mb][0] + orr[mb][1];
-            Ow[c * kD + 16 * mb + 8 + g] += orr[mb][2] + orr[mb][3];
-        }
         if (g == 0) {
             ml[(warp * 4 + c) * 2 + 0] = m_run;
             ml[(warp * 4 + c) * 2 + 1] = l_run;
@@ -634,9 +672,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
     }
     pdl_trigger();
     __syncthreads();
-    const int d = tid;
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) {
+    const int d = tid & (kD - 1);
+    for (int h = tid / kD; h < GQ; h += kThreads / kD) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 4 + h) * 2]);
@@ -660,33 +697,44 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
             }
         }
     }
+    if (a.n_split == 1) return;
+    if (take_last_ticket(a, bh, reinterpret_cast<int*>(misc + 96)))
+        merge_splits<16>(a, (long long)b * a.Hq + h0, GQ, warp, kWarps, lane, reinterpret_cast<float*>(smem));
 }
 
-template <int BITS, int GQ>
+template <int BITS, int GQ, int NW>
 cudaError_t launch_mma_typed(const DecodeArgs& a, cudaStream_t stream) {
     static bool configured = false;  // benign race: every caller sets the same value
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ, NW>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<NW>::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    return launch_pdl(decode_mma_kernel<BITS, GQ>, dim3(a.n_split, a.Hkv, a.B), kThreads, kSmemBytes, stream, a);
+    return launch_pdl(decode_mma_kernel<BITS, GQ, NW>, dim3(a.n_split, a.Hkv, a.B), 32 * NW, Layout<NW>::kSmemBytes,
+                      stream, a);
+}
+
+template <int BITS, int GQ>
+cudaError_t launch_mma_warps(const DecodeArgs& a, cudaStream_t stream) {
+    return a.warps_per_cta == 8 ? launch_mma_typed<BITS, GQ, 8>(a, stream) : launch_mma_typed<BITS, GQ, 4>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, int bits, int gq, cudaStream_t stream) {
+    cudaError_t e = cudaErrorInvalidValue;
     if (bits == 4) {
-        if (gq == 1) return launch_mma_typed<4, 1>(a, stream);
-        if (gq == 2) return launch_mma_typed<4, 2>(a, stream);
-        if (gq == 4) return launch_mma_typed<4, 4>(a, stream);
+        if (gq == 1) e = launch_mma_warps<4, 1>(a, stream);
+        if (gq == 2) e = launch_mma_warps<4, 2>(a, stream);
+        if (gq == 4) e = launch_mma_warps<4, 4>(a, stream);
     } else {
-        if (gq == 1) return launch_mma_typed<2, 1>(a, stream);
-        if (gq == 2) return launch_mma_typed<2, 2>(a, stream);
-        if (gq == 4) return launch_mma_typed<2, 4>(a, stream);
+        if (gq == 1) e = launch_mma_warps<2, 1>(a, stream);
+        if (gq == 2) e = launch_mma_warps<2, 2>(a, stream);
+        if (gq == 4) e = launch_mma_warps<2, 4>(a, stream);
     }
-    return cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 }  // namespace kivi

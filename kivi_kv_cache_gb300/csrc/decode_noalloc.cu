@@ -15,8 +15,10 @@
 //   * calls whose kernels overlap on that device (e.g. issued on two streams
 //     without ordering) race on the scratch and give wrong results -- order them
 //     on one stream or with events;
-//   * nothing in the scratch needs to start at zero: each call writes every
-//     partial it later reads, and keeps the last call's contents afterwards.
+//   * the merge counters at its start must be zero when a call begins: a
+//     __device__ array is zero-initialised when the module loads, and every
+//     completed call leaves the counters zero; each call writes every partial
+//     it later reads, and the array keeps the last call's contents afterwards.
 // Host code cannot use the array's name as a device address, so the first call
 // on each device looks the address up with cudaGetSymbolAddress (with that
 // device current) and caches it; that first call may load the library's

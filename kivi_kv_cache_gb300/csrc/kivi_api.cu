@@ -43,39 +43,72 @@ kivi_status shape_check(int D, int G, int bits) {
 
 kivi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ERR_CUDA; }
 
-// Split plan for the decode. The tensor-core kernel (<= 4 query heads per KV
-// head) gives each of its 4 warps a run of tiles_per_warp 32-token tiles,
-// sized for about 12 warps (3 CTAs) per SM over the whole batch; the fp32 kernel (8
-// query heads per KV head) targets two CTAs per SM. Whole tiles per split,
-// no empty split.
+// Split plan for the decode. Groups of 1, 2 or 4 query heads per KV head run
+// the one-warp-per-tile kernel: each warp of a CTA takes a run of
+// tiles_per_warp tiles (32-token store tiles, then 16-token residual tiles),
+// sized for about kMmaWarpsPerSm warps per SM over the whole batch. CTAs have
+// 4 warps, or 8 when 4-warp CTAs would leave a (batch, KV head) more than
+// kMmaMaxSplits4 partials to merge. Other groups run the channel-split kernel:
+// a CTA takes a run of tiles (16-token residual tiles) sized for about
+// kSplitCtasPerSm CTAs per SM in one wave, never shorter than kSplitMinTiles
+// tiles. When the batch has more (batch, KV head) pairs than the workspace has
+// merge counters, each pair gets one split.
+#ifndef KIVI_DECODE_MMA_WARPS_PER_SM
+#define KIVI_DECODE_MMA_WARPS_PER_SM 24
+#endif
+#ifndef KIVI_DECODE_MMA_MAX_SPLITS4
+#define KIVI_DECODE_MMA_MAX_SPLITS4 16
+#endif
+#ifndef KIVI_DECODE_CTAS_PER_SM
+#define KIVI_DECODE_CTAS_PER_SM 4
+#endif
+#ifndef KIVI_DECODE_MIN_TILES
+#define KIVI_DECODE_MIN_TILES 3
+#endif
+constexpr int kMmaWarpsPerSm = KIVI_DECODE_MMA_WARPS_PER_SM;
+constexpr int kMmaMaxSplits4 = KIVI_DECODE_MMA_MAX_SPLITS4;
+constexpr int kSplitCtasPerSm = KIVI_DECODE_CTAS_PER_SM;
+constexpr int kSplitMinTiles = KIVI_DECODE_MIN_TILES;
+
+bool mma_group(int gq) { return gq == 1 || gq == 2 || gq == 4; }
+
 DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res) {
     DecodePlan p;
+    const bool mma = Hkv > 0 && Hq % Hkv == 0 && mma_group(Hq / Hkv);
+    const int rt = mma ? kResTileTokensMma : kResTileTokensSplit;
     p.n_store_tiles = (S_q + kG - 1) / kG;
-    p.n_tiles = p.n_store_tiles + (n_res + kG - 1) / kG;
+    p.n_tiles = p.n_store_tiles + (n_res + rt - 1) / rt;
     const long long heads = (long long)B * Hkv;
-    if (Hkv > 0 && Hq / Hkv <= 4) {
-        const long long target = 12LL * sm_count();
+    if (mma) {
+        const long long target = (long long)kMmaWarpsPerSm * sm_count();
         long long tpw = (heads * p.n_tiles + target - 1) / target;
         if (tpw < 1) tpw = 1;
+        p.warps_per_cta = (p.n_tiles + 4 * tpw - 1) / (4 * tpw) > kMmaMaxSplits4 ? 8 : 4;
+        if (heads > kMergeCounters) tpw = (p.n_tiles + p.warps_per_cta - 1) / p.warps_per_cta;  // one split per pair
         p.tiles_per_warp = (int)tpw;
-        p.tiles_per_split = 4 * p.tiles_per_warp;
+        p.tiles_per_split = (int)(p.warps_per_cta * tpw);
     } else {
-        const long long target = 2LL * sm_count();
-        long long per_head = (target + heads - 1) / heads;
-        if (per_head < 1) per_head = 1;
-        if (per_head > p.n_tiles) per_head = p.n_tiles;
-        p.tiles_per_split = (int)((p.n_tiles + per_head - 1) / per_head);
-        p.tiles_per_warp = p.tiles_per_split;
+        const long long slots = (long long)kSplitCtasPerSm * sm_count();
+        long long per = (heads * p.n_tiles + slots - 1) / slots;
+        if (per < kSplitMinTiles) per = kSplitMinTiles;
+        if (heads > kMergeCounters || per > p.n_tiles) per = p.n_tiles;
+        p.tiles_per_split = (int)per;
+        p.tiles_per_warp = (int)per;
+        p.warps_per_cta = 4;
     }
     p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
     return p;
 }
 
+// Workspace: [merge counters, KIVI_DECODE_COUNTER_BYTES][part_o, 256-aligned][part_ml]
+size_t part_o_bytes(int B, int Hq, const DecodePlan& p) {
+    return (((size_t)B * Hq * p.n_split * kD * sizeof(float)) + 255) & ~(size_t)255;
+}
+
 size_t workspace_bytes(int B, int Hq, const DecodePlan& p) {
     if (p.n_split <= 1) return 0;
-    const size_t o = (size_t)B * Hq * p.n_split * kD * sizeof(float);
     const size_t ml = (size_t)B * Hq * p.n_split * 2 * sizeof(float);
-    return ((o + 255) & ~(size_t)255) + ml;
+    return (size_t)KIVI_DECODE_COUNTER_BYTES + part_o_bytes(B, Hq, p) + ml;
 }
 
 kivi_status flush_check(const void* x, int BH, int S, int x_bh_stride, int D, int G, int bits,
@@ -311,7 +344,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
         (S_q > 0 && s_cap % group_size != 0) || !std::isfinite(sm_scale))
         return KIVI_ERR_INVALID_ARG;
     const int gq = Hq / Hkv;
-    if (gq != 1 && gq != 2 && gq != 4 && gq != 8) return KIVI_ERR_UNSUPPORTED;
+    if (gq > 8) return KIVI_ERR_UNSUPPORTED;
     if (!q_f16 || !out_f32) return KIVI_ERR_INVALID_ARG;
     if (S_q > 0 && (!kcodes_u8 || !kscale || !kzero_f16 || !vcodes_u8 || !vscale || !vzero_f16))
         return KIVI_ERR_INVALID_ARG;
@@ -346,22 +379,26 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
     a.n_split = p.n_split;
     a.tiles_per_split = p.tiles_per_split;
     a.tiles_per_warp = p.tiles_per_warp;
+    a.warps_per_cta = p.warps_per_cta;
     a.n_store_tiles = p.n_store_tiles;
     a.n_tiles = p.n_tiles;
-    float* ws = static_cast<float*>(workspace);
-    a.part_o = ws;
-    a.part_ml = need > 0 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                    (((size_t)B * Hq * p.n_split * kD * sizeof(float) + 255) &
-                                                     ~(size_t)255))
+    char* ws = static_cast<char*>(workspace);
+    a.counters = need > 0 ? reinterpret_cast<unsigned int*>(ws) : nullptr;
+    a.part_o = need > 0 ? reinterpret_cast<float*>(ws + KIVI_DECODE_COUNTER_BYTES) : nullptr;
+    a.part_ml = need > 0 ? reinterpret_cast<float*>(ws + KIVI_DECODE_COUNTER_BYTES + part_o_bytes(B, Hq, p))
                          : nullptr;
     a.out = out_f32;
     const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
-    if (gq <= 4) {
-        cudaError_t e = launch_decode_mma(a, bits, gq, strm);
-        if (e == cudaSuccess) e = launch_decode_combine(a, strm);
-        return from_cuda(e);
-    }
-    return from_cuda(launch_decode(a, bits, gq, strm));
+    return from_cuda(mma_group(gq) ? launch_decode_mma(a, bits, gq, strm)
+                                   : launch_decode_channel_split(a, bits, gq, strm));
+}
+
+kivi_status kivi_decode_workspace_init(void* workspace, size_t workspace_bytes_, kivi_stream_t stream) {
+    if (workspace_bytes_ == 0) return KIVI_OK;
+    if (!workspace) return KIVI_ERR_INVALID_ARG;
+    const size_t n = workspace_bytes_ < (size_t)KIVI_DECODE_COUNTER_BYTES ? workspace_bytes_
+                                                                         : (size_t)KIVI_DECODE_COUNTER_BYTES;
+    return from_cuda(cudaMemsetAsync(workspace, 0, n, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -53,10 +53,12 @@ struct DecodeArgs {
     int Hkv;
     float score_scale;    // sm_scale * log2(e): scores live in the exp2 domain
     int n_split;
-    int tiles_per_split;
-    int tiles_per_warp;   // tensor-core kernel: contiguous tiles per warp (4 warps)
+    int tiles_per_split;  // tiles: 32-token store tiles, then residual tiles
+    int tiles_per_warp;   // one-warp-per-tile kernel: contiguous tiles per warp
+    int warps_per_cta;    // one-warp-per-tile kernel: 4 or 8
     int n_store_tiles;
     int n_tiles;
+    unsigned int* counters;  // [B*Hkv] merge tickets, zero between calls (n_split > 1)
     float* part_o;        // [B, Hq, n_split, D]
     float* part_ml;       // [B, Hq, n_split, 2]  (running max, running sum)
     float* out;           // [B, Hq, D]
@@ -66,9 +68,16 @@ struct DecodePlan {
     int n_split;
     int tiles_per_split;
     int tiles_per_warp;
+    int warps_per_cta;
     int n_store_tiles;
     int n_tiles;
 };
+
+// Tokens per residual tile: the one-warp-per-tile kernel (1, 2 or 4 query
+// heads per KV head) and the channel-split kernel (any group up to 8).
+constexpr int kResTileTokensMma = 16;
+constexpr int kResTileTokensSplit = 16;
+constexpr int kMergeCounters = 8192;    // (batch, KV head) pairs that can take split merges
 
 // Launch with programmatic stream serialization allowed: the kernel may start
 // while the previous kernel on the stream finishes; it must (and every kernel
@@ -99,9 +108,10 @@ cudaError_t launch_residual_append(const __half* src0, const __half* src1, long 
                                    cudaStream_t stream);
 cudaError_t launch_residual_compact(__half* res0, __half* res1, int BH, int res_cap, int n_res, int n_drop,
                                     cudaStream_t stream);
-cudaError_t launch_decode(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
-// tensor-core decode for gq in {1, 2, 4}; the combine pass is shared
+// Fused decodes; each merges its own splits in the same launch.
+// gq in {1, 2, 4}: one warp per tile.
 cudaError_t launch_decode_mma(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
-cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream);
+// any 1 <= gq <= 8: the channels of a tile split over 4 warps.
+cudaError_t launch_decode_channel_split(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 
 }  // namespace kivi

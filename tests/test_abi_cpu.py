@@ -127,7 +127,7 @@ def decode(L, q=FAKE, S_q=2080, s_cap=2080, n_res=158, res_cap=160, B=1, Hq=32, 
 @no_gpu
 def test_decode_rejects_bad_arguments(L):
     assert decode(L, Hq=12) == INVALID               # 12 / 8 is not an integer
-    assert decode(L, Hq=24) == UNSUPPORTED           # 3 query heads per KV head
+    assert decode(L, Hq=72) == UNSUPPORTED           # 9 query heads per KV head
     assert decode(L, Hq=128) == UNSUPPORTED          # 16 query heads per KV head
     assert decode(L, S_q=0, n_res=0) == INVALID
     assert decode(L, S_q=3000) == INVALID            # S_q > s_cap
@@ -141,6 +141,12 @@ def test_decode_rejects_bad_arguments(L):
     assert decode(L, wbytes=need - 1) == WORKSPACE
 
 
+@no_gpu
+def test_workspace_init_rejects_null(L):
+    assert L.kivi_decode_workspace_init(None, 0, None) == OK      # nothing to zero
+    assert L.kivi_decode_workspace_init(None, 1024, None) == INVALID
+
+
 def test_workspace_size(L):
     assert L.kivi_decode_workspace_size(1, 32, 8, 0, 0, 128) == 0
     assert L.kivi_decode_workspace_size(1, 32, 8, 64, 0, 64) == 0
@@ -149,3 +155,7 @@ def test_workspace_size(L):
     assert 0 < small <= big
     # a single 32-token tile needs no split and no workspace
     assert L.kivi_decode_workspace_size(1, 32, 8, 32, 0, 128) == 0
+    # a split plan's workspace starts with the fixed merge-counter block
+    assert small > 32768
+    # more (batch, KV head) pairs than merge counters: one split each, no workspace
+    assert L.kivi_decode_workspace_size(2048, 32, 8, 32640, 128, 128) == 0

@@ -163,7 +163,7 @@ def test_residual_append_and_compact():
 # decode-attend
 # ---------------------------------------------------------------------------
 
-def decode_case(w, S_q, n_res, k, v, q, res_k=None, res_v=None):
+def decode_case(w, S_q, n_res, k, v, q, res_k=None, res_v=None, workspace=None):
     BH = w.BH
     s_cap = max(w.G, -(-S_q // w.G) * w.G)
     gk = kv.KiviStore(0, BH, s_cap, w.D, w.G, w.bits, device=DEV)
@@ -178,7 +178,8 @@ def decode_case(w, S_q, n_res, k, v, q, res_k=None, res_v=None):
     vr = res_v if res_v is not None else v[:, S_q:S_q + n_res]
     kr = np.ascontiguousarray(kr)
     vr = np.ascontiguousarray(vr)
-    out = kv.kivi_decode_attend(dev(q), gk, gv, S_q, dev(kr), dev(vr), n_res, w.Hkv, w.sm_scale)
+    out = kv.kivi_decode_attend(dev(q), gk, gv, S_q, dev(kr), dev(vr), n_res, w.Hkv, w.sm_scale,
+                                workspace=workspace)
     ref = oracle.decode_attend(q, rk, rv, S_q, kr, vr, n_res, w.Hkv, w.sm_scale)
     return host(out).astype(np.float64), ref
 
@@ -222,7 +223,7 @@ def test_decode_batched_workload_sampled():
 @pytest.mark.parametrize("S_q,n_res", [(0, 1), (0, 37), (32, 0), (33, 0), (64, 5), (77, 31),
                                        (1000, 200), (4096, 0), (96, 128)])
 @pytest.mark.parametrize("bits", [2, 4])
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (32, 8), (16, 2)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (24, 8), (32, 8), (12, 2), (16, 2)])
 def test_decode_edge_shapes(S_q, n_res, bits, hq, hkv):
     B = 2
     w = synth.Workload("edge", B=B, Hkv=hkv, Hq=hq, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
@@ -234,6 +235,29 @@ def test_decode_edge_shapes(S_q, n_res, bits, hq, hkv):
     out, ref = decode_case(w, S_q, n_res, k, v, q)
     err = np.max(np.abs(out - ref))
     assert err <= TOL, err
+
+
+def test_decode_one_workspace_across_sizes():
+    """One workspace serves calls of different sizes in turn: after every call
+    the merge counters at its start are zero again, and every call matches the
+    oracle (counters left non-zero would make a later merge fire early or
+    never)."""
+    cases = [(1, 8, 32, 2080, 158, 4), (3, 8, 32, 1000, 40, 2), (2, 4, 32, 4096, 16, 4), (1, 8, 64, 700, 3, 4)]
+    need = max(kv.kivi_decode_workspace_size(B, hq, hkv, S_q, n_res) for B, hkv, hq, S_q, n_res, _ in cases)
+    ws = kv.kivi_decode_workspace(need, DEV)
+    for i, (B, hkv, hq, S_q, n_res, bits) in enumerate(cases + cases[:1]):
+        assert kv.kivi_decode_workspace_size(B, hq, hkv, S_q, n_res) > 0  # all are split plans
+        w = synth.Workload("ws", B=B, Hkv=hkv, Hq=hq, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
+                           n_outlier=4, outlier_scale=8.0, seed=500 + i)
+        rng = np.random.default_rng(w.seed)
+        k = synth.keys(rng, (w.BH, S_q + n_res), 128, synth.outlier_channels(w), 8.0)
+        v = synth.normal(rng, (w.BH, S_q + n_res, 128))
+        q = synth.normal(rng, (B, hq, 128))
+        out, ref = decode_case(w, S_q, n_res, k, v, q, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(torch.count_nonzero(ws[:32768])) == 0, i
+        err = np.max(np.abs(out - ref))
+        assert err <= TOL, (i, err)
 
 
 @pytest.mark.parametrize("S_kv", [128, 512, 2048, 8192, 16384])

@@ -2,7 +2,7 @@
 device memory when they decode (runtimes that pre-assign all of HBM, C callers
 without an allocator of their own). It must give the same result as
 kivi_decode_attend with a caller-provided workspace, call after call, while
-using only the library's fixed 2 MiB device scratch.
+using only the library's fixed 4 MiB device scratch.
 
 This file is named so that pytest collects it last; it needs nothing from the
 other test files and also passes when run alone in a fresh process."""
@@ -16,7 +16,7 @@ from kivi_kv_cache_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-3
-SCRATCH_BYTES = 2 * 1024 * 1024
+SCRATCH_BYTES = 4 * 1024 * 1024
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,17 +55,17 @@ def test_noalloc_matches_workspace_entry_point_twice(name, S_q, n_res):
 
 
 def test_noalloc_rejects_work_beyond_the_scratch():
-    """B*Hkv = 303 and Hq/Hkv = 8 need two splits of 8 query heads each:
-    about 2.5 MB of partials, over the 2 MiB scratch."""
-    w = synth.Workload("big", B=101, Hkv=3, Hq=24, D=128, S=64, bits=4, G=32, R=0, n_outlier=4,
+    """B*Hkv = 512 pairs of 8 query heads over 512 tokens split in two: about
+    4.3 MB of partials and counters, over the 4 MiB scratch."""
+    w = synth.Workload("big", B=64, Hkv=8, Hq=64, D=128, S=512, bits=4, G=32, R=0, n_outlier=4,
                        outlier_scale=8.0, seed=9)
-    need = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, 64, 0, w.D)
+    need = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, 512, 0, w.D)
     if need <= SCRATCH_BYTES:
         pytest.skip("this device's split plan fits the scratch (%d bytes)" % need)
-    q, ks, vs, kr, vr = _decode_inputs(w, 64, 0, seed=3)
+    q, ks, vs, kr, vr = _decode_inputs(w, 512, 0, seed=3)
     out = torch.zeros((w.B, w.Hq, w.D), dtype=torch.float32, device="cuda")
     with pytest.raises(kv.KiviError) as e:
-        kv.kivi_decode_attend_noalloc(q, ks, vs, 64, None, None, 0, w.Hkv, w.sm_scale, out=out)
+        kv.kivi_decode_attend_noalloc(q, ks, vs, 512, None, None, 0, w.Hkv, w.sm_scale, out=out)
     assert e.value.status == 3  # KIVI_ERR_WORKSPACE, nothing launched
     torch.cuda.synchronize()
     assert (out == 0).all()
