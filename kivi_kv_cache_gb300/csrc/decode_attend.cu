@@ -453,8 +453,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attend_kernel(DecodeArgs a
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int bh = b * a.Hkv + hk;
     const int gq = a.Hq / a.Hkv, h0 = hk * gq;
-    const int t0 = split * a.tiles_per_split;
-    const int nt = min(a.tiles_per_split, a.n_tiles - t0);  // >= 1 by the plan
+    // this CTA's tiles: the head's n_tiles spread evenly over its n_split CTAs (>= 1 each)
+    const int t0 = (int)((long long)split * a.n_tiles / a.n_split);
+    const int nt = (int)((long long)(split + 1) * a.n_tiles / a.n_split) - t0;
 
     pdl_wait();
 #pragma unroll

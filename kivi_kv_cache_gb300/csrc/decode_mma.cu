@@ -201,11 +201,10 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     float* q_s = reinterpret_cast<float*>(smem + LY::kQOff);                   // [head][channel]
     float* misc = reinterpret_cast<float*>(smem + LY::kMiscOff);
 
-    // this warp's tiles
-    const int tile_begin = split * a.tiles_per_split;
-    const int split_end = min(tile_begin + a.tiles_per_split, a.n_tiles);
-    const int w0 = min(tile_begin + warp * a.tiles_per_warp, split_end);
-    const int w1 = min(w0 + a.tiles_per_warp, split_end);
+    // this warp's tiles: the head's n_tiles spread evenly over its n_split * NW warps
+    const long long nw_head = (long long)a.n_split * kWarps, gw = (long long)split * kWarps + warp;
+    const int w0 = (int)(gw * a.n_tiles / nw_head);
+    const int w1 = (int)((gw + 1) * a.n_tiles / nw_head);
     const int s_end = min(w1, a.n_store_tiles);           // store tiles [w0, s_end)
     const int r_begin = max(w0, a.n_store_tiles);         // residual tiles [r_begin, w1)
     const int ns = s_end - w0;

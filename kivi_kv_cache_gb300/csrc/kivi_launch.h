@@ -53,8 +53,8 @@ struct DecodeArgs {
     int Hkv;
     float score_scale;    // sm_scale * log2(e): scores live in the exp2 domain
     int n_split;
-    int tiles_per_split;  // tiles: 32-token store tiles, then residual tiles
-    int tiles_per_warp;   // one-warp-per-tile kernel: contiguous tiles per warp
+    int tiles_per_split;  // planned tiles per split (the kernels spread n_tiles evenly)
+    int tiles_per_warp;   // planned tiles per warp of the one-warp-per-tile kernel
     int warps_per_cta;    // one-warp-per-tile kernel: 4 or 8
     int n_store_tiles;
     int n_tiles;
