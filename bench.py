@@ -89,6 +89,22 @@ def op_bytes(w, n_flush: int, n_res: int) -> dict:
     return {"flush_kv": flush, "residual_append": append, "dequant_kv": dequant, "decode_attend": decode}
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest x over all ranks (a job takes as long as its slowest rank)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_step: float, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of `bytes_per_step`
+    within `elapsed_ms` (the max over ranks)."""
+    return world * bytes_per_step * steps / (elapsed_ms * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -313,11 +329,7 @@ def run_gb300(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     clock = clocks.stop()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
 
     # per-op average launch duration: CUDA events on the launching stream
     # around replays of a graph of GRAPH_STEPS launches of that op alone, on
@@ -351,7 +363,7 @@ def run_gb300(args, rank, world, local_rank):
     ob = op_bytes(w, probe.n_flush, probe.n_res)
     step_bytes = sum(ob.values())
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+    value = job_gbs(world, step_bytes, args.steps, elapsed_ms)
     peak, peak_kind = measured_peaks()
     ops = {}
     for op in OPS:
@@ -387,13 +399,9 @@ def run_gb300(args, rank, world, local_rank):
             hout.copy_(inst.out, non_blocking=True)
         s1.record()
         torch.cuda.synchronize()
-        e2e_ms = s0.elapsed_time(s1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(s0.elapsed_time(s1), world, dev)
         h2d = sum(t.numel() * t.element_size() for t in (hk[0], hv[0], hq[0]))
-        e2e = {"value": round(world * step_bytes * args.e2e_steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e = {"value": round(job_gbs(world, step_bytes, args.e2e_steps, e2e_ms), 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 4),
                "ms_per_step": round(e2e_ms / args.e2e_steps, 5)}
 
