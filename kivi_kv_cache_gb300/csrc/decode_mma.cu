@@ -80,6 +80,25 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// thread-block cluster: rank of this CTA, the cluster-wide barrier (release /
+// acquire: shared-memory writes before it are visible to every CTA of the
+// cluster after it), and a load from another CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool fill) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
                  "r"(fill ? 16 : 0)
@@ -186,7 +205,9 @@ __device__ __forceinline__ void fetch_res_tile(const DecodeArgs& a, int bh, int 
 // ---------------------------------------------------------------------------
 
 // NW warps per CTA (4 or 8): 16 warps per SM either way, at 128 registers.
-template <int BITS, int GQ, int NW>
+// CL: the n_split CTAs of a (batch, KV head) form one thread-block cluster
+// (n_split <= kMaxClusterSplits) and merge through distributed shared memory.
+template <int BITS, int GQ, int NW, bool CL>
 __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs a) {
     constexpr int kWarps = NW;
     constexpr int kThreads = 32 * NW;
@@ -688,6 +709,12 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         const long long bq = (long long)b * a.Hq + h0 + h;
         if (a.n_split == 1) {
             a.out[bq * kD + d] = acc / L;
+        } else if (CL) {  // the partial stays in this CTA's shared memory (the q area is free now)
+            q_s[h * kD + d] = acc;
+            if (d == 0) {
+                misc[100 + 2 * h] = M;
+                misc[101 + 2 * h] = L;
+            }
         } else {
             a.part_o[(bq * a.n_split + split) * kD + d] = acc;
             if (d == 0) {
@@ -697,21 +724,125 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         }
     }
     if (a.n_split == 1) return;
+    if (CL) {
+        // Every CTA of the cluster holds one partial; CTA r merges outputs
+        // r * kThreads + tid, ... of the head group, reading all partials
+        // through distributed shared memory (n_split * kThreads >= 2 * 256
+        // covers the GQ * kD outputs).
+        cluster_sync();
+        const uint32_t rank = cluster_ctarank();
+        const int n = a.n_split;
+        for (int idx = (int)rank * kThreads + tid; idx < GQ * kD; idx += n * kThreads) {
+            const int h = idx / kD, dd = idx % kD;
+            float mk[kMaxClusterSplits];
+            float M = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kMaxClusterSplits; ++k) {
+                mk[k] = k < n ? ld_cluster(misc + 100 + 2 * h, k) : -INFINITY;
+                M = fmaxf(M, mk[k]);
+            }
+            float L = 0.f, acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < kMaxClusterSplits; ++k) {
+                if (k < n && mk[k] != -INFINITY) {  // -inf: a CTA without tiles
+                    const float wk = exp2f(mk[k] - M);
+                    L = fmaf(ld_cluster(misc + 101 + 2 * h, k), wk, L);
+                    acc = fmaf(ld_cluster(q_s + h * kD + dd, k), wk, acc);
+                }
+            }
+            a.out[((long long)b * a.Hq + h0 + h) * kD + dd] = acc / L;
+        }
+        cluster_sync();  // no CTA leaves while another still reads its shared memory
+        return;
+    }
     if (take_last_ticket(a, bh, reinterpret_cast<int*>(misc + 96)))
         merge_splits<16>(a, (long long)b * a.Hq + h0, GQ, warp, kWarps, lane, reinterpret_cast<float*>(smem));
 }
 
+template <int BITS, int GQ, int NW, bool CL>
+cudaError_t configure_mma() {
+    static cudaError_t status = cudaErrorNotReady;  // benign race: every caller sets the same values
+    if (status == cudaErrorNotReady) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ, NW, CL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<NW>::kSmemBytes);
+        if (e == cudaSuccess && CL)
+            e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ, NW, CL>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        status = e;
+    }
+    return status;
+}
+
+// Resident CTAs of this kernel on the device: without clusters (n = 1) or in
+// clusters of n CTAs (0 if such clusters cannot be resident). Computed once
+// per device and n with the occupancy calculator.
+template <int BITS, int GQ, int NW>
+int resident_ctas(int n, cudaStream_t stream) {
+    constexpr int kDevs = 16;
+    static int cache[kDevs][kMaxClusterSplits + 1];  // 0 unknown, -1 none, else CTAs + 1
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs || n < 1 || n > kMaxClusterSplits) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cache[dev][n] == 0) {
+        int ctas = 0;
+        if (n == 1) {
+            int per_sm = 0, sms = 0;
+            if (configure_mma<BITS, GQ, NW, false>() == cudaSuccess &&
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<BITS, GQ, NW, false>,
+                                                              32 * NW, Layout<NW>::kSmemBytes) == cudaSuccess &&
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+                ctas = per_sm * sms;
+        } else if (configure_mma<BITS, GQ, NW, true>() == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(n, 1, 1);
+            cfg.blockDim = dim3(32 * NW);
+            cfg.dynamicSmemBytes = Layout<NW>::kSmemBytes;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = n;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, decode_mma_kernel<BITS, GQ, NW, true>, &cfg) == cudaSuccess)
+                ctas = clusters * n;
+        }
+        cudaGetLastError();
+        cache[dev][n] = ctas > 0 ? ctas + 1 : -1;
+    }
+    return cache[dev][n] > 0 ? cache[dev][n] - 1 : 0;
+}
+
+// Merge the splits inside clusters when they can be resident and either the
+// whole grid fits in one wave of clusters (the latency case) or clusters keep
+// at least 95 % of the resident CTAs (otherwise a cluster size that packs the
+// GPU's processor clusters badly costs more than the merge saves).
+template <int BITS, int GQ, int NW>
+bool use_cluster(const DecodeArgs& a, cudaStream_t stream) {
+    const int n = a.n_split;
+    if (n < 2 || n > kMaxClusterSplits) return false;
+    const long long with = resident_ctas<BITS, GQ, NW>(n, stream);
+    if (with <= 0) return false;
+    const long long ctas = (long long)n * a.Hkv * a.B;
+    return ctas <= with || 20 * with >= 19LL * resident_ctas<BITS, GQ, NW>(1, stream);
+}
+
 template <int BITS, int GQ, int NW>
 cudaError_t launch_mma_typed(const DecodeArgs& a, cudaStream_t stream) {
-    static bool configured = false;  // benign race: every caller sets the same value
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ, NW>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<NW>::kSmemBytes);
+    const dim3 grid(a.n_split, a.Hkv, a.B);
+    if (use_cluster<BITS, GQ, NW>(a, stream)) {
+        cudaError_t e = configure_mma<BITS, GQ, NW, true>();
         if (e != cudaSuccess) return e;
-        configured = true;
+        return launch_pdl_cluster(decode_mma_kernel<BITS, GQ, NW, true>, grid, 32 * NW, Layout<NW>::kSmemBytes,
+                                  stream, a.n_split, a);
     }
-    return launch_pdl(decode_mma_kernel<BITS, GQ, NW>, dim3(a.n_split, a.Hkv, a.B), 32 * NW, Layout<NW>::kSmemBytes,
-                      stream, a);
+    cudaError_t e = configure_mma<BITS, GQ, NW, false>();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_mma_kernel<BITS, GQ, NW, false>, grid, 32 * NW, Layout<NW>::kSmemBytes, stream, a);
 }
 
 template <int BITS, int GQ>

@@ -78,6 +78,7 @@ struct DecodePlan {
 constexpr int kResTileTokensMma = 16;
 constexpr int kResTileTokensSplit = 16;
 constexpr int kMergeCounters = 8192;    // (batch, KV head) pairs that can take split merges
+constexpr int kMaxClusterSplits = 16;   // splits of one head merged inside a thread-block cluster
 
 // Launch with programmatic stream serialization allowed: the kernel may start
 // while the previous kernel on the stream finishes; it must (and every kernel
@@ -95,6 +96,28 @@ inline cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, siz
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+}
+
+// The same launch with the grid's x dimension cut into thread-block clusters
+// of cluster_x CTAs.
+template <typename... Exp, typename... Act>
+inline cudaError_t launch_pdl_cluster(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t stream, unsigned cluster_x, Act&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
 }
 
