@@ -184,7 +184,8 @@ kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, i
 
 /*
  * Bytes of device workspace kivi_decode_attend needs for these sizes on the
- * current device (the split count depends on the device's SM count). Returns
+ * current device, for either bit width (the split count depends on the
+ * device's SM count and on the bit width). Returns
  * 0 when the decode runs as a single split per (batch, KV head) and needs no
  * workspace, and 0 for invalid sizes. Host only (reads the device's SM count
  * once).

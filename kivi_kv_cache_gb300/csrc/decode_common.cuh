@@ -1,0 +1,102 @@
+// decode_common.cuh -- PTX helpers shared by the decode kernels: cp.async
+// staging, ldmatrix, the m16n8k16 fp16 MMA, exact code conversion, the fp16
+// hi/lo split of fp32 operands, and thread-block cluster access.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "kivi_device.cuh"
+
+namespace kivi {
+namespace dec {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async copy; with fill == false nothing is read and 16 zero bytes land.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool fill) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(fill ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bytes 0,1 of w (as e4m3) -> lo, bytes 2,3 -> hi; exact for codes (a code
+// nibble or crumb alone in a byte, read as e4m3, is c * 2^-9)
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// fp16 hi (lo == false) or lo (lo == true) part of the pair (x, y)
+__device__ __forceinline__ uint32_t split_pair(float x, float y, bool lo) {
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(__fsub_rn(x, hf.x), __fsub_rn(y, hf.y));
+    return lo ? h2_as_u32(l) : h2_as_u32(h);
+}
+
+// 2^e as fp32 for e in [-126, 127]
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// exponent E with m * 2^E < 2^14 (m >= 0); 0 for m == 0, clamped
+__device__ __forceinline__ int safe_exp(float m) {
+    if (!(m > 0.f)) return 0;
+    const int ex = ((__float_as_int(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
+    const int e = 13 - ex;
+    return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
+// thread-block cluster: rank of this CTA, the cluster-wide barrier (release /
+// acquire: shared-memory writes before it are visible to every CTA of the
+// cluster after it), and a load from another CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// barrier over `threads` threads (a multiple of 32) with named barrier `id`
+// (1..15; 0 is the CTA-wide __syncthreads barrier)
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace dec
+}  // namespace kivi

@@ -87,10 +87,10 @@ __device__ __forceinline__ float4 merge_range(const float2* ml, const float4* po
 constexpr int kScratchRow = kD + 4;  // o[kD], m, l; a multiple of 4 floats keeps float4 rows aligned
 
 // Merge of the partials of query heads bq0 .. bq0 + nheads - 1 (nheads <= 4)
-// by a CTA of nwarps (4 or 8) warps: warp w takes head w % 4 and the w / 4-th
-// of the splits, so 8 warps halve the L2 round trips; the halves meet in
-// `scratch` (16-byte aligned shared memory, 2 * 4 * kScratchRow floats).
-// Every thread of the CTA must call it (it holds a CTA barrier when nwarps == 8).
+// by a CTA of nwarps (4, 8 or 16) warps: warp w takes head w % 4 and the w / 4-th
+// of the splits, so more warps cut the L2 round trips; the shares meet in
+// `scratch` (16-byte aligned shared memory, nwarps * kScratchRow floats).
+// Every thread of the CTA must call it (it holds a CTA barrier when nwarps > 4).
 
 template <int CHUNK>
 __device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0, int nheads, int warp,

@@ -65,14 +65,43 @@ kivi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_
 #ifndef KIVI_DECODE_MIN_TILES
 #define KIVI_DECODE_MIN_TILES 3
 #endif
+// Warp-pair kernel: 0 never, 1 always, 2 when the one-warp-per-tile plan gives
+// warps at most kPairMaxWarpTiles tiles and the pair plan at most
+// kPairMaxSplits splits per head (small batches with short caches, where one
+// tile's chain and the merge bound the launch). A pair takes at least
+// kPairMinTiles tiles.
+#ifndef KIVI_DECODE_PAIR_MODE
+#define KIVI_DECODE_PAIR_MODE 2
+#endif
+#ifndef KIVI_DECODE_PAIR_MAX_WARP_TILES
+#define KIVI_DECODE_PAIR_MAX_WARP_TILES 1
+#endif
+#ifndef KIVI_DECODE_PAIR_MAX_SPLITS
+#define KIVI_DECODE_PAIR_MAX_SPLITS 24
+#endif
+#ifndef KIVI_DECODE_PAIR_MIN_TILES
+#define KIVI_DECODE_PAIR_MIN_TILES 1
+#endif
+#ifndef KIVI_DECODE_PAIRS_PER_SM
+#define KIVI_DECODE_PAIRS_PER_SM 8
+#endif
+constexpr int kPairMode = KIVI_DECODE_PAIR_MODE;
+constexpr int kPairMaxWarpTiles = KIVI_DECODE_PAIR_MAX_WARP_TILES;
+constexpr int kPairMinTiles = KIVI_DECODE_PAIR_MIN_TILES;
+constexpr int kPairMaxSplits = KIVI_DECODE_PAIR_MAX_SPLITS;
+constexpr int kPairsPerSm = KIVI_DECODE_PAIRS_PER_SM;
 constexpr int kMmaWarpsPerSm = KIVI_DECODE_MMA_WARPS_PER_SM;
+#ifndef KIVI_DECODE_MMA_WARPS_PER_SM_2BIT
+#define KIVI_DECODE_MMA_WARPS_PER_SM_2BIT 16
+#endif
+constexpr int kMmaWarpsPerSm2 = KIVI_DECODE_MMA_WARPS_PER_SM_2BIT;
 constexpr int kMmaMaxSplits4 = KIVI_DECODE_MMA_MAX_SPLITS4;
 constexpr int kSplitCtasPerSm = KIVI_DECODE_CTAS_PER_SM;
 constexpr int kSplitMinTiles = KIVI_DECODE_MIN_TILES;
 
 bool mma_group(int gq) { return gq == 1 || gq == 2 || gq == 4; }
 
-DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res) {
+DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits) {
     DecodePlan p;
     const bool mma = Hkv > 0 && Hq % Hkv == 0 && mma_group(Hq / Hkv);
     const int rt = mma ? kResTileTokensMma : kResTileTokensSplit;
@@ -80,13 +109,27 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res) {
     p.n_tiles = p.n_store_tiles + (n_res + rt - 1) / rt;
     const long long heads = (long long)B * Hkv;
     if (mma) {
-        const long long target = (long long)kMmaWarpsPerSm * sm_count();
+        // 2-bit tiles carry half the codes: fewer, longer-running warps measured faster
+        const long long target = (long long)(bits == 2 ? kMmaWarpsPerSm2 : kMmaWarpsPerSm) * sm_count();
         long long tpw = (heads * p.n_tiles + target - 1) / target;
         if (tpw < 1) tpw = 1;
         p.warps_per_cta = (p.n_tiles + 4 * tpw - 1) / (4 * tpw) > kMmaMaxSplits4 ? 8 : 4;
         if (heads > kMergeCounters) tpw = (p.n_tiles + p.warps_per_cta - 1) / p.warps_per_cta;  // one split per pair
         p.tiles_per_warp = (int)tpw;
         p.tiles_per_split = (int)(p.warps_per_cta * tpw);
+        p.pair_kernel = 0;
+        if (kPairMode == 1 || (kPairMode == 2 && tpw <= kPairMaxWarpTiles && heads <= kMergeCounters)) {
+            const long long slots = (long long)kPairsPerSm * sm_count();
+            long long tpp = (heads * p.n_tiles + slots - 1) / slots;  // tiles per pair
+            if (tpp < kPairMinTiles) tpp = kPairMinTiles;
+            if (heads > kMergeCounters) tpp = (p.n_tiles + kPairsPerCta - 1) / kPairsPerCta;
+            const long long splits = (p.n_tiles + kPairsPerCta * tpp - 1) / (kPairsPerCta * tpp);
+            if (kPairMode == 1 || splits <= kPairMaxSplits) {
+                p.pair_kernel = 1;
+                p.tiles_per_warp = (int)tpp;
+                p.tiles_per_split = (int)(kPairsPerCta * tpp);
+            }
+        }
     } else {
         const long long slots = (long long)kSplitCtasPerSm * sm_count();
         long long per = (heads * p.n_tiles + slots - 1) / slots;
@@ -95,6 +138,7 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res) {
         p.tiles_per_split = (int)per;
         p.tiles_per_warp = (int)per;
         p.warps_per_cta = 4;
+        p.pair_kernel = 0;
     }
     p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
     return p;
@@ -328,7 +372,10 @@ kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, i
 size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || S_q < 0 || n_res < 0 || D != kD || S_q + n_res == 0)
         return 0;
-    return workspace_bytes(B, Hq, make_plan(B, Hkv, Hq, S_q, n_res));
+    // the plan depends on the bit width; the size covers both
+    const size_t w2 = workspace_bytes(B, Hq, make_plan(B, Hkv, Hq, S_q, n_res, 2));
+    const size_t w4 = workspace_bytes(B, Hq, make_plan(B, Hkv, Hq, S_q, n_res, 4));
+    return w2 > w4 ? w2 : w4;
 }
 
 kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const float* kscale,
@@ -354,7 +401,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
         !aligned16(vzero_f16) || !aligned16(k_res_f16) || !aligned16(v_res_f16) ||
         !aligned16(workspace))
         return KIVI_ERR_ALIGNMENT;
-    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res);
+    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res, bits);
     const size_t need = workspace_bytes(B, Hq, p);
     if (need > 0 && (!workspace || workspace_bytes_ < need)) return KIVI_ERR_WORKSPACE;
 
@@ -380,6 +427,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
     a.tiles_per_split = p.tiles_per_split;
     a.tiles_per_warp = p.tiles_per_warp;
     a.warps_per_cta = p.warps_per_cta;
+    a.pair_kernel = p.pair_kernel;
     a.n_store_tiles = p.n_store_tiles;
     a.n_tiles = p.n_tiles;
     char* ws = static_cast<char*>(workspace);
@@ -389,8 +437,8 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
                          : nullptr;
     a.out = out_f32;
     const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
-    return from_cuda(mma_group(gq) ? launch_decode_mma(a, bits, gq, strm)
-                                   : launch_decode_channel_split(a, bits, gq, strm));
+    if (!mma_group(gq)) return from_cuda(launch_decode_channel_split(a, bits, gq, strm));
+    return from_cuda(p.pair_kernel ? launch_decode_pair(a, bits, gq, strm) : launch_decode_mma(a, bits, gq, strm));
 }
 
 kivi_status kivi_decode_workspace_init(void* workspace, size_t workspace_bytes_, kivi_stream_t stream) {

@@ -56,6 +56,7 @@ struct DecodeArgs {
     int tiles_per_split;  // planned tiles per split (the kernels spread n_tiles evenly)
     int tiles_per_warp;   // planned tiles per warp of the one-warp-per-tile kernel
     int warps_per_cta;    // one-warp-per-tile kernel: 4 or 8
+    int pair_kernel;      // 1: groups of 1, 2 or 4 heads run the warp-pair kernel
     int n_store_tiles;
     int n_tiles;
     unsigned int* counters;  // [B*Hkv] merge tickets, zero between calls (n_split > 1)
@@ -69,6 +70,7 @@ struct DecodePlan {
     int tiles_per_split;
     int tiles_per_warp;
     int warps_per_cta;
+    int pair_kernel;
     int n_store_tiles;
     int n_tiles;
 };
@@ -79,6 +81,7 @@ constexpr int kResTileTokensMma = 16;
 constexpr int kResTileTokensSplit = 16;
 constexpr int kMergeCounters = 8192;    // (batch, KV head) pairs that can take split merges
 constexpr int kMaxClusterSplits = 16;   // splits of one head merged inside a thread-block cluster
+constexpr int kPairsPerCta = 4;         // warp pairs per CTA of the warp-pair kernel
 
 // Launch with programmatic stream serialization allowed: the kernel may start
 // while the previous kernel on the stream finishes; it must (and every kernel
@@ -134,6 +137,8 @@ cudaError_t launch_residual_compact(__half* res0, __half* res1, int BH, int res_
 // Fused decodes; each merges its own splits in the same launch.
 // gq in {1, 2, 4}: one warp per tile.
 cudaError_t launch_decode_mma(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
+// gq in {1, 2, 4}: two warps per tile, 4 warp pairs per CTA (small batches).
+cudaError_t launch_decode_pair(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 // any 1 <= gq <= 8: the channels of a tile split over 4 warps.
 cudaError_t launch_decode_channel_split(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 
