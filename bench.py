@@ -256,7 +256,7 @@ class Instance:
 OPS = ["flush_kv", "residual_append", "dequant_kv", "decode_attend"]
 GRAPH_STEPS = 8
 OP_KERNEL_FILES = {"flush_kv": ["flush.cu"], "residual_append": ["residual.cu"], "dequant_kv": ["dequant.cu"],
-                   "decode_attend": ["decode_mma.cu", "decode_merge.cuh"]}
+                   "decode_attend": ["decode_pair.cu", "decode_merge.cuh", "decode_common.cuh"]}
 LAUNCHES = {"flush_kv": 1, "residual_append": 1, "dequant_kv": 1, "decode_attend": 1}
 
 
