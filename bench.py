@@ -593,6 +593,11 @@ def run_sweep(args):
               ob["flush_kv"], "flush_kv", {"workload": name, "tokens": n, "bits": w.bits, "pool": P})
         timed([lambda i=i: kv.kivi_dequant_kv(ks[i], vs[i], n, kout=kd[i], vout=vd[i]) for i in range(P)],
               ob["dequant_kv"], "dequant_kv", {"workload": name, "tokens": n, "bits": w.bits, "pool": P})
+        # fake quantization of the same tokens: read 2 B and write 2 B per element of K and V (the kd/vd
+        # buffers hold the n flushed tokens, so the S - n fp16 tokens are not part of this launch)
+        timed([lambda i=i: kv.kivi_fake_quant_kv(xs[i][0][:, :n], xs[i][1][:, :n], 0, kout=kd[i], vout=vd[i],
+                                                 bits=w.bits) for i in range(P)],
+              2 * w.BH * n * w.D * 4, "fake_quant_kv", {"workload": name, "tokens": n, "bits": w.bits, "pool": P})
         del ks, vs, kd, vd, xs
         torch.cuda.empty_cache()
 
@@ -625,6 +630,59 @@ def run_sweep(args):
                                              "pool": P, "tokens_per_s": None})
         del entries, fns
         torch.cuda.empty_cache()
+
+    # batched decode, 30 consecutive steps: B=32 sequences of 4032 packed + 64
+    # fp16 tokens; each step appends one token per sequence to the residual
+    # window (n_res 64 -> 93, no flush) and decodes one query token per head
+    B, S_q, n0, steps = 32, 4032, 64, 30
+    w = synth.Workload("batched", B=B, Hkv=8, Hq=32, D=128, S=S_q + n0 + steps, bits=4, G=32, R=0,
+                       n_outlier=4, outlier_scale=8.0, seed=4)
+    k, v, _ = synth.prefill_inputs_torch(w, 31, dev)
+    gk = kv.KiviStore(0, w.BH, S_q, w.D, w.G, 4, device=dev)
+    gv = kv.KiviStore(1, w.BH, S_q, w.D, w.G, 4, device=dev)
+    kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
+    res_cap = 128
+    kres = torch.zeros((w.BH, res_cap, w.D), dtype=torch.float16, device=dev)
+    vres = torch.zeros_like(kres)
+    kv.kivi_residual_append_kv(k[:, S_q:S_q + n0], v[:, S_q:S_q + n0], kres, vres, 0)
+    new_k = k[:, S_q + n0:].contiguous()
+    new_v = v[:, S_q + n0:].contiguous()
+    del k, v
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(32)
+    qs = torch.randn((steps, B, w.Hq, w.D), generator=gen, device=dev).to(torch.float16)
+    out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    ws = kv.kivi_decode_workspace(kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, S_q, n0 + steps, w.D), dev)
+
+    def run_steps():
+        for i in range(steps):
+            kv.kivi_residual_append_kv(new_k[:, i:i + 1], new_v[:, i:i + 1], kres, vres, n0 + i)
+            kv.kivi_decode_attend(qs[i], gk, gv, S_q, kres[:, :n0 + i + 1], vres[:, :n0 + i + 1], n0 + i + 1,
+                                  w.Hkv, w.sm_scale, out=out, workspace=ws)
+
+    run_steps()  # eager warm-up (loads the kernels, sets attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run_steps()
+    g.replay()
+    torch.cuda.synchronize()
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * steps)
+    per_step = sum(B * w.Hkv * S_q * (2 * w.D * 4 / 8 + w.D * 6 / w.G + (w.D // w.G) * 6) +
+                   B * w.Hkv * (n0 + i + 1) * w.D * 4 + B * w.Hq * w.D * 6 + B * w.Hkv * w.D * 2 * 2 * 2
+                   for i in range(steps)) / steps
+    gbs = per_step / (us * 1e-6) / 1e9
+    print(json.dumps({"op": "batched_decode_steps", "B": B, "S_kv": S_q + n0, "steps": steps,
+                      "us_per_step": round(us, 3), "tokens_per_s": round(B / (us * 1e-6), 1),
+                      "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "peak": peak,
+                      "peak_kind": kind, "step": "append 1 token (K, V) + decode"}), flush=True)
 
 
 def run_profile_case(name: str, reps: int = 3):

@@ -183,6 +183,33 @@ kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, i
                                      int n_res, int n_drop, kivi_stream_t stream);
 
 /*
+ * Fake quantization ([F] "What we're actually optimizing": the pages' kernels
+ * write the quantize-then-dequantize fp16 tensor; "So why does the kernel
+ * ship?"). For the tokens a flush would quantize, n = kivi_flush_count(S,
+ * residual_length, group_size), out[bh, t, :] = fp16(RN(RN(q * scale) + zero))
+ * with q, scale and zero exactly those of kivi_flush_keys (per-channel
+ * groups along the tokens) or kivi_flush_values (per-token groups along D):
+ * bit-identical to kivi_dequant of the flushed store. Tokens [n, S) are copied
+ * unchanged. Nothing else is written: no codes, scales or zeros.
+ * x: fp16 [BH, S, D] with a head stride of x_bh_stride tokens; out: fp16
+ * [BH, S, D] with a head stride of out_bh_stride tokens. out may be x itself
+ * (in place, same stride); otherwise it must not overlap x.
+ * Errors: as kivi_flush_keys; INVALID_ARG if out == x with another stride.
+ * *n_quantized (may be NULL) receives n.
+ */
+kivi_status kivi_fake_quant_keys(const void* x_f16, int BH, int S, int x_bh_stride, int D,
+                                 int group_size, int bits, int residual_length, void* out_f16,
+                                 int out_bh_stride, int* n_quantized, kivi_stream_t stream);
+kivi_status kivi_fake_quant_values(const void* x_f16, int BH, int S, int x_bh_stride, int D,
+                                   int group_size, int bits, int residual_length, void* out_f16,
+                                   int out_bh_stride, int* n_quantized, kivi_stream_t stream);
+/* Keys and values of equal geometry in one launch (plus one for the copies). */
+kivi_status kivi_fake_quant_kv(const void* k_f16, const void* v_f16, int BH, int S, int x_bh_stride,
+                               int D, int group_size, int bits, int residual_length,
+                               void* k_out_f16, void* v_out_f16, int out_bh_stride,
+                               int* n_quantized, kivi_stream_t stream);
+
+/*
  * Bytes of device workspace kivi_decode_attend needs for these sizes on the
  * current device, for either bit width (the split count depends on the
  * device's SM count and on the bit width). Returns

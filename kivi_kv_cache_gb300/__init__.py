@@ -21,6 +21,7 @@ __all__ = [
     "kivi_status_string", "kivi_version", "kivi_flush_count",
     "kivi_flush_keys", "kivi_flush_values", "kivi_flush_kv", "kivi_dequant", "kivi_dequant_kv",
     "kivi_residual_append", "kivi_residual_compact", "kivi_residual_append_kv", "kivi_residual_compact_kv",
+    "kivi_fake_quant_keys", "kivi_fake_quant_values", "kivi_fake_quant_kv",
     "kivi_decode_workspace_size", "kivi_decode_workspace", "kivi_decode_workspace_init",
     "kivi_decode_attend", "kivi_decode_attend_noalloc",
 ]
@@ -70,6 +71,9 @@ def lib() -> ctypes.CDLL:
             "kivi_residual_compact_kv": ([P, P, I, I, I, I, I, P], I),
             "kivi_residual_append": ([P, I, I, P, I, I, I, I, P], I),
             "kivi_residual_compact": ([P, I, I, I, I, I, P], I),
+            "kivi_fake_quant_keys": ([P, I, I, I, I, I, I, I, P, I, IP, P], I),
+            "kivi_fake_quant_values": ([P, I, I, I, I, I, I, I, P, I, IP, P], I),
+            "kivi_fake_quant_kv": ([P, P, I, I, I, I, I, I, I, P, P, I, IP, P], I),
             "kivi_decode_workspace_size": ([I, I, I, I, I, I], Z),
             "kivi_decode_workspace_init": ([P, Z, P], I),
             "kivi_decode_attend": ([P, P, P, P, P, P, P, I, I, P, P, I, I, I, I, I, I, I, I, F, P, P, Z, P], I),
@@ -104,6 +108,8 @@ def _check(fn: str, status: int):
 def _rows(x, D: int):
     """Head stride (in tokens) of a [BH, S, D] fp16 view with dense token rows."""
     assert x.dim() == 3 and x.shape[2] == D, tuple(x.shape)
+    if x.numel() == 0:  # no rows: any head stride of at least S serves
+        return x.shape[1]
     assert x.stride(2) == 1 and x.stride(1) == D and x.stride(0) % D == 0, x.stride()
     return x.stride(0) // D
 
@@ -241,6 +247,46 @@ def kivi_residual_compact(res, n_res: int, n_drop: int, stream=None):
                                      _stream(stream))
     _check("kivi_residual_compact", st)
     return n_res - n_drop
+
+
+def _fake_quant(fn: str, x, residual_length: int, out, G: int, bits: int, stream):
+    import torch
+    BH, S, D = x.shape
+    if out is None:
+        out = torch.empty((BH, S, D), dtype=torch.float16, device=x.device)
+    n = ctypes.c_int(-1)
+    st = getattr(lib(), fn)(_ptr(x), BH, S, _rows(x, D), D, G, bits, residual_length, _ptr(out), _rows(out, D),
+                            ctypes.byref(n), _stream(stream))
+    _check(fn, st)
+    return out, n.value
+
+
+def kivi_fake_quant_keys(x, residual_length: int, out=None, G: int = 32, bits: int = 4, stream=None):
+    """Fake-quantized keys x [BH, S, D] fp16 -> (out, n_quantized); out may be x (in place)."""
+    return _fake_quant("kivi_fake_quant_keys", x, residual_length, out, G, bits, stream)
+
+
+def kivi_fake_quant_values(x, residual_length: int, out=None, G: int = 32, bits: int = 4, stream=None):
+    """Fake-quantized values x [BH, S, D] fp16 -> (out, n_quantized); out may be x (in place)."""
+    return _fake_quant("kivi_fake_quant_values", x, residual_length, out, G, bits, stream)
+
+
+def kivi_fake_quant_kv(k, v, residual_length: int, kout=None, vout=None, G: int = 32, bits: int = 4,
+                       stream=None):
+    """Fake quantization of keys and values of equal geometry -> (kout, vout, n_quantized)."""
+    import torch
+    BH, S, D = k.shape
+    if kout is None:
+        kout = torch.empty((BH, S, D), dtype=torch.float16, device=k.device)
+    if vout is None:
+        vout = torch.empty((BH, S, D), dtype=torch.float16, device=v.device)
+    stride = _rows(k, D)
+    assert _rows(v, D) == stride and _rows(kout, D) == _rows(vout, D)
+    n = ctypes.c_int(-1)
+    st = lib().kivi_fake_quant_kv(_ptr(k), _ptr(v), BH, S, stride, D, G, bits, residual_length, _ptr(kout), _ptr(vout),
+                                  _rows(kout, D), ctypes.byref(n), _stream(stream))
+    _check("kivi_fake_quant_kv", st)
+    return kout, vout, n.value
 
 
 def kivi_decode_workspace_size(B: int, Hq: int, Hkv: int, S_q: int, n_res: int, D: int = 128) -> int:

@@ -67,11 +67,11 @@ __device__ __forceinline__ uint32_t pack8(const uint32_t (&tb)[8]) {
     }
 }
 
-// Codes of 8 fp16 elements (one 16-byte vector) packed into BITS*8 bits.
-// z2/r2: per-element zero and RN(1/scale) as fp32x2 pairs; s: scales.
-template <int BITS>
-__device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
-                                           const float (&s)[8]) {
+// Codes of 8 fp16 elements (one 16-byte vector), each as the fp32 bit
+// pattern of 2^23 + q in tb[i]. z2/r2: per-element zero and RN(1/scale) as
+// fp32x2 pairs; s: scales.
+__device__ __forceinline__ void quant8_codes(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
+                                             const float (&s)[8], uint32_t (&tb)[8]) {
     const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
     const f32x2 M2 = pk(kMagic, kMagic);
     f32x2 a[4], y[4], t[4];
@@ -85,7 +85,6 @@ __device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4],
         const float2 f = upk(sub2(y[k], sub2(t[k], M2)));
         fm = fmaxf(fm, fmaxf(fabsf(f.x), fabsf(f.y)));
     }
-    uint32_t tb[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const float2 tt = upk(t[k]);
@@ -102,7 +101,36 @@ __device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4],
                 tb[2 * k + 1] = exact_code_bits(aa.y, s[2 * k + 1]);
         }
     }
+}
+
+// The codes of quant8_codes packed into BITS*8 bits.
+template <int BITS>
+__device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
+                                           const float (&s)[8]) {
+    uint32_t tb[8];
+    quant8_codes(xv, z2, r2, s, tb);
     return pack8<BITS>(tb);
+}
+
+// Fake quantization of the same 8 elements: fp16(RN(RN(q * s) + z)), the
+// dequantized value of each code (VeloxQuant-MLX blog, "A 5.65x Metal Kernel
+// That Made My LLM Exactly 0% Faster", "What we're actually optimizing";
+// multiply, then a separate add: "Three ways to be off by one bit" #1).
+// With tb = bits of 2^23 + q, fma(2^23 + q, s, -2^23 s) is q * s rounded once.
+__device__ __forceinline__ uint4 fake8(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
+                                       const float (&s)[8]) {
+    uint32_t tb[8];
+    quant8_codes(xv, z2, r2, s, tb);
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const f32x2 q2 = pk(__uint_as_float(tb[2 * k]), __uint_as_float(tb[2 * k + 1]));
+        const f32x2 s2 = pk(s[2 * k], s[2 * k + 1]);
+        const f32x2 n2 = pk(-kMagic * s[2 * k], -kMagic * s[2 * k + 1]);
+        const float2 r = upk(add2(fma2(q2, s2, n2), z2[k]));
+        h[k] = h2_as_u32(__floats2half2_rn(r.x, r.y));
+    }
+    return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 // -0 -> +0 (applied to min and max, so zero and scale carry no negative sign)
@@ -121,7 +149,10 @@ __device__ __forceinline__ float canon(float v) { return __fadd_rn(v, 0.0f); }
 
 constexpr int kItemBytes = 4096;
 constexpr int kWarpSmem = 2 * kItemBytes;  // two stages
-constexpr int kBlocksPerSm = 4;
+#ifndef KIVI_FLUSH_BLOCKS_PER_SM
+#define KIVI_FLUSH_BLOCKS_PER_SM 4
+#endif
+constexpr int kBlocksPerSm = KIVI_FLUSH_BLOCKS_PER_SM;  // resident CTAs per SM the grid is sized for
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -166,8 +197,9 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
 }
 
 // keys: lane = part * 8 + oc; part owns tokens [8 part, 8 part + 8) of the
-// group, oc owns 8 channels of this 64-channel half.
-template <int BITS>
+// group, oc owns 8 channels of this 64-channel half. FAKE: write the fake-
+// quantized fp16 rows to a.fq instead of codes, scales and zeros.
+template <int BITS, bool FAKE>
 __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st, int lane) {
     const int half = item & 1, g = (item >> 1) % it.ng, bh = (item >> 1) / it.ng;
     const int oc = lane & 7, part = lane >> 3;
@@ -236,6 +268,12 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         z2[k] = pk(z[2 * k], z[2 * k + 1]);
         r2[k] = pk(r[2 * k], r[2 * k + 1]);
     }
+    if (FAKE) {
+        uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * kD) + octet;
+#pragma unroll 1
+        for (int i = 0; i < nv; ++i) frow[i * (kD / 8)] = fake8(xs[i * 8], z2, r2, s);
+        return;
+    }
     if (part == 0) {
         const long long m = ((long long)bh * (a.s_cap / kG) + a.s_off / kG + g) * kD + octet * 8;
         float4* sp = reinterpret_cast<float4*>(a.scale + m);
@@ -262,7 +300,7 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
 // 2 jp + 1 (32 channels each) of row `row` of the item: min/max, scale and
 // codes of a whole group in one lane, no shuffles, one 16-byte code store
 // (4-bit) per group.
-template <int BITS>
+template <int BITS, bool FAKE>
 __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
                                            int lane) {
     const int vi = item - it.key_items;
@@ -294,6 +332,12 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
         const f32x2 z1 = pk(z, z), r1 = pk(rc, rc);
         const f32x2 z2[4] = {z1, z1, z1, z1}, r2[4] = {r1, r1, r1, r1};
         const float sv[8] = {sc, sc, sc, sc, sc, sc, sc, sc};
+        if (FAKE) {
+            uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * kD + 32 * j);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) frow[k] = fake8(x[k], z2, r2, sv);
+            continue;
+        }
         uint32_t pq[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS>(x[k], z2, r2, sv);
@@ -310,7 +354,7 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
 
 // Keys, values, or both: warp w of the grid handles items w, w + W, ... of the
 // list [key items | value items] (W = total warps).
-template <int BITS>
+template <int BITS, bool FAKE>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -329,21 +373,21 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs
         uint8_t* S = st[n & 1];
         cp_async_wait1();
         __syncwarp();
-        if (item < it.key_items) key_item<BITS>(k, it, item, S, lane);
-        else value_item<BITS>(v, it, item, S, lane);
+        if (item < it.key_items) key_item<BITS, FAKE>(k, it, item, S, lane);
+        else value_item<BITS, FAKE>(v, it, item, S, lane);
         __syncwarp();
         if (item + 2 * stride < total) fetch_item(k, v, it, item + 2 * stride, S, lane);
         cp_async_commit();
     }
 }
 
-template <int BITS>
+template <int BITS, bool FAKE>
 cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
     static int grid_cap = 0;
     static bool configured = false;
     const int smem = (kThreads / 32) * kWarpSmem;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, FAKE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -355,7 +399,7 @@ cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it
     if (total <= 0) return cudaSuccess;
     long long blocks = (total + 3) / 4;
     if (blocks > grid_cap) blocks = grid_cap;
-    return launch_pdl(flush_kernel<BITS>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
+    return launch_pdl(flush_kernel<BITS, FAKE>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
 }
 
 // Pointers of heads [h0, h0 + nh) of a flush.
@@ -363,6 +407,10 @@ FlushArgs head_slice(const FlushArgs& a, int h0, int nh, int bits, int axis) {
     FlushArgs s = a;
     s.BH = nh;
     s.x += (long long)h0 * a.x_bh_stride * kD;
+    if (a.fq) {
+        s.fq += (long long)h0 * a.fq_bh_stride * kD;
+        return s;
+    }
     s.codes += (long long)h0 * a.s_cap * (kD * bits / 8);
     const long long meta = axis == 0 ? (long long)(a.s_cap / kG) * kD : (long long)a.s_cap * (kD / kG);
     s.scale += h0 * meta;
@@ -390,7 +438,9 @@ cudaError_t launch_flush_impl(const FlushArgs& k, const FlushArgs& v, bool do_k,
         it.nv = nv;
         it.key_items = do_k ? nh * 2 * ng : 0;
         it.val_items = do_v ? nh * nv : 0;
-        cudaError_t e = bits == 4 ? launch_items<4>(ks, vs, it, stream) : launch_items<2>(ks, vs, it, stream);
+        const bool fake = a.fq != nullptr;
+        cudaError_t e = bits == 4 ? (fake ? launch_items<4, true>(ks, vs, it, stream) : launch_items<4, false>(ks, vs, it, stream))
+                                  : (fake ? launch_items<2, true>(ks, vs, it, stream) : launch_items<2, false>(ks, vs, it, stream));
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
@@ -402,6 +452,11 @@ cudaError_t launch_flush(int axis, const FlushArgs& a, int bits, cudaStream_t st
 
 cudaError_t launch_flush_kv(const FlushArgs& k, const FlushArgs& v, int bits, cudaStream_t stream) {
     return launch_flush_impl(k, v, true, true, bits, stream);
+}
+
+cudaError_t launch_fake_quant(const FlushArgs& k, const FlushArgs& v, bool do_k, bool do_v, int bits,
+                              cudaStream_t stream) {
+    return launch_flush_impl(k, v, do_k, do_v, bits, stream);
 }
 
 }  // namespace kivi

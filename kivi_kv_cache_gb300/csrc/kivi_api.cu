@@ -200,9 +200,73 @@ kivi_status flush_one(int axis, const void* x, int BH, int S, int x_bh_stride, i
                                   bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Fake quantization of keys (do_k) and/or values (do_v): the first
+// kivi_flush_count(S, R, G) tokens of each input become their KIVI
+// reconstructions in the output; the remaining tokens are copied unchanged
+// unless the output is the input (in place).
+kivi_status fake_quant(const void* k, const void* v, bool do_k, bool do_v, int BH, int S, int x_bh_stride,
+                       int D, int G, int bits, int R, void* k_out, void* v_out, int out_bh_stride,
+                       int* n_quantized, kivi_stream_t stream) {
+    kivi_status st = shape_check(D, G, bits);
+    if (st != KIVI_OK) return st;
+    if (BH <= 0 || S < 0 || R < 0 || x_bh_stride < S || out_bh_stride < S) return KIVI_ERR_INVALID_ARG;
+    const int n = kivi_flush_count(S, R, G);
+    if (n < 0) return KIVI_ERR_INVALID_ARG;
+    if (n_quantized) *n_quantized = n;
+    if (S == 0) return KIVI_OK;
+    if ((do_k && (!k || !k_out)) || (do_v && (!v || !v_out))) return KIVI_ERR_INVALID_ARG;
+    // the output either is the input (same place and stride) or leaves it alone
+    if ((do_k && k_out == k && out_bh_stride != x_bh_stride) || (do_v && v_out == v && out_bh_stride != x_bh_stride))
+        return KIVI_ERR_INVALID_ARG;
+    if ((do_k && (!aligned16(k) || !aligned16(k_out))) || (do_v && (!aligned16(v) || !aligned16(v_out))))
+        return KIVI_ERR_ALIGNMENT;
+    const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+    if (n > 0) {
+        FlushArgs ka = flush_args(do_k ? k : v, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G);
+        FlushArgs va = flush_args(do_v ? v : k, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G);
+        ka.fq = static_cast<__half*>(do_k ? k_out : v_out);
+        va.fq = static_cast<__half*>(do_v ? v_out : k_out);
+        ka.fq_bh_stride = va.fq_bh_stride = out_bh_stride;
+        cudaError_t e = launch_fake_quant(ka, va, do_k, do_v, bits, strm);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    // tokens [n, S) stay fp16: copy them behind the reconstructions
+    const int tail = S - n;
+    const bool copy_k = do_k && k_out != k, copy_v = do_v && v_out != v;
+    if (tail > 0 && (copy_k || copy_v)) {
+        const __half* src0 = static_cast<const __half*>(copy_k ? k : v) + (long long)n * kD;
+        const __half* src1 = copy_k && copy_v ? static_cast<const __half*>(v) + (long long)n * kD : nullptr;
+        __half* dst0 = static_cast<__half*>(copy_k ? k_out : v_out);
+        __half* dst1 = copy_k && copy_v ? static_cast<__half*>(v_out) : nullptr;
+        return from_cuda(launch_residual_append(src0, src1, x_bh_stride, tail, dst0, dst1, BH, out_bh_stride, n, strm));
+    }
+    return KIVI_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+kivi_status kivi_fake_quant_keys(const void* x_f16, int BH, int S, int x_bh_stride, int D, int group_size,
+                                 int bits, int residual_length, void* out_f16, int out_bh_stride,
+                                 int* n_quantized, kivi_stream_t stream) {
+    return fake_quant(x_f16, nullptr, true, false, BH, S, x_bh_stride, D, group_size, bits, residual_length,
+                      out_f16, nullptr, out_bh_stride, n_quantized, stream);
+}
+
+kivi_status kivi_fake_quant_values(const void* x_f16, int BH, int S, int x_bh_stride, int D, int group_size,
+                                   int bits, int residual_length, void* out_f16, int out_bh_stride,
+                                   int* n_quantized, kivi_stream_t stream) {
+    return fake_quant(nullptr, x_f16, false, true, BH, S, x_bh_stride, D, group_size, bits, residual_length,
+                      nullptr, out_f16, out_bh_stride, n_quantized, stream);
+}
+
+kivi_status kivi_fake_quant_kv(const void* k_f16, const void* v_f16, int BH, int S, int x_bh_stride, int D,
+                               int group_size, int bits, int residual_length, void* k_out_f16,
+                               void* v_out_f16, int out_bh_stride, int* n_quantized, kivi_stream_t stream) {
+    return fake_quant(k_f16, v_f16, true, true, BH, S, x_bh_stride, D, group_size, bits, residual_length,
+                      k_out_f16, v_out_f16, out_bh_stride, n_quantized, stream);
+}
 
 const char* kivi_status_string(kivi_status s) {
     switch (s) {

@@ -22,6 +22,8 @@ struct FlushArgs {
     __half* zero;
     int s_off;
     int s_cap;
+    __half* fq = nullptr;      // fake quantization: fp16 reconstructions [BH, fq_bh_stride, D] instead of a store
+    long long fq_bh_stride = 0;
 };
 
 struct DequantArgs {
@@ -126,6 +128,10 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(Exp...), dim3 grid, dim3 bl
 
 cudaError_t launch_flush(int axis, const FlushArgs& a, int bits, cudaStream_t stream);
 cudaError_t launch_flush_kv(const FlushArgs& k, const FlushArgs& v, int bits, cudaStream_t stream);
+// fake quantization (k.fq / v.fq set): the first n_flush tokens of x become
+// their KIVI reconstructions in fq; keys if do_k, values if do_v, one launch
+cudaError_t launch_fake_quant(const FlushArgs& k, const FlushArgs& v, bool do_k, bool do_v, int bits,
+                              cudaStream_t stream);
 cudaError_t launch_dequant(int axis, const DequantArgs& a, int bits, cudaStream_t stream);
 cudaError_t launch_dequant_kv(const DequantArgs& k, const DequantArgs& v, int bits, cudaStream_t stream);
 // src1/res1 may be null (one tensor); otherwise both pairs are handled in one launch

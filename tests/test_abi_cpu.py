@@ -142,6 +142,25 @@ def test_decode_rejects_bad_arguments(L):
 
 
 @no_gpu
+def test_fake_quant_argument_checks(L):
+    n = ctypes.c_int(-7)
+    fk = L.kivi_fake_quant_keys
+    assert fk(FAKE, 8, 256, 256, 64, 32, 4, 128, FAKE + 4096, 256, ctypes.byref(n), None) == UNSUPPORTED
+    assert fk(FAKE, 8, 256, 256, 128, 32, 3, 128, FAKE + 4096, 256, ctypes.byref(n), None) == UNSUPPORTED
+    assert fk(FAKE, 8, 256, 200, 128, 32, 4, 128, FAKE + 4096, 256, ctypes.byref(n), None) == INVALID  # stride < S
+    assert fk(FAKE, 8, 256, 256, 128, 32, 4, 128, FAKE + 4096, 255, ctypes.byref(n), None) == INVALID
+    assert fk(FAKE, 8, 256, 256, 128, 32, 4, -1, FAKE + 4096, 256, ctypes.byref(n), None) == INVALID
+    assert fk(None, 8, 256, 256, 128, 32, 4, 128, FAKE + 4096, 256, ctypes.byref(n), None) == INVALID
+    assert fk(FAKE, 8, 256, 256, 128, 32, 4, 128, None, 256, ctypes.byref(n), None) == INVALID
+    assert fk(FAKE, 8, 256, 256, 128, 32, 4, 128, FAKE, 300, ctypes.byref(n), None) == INVALID  # in place, other stride
+    assert fk(FAKE + 8, 8, 256, 256, 128, 32, 4, 128, FAKE + 4096, 256, ctypes.byref(n), None) == ALIGN
+    # nothing to do: S == 0 reports n = 0 without touching the device
+    assert fk(None, 8, 0, 0, 128, 32, 4, 128, None, 0, ctypes.byref(n), None) == OK and n.value == 0
+    assert L.kivi_fake_quant_kv(FAKE, None, 8, 256, 256, 128, 32, 4, 128, FAKE + 4096, FAKE + 8192, 256,
+                                ctypes.byref(n), None) == INVALID
+
+
+@no_gpu
 def test_workspace_init_rejects_null(L):
     assert L.kivi_decode_workspace_init(None, 0, None) == OK      # nothing to zero
     assert L.kivi_decode_workspace_init(None, 1024, None) == INVALID
