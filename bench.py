@@ -62,6 +62,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--hashes", action="store_true", help="print the source hash of each op and exit")
+    p.add_argument("--stream", action="store_true",
+                   help="instead of the step line: the 36-layer streaming serving simulation (tokens/s)")
+    p.add_argument("--stream-steps", type=int, default=3072, help="decode steps of --stream (multiple of 32)")
     p.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
                    help="run one op on one case a few times, untimed (a target for ncu captures)")
     p.add_argument("--sweep", nargs="?", const="all", choices=["all", "decode"],
@@ -631,6 +634,71 @@ def run_sweep(args):
         del entries, fns
         torch.cuda.empty_cache()
 
+    # two-pass "decode-once" against the fused decode (B=1 and B=32, 4032
+    # packed + 64 fp16 tokens): the store changes only when a flush folds G
+    # tokens in, so a two-pass decoder dequantizes it once per G steps and
+    # attends over an all-fp16 cache every step. Reported: the fused decode,
+    # the dequant, the fp16 attend (the same decode kernels over S_q = 0 and
+    # S_kv fp16 tokens) and the two-pass cost per step, attend + dequant / G.
+    for B in (1, 32):
+        S_q, n_res = 4032, 64
+        S = S_q + n_res
+        w = synth.Workload("twopass", B=B, Hkv=8, Hq=32, D=128, S=S, bits=4, G=32, R=0, n_outlier=4,
+                           outlier_scale=8.0, seed=12)
+        k, v, q = synth.prefill_inputs_torch(w, 41, dev)
+        gk = kv.KiviStore(0, w.BH, S_q, w.D, w.G, 4, device=dev)
+        gv = kv.KiviStore(1, w.BH, S_q, w.D, w.G, 4, device=dev)
+        kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
+        kr, vr = k[:, S_q:].contiguous(), v[:, S_q:].contiguous()
+        kd = torch.empty((w.BH, S_q, w.D), dtype=torch.float16, device=dev)
+        vd = torch.empty_like(kd)
+        kfull = torch.cat([kd, kr], dim=1)  # the fp16 cache the attend reads (contents: any fp16)
+        vfull = torch.cat([vd, vr], dim=1)
+        del k, v
+        out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device=dev)
+        ws = kv.kivi_decode_workspace(max(kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, S_q, n_res, w.D),
+                                          kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, 0, S, w.D)), dev)
+        per_tok = 2 * w.D * 4 / 8 + w.D * 6 / w.G + (w.D // w.G) * 6
+        fused_b = w.BH * S_q * per_tok + w.BH * n_res * w.D * 4 + B * w.Hq * w.D * 6
+        deq_b = 2 * w.BH * S_q * w.D * (2 + 4 / 8 + 6 / w.G)
+        att_b = w.BH * S * w.D * 4 + B * w.Hq * w.D * 6
+        res = {}
+        for label, fn, nbytes in (
+                ("fused", lambda: kv.kivi_decode_attend(q, gk, gv, S_q, kr, vr, n_res, w.Hkv, w.sm_scale, out=out,
+                                                        workspace=ws), fused_b),
+                ("dequant", lambda: kv.kivi_dequant_kv(gk, gv, S_q, kout=kd, vout=vd), deq_b),
+                ("fp16_attend", lambda: kv.kivi_decode_attend(q, gk, gv, 0, kfull, vfull, S, w.Hkv, w.sm_scale,
+                                                              out=out, workspace=ws), att_b)):
+            g = torch.cuda.CUDAGraph()
+            fn()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g):
+                for _ in range(8):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            reps = 25
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            res[label] = e0.elapsed_time(e1) * 1e3 / (reps * 8)
+            res[label + "_GB/s"] = round(nbytes / (res[label] * 1e-6) / 1e9, 1)
+        two_pass = res["fp16_attend"] + res["dequant"] / w.G
+        print(json.dumps({"op": "decode_two_pass_vs_fused", "B": B, "S_kv": S, "bits": 4,
+                          "fused_us": round(res["fused"], 3), "dequant_us": round(res["dequant"], 3),
+                          "fp16_attend_us": round(res["fp16_attend"], 3),
+                          "two_pass_us_per_step": round(two_pass, 3),
+                          "fused_over_two_pass": round(two_pass / res["fused"], 3),
+                          "GB/s": {k2: v2 for k2, v2 in res.items() if k2.endswith("GB/s")},
+                          "note": "two-pass per step = fp16 attend + dequant / G (one dequant per G steps); "
+                                  "L2 not flushed between launches: one instance, 8 launches per graph"}),
+              flush=True)
+        del gk, gv, kr, vr, kd, vd, kfull, vfull, ws
+        torch.cuda.empty_cache()
+
     # batched decode, 30 consecutive steps: B=32 sequences of 4032 packed + 64
     # fp16 tokens; each step appends one token per sequence to the residual
     # window (n_res 64 -> 93, no flush) and decodes one query token per head
@@ -685,6 +753,99 @@ def run_sweep(args):
                       "peak_kind": kind, "step": "append 1 token (K, V) + decode"}), flush=True)
 
 
+def run_stream(args):
+    """Streaming serving simulation of the KV-cache work: 36 layers, B=16,
+    H_kv=8, Hq=32, D=128, 4-bit, G=32, R=128, context growing from 1024 tokens
+    by one token per step. Every layer-step appends the new token's K and V to
+    the fp16 residual window, flushes G tokens into the packed store and
+    compacts the window when it reaches R + G tokens, and decodes one query
+    token per head. The launches of each 32-step flush cycle (all layers) are
+    captured in a CUDA graph beforehand; the timed region replays them all.
+    tokens/s = B * steps / time (KV-cache work only: no projections or MLP)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import kivi_kv_cache_gb300 as kv
+    from kivi_kv_cache_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, kind = measured_peaks()
+    L, B, Hkv, Hq, D, G, R, bits = 36, 16, 8, 32, 128, 32, 128, 4
+    ctx0 = 1024
+    steps = (args.stream_steps // G) * G
+    BH = B * Hkv
+    s_cap = ctx0 + steps
+    res_cap = R + G
+    w = synth.Workload("stream", B=B, Hkv=Hkv, Hq=Hq, D=D, S=ctx0, bits=bits, G=G, R=R, n_outlier=4,
+                       outlier_scale=8.0, seed=5)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    new_k = torch.randn((BH, G, D), generator=gen, device=dev).to(torch.float16)  # tokens appended, cyclically
+    new_v = torch.randn((BH, G, D), generator=gen, device=dev).to(torch.float16)
+    qs = torch.randn((G, B, Hq, D), generator=gen, device=dev).to(torch.float16)
+    layers = []
+    for l in range(L):
+        k, v, _ = synth.prefill_inputs_torch(w, 100 + l, dev)
+        ks = kv.KiviStore(0, BH, s_cap, D, G, bits, device=dev)
+        vs = kv.KiviStore(1, BH, s_cap, D, G, bits, device=dev)
+        S_q = kv.kivi_flush_kv(k, v, R, ks, vs)
+        kres = torch.zeros((BH, res_cap, D), dtype=torch.float16, device=dev)
+        vres = torch.zeros_like(kres)
+        n_res = kv.kivi_residual_append_kv(k[:, S_q:], v[:, S_q:], kres, vres, 0)
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+        layers.append({"ks": ks, "vs": vs, "kres": kres, "vres": vres, "S_q": S_q, "n_res": n_res, "out": out})
+        del k, v
+    need = max(kv.kivi_decode_workspace_size(B, Hq, Hkv, sq, nr, D)  # the largest plan of any step
+               for sq in range(ctx0 - R, s_cap + 1, G) for nr in range(R, R + G + 1))
+    ws = kv.kivi_decode_workspace(need, dev)
+
+    def layer_step(st, i):
+        st["n_res"] = kv.kivi_residual_append_kv(new_k[:, i % G:i % G + 1], new_v[:, i % G:i % G + 1], st["kres"],
+                                                 st["vres"], st["n_res"])
+        if st["n_res"] >= R + G:
+            n = kv.kivi_flush_kv(st["kres"], st["vres"], R, st["ks"], st["vs"], s_off=st["S_q"],
+                                 n_tokens=st["n_res"])
+            st["S_q"] += n
+            st["n_res"] = kv.kivi_residual_compact_kv(st["kres"], st["vres"], st["n_res"], n)
+        nr = st["n_res"]
+        kv.kivi_decode_attend(qs[i % G], st["ks"], st["vs"], st["S_q"], st["kres"][:, :nr], st["vres"][:, :nr],
+                              nr, Hkv, w.sm_scale, out=st["out"], workspace=ws)
+
+    # warm-up on a copy of nothing: one eager cycle would change the state, so
+    # run the first cycle eagerly only to load the kernels, then restart it
+    snapshot = [(st["S_q"], st["n_res"]) for st in layers]
+    for st in layers:
+        layer_step(st, 0)
+    torch.cuda.synchronize()
+    for st, (sq, nr) in zip(layers, snapshot):  # the appended token is overwritten by the replay
+        st["S_q"], st["n_res"] = sq, nr
+    graphs = []
+    for c in range(steps // G):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for j in range(G):
+                for st in layers:
+                    layer_step(st, c * G + j)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for g in graphs:
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    print(json.dumps({"op": "stream_simulation", "layers": L, "B": B, "Hkv": Hkv, "Hq": Hq, "D": D, "bits": bits,
+                      "G": G, "R": R, "context": [ctx0, ctx0 + steps], "steps": steps,
+                      "ms": round(ms, 3), "tokens_per_s": round(B * steps / (ms * 1e-3), 1),
+                      "us_per_layer_step": round(ms * 1e3 / (steps * L), 3),
+                      "flushes_per_layer": steps // G, "peak": peak, "peak_kind": kind,
+                      "note": "KV-cache work only (append, flush, compact, decode per layer-step); "
+                              "no projections or MLP"}), flush=True)
+
+
 def run_profile_case(name: str, reps: int = 3):
     """A few untimed launches of one op, for profiler captures of a size the
     step bench does not run."""
@@ -727,6 +888,9 @@ def main():
     args = parse_args()
     if args.profile_case:
         run_profile_case(args.profile_case)
+        return
+    if args.stream:
+        run_stream(args)
         return
     if args.hashes:
         for op, files in OP_KERNEL_FILES.items():

@@ -292,6 +292,29 @@ def test_decode_stream_sweep_sampled(S_kv):
         assert np.max(np.abs(out[b:b + 1] - ref)) <= TOL
 
 
+def test_two_pass_decode_once_equals_fused():
+    """The two-pass "decode-once" composition (dequantize the store, then the
+    decode over an all-fp16 cache: S_q = 0) gives the fused decode's result
+    within the decode tolerance, and both match the oracle."""
+    w = synth.Workload("twopass", B=2, Hkv=8, Hq=32, D=128, S=1000 + 40, bits=4, G=32, R=0, n_outlier=4,
+                       outlier_scale=8.0, seed=61)
+    rng = np.random.default_rng(w.seed)
+    S_q, n_res = 992, 48
+    k = synth.keys(rng, (w.BH, S_q + n_res), 128, synth.outlier_channels(w), 8.0)
+    v = synth.normal(rng, (w.BH, S_q + n_res, 128))
+    q = synth.normal(rng, (w.B, w.Hq, 128))
+    fused, ref = decode_case(w, S_q, n_res, k, v, q)
+    gk = kv.KiviStore(0, w.BH, S_q, device=DEV)
+    gv = kv.KiviStore(1, w.BH, S_q, device=DEV)
+    kv.kivi_flush_kv(dev(k), dev(v), 0, gk, gv, n_tokens=S_q)
+    kd, vd = kv.kivi_dequant_kv(gk, gv, S_q)
+    kfull = torch.cat([kd, dev(k[:, S_q:])], dim=1)
+    vfull = torch.cat([vd, dev(v[:, S_q:])], dim=1)
+    two = host(kv.kivi_decode_attend(dev(q), gk, gv, 0, kfull, vfull, S_q + n_res, w.Hkv, w.sm_scale))
+    assert np.max(np.abs(two - ref)) <= TOL
+    assert np.max(np.abs(two - fused)) <= TOL
+
+
 def test_decode_workspace_too_small_is_rejected():
     w = synth.WORKLOADS["qwen8b"]
     q = torch.zeros((1, 32, 128), dtype=torch.float16, device=DEV)
