@@ -17,21 +17,28 @@
 
 namespace kivi {
 
+// Ticket add with acquire-release semantics at GPU scope: the release half
+// publishes every write this thread has observed (the CTA's partial stores,
+// ordered before it by the CTA barrier); the acquire half makes the writes
+// published by earlier tickets visible to the ticket holder.
+__device__ __forceinline__ unsigned ticket_add_acq_rel(unsigned* p) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
 // Called by all threads of the CTA after its partials are written. Returns
 // true in the CTA that must merge; *flag is a shared-memory int.
 __device__ __forceinline__ bool take_last_ticket(const DecodeArgs& a, int bh, int* flag) {
-    __syncthreads();  // every thread's partial stores precede thread 0's fence
+    __syncthreads();  // every thread's partial stores precede thread 0's ticket
     if (threadIdx.x == 0) {
-        __threadfence();  // cumulative: the CTA's partials are visible before the ticket
-        const unsigned ticket = atomicAdd(a.counters + bh, 1u);
+        const unsigned ticket = ticket_add_acq_rel(a.counters + bh);
         const bool last = ticket == (unsigned)(a.n_split - 1);
         if (last) atomicExch(a.counters + bh, 0u);  // ready for the next call
         *flag = last;
     }
-    __syncthreads();
-    const bool last = *flag != 0;
-    if (last) __threadfence();  // every other CTA's partials are visible
-    return last;
+    __syncthreads();  // the ticket holder's acquire covers its CTA's reads after this barrier
+    return *flag != 0;
 }
 
 // Log-sum-exp sum of the partials lo .. hi-1 of one query head: *M = their
