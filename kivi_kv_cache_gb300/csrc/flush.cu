@@ -336,19 +336,19 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
             uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * kD + 32 * j);
 #pragma unroll
             for (int k = 0; k < 4; ++k) frow[k] = fake8(x[k], z2, r2, sv);
-            continue;
-        }
-        uint32_t pq[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS>(x[k], z2, r2, sv);
-        if (BITS == 4) {
-            *reinterpret_cast<uint4*>(a.codes + grow * 64 + 16 * j) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
         } else {
-            *reinterpret_cast<uint2*>(a.codes + grow * 32 + 8 * j) =
-                make_uint2(pq[0] | (pq[1] << 16), pq[2] | (pq[3] << 16));
+            uint32_t pq[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS>(x[k], z2, r2, sv);
+            if (BITS == 4) {
+                *reinterpret_cast<uint4*>(a.codes + grow * 64 + 16 * j) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
+            } else {
+                *reinterpret_cast<uint2*>(a.codes + grow * 32 + 8 * j) =
+                    make_uint2(pq[0] | (pq[1] << 16), pq[2] | (pq[3] << 16));
+            }
+            a.scale[grow * (kD / kG) + j] = sc;
+            a.zero[grow * (kD / kG) + j] = __float2half_rn(z);
         }
-        a.scale[grow * (kD / kG) + j] = sc;
-        a.zero[grow * (kD / kG) + j] = __float2half_rn(z);
     }
 }
 
