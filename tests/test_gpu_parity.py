@@ -378,3 +378,57 @@ def test_residual_kv_append_and_compact():
     oracle.residual_compact(kres, 160, 32)
     oracle.residual_compact(vres, 160, 32)
     assert np.array_equal(host(gk), kres) and np.array_equal(host(gv), vres)
+
+
+# ---------------------------------------------------------------------------
+# maximum sizes: more heads than one grid dimension holds, more (batch, KV
+# head) pairs than the decode has merge counters
+# ---------------------------------------------------------------------------
+
+def test_flush_dequant_fake_quant_beyond_65535_heads():
+    """BH = 65543 heads of one 32-token group each: the launches cut the heads
+    into slices of at most 65535 (grid y). Checked against the oracle on a
+    sample of heads on both sides of each cut (the oracle runs per head)."""
+    BH, S = 65535 + 8, 32
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(11)
+    x = torch.randn((BH, S, 128), generator=gen, device=DEV).to(torch.float16)
+    sample = [0, 1, 65533, 65534, 65535, 65536, BH - 1]
+    xs = host(x[sample])
+    for axis in (0, 1):
+        gs = kv.KiviStore(axis, BH, S, device=DEV)
+        fn = kv.kivi_flush_keys if axis == 0 else kv.kivi_flush_values
+        assert fn(x, 0, gs) == S
+        rs = oracle.Store(axis, len(sample), S, 128, 32, 4)
+        oracle.flush(axis, xs, S, rs)
+        assert np.array_equal(host(gs.codes[sample]), rs.codes)
+        assert np.array_equal(host(gs.scale[sample]).view(np.uint32), rs.scale.view(np.uint32))
+        d = host(kv.kivi_dequant(gs, S)[sample])
+        assert np.array_equal(d.view(np.uint16), oracle.dequant(rs, S).view(np.uint16))
+        ffn = kv.kivi_fake_quant_keys if axis == 0 else kv.kivi_fake_quant_values
+        out, n = ffn(x, 0)
+        assert n == S
+        assert np.array_equal(host(out[sample]).view(np.uint16), d.view(np.uint16))
+        del gs, out
+
+
+def test_decode_beyond_merge_counters():
+    """B * Hkv = 8800 > 8192 pairs: the plan gives every pair one split (no
+    merge counters). Sampled sequences are checked against the oracle."""
+    B, Hkv, Hq, S_q, n_res = 1100, 8, 32, 64, 5
+    assert kv.kivi_decode_workspace_size(B, Hq, Hkv, S_q, n_res) == 0
+    w = synth.Workload("wide", B=B, Hkv=Hkv, Hq=Hq, D=128, S=S_q + n_res, bits=4, G=32, R=0, n_outlier=4,
+                       outlier_scale=8.0, seed=21)
+    k, v, q = synth.prefill_inputs_torch(w, 3, DEV)
+    gk = kv.KiviStore(0, w.BH, S_q, device=DEV)
+    gv = kv.KiviStore(1, w.BH, S_q, device=DEV)
+    kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
+    out = host(kv.kivi_decode_attend(q, gk, gv, S_q, k[:, S_q:], v[:, S_q:], n_res, Hkv, w.sm_scale))
+    kh, vh, qh = host(k), host(v), host(q)
+    for b in (0, 549, 1099):
+        sl = slice(b * Hkv, (b + 1) * Hkv)
+        rk = oracle.flush(0, kh[sl].copy(), S_q, oracle.Store(0, Hkv, S_q, 128, 32, 4))
+        rv = oracle.flush(1, vh[sl].copy(), S_q, oracle.Store(1, Hkv, S_q, 128, 32, 4))
+        ref = oracle.decode_attend(qh[b:b + 1], rk, rv, S_q, np.ascontiguousarray(kh[sl, S_q:]),
+                                   np.ascontiguousarray(vh[sl, S_q:]), n_res, Hkv, w.sm_scale)
+        assert np.max(np.abs(out[b:b + 1] - ref)) <= TOL, b
