@@ -153,6 +153,10 @@ constexpr int kWarpSmem = 2 * kItemBytes;  // two stages
 #define KIVI_FLUSH_BLOCKS_PER_SM 4
 #endif
 constexpr int kBlocksPerSm = KIVI_FLUSH_BLOCKS_PER_SM;  // resident CTAs per SM the grid is sized for
+#ifndef KIVI_FLUSH_KEY_UNROLL
+#define KIVI_FLUSH_KEY_UNROLL 1
+#endif
+constexpr int kKeyUnroll = KIVI_FLUSH_KEY_UNROLL;  // key rows per loop trip (instruction footprint vs overlap)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -288,7 +292,7 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     }
     constexpr int ROWB = kD * BITS / 8;
     uint8_t* crow = a.codes + ((long long)bh * a.s_cap + a.s_off + t0) * ROWB + octet * BITS;
-#pragma unroll 1
+#pragma unroll (kKeyUnroll)
     for (int i = 0; i < nv; ++i) {
         const uint32_t packed = quant8<BITS>(xs[i * 8], z2, r2, s);
         if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
@@ -316,16 +320,17 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
         uint4 x[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) x[k] = xs[(4 * j + k) ^ (row & 7)];
-        __half2 m2 = u32_as_h2(x[0].x), x2 = m2;
+        // min / max as a tree (min and max of fp16 are exact, so the order is free)
+        __half2 mk[4], xk[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                m2 = __hmin2(m2, u32_as_h2(w[i]));
-                x2 = __hmax2(x2, u32_as_h2(w[i]));
-            }
+            const __half2 a = u32_as_h2(x[k].x), b = u32_as_h2(x[k].y), c = u32_as_h2(x[k].z),
+                          d = u32_as_h2(x[k].w);
+            mk[k] = __hmin2(__hmin2(a, b), __hmin2(c, d));
+            xk[k] = __hmax2(__hmax2(a, b), __hmax2(c, d));
         }
+        const __half2 m2 = __hmin2(__hmin2(mk[0], mk[1]), __hmin2(mk[2], mk[3]));
+        const __half2 x2 = __hmax2(__hmax2(xk[0], xk[1]), __hmax2(xk[2], xk[3]));
         const float z = canon(__half2float(__hmin(__low2half(m2), __high2half(m2))));
         const float sc = __fdiv_rn(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z), L);
         const float rc = sc == 0.0f ? 0.0f : __frcp_rn(sc);
