@@ -9,8 +9,9 @@
  *   - the dequantize of the packed store back to fp16,
  *   - the fp16 residual window's append / compact,
  *   - a fused dequantize-and-attend single-token decode over the packed store
- *     plus the residual window (split over the cached tokens, then a
- *     log-sum-exp combine pass).
+ *     plus the residual window (split over the cached tokens; the splits are
+ *     merged by a log-sum-exp combine inside the same launch),
+ *   - fake quantization: the quantize-then-dequantize fp16 tensor in one pass.
  *
  * Sources (page title, section):
  *   [F] VeloxQuant-MLX blog, "A 5.65x Metal Kernel That Made My LLM Exactly 0%
