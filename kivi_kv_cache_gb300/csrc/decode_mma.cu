@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         ps += __shfl_xor_sync(0xffffffffu, ps, 16);
         l_run = fmaf(l_run, corr, ps);
         m_run = m_new;
-        {
+        if (__any_sync(0xffffffffu, corr != 1.f)) {  // the running max moved (x * 1 == x: skip)
             const f32x2 c2 = pk(corr, corr);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -522,10 +522,12 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         ps += __shfl_xor_sync(0xffffffffu, ps, 16);
         l_run = fmaf(l_run, corr, ps);
         m_run = m_new;
+        if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) o[i][k] *= corr;
+                for (int k = 0; k < 4; ++k) o[i][k] *= corr;
+        }
         pbuf[g * 4 + c] = p0;
         pbuf[(g + 8) * 4 + c] = p1;
         __syncwarp();

@@ -342,10 +342,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
         ps += __shfl_xor_sync(0xffffffffu, ps, 16);
         l_run = fmaf(l_run, corr, ps);
         m_run = m_new;
+        if (__any_sync(0xffffffffu, corr != 1.f)) {  // the running max moved (x * 1 == x: skip)
 #pragma unroll
-        for (int i = 0; i < NO; ++i)
+            for (int i = 0; i < NO; ++i)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) o[i][k] *= corr;
+                for (int k = 0; k < 4; ++k) o[i][k] *= corr;
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             if (i < ni) pbuf[(g + 8 * i) * 4 + c] = p[i];
