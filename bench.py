@@ -67,9 +67,9 @@ def parse_args():
     p.add_argument("--stream-steps", type=int, default=3072, help="decode steps of --stream (multiple of 32)")
     p.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
                    help="run one op on one case a few times, untimed (a target for ncu captures)")
-    p.add_argument("--sweep", nargs="?", const="all", choices=["all", "decode"],
+    p.add_argument("--sweep", nargs="?", const="all", choices=["all", "decode", "flush"],
                    help="instead of the step line: per-op GB/s at larger sizes and a decode S_kv sweep "
-                        "('decode': the decode cases only)")
+                        "('decode': the decode cases only; 'flush': flush, dequant and fake quantization only)")
     return p.parse_args()
 
 
@@ -607,7 +607,7 @@ def run_sweep(args):
         return max(8, min(64, int(math.ceil(4 * l2 / max(bytes_each, 1) / 8)) * 8))
 
     # flush / dequant at the long-context 2-bit and qwen8b sizes
-    for name in (("qwen8b", "long2bit") if args.sweep == "all" else ()):
+    for name in (("qwen8b", "long2bit") if args.sweep in ("all", "flush") else ()):
         w = synth.WORKLOADS[name]
         n = kv.kivi_flush_count(w.S, w.R, w.G)
         per = w.BH * w.S * w.D * 2 * 2 + 2 * w.BH * n * (w.D * w.bits // 8 + w.D * 6 // w.G) + w.BH * n * w.D * 4
@@ -632,6 +632,8 @@ def run_sweep(args):
               2 * w.BH * n * w.D * 4, "fake_quant_kv", {"workload": name, "tokens": n, "bits": w.bits, "pool": P})
         del ks, vs, kd, vd, xs
         torch.cuda.empty_cache()
+    if args.sweep == "flush":
+        return
 
     # decode over a packed store + fp16 residual
     cases = [(1, 2080, 158, 4), (1, 4096 - 128, 128, 4), (1, 8192 - 128, 128, 4), (1, 16384 - 128, 128, 4),

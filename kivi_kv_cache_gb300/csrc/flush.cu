@@ -20,18 +20,20 @@
 //  * values: one lane owns whole 32-channel groups of a row (min/max, scale
 //    and the 16-byte code word of a group in one lane, no shuffles); shared
 //    memory chunks are swizzled by row so a warp's reads are conflict-free.
-//  * min/max run on packed fp16 (exact). The quantizer runs on packed fp32x2
-//    IEEE operations. The quotient: y = RN(a * RN(1/s)) lies within 2^-18 of
-//    RN(a/s) for quotients below 16, so rint(y) == rint(RN(a/s)) whenever y is
-//    farther than 2^-14 from every half-integer; one check per 8 elements
+//  * min/max run on packed fp16 (exact). x - zero is one mixed-precision
+//    subtraction (fp16 operand, fp32 result: no separate conversion). The
+//    quotient: with r = RN(1/s), the exact product a * r lies within 2^-19 of
+//    RN(a/s) for quotients below 16, so one fp32x2 fma RN(a r + 2^23) rounds
+//    it half to even and leaves the code in the low byte, and a second fma
+//    measures its distance from that integer; when the distance is within
+//    0.5 - 2^-14 the code equals rint(RN(a/s)). One check per 8 elements
 //    sends the rare near-tie element to an exact IEEE division (out of line).
-//    RN(y + 2^23) rounds half to even and leaves the code in the low byte;
-//    byte permutes pack 8 codes per 32-bit word.
+//    Byte permutes pack 8 codes per 32-bit word.
 //  * work is cut into 4 KB items (a key group's 32 tokens x 64 channels, or
 //    16 value rows); each warp walks the items with a grid stride, staging
 //    two at a time in shared memory with cp.async, so the copy of the next
-//    item overlaps the quantization of the current one, and the quantize
-//    loop is one copy of the code per path (small instruction footprint).
+//    item overlaps the quantization of the current one; the key loop takes
+//    two token rows per trip.
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
@@ -67,38 +69,55 @@ __device__ __forceinline__ uint32_t pack8(const uint32_t (&tb)[8]) {
     }
 }
 
+// RN(x - z) for the two fp16 elements of w (x exact in fp32): one mixed-
+// precision subtraction each, no separate fp16 -> fp32 conversion.
+__device__ __forceinline__ f32x2 sub_h2(uint32_t w, f32x2 z) {
+    const float2 zz = upk(z);
+    float a, b;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "sub.rn.f32.f16 %0, l, %3;\n\tsub.rn.f32.f16 %1, h, %4;\n\t}"
+        : "=f"(a), "=f"(b)
+        : "r"(w), "f"(zz.x), "f"(zz.y));
+    return pk(a, b);
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Codes of 8 fp16 elements (one 16-byte vector), each as the fp32 bit
-// pattern of 2^23 + q in tb[i]. z2/r2: per-element zero and RN(1/scale) as
-// fp32x2 pairs; s: scales.
+// pattern of 2^23 + q in tb[i]. z2/r2: per-element zero and r = RN(1/scale)
+// as fp32x2 pairs; s: scales. With a = RN(x - z), the exact product a * r
+// lies within 2^-19 of RN(a / s) (quotients below 16), so t = RN(a r + 2^23)
+// (one fma) holds q = rint(RN(a / s)) whenever f = RN(a r - (t - 2^23)) is
+// within 0.5 - 2^-14 of zero; the rare element outside that band takes an
+// IEEE division (out of line).
 __device__ __forceinline__ void quant8_codes(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
                                              const float (&s)[8], uint32_t (&tb)[8]) {
     const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
     const f32x2 M2 = pk(kMagic, kMagic);
-    f32x2 a[4], y[4], t[4];
-    float fm = 0.f;
+    f32x2 a[4];
+    float d[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float2 xf = __half22float2(u32_as_h2(w[k]));
-        a[k] = sub2(pk(xf.x, xf.y), z2[k]);
-        y[k] = mul2(a[k], r2[k]);
-        t[k] = add2(y[k], M2);
-        const float2 f = upk(sub2(y[k], sub2(t[k], M2)));
-        fm = fmaxf(fm, fmaxf(fabsf(f.x), fabsf(f.y)));
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float2 tt = upk(t[k]);
+        a[k] = sub_h2(w[k], z2[k]);
+        const f32x2 t = fma2(a[k], r2[k], M2);
+        const float2 f = upk(fma2(a[k], r2[k], sub2(M2, t)));
+        d[2 * k] = fabsf(f.x);
+        d[2 * k + 1] = fabsf(f.y);
+        const float2 tt = upk(t);
         tb[2 * k] = __float_as_uint(tt.x);
         tb[2 * k + 1] = __float_as_uint(tt.y);
     }
-    if (fm > kTieBand) {  // rare: a quotient within 2^-14 of a half-integer
+    const float fm = max3f(max3f(d[0], d[1], d[2]), max3f(d[3], d[4], d[5]), fmaxf(d[6], d[7]));
+    if (fm > kTieBand) {  // rare: a quotient within about 2^-14 of a half-integer
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float2 aa = upk(a[k]), yy = upk(y[k]), tt = upk(t[k]);
-            if (fabsf(__fsub_rn(yy.x, __fsub_rn(tt.x, kMagic))) > kTieBand)
-                tb[2 * k] = exact_code_bits(aa.x, s[2 * k]);
-            if (fabsf(__fsub_rn(yy.y, __fsub_rn(tt.y, kMagic))) > kTieBand)
-                tb[2 * k + 1] = exact_code_bits(aa.y, s[2 * k + 1]);
+            const float2 aa = upk(a[k]);
+            if (d[2 * k] > kTieBand) tb[2 * k] = exact_code_bits(aa.x, s[2 * k]);
+            if (d[2 * k + 1] > kTieBand) tb[2 * k + 1] = exact_code_bits(aa.y, s[2 * k + 1]);
         }
     }
 }
@@ -154,7 +173,7 @@ constexpr int kWarpSmem = 2 * kItemBytes;  // two stages
 #endif
 constexpr int kBlocksPerSm = KIVI_FLUSH_BLOCKS_PER_SM;  // resident CTAs per SM the grid is sized for
 #ifndef KIVI_FLUSH_KEY_UNROLL
-#define KIVI_FLUSH_KEY_UNROLL 1
+#define KIVI_FLUSH_KEY_UNROLL 2
 #endif
 constexpr int kKeyUnroll = KIVI_FLUSH_KEY_UNROLL;  // key rows per loop trip (instruction footprint vs overlap)
 
@@ -292,12 +311,12 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     }
     constexpr int ROWB = kD * BITS / 8;
     uint8_t* crow = a.codes + ((long long)bh * a.s_cap + a.s_off + t0) * ROWB + octet * BITS;
-#pragma unroll (kKeyUnroll)
-    for (int i = 0; i < nv; ++i) {
-        const uint32_t packed = quant8<BITS>(xs[i * 8], z2, r2, s);
+    auto store_row = [&](int i, uint32_t packed) {
         if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
         else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
-    }
+    };
+#pragma unroll (kKeyUnroll)
+    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS>(xs[i * 8], z2, r2, s));
 }
 
 // values: lane = 16 jp + row; the lane quantizes the groups j = 2 jp and
@@ -342,15 +361,18 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
 #pragma unroll
             for (int k = 0; k < 4; ++k) frow[k] = fake8(x[k], z2, r2, sv);
         } else {
+            auto store_group = [&](const uint32_t (&pq)[4]) {
+                if (BITS == 4) {
+                    *reinterpret_cast<uint4*>(a.codes + grow * 64 + 16 * j) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
+                } else {
+                    *reinterpret_cast<uint2*>(a.codes + grow * 32 + 8 * j) =
+                        make_uint2(pq[0] | (pq[1] << 16), pq[2] | (pq[3] << 16));
+                }
+            };
             uint32_t pq[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS>(x[k], z2, r2, sv);
-            if (BITS == 4) {
-                *reinterpret_cast<uint4*>(a.codes + grow * 64 + 16 * j) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
-            } else {
-                *reinterpret_cast<uint2*>(a.codes + grow * 32 + 8 * j) =
-                    make_uint2(pq[0] | (pq[1] << 16), pq[2] | (pq[3] << 16));
-            }
+            store_group(pq);
             a.scale[grow * (kD / kG) + j] = sc;
             a.zero[grow * (kD / kG) + j] = __float2half_rn(z);
         }
@@ -363,19 +385,18 @@ template <int BITS, bool FAKE>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint8_t* base = smem + warp * kWarpSmem;
-    uint8_t* st[2] = {base, base + kItemBytes};
+    uint8_t* const base = smem + warp * kWarpSmem;
     const int total = it.key_items + it.val_items;
     const int stride = gridDim.x * (kThreads / 32);
     int item = blockIdx.x * (kThreads / 32) + warp;
     pdl_wait();
-    if (item < total) fetch_item(k, v, it, item, st[0], lane);
+    if (item < total) fetch_item(k, v, it, item, base, lane);
     cp_async_commit();
-    if (item + stride < total) fetch_item(k, v, it, item + stride, st[1], lane);
+    if (item + stride < total) fetch_item(k, v, it, item + stride, base + kItemBytes, lane);
     cp_async_commit();
     pdl_trigger();
     for (int n = 0; item < total; item += stride, ++n) {
-        uint8_t* S = st[n & 1];
+        uint8_t* S = base + (n & 1) * kItemBytes;  // stage n mod 2
         cp_async_wait1();
         __syncwarp();
         if (item < it.key_items) key_item<BITS, FAKE>(k, it, item, S, lane);

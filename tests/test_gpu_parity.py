@@ -110,6 +110,11 @@ def adversarial(rng, BH, S):
     x[1 % BH, 9, ::3] = np.float16(-6e-8)
     x[1 % BH, 10, :] = (rng.integers(-2, 3, 128) * 2.0 ** -24).astype(np.float16)
     x[0, 40:72, 3] = (np.arange(32) * 1.5 - 3).astype(np.float16)
+    # exact half-integer quotients: groups spanning [0, 15] on a 0.5 grid give
+    # scale 1 (4-bit) or 5 (2-bit), so x = k + 0.5 (4-bit) or 2.5, 7.5, 12.5
+    # (2-bit) round half to even
+    x[0, 11, :] = (np.arange(128) % 31 * 0.5).astype(np.float16)
+    x[0, :32, 4] = (np.arange(32) % 31 * 0.5).astype(np.float16)
     return x
 
 
