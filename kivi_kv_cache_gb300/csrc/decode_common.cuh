@@ -54,12 +54,33 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t
         : "r"(w));
 }
 
-// fp16 hi (lo == false) or lo (lo == true) part of the pair (x, y)
+#ifndef KIVI_DECODE_SPLIT_FMA
+#define KIVI_DECODE_SPLIT_FMA 1
+#endif
+
+// fp16 hi (lo == false) or lo (lo == true) part of the pair (x, y):
+// hi = fp16(x), lo = fp16(x - hi) (x - hi is exact in fp32). One mixed-
+// precision fma per element, x + hi * m with the fp16 m = -1 (lo) or 0 (hi),
+// gives x - hi or x itself, and one conversion rounds either to fp16.
 __device__ __forceinline__ uint32_t split_pair(float x, float y, bool lo) {
+#if KIVI_DECODE_SPLIT_FMA
+    const unsigned short m = lo ? 0xbc00 : 0;  // fp16 -1 or +0
+    uint32_t r;
+    asm("{\n\t.reg .b32 h;\n\t.reg .b16 hl, hh;\n\t.reg .f32 rx, ry;\n\t"
+        "cvt.rn.f16x2.f32 h, %2, %1;\n\t"
+        "mov.b32 {hl, hh}, h;\n\t"
+        "fma.rn.f32.f16 rx, hl, %3, %1;\n\t"
+        "fma.rn.f32.f16 ry, hh, %3, %2;\n\t"
+        "cvt.rn.f16x2.f32 %0, ry, rx;\n\t}"
+        : "=r"(r)
+        : "f"(x), "f"(y), "h"(m));
+    return r;
+#else
     const __half2 h = __floats2half2_rn(x, y);
     const float2 hf = __half22float2(h);
     const __half2 l = __floats2half2_rn(__fsub_rn(x, hf.x), __fsub_rn(y, hf.y));
     return lo ? h2_as_u32(l) : h2_as_u32(h);
+#endif
 }
 
 // 2^e as fp32 for e in [-126, 127]

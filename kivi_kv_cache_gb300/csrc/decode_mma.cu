@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     const int g = lane >> 2, c = lane & 3;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int bh = b * a.Hkv + hk, h0 = hk * GQ;
-    uint8_t* st[2] = {smem + warp * kWarpSmem, smem + warp * kWarpSmem + kStage};
+    uint8_t* const st0 = smem + warp * kWarpSmem;  // two stages: st0, st0 + kStage
     float* pbuf = reinterpret_cast<float*>(smem + LY::kPbufOff + warp * 512);  // [token][head]
     float* q_s = reinterpret_cast<float*>(smem + LY::kQOff);                   // [head][channel]
     float* misc = reinterpret_cast<float*>(smem + LY::kMiscOff);
@@ -152,9 +152,9 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
 
     pdl_wait();
     // start the first two store tiles' copies, then stage q while they fly
-    if (ns > 0) fetch_store_tile<BITS>(a, bh, w0, st[0], lane);
+    if (ns > 0) fetch_store_tile<BITS>(a, bh, w0, st0, lane);
     cp_async_commit();
-    if (ns > 1) fetch_store_tile<BITS>(a, bh, w0 + 1, st[1], lane);
+    if (ns > 1) fetch_store_tile<BITS>(a, bh, w0 + 1, st0 + kStage, lane);
     cp_async_commit();
 
     // q * score_scale for the GQ heads of this KV head (heads >= GQ are zero)
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     // ---------------------------- store tiles ----------------------------
     for (int it = 0; it < ns; ++it) {
         const int tile = w0 + it;
-        uint8_t* S = st[it & 1];
+        uint8_t* S = st0 + (it & 1) * kStage;
         cp_async_wait<1>();
         __syncwarp();
         const int nvalid = min(32, a.S_q - tile * 32);
@@ -482,12 +482,12 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     for (int rt = r_begin; rt < w1; ++rt) {
         const int rtile = rt - a.n_store_tiles;
         const int nvalid = min(kResTok, a.n_res - rtile * kResTok);
-        fetch_res_tile(a, bh, rtile, nvalid, st[0], st[1], lane);
+        fetch_res_tile(a, bh, rtile, nvalid, st0, st0 + kStage, lane);
         cp_async_commit();
         cp_async_wait<0>();
         __syncwarp();
-        const uint8_t* KR = st[0];
-        const uint8_t* VR = st[1];
+        const uint8_t* KR = st0;
+        const uint8_t* VR = st0 + kStage;
         float sc[4];
         {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -586,7 +586,7 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
 
     // ---------------------------- merge the warps ----------------------------
     __syncthreads();  // every warp is done with its stages
-    float* Ow = reinterpret_cast<float*>(st[0]);          // [4 heads][128] of this warp
+    float* Ow = reinterpret_cast<float*>(st0);          // [4 heads][128] of this warp
     float* ml = misc + 16;                                 // [warp][head][2]
     {
         const float sc9 = 512.f;  // o holds sum p s c 2^-9 + pz 2^-9
