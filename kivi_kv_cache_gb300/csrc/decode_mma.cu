@@ -49,10 +49,6 @@
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
-#ifndef KIVI_DECODE_SUBN
-#define KIVI_DECODE_SUBN 1
-#endif
-
 namespace kivi {
 
 namespace {
@@ -78,6 +74,7 @@ constexpr int kKC = 0, kVC = 2048, kKS = 4096, kKZ = 4672, kVS = 4928, kVZ = 544
 constexpr int kResTok = kResTileTokensMma;  // residual tile: 16 K rows in stage 0, 16 V rows in stage 1
 
 __device__ __forceinline__ int padc(int ch) { return ch + ((ch >> 5) << 2); }
+
 
 // ---------------------------------------------------------------------------
 // tile staging
@@ -462,10 +459,19 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                 uint32_t xl[2][4], xh[2][4];  // [u][token block] -> (row g, row g+8) halves
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
+#if KIVI_DECODE_SUBN
+                    // bytes of W: token 2c (channels 4g, 4g+1 | 4g+2, 4g+3), token 2c+1 (same)
+                    const uint32_t Ws = W[q] >> 8;
+                    xl[0][q] = W[q] & 0x000f000fu;  // channel 4g, units 2^-24
+                    xh[0][q] = Ws & 0x000f000fu;    // channel 4g+2
+                    xl[1][q] = W[q] & 0x00f000f0u;  // channel 4g+1, units 2^-20
+                    xh[1][q] = Ws & 0x00f000f0u;    // channel 4g+3
+#else
                     const uint32_t E = __byte_perm(W[q] & 0x0f0f0f0fu, 0, 0x3120);
                     const uint32_t O = __byte_perm((W[q] >> 4) & 0x0f0f0f0fu, 0, 0x3120);
                     e4m3x4_to_f16(E, xl[0][q], xh[0][q]);
                     e4m3x4_to_f16(O, xl[1][q], xh[1][q]);
+#endif
                 }
 #pragma unroll
                 for (int u = 0; u < 2; ++u)
@@ -478,8 +484,8 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
             for (int j = 0; j < 4; ++j)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    o[2 * j + u][0] += pz[j] * (1.0f / 512.f);  // o is kept in units of 2^-9 (codes)
-                    o[2 * j + u][2] += pz[j] * (1.0f / 512.f);
+                    o[2 * j + u][0] += pz[j] * kOUnit4[u];  // o[2j + u] is kept in units of kOUnit4[u]
+                    o[2 * j + u][2] += pz[j] * kOUnit4[u];
                 }
         } else {
             // o[4h + k]: rows g -> channel 64h + 8g + k, g+8 -> 64h + 8g + 4 + k;
@@ -493,8 +499,15 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                 for (int k = 0; k < 4; ++k) {
                     uint32_t xl[4], xh[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                    for (int q = 0; q < 4; ++q) {
+#if KIVI_DECODE_SUBN
+                        const uint32_t mk = 0x00030003u << (2 * k);  // channel 8g + k | 8g + 4 + k, units 4^k 2^-24
+                        xl[q] = W[q] & mk;
+                        xh[q] = (W[q] >> 8) & mk;
+#else
                         e4m3x4_to_f16(__byte_perm((W[q] >> (2 * k)) & 0x03030303u, 0, 0x3120), xl[q], xh[q]);
+#endif
+                    }
                     const bool first = g < 4;
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
@@ -511,8 +524,8 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                 const float pzj = g < 4 ? pz[2 * hc] : pz[2 * hc + 1];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    o[4 * hc + k][0] += pzj * (1.0f / 512.f);
-                    o[4 * hc + k][2] += pzj * (1.0f / 512.f);
+                    o[4 * hc + k][0] += pzj * kOUnit2[k];
+                    o[4 * hc + k][2] += pzj * kOUnit2[k];
                 }
             }
         }
@@ -599,7 +612,7 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                     mma16816(tmp, __byte_perm(rv[0].x, rv[1].x, sel), __byte_perm(rv[0].y, rv[1].y, sel),
                              __byte_perm(rv[2].x, rv[3].x, sel), __byte_perm(rv[2].y, rv[3].y, sel), bp0, bp1);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) o[2 * j + u][k] = fmaf(tmp[k], 1.0f / 512.f, o[2 * j + u][k]);
+                    for (int k = 0; k < 4; ++k) o[2 * j + u][k] = fmaf(tmp[k], kOUnit4[u], o[2 * j + u][k]);
                 }
             }
         } else {
@@ -624,7 +637,7 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                     mma16816(tmp, __byte_perm(rv[0][wa], rv[1][wa], sel), __byte_perm(rv[0][wb], rv[1][wb], sel),
                              __byte_perm(rv[2][wa], rv[3][wa], sel), __byte_perm(rv[2][wb], rv[3][wb], sel), bp0, bp1);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[4 * hc + k][e] = fmaf(tmp[e], 1.0f / 512.f, o[4 * hc + k][e]);
+                    for (int e = 0; e < 4; ++e) o[4 * hc + k][e] = fmaf(tmp[e], kOUnit2[k], o[4 * hc + k][e]);
                 }
             }
         }
@@ -636,22 +649,24 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     float* Ow = reinterpret_cast<float*>(st0);          // [4 heads][128] of this warp
     float* ml = misc + 16;                                 // [warp][head][2]
     {
-        const float sc9 = 512.f;  // o holds sum p s c 2^-9 + pz 2^-9
+        // o holds (sum p s c + pz) in units of kOUnit4 / kOUnit2
         if (BITS == 4) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    Ow[c * kD + 32 * j + 4 * g + u] = (o[2 * j + u][0] + o[2 * j + u][1]) * sc9;
-                    Ow[c * kD + 32 * j + 4 * g + 2 + u] = (o[2 * j + u][2] + o[2 * j + u][3]) * sc9;
+                    const float sc = 1.0f / kOUnit4[u];
+                    Ow[c * kD + 32 * j + 4 * g + u] = (o[2 * j + u][0] + o[2 * j + u][1]) * sc;
+                    Ow[c * kD + 32 * j + 4 * g + 2 + u] = (o[2 * j + u][2] + o[2 * j + u][3]) * sc;
                 }
         } else {
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    Ow[c * kD + 64 * hc + 8 * g + k] = (o[4 * hc + k][0] + o[4 * hc + k][1]) * sc9;
-                    Ow[c * kD + 64 * hc + 8 * g + 4 + k] = (o[4 * hc + k][2] + o[4 * hc + k][3]) * sc9;
+                    const float sc = 1.0f / kOUnit2[k];
+                    Ow[c * kD + 64 * hc + 8 * g + k] = (o[4 * hc + k][0] + o[4 * hc + k][1]) * sc;
+                    Ow[c * kD + 64 * hc + 8 * g + 4 + k] = (o[4 * hc + k][2] + o[4 * hc + k][3]) * sc;
                 }
         }
         if (g == 0) {
