@@ -1,6 +1,7 @@
 // decode_common.cuh -- PTX helpers shared by the decode kernels: cp.async
-// staging, ldmatrix, the m16n8k16 fp16 MMA, exact code conversion, the fp16
-// hi/lo split of fp32 operands, and thread-block cluster access.
+// staging, ldmatrix, the m16n8k16 fp16 MMA, exact code operands (fp8 e4m3
+// conversion, or fp16 subnormals by masking), the fp16 hi/lo split of fp32
+// operands, and thread-block cluster access.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -83,24 +84,14 @@ __device__ __forceinline__ uint32_t split_pair(float x, float y, bool lo) {
 #endif
 }
 
-// Code operands of the MMAs. With KIVI_DECODE_SUBN a code enters as the
-// fp16 subnormal it forms when masked in place: a nibble at bit 4j of a half
-// is c 16^j 2^-24, a crumb at bit 2j is c 4^j 2^-24 (fp16 subnormals are
-// exact MMA operands); the per-position factor is folded into the other
-// operand or into the accumulator's units. Otherwise codes are converted as
-// fp8 e4m3 (c 2^-9).
-#ifndef KIVI_DECODE_SUBN
-#define KIVI_DECODE_SUBN 1
-#endif
-// Units of the P.V accumulators (the value of a code c in the MMA): 4-bit
-// nibble position u (kOUnit4[u]), 2-bit crumb position k (kOUnit2[k]).
-#if KIVI_DECODE_SUBN
+// Code operands of the decode MMAs: a code masked in place within a 16-bit
+// half is an fp16 subnormal, exact as an MMA operand: a nibble at bit 4j is
+// c 16^j 2^-24, a crumb at bit 2j is c 4^j 2^-24. The per-position factor
+// 16^j or 4^j is folded into the other operand (scores) or into the units of
+// the accumulator (P.V): kOUnit4[u] for nibble position u, kOUnit2[k] for
+// crumb position k.
 __device__ constexpr float kOUnit4[2] = {0x1p-24f, 0x1p-20f};
 __device__ constexpr float kOUnit2[4] = {0x1p-24f, 0x1p-22f, 0x1p-20f, 0x1p-18f};
-#else
-__device__ constexpr float kOUnit4[2] = {0x1p-9f, 0x1p-9f};
-__device__ constexpr float kOUnit2[4] = {0x1p-9f, 0x1p-9f, 0x1p-9f, 0x1p-9f};
-#endif
 
 // 2^e as fp32 for e in [-126, 127]
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }

@@ -18,9 +18,12 @@
 //     sum_t p_t vhat_td = sum_t (p_t s_tj) c_td + sum_t p_t z_tj
 // so the codes c are one MMA operand, exactly representable in fp16, and the
 // fp32 products q_d s_d / p_t s_tj the other. Exactness of the operands:
-//   * a code nibble (or 2-bit crumb) alone in a byte, read as fp8 e4m3, is
-//     c * 2^-9 exactly (subnormal for c < 8, normal 2^-6 (1 + (c-8)/8) for
-//     c >= 8), so cvt.rn.f16x2.e4m3x2 turns two codes into fp16 in one step;
+//   * a code masked in place within a 16-bit half is an fp16 subnormal: a
+//     nibble at bit 4j is c 16^j 2^-24, a crumb at bit 2j is c 4^j 2^-24, so
+//     one AND turns two codes into an exact fp16 pair; the factor 16^j or 4^j
+//     goes into the q_d s_d operand (scores) or into the units of the P.V
+//     accumulator (one per nibble or crumb position), and the tensor cores
+//     take subnormal fp16 operands exactly;
 //   * each fp32 operand is split into fp16 hi + lo (hi = fp16(x), lo =
 //     fp16(x - hi)), carried as two MMA columns per query head: n = 2h + part.
 //     The sum keeps ~22 significant bits, far below the 2e-3 output budget;
@@ -216,24 +219,17 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         }
         const int E = safe_exp(qmax * smax);
         const float fB = pow2i(E);  // B = q s 2^E
-#if KIVI_DECODE_SUBN
-        // codes enter the MMA as fp16 subnormals c 2^-24 (a masked nibble or
-        // crumb at bit 4j of a half is c 16^j 2^-24 (4-bit) or at bit 2j,
-        // c 4^j 2^-24 (2-bit)); B of that channel carries 16^-j or 4^-j
+        // codes enter the MMA as fp16 subnormals (a nibble at bit 4j of a half
+        // is c 16^j 2^-24, a crumb at bit 2j is c 4^j 2^-24); B of that
+        // channel carries 16^-j or 4^-j
         const float fC = pow2i(24 - E);  // score = C 2^(24-E)
         const f32x2 fB2 = BITS == 4 ? pk(fB, fB * 0.0625f) : pk(fB, fB * 0.25f);
         const f32x2 fB2h = pk(fB * 0.0625f, fB * 0.015625f);  // 2-bit crumbs 2, 3 of a byte
-#else
-        const float fC = pow2i(9 - E);  // score = C 2^(9-E) (codes are c 2^-9)
-        const f32x2 fB2 = pk(fB, fB);
-        const f32x2 fB2h = fB2;
-#endif
         uint32_t bq[8][2];
         if (BITS == 4) {
             // word m of this lane's 16-byte chunk: channels 32c + 8m + {0..7}
-            // (channel 8m + j in nibble j); e4m3 conversion: K-step 2m pairs
-            // channels (0,2),(4,6), K-step 2m+1 pairs (1,3),(5,7); subnormal
-            // codes: K-step 2m pairs (0,4),(2,6), K-step 2m+1 pairs (1,5),(3,7)
+            // (channel 8m + j in nibble j); K-step 2m pairs channels (0,4),(2,6),
+            // K-step 2m+1 pairs (1,5),(3,7)
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const float4 sa = *reinterpret_cast<const float4*>(KS + padc(32 * c + 8 * m));
@@ -244,23 +240,15 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                 const float2 v23 = upk(mul2(mul2(pk(qa.z, qa.w), pk(sa.z, sa.w)), fB2));
                 const float2 v45 = upk(mul2(mul2(pk(qb.x, qb.y), pk(sb.x, sb.y)), fB2));
                 const float2 v67 = upk(mul2(mul2(pk(qb.z, qb.w), pk(sb.z, sb.w)), fB2));
-#if KIVI_DECODE_SUBN
                 bq[2 * m][0] = split_pair(v01.x, v45.x, lo_part);
                 bq[2 * m][1] = split_pair(v23.x, v67.x, lo_part);
                 bq[2 * m + 1][0] = split_pair(v01.y, v45.y, lo_part);
                 bq[2 * m + 1][1] = split_pair(v23.y, v67.y, lo_part);
-#else
-                bq[2 * m][0] = split_pair(v01.x, v23.x, lo_part);
-                bq[2 * m][1] = split_pair(v45.x, v67.x, lo_part);
-                bq[2 * m + 1][0] = split_pair(v01.y, v23.y, lo_part);
-                bq[2 * m + 1][1] = split_pair(v45.y, v67.y, lo_part);
-#endif
             }
         } else {
             // word m (4 bytes) of this lane's 8 bytes: channels 32c + 16m + {0..15}
-            // (channel 16m + 4b + j in crumb j of byte b); e4m3 conversion:
-            // K-step 4m + k pairs channels (k, k+4), (k+8, k+12); subnormal
-            // codes: (k, k+8), (k+4, k+12)
+            // (channel 16m + 4b + j in crumb j of byte b); K-step 4m + k pairs
+            // channels (k, k+8), (k+4, k+12)
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 float v[16];
@@ -277,13 +265,8 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                 }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-#if KIVI_DECODE_SUBN
                     bq[4 * m + k][0] = split_pair(v[k], v[k + 8], lo_part);
                     bq[4 * m + k][1] = split_pair(v[k + 4], v[k + 12], lo_part);
-#else
-                    bq[4 * m + k][0] = split_pair(v[k], v[k + 4], lo_part);
-                    bq[4 * m + k][1] = split_pair(v[k + 8], v[k + 12], lo_part);
-#endif
                 }
             }
         }
@@ -325,21 +308,11 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                 const uint32_t w0v[4] = {x0.x, x0.y, x0.z, x0.w}, w1v[4] = {x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-#if KIVI_DECODE_SUBN
                     const uint32_t u0 = w0v[m], u1 = w1v[m], u0s = u0 >> 8, u1s = u1 >> 8;
                     mma16816(acc, u0 & 0x000f000fu, u1 & 0x000f000fu, u0s & 0x000f000fu, u1s & 0x000f000fu,
                              bq[2 * m][0], bq[2 * m][1]);
                     mma16816(acc, u0 & 0x00f000f0u, u1 & 0x00f000f0u, u0s & 0x00f000f0u, u1s & 0x00f000f0u,
                              bq[2 * m + 1][0], bq[2 * m + 1][1]);
-#else
-                    uint32_t e0l, e0h, e1l, e1h, o0l, o0h, o1l, o1h;
-                    e4m3x4_to_f16(w0v[m] & 0x0f0f0f0fu, e0l, e0h);
-                    e4m3x4_to_f16(w1v[m] & 0x0f0f0f0fu, e1l, e1h);
-                    e4m3x4_to_f16((w0v[m] >> 4) & 0x0f0f0f0fu, o0l, o0h);
-                    e4m3x4_to_f16((w1v[m] >> 4) & 0x0f0f0f0fu, o1l, o1h);
-                    mma16816(acc, e0l, e1l, e0h, e1h, bq[2 * m][0], bq[2 * m][1]);
-                    mma16816(acc, o0l, o1l, o0h, o1h, bq[2 * m + 1][0], bq[2 * m + 1][1]);
-#endif
                 }
             } else {
                 const uint2 x0 = *reinterpret_cast<const uint2*>(KC + r0 * 32 + 8 * c);
@@ -347,22 +320,12 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                 const uint32_t w0v[2] = {x0.x, x0.y}, w1v[2] = {x1.x, x1.y};
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
-#if KIVI_DECODE_SUBN
                     const uint32_t u0 = w0v[m], u1 = w1v[m], u0s = u0 >> 8, u1s = u1 >> 8;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t mk = 0x00030003u << (2 * k);
                         mma16816(acc, u0 & mk, u1 & mk, u0s & mk, u1s & mk, bq[4 * m + k][0], bq[4 * m + k][1]);
                     }
-#else
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t p0l, p0h, p1l, p1h;
-                        e4m3x4_to_f16((w0v[m] >> (2 * k)) & 0x03030303u, p0l, p0h);
-                        e4m3x4_to_f16((w1v[m] >> (2 * k)) & 0x03030303u, p1l, p1h);
-                        mma16816(acc, p0l, p1l, p0h, p1h, bq[4 * m + k][0], bq[4 * m + k][1]);
-                    }
-#endif
                 }
             }
             const int t0 = mt * 16 + g;
@@ -459,19 +422,12 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                 uint32_t xl[2][4], xh[2][4];  // [u][token block] -> (row g, row g+8) halves
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-#if KIVI_DECODE_SUBN
                     // bytes of W: token 2c (channels 4g, 4g+1 | 4g+2, 4g+3), token 2c+1 (same)
                     const uint32_t Ws = W[q] >> 8;
                     xl[0][q] = W[q] & 0x000f000fu;  // channel 4g, units 2^-24
                     xh[0][q] = Ws & 0x000f000fu;    // channel 4g+2
                     xl[1][q] = W[q] & 0x00f000f0u;  // channel 4g+1, units 2^-20
                     xh[1][q] = Ws & 0x00f000f0u;    // channel 4g+3
-#else
-                    const uint32_t E = __byte_perm(W[q] & 0x0f0f0f0fu, 0, 0x3120);
-                    const uint32_t O = __byte_perm((W[q] >> 4) & 0x0f0f0f0fu, 0, 0x3120);
-                    e4m3x4_to_f16(E, xl[0][q], xh[0][q]);
-                    e4m3x4_to_f16(O, xl[1][q], xh[1][q]);
-#endif
                 }
 #pragma unroll
                 for (int u = 0; u < 2; ++u)
@@ -500,13 +456,9 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                     uint32_t xl[4], xh[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-#if KIVI_DECODE_SUBN
                         const uint32_t mk = 0x00030003u << (2 * k);  // channel 8g + k | 8g + 4 + k, units 4^k 2^-24
                         xl[q] = W[q] & mk;
                         xh[q] = (W[q] >> 8) & mk;
-#else
-                        e4m3x4_to_f16(__byte_perm((W[q] >> (2 * k)) & 0x03030303u, 0, 0x3120), xl[q], xh[q]);
-#endif
                     }
                     const bool first = g < 4;
 #pragma unroll
@@ -538,7 +490,7 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
 
     // ---------------------------- residual tiles ----------------------------
     // kResTok fp16 K and V rows per tile. Their P.V is accumulated in fp32 per
-    // 16-channel block and added into o (store-tile channel layout, units of 2^-9).
+    // 16-channel block and added into o (store-tile channel layout, o's units).
     for (int rt = r_begin; rt < w1; ++rt) {
         const int rtile = rt - a.n_store_tiles;
         const int nvalid = min(kResTok, a.n_res - rtile * kResTok);

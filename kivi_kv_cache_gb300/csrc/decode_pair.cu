@@ -9,9 +9,10 @@
 // tokens are split across CTAs and merged by a log-sum-exp combine).
 //
 // The arithmetic is that of decode_mma.cu: the affine dequant is folded out
-// of both contractions, codes enter the tensor cores exactly as e4m3 -> fp16
-// (c * 2^-9), and the fp32 products q_d s_d and p_t s_tj enter as fp16 hi/lo
-// column pairs, scaled by a power of two per tile and warp.
+// of both contractions, codes enter the tensor cores exactly as the fp16
+// subnormals they form when masked in place, and the fp32 products q_d s_d
+// and p_t s_tj enter as fp16 hi/lo column pairs, scaled by a power of two per
+// tile and warp.
 //
 // Work split: a CTA has 4 warp pairs (8 warps; two CTAs per SM). A pair owns
 // a contiguous run of tiles
@@ -208,50 +209,31 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
             smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
             const int E = safe_exp(qmax * smax);
             const float fB = pow2i(E);
-#if KIVI_DECODE_SUBN
-            // subnormal codes: channel i of the word sits at nibble i % 8 (4-bit) or crumb i % 4
-            // (2-bit) of its byte pair, worth 16^(i % 2) or 4^(i % 4) times c 2^-24
+            // codes enter as fp16 subnormals: channel i's nibble (4-bit) or crumb (2-bit) is worth
+            // 16^(i % 2) or 4^(i % 4) times c 2^-24, so its B carries the inverse factor
             const float fC = pow2i(24 - E);
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 v[i] = q16[i] * s16[i] * (BITS == 4 ? ((i & 1) ? fB * 0.0625f : fB) : fB * kOUnit2[0] / kOUnit2[i & 3]);
-#else
-            const float fC = pow2i(9 - E);  // codes enter as c 2^-9
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = q16[i] * s16[i] * fB;
-#endif
             uint32_t bq[4][2];  // K-step ks
             if (BITS == 4) {
-                // word m: channels cb + 8m + 0..7 (nibble j: channel 8m + j); e4m3 codes: K-step
-                // 2m pairs (0,2),(4,6), 2m+1 pairs (1,3),(5,7); subnormal codes: (0,4),(2,6) and (1,5),(3,7)
+                // word m: channels cb + 8m + 0..7 (nibble j: channel 8m + j); K-step 2m pairs
+                // channels (0,4),(2,6), K-step 2m+1 pairs (1,5),(3,7)
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
-#if KIVI_DECODE_SUBN
                     bq[2 * m][0] = split_pair(v[8 * m + 0], v[8 * m + 4], lo_part);
                     bq[2 * m][1] = split_pair(v[8 * m + 2], v[8 * m + 6], lo_part);
                     bq[2 * m + 1][0] = split_pair(v[8 * m + 1], v[8 * m + 5], lo_part);
                     bq[2 * m + 1][1] = split_pair(v[8 * m + 3], v[8 * m + 7], lo_part);
-#else
-                    bq[2 * m][0] = split_pair(v[8 * m + 0], v[8 * m + 2], lo_part);
-                    bq[2 * m][1] = split_pair(v[8 * m + 4], v[8 * m + 6], lo_part);
-                    bq[2 * m + 1][0] = split_pair(v[8 * m + 1], v[8 * m + 3], lo_part);
-                    bq[2 * m + 1][1] = split_pair(v[8 * m + 5], v[8 * m + 7], lo_part);
-#endif
                 }
             } else {
-                // one word: channels cb + 0..15 (crumb j of byte b: channel 4b + j); e4m3 codes:
-                // K-step k pairs (k, k+4), (k+8, k+12); subnormal codes: (k, k+8), (k+4, k+12)
+                // one word: channels cb + 0..15 (crumb j of byte b: channel 4b + j); K-step k
+                // pairs channels (k, k+8), (k+4, k+12)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-#if KIVI_DECODE_SUBN
                     bq[k][0] = split_pair(v[k], v[k + 8], lo_part);
                     bq[k][1] = split_pair(v[k + 4], v[k + 12], lo_part);
-#else
-                    bq[k][0] = split_pair(v[k], v[k + 4], lo_part);
-                    bq[k][1] = split_pair(v[k + 8], v[k + 12], lo_part);
-#endif
                 }
             }
             // ---- sum_d q_d z_d of head c over this warp's 64 channels ----
@@ -287,36 +269,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
                     const uint32_t w0v[2] = {x0.x, x0.y}, w1v[2] = {x1.x, x1.y};
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
-#if KIVI_DECODE_SUBN
                         const uint32_t u0 = w0v[m], u1 = w1v[m], u0s = u0 >> 8, u1s = u1 >> 8;
                         mma16816(acc, u0 & 0x000f000fu, u1 & 0x000f000fu, u0s & 0x000f000fu, u1s & 0x000f000fu,
                                  bq[2 * m][0], bq[2 * m][1]);
                         mma16816(acc, u0 & 0x00f000f0u, u1 & 0x00f000f0u, u0s & 0x00f000f0u, u1s & 0x00f000f0u,
                                  bq[2 * m + 1][0], bq[2 * m + 1][1]);
-#else
-                        uint32_t e0l, e0h, e1l, e1h, o0l, o0h, o1l, o1h;
-                        e4m3x4_to_f16(w0v[m] & 0x0f0f0f0fu, e0l, e0h);
-                        e4m3x4_to_f16(w1v[m] & 0x0f0f0f0fu, e1l, e1h);
-                        e4m3x4_to_f16((w0v[m] >> 4) & 0x0f0f0f0fu, o0l, o0h);
-                        e4m3x4_to_f16((w1v[m] >> 4) & 0x0f0f0f0fu, o1l, o1h);
-                        mma16816(acc, e0l, e1l, e0h, e1h, bq[2 * m][0], bq[2 * m][1]);
-                        mma16816(acc, o0l, o1l, o0h, o1h, bq[2 * m + 1][0], bq[2 * m + 1][1]);
-#endif
                     }
                 } else {
                     const uint32_t w0 = *reinterpret_cast<const uint32_t*>(S + kKC + r0 * 32 + 16 * hf + 4 * c);
                     const uint32_t w1 = *reinterpret_cast<const uint32_t*>(S + kKC + r1 * 32 + 16 * hf + 4 * c);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-#if KIVI_DECODE_SUBN
                         const uint32_t mk = 0x00030003u << (2 * k);
                         mma16816(acc, w0 & mk, w1 & mk, (w0 >> 8) & mk, (w1 >> 8) & mk, bq[k][0], bq[k][1]);
-#else
-                        uint32_t p0l, p0h, p1l, p1h;
-                        e4m3x4_to_f16((w0 >> (2 * k)) & 0x03030303u, p0l, p0h);
-                        e4m3x4_to_f16((w1 >> (2 * k)) & 0x03030303u, p1l, p1h);
-                        mma16816(acc, p0l, p1l, p0h, p1h, bq[k][0], bq[k][1]);
-#endif
                     }
                 }
                 sc[2 * mt] = fmaf(acc[0] + acc[1], fC, qz_c);
@@ -441,17 +406,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
                     uint32_t xl[2][4], xh[2][4];
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
-#if KIVI_DECODE_SUBN
                         // bytes of W: token 2c (channels 4g, 4g+1 | 4g+2, 4g+3), token 2c+1 (same)
                         const uint32_t Ws = W[qq] >> 8;
                         xl[0][qq] = W[qq] & 0x000f000fu;
                         xh[0][qq] = Ws & 0x000f000fu;
                         xl[1][qq] = W[qq] & 0x00f000f0u;
                         xh[1][qq] = Ws & 0x00f000f0u;
-#else
-                        e4m3x4_to_f16(__byte_perm(W[qq] & 0x0f0f0f0fu, 0, 0x3120), xl[0][qq], xh[0][qq]);
-                        e4m3x4_to_f16(__byte_perm((W[qq] >> 4) & 0x0f0f0f0fu, 0, 0x3120), xl[1][qq], xh[1][qq]);
-#endif
                     }
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
@@ -475,13 +435,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
                     uint32_t xl[4], xh[4];
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
-#if KIVI_DECODE_SUBN
                         const uint32_t mk = 0x00030003u << (2 * k);  // channel 8g + k | 8g + 4 + k
                         xl[qq] = W[qq] & mk;
                         xh[qq] = (W[qq] >> 8) & mk;
-#else
-                        e4m3x4_to_f16(__byte_perm((W[qq] >> (2 * k)) & 0x03030303u, 0, 0x3120), xl[qq], xh[qq]);
-#endif
                     }
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
