@@ -636,8 +636,12 @@ def run_sweep(args):
         return
 
     # decode over a packed store + fp16 residual
+    # (B, packed tokens, fp16 residual tokens, bits): the qwen8b decode, the long-context and batched
+    # decodes, and the streaming workload's S_kv sweep (128 / 512 / 2048 / 8192 / 16384 at B=1 and B=16)
     cases = [(1, 2080, 158, 4), (1, 4096 - 128, 128, 4), (1, 8192 - 128, 128, 4), (1, 16384 - 128, 128, 4),
-             (1, 32768 - 128, 128, 2), (32, 4032, 64, 4), (16, 2048 - 128, 128, 4), (16, 16384 - 128, 128, 4)]
+             (1, 32768 - 128, 128, 2), (32, 4032, 64, 4), (16, 2048 - 128, 128, 4), (16, 16384 - 128, 128, 4),
+             (1, 0, 128, 4), (1, 512 - 128, 128, 4), (1, 2048 - 128, 128, 4),
+             (16, 0, 128, 4), (16, 512 - 128, 128, 4), (16, 8192 - 128, 128, 4)]
     for B, S_q, n_res, bits in cases:
         w = synth.Workload("decode", B=B, Hkv=8, Hq=32, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
                            n_outlier=4, outlier_scale=8.0, seed=11)
@@ -647,9 +651,10 @@ def run_sweep(args):
         entries = []
         for i in range(P):
             k, v, q = synth.prefill_inputs_torch(w, 9000 + i, dev)
-            gk = kv.KiviStore(0, w.BH, S_q, w.D, w.G, bits, device=dev)
-            gv = kv.KiviStore(1, w.BH, S_q, w.D, w.G, bits, device=dev)
-            kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
+            gk = kv.KiviStore(0, w.BH, max(S_q, w.G), w.D, w.G, bits, device=dev)
+            gv = kv.KiviStore(1, w.BH, max(S_q, w.G), w.D, w.G, bits, device=dev)
+            if S_q > 0:
+                kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
             kr = k[:, S_q:].contiguous()
             vr = v[:, S_q:].contiguous()
             out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device=dev)

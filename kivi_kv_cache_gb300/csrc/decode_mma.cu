@@ -185,7 +185,11 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     const int Er = safe_exp(qmax);
     const float fBr = pow2i(Er), fCr = pow2i(-Er);
 
-    float m_run = -INFINITY, l_run = 0.f;  // online softmax of head c
+    // online softmax of head c: m_run is shared by the lanes of equal c; l_run
+    // and pzl (sum_t p_t z_tj per value group j) are this lane's shares, summed
+    // over the lanes of equal c once, after the last tile
+    float m_run = -INFINITY, l_run = 0.f;
+    float pzl[4] = {0.f, 0.f, 0.f, 0.f};
     float o[8][4];                         // P.V of head c, store-tile channel layout
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -342,16 +346,10 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
         const float m_new = fmaxf(m_run, tmax);
         const float corr = exp2f(m_run - m_new);
-        float p[4], ps = 0.f;
+        float p[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            p[i] = exp2f(sc[i] - m_new);
-            ps += p[i];
-        }
-        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l_run = fmaf(l_run, corr, ps);
+        for (int i = 0; i < 4; ++i) p[i] = exp2f(sc[i] - m_new);
+        l_run = fmaf(l_run, corr, (p[0] + p[1]) + (p[2] + p[3]));
         m_run = m_new;
         if (__any_sync(0xffffffffu, corr != 1.f)) {  // the running max moved (x * 1 == x: skip)
             const f32x2 c2 = pk(corr, corr);
@@ -363,28 +361,23 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                 o[i][2] = hi.x;
                 o[i][3] = hi.y;
             }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pzl[j] *= corr;
         }
         // p of tokens g, g+8, g+16, g+24 (head c) -> pbuf; p.vzero partials
         pbuf[(g) * 4 + c] = p[0];
         pbuf[(g + 8) * 4 + c] = p[1];
         pbuf[(g + 16) * 4 + c] = p[2];
         pbuf[(g + 24) * 4 + c] = p[3];
-        float pz[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int t = g + 8 * i;
             const uint2 z4 = *reinterpret_cast<const uint2*>(VZ + t * 4);
             const float2 za = __half22float2(u32_as_h2(z4.x)), zb = __half22float2(u32_as_h2(z4.y));
-            pz[0] = fmaf(p[i], za.x, pz[0]);
-            pz[1] = fmaf(p[i], za.y, pz[1]);
-            pz[2] = fmaf(p[i], zb.x, pz[2]);
-            pz[3] = fmaf(p[i], zb.y, pz[3]);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            pz[j] += __shfl_xor_sync(0xffffffffu, pz[j], 4);
-            pz[j] += __shfl_xor_sync(0xffffffffu, pz[j], 8);
-            pz[j] += __shfl_xor_sync(0xffffffffu, pz[j], 16);
+            pzl[0] = fmaf(p[i], za.x, pzl[0]);
+            pzl[1] = fmaf(p[i], za.y, pzl[1]);
+            pzl[2] = fmaf(p[i], zb.x, pzl[2]);
+            pzl[3] = fmaf(p[i], zb.y, pzl[3]);
         }
         __syncwarp();
 
@@ -436,13 +429,6 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                         mma16816(o[2 * j + u], xl[u][2 * ks], xh[u][2 * ks], xl[u][2 * ks + 1], xh[u][2 * ks + 1],
                                  bp[j][ks][0], bp[j][ks][1]);
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    o[2 * j + u][0] += pz[j] * kOUnit4[u];  // o[2j + u] is kept in units of kOUnit4[u]
-                    o[2 * j + u][2] += pz[j] * kOUnit4[u];
-                }
         } else {
             // o[4h + k]: rows g -> channel 64h + 8g + k, g+8 -> 64h + 8g + 4 + k;
             // rows of lanes g < 4 lie in group 2h, of lanes g >= 4 in group 2h+1
@@ -469,15 +455,6 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
                         mma16816(o[4 * hc + k], first ? 0u : a0, first ? 0u : a1, first ? 0u : a2,
                                  first ? 0u : a3, bp[2 * hc + 1][ks][0], bp[2 * hc + 1][ks][1]);
                     }
-                }
-            }
-#pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {
-                const float pzj = g < 4 ? pz[2 * hc] : pz[2 * hc + 1];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    o[4 * hc + k][0] += pzj * kOUnit2[k];
-                    o[4 * hc + k][2] += pzj * kOUnit2[k];
                 }
             }
         }
@@ -528,17 +505,15 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         const float m_new = fmaxf(m_run, tmax);
         const float corr = exp2f(m_run - m_new);
         const float p0 = exp2f(sc[0] - m_new), p1 = exp2f(sc[1] - m_new);
-        float ps = p0 + p1;
-        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l_run = fmaf(l_run, corr, ps);
+        l_run = fmaf(l_run, corr, p0 + p1);
         m_run = m_new;
         if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) o[i][k] *= corr;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pzl[j] *= corr;
         }
         pbuf[g * 4 + c] = p0;
         pbuf[(g + 8) * 4 + c] = p1;
@@ -601,25 +576,34 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     float* Ow = reinterpret_cast<float*>(st0);          // [4 heads][128] of this warp
     float* ml = misc + 16;                                 // [warp][head][2]
     {
-        // o holds (sum p s c + pz) in units of kOUnit4 / kOUnit2
+        // l and sum_t p_t z_tj of head c: the lanes of equal c hold disjoint tokens
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+            l_run += __shfl_xor_sync(0xffffffffu, l_run, x);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pzl[j] += __shfl_xor_sync(0xffffffffu, pzl[j], x);
+        }
+        // o holds sum p s c in units of kOUnit4 / kOUnit2; the z term adds per value group
         if (BITS == 4) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const float sc = 1.0f / kOUnit4[u];
-                    Ow[c * kD + 32 * j + 4 * g + u] = (o[2 * j + u][0] + o[2 * j + u][1]) * sc;
-                    Ow[c * kD + 32 * j + 4 * g + 2 + u] = (o[2 * j + u][2] + o[2 * j + u][3]) * sc;
+                    Ow[c * kD + 32 * j + 4 * g + u] = fmaf(o[2 * j + u][0] + o[2 * j + u][1], sc, pzl[j]);
+                    Ow[c * kD + 32 * j + 4 * g + 2 + u] = fmaf(o[2 * j + u][2] + o[2 * j + u][3], sc, pzl[j]);
                 }
         } else {
 #pragma unroll
-            for (int hc = 0; hc < 2; ++hc)
+            for (int hc = 0; hc < 2; ++hc) {
+                const float pzj = g < 4 ? pzl[2 * hc] : pzl[2 * hc + 1];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const float sc = 1.0f / kOUnit2[k];
-                    Ow[c * kD + 64 * hc + 8 * g + k] = (o[4 * hc + k][0] + o[4 * hc + k][1]) * sc;
-                    Ow[c * kD + 64 * hc + 8 * g + 4 + k] = (o[4 * hc + k][2] + o[4 * hc + k][3]) * sc;
+                    Ow[c * kD + 64 * hc + 8 * g + k] = fmaf(o[4 * hc + k][0] + o[4 * hc + k][1], sc, pzj);
+                    Ow[c * kD + 64 * hc + 8 * g + 4 + k] = fmaf(o[4 * hc + k][2] + o[4 * hc + k][3], sc, pzj);
                 }
+            }
         }
         if (g == 0) {
             ml[(warp * 4 + c) * 2 + 0] = m_run;
