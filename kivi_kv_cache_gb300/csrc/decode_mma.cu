@@ -392,14 +392,24 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
             const float4 va1 = *reinterpret_cast<const float4*>(VS + (ta + 1) * 4);
             const float4 vb0 = *reinterpret_cast<const float4*>(VS + tb * 4);
             const float4 vb1 = *reinterpret_cast<const float4*>(VS + (tb + 1) * 4);
-            const float sa0[4] = {va0.x, va0.y, va0.z, va0.w}, sa1[4] = {va1.x, va1.y, va1.z, va1.w};
-            const float sb0[4] = {vb0.x, vb0.y, vb0.z, vb0.w}, sb1[4] = {vb1.x, vb1.y, vb1.z, vb1.w};
+            // p of one token times its 4 group scales: pairs (s_t0, s_t1), (s_t2, s_t3) of one load
+            float xa0[4], xa1[4], xb0[4], xb1[4];
+            auto prod4 = [](float pt, const float4& v, float (&x)[4]) {
+                const f32x2 p2 = pk(pt, pt);
+                const float2 lo = upk(mul2(p2, pk(v.x, v.y))), hi = upk(mul2(p2, pk(v.z, v.w)));
+                x[0] = lo.x;
+                x[1] = lo.y;
+                x[2] = hi.x;
+                x[3] = hi.y;
+            };
+            prod4(pa0, va0, xa0);
+            prod4(pa1, va1, xa1);
+            prod4(pb0, vb0, xb0);
+            prod4(pb1, vb1, xb1);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float2 a2 = upk(mul2(pk(pa0, pa1), pk(sa0[j], sa1[j])));
-                const float2 b2 = upk(mul2(pk(pb0, pb1), pk(sb0[j], sb1[j])));
-                bp[j][ks][0] = split_pair(a2.x, a2.y, lo_part);
-                bp[j][ks][1] = split_pair(b2.x, b2.y, lo_part);
+                bp[j][ks][0] = split_pair(xa0[j], xa1[j], lo_part);
+                bp[j][ks][1] = split_pair(xb0[j], xb1[j], lo_part);
             }
         }
 

@@ -174,7 +174,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
     const int Er = safe_exp(qmax);  // residual tiles: B operand q 2^Er
     const float fBr = pow2i(Er), fCr = pow2i(-Er);
 
-    float m_run = -INFINITY, l_run = 0.f;  // online softmax of head c (identical in both warps)
+    // online softmax of head c: m_run is shared by the lanes of equal c (and by both warps);
+    // l_run and pzl (sum_t p_t z_tj for this warp's value groups 2hf + jj) are this lane's
+    // shares, summed over the lanes of equal c once, after the last tile
+    float m_run = -INFINITY, l_run = 0.f;
+    float pzl[2] = {0.f, 0.f};
     float o[NO][4];
 #pragma unroll
     for (int i = 0; i < NO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -334,22 +338,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
         const float m_new = fmaxf(m_run, tmax);  // finite: every tile has a valid token
         const float corr = exp2f(m_run - m_new);
-        float p[4], ps = 0.f;
+        float p[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            p[i] = exp2f(s4[i] - m_new);
-            ps += p[i];
-        }
-        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l_run = fmaf(l_run, corr, ps);
+        for (int i = 0; i < 4; ++i) p[i] = exp2f(s4[i] - m_new);
+        l_run = fmaf(l_run, corr, (p[0] + p[1]) + (p[2] + p[3]));
         m_run = m_new;
         if (__any_sync(0xffffffffu, corr != 1.f)) {  // the running max moved (x * 1 == x: skip)
 #pragma unroll
             for (int i = 0; i < NO; ++i)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) o[i][k] *= corr;
+            pzl[0] *= corr;
+            pzl[1] *= corr;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -359,22 +359,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
         if (store) {
             const float* VS = reinterpret_cast<const float*>(S + kVS);
             const __half* VZ = reinterpret_cast<const __half*>(S + kVZ);
-            // sum_t p_t z_tj of head c for this warp's groups j = 2hf + jj (stale rows past nvalid masked)
-            float pz[2];
+            // this lane's share of sum_t p_t z_tj (head c, groups j = 2hf + jj; stale rows past
+            // nvalid masked)
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
                 const int j = 2 * hf + jj;
-                float t = 0.f;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int tk = g + 8 * i;
                     const float z = tk < nvalid ? __half2float(VZ[tk * 4 + j]) : 0.f;
-                    t = fmaf(p[i], z, t);
+                    pzl[jj] = fmaf(p[i], z, pzl[jj]);
                 }
-                t += __shfl_xor_sync(0xffffffffu, t, 4);
-                t += __shfl_xor_sync(0xffffffffu, t, 8);
-                t += __shfl_xor_sync(0xffffffffu, t, 16);
-                pz[jj] = t;  // added to o in o's units (kOUnit4 / kOUnit2)
             }
             // B operand: p_t s_tj of head hh; K-step ks: tokens 16ks + {2c, 2c+1 | 2c+8, 2c+9}
             uint32_t bp[2][2][2];  // [jj][ks][b0/b1]
@@ -419,8 +414,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
                         for (int ks = 0; ks < 2; ++ks)
                             mma16816(o[2 * jj + u], xl[u][2 * ks], xh[u][2 * ks], xl[u][2 * ks + 1],
                                      xh[u][2 * ks + 1], bp[jj][ks][0], bp[jj][ks][1]);
-                        o[2 * jj + u][0] += pz[jj] * kOUnit4[u];
-                        o[2 * jj + u][2] += pz[jj] * kOUnit4[u];
                     }
                 }
             } else {
@@ -447,9 +440,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
                         mma16816(o[k], first ? 0u : a0, first ? 0u : a1, first ? 0u : a2, first ? 0u : a3,
                                  bp[1][ks][0], bp[1][ks][1]);
                     }
-                    const float pzk = (first ? pz[0] : pz[1]) * kOUnit2[k];
-                    o[k][0] += pzk;
-                    o[k][2] += pzk;
                 }
             }
         } else {
@@ -511,20 +501,31 @@ __global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) 
     float* Ow = reinterpret_cast<float*>(ring);  // [4 heads][128] of this pair (each warp its 64 channels)
     float* ml = misc + 16;                        // [pair][head][2]
     {
+        // l and sum_t p_t z_tj of head c: the lanes of equal c hold disjoint tokens
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+            l_run += __shfl_xor_sync(0xffffffffu, l_run, x);
+            pzl[0] += __shfl_xor_sync(0xffffffffu, pzl[0], x);
+            pzl[1] += __shfl_xor_sync(0xffffffffu, pzl[1], x);
+        }
+        // o holds sum p s c in units of kOUnit4 / kOUnit2; the z term adds per value group
         if (BITS == 4) {
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int j = 2 * hf + jj;
-                    Ow[c * kD + 32 * j + 4 * g + u] = (o[2 * jj + u][0] + o[2 * jj + u][1]) * (1.0f / kOUnit4[u]);
-                    Ow[c * kD + 32 * j + 4 * g + 2 + u] = (o[2 * jj + u][2] + o[2 * jj + u][3]) * (1.0f / kOUnit4[u]);
+                    const float sc = 1.0f / kOUnit4[u];
+                    Ow[c * kD + 32 * j + 4 * g + u] = fmaf(o[2 * jj + u][0] + o[2 * jj + u][1], sc, pzl[jj]);
+                    Ow[c * kD + 32 * j + 4 * g + 2 + u] = fmaf(o[2 * jj + u][2] + o[2 * jj + u][3], sc, pzl[jj]);
                 }
         } else {
+            const float pzj = g < 4 ? pzl[0] : pzl[1];  // rows of lanes g < 4 lie in group 2hf
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                Ow[c * kD + 64 * hf + 8 * g + k] = (o[k][0] + o[k][1]) * (1.0f / kOUnit2[k]);
-                Ow[c * kD + 64 * hf + 8 * g + 4 + k] = (o[k][2] + o[k][3]) * (1.0f / kOUnit2[k]);
+                const float sc = 1.0f / kOUnit2[k];
+                Ow[c * kD + 64 * hf + 8 * g + k] = fmaf(o[k][0] + o[k][1], sc, pzj);
+                Ow[c * kD + 64 * hf + 8 * g + 4 + k] = fmaf(o[k][2] + o[k][3], sc, pzj);
             }
         }
         if (hf == 0 && g == 0) {
