@@ -59,6 +59,8 @@ def parse_args():
     p.add_argument("--workload", default="qwen8b", choices=["tiny", "qwen8b", "long2bit"])
     p.add_argument("--pool", type=int, default=0, help="instances in the rotating pool (0 = auto)")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--e2e-streams", type=int, default=2,
+                   help="streams the end-to-end instances alternate between (copies of one overlap the others)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--hashes", action="store_true", help="print the source hash of each op and exit")
@@ -388,12 +390,13 @@ def run_gb300(args, rank, world, local_rank):
     # and its result through the copy engines inside the timed region.
     e2e = None
     if args.e2e_steps > 0:
-        ne = max(2, min(pool, 4))
+        nl = max(1, args.e2e_streams)
+        ne = min(pool, max(2 * nl, 4))  # instances: two per stream, at least 4
         hk = [insts[i].k.cpu().pin_memory() for i in range(ne)]
         hv = [insts[i].v.cpu().pin_memory() for i in range(ne)]
         hq = [insts[i].q.cpu().pin_memory() for i in range(ne)]
         hout = [torch.empty((w.B, w.Hq, w.D), dtype=torch.float32).pin_memory() for _ in range(ne)]
-        lanes = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        lanes = [torch.cuda.Stream(dev) for _ in range(nl)]
 
         def e2e_step(i):
             insts[i].k.copy_(hk[i], non_blocking=True)
@@ -404,7 +407,7 @@ def run_gb300(args, rank, world, local_rank):
 
         e2e_graphs = []
         for i in range(ne):
-            lane = lanes[i % 2]
+            lane = lanes[i % nl]
             lane.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(lane):
                 e2e_step(i)  # eager once on this stream before the capture
@@ -423,7 +426,7 @@ def run_gb300(args, rank, world, local_rank):
             lane.wait_stream(main)
         for j in range(args.e2e_steps):
             i = j % ne
-            with torch.cuda.stream(lanes[i % 2]):
+            with torch.cuda.stream(lanes[i % nl]):
                 e2e_graphs[i].replay()
         for lane in lanes:
             main.wait_stream(lane)
@@ -435,7 +438,7 @@ def run_gb300(args, rank, world, local_rank):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout[0].numel() * 4),
                "ms_per_step": round(e2e_ms / args.e2e_steps, 5),
                "how": "per-instance CUDA graphs of the public-API calls: pinned H2D copies of K, V, q, the step, "
-                      "D2H of the output; two streams alternate instances so copies overlap kernels"}
+                      "D2H of the output; %d streams alternate instances so copies overlap kernels" % nl}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
