@@ -645,8 +645,13 @@ def run_sweep(args):
              (1, 32768 - 128, 128, 2), (32, 4032, 64, 4), (16, 2048 - 128, 128, 4), (16, 16384 - 128, 128, 4),
              (1, 0, 128, 4), (1, 512 - 128, 128, 4), (1, 2048 - 128, 128, 4),
              (16, 0, 128, 4), (16, 512 - 128, 128, 4), (16, 8192 - 128, 128, 4)]
-    for B, S_q, n_res, bits in cases:
-        w = synth.Workload("decode", B=B, Hkv=8, Hq=32, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
+    # 8, 6 and 3 query heads per KV head (sub-groups of up to 4 heads)
+    cases += [(1, 16384 - 128, 128, 4, 64), (32, 4032, 64, 4, 64), (1, 4096 - 128, 128, 4, 64),
+              (32, 4032, 64, 4, 48), (32, 4032, 64, 4, 24)]
+    for case in cases:
+        B, S_q, n_res, bits = case[:4]
+        Hq = case[4] if len(case) > 4 else 32
+        w = synth.Workload("decode", B=B, Hkv=8, Hq=Hq, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
                            n_outlier=4, outlier_scale=8.0, seed=11)
         per_tok = 2 * w.D * bits / 8 + w.D * 6 / w.G + (w.D // w.G) * 6
         nbytes = w.BH * S_q * per_tok + w.BH * n_res * w.D * 4 + B * w.Hq * w.D * 6
@@ -668,7 +673,7 @@ def run_sweep(args):
         torch.cuda.synchronize()
         fns = [lambda e=e: kv.kivi_decode_attend(e[0], e[1], e[2], S_q, e[3], e[4], n_res, w.Hkv, w.sm_scale,
                                                  out=e[5], workspace=e[6]) for e in entries]
-        timed(fns, nbytes, "decode_attend", {"B": B, "Hkv": 8, "Hq": 32, "S_kv": S_q + n_res, "bits": bits,
+        timed(fns, nbytes, "decode_attend", {"B": B, "Hkv": 8, "Hq": Hq, "S_kv": S_q + n_res, "bits": bits,
                                              "pool": P, "tokens_per_s": None})
         del entries, fns
         torch.cuda.empty_cache()

@@ -219,7 +219,8 @@ kivi_status kivi_fake_quant_kv(const void* k_f16, const void* v_f16, int BH, int
  * once).
  *
  * Workspace layout: the first KIVI_DECODE_COUNTER_BYTES bytes hold the merge
- * counters of the split decode, one per (batch, KV head); the split partials
+ * counters of the split decode, one per head group (batch, KV head, and
+ * sub-group of up to 4 query heads when Hq/Hkv is not 1, 2 or 4); the split partials
  * follow. The counters must be zero before a workspace's first use
  * (kivi_decode_workspace_init, or any zero fill), and every completed call
  * leaves them zero again, whatever its sizes. The rest of the workspace is
@@ -255,7 +256,7 @@ kivi_status kivi_decode_workspace_init(void* workspace, size_t workspace_bytes, 
  * laid out and initialised as described there (may be NULL when that size is
  * 0).
  * Errors: INVALID_ARG if S_q + n_res == 0, S_q > s_cap, n_res > res_cap or
- * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv > 8; WORKSPACE if the workspace is
+ * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv > 64; WORKSPACE if the workspace is
  * NULL or too small.
  */
 kivi_status kivi_decode_attend(const void* q_f16,

@@ -141,21 +141,4 @@ __device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0,
         reinterpret_cast<float4*>(a.out + bq * kD)[lane] = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
 }
 
-// The same merge for the channel-split kernel: 4 warps, query heads warp,
-// warp + 4 (up to 8 heads), no barrier.
-template <int CHUNK>
-__device__ __forceinline__ void merge_splits_by_head(const DecodeArgs& a, long long bq0, int nheads, int warp,
-                                                     int lane) {
-    for (int h = warp; h < nheads; h += 4) {
-        const long long bq = bq0 + h;
-        float M, L;
-        const float4 acc = merge_range<CHUNK>(reinterpret_cast<const float2*>(a.part_ml) + bq * a.n_split,
-                                              reinterpret_cast<const float4*>(a.part_o + bq * a.n_split * kD) +
-                                                  lane,
-                                              0, a.n_split, lane, &M, &L);
-        reinterpret_cast<float4*>(a.out + bq * kD)[lane] =
-            make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
-    }
-}
-
 }  // namespace kivi

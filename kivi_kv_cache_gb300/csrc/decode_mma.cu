@@ -1,6 +1,7 @@
 // decode_mma.cu -- fused dequantize-and-attend single-token decode on the
-// tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation), for
-// grouped-query groups of up to 4 query heads per KV head.
+// tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation), one warp
+// per tile, for groups of up to 4 query heads per KV head; larger groups run
+// in sub-groups of up to 4 heads (one CTA group each, reading the same tiles).
 //
 // Method: VeloxQuant-MLX blog, "A 5.65x Metal Kernel That Made My LLM Exactly
 // 0% Faster", "So why does the kernel ship?" (attention reads the packed
@@ -30,7 +31,7 @@
 //   * a per-tile power-of-two factor keeps every hi below 2^14 (no fp16
 //     overflow for any finite input); it is divided out exactly afterwards.
 //
-// Work split: grid (n_split, Hkv, B), 4 or 8 warps per CTA; each warp owns a
+// Work split: grid (n_split, Hkv * q_sub, B), 4 or 8 warps per CTA; each warp owns a
 // contiguous run of tiles of its split (32-token store tiles, then 16-token
 // residual tiles) and keeps its own online softmax; the warps merge in shared
 // memory and the CTA writes one partial (or the output when n_split == 1; the
@@ -128,6 +129,28 @@ __device__ __forceinline__ void fetch_res_tile(const DecodeArgs& a, int bh, int 
 // the kernel
 // ---------------------------------------------------------------------------
 
+// GQ = 1, 2 or 4: the group size, blockIdx.y = KV head. GQ = kSubGroupGQ: any
+// other group size, in sub-groups of 4 heads (blockIdx.y = KV head times q_sub
+// + sub-group; the last sub-group possibly partial).
+constexpr int kSubGroupGQ = 8;
+template <int GQ>
+__device__ __forceinline__ int cta_kv_head(const DecodeArgs& a) {
+    return GQ == kSubGroupGQ ? (int)blockIdx.y / a.q_sub : (int)blockIdx.y;
+}
+// Query heads h0 .. h0 + nh - 1 (of the batch row) of this CTA.
+template <int GQ>
+__device__ __forceinline__ void cta_heads(const DecodeArgs& a, int& h0, int& nh) {
+    if (GQ == kSubGroupGQ) {
+        const int gq = a.Hq / a.Hkv;
+        const int hk = (int)blockIdx.y / a.q_sub, sg = (int)blockIdx.y - hk * a.q_sub;
+        h0 = hk * gq + 4 * sg;
+        nh = min(4, gq - 4 * sg);
+    } else {
+        h0 = (int)blockIdx.y * GQ;
+        nh = GQ;
+    }
+}
+
 // NW warps per CTA (4 or 8): 16 warps per SM either way, at 128 registers.
 // CL: the n_split CTAs of a (batch, KV head) form one thread-block cluster
 // (n_split <= kMaxClusterSplits) and merge through distributed shared memory.
@@ -139,8 +162,8 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c = lane & 3;
-    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-    const int bh = b * a.Hkv + hk, h0 = hk * GQ;
+    const int split = blockIdx.x, b = blockIdx.z;
+    const int bh = b * a.Hkv + cta_kv_head<GQ>(a);
     uint8_t* const st0 = smem + warp * kWarpSmem;  // two stages: st0, st0 + kStage
     float* pbuf = reinterpret_cast<float*>(smem + LY::kPbufOff + warp * 512);  // [token][head]
     float* q_s = reinterpret_cast<float*>(smem + LY::kQOff);                   // [head][channel]
@@ -161,14 +184,18 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     if (ns > 1) fetch_store_tile<BITS>(a, bh, w0 + 1, st0 + kStage, lane);
     cp_async_commit();
 
-    // q * score_scale for the GQ heads of this KV head (heads >= GQ are zero)
+    // q * score_scale for the nh heads of this CTA (heads >= nh are zero)
     float qm = 0.f;
+    {
+        int h0, nh;
+        cta_heads<GQ>(a, h0, nh);
 #pragma unroll
-    for (int i = tid; i < 4 * kD; i += kThreads) {
-        const int h = i / kD, d = i % kD;
-        const float v = h < GQ ? __half2float(a.q[((long long)b * a.Hq + h0 + h) * kD + d]) * a.score_scale : 0.f;
-        q_s[h * kQRow + padc(d)] = v;
-        qm = fmaxf(qm, fabsf(v));
+        for (int i = tid; i < 4 * kD; i += kThreads) {
+            const int h = i / kD, d = i % kD;
+            const float v = h < nh ? __half2float(a.q[((long long)b * a.Hq + h0 + h) * kD + d]) * a.score_scale : 0.f;
+            q_s[h * kQRow + padc(d)] = v;
+            qm = fmaxf(qm, fabsf(v));
+        }
     }
     qm = warp_max(qm);
     if (lane == 0) misc[warp] = qm;
@@ -622,8 +649,10 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
     }
     pdl_trigger();
     __syncthreads();
+    int h0, nh;  // recomputed here rather than held through the tile loop
+    cta_heads<GQ>(a, h0, nh);
     const int d = tid & (kD - 1);
-    for (int h = tid / kD; h < GQ; h += kThreads / kD) {
+    for (int h = tid / kD; h < nh; h += kThreads / kD) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 4 + h) * 2]);
@@ -662,7 +691,7 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         cluster_sync();
         const uint32_t rank = cluster_ctarank();
         const int n = a.n_split;
-        for (int idx = (int)rank * kThreads + tid; idx < GQ * kD; idx += n * kThreads) {
+        for (int idx = (int)rank * kThreads + tid; idx < nh * kD; idx += n * kThreads) {
             const int h = idx / kD, dd = idx % kD;
             float mk[kMaxClusterSplits];
             float M = -INFINITY;
@@ -685,8 +714,9 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         cluster_sync();  // no CTA leaves while another still reads its shared memory
         return;
     }
-    if (take_last_ticket(a, bh, reinterpret_cast<int*>(misc + 96)))
-        merge_splits<16>(a, (long long)b * a.Hq + h0, GQ, warp, kWarps, lane, reinterpret_cast<float*>(smem));
+    // one ticket counter per (batch, KV head, sub-group)
+    if (take_last_ticket(a, b * (int)gridDim.y + (int)blockIdx.y, reinterpret_cast<int*>(misc + 96)))
+        merge_splits<16>(a, (long long)b * a.Hq + h0, nh, warp, kWarps, lane, reinterpret_cast<float*>(smem));
 }
 
 template <int BITS, int GQ, int NW, bool CL>
@@ -757,13 +787,13 @@ bool use_cluster(const DecodeArgs& a, cudaStream_t stream) {
     if (n < 2 || n > kMaxClusterSplits) return false;
     const long long with = resident_ctas<BITS, GQ, NW>(n, stream);
     if (with <= 0) return false;
-    const long long ctas = (long long)n * a.Hkv * a.B;
+    const long long ctas = (long long)n * a.Hkv * a.q_sub * a.B;
     return ctas <= with || 20 * with >= 19LL * resident_ctas<BITS, GQ, NW>(1, stream);
 }
 
 template <int BITS, int GQ, int NW>
 cudaError_t launch_mma_typed(const DecodeArgs& a, cudaStream_t stream) {
-    const dim3 grid(a.n_split, a.Hkv, a.B);
+    const dim3 grid(a.n_split, a.Hkv * a.q_sub, a.B);
     if (use_cluster<BITS, GQ, NW>(a, stream)) {
         cudaError_t e = configure_mma<BITS, GQ, NW, true>();
         if (e != cudaSuccess) return e;
@@ -783,15 +813,20 @@ cudaError_t launch_mma_warps(const DecodeArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, int bits, int gq, cudaStream_t stream) {
+    // groups of 1 or 2 heads run their own width; larger groups run in
+    // sub-groups of 4 heads (a.q_sub of them per KV head, the last possibly partial)
     cudaError_t e = cudaErrorInvalidValue;
+    if (gq < 1 || (gq > 2 && (gq + 3) / 4 != a.q_sub) || (gq <= 2 && a.q_sub != 1)) return e;
     if (bits == 4) {
         if (gq == 1) e = launch_mma_warps<4, 1>(a, stream);
-        if (gq == 2) e = launch_mma_warps<4, 2>(a, stream);
-        if (gq == 4) e = launch_mma_warps<4, 4>(a, stream);
+        else if (gq == 2) e = launch_mma_warps<4, 2>(a, stream);
+        else if (gq == 4) e = launch_mma_warps<4, 4>(a, stream);
+        else e = launch_mma_warps<4, kSubGroupGQ>(a, stream);
     } else {
         if (gq == 1) e = launch_mma_warps<2, 1>(a, stream);
-        if (gq == 2) e = launch_mma_warps<2, 2>(a, stream);
-        if (gq == 4) e = launch_mma_warps<2, 4>(a, stream);
+        else if (gq == 2) e = launch_mma_warps<2, 2>(a, stream);
+        else if (gq == 4) e = launch_mma_warps<2, 4>(a, stream);
+        else e = launch_mma_warps<2, kSubGroupGQ>(a, stream);
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -43,27 +43,21 @@ kivi_status shape_check(int D, int G, int bits) {
 
 kivi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ERR_CUDA; }
 
-// Split plan for the decode. Groups of 1, 2 or 4 query heads per KV head run
-// the one-warp-per-tile kernel: each warp of a CTA takes a run of
-// tiles_per_warp tiles (32-token store tiles, then 16-token residual tiles),
-// sized for about kMmaWarpsPerSm warps per SM over the whole batch. CTAs have
-// 4 warps, or 8 when 4-warp CTAs would leave a (batch, KV head) more than
-// kMmaMaxSplits4 partials to merge. Other groups run the channel-split kernel:
-// a CTA takes a run of tiles (16-token residual tiles) sized for about
-// kSplitCtasPerSm CTAs per SM in one wave, never shorter than kSplitMinTiles
-// tiles. When the batch has more (batch, KV head) pairs than the workspace has
-// merge counters, each pair gets one split.
+// Split plan for the decode, run by the one-warp-per-tile kernel: each warp of
+// a CTA takes a run of tiles_per_warp tiles (32-token store tiles, then
+// 16-token residual tiles), sized for about kMmaWarpsPerSm warps per SM over
+// the whole batch. CTAs have 4 warps, or 8 when 4-warp CTAs would leave a
+// head group more than kMmaMaxSplits4 partials to merge. Groups of 1, 2 or 4
+// query heads per KV head run as one head group; any other group size runs in
+// q_sub = ceil(gq / 4) sub-groups of up to 4 heads, each a head group of its
+// own (the sub-groups of one split read the same tiles side by side, so L2
+// serves the repeated reads). When the batch has more head groups than the
+// workspace has merge counters, each gets one split.
 #ifndef KIVI_DECODE_MMA_WARPS_PER_SM
 #define KIVI_DECODE_MMA_WARPS_PER_SM 24
 #endif
 #ifndef KIVI_DECODE_MMA_MAX_SPLITS4
 #define KIVI_DECODE_MMA_MAX_SPLITS4 16
-#endif
-#ifndef KIVI_DECODE_CTAS_PER_SM
-#define KIVI_DECODE_CTAS_PER_SM 4
-#endif
-#ifndef KIVI_DECODE_MIN_TILES
-#define KIVI_DECODE_MIN_TILES 3
 #endif
 // Warp-pair kernel: 0 never, 1 always, 2 when the one-warp-per-tile plan gives
 // warps at most kPairMaxWarpTiles tiles and the pair plan at most
@@ -96,49 +90,36 @@ constexpr int kMmaWarpsPerSm = KIVI_DECODE_MMA_WARPS_PER_SM;
 #endif
 constexpr int kMmaWarpsPerSm2 = KIVI_DECODE_MMA_WARPS_PER_SM_2BIT;
 constexpr int kMmaMaxSplits4 = KIVI_DECODE_MMA_MAX_SPLITS4;
-constexpr int kSplitCtasPerSm = KIVI_DECODE_CTAS_PER_SM;
-constexpr int kSplitMinTiles = KIVI_DECODE_MIN_TILES;
 
 bool mma_group(int gq) { return gq == 1 || gq == 2 || gq == 4; }
 
 DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits) {
     DecodePlan p;
-    const bool mma = Hkv > 0 && Hq % Hkv == 0 && mma_group(Hq / Hkv);
-    const int rt = mma ? kResTileTokensMma : kResTileTokensSplit;
+    const int gq = Hkv > 0 && Hq >= Hkv ? Hq / Hkv : 1;
+    p.q_sub = mma_group(gq) ? 1 : (gq + 3) / 4;
     p.n_store_tiles = (S_q + kG - 1) / kG;
-    p.n_tiles = p.n_store_tiles + (n_res + rt - 1) / rt;
-    const long long heads = (long long)B * Hkv;
-    if (mma) {
-        // 2-bit tiles carry half the codes: fewer, longer-running warps measured faster
-        const long long target = (long long)(bits == 2 ? kMmaWarpsPerSm2 : kMmaWarpsPerSm) * sm_count();
-        long long tpw = (heads * p.n_tiles + target - 1) / target;
-        if (tpw < 1) tpw = 1;
-        p.warps_per_cta = (p.n_tiles + 4 * tpw - 1) / (4 * tpw) > kMmaMaxSplits4 ? 8 : 4;
-        if (heads > kMergeCounters) tpw = (p.n_tiles + p.warps_per_cta - 1) / p.warps_per_cta;  // one split per pair
-        p.tiles_per_warp = (int)tpw;
-        p.tiles_per_split = (int)(p.warps_per_cta * tpw);
-        p.pair_kernel = 0;
-        if (kPairMode == 1 || (kPairMode == 2 && tpw <= kPairMaxWarpTiles && heads <= kMergeCounters)) {
-            const long long slots = (long long)kPairsPerSm * sm_count();
-            long long tpp = (heads * p.n_tiles + slots - 1) / slots;  // tiles per pair
-            if (tpp < kPairMinTiles) tpp = kPairMinTiles;
-            if (heads > kMergeCounters) tpp = (p.n_tiles + kPairsPerCta - 1) / kPairsPerCta;
-            const long long splits = (p.n_tiles + kPairsPerCta * tpp - 1) / (kPairsPerCta * tpp);
-            if (kPairMode == 1 || splits <= kPairMaxSplits) {
-                p.pair_kernel = 1;
-                p.tiles_per_warp = (int)tpp;
-                p.tiles_per_split = (int)(kPairsPerCta * tpp);
-            }
+    p.n_tiles = p.n_store_tiles + (n_res + kResTileTokensMma - 1) / kResTileTokensMma;
+    const long long heads = (long long)B * Hkv * p.q_sub;  // head groups (batch, KV head, sub-group)
+    // 2-bit tiles carry half the codes: fewer, longer-running warps measured faster
+    const long long target = (long long)(bits == 2 ? kMmaWarpsPerSm2 : kMmaWarpsPerSm) * sm_count();
+    long long tpw = (heads * p.n_tiles + target - 1) / target;
+    if (tpw < 1) tpw = 1;
+    p.warps_per_cta = (p.n_tiles + 4 * tpw - 1) / (4 * tpw) > kMmaMaxSplits4 ? 8 : 4;
+    if (heads > kMergeCounters) tpw = (p.n_tiles + p.warps_per_cta - 1) / p.warps_per_cta;  // one split each
+    p.tiles_per_warp = (int)tpw;
+    p.tiles_per_split = (int)(p.warps_per_cta * tpw);
+    p.pair_kernel = 0;
+    if (mma_group(gq) && (kPairMode == 1 || (kPairMode == 2 && tpw <= kPairMaxWarpTiles && heads <= kMergeCounters))) {
+        const long long slots = (long long)kPairsPerSm * sm_count();
+        long long tpp = (heads * p.n_tiles + slots - 1) / slots;  // tiles per pair
+        if (tpp < kPairMinTiles) tpp = kPairMinTiles;
+        if (heads > kMergeCounters) tpp = (p.n_tiles + kPairsPerCta - 1) / kPairsPerCta;
+        const long long splits = (p.n_tiles + kPairsPerCta * tpp - 1) / (kPairsPerCta * tpp);
+        if (kPairMode == 1 || splits <= kPairMaxSplits) {
+            p.pair_kernel = 1;
+            p.tiles_per_warp = (int)tpp;
+            p.tiles_per_split = (int)(kPairsPerCta * tpp);
         }
-    } else {
-        const long long slots = (long long)kSplitCtasPerSm * sm_count();
-        long long per = (heads * p.n_tiles + slots - 1) / slots;
-        if (per < kSplitMinTiles) per = kSplitMinTiles;
-        if (heads > kMergeCounters || per > p.n_tiles) per = p.n_tiles;
-        p.tiles_per_split = (int)per;
-        p.tiles_per_warp = (int)per;
-        p.warps_per_cta = 4;
-        p.pair_kernel = 0;
     }
     p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
     return p;
@@ -455,7 +436,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
         (S_q > 0 && s_cap % group_size != 0) || !std::isfinite(sm_scale))
         return KIVI_ERR_INVALID_ARG;
     const int gq = Hq / Hkv;
-    if (gq > 8) return KIVI_ERR_UNSUPPORTED;
+    if (gq > 64) return KIVI_ERR_UNSUPPORTED;  // up to 16 sub-groups of 4 query heads
     if (!q_f16 || !out_f32) return KIVI_ERR_INVALID_ARG;
     if (S_q > 0 && (!kcodes_u8 || !kscale || !kzero_f16 || !vcodes_u8 || !vscale || !vzero_f16))
         return KIVI_ERR_INVALID_ARG;
@@ -501,7 +482,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
                          : nullptr;
     a.out = out_f32;
     const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
-    if (!mma_group(gq)) return from_cuda(launch_decode_channel_split(a, bits, gq, strm));
+    a.q_sub = p.q_sub;
     return from_cuda(p.pair_kernel ? launch_decode_pair(a, bits, gq, strm) : launch_decode_mma(a, bits, gq, strm));
 }
 

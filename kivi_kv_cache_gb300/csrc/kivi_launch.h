@@ -61,7 +61,8 @@ struct DecodeArgs {
     int pair_kernel;      // 1: groups of 1, 2 or 4 heads run the warp-pair kernel
     int n_store_tiles;
     int n_tiles;
-    unsigned int* counters;  // [B*Hkv] merge tickets, zero between calls (n_split > 1)
+    int q_sub;            // one-warp-per-tile kernel: query sub-groups of up to 4 heads per KV head
+    unsigned int* counters;  // [B*Hkv*q_sub] merge tickets, zero between calls (n_split > 1)
     float* part_o;        // [B, Hq, n_split, D]
     float* part_ml;       // [B, Hq, n_split, 2]  (running max, running sum)
     float* out;           // [B, Hq, D]
@@ -75,13 +76,12 @@ struct DecodePlan {
     int pair_kernel;
     int n_store_tiles;
     int n_tiles;
+    int q_sub;
 };
 
-// Tokens per residual tile: the one-warp-per-tile kernel (1, 2 or 4 query
-// heads per KV head) and the channel-split kernel (any group up to 8).
+// Tokens per residual tile of the decode kernels.
 constexpr int kResTileTokensMma = 16;
-constexpr int kResTileTokensSplit = 16;
-constexpr int kMergeCounters = 8192;    // (batch, KV head) pairs that can take split merges
+constexpr int kMergeCounters = 8192;    // (batch, KV head, sub-group) CTA groups that can take split merges
 constexpr int kMaxClusterSplits = 16;   // splits of one head merged inside a thread-block cluster
 constexpr int kPairsPerCta = 4;         // warp pairs per CTA of the warp-pair kernel
 
@@ -141,11 +141,10 @@ cudaError_t launch_residual_append(const __half* src0, const __half* src1, long 
 cudaError_t launch_residual_compact(__half* res0, __half* res1, int BH, int res_cap, int n_res, int n_drop,
                                     cudaStream_t stream);
 // Fused decodes; each merges its own splits in the same launch.
-// gq in {1, 2, 4}: one warp per tile.
+// One warp per tile: gq in {1, 2, 4}, or any other gq in a.q_sub sub-groups of
+// up to 4 query heads.
 cudaError_t launch_decode_mma(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 // gq in {1, 2, 4}: two warps per tile, 4 warp pairs per CTA (small batches).
 cudaError_t launch_decode_pair(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
-// any 1 <= gq <= 8: the channels of a tile split over 4 warps.
-cudaError_t launch_decode_channel_split(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 
 }  // namespace kivi

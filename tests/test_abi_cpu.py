@@ -127,8 +127,8 @@ def decode(L, q=FAKE, S_q=2080, s_cap=2080, n_res=158, res_cap=160, B=1, Hq=32, 
 @no_gpu
 def test_decode_rejects_bad_arguments(L):
     assert decode(L, Hq=12) == INVALID               # 12 / 8 is not an integer
-    assert decode(L, Hq=72) == UNSUPPORTED           # 9 query heads per KV head
-    assert decode(L, Hq=128) == UNSUPPORTED          # 16 query heads per KV head
+    assert decode(L, Hq=520) == UNSUPPORTED          # 65 query heads per KV head
+    assert decode(L, Hq=1024) == UNSUPPORTED         # 128 query heads per KV head
     assert decode(L, S_q=0, n_res=0) == INVALID
     assert decode(L, S_q=3000) == INVALID            # S_q > s_cap
     assert decode(L, n_res=200) == INVALID           # n_res > res_cap
@@ -178,3 +178,19 @@ def test_workspace_size(L):
     assert small > 32768
     # more (batch, KV head) pairs than merge counters: one split each, no workspace
     assert L.kivi_decode_workspace_size(2048, 32, 8, 32640, 128, 128) == 0
+
+
+@no_gpu
+def test_every_plan_fits_the_noalloc_scratch(L):
+    """Without a device the planner sizes for 152 SMs (a GB300). Its split
+    count keeps the partials near one per planned warp, so over a wide grid of
+    shapes (group sizes 1 to 64, sub-groups included) no workspace exceeds
+    the 4 MiB library-owned scratch of kivi_decode_attend_noalloc."""
+    worst = 0
+    for hkv in (1, 2, 8, 32):
+        for gq in (1, 2, 3, 4, 6, 8, 12, 32, 64):
+            for B in (1, 3, 16, 64, 256):
+                for S in (32, 100, 1024, 4096, 32768, 131072):
+                    for n_res in (0, 37):
+                        worst = max(worst, L.kivi_decode_workspace_size(B, hkv * gq, hkv, S, n_res, 128))
+    assert 3 << 20 < worst <= 4 * 1024 * 1024

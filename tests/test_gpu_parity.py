@@ -2,6 +2,7 @@
 
 Bar: packed codes, scales and zeros bit-exact; dequantized fp16 bit-exact;
 decode-attend max-abs error <= 2e-3 against the float64 oracle."""
+import dataclasses
 import math
 
 import numpy as np
@@ -199,10 +200,13 @@ def test_decode_prefill_workloads(name):
     assert err <= TOL, err
 
 
-def test_decode_batched_workload_sampled():
-    """Batched decode (32 sequences x 4096 cached tokens); the oracle checks a
-    sample of 4 sequences, the GPU runs the full batch and is sliced."""
-    w = synth.WORKLOADS["batched"]
+@pytest.mark.parametrize("hq", [32, 64])
+def test_decode_batched_workload_sampled(hq):
+    """Batched decode (32 sequences x 4096 cached tokens; 4 query heads per KV
+    head as configured, and 8, which runs in two sub-groups of 4 heads); the
+    oracle checks a sample of 4 sequences, the GPU runs the full batch and is
+    sliced."""
+    w = dataclasses.replace(synth.WORKLOADS["batched"], Hq=hq)
     rng = np.random.default_rng(w.seed)
     ch = synth.outlier_channels(w)
     k = synth.keys(rng, (w.BH, w.S_q + w.n_res), w.D, ch, w.outlier_scale)
@@ -228,7 +232,8 @@ def test_decode_batched_workload_sampled():
 @pytest.mark.parametrize("S_q,n_res", [(0, 1), (0, 37), (32, 0), (33, 0), (64, 5), (77, 31),
                                        (1000, 200), (4096, 0), (96, 128)])
 @pytest.mark.parametrize("bits", [2, 4])
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (24, 8), (32, 8), (12, 2), (16, 2)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (24, 8), (32, 8), (40, 8), (12, 2), (28, 4), (16, 2),
+                                     (18, 2), (32, 1)])
 def test_decode_edge_shapes(S_q, n_res, bits, hq, hkv):
     B = 2
     w = synth.Workload("edge", B=B, Hkv=hkv, Hq=hq, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
