@@ -265,6 +265,13 @@ OP_KERNEL_FILES = {"flush_kv": ["flush.cu"], "residual_append": ["residual.cu"],
 LAUNCHES = {"flush_kv": 1, "residual_append": 1, "dequant_kv": 1, "decode_attend": 1}
 
 
+def workload_label(w) -> str:
+    """The step's workload, named the same way by both arms."""
+    return ("%s: single-layer prefill flush + residual append + dequant + decode "
+            "(B=%d, H_kv=%d, Hq=%d, D=%d, S=%d, bits=%d, G=%d, residual_length=%d)"
+            % (w.name, w.B, w.Hkv, w.Hq, w.D, w.S, w.bits, w.G, w.R))
+
+
 def run_gb300(args, rank, world, local_rank):
     import torch
 
@@ -450,9 +457,7 @@ def run_gb300(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "%s: single-layer prefill flush + residual append + dequant + decode "
-                               "(B=%d, H_kv=%d, Hq=%d, D=%d, S=%d, bits=%d, G=%d, residual_length=%d)"
-                               % (w.name, w.B, w.Hkv, w.Hq, w.D, w.S, w.bits, w.G, w.R),
+        "config": {"workload": workload_label(w),
                    "n_flush": probe.n_flush, "n_res": probe.n_res,
                    "l2": "rotating pool of %d independent instances, %.0f MB total (L2 %d MB)"
                          % (pool, pool * inst_bytes / 2 ** 20, l2 >> 20),
@@ -557,7 +562,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * el / steps, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "note": "plain C CPU oracle as the reference arm"},
+            "config": {"workload": workload_label(w), "note": "plain C CPU oracle as the reference arm"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
