@@ -126,7 +126,7 @@ __device__ __forceinline__ void fetch_tile(const DecodeArgs& a, int bh, int tile
 // ---------------------------------------------------------------------------
 
 template <int BITS, int GQ, bool CL>
-__global__ void __launch_bounds__(kThreads, 2) decode_pair_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, kPairs <= 4 ? 2 : 1) decode_pair_kernel(DecodeArgs a) {
     constexpr int NO = 4;  // P.V accumulators per warp: 4-bit [group jj][u], 2-bit [k]
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

@@ -83,7 +83,10 @@ struct DecodePlan {
 constexpr int kResTileTokensMma = 16;
 constexpr int kMergeCounters = 8192;    // (batch, KV head, sub-group) CTA groups that can take split merges
 constexpr int kMaxClusterSplits = 16;   // splits of one head merged inside a thread-block cluster
-constexpr int kPairsPerCta = 4;         // warp pairs per CTA of the warp-pair kernel
+#ifndef KIVI_PAIRS_PER_CTA
+#define KIVI_PAIRS_PER_CTA 4
+#endif
+constexpr int kPairsPerCta = KIVI_PAIRS_PER_CTA;  // warp pairs per CTA of the warp-pair kernel
 
 // Launch with programmatic stream serialization allowed: the kernel may start
 // while the previous kernel on the stream finishes; it must (and every kernel
