@@ -247,6 +247,23 @@ def test_decode_edge_shapes(S_q, n_res, bits, hq, hkv):
     assert err <= TOL, err
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("hq,hkv", [(16, 2), (6, 2)])
+def test_decode_subgroups_many_splits(hq, hkv, bits):
+    """Groups of 8 or 3 query heads per KV head over a long cache: sub-groups of
+    up to 4 heads, each a head group with more splits than a cluster holds
+    (merged through its own ticket counter)."""
+    S_q, n_res = 16384, 100
+    w = synth.Workload("subgroups", B=1, Hkv=hkv, Hq=hq, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
+                       n_outlier=4, outlier_scale=8.0, seed=77 + hq)
+    rng = np.random.default_rng(w.seed)
+    k = synth.keys(rng, (w.BH, S_q + n_res), 128, synth.outlier_channels(w), 8.0)
+    v = synth.normal(rng, (w.BH, S_q + n_res, 128))
+    q = synth.normal(rng, (1, hq, 128))
+    out, ref = decode_case(w, S_q, n_res, k, v, q)
+    assert np.max(np.abs(out - ref)) <= TOL
+
+
 def test_decode_one_workspace_across_sizes():
     """One workspace serves calls of different sizes in turn: after every call
     the merge counters at its start are zero again, and every call matches the
