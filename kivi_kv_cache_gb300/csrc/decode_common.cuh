@@ -1,7 +1,7 @@
 // decode_common.cuh -- PTX helpers shared by the decode kernels: cp.async
-// staging, ldmatrix, the m16n8k16 fp16 MMA, exact code operands (fp8 e4m3
-// conversion, or fp16 subnormals by masking), the fp16 hi/lo split of fp32
-// operands, and thread-block cluster access.
+// staging, ldmatrix, the m16n8k16 fp16 MMA, the units of code operands
+// (fp16 subnormals by masking), the fp16 hi/lo split of fp32 operands, and
+// thread-block cluster access.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -46,25 +46,11 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// bytes 0,1 of w (as e4m3) -> lo, bytes 2,3 -> hi; exact for codes (a code
-// nibble or crumb alone in a byte, read as e4m3, is c * 2^-9)
-__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
-}
-
-#ifndef KIVI_DECODE_SPLIT_FMA
-#define KIVI_DECODE_SPLIT_FMA 1
-#endif
-
 // fp16 hi (lo == false) or lo (lo == true) part of the pair (x, y):
 // hi = fp16(x), lo = fp16(x - hi) (x - hi is exact in fp32). One mixed-
 // precision fma per element, x + hi * m with the fp16 m = -1 (lo) or 0 (hi),
 // gives x - hi or x itself, and one conversion rounds either to fp16.
 __device__ __forceinline__ uint32_t split_pair(float x, float y, bool lo) {
-#if KIVI_DECODE_SPLIT_FMA
     const unsigned short m = lo ? 0xbc00 : 0;  // fp16 -1 or +0
     uint32_t r;
     asm("{\n\t.reg .b32 h;\n\t.reg .b16 hl, hh;\n\t.reg .f32 rx, ry;\n\t"
@@ -76,12 +62,6 @@ __device__ __forceinline__ uint32_t split_pair(float x, float y, bool lo) {
         : "=r"(r)
         : "f"(x), "f"(y), "h"(m));
     return r;
-#else
-    const __half2 h = __floats2half2_rn(x, y);
-    const float2 hf = __half22float2(h);
-    const __half2 l = __floats2half2_rn(__fsub_rn(x, hf.x), __fsub_rn(y, hf.y));
-    return lo ? h2_as_u32(l) : h2_as_u32(h);
-#endif
 }
 
 // Code operands of the decode MMAs: a code masked in place within a 16-bit
