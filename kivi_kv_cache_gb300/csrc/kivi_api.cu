@@ -90,6 +90,10 @@ constexpr int kMmaWarpsPerSm = KIVI_DECODE_MMA_WARPS_PER_SM;
 #endif
 constexpr int kMmaWarpsPerSm2 = KIVI_DECODE_MMA_WARPS_PER_SM_2BIT;
 constexpr int kMmaMaxSplits4 = KIVI_DECODE_MMA_MAX_SPLITS4;
+#ifndef KIVI_DECODE_ONE_WAVE
+#define KIVI_DECODE_ONE_WAVE 1
+#endif
+constexpr bool kOneWave = KIVI_DECODE_ONE_WAVE != 0;
 
 bool mma_group(int gq) { return gq == 1 || gq == 2 || gq == 4; }
 
@@ -106,6 +110,18 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits) {
     if (tpw < 1) tpw = 1;
     p.warps_per_cta = (p.n_tiles + 4 * tpw - 1) / (4 * tpw) > kMmaMaxSplits4 ? 8 : 4;
     if (heads > kMergeCounters) tpw = (p.n_tiles + p.warps_per_cta - 1) / p.warps_per_cta;  // one split each
+    if (kOneWave && tpw >= 2 && heads <= kMergeCounters) {
+        // a grid of multi-tile warps that just spills into a second wave of
+        // resident CTAs (at most 1.25 waves) takes up to half again as many
+        // tiles per warp instead
+        const long long slots = (long long)(16 / p.warps_per_cta) * sm_count();  // 16 warps per SM
+        auto ctas = [&](long long t) { return heads * ((p.n_tiles + p.warps_per_cta * t - 1) / (p.warps_per_cta * t)); };
+        if (ctas(tpw) > slots && 4 * ctas(tpw) <= 5 * slots) {
+            long long t = tpw;
+            while (ctas(t) > slots && 2 * t < 3 * tpw + 2) ++t;
+            if (ctas(t) <= slots) tpw = t;
+        }
+    }
     p.tiles_per_warp = (int)tpw;
     p.tiles_per_split = (int)(p.warps_per_cta * tpw);
     p.pair_kernel = 0;
