@@ -34,7 +34,9 @@
  *   - Numbers: fp16 is IEEE binary16 passed as raw 16-bit words. Inputs must
  *     be finite; NaN/Inf inputs give unspecified codes but every access stays
  *     in bounds.
- *   - Supported shapes: head_dim D = 128, group_size G = 32, bits in {2, 4}.
+ *   - Supported shapes: head_dim D = 128, bits in {2, 4}; group_size G in
+ *     {32, 64, 128} for the flush, dequant and fake quantization, and
+ *     G = 32 for a decode that reads a packed store (S_q > 0).
  *     Other values return KIVI_ERR_UNSUPPORTED.
  *
  * Store layout (one store per tensor, keys and values separately):
@@ -256,7 +258,7 @@ kivi_status kivi_decode_workspace_init(void* workspace, size_t workspace_bytes, 
  * laid out and initialised as described there (may be NULL when that size is
  * 0).
  * Errors: INVALID_ARG if S_q + n_res == 0, S_q > s_cap, n_res > res_cap or
- * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv > 64; WORKSPACE if the workspace is
+ * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv > 64, or if group_size != 32 with S_q > 0; WORKSPACE if the workspace is
  * NULL or too small.
  */
 kivi_status kivi_decode_attend(const void* q_f16,

@@ -74,23 +74,25 @@ __device__ __forceinline__ uint32_t load_word(const uint8_t* p) {
     return __ldg(reinterpret_cast<const uint16_t*>(p));
 }
 
-// keys: one warp per (head, key group, 64-channel half); lane = part*8 + oc,
-// part owns 8 tokens of the group. Scale and zero are per (group, channel).
-template <int BITS>
+// keys: one warp per (head, 32-token block, 64-channel half); lane = part*8
+// + oc, part owns 8 tokens of the block. Scale and zero are per (key group
+// of G tokens, channel): the block's group is block * 32 / G.
+template <int BITS, int G>
 __device__ __forceinline__ void dequant_keys_warp(const DequantArgs& a, int warp_id, int bh) {
     constexpr int ROWB = kD * BITS / 8;
     const int lane = threadIdx.x & 31;
     const int octet = (warp_id & 1) * 8 + (lane & 7);
     const int part = lane >> 3;
-    const int g = warp_id >> 1;
-    if (g >= (a.S + kG - 1) / kG) return;
-    const int t0 = g * kG + part * 8;
+    const int tb = warp_id >> 1;
+    if (tb >= (a.S + 31) / 32) return;
+    const int g = tb * 32 / G;
+    const int t0 = tb * 32 + part * 8;
 
     const uint8_t* crow = a.codes + ((long long)bh * a.s_cap + t0) * ROWB + octet * BITS;
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = (t0 + i < a.S) ? load_word<BITS>(crow + i * ROWB) : 0u;
-    const long long m = ((long long)bh * (a.s_cap / kG) + g) * kD + octet * 8;
+    const long long m = ((long long)bh * (a.s_cap / G) + g) * kD + octet * 8;
     const float4 sa = __ldg(reinterpret_cast<const float4*>(a.scale + m));
     const float4 sb = __ldg(reinterpret_cast<const float4*>(a.scale + m) + 1);
     const uint4 zw = __ldg(reinterpret_cast<const uint4*>(a.zero + m));
@@ -113,8 +115,8 @@ __device__ __forceinline__ void dequant_keys_warp(const DequantArgs& a, int warp
 
 // values: one warp per 8 consecutive tokens of one head; lane = sub*16 +
 // octet, iteration i handles token 2*i + sub. Scale and zero are per (token,
-// 32-channel group).
-template <int BITS>
+// G-channel group).
+template <int BITS, int G>
 __device__ __forceinline__ void dequant_values_warp(const DequantArgs& a, int warp_id, int bh) {
     constexpr int ROWB = kD * BITS / 8;
     constexpr int RPT = 4;
@@ -131,8 +133,8 @@ __device__ __forceinline__ void dequant_values_warp(const DequantArgs& a, int wa
         const long long row = row0 + 2 * i;
         if (tw + 2 * i + sub < a.S) {
             w[i] = load_word<BITS>(a.codes + row * ROWB + octet * BITS);
-            s[i] = __ldg(a.scale + row * (kD / kG) + (octet >> 2));
-            z[i] = __half2float(a.zero[row * (kD / kG) + (octet >> 2)]);
+            s[i] = __ldg(a.scale + row * (kD / G) + octet / (G / 8));
+            z[i] = __half2float(a.zero[row * (kD / G) + octet / (G / 8)]);
         } else {
             w[i] = 0u;
             s[i] = 0.f;
@@ -151,74 +153,95 @@ __device__ __forceinline__ void dequant_values_warp(const DequantArgs& a, int wa
     }
 }
 
-int key_blocks_x(int S) { return ((S + kG - 1) / kG * 2 + 3) / 4; }
+int key_blocks_x(int S) { return ((S + 31) / 32 * 2 + 3) / 4; }
 int value_blocks_x(int S) { return (S + 31) / 32; }
 
-template <int BITS>
+template <int BITS, int G>
 __global__ void __launch_bounds__(kThreads) dequant_keys_kernel(DequantArgs a) {
     pdl_wait();
-    dequant_keys_warp<BITS>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+    dequant_keys_warp<BITS, G>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
 
-template <int BITS>
+template <int BITS, int G>
 __global__ void __launch_bounds__(kThreads) dequant_values_kernel(DequantArgs a) {
     pdl_wait();
-    dequant_values_warp<BITS>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+    dequant_values_warp<BITS, G>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
 
-template <int BITS>
+template <int BITS, int G>
 __global__ void __launch_bounds__(kThreads) dequant_kv_kernel(DequantArgs k, DequantArgs v, int kbx) {
     pdl_wait();
     if ((int)blockIdx.x < kbx)
-        dequant_keys_warp<BITS>(k, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+        dequant_keys_warp<BITS, G>(k, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
     else
-        dequant_values_warp<BITS>(v, (blockIdx.x - kbx) * 4 + (threadIdx.x >> 5), blockIdx.y);
+        dequant_values_warp<BITS, G>(v, (blockIdx.x - kbx) * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
+
 
 DequantArgs head_slice(const DequantArgs& a, int h0, int nh, int bits, int axis) {
     DequantArgs s = a;
     s.BH = nh;
     s.codes += (long long)h0 * a.s_cap * (kD * bits / 8);
-    const long long meta = axis == 0 ? (long long)(a.s_cap / kG) * kD : (long long)a.s_cap * (kD / kG);
+    const long long meta = axis == 0 ? (long long)(a.s_cap / a.G) * kD : (long long)a.s_cap * (kD / a.G);
     s.scale += h0 * meta;
     s.zero += h0 * meta;
     s.out += (long long)h0 * a.S * kD;
     return s;
 }
 
-}  // namespace
-
-cudaError_t launch_dequant(int axis, const DequantArgs& a, int bits, cudaStream_t stream) {
-    if (a.S <= 0 || a.BH <= 0) return cudaSuccess;
+template <int BITS, int G>
+cudaError_t launch_dequant_typed(int axis, const DequantArgs& a, cudaStream_t stream) {
     const int bx = axis == 0 ? key_blocks_x(a.S) : value_blocks_x(a.S);
     for (int h0 = 0; h0 < a.BH; h0 += 65535) {
         const int nh = a.BH - h0 < 65535 ? a.BH - h0 : 65535;
-        const DequantArgs s = head_slice(a, h0, nh, bits, axis);
+        const DequantArgs s = head_slice(a, h0, nh, BITS, axis);
         const dim3 grid(bx, nh);
-        cudaError_t e;
-        if (axis == 0)
-            e = bits == 4 ? launch_pdl(dequant_keys_kernel<4>, grid, kThreads, 0, stream, s)
-                          : launch_pdl(dequant_keys_kernel<2>, grid, kThreads, 0, stream, s);
-        else
-            e = bits == 4 ? launch_pdl(dequant_values_kernel<4>, grid, kThreads, 0, stream, s)
-                          : launch_pdl(dequant_values_kernel<2>, grid, kThreads, 0, stream, s);
+        const cudaError_t e = axis == 0 ? launch_pdl(dequant_keys_kernel<BITS, G>, grid, kThreads, 0, stream, s)
+                                        : launch_pdl(dequant_values_kernel<BITS, G>, grid, kThreads, 0, stream, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_dequant_kv(const DequantArgs& k, const DequantArgs& v, int bits, cudaStream_t stream) {
-    if (k.S <= 0 || k.BH <= 0) return cudaSuccess;
+template <int BITS, int G>
+cudaError_t launch_dequant_kv_typed(const DequantArgs& k, const DequantArgs& v, cudaStream_t stream) {
     const int kbx = key_blocks_x(k.S), vbx = value_blocks_x(v.S);
     for (int h0 = 0; h0 < k.BH; h0 += 65535) {
         const int nh = k.BH - h0 < 65535 ? k.BH - h0 : 65535;
-        const DequantArgs ks = head_slice(k, h0, nh, bits, 0), vs = head_slice(v, h0, nh, bits, 1);
+        const DequantArgs ks = head_slice(k, h0, nh, BITS, 0), vs = head_slice(v, h0, nh, BITS, 1);
         const dim3 grid(kbx + vbx, nh);
-        cudaError_t e = bits == 4 ? launch_pdl(dequant_kv_kernel<4>, grid, kThreads, 0, stream, ks, vs, kbx)
-                                  : launch_pdl(dequant_kv_kernel<2>, grid, kThreads, 0, stream, ks, vs, kbx);
+        const cudaError_t e = launch_pdl(dequant_kv_kernel<BITS, G>, grid, kThreads, 0, stream, ks, vs, kbx);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(int axis, const DequantArgs& a, int bits, cudaStream_t stream) {
+    if (a.S <= 0 || a.BH <= 0) return cudaSuccess;
+    switch (bits * 1000 + a.G) {
+        case 4032: return launch_dequant_typed<4, 32>(axis, a, stream);
+        case 4064: return launch_dequant_typed<4, 64>(axis, a, stream);
+        case 4128: return launch_dequant_typed<4, 128>(axis, a, stream);
+        case 2032: return launch_dequant_typed<2, 32>(axis, a, stream);
+        case 2064: return launch_dequant_typed<2, 64>(axis, a, stream);
+        case 2128: return launch_dequant_typed<2, 128>(axis, a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_dequant_kv(const DequantArgs& k, const DequantArgs& v, int bits, cudaStream_t stream) {
+    if (k.S <= 0 || k.BH <= 0) return cudaSuccess;
+    switch (bits * 1000 + k.G) {
+        case 4032: return launch_dequant_kv_typed<4, 32>(k, v, stream);
+        case 4064: return launch_dequant_kv_typed<4, 64>(k, v, stream);
+        case 4128: return launch_dequant_kv_typed<4, 128>(k, v, stream);
+        case 2032: return launch_dequant_kv_typed<2, 32>(k, v, stream);
+        case 2064: return launch_dequant_kv_typed<2, 64>(k, v, stream);
+        case 2128: return launch_dequant_kv_typed<2, 128>(k, v, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace kivi

@@ -166,8 +166,13 @@ __device__ __forceinline__ float canon(float v) { return __fadd_rn(v, 0.0f); }
 // the quantization of the current one. Rows past n_flush are zero-filled and
 // never read from global memory.
 
-constexpr int kItemBytes = 4096;
-constexpr int kWarpSmem = 2 * kItemBytes;  // two stages
+// A stage holds one 4 KB item; with G > 32 a key item's 8-token parts are padded
+// by one row (kNOc 16-byte chunks) so that the parts of a quarter warp read
+// different banks. Each warp has two stages.
+template <int G>
+struct Stage {
+    static constexpr int kBytes = G > 32 ? 4096 + 512 : 4096;
+};
 #ifndef KIVI_FLUSH_BLOCKS_PER_SM
 #define KIVI_FLUSH_BLOCKS_PER_SM 4
 #endif
@@ -189,22 +194,39 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 struct Items {
-    int key_items;   // BH * ng * 2
+    int key_items;   // BH * ng * (128 / key item channels)
     int val_items;   // BH * ceil(n_flush / 16)
     int ng;          // key groups per head
     int nv;          // value items per head
 };
 
+// Key items of group size G: G tokens x kKeyCh(G) channels (4 KB); a lane owns
+// 8 tokens x 8 channels, lane = part * kNOc + oc.
+template <int G>
+struct KeyShape {
+    static constexpr int kCh = 2048 / G;      // channels of an item: 64, 32 or 16
+    static constexpr int kNOc = kCh / 8;      // 8-channel octets: 8, 4 or 2
+    static constexpr int kNPart = 32 / kNOc;  // 8-token parts: 4, 8 or 16 (= G / 8)
+    static constexpr int kQ = kD / kCh;       // items per key group: 2, 4 or 8
+    static constexpr int kPad = G > 32 ? 1 : 0;  // pad rows per 8-token part in shared memory
+};
+
+template <int G>
 __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& v, const Items& it, int item,
                                            uint8_t* st, int lane) {
+    using KS = KeyShape<G>;
     if (item < it.key_items) {
-        const int half = item & 1, g = (item >> 1) % it.ng, bh = (item >> 1) / it.ng;
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(k.x) + ((long long)bh * k.x_bh_stride + g * kG) * 256 + half * 128;
+        const unsigned u = item;  // item >= 0: unsigned division by the power of two kQ is a shift
+        const int qs = u % KS::kQ, g = (u / KS::kQ) % it.ng, bh = (u / KS::kQ) / it.ng;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(k.x) + ((long long)bh * k.x_bh_stride + g * G) * 256 +
+                             qs * (KS::kCh * 2);
+        constexpr int CPR = KS::kNOc;  // 16-byte chunks per token row
 #pragma unroll
-        for (int i = lane; i < 256; i += 32) {  // 32 rows x 8 chunks
-            const int row = i >> 3, col = i & 7;
-            const bool ok = g * kG + row < k.n_flush;
-            cp_async16(st + i * 16, ok ? (const void*)(src + row * 256 + col * 16) : (const void*)src, ok);
+        for (int i = lane; i < 256; i += 32) {  // G rows x CPR chunks
+            const int row = i / CPR, col = i % CPR;
+            const bool ok = g * G + row < k.n_flush;
+            cp_async16(st + ((row + KS::kPad * (row >> 3)) * CPR + col) * 16,
+                       ok ? (const void*)(src + row * 256 + col * 16) : (const void*)src, ok);
         }
     } else {
         const int vi = item - it.key_items;
@@ -219,11 +241,207 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
     }
 }
 
-// keys: lane = part * 8 + oc; part owns tokens [8 part, 8 part + 8) of the
+// keys: lane = part * kNOc + oc; part owns tokens [8 part, 8 part + 8) of the
+// group, oc owns 8 channels of this item's channel slice. FAKE: write the
+// fake-quantized fp16 rows to a.fq instead of codes, scales and zeros.
+template <int BITS, bool FAKE, int G>
+__device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st, int lane) {
+    using KS = KeyShape<G>;
+    const unsigned u = item;
+    const int qs = u % KS::kQ, g = (u / KS::kQ) % it.ng, bh = (u / KS::kQ) / it.ng;
+    const int oc = lane % KS::kNOc, part = lane / KS::kNOc;
+    const int octet = qs * KS::kNOc + oc;
+    const int t0 = g * G + part * 8;
+    const int nv = min(8, a.n_flush - t0);  // may be <= 0 in a ragged last group
+    const uint4* xs = reinterpret_cast<const uint4*>(st) + (part * (8 + KS::kPad)) * KS::kNOc + oc;  // row stride kNOc
+
+    const __half2 pinf = __half2half2(__ushort_as_half(0x7c00));
+    const __half2 ninf = __half2half2(__ushort_as_half(0xfc00));
+    __half2 mn[4] = {pinf, pinf, pinf, pinf};
+    __half2 mx[4] = {ninf, ninf, ninf, ninf};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i < nv) {
+            const uint4 x = xs[i * KS::kNOc];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                mn[k] = __hmin2(mn[k], u32_as_h2(w[k]));
+                mx[k] = __hmax2(mx[k], u32_as_h2(w[k]));
+            }
+        }
+    }
+#pragma unroll
+    for (int o = KS::kNOc; o < 32; o <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            mn[k] = __hmin2(mn[k], u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(mn[k]), o)));
+            mx[k] = __hmax2(mx[k], u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(mx[k]), o)));
+        }
+    }
+    float z[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 lo = __half22float2(mn[k]);
+        z[2 * k] = canon(lo.x);
+        z[2 * k + 1] = canon(lo.y);
+    }
+    const float L = (float)Levels<BITS>::value;
+    // the part lanes of a column compute its 8 scales: 2 each (4 parts), 1 each
+    // (8 parts), or 1 each in parts 0..7 and again in parts 8..15 (16 parts)
+    constexpr int CPP = KS::kNPart >= 8 ? 1 : 8 / KS::kNPart;
+    float my_s[CPP], my_r[CPP];
+    {
+        const int ch0 = CPP == 1 ? (part & 7) : part * CPP;  // first channel of the octet this lane scales
+        __half2 hx = mx[0], hn = mn[0];                      // the half2 pair holding it (and its neighbour)
+#pragma unroll
+        for (int k = 1; k < 4; ++k)
+            if ((ch0 >> 1) == k) {
+                hx = mx[k];
+                hn = mn[k];
+            }
+        const float2 hi = __half22float2(hx), lo = __half22float2(hn);
+#pragma unroll
+        for (int c = 0; c < CPP; ++c) {
+            const bool odd = ((ch0 + c) & 1) != 0;
+            my_s[c] = __fdiv_rn(__fsub_rn(canon(odd ? hi.y : hi.x), canon(odd ? lo.y : lo.x)), L);
+            my_r[c] = my_s[c] == 0.0f ? 0.0f : __frcp_rn(my_s[c]);
+        }
+    }
+    float s[8], r[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int src = (k / CPP) * KS::kNOc + oc;
+        s[k] = __shfl_sync(0xffffffffu, my_s[k % CPP], src);
+        r[k] = __shfl_sync(0xffffffffu, my_r[k % CPP], src);
+    }
+    f32x2 z2[4], r2[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        z2[k] = pk(z[2 * k], z[2 * k + 1]);
+        r2[k] = pk(r[2 * k], r[2 * k + 1]);
+    }
+    if (FAKE) {
+        uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * kD) + octet;
+#pragma unroll 1
+        for (int i = 0; i < nv; ++i) frow[i * (kD / 8)] = fake8(xs[i * KS::kNOc], z2, r2, s);
+        return;
+    }
+    if (part == 0) {
+        const long long m = ((long long)bh * (a.s_cap / G) + a.s_off / G + g) * kD + octet * 8;
+        float4* sp = reinterpret_cast<float4*>(a.scale + m);
+        sp[0] = make_float4(s[0], s[1], s[2], s[3]);
+        sp[1] = make_float4(s[4], s[5], s[6], s[7]);
+        uint4 zp;
+        zp.x = h2_as_u32(__floats2half2_rn(z[0], z[1]));
+        zp.y = h2_as_u32(__floats2half2_rn(z[2], z[3]));
+        zp.z = h2_as_u32(__floats2half2_rn(z[4], z[5]));
+        zp.w = h2_as_u32(__floats2half2_rn(z[6], z[7]));
+        *reinterpret_cast<uint4*>(a.zero + m) = zp;
+    }
+    constexpr int ROWB = kD * BITS / 8;
+    uint8_t* crow = a.codes + ((long long)bh * a.s_cap + a.s_off + t0) * ROWB + octet * BITS;
+    auto store_row = [&](int i, uint32_t packed) {
+        if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
+        else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
+    };
+#pragma unroll (kKeyUnroll)
+    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS>(xs[i * KS::kNOc], z2, r2, s));
+}
+
+// min and max of the 8 fp16 of each vector of x, as half2 (min and max of fp16
+// are exact, so the order is free)
+template <int N>
+__device__ __forceinline__ void minmax_tree(const uint4 (&x)[N], __half2& m2, __half2& x2) {
+    __half2 mk[N], xk[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        const __half2 a = u32_as_h2(x[k].x), b = u32_as_h2(x[k].y), c = u32_as_h2(x[k].z), d = u32_as_h2(x[k].w);
+        mk[k] = __hmin2(__hmin2(a, b), __hmin2(c, d));
+        xk[k] = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    }
+#pragma unroll
+    for (int w = 1; w < N; w <<= 1)
+#pragma unroll
+        for (int k = 0; k + w < N; k += 2 * w) {
+            mk[k] = __hmin2(mk[k], mk[k + w]);
+            xk[k] = __hmax2(xk[k], xk[k + w]);
+        }
+    m2 = mk[0];
+    x2 = xk[0];
+}
+
+// values: lane = 16 jp + row holds 64 channels of row `row` of the item,
+// channels 64 jp .. 64 jp + 63: two groups (G = 32), one (G = 64), or half of
+// one, whose min/max it shares with its partner lane (lane ^ 16) (G = 128).
+// Min/max, scale and codes of a group stay in its lane(s); one code store per
+// group or half group.
+template <int BITS, bool FAKE, int G>
+__device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
+                                           int lane) {
+    const int vi = item - it.key_items;
+    const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
+    const int row = lane & 15, jp = lane >> 4;
+    const bool valid = t0 + row < a.n_flush;
+    if (G != 128 && !valid) return;  // (G = 128: both lanes of a row leave together below)
+    const float L = (float)Levels<BITS>::value;
+    const uint4* xs = reinterpret_cast<const uint4*>(st + row * 256);
+    const long long grow = (long long)bh * a.s_cap + a.s_off + t0 + row;
+    constexpr int NG = G == 32 ? 2 : 1;      // groups (or half groups) per lane
+    constexpr int NVEC = G == 32 ? 4 : 8;    // 16-byte vectors per group (or half group) in this lane
+#pragma unroll
+    for (int e = 0; e < NG; ++e) {
+        const int cv = (64 * jp + (G == 32 ? 32 * e : 0)) / 8;  // first vector of this lane's channels
+        uint4 x[NVEC];
+#pragma unroll
+        for (int k = 0; k < NVEC; ++k) x[k] = xs[(cv + k) ^ (row & 7)];
+        __half2 m2, x2;
+        minmax_tree<NVEC>(x, m2, x2);
+        if (G == 128) {  // the other half of the group sits in lane ^ 16 (same row)
+            m2 = __hmin2(m2, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(m2), 16)));
+            x2 = __hmax2(x2, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(x2), 16)));
+            if (!valid) return;
+        }
+        const float z = canon(__half2float(__hmin(__low2half(m2), __high2half(m2))));
+        const float sc = __fdiv_rn(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z), L);
+        const float rc = sc == 0.0f ? 0.0f : __frcp_rn(sc);
+        const f32x2 z1 = pk(z, z), r1 = pk(rc, rc);
+        const f32x2 z2[4] = {z1, z1, z1, z1}, r2[4] = {r1, r1, r1, r1};
+        const float sv[8] = {sc, sc, sc, sc, sc, sc, sc, sc};
+        const int j = (64 * jp + (G == 32 ? 32 * e : 0)) / G;  // this group's index in the row
+        if (FAKE) {
+            uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * kD) + cv;
+#pragma unroll
+            for (int k = 0; k < NVEC; ++k) frow[k] = fake8(x[k], z2, r2, sv);
+        } else {
+            uint32_t pq[NVEC];
+#pragma unroll
+            for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS>(x[k], z2, r2, sv);
+            uint8_t* cdst = a.codes + grow * (kD * BITS / 8) + cv * BITS;  // 8 channels per vector
+            if (BITS == 4) {
+#pragma unroll
+                for (int k = 0; k < NVEC; k += 4)
+                    *reinterpret_cast<uint4*>(cdst + 4 * k) = make_uint4(pq[k], pq[k + 1], pq[k + 2], pq[k + 3]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NVEC; k += 4)
+                    *reinterpret_cast<uint2*>(cdst + 2 * k) =
+                        make_uint2(pq[k] | (pq[k + 1] << 16), pq[k + 2] | (pq[k + 3] << 16));
+            }
+            if (G != 128 || jp == 0) {
+                a.scale[grow * (kD / G) + j] = sc;
+                a.zero[grow * (kD / G) + j] = __float2half_rn(z);
+            }
+        }
+    }
+}
+
+// G = 32 keys (the measured fast path, kept as written for that size):
+// lane = part * 8 + oc; part owns tokens [8 part, 8 part + 8) of the
 // group, oc owns 8 channels of this 64-channel half. FAKE: write the fake-
 // quantized fp16 rows to a.fq instead of codes, scales and zeros.
 template <int BITS, bool FAKE>
-__device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st, int lane) {
+__device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it, int item, const uint8_t* st, int lane) {
     const int half = item & 1, g = (item >> 1) % it.ng, bh = (item >> 1) / it.ng;
     const int oc = lane & 7, part = lane >> 3;
     const int octet = half * 8 + oc;
@@ -319,12 +537,12 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS>(xs[i * 8], z2, r2, s));
 }
 
-// values: lane = 16 jp + row; the lane quantizes the groups j = 2 jp and
+// G = 32 values: lane = 16 jp + row; the lane quantizes the groups j = 2 jp and
 // 2 jp + 1 (32 channels each) of row `row` of the item: min/max, scale and
 // codes of a whole group in one lane, no shuffles, one 16-byte code store
 // (4-bit) per group.
 template <int BITS, bool FAKE>
-__device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
+__device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
                                            int lane) {
     const int vi = item - it.key_items;
     const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
@@ -381,39 +599,45 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
 
 // Keys, values, or both: warp w of the grid handles items w, w + W, ... of the
 // list [key items | value items] (W = total warps).
-template <int BITS, bool FAKE>
+template <int BITS, bool FAKE, int G>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint8_t* const base = smem + warp * kWarpSmem;
+    constexpr int kStageBytes = Stage<G>::kBytes;
+    uint8_t* const base = smem + warp * 2 * kStageBytes;
     const int total = it.key_items + it.val_items;
     const int stride = gridDim.x * (kThreads / 32);
     int item = blockIdx.x * (kThreads / 32) + warp;
     pdl_wait();
-    if (item < total) fetch_item(k, v, it, item, base, lane);
+    if (item < total) fetch_item<G>(k, v, it, item, base, lane);
     cp_async_commit();
-    if (item + stride < total) fetch_item(k, v, it, item + stride, base + kItemBytes, lane);
+    if (item + stride < total) fetch_item<G>(k, v, it, item + stride, base + kStageBytes, lane);
     cp_async_commit();
     pdl_trigger();
     for (int n = 0; item < total; item += stride, ++n) {
-        uint8_t* S = base + (n & 1) * kItemBytes;  // stage n mod 2
+        uint8_t* S = base + (n & 1) * kStageBytes;  // stage n mod 2
         cp_async_wait1();
         __syncwarp();
-        if (item < it.key_items) key_item<BITS, FAKE>(k, it, item, S, lane);
-        else value_item<BITS, FAKE>(v, it, item, S, lane);
+        if (G == 32) {  // the generic item code at G = 32 measured 0.7 % slower than this form
+            if (item < it.key_items) key_item_g32<BITS, FAKE>(k, it, item, S, lane);
+            else value_item_g32<BITS, FAKE>(v, it, item, S, lane);
+        } else {
+            if (item < it.key_items) key_item<BITS, FAKE, G>(k, it, item, S, lane);
+            else value_item<BITS, FAKE, G>(v, it, item, S, lane);
+        }
         __syncwarp();
-        if (item + 2 * stride < total) fetch_item(k, v, it, item + 2 * stride, S, lane);
+        if (item + 2 * stride < total) fetch_item<G>(k, v, it, item + 2 * stride, S, lane);
         cp_async_commit();
     }
 }
 
-template <int BITS, bool FAKE>
+template <int BITS, bool FAKE, int G>
 cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
     static int grid_cap = 0;
-    static bool configured = false;
-    const int smem = (kThreads / 32) * kWarpSmem;
+    static bool configured = false;  // benign race: every caller sets the same values
+    const int smem = (kThreads / 32) * 2 * Stage<G>::kBytes;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, FAKE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, FAKE, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -425,7 +649,7 @@ cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it
     if (total <= 0) return cudaSuccess;
     long long blocks = (total + 3) / 4;
     if (blocks > grid_cap) blocks = grid_cap;
-    return launch_pdl(flush_kernel<BITS, FAKE>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
+    return launch_pdl(flush_kernel<BITS, FAKE, G>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
 }
 
 // Pointers of heads [h0, h0 + nh) of a flush.
@@ -438,10 +662,18 @@ FlushArgs head_slice(const FlushArgs& a, int h0, int nh, int bits, int axis) {
         return s;
     }
     s.codes += (long long)h0 * a.s_cap * (kD * bits / 8);
-    const long long meta = axis == 0 ? (long long)(a.s_cap / kG) * kD : (long long)a.s_cap * (kD / kG);
+    const long long meta = axis == 0 ? (long long)(a.s_cap / a.G) * kD : (long long)a.s_cap * (kD / a.G);
     s.scale += h0 * meta;
     s.zero += h0 * meta;
     return s;
+}
+
+template <int BITS, bool FAKE>
+cudaError_t launch_items_g(const FlushArgs& k, const FlushArgs& v, const Items& it, int G, cudaStream_t stream) {
+    if (G == 32) return launch_items<BITS, FAKE, 32>(k, v, it, stream);
+    if (G == 64) return launch_items<BITS, FAKE, 64>(k, v, it, stream);
+    if (G == 128) return launch_items<BITS, FAKE, 128>(k, v, it, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -451,8 +683,10 @@ cudaError_t launch_flush_impl(const FlushArgs& k, const FlushArgs& v, bool do_k,
                               cudaStream_t stream) {
     const FlushArgs& a = do_k ? k : v;
     if (a.n_flush <= 0 || a.BH <= 0) return cudaSuccess;
-    const int ng = (a.n_flush + kG - 1) / kG, nv = (a.n_flush + 15) / 16;
-    const int per_head = (do_k ? 2 * ng : 0) + (do_v ? nv : 0);
+    const int G = a.G;
+    const int ng = (a.n_flush + G - 1) / G, nv = (a.n_flush + 15) / 16;
+    const int kq = kD / (2048 / G);  // key items per group
+    const int per_head = (do_k ? kq * ng : 0) + (do_v ? nv : 0);
     const int max_heads = (int)(0x3fffffff / per_head) > 0 ? (int)(0x3fffffff / per_head) : 1;
     for (int h0 = 0; h0 < a.BH; h0 += max_heads) {
         const int nh = a.BH - h0 < max_heads ? a.BH - h0 : max_heads;
@@ -462,11 +696,13 @@ cudaError_t launch_flush_impl(const FlushArgs& k, const FlushArgs& v, bool do_k,
         Items it;
         it.ng = ng;
         it.nv = nv;
-        it.key_items = do_k ? nh * 2 * ng : 0;
+        it.key_items = do_k ? nh * kq * ng : 0;
         it.val_items = do_v ? nh * nv : 0;
         const bool fake = a.fq != nullptr;
-        cudaError_t e = bits == 4 ? (fake ? launch_items<4, true>(ks, vs, it, stream) : launch_items<4, false>(ks, vs, it, stream))
-                                  : (fake ? launch_items<2, true>(ks, vs, it, stream) : launch_items<2, false>(ks, vs, it, stream));
+        cudaError_t e = bits == 4 ? (fake ? launch_items_g<4, true>(ks, vs, it, G, stream)
+                                          : launch_items_g<4, false>(ks, vs, it, G, stream))
+                                  : (fake ? launch_items_g<2, true>(ks, vs, it, G, stream)
+                                          : launch_items_g<2, false>(ks, vs, it, G, stream));
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

@@ -36,8 +36,9 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Flush, dequant and fake quantization: D = 128, G in {32, 64, 128}, 2 or 4 bits.
 kivi_status shape_check(int D, int G, int bits) {
-    if (D != kD || G != kG || (bits != 2 && bits != 4)) return KIVI_ERR_UNSUPPORTED;
+    if (D != kD || (G != 32 && G != 64 && G != 128) || (bits != 2 && bits != 4)) return KIVI_ERR_UNSUPPORTED;
     return KIVI_OK;
 }
 
@@ -170,8 +171,9 @@ kivi_status flush_check(const void* x, int BH, int S, int x_bh_stride, int D, in
 }
 
 FlushArgs flush_args(const void* x, int BH, int x_bh_stride, int n, void* codes, float* scale,
-                     void* zero, int s_off, int s_cap) {
+                     void* zero, int s_off, int s_cap, int G) {
     FlushArgs a;
+    a.G = G;
     a.x = static_cast<const __half*>(x);
     a.x_bh_stride = x_bh_stride;
     a.BH = BH;
@@ -193,7 +195,7 @@ kivi_status flush_one(int axis, const void* x, int BH, int S, int x_bh_stride, i
     if (st != KIVI_OK) return st;
     if (n_flushed) *n_flushed = n;
     if (n == 0) return KIVI_OK;
-    return from_cuda(launch_flush(axis, flush_args(x, BH, x_bh_stride, n, codes, scale, zero, s_off, s_cap),
+    return from_cuda(launch_flush(axis, flush_args(x, BH, x_bh_stride, n, codes, scale, zero, s_off, s_cap, G),
                                   bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -219,8 +221,8 @@ kivi_status fake_quant(const void* k, const void* v, bool do_k, bool do_v, int B
         return KIVI_ERR_ALIGNMENT;
     const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
     if (n > 0) {
-        FlushArgs ka = flush_args(do_k ? k : v, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G);
-        FlushArgs va = flush_args(do_v ? v : k, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G);
+        FlushArgs ka = flush_args(do_k ? k : v, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G);
+        FlushArgs va = flush_args(do_v ? v : k, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G);
         ka.fq = static_cast<__half*>(do_k ? k_out : v_out);
         va.fq = static_cast<__half*>(do_v ? v_out : k_out);
         ka.fq_bh_stride = va.fq_bh_stride = out_bh_stride;
@@ -319,8 +321,8 @@ kivi_status kivi_flush_kv(const void* k_f16, const void* v_f16, int BH, int S, i
     if (n_flushed) *n_flushed = nk;
     if (nk == 0) return KIVI_OK;
     return from_cuda(launch_flush_kv(
-        flush_args(k_f16, BH, x_bh_stride, nk, kcodes_u8, kscale, kzero_f16, s_off, s_cap),
-        flush_args(v_f16, BH, x_bh_stride, nv, vcodes_u8, vscale, vzero_f16, s_off, s_cap), bits,
+        flush_args(k_f16, BH, x_bh_stride, nk, kcodes_u8, kscale, kzero_f16, s_off, s_cap, group_size),
+        flush_args(v_f16, BH, x_bh_stride, nv, vcodes_u8, vscale, vzero_f16, s_off, s_cap, group_size), bits,
         reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -344,6 +346,7 @@ kivi_status kivi_dequant(kivi_axis axis, const void* codes_u8, const float* scal
     a.S = S;
     a.s_cap = s_cap;
     a.out = static_cast<__half*>(out_f16);
+    a.G = group_size;
     return from_cuda(launch_dequant((int)axis, a, bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -372,6 +375,7 @@ kivi_status kivi_dequant_kv(const void* kcodes_u8, const float* kscale, const vo
     k.BH = v.BH = BH;
     k.S = v.S = S;
     k.s_cap = v.s_cap = s_cap;
+    k.G = v.G = group_size;
     return from_cuda(launch_dequant_kv(k, v, bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -446,6 +450,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
                                int D, int group_size, int bits, float sm_scale, float* out_f32,
                                void* workspace, size_t workspace_bytes_, kivi_stream_t stream) {
     kivi_status st = shape_check(D, group_size, bits);
+    if (st == KIVI_OK && group_size != kG && S_q > 0) st = KIVI_ERR_UNSUPPORTED;  // the decode reads G = 32 stores
     if (st != KIVI_OK) return st;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S_q < 0 || n_res < 0 ||
         S_q + n_res == 0 || S_q > s_cap || n_res > res_cap || s_cap < 0 || res_cap < 0 ||

@@ -24,6 +24,7 @@ struct FlushArgs {
     int s_cap;
     __half* fq = nullptr;      // fake quantization: fp16 reconstructions [BH, fq_bh_stride, D] instead of a store
     long long fq_bh_stride = 0;
+    int G = kG;                // group size: 32, 64 or 128
 };
 
 struct DequantArgs {
@@ -34,6 +35,7 @@ struct DequantArgs {
     int S;
     int s_cap;
     __half* out;          // [BH, S, D]
+    int G = kG;           // group size: 32, 64 or 128
 };
 
 struct DecodeArgs {

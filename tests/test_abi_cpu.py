@@ -76,7 +76,10 @@ def flush(L, name="kivi_flush_keys", x=FAKE, BH=8, S=256, stride=256, D=128, G=3
 def test_flush_rejects_bad_arguments_without_launching(L, name):
     assert flush(L, name, bits=3)[0] == UNSUPPORTED
     assert flush(L, name, D=64)[0] == UNSUPPORTED
-    assert flush(L, name, G=64)[0] == UNSUPPORTED
+    assert flush(L, name, G=16)[0] == UNSUPPORTED
+    assert flush(L, name, G=256)[0] == UNSUPPORTED
+    assert flush(L, name, G=96)[0] == UNSUPPORTED
+    assert flush(L, name, G=64, s_cap=288)[0] == INVALID     # not a multiple of G
     assert flush(L, name, BH=0)[0] == INVALID
     assert flush(L, name, S=-1)[0] == INVALID
     assert flush(L, name, stride=100)[0] == INVALID          # head stride < S
@@ -127,6 +130,7 @@ def decode(L, q=FAKE, S_q=2080, s_cap=2080, n_res=158, res_cap=160, B=1, Hq=32, 
 @no_gpu
 def test_decode_rejects_bad_arguments(L):
     assert decode(L, Hq=12) == INVALID               # 12 / 8 is not an integer
+    assert decode(L, G=64) == UNSUPPORTED            # the decode reads G = 32 stores
     assert decode(L, Hq=520) == UNSUPPORTED          # 65 query heads per KV head
     assert decode(L, Hq=1024) == UNSUPPORTED         # 128 query heads per KV head
     assert decode(L, S_q=0, n_res=0) == INVALID

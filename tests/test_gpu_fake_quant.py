@@ -106,3 +106,18 @@ def test_fake_quant_short_inputs(S, R):
         ref, n_ref = oracle_fake(axis, x, R)
         assert n == n_ref
         assert same(host(out), ref), (S, R, axis)
+
+
+@pytest.mark.parametrize("G", [64, 128])
+@pytest.mark.parametrize("bits", [2, 4])
+def test_fake_quant_group_sizes(G, bits):
+    rng = np.random.default_rng(90 + G + bits)
+    for S, R in [(100, 0), (700, 128)]:
+        k = synth.keys(rng, (3, S), 128, np.array([3, 64, 65, 127]), 10.0)
+        v = synth.normal(rng, (3, S, 128))
+        for axis, x in ((0, k), (1, v)):
+            fn = kv.kivi_fake_quant_keys if axis == 0 else kv.kivi_fake_quant_values
+            out, n = fn(dev(x), R, G=G, bits=bits)
+            ref, n_ref = oracle_fake(axis, x, R, G, bits)
+            assert n == n_ref
+            assert same(host(out), ref), (G, bits, S, axis)

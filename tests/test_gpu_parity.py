@@ -129,6 +129,47 @@ def test_flush_adversarial(bits, axis):
     assert np.array_equal(host(kv.kivi_dequant(gs, n)).view(np.uint16), oracle.dequant(rs, n).view(np.uint16))
 
 
+@pytest.mark.parametrize("G", [64, 128])
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("axis", [0, 1])
+def test_flush_dequant_group_sizes(G, bits, axis):
+    """Group sizes 64 and 128: ragged lengths (residual_length 0 flushes every
+    token), residual windows, and the adversarial rows; codes, scales, zeros
+    and dequantized fp16 bit-exact against the oracle."""
+    rng = np.random.default_rng(300 + G + bits + axis)
+    ch = np.array([3, 64, 65, 127])
+    for S, R in [(1, 0), (63, 0), (64, 0), (129, 0), (300, 0), (700, 128), (2238, 128)]:
+        BH = int(rng.integers(1, 5))
+        x = synth.keys(rng, (BH, S), 128, ch, 10.0) if axis == 0 else synth.normal(rng, (BH, S, 128))
+        n, gs, rs = flush_both(axis, x, R, G, bits)
+        assert n == oracle.flush_count(S, R, G)
+        assert_store_equal(gs, rs, "G=%d S=%d" % (G, S))
+        if n:
+            d = host(kv.kivi_dequant(gs, n))
+            assert np.array_equal(d.view(np.uint16), oracle.dequant(rs, n).view(np.uint16)), (G, S)
+    x = adversarial(rng, 3, 2 * G + 17)
+    n, gs, rs = flush_both(axis, x, 0, G, bits)
+    assert_store_equal(gs, rs, "adversarial G=%d" % G)
+    assert np.array_equal(host(kv.kivi_dequant(gs, n)).view(np.uint16), oracle.dequant(rs, n).view(np.uint16))
+
+
+@pytest.mark.parametrize("G", [64, 128])
+def test_fused_kv_flush_and_dequant_group_sizes(G):
+    w = synth.WORKLOADS["qwen8b"]
+    k, v, _ = synth.prefill_inputs(w)
+    n = kv.kivi_flush_count(w.S, w.R, G)
+    ks = kv.KiviStore(0, w.BH, n, w.D, G, w.bits, device=DEV)
+    vs = kv.KiviStore(1, w.BH, n, w.D, G, w.bits, device=DEV)
+    assert kv.kivi_flush_kv(dev(k), dev(v), w.R, ks, vs) == n
+    rk = oracle.flush(0, k, n, oracle.Store(0, w.BH, n, w.D, G, w.bits))
+    rv = oracle.flush(1, v, n, oracle.Store(1, w.BH, n, w.D, G, w.bits))
+    assert_store_equal(ks, rk)
+    assert_store_equal(vs, rv)
+    kd, vd = kv.kivi_dequant_kv(ks, vs, n)
+    assert np.array_equal(host(kd).view(np.uint16), oracle.dequant(rk, n).view(np.uint16))
+    assert np.array_equal(host(vd).view(np.uint16), oracle.dequant(rv, n).view(np.uint16))
+
+
 @pytest.mark.parametrize("axis", [0, 1])
 def test_flush_into_offset_of_larger_cache(axis):
     """Flush a strided view (head stride 300 tokens) at store offset 64."""
