@@ -656,19 +656,24 @@ def run_sweep(args):
     # 8, 6 and 3 query heads per KV head (sub-groups of up to 4 heads)
     cases += [(1, 16384 - 128, 128, 4, 64), (32, 4032, 64, 4, 64), (1, 4096 - 128, 128, 4, 64),
               (32, 4032, 64, 4, 48), (32, 4032, 64, 4, 24)]
+    # stores of group size 64 and 128
+    cases += [(1, 2080, 158, 4, 32, 64), (1, 16384 - 128, 128, 4, 32, 64), (1, 16384 - 128, 128, 4, 32, 128),
+              (32, 4032, 64, 4, 32, 64), (32, 4032, 64, 4, 32, 128), (1, 32768 - 128, 128, 2, 32, 128)]
     for case in cases:
         B, S_q, n_res, bits = case[:4]
         Hq = case[4] if len(case) > 4 else 32
-        w = synth.Workload("decode", B=B, Hkv=8, Hq=Hq, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
+        G = case[5] if len(case) > 5 else 32
+        w = synth.Workload("decode", B=B, Hkv=8, Hq=Hq, D=128, S=S_q + n_res, bits=bits, G=G, R=0,
                            n_outlier=4, outlier_scale=8.0, seed=11)
+        s_cap = max(1, -(-S_q // G)) * G
         per_tok = 2 * w.D * bits / 8 + w.D * 6 / w.G + (w.D // w.G) * 6
         nbytes = w.BH * S_q * per_tok + w.BH * n_res * w.D * 4 + B * w.Hq * w.D * 6
         P = pool_count(nbytes)
         entries = []
         for i in range(P):
             k, v, q = synth.prefill_inputs_torch(w, 9000 + i, dev)
-            gk = kv.KiviStore(0, w.BH, max(S_q, w.G), w.D, w.G, bits, device=dev)
-            gv = kv.KiviStore(1, w.BH, max(S_q, w.G), w.D, w.G, bits, device=dev)
+            gk = kv.KiviStore(0, w.BH, s_cap, w.D, w.G, bits, device=dev)
+            gv = kv.KiviStore(1, w.BH, s_cap, w.D, w.G, bits, device=dev)
             if S_q > 0:
                 kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
             kr = k[:, S_q:].contiguous()
@@ -682,7 +687,7 @@ def run_sweep(args):
         fns = [lambda e=e: kv.kivi_decode_attend(e[0], e[1], e[2], S_q, e[3], e[4], n_res, w.Hkv, w.sm_scale,
                                                  out=e[5], workspace=e[6]) for e in entries]
         timed(fns, nbytes, "decode_attend", {"B": B, "Hkv": 8, "Hq": Hq, "S_kv": S_q + n_res, "bits": bits,
-                                             "pool": P, "tokens_per_s": None})
+                                             "G": G, "pool": P, "tokens_per_s": None})
         del entries, fns
         torch.cuda.empty_cache()
 

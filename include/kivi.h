@@ -35,8 +35,7 @@
  *     be finite; NaN/Inf inputs give unspecified codes but every access stays
  *     in bounds.
  *   - Supported shapes: head_dim D = 128, bits in {2, 4}; group_size G in
- *     {32, 64, 128} for the flush, dequant and fake quantization, and
- *     G = 32 for a decode that reads a packed store (S_q > 0).
+ *     {32, 64, 128} for the flush, dequant, fake quantization and the decode.
  *     Other values return KIVI_ERR_UNSUPPORTED.
  *
  * Store layout (one store per tensor, keys and values separately):
@@ -214,8 +213,8 @@ kivi_status kivi_fake_quant_kv(const void* k_f16, const void* v_f16, int BH, int
 
 /*
  * Bytes of device workspace kivi_decode_attend needs for these sizes on the
- * current device, for either bit width (the split count depends on the
- * device's SM count and on the bit width). Returns
+ * current device, for any bit width and group size (the split count depends
+ * on the device's SM count, the bit width and the group size). Returns
  * 0 when the decode runs as a single split per (batch, KV head) and needs no
  * workspace, and 0 for invalid sizes. Host only (reads the device's SM count
  * once).
@@ -258,8 +257,10 @@ kivi_status kivi_decode_workspace_init(void* workspace, size_t workspace_bytes, 
  * laid out and initialised as described there (may be NULL when that size is
  * 0).
  * Errors: INVALID_ARG if S_q + n_res == 0, S_q > s_cap, n_res > res_cap or
- * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv > 64, or if group_size != 32 with S_q > 0; WORKSPACE if the workspace is
- * NULL or too small.
+ * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv > 64 (or D, group_size, bits as for
+ * the flush); WORKSPACE if the workspace is NULL or too small. Stores of
+ * every supported group size (32, 64, 128) are read; their key groups align
+ * with the kernels' 32-token tiles.
  */
 kivi_status kivi_decode_attend(const void* q_f16,
                                const void* kcodes_u8, const float* kscale, const void* kzero_f16,

@@ -98,14 +98,47 @@ __device__ __forceinline__ void fetch_store_tile(const DecodeArgs& a, int bh, in
         const int sw = BITS == 4 ? (col ^ ((row >> 1) & 3)) : (col ^ ((row >> 2) & 1));
         cp_async16(st + kVC + row * ROWB + sw * 16, vc + i * 16, true);
     }
-    const float* ks = a.kscale + ((long long)bh * (a.s_cap / kG) + tile) * kD;
-    const __half* kz = a.kzero + ((long long)bh * (a.s_cap / kG) + tile) * kD;
+    // the key group (32 << g_shift tokens) holding this tile, and the value
+    // metadata of its 32 tokens: (kD / 32) >> g_shift entries per token, packed
+    // at the front of VS and VZ (widen_value_meta spreads them for G > 32)
+    const int sh = a.g_shift;
+    const long long krow = (long long)bh * (a.s_cap >> (5 + sh)) + (tile >> sh);
+    const float* ks = a.kscale + krow * kD;
+    const __half* kz = a.kzero + krow * kD;
     cp_async16(st + kKS + padc(lane * 4) * 4, ks + lane * 4, true);
     if (lane < 16) cp_async16(st + kKZ + lane * 16, kz + lane * 8, true);
-    const float* vs = a.vscale + ((long long)bh * a.s_cap + tok0) * (kD / kG);
-    const __half* vz = a.vzero + ((long long)bh * a.s_cap + tok0) * (kD / kG);
-    cp_async16(st + kVS + lane * 16, vs + lane * 4, true);
-    if (lane < 16) cp_async16(st + kVZ + lane * 16, vz + lane * 8, true);
+    const long long vrow = ((long long)bh * a.s_cap + tok0) * ((kD / 32) >> sh);
+    const float* vs = a.vscale + vrow;
+    const __half* vz = a.vzero + vrow;
+    if (lane < (32 >> sh)) cp_async16(st + kVS + lane * 16, vs + lane * 4, true);
+    if (lane < (16 >> sh)) cp_async16(st + kVZ + lane * 16, vz + lane * 8, true);
+}
+
+// A store of group size 64 (g_shift 1) or 128 (g_shift 2) has 2 or 1 value
+// scale and zero per token; the tile code reads one per 32 channels (VS and VZ
+// [32 tokens][4]). Each lane takes its token's entries, then, once the warp has
+// read them all, writes them back repeated 2 or 4 times.
+__device__ __forceinline__ void widen_value_meta(uint8_t* st, int sh, int lane) {
+    float* vs = reinterpret_cast<float*>(st + kVS);
+    uint8_t* vz = st + kVZ;
+    float4 s4;
+    uint2 z4;
+    if (sh == 1) {
+        const float2 s = reinterpret_cast<const float2*>(vs)[lane];
+        const uint32_t z = reinterpret_cast<const uint32_t*>(vz)[lane];
+        const uint32_t z0 = z & 0xffffu, z1 = z >> 16;
+        s4 = make_float4(s.x, s.x, s.y, s.y);
+        z4 = make_uint2(z0 | (z0 << 16), z1 | (z1 << 16));
+    } else {
+        const float s = vs[lane];
+        const uint32_t z = reinterpret_cast<const uint16_t*>(vz)[lane];
+        s4 = make_float4(s, s, s, s);
+        z4 = make_uint2(z | (z << 16), z | (z << 16));
+    }
+    __syncwarp();
+    reinterpret_cast<float4*>(vs)[lane] = s4;
+    reinterpret_cast<uint2*>(vz)[lane] = z4;
+    __syncwarp();
 }
 
 // kResTok fp16 rows of K into st0 and of V into st1, 16-byte chunk c of row r
@@ -227,6 +260,7 @@ __global__ void __launch_bounds__(32 * NW, 16 / NW) decode_mma_kernel(DecodeArgs
         uint8_t* S = st0 + (it & 1) * kStage;
         cp_async_wait<1>();
         __syncwarp();
+        if (a.g_shift != 0) widen_value_meta(S, a.g_shift, lane);
         const int nvalid = min(32, a.S_q - tile * 32);
         if (nvalid < 32) {  // zero the value metadata of rows past S_q
             float* vsz = reinterpret_cast<float*>(S + kVS);

@@ -98,7 +98,8 @@ constexpr bool kOneWave = KIVI_DECODE_ONE_WAVE != 0;
 
 bool mma_group(int gq) { return gq == 1 || gq == 2 || gq == 4; }
 
-DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits) {
+// pair_ok: the warp-pair kernel may run (it reads stores of group size 32 only)
+DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool pair_ok) {
     DecodePlan p;
     const int gq = Hkv > 0 && Hq >= Hkv ? Hq / Hkv : 1;
     p.q_sub = mma_group(gq) ? 1 : (gq + 3) / 4;
@@ -126,7 +127,7 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits) {
     p.tiles_per_warp = (int)tpw;
     p.tiles_per_split = (int)(p.warps_per_cta * tpw);
     p.pair_kernel = 0;
-    if (mma_group(gq) && (kPairMode == 1 || (kPairMode == 2 && tpw <= kPairMaxWarpTiles && heads <= kMergeCounters))) {
+    if (pair_ok && mma_group(gq) && (kPairMode == 1 || (kPairMode == 2 && tpw <= kPairMaxWarpTiles && heads <= kMergeCounters))) {
         const long long slots = (long long)kPairsPerSm * sm_count();
         long long tpp = (heads * p.n_tiles + slots - 1) / slots;  // tiles per pair
         if (tpp < kPairMinTiles) tpp = kPairMinTiles;
@@ -437,10 +438,15 @@ kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, i
 size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || S_q < 0 || n_res < 0 || D != kD || S_q + n_res == 0)
         return 0;
-    // the plan depends on the bit width; the size covers both
-    const size_t w2 = workspace_bytes(B, Hq, make_plan(B, Hkv, Hq, S_q, n_res, 2));
-    const size_t w4 = workspace_bytes(B, Hq, make_plan(B, Hkv, Hq, S_q, n_res, 4));
-    return w2 > w4 ? w2 : w4;
+    // the plan depends on the bit width and, through the choice of kernel, on
+    // the group size; the size covers every plan
+    size_t w = 0;
+    for (int bits : {2, 4})
+        for (bool pair_ok : {false, true}) {
+            const size_t wb = workspace_bytes(B, Hq, make_plan(B, Hkv, Hq, S_q, n_res, bits, pair_ok));
+            if (wb > w) w = wb;
+        }
+    return w;
 }
 
 kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const float* kscale,
@@ -450,7 +456,6 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
                                int D, int group_size, int bits, float sm_scale, float* out_f32,
                                void* workspace, size_t workspace_bytes_, kivi_stream_t stream) {
     kivi_status st = shape_check(D, group_size, bits);
-    if (st == KIVI_OK && group_size != kG && S_q > 0) st = KIVI_ERR_UNSUPPORTED;  // the decode reads G = 32 stores
     if (st != KIVI_OK) return st;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S_q < 0 || n_res < 0 ||
         S_q + n_res == 0 || S_q > s_cap || n_res > res_cap || s_cap < 0 || res_cap < 0 ||
@@ -467,7 +472,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
         !aligned16(vzero_f16) || !aligned16(k_res_f16) || !aligned16(v_res_f16) ||
         !aligned16(workspace))
         return KIVI_ERR_ALIGNMENT;
-    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res, bits);
+    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res, bits, group_size == kG);
     const size_t need = workspace_bytes(B, Hq, p);
     if (need > 0 && (!workspace || workspace_bytes_ < need)) return KIVI_ERR_WORKSPACE;
 
@@ -481,6 +486,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
     a.vzero = static_cast<const __half*>(vzero_f16);
     a.S_q = S_q;
     a.s_cap = s_cap;
+    a.g_shift = group_size == 128 ? 2 : (group_size == 64 ? 1 : 0);
     a.k_res = static_cast<const __half*>(k_res_f16);
     a.v_res = static_cast<const __half*>(v_res_f16);
     a.n_res = n_res;

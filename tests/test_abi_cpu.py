@@ -130,7 +130,9 @@ def decode(L, q=FAKE, S_q=2080, s_cap=2080, n_res=158, res_cap=160, B=1, Hq=32, 
 @no_gpu
 def test_decode_rejects_bad_arguments(L):
     assert decode(L, Hq=12) == INVALID               # 12 / 8 is not an integer
-    assert decode(L, G=64) == UNSUPPORTED            # the decode reads G = 32 stores
+    assert decode(L, G=16) == UNSUPPORTED            # group sizes 32, 64, 128
+    assert decode(L, G=64) == INVALID                # s_cap 2080 is not a multiple of 64
+    assert decode(L, G=128, S_q=2048, s_cap=2048, ws=None) == WORKSPACE  # G = 128 passes the checks
     assert decode(L, Hq=520) == UNSUPPORTED          # 65 query heads per KV head
     assert decode(L, Hq=1024) == UNSUPPORTED         # 128 query heads per KV head
     assert decode(L, S_q=0, n_res=0) == INVALID

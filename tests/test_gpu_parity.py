@@ -305,6 +305,29 @@ def test_decode_subgroups_many_splits(hq, hkv, bits):
     assert np.max(np.abs(out - ref)) <= TOL
 
 
+@pytest.mark.parametrize("G", [64, 128])
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("B,hq,hkv,S_q,n_res", [
+    (2, 8, 8, 70, 9),        # ragged last key group; a tile of 6 valid tokens
+    (2, 32, 8, 4096, 37),    # 4 heads per KV head, several splits per head
+    (1, 24, 8, 1000, 200),   # 3 heads per KV head (sub-group kernel), ragged store
+    (1, 16, 2, 16384, 100),  # sub-groups of a long cache: more splits than a cluster holds
+    (3, 4, 4, 64, 0),        # one key group, store only
+])
+def test_decode_group_sizes(G, bits, B, hq, hkv, S_q, n_res):
+    """The fused decode over stores of group size 64 and 128: a key group spans
+    2 or 4 of the decode's 32-token tiles and a token has 2 or 1 value groups."""
+    w = synth.Workload("groups", B=B, Hkv=hkv, Hq=hq, D=128, S=S_q + n_res, bits=bits, G=G, R=0,
+                       n_outlier=4, outlier_scale=8.0, seed=1000 + G + S_q + hq)
+    rng = np.random.default_rng(w.seed)
+    k = synth.keys(rng, (w.BH, S_q + n_res), 128, synth.outlier_channels(w), 8.0)
+    v = synth.normal(rng, (w.BH, S_q + n_res, 128))
+    q = synth.normal(rng, (B, hq, 128))
+    out, ref = decode_case(w, S_q, n_res, k, v, q)
+    err = np.max(np.abs(out - ref))
+    assert err <= TOL, err
+
+
 def test_decode_one_workspace_across_sizes():
     """One workspace serves calls of different sizes in turn: after every call
     the merge counters at its start are zero again, and every call matches the
