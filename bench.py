@@ -615,10 +615,13 @@ def run_sweep(args):
     def pool_count(bytes_each):
         return max(8, min(64, int(math.ceil(4 * l2 / max(bytes_each, 1) / 8)) * 8))
 
-    # flush / dequant at the long-context 2-bit and qwen8b sizes
-    shapes = (("qwen8b", 32), ("long2bit", 32), ("long2bit", 64), ("long2bit", 128))
-    for name, G in (shapes if args.sweep in ("all", "flush") else ()):
-        w = dataclasses.replace(synth.WORKLOADS[name], G=G)
+    # flush / dequant at the long-context 2-bit and qwen8b sizes; head dims 64
+    # and 256 at the long 2-bit size with the same element count (16 or 4 KV heads)
+    shapes = (("qwen8b", 32, 128), ("long2bit", 32, 128), ("long2bit", 64, 128), ("long2bit", 128, 128),
+              ("long2bit", 32, 64), ("long2bit", 64, 64), ("long2bit", 32, 256), ("long2bit", 128, 256))
+    for name, G, D in (shapes if args.sweep in ("all", "flush") else ()):
+        w = dataclasses.replace(synth.WORKLOADS[name], G=G, D=D, Hkv=synth.WORKLOADS[name].Hkv * 128 // D,
+                                Hq=synth.WORKLOADS[name].Hq * 128 // D)
         n = kv.kivi_flush_count(w.S, w.R, w.G)
         per = w.BH * w.S * w.D * 2 * 2 + 2 * w.BH * n * (w.D * w.bits // 8 + w.D * 6 // w.G) + w.BH * n * w.D * 4
         P = pool_count(per)
@@ -632,15 +635,15 @@ def run_sweep(args):
             vd.append(torch.empty_like(kd[-1]))
         ob = op_bytes(w, n, w.S - n)
         timed([lambda i=i: kv.kivi_flush_kv(xs[i][0], xs[i][1], w.R, ks[i], vs[i]) for i in range(P)],
-              ob["flush_kv"], "flush_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "pool": P})
+              ob["flush_kv"], "flush_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "D": D, "pool": P})
         timed([lambda i=i: kv.kivi_dequant_kv(ks[i], vs[i], n, kout=kd[i], vout=vd[i]) for i in range(P)],
-              ob["dequant_kv"], "dequant_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "pool": P})
+              ob["dequant_kv"], "dequant_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "D": D, "pool": P})
         # fake quantization of the same tokens: read 2 B and write 2 B per element of K and V (the kd/vd
         # buffers hold the n flushed tokens, so the S - n fp16 tokens are not part of this launch)
         timed([lambda i=i: kv.kivi_fake_quant_kv(xs[i][0][:, :n], xs[i][1][:, :n], 0, kout=kd[i], vout=vd[i],
                                                  G=G, bits=w.bits) for i in range(P)],
               2 * w.BH * n * w.D * 4, "fake_quant_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G,
-                                                        "pool": P})
+                                                        "D": D, "pool": P})
         del ks, vs, kd, vd, xs
         torch.cuda.empty_cache()
     if args.sweep == "flush":

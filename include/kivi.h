@@ -34,9 +34,11 @@
  *   - Numbers: fp16 is IEEE binary16 passed as raw 16-bit words. Inputs must
  *     be finite; NaN/Inf inputs give unspecified codes but every access stays
  *     in bounds.
- *   - Supported shapes: head_dim D = 128, bits in {2, 4}; group_size G in
- *     {32, 64, 128} for the flush, dequant, fake quantization and the decode.
- *     Other values return KIVI_ERR_UNSUPPORTED.
+ *   - Supported shapes: bits in {2, 4}; group_size G in {32, 64, 128};
+ *     head_dim D in {64, 128, 256} with G <= D (a value group lies within one
+ *     token row) for the flush, dequant, fake quantization and the residual
+ *     window; the decode takes D = 128. Other values return
+ *     KIVI_ERR_UNSUPPORTED.
  *
  * Store layout (one store per tensor, keys and values separately):
  *   codes  uint8   [BH, s_cap, D*bits/8]  codes packed along D inside each
@@ -169,6 +171,7 @@ kivi_status kivi_dequant_kv(const void* kcodes_u8, const float* kscale, const vo
  * compact: drops the oldest n_drop of n_res tokens and moves the other
  *          n_res - n_drop to the front (overlap-safe). INVALID_ARG if
  *          n_drop > n_res or n_res > res_cap.
+ * UNSUPPORTED unless D is 64, 128 or 256.
  */
 kivi_status kivi_residual_append(const void* src_f16, int src_bh_stride, int n_new,
                                  void* res_f16, int BH, int res_cap, int D, int n_res,
@@ -257,8 +260,8 @@ kivi_status kivi_decode_workspace_init(void* workspace, size_t workspace_bytes, 
  * laid out and initialised as described there (may be NULL when that size is
  * 0).
  * Errors: INVALID_ARG if S_q + n_res == 0, S_q > s_cap, n_res > res_cap or
- * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv > 64 (or D, group_size, bits as for
- * the flush); WORKSPACE if the workspace is NULL or too small. Stores of
+ * Hq % Hkv != 0; UNSUPPORTED if D != 128, Hq/Hkv > 64, or group_size or bits
+ * as for the flush; WORKSPACE if the workspace is NULL or too small. Stores of
  * every supported group size (32, 64, 128) are read; their key groups align
  * with the kernels' 32-token tiles.
  */

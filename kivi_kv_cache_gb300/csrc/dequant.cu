@@ -74,16 +74,18 @@ __device__ __forceinline__ uint32_t load_word(const uint8_t* p) {
     return __ldg(reinterpret_cast<const uint16_t*>(p));
 }
 
-// keys: one warp per (head, 32-token block, 64-channel half); lane = part*8
-// + oc, part owns 8 tokens of the block. Scale and zero are per (key group
-// of G tokens, channel): the block's group is block * 32 / G.
-template <int BITS, int G>
+// keys: one warp per (head, 32-token block, 64-channel slice); lane =
+// part*8 + oc, part owns 8 tokens of the block. Scale and zero are per (key
+// group of G tokens, channel): the block's group is block * 32 / G.
+template <int BITS, int G, int D>
 __device__ __forceinline__ void dequant_keys_warp(const DequantArgs& a, int warp_id, int bh) {
-    constexpr int ROWB = kD * BITS / 8;
+    constexpr int ROWB = D * BITS / 8;
+    constexpr int NSL = D / 64;  // 64-channel slices per row
     const int lane = threadIdx.x & 31;
-    const int octet = (warp_id & 1) * 8 + (lane & 7);
+    const unsigned wu = warp_id;
+    const int octet = (wu % NSL) * 8 + (lane & 7);
     const int part = lane >> 3;
-    const int tb = warp_id >> 1;
+    const int tb = wu / NSL;
     if (tb >= (a.S + 31) / 32) return;
     const int g = tb * 32 / G;
     const int t0 = tb * 32 + part * 8;
@@ -92,7 +94,7 @@ __device__ __forceinline__ void dequant_keys_warp(const DequantArgs& a, int warp
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = (t0 + i < a.S) ? load_word<BITS>(crow + i * ROWB) : 0u;
-    const long long m = ((long long)bh * (a.s_cap / G) + g) * kD + octet * 8;
+    const long long m = ((long long)bh * (a.s_cap / G) + g) * D + octet * 8;
     const float4 sa = __ldg(reinterpret_cast<const float4*>(a.scale + m));
     const float4 sb = __ldg(reinterpret_cast<const float4*>(a.scale + m) + 1);
     const uint4 zw = __ldg(reinterpret_cast<const uint4*>(a.zero + m));
@@ -107,34 +109,36 @@ __device__ __forceinline__ void dequant_keys_warp(const DequantArgs& a, int warp
         const float2 f = __half22float2(u32_as_h2(zz[k]));
         z2[k] = pk(f.x, f.y);
     }
-    uint4* orow = reinterpret_cast<uint4*>(a.out) + ((long long)bh * a.S + t0) * (kD / 8) + octet;
+    uint4* orow = reinterpret_cast<uint4*>(a.out) + ((long long)bh * a.S + t0) * (D / 8) + octet;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        if (t0 + i < a.S) orow[i * (kD / 8)] = recon8<BITS>(w[i], s2, ns2, z2);
+        if (t0 + i < a.S) orow[i * (D / 8)] = recon8<BITS>(w[i], s2, ns2, z2);
 }
 
-// values: one warp per 8 consecutive tokens of one head; lane = sub*16 +
-// octet, iteration i handles token 2*i + sub. Scale and zero are per (token,
-// G-channel group).
-template <int BITS, int G>
+// values: one warp per NR * RPT consecutive tokens of one head (NR = 32 / (D /
+// 8) rows per pass); lane = sub * (D / 8) + octet, iteration i handles token
+// NR * i + sub. Scale and zero are per (token, G-channel group).
+template <int BITS, int G, int D>
 __device__ __forceinline__ void dequant_values_warp(const DequantArgs& a, int warp_id, int bh) {
-    constexpr int ROWB = kD * BITS / 8;
+    constexpr int ROWB = D * BITS / 8;
     constexpr int RPT = 4;
+    constexpr int OPR = D / 8;    // octets per row: 8, 16 or 32
+    constexpr int NR = 32 / OPR;  // rows per pass: 4, 2 or 1
     const int lane = threadIdx.x & 31;
-    const int octet = lane & 15;
-    const int sub = lane >> 4;
-    const int tw = warp_id * (2 * RPT);
+    const int octet = lane % OPR;
+    const int sub = lane / OPR;
+    const int tw = warp_id * (NR * RPT);
     if (tw >= a.S) return;
     const long long row0 = (long long)bh * a.s_cap + tw + sub;
     uint32_t w[RPT];
     float s[RPT], z[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        const long long row = row0 + 2 * i;
-        if (tw + 2 * i + sub < a.S) {
+        const long long row = row0 + NR * i;
+        if (tw + NR * i + sub < a.S) {
             w[i] = load_word<BITS>(a.codes + row * ROWB + octet * BITS);
-            s[i] = __ldg(a.scale + row * (kD / G) + octet / (G / 8));
-            z[i] = __half2float(a.zero[row * (kD / G) + octet / (G / 8)]);
+            s[i] = __ldg(a.scale + row * (D / G) + octet / (G / 8));
+            z[i] = __half2float(a.zero[row * (D / G) + octet / (G / 8)]);
         } else {
             w[i] = 0u;
             s[i] = 0.f;
@@ -142,106 +146,134 @@ __device__ __forceinline__ void dequant_values_warp(const DequantArgs& a, int wa
         }
     }
     pdl_trigger();
-    uint4* orow = reinterpret_cast<uint4*>(a.out) + ((long long)bh * a.S + tw + sub) * (kD / 8) + octet;
+    uint4* orow = reinterpret_cast<uint4*>(a.out) + ((long long)bh * a.S + tw + sub) * (D / 8) + octet;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-        if (tw + 2 * i + sub < a.S) {
+        if (tw + NR * i + sub < a.S) {
             const f32x2 s1 = pk(s[i], s[i]), n1 = pk(-kMagic * s[i], -kMagic * s[i]), z1 = pk(z[i], z[i]);
             const f32x2 s2[4] = {s1, s1, s1, s1}, ns2[4] = {n1, n1, n1, n1}, z2[4] = {z1, z1, z1, z1};
-            orow[2 * i * (kD / 8)] = recon8<BITS>(w[i], s2, ns2, z2);
+            orow[NR * i * (D / 8)] = recon8<BITS>(w[i], s2, ns2, z2);
         }
     }
 }
 
-int key_blocks_x(int S) { return ((S + 31) / 32 * 2 + 3) / 4; }
-int value_blocks_x(int S) { return (S + 31) / 32; }
+// blocks of 4 warps: keys take one warp per (32-token block, 64-channel
+// slice); values one warp per 4 passes of 32 / (D / 8) rows
+int key_blocks_x(int S, int D) { return ((S + 31) / 32 * (D / 64) + 3) / 4; }
+int value_blocks_x(int S, int D) {
+    const int tokens_per_block = 4 * 4 * (256 / D);
+    return (S + tokens_per_block - 1) / tokens_per_block;
+}
 
-template <int BITS, int G>
+template <int BITS, int G, int D>
 __global__ void __launch_bounds__(kThreads) dequant_keys_kernel(DequantArgs a) {
     pdl_wait();
-    dequant_keys_warp<BITS, G>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+    dequant_keys_warp<BITS, G, D>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
 
-template <int BITS, int G>
+template <int BITS, int G, int D>
 __global__ void __launch_bounds__(kThreads) dequant_values_kernel(DequantArgs a) {
     pdl_wait();
-    dequant_values_warp<BITS, G>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+    dequant_values_warp<BITS, G, D>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
 
-template <int BITS, int G>
+template <int BITS, int G, int D>
 __global__ void __launch_bounds__(kThreads) dequant_kv_kernel(DequantArgs k, DequantArgs v, int kbx) {
     pdl_wait();
     if ((int)blockIdx.x < kbx)
-        dequant_keys_warp<BITS, G>(k, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+        dequant_keys_warp<BITS, G, D>(k, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
     else
-        dequant_values_warp<BITS, G>(v, (blockIdx.x - kbx) * 4 + (threadIdx.x >> 5), blockIdx.y);
+        dequant_values_warp<BITS, G, D>(v, (blockIdx.x - kbx) * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
 
 
 DequantArgs head_slice(const DequantArgs& a, int h0, int nh, int bits, int axis) {
     DequantArgs s = a;
     s.BH = nh;
-    s.codes += (long long)h0 * a.s_cap * (kD * bits / 8);
-    const long long meta = axis == 0 ? (long long)(a.s_cap / a.G) * kD : (long long)a.s_cap * (kD / a.G);
+    s.codes += (long long)h0 * a.s_cap * (a.D * bits / 8);
+    const long long meta = axis == 0 ? (long long)(a.s_cap / a.G) * a.D : (long long)a.s_cap * (a.D / a.G);
     s.scale += h0 * meta;
     s.zero += h0 * meta;
-    s.out += (long long)h0 * a.S * kD;
+    s.out += (long long)h0 * a.S * a.D;
     return s;
 }
 
-template <int BITS, int G>
+template <int BITS, int G, int D>
 cudaError_t launch_dequant_typed(int axis, const DequantArgs& a, cudaStream_t stream) {
-    const int bx = axis == 0 ? key_blocks_x(a.S) : value_blocks_x(a.S);
+    const int bx = axis == 0 ? key_blocks_x(a.S, D) : value_blocks_x(a.S, D);
     for (int h0 = 0; h0 < a.BH; h0 += 65535) {
         const int nh = a.BH - h0 < 65535 ? a.BH - h0 : 65535;
         const DequantArgs s = head_slice(a, h0, nh, BITS, axis);
         const dim3 grid(bx, nh);
-        const cudaError_t e = axis == 0 ? launch_pdl(dequant_keys_kernel<BITS, G>, grid, kThreads, 0, stream, s)
-                                        : launch_pdl(dequant_values_kernel<BITS, G>, grid, kThreads, 0, stream, s);
+        const cudaError_t e = axis == 0 ? launch_pdl(dequant_keys_kernel<BITS, G, D>, grid, kThreads, 0, stream, s)
+                                        : launch_pdl(dequant_values_kernel<BITS, G, D>, grid, kThreads, 0, stream, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
 
-template <int BITS, int G>
+template <int BITS, int G, int D>
 cudaError_t launch_dequant_kv_typed(const DequantArgs& k, const DequantArgs& v, cudaStream_t stream) {
-    const int kbx = key_blocks_x(k.S), vbx = value_blocks_x(v.S);
+    const int kbx = key_blocks_x(k.S, D), vbx = value_blocks_x(v.S, D);
     for (int h0 = 0; h0 < k.BH; h0 += 65535) {
         const int nh = k.BH - h0 < 65535 ? k.BH - h0 : 65535;
         const DequantArgs ks = head_slice(k, h0, nh, BITS, 0), vs = head_slice(v, h0, nh, BITS, 1);
         const dim3 grid(kbx + vbx, nh);
-        const cudaError_t e = launch_pdl(dequant_kv_kernel<BITS, G>, grid, kThreads, 0, stream, ks, vs, kbx);
+        const cudaError_t e = launch_pdl(dequant_kv_kernel<BITS, G, D>, grid, kThreads, 0, stream, ks, vs, kbx);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
+
+// (G, D) pairs: G in {32, 64, 128}, D in {64, 128, 256}, G <= D. One
+// launch function per (BITS, G, D); F<BITS, G, D>::run forwards to it.
+template <template <int, int, int> class F, typename... A>
+cudaError_t by_shape(int bits, int G, int D, A&&... args) {
+    switch (bits * 1000000 + G * 1000 + D) {
+        case 4032064: return F<4, 32, 64>::run(args...);
+        case 4032128: return F<4, 32, 128>::run(args...);
+        case 4032256: return F<4, 32, 256>::run(args...);
+        case 4064064: return F<4, 64, 64>::run(args...);
+        case 4064128: return F<4, 64, 128>::run(args...);
+        case 4064256: return F<4, 64, 256>::run(args...);
+        case 4128128: return F<4, 128, 128>::run(args...);
+        case 4128256: return F<4, 128, 256>::run(args...);
+        case 2032064: return F<2, 32, 64>::run(args...);
+        case 2032128: return F<2, 32, 128>::run(args...);
+        case 2032256: return F<2, 32, 256>::run(args...);
+        case 2064064: return F<2, 64, 64>::run(args...);
+        case 2064128: return F<2, 64, 128>::run(args...);
+        case 2064256: return F<2, 64, 256>::run(args...);
+        case 2128128: return F<2, 128, 128>::run(args...);
+        case 2128256: return F<2, 128, 256>::run(args...);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int BITS, int G, int D>
+struct DequantOne {
+    static cudaError_t run(int axis, const DequantArgs& a, cudaStream_t stream) {
+        return launch_dequant_typed<BITS, G, D>(axis, a, stream);
+    }
+};
+
+template <int BITS, int G, int D>
+struct DequantKV {
+    static cudaError_t run(const DequantArgs& k, const DequantArgs& v, cudaStream_t stream) {
+        return launch_dequant_kv_typed<BITS, G, D>(k, v, stream);
+    }
+};
 
 }  // namespace
 
 cudaError_t launch_dequant(int axis, const DequantArgs& a, int bits, cudaStream_t stream) {
     if (a.S <= 0 || a.BH <= 0) return cudaSuccess;
-    switch (bits * 1000 + a.G) {
-        case 4032: return launch_dequant_typed<4, 32>(axis, a, stream);
-        case 4064: return launch_dequant_typed<4, 64>(axis, a, stream);
-        case 4128: return launch_dequant_typed<4, 128>(axis, a, stream);
-        case 2032: return launch_dequant_typed<2, 32>(axis, a, stream);
-        case 2064: return launch_dequant_typed<2, 64>(axis, a, stream);
-        case 2128: return launch_dequant_typed<2, 128>(axis, a, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return by_shape<DequantOne>(bits, a.G, a.D, axis, a, stream);
 }
 
 cudaError_t launch_dequant_kv(const DequantArgs& k, const DequantArgs& v, int bits, cudaStream_t stream) {
     if (k.S <= 0 || k.BH <= 0) return cudaSuccess;
-    switch (bits * 1000 + k.G) {
-        case 4032: return launch_dequant_kv_typed<4, 32>(k, v, stream);
-        case 4064: return launch_dequant_kv_typed<4, 64>(k, v, stream);
-        case 4128: return launch_dequant_kv_typed<4, 128>(k, v, stream);
-        case 2032: return launch_dequant_kv_typed<2, 32>(k, v, stream);
-        case 2064: return launch_dequant_kv_typed<2, 64>(k, v, stream);
-        case 2128: return launch_dequant_kv_typed<2, 128>(k, v, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return by_shape<DequantKV>(bits, k.G, k.D, k, v, stream);
 }
 
 }  // namespace kivi

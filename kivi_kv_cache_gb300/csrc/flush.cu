@@ -29,8 +29,8 @@
 //    0.5 - 2^-14 the code equals rint(RN(a/s)). One check per 8 elements
 //    sends the rare near-tie element to an exact IEEE division (out of line).
 //    Byte permutes pack 8 codes per 32-bit word.
-//  * work is cut into 4 KB items (a key group's 32 tokens x 64 channels, or
-//    16 value rows); each warp walks the items with a grid stride, staging
+//  * work is cut into 4 KB items (a key group's G tokens x 2048 / G channels,
+//    or 2048 / D value rows); each warp walks the items with a grid stride, staging
 //    two at a time in shared memory with cp.async, so the copy of the next
 //    item overlaps the quantization of the current one; the key loop takes
 //    two token rows per trip.
@@ -194,31 +194,42 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 struct Items {
-    int key_items;   // BH * ng * (128 / key item channels)
-    int val_items;   // BH * ceil(n_flush / 16)
+    int key_items;   // BH * ng * (D / key item channels)
+    int val_items;   // BH * ceil(n_flush / value item rows)
     int ng;          // key groups per head
     int nv;          // value items per head
 };
 
-// Key items of group size G: G tokens x kKeyCh(G) channels (4 KB); a lane owns
-// 8 tokens x 8 channels, lane = part * kNOc + oc.
-template <int G>
+// Key items of group size G and head dim D: G tokens x kCh channels (4 KB); a
+// lane owns 8 tokens x 8 channels, lane = part * kNOc + oc.
+template <int G, int D>
 struct KeyShape {
     static constexpr int kCh = 2048 / G;      // channels of an item: 64, 32 or 16
     static constexpr int kNOc = kCh / 8;      // 8-channel octets: 8, 4 or 2
     static constexpr int kNPart = 32 / kNOc;  // 8-token parts: 4, 8 or 16 (= G / 8)
-    static constexpr int kQ = kD / kCh;       // items per key group: 2, 4 or 8
+    static constexpr int kQ = D / kCh;        // items per key group: 1 to 16
     static constexpr int kPad = G > 32 ? 1 : 0;  // pad rows per 8-token part in shared memory
+    static_assert(kQ >= 1, "a key item spans at most the head dim");
 };
 
-template <int G>
+// Value items of head dim D: kRows token rows of D channels (4 KB); a lane
+// owns 64 channels of one row, lane = jp * kRows + row.
+template <int D>
+struct ValueShape {
+    static constexpr int kRows = 2048 / D;  // rows of an item: 32, 16 or 8
+    static constexpr int kCpr = D / 8;      // 16-byte chunks per row: 8, 16 or 32
+};
+
+template <int G, int D>
 __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& v, const Items& it, int item,
                                            uint8_t* st, int lane) {
-    using KS = KeyShape<G>;
+    using KS = KeyShape<G, D>;
+    using VS = ValueShape<D>;
+    constexpr int RB = 2 * D;  // bytes per fp16 token row
     if (item < it.key_items) {
         const unsigned u = item;  // item >= 0: unsigned division by the power of two kQ is a shift
         const int qs = u % KS::kQ, g = (u / KS::kQ) % it.ng, bh = (u / KS::kQ) / it.ng;
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(k.x) + ((long long)bh * k.x_bh_stride + g * G) * 256 +
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(k.x) + ((long long)bh * k.x_bh_stride + g * G) * RB +
                              qs * (KS::kCh * 2);
         constexpr int CPR = KS::kNOc;  // 16-byte chunks per token row
 #pragma unroll
@@ -226,17 +237,17 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
             const int row = i / CPR, col = i % CPR;
             const bool ok = g * G + row < k.n_flush;
             cp_async16(st + ((row + KS::kPad * (row >> 3)) * CPR + col) * 16,
-                       ok ? (const void*)(src + row * 256 + col * 16) : (const void*)src, ok);
+                       ok ? (const void*)(src + row * RB + col * 16) : (const void*)src, ok);
         }
     } else {
-        const int vi = item - it.key_items;
-        const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(v.x) + ((long long)bh * v.x_bh_stride + t0) * 256;
+        const unsigned vi = item - it.key_items;
+        const int t0 = (vi % it.nv) * VS::kRows, bh = vi / it.nv;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(v.x) + ((long long)bh * v.x_bh_stride + t0) * RB;
 #pragma unroll
-        for (int i = lane; i < 256; i += 32) {  // 16 rows x 16 chunks, chunk c of row r at c ^ (r & 7)
-            const int row = i >> 4, col = i & 15;
+        for (int i = lane; i < 256; i += 32) {  // kRows rows x kCpr chunks, chunk c of row r at c ^ (r & 7)
+            const int row = i / VS::kCpr, col = i % VS::kCpr;
             const bool ok = t0 + row < v.n_flush;
-            cp_async16(st + row * 256 + ((col ^ (row & 7)) << 4), ok ? (const void*)(src + i * 16) : (const void*)src, ok);
+            cp_async16(st + row * RB + ((col ^ (row & 7)) << 4), ok ? (const void*)(src + i * 16) : (const void*)src, ok);
         }
     }
 }
@@ -244,9 +255,9 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
 // keys: lane = part * kNOc + oc; part owns tokens [8 part, 8 part + 8) of the
 // group, oc owns 8 channels of this item's channel slice. FAKE: write the
 // fake-quantized fp16 rows to a.fq instead of codes, scales and zeros.
-template <int BITS, bool FAKE, int G>
+template <int BITS, bool FAKE, int G, int D>
 __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st, int lane) {
-    using KS = KeyShape<G>;
+    using KS = KeyShape<G, D>;
     const unsigned u = item;
     const int qs = u % KS::kQ, g = (u / KS::kQ) % it.ng, bh = (u / KS::kQ) / it.ng;
     const int oc = lane % KS::kNOc, part = lane / KS::kNOc;
@@ -322,13 +333,13 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         r2[k] = pk(r[2 * k], r[2 * k + 1]);
     }
     if (FAKE) {
-        uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * kD) + octet;
+        uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * D) + octet;
 #pragma unroll 1
-        for (int i = 0; i < nv; ++i) frow[i * (kD / 8)] = fake8(xs[i * KS::kNOc], z2, r2, s);
+        for (int i = 0; i < nv; ++i) frow[i * (D / 8)] = fake8(xs[i * KS::kNOc], z2, r2, s);
         return;
     }
     if (part == 0) {
-        const long long m = ((long long)bh * (a.s_cap / G) + a.s_off / G + g) * kD + octet * 8;
+        const long long m = ((long long)bh * (a.s_cap / G) + a.s_off / G + g) * D + octet * 8;
         float4* sp = reinterpret_cast<float4*>(a.scale + m);
         sp[0] = make_float4(s[0], s[1], s[2], s[3]);
         sp[1] = make_float4(s[4], s[5], s[6], s[7]);
@@ -339,7 +350,7 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         zp.w = h2_as_u32(__floats2half2_rn(z[6], z[7]));
         *reinterpret_cast<uint4*>(a.zero + m) = zp;
     }
-    constexpr int ROWB = kD * BITS / 8;
+    constexpr int ROWB = D * BITS / 8;
     uint8_t* crow = a.codes + ((long long)bh * a.s_cap + a.s_off + t0) * ROWB + octet * BITS;
     auto store_row = [&](int i, uint32_t packed) {
         if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
@@ -371,21 +382,23 @@ __device__ __forceinline__ void minmax_tree(const uint4 (&x)[N], __half2& m2, __
     x2 = xk[0];
 }
 
-// values: lane = 16 jp + row holds 64 channels of row `row` of the item,
+// values: lane = kRows jp + row holds 64 channels of row `row` of the item,
 // channels 64 jp .. 64 jp + 63: two groups (G = 32), one (G = 64), or half of
-// one, whose min/max it shares with its partner lane (lane ^ 16) (G = 128).
-// Min/max, scale and codes of a group stay in its lane(s); one code store per
-// group or half group.
-template <int BITS, bool FAKE, int G>
+// one, whose min/max it shares with its partner lane (lane ^ kRows, the other
+// half of the same row's group) (G = 128). Min/max, scale and codes of a
+// group stay in its lane(s); one code store per group or half group.
+template <int BITS, bool FAKE, int G, int D>
 __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
                                            int lane) {
-    const int vi = item - it.key_items;
-    const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
-    const int row = lane & 15, jp = lane >> 4;
+    using VS = ValueShape<D>;
+    static_assert(G <= D, "a value group lies within one token row");
+    const unsigned vi = item - it.key_items;
+    const int t0 = (vi % it.nv) * VS::kRows, bh = vi / it.nv;
+    const int row = lane % VS::kRows, jp = lane / VS::kRows;
     const bool valid = t0 + row < a.n_flush;
     if (G != 128 && !valid) return;  // (G = 128: both lanes of a row leave together below)
     const float L = (float)Levels<BITS>::value;
-    const uint4* xs = reinterpret_cast<const uint4*>(st + row * 256);
+    const uint4* xs = reinterpret_cast<const uint4*>(st + row * (2 * D));
     const long long grow = (long long)bh * a.s_cap + a.s_off + t0 + row;
     constexpr int NG = G == 32 ? 2 : 1;      // groups (or half groups) per lane
     constexpr int NVEC = G == 32 ? 4 : 8;    // 16-byte vectors per group (or half group) in this lane
@@ -397,9 +410,9 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
         for (int k = 0; k < NVEC; ++k) x[k] = xs[(cv + k) ^ (row & 7)];
         __half2 m2, x2;
         minmax_tree<NVEC>(x, m2, x2);
-        if (G == 128) {  // the other half of the group sits in lane ^ 16 (same row)
-            m2 = __hmin2(m2, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(m2), 16)));
-            x2 = __hmax2(x2, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(x2), 16)));
+        if (G == 128) {  // the other half of the group sits in lane ^ kRows (same row)
+            m2 = __hmin2(m2, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(m2), VS::kRows)));
+            x2 = __hmax2(x2, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(x2), VS::kRows)));
             if (!valid) return;
         }
         const float z = canon(__half2float(__hmin(__low2half(m2), __high2half(m2))));
@@ -410,14 +423,14 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
         const float sv[8] = {sc, sc, sc, sc, sc, sc, sc, sc};
         const int j = (64 * jp + (G == 32 ? 32 * e : 0)) / G;  // this group's index in the row
         if (FAKE) {
-            uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * kD) + cv;
+            uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * D) + cv;
 #pragma unroll
             for (int k = 0; k < NVEC; ++k) frow[k] = fake8(x[k], z2, r2, sv);
         } else {
             uint32_t pq[NVEC];
 #pragma unroll
             for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS>(x[k], z2, r2, sv);
-            uint8_t* cdst = a.codes + grow * (kD * BITS / 8) + cv * BITS;  // 8 channels per vector
+            uint8_t* cdst = a.codes + grow * (D * BITS / 8) + cv * BITS;  // 8 channels per vector
             if (BITS == 4) {
 #pragma unroll
                 for (int k = 0; k < NVEC; k += 4)
@@ -428,9 +441,9 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
                     *reinterpret_cast<uint2*>(cdst + 2 * k) =
                         make_uint2(pq[k] | (pq[k + 1] << 16), pq[k + 2] | (pq[k + 3] << 16));
             }
-            if (G != 128 || jp == 0) {
-                a.scale[grow * (kD / G) + j] = sc;
-                a.zero[grow * (kD / G) + j] = __float2half_rn(z);
+            if (G != 128 || (jp & 1) == 0) {
+                a.scale[grow * (D / G) + j] = sc;
+                a.zero[grow * (D / G) + j] = __float2half_rn(z);
             }
         }
     }
@@ -599,7 +612,7 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
 
 // Keys, values, or both: warp w of the grid handles items w, w + W, ... of the
 // list [key items | value items] (W = total warps).
-template <int BITS, bool FAKE, int G>
+template <int BITS, bool FAKE, int G, int D>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -609,35 +622,35 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs
     const int stride = gridDim.x * (kThreads / 32);
     int item = blockIdx.x * (kThreads / 32) + warp;
     pdl_wait();
-    if (item < total) fetch_item<G>(k, v, it, item, base, lane);
+    if (item < total) fetch_item<G, D>(k, v, it, item, base, lane);
     cp_async_commit();
-    if (item + stride < total) fetch_item<G>(k, v, it, item + stride, base + kStageBytes, lane);
+    if (item + stride < total) fetch_item<G, D>(k, v, it, item + stride, base + kStageBytes, lane);
     cp_async_commit();
     pdl_trigger();
     for (int n = 0; item < total; item += stride, ++n) {
         uint8_t* S = base + (n & 1) * kStageBytes;  // stage n mod 2
         cp_async_wait1();
         __syncwarp();
-        if (G == 32) {  // the generic item code at G = 32 measured 0.7 % slower than this form
+        if (G == 32 && D == kD) {  // the generic item code at G = 32 measured 0.7 % slower than this form
             if (item < it.key_items) key_item_g32<BITS, FAKE>(k, it, item, S, lane);
             else value_item_g32<BITS, FAKE>(v, it, item, S, lane);
         } else {
-            if (item < it.key_items) key_item<BITS, FAKE, G>(k, it, item, S, lane);
-            else value_item<BITS, FAKE, G>(v, it, item, S, lane);
+            if (item < it.key_items) key_item<BITS, FAKE, G, D>(k, it, item, S, lane);
+            else value_item<BITS, FAKE, G, D>(v, it, item, S, lane);
         }
         __syncwarp();
-        if (item + 2 * stride < total) fetch_item<G>(k, v, it, item + 2 * stride, S, lane);
+        if (item + 2 * stride < total) fetch_item<G, D>(k, v, it, item + 2 * stride, S, lane);
         cp_async_commit();
     }
 }
 
-template <int BITS, bool FAKE, int G>
+template <int BITS, bool FAKE, int G, int D>
 cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
     static int grid_cap = 0;
     static bool configured = false;  // benign race: every caller sets the same values
     const int smem = (kThreads / 32) * 2 * Stage<G>::kBytes;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, FAKE, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, FAKE, G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -649,31 +662,40 @@ cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it
     if (total <= 0) return cudaSuccess;
     long long blocks = (total + 3) / 4;
     if (blocks > grid_cap) blocks = grid_cap;
-    return launch_pdl(flush_kernel<BITS, FAKE, G>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
+    return launch_pdl(flush_kernel<BITS, FAKE, G, D>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
 }
 
 // Pointers of heads [h0, h0 + nh) of a flush.
 FlushArgs head_slice(const FlushArgs& a, int h0, int nh, int bits, int axis) {
     FlushArgs s = a;
     s.BH = nh;
-    s.x += (long long)h0 * a.x_bh_stride * kD;
+    s.x += (long long)h0 * a.x_bh_stride * a.D;
     if (a.fq) {
-        s.fq += (long long)h0 * a.fq_bh_stride * kD;
+        s.fq += (long long)h0 * a.fq_bh_stride * a.D;
         return s;
     }
-    s.codes += (long long)h0 * a.s_cap * (kD * bits / 8);
-    const long long meta = axis == 0 ? (long long)(a.s_cap / a.G) * kD : (long long)a.s_cap * (kD / a.G);
+    s.codes += (long long)h0 * a.s_cap * (a.D * bits / 8);
+    const long long meta = axis == 0 ? (long long)(a.s_cap / a.G) * a.D : (long long)a.s_cap * (a.D / a.G);
     s.scale += h0 * meta;
     s.zero += h0 * meta;
     return s;
 }
 
+// (G, D) pairs: G in {32, 64, 128}, D in {64, 128, 256}, G <= D
 template <int BITS, bool FAKE>
-cudaError_t launch_items_g(const FlushArgs& k, const FlushArgs& v, const Items& it, int G, cudaStream_t stream) {
-    if (G == 32) return launch_items<BITS, FAKE, 32>(k, v, it, stream);
-    if (G == 64) return launch_items<BITS, FAKE, 64>(k, v, it, stream);
-    if (G == 128) return launch_items<BITS, FAKE, 128>(k, v, it, stream);
-    return cudaErrorInvalidValue;
+cudaError_t launch_items_g(const FlushArgs& k, const FlushArgs& v, const Items& it, int G, int D,
+                           cudaStream_t stream) {
+    switch (G * 1000 + D) {
+        case 32064: return launch_items<BITS, FAKE, 32, 64>(k, v, it, stream);
+        case 32128: return launch_items<BITS, FAKE, 32, 128>(k, v, it, stream);
+        case 32256: return launch_items<BITS, FAKE, 32, 256>(k, v, it, stream);
+        case 64064: return launch_items<BITS, FAKE, 64, 64>(k, v, it, stream);
+        case 64128: return launch_items<BITS, FAKE, 64, 128>(k, v, it, stream);
+        case 64256: return launch_items<BITS, FAKE, 64, 256>(k, v, it, stream);
+        case 128128: return launch_items<BITS, FAKE, 128, 128>(k, v, it, stream);
+        case 128256: return launch_items<BITS, FAKE, 128, 256>(k, v, it, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -683,9 +705,10 @@ cudaError_t launch_flush_impl(const FlushArgs& k, const FlushArgs& v, bool do_k,
                               cudaStream_t stream) {
     const FlushArgs& a = do_k ? k : v;
     if (a.n_flush <= 0 || a.BH <= 0) return cudaSuccess;
-    const int G = a.G;
-    const int ng = (a.n_flush + G - 1) / G, nv = (a.n_flush + 15) / 16;
-    const int kq = kD / (2048 / G);  // key items per group
+    const int G = a.G, D = a.D;
+    const int rows = 2048 / D;  // token rows per value item
+    const int ng = (a.n_flush + G - 1) / G, nv = (a.n_flush + rows - 1) / rows;
+    const int kq = D / (2048 / G);  // key items per group
     const int per_head = (do_k ? kq * ng : 0) + (do_v ? nv : 0);
     const int max_heads = (int)(0x3fffffff / per_head) > 0 ? (int)(0x3fffffff / per_head) : 1;
     for (int h0 = 0; h0 < a.BH; h0 += max_heads) {
@@ -699,10 +722,10 @@ cudaError_t launch_flush_impl(const FlushArgs& k, const FlushArgs& v, bool do_k,
         it.key_items = do_k ? nh * kq * ng : 0;
         it.val_items = do_v ? nh * nv : 0;
         const bool fake = a.fq != nullptr;
-        cudaError_t e = bits == 4 ? (fake ? launch_items_g<4, true>(ks, vs, it, G, stream)
-                                          : launch_items_g<4, false>(ks, vs, it, G, stream))
-                                  : (fake ? launch_items_g<2, true>(ks, vs, it, G, stream)
-                                          : launch_items_g<2, false>(ks, vs, it, G, stream));
+        cudaError_t e = bits == 4 ? (fake ? launch_items_g<4, true>(ks, vs, it, G, D, stream)
+                                          : launch_items_g<4, false>(ks, vs, it, G, D, stream))
+                                  : (fake ? launch_items_g<2, true>(ks, vs, it, G, D, stream)
+                                          : launch_items_g<2, false>(ks, vs, it, G, D, stream));
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

@@ -36,9 +36,14 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Flush, dequant and fake quantization: D = 128, G in {32, 64, 128}, 2 or 4 bits.
+bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
+
+// Flush, dequant and fake quantization: D in {64, 128, 256}, G in {32, 64,
+// 128} with G <= D (a value group lies within one token row), 2 or 4 bits.
+// The decode also needs D = 128.
 kivi_status shape_check(int D, int G, int bits) {
-    if (D != kD || (G != 32 && G != 64 && G != 128) || (bits != 2 && bits != 4)) return KIVI_ERR_UNSUPPORTED;
+    if (!head_dim_ok(D) || (G != 32 && G != 64 && G != 128) || G > D || (bits != 2 && bits != 4))
+        return KIVI_ERR_UNSUPPORTED;
     return KIVI_OK;
 }
 
@@ -172,9 +177,10 @@ kivi_status flush_check(const void* x, int BH, int S, int x_bh_stride, int D, in
 }
 
 FlushArgs flush_args(const void* x, int BH, int x_bh_stride, int n, void* codes, float* scale,
-                     void* zero, int s_off, int s_cap, int G) {
+                     void* zero, int s_off, int s_cap, int G, int D) {
     FlushArgs a;
     a.G = G;
+    a.D = D;
     a.x = static_cast<const __half*>(x);
     a.x_bh_stride = x_bh_stride;
     a.BH = BH;
@@ -196,7 +202,7 @@ kivi_status flush_one(int axis, const void* x, int BH, int S, int x_bh_stride, i
     if (st != KIVI_OK) return st;
     if (n_flushed) *n_flushed = n;
     if (n == 0) return KIVI_OK;
-    return from_cuda(launch_flush(axis, flush_args(x, BH, x_bh_stride, n, codes, scale, zero, s_off, s_cap, G),
+    return from_cuda(launch_flush(axis, flush_args(x, BH, x_bh_stride, n, codes, scale, zero, s_off, s_cap, G, D),
                                   bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -222,8 +228,8 @@ kivi_status fake_quant(const void* k, const void* v, bool do_k, bool do_v, int B
         return KIVI_ERR_ALIGNMENT;
     const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
     if (n > 0) {
-        FlushArgs ka = flush_args(do_k ? k : v, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G);
-        FlushArgs va = flush_args(do_v ? v : k, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G);
+        FlushArgs ka = flush_args(do_k ? k : v, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G, D);
+        FlushArgs va = flush_args(do_v ? v : k, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G, D);
         ka.fq = static_cast<__half*>(do_k ? k_out : v_out);
         va.fq = static_cast<__half*>(do_v ? v_out : k_out);
         ka.fq_bh_stride = va.fq_bh_stride = out_bh_stride;
@@ -234,11 +240,12 @@ kivi_status fake_quant(const void* k, const void* v, bool do_k, bool do_v, int B
     const int tail = S - n;
     const bool copy_k = do_k && k_out != k, copy_v = do_v && v_out != v;
     if (tail > 0 && (copy_k || copy_v)) {
-        const __half* src0 = static_cast<const __half*>(copy_k ? k : v) + (long long)n * kD;
-        const __half* src1 = copy_k && copy_v ? static_cast<const __half*>(v) + (long long)n * kD : nullptr;
+        const __half* src0 = static_cast<const __half*>(copy_k ? k : v) + (long long)n * D;
+        const __half* src1 = copy_k && copy_v ? static_cast<const __half*>(v) + (long long)n * D : nullptr;
         __half* dst0 = static_cast<__half*>(copy_k ? k_out : v_out);
         __half* dst1 = copy_k && copy_v ? static_cast<__half*>(v_out) : nullptr;
-        return from_cuda(launch_residual_append(src0, src1, x_bh_stride, tail, dst0, dst1, BH, out_bh_stride, n, strm));
+        return from_cuda(
+            launch_residual_append(src0, src1, x_bh_stride, tail, dst0, dst1, BH, out_bh_stride, n, D, strm));
     }
     return KIVI_OK;
 }
@@ -322,8 +329,8 @@ kivi_status kivi_flush_kv(const void* k_f16, const void* v_f16, int BH, int S, i
     if (n_flushed) *n_flushed = nk;
     if (nk == 0) return KIVI_OK;
     return from_cuda(launch_flush_kv(
-        flush_args(k_f16, BH, x_bh_stride, nk, kcodes_u8, kscale, kzero_f16, s_off, s_cap, group_size),
-        flush_args(v_f16, BH, x_bh_stride, nv, vcodes_u8, vscale, vzero_f16, s_off, s_cap, group_size), bits,
+        flush_args(k_f16, BH, x_bh_stride, nk, kcodes_u8, kscale, kzero_f16, s_off, s_cap, group_size, D),
+        flush_args(v_f16, BH, x_bh_stride, nv, vcodes_u8, vscale, vzero_f16, s_off, s_cap, group_size, D), bits,
         reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -348,6 +355,7 @@ kivi_status kivi_dequant(kivi_axis axis, const void* codes_u8, const float* scal
     a.s_cap = s_cap;
     a.out = static_cast<__half*>(out_f16);
     a.G = group_size;
+    a.D = D;
     return from_cuda(launch_dequant((int)axis, a, bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -377,12 +385,13 @@ kivi_status kivi_dequant_kv(const void* kcodes_u8, const float* kscale, const vo
     k.S = v.S = S;
     k.s_cap = v.s_cap = s_cap;
     k.G = v.G = group_size;
+    k.D = v.D = D;
     return from_cuda(launch_dequant_kv(k, v, bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kivi_status kivi_residual_append(const void* src_f16, int src_bh_stride, int n_new, void* res_f16,
                                  int BH, int res_cap, int D, int n_res, kivi_stream_t stream) {
-    if (D != kD) return KIVI_ERR_UNSUPPORTED;
+    if (!head_dim_ok(D)) return KIVI_ERR_UNSUPPORTED;
     if (BH <= 0 || n_new < 0 || n_res < 0 || res_cap <= 0 || src_bh_stride < n_new ||
         (long long)n_res + n_new > res_cap)
         return KIVI_ERR_INVALID_ARG;
@@ -390,26 +399,26 @@ kivi_status kivi_residual_append(const void* src_f16, int src_bh_stride, int n_n
     if (!src_f16 || !res_f16) return KIVI_ERR_INVALID_ARG;
     if (!aligned16(src_f16) || !aligned16(res_f16)) return KIVI_ERR_ALIGNMENT;
     return from_cuda(launch_residual_append(static_cast<const __half*>(src_f16), nullptr, src_bh_stride, n_new,
-                                            static_cast<__half*>(res_f16), nullptr, BH, res_cap, n_res,
+                                            static_cast<__half*>(res_f16), nullptr, BH, res_cap, n_res, D,
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kivi_status kivi_residual_compact(void* res_f16, int BH, int res_cap, int D, int n_res, int n_drop,
                                   kivi_stream_t stream) {
-    if (D != kD) return KIVI_ERR_UNSUPPORTED;
+    if (!head_dim_ok(D)) return KIVI_ERR_UNSUPPORTED;
     if (BH <= 0 || res_cap <= 0 || n_res < 0 || n_res > res_cap || n_drop < 0 || n_drop > n_res)
         return KIVI_ERR_INVALID_ARG;
     if (n_drop == 0 || n_drop == n_res) return KIVI_OK;
     if (!res_f16) return KIVI_ERR_INVALID_ARG;
     if (!aligned16(res_f16)) return KIVI_ERR_ALIGNMENT;
-    return from_cuda(launch_residual_compact(static_cast<__half*>(res_f16), nullptr, BH, res_cap, n_res, n_drop,
+    return from_cuda(launch_residual_compact(static_cast<__half*>(res_f16), nullptr, BH, res_cap, n_res, n_drop, D,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kivi_status kivi_residual_append_kv(const void* k_src_f16, const void* v_src_f16, int src_bh_stride, int n_new,
                                     void* k_res_f16, void* v_res_f16, int BH, int res_cap, int D, int n_res,
                                     kivi_stream_t stream) {
-    if (D != kD) return KIVI_ERR_UNSUPPORTED;
+    if (!head_dim_ok(D)) return KIVI_ERR_UNSUPPORTED;
     if (BH <= 0 || n_new < 0 || n_res < 0 || res_cap <= 0 || src_bh_stride < n_new ||
         (long long)n_res + n_new > res_cap)
         return KIVI_ERR_INVALID_ARG;
@@ -420,19 +429,19 @@ kivi_status kivi_residual_append_kv(const void* k_src_f16, const void* v_src_f16
     return from_cuda(launch_residual_append(static_cast<const __half*>(k_src_f16),
                                             static_cast<const __half*>(v_src_f16), src_bh_stride, n_new,
                                             static_cast<__half*>(k_res_f16), static_cast<__half*>(v_res_f16), BH,
-                                            res_cap, n_res, reinterpret_cast<cudaStream_t>(stream)));
+                                            res_cap, n_res, D, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, int res_cap, int D, int n_res,
                                      int n_drop, kivi_stream_t stream) {
-    if (D != kD) return KIVI_ERR_UNSUPPORTED;
+    if (!head_dim_ok(D)) return KIVI_ERR_UNSUPPORTED;
     if (BH <= 0 || res_cap <= 0 || n_res < 0 || n_res > res_cap || n_drop < 0 || n_drop > n_res)
         return KIVI_ERR_INVALID_ARG;
     if (n_drop == 0 || n_drop == n_res) return KIVI_OK;
     if (!k_res_f16 || !v_res_f16) return KIVI_ERR_INVALID_ARG;
     if (!aligned16(k_res_f16) || !aligned16(v_res_f16)) return KIVI_ERR_ALIGNMENT;
     return from_cuda(launch_residual_compact(static_cast<__half*>(k_res_f16), static_cast<__half*>(v_res_f16), BH,
-                                             res_cap, n_res, n_drop, reinterpret_cast<cudaStream_t>(stream)));
+                                             res_cap, n_res, n_drop, D, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D) {
@@ -456,6 +465,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
                                int D, int group_size, int bits, float sm_scale, float* out_f32,
                                void* workspace, size_t workspace_bytes_, kivi_stream_t stream) {
     kivi_status st = shape_check(D, group_size, bits);
+    if (st == KIVI_OK && D != kD) st = KIVI_ERR_UNSUPPORTED;  // the decode's fragments span 128 channels
     if (st != KIVI_OK) return st;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S_q < 0 || n_res < 0 ||
         S_q + n_res == 0 || S_q > s_cap || n_res > res_cap || s_cap < 0 || res_cap < 0 ||

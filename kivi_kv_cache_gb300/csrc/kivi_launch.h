@@ -9,8 +9,8 @@
 
 namespace kivi {
 
-constexpr int kD = 128;  // head_dim compiled in
-constexpr int kG = 32;   // group_size compiled in
+constexpr int kD = 128;  // head dim of the decode (the flush, dequant and residual also take 64 and 256)
+constexpr int kG = 32;   // the default group size
 
 struct FlushArgs {
     const __half* x;      // [BH, x_bh_stride, D], tokens [0, n_flush) used
@@ -25,6 +25,7 @@ struct FlushArgs {
     __half* fq = nullptr;      // fake quantization: fp16 reconstructions [BH, fq_bh_stride, D] instead of a store
     long long fq_bh_stride = 0;
     int G = kG;                // group size: 32, 64 or 128
+    int D = kD;                // head dim: 64, 128 or 256 (G <= D)
 };
 
 struct DequantArgs {
@@ -36,6 +37,7 @@ struct DequantArgs {
     int s_cap;
     __half* out;          // [BH, S, D]
     int G = kG;           // group size: 32, 64 or 128
+    int D = kD;           // head dim: 64, 128 or 256 (G <= D)
 };
 
 struct DecodeArgs {
@@ -142,9 +144,9 @@ cudaError_t launch_dequant(int axis, const DequantArgs& a, int bits, cudaStream_
 cudaError_t launch_dequant_kv(const DequantArgs& k, const DequantArgs& v, int bits, cudaStream_t stream);
 // src1/res1 may be null (one tensor); otherwise both pairs are handled in one launch
 cudaError_t launch_residual_append(const __half* src0, const __half* src1, long long src_bh_stride,
-                                   int n_new, __half* res0, __half* res1, int BH, int res_cap, int n_res,
+                                   int n_new, __half* res0, __half* res1, int BH, int res_cap, int n_res, int D,
                                    cudaStream_t stream);
-cudaError_t launch_residual_compact(__half* res0, __half* res1, int BH, int res_cap, int n_res, int n_drop,
+cudaError_t launch_residual_compact(__half* res0, __half* res1, int BH, int res_cap, int n_res, int n_drop, int D,
                                     cudaStream_t stream);
 // Fused decodes; each merges its own splits in the same launch.
 // One warp per tile: gq in {1, 2, 4}, or any other gq in a.q_sub sub-groups of

@@ -75,7 +75,9 @@ def flush(L, name="kivi_flush_keys", x=FAKE, BH=8, S=256, stride=256, D=128, G=3
 @pytest.mark.parametrize("name", ["kivi_flush_keys", "kivi_flush_values"])
 def test_flush_rejects_bad_arguments_without_launching(L, name):
     assert flush(L, name, bits=3)[0] == UNSUPPORTED
-    assert flush(L, name, D=64)[0] == UNSUPPORTED
+    assert flush(L, name, D=96)[0] == UNSUPPORTED
+    assert flush(L, name, D=512)[0] == UNSUPPORTED
+    assert flush(L, name, D=64, G=128)[0] == UNSUPPORTED  # a value group would outgrow the row
     assert flush(L, name, G=16)[0] == UNSUPPORTED
     assert flush(L, name, G=256)[0] == UNSUPPORTED
     assert flush(L, name, G=96)[0] == UNSUPPORTED
@@ -112,7 +114,7 @@ def test_dequant_rejects_bad_arguments(L):
 def test_residual_rejects_bad_arguments(L):
     assert L.kivi_residual_append(FAKE, 4, 4, FAKE, 8, 160, 128, 158, None) == INVALID  # overflow
     assert L.kivi_residual_append(FAKE, 2, 4, FAKE, 8, 160, 128, 0, None) == INVALID    # stride < n_new
-    assert L.kivi_residual_append(FAKE, 4, 4, FAKE, 8, 160, 64, 0, None) == UNSUPPORTED
+    assert L.kivi_residual_append(FAKE, 4, 4, FAKE, 8, 160, 96, 0, None) == UNSUPPORTED  # D in {64, 128, 256}
     assert L.kivi_residual_append(FAKE + 2, 4, 4, FAKE, 8, 160, 128, 0, None) == ALIGN
     assert L.kivi_residual_append(None, 4, 0, None, 8, 160, 128, 0, None) == OK
     assert L.kivi_residual_compact(FAKE, 8, 160, 128, 100, 101, None) == INVALID
@@ -131,6 +133,8 @@ def decode(L, q=FAKE, S_q=2080, s_cap=2080, n_res=158, res_cap=160, B=1, Hq=32, 
 def test_decode_rejects_bad_arguments(L):
     assert decode(L, Hq=12) == INVALID               # 12 / 8 is not an integer
     assert decode(L, G=16) == UNSUPPORTED            # group sizes 32, 64, 128
+    assert decode(L, D=64) == UNSUPPORTED            # the decode takes D = 128 only
+    assert decode(L, D=256) == UNSUPPORTED
     assert decode(L, G=64) == INVALID                # s_cap 2080 is not a multiple of 64
     assert decode(L, G=128, S_q=2048, s_cap=2048, ws=None) == WORKSPACE  # G = 128 passes the checks
     assert decode(L, Hq=520) == UNSUPPORTED          # 65 query heads per KV head
@@ -151,7 +155,7 @@ def test_decode_rejects_bad_arguments(L):
 def test_fake_quant_argument_checks(L):
     n = ctypes.c_int(-7)
     fk = L.kivi_fake_quant_keys
-    assert fk(FAKE, 8, 256, 256, 64, 32, 4, 128, FAKE + 4096, 256, ctypes.byref(n), None) == UNSUPPORTED
+    assert fk(FAKE, 8, 256, 256, 96, 32, 4, 128, FAKE + 4096, 256, ctypes.byref(n), None) == UNSUPPORTED
     assert fk(FAKE, 8, 256, 256, 128, 32, 3, 128, FAKE + 4096, 256, ctypes.byref(n), None) == UNSUPPORTED
     assert fk(FAKE, 8, 256, 200, 128, 32, 4, 128, FAKE + 4096, 256, ctypes.byref(n), None) == INVALID  # stride < S
     assert fk(FAKE, 8, 256, 256, 128, 32, 4, 128, FAKE + 4096, 255, ctypes.byref(n), None) == INVALID
