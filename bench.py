@@ -662,11 +662,15 @@ def run_sweep(args):
     # stores of group size 64 and 128
     cases += [(1, 2080, 158, 4, 32, 64), (1, 16384 - 128, 128, 4, 32, 64), (1, 16384 - 128, 128, 4, 32, 128),
               (32, 4032, 64, 4, 32, 64), (32, 4032, 64, 4, 32, 128), (1, 32768 - 128, 128, 2, 32, 128)]
+    # head dims 64 and 256
+    cases += [(1, 16384 - 128, 128, 4, 32, 32, 64), (32, 4032, 64, 4, 32, 32, 64),
+              (1, 16384 - 128, 128, 4, 32, 32, 256), (32, 4032, 64, 4, 32, 32, 256)]
     for case in cases:
         B, S_q, n_res, bits = case[:4]
         Hq = case[4] if len(case) > 4 else 32
         G = case[5] if len(case) > 5 else 32
-        w = synth.Workload("decode", B=B, Hkv=8, Hq=Hq, D=128, S=S_q + n_res, bits=bits, G=G, R=0,
+        D = case[6] if len(case) > 6 else 128
+        w = synth.Workload("decode", B=B, Hkv=8, Hq=Hq, D=D, S=S_q + n_res, bits=bits, G=G, R=0,
                            n_outlier=4, outlier_scale=8.0, seed=11)
         s_cap = max(1, -(-S_q // G)) * G
         per_tok = 2 * w.D * bits / 8 + w.D * 6 / w.G + (w.D // w.G) * 6
@@ -690,7 +694,7 @@ def run_sweep(args):
         fns = [lambda e=e: kv.kivi_decode_attend(e[0], e[1], e[2], S_q, e[3], e[4], n_res, w.Hkv, w.sm_scale,
                                                  out=e[5], workspace=e[6]) for e in entries]
         timed(fns, nbytes, "decode_attend", {"B": B, "Hkv": 8, "Hq": Hq, "S_kv": S_q + n_res, "bits": bits,
-                                             "G": G, "pool": P, "tokens_per_s": None})
+                                             "G": G, "D": D, "pool": P, "tokens_per_s": None})
         del entries, fns
         torch.cuda.empty_cache()
 

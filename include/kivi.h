@@ -36,8 +36,7 @@
  *     in bounds.
  *   - Supported shapes: bits in {2, 4}; group_size G in {32, 64, 128};
  *     head_dim D in {64, 128, 256} with G <= D (a value group lies within one
- *     token row) for the flush, dequant, fake quantization and the residual
- *     window; the decode takes D = 128. Other values return
+ *     token row), for every entry point. Other values return
  *     KIVI_ERR_UNSUPPORTED.
  *
  * Store layout (one store per tensor, keys and values separately):
@@ -260,8 +259,8 @@ kivi_status kivi_decode_workspace_init(void* workspace, size_t workspace_bytes, 
  * laid out and initialised as described there (may be NULL when that size is
  * 0).
  * Errors: INVALID_ARG if S_q + n_res == 0, S_q > s_cap, n_res > res_cap or
- * Hq % Hkv != 0; UNSUPPORTED if D != 128, Hq/Hkv > 64, or group_size or bits
- * as for the flush; WORKSPACE if the workspace is NULL or too small. Stores of
+ * Hq % Hkv != 0; UNSUPPORTED if Hq/Hkv > 64, or D, group_size or bits as for
+ * the flush; WORKSPACE if the workspace is NULL or too small. Stores of
  * every supported group size (32, 64, 128) are read; their key groups align
  * with the kernels' 32-token tiles.
  */

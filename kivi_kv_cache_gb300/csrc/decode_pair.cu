@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, kPairs <= 4 ? 2 : 1) decode_pair_ker
         return;
     }
     if (take_last_ticket(a, bh, reinterpret_cast<int*>(misc + 96)))
-        merge_splits<16>(a, (long long)b * a.Hq + h0, GQ, warp, kWarps, lane, reinterpret_cast<float*>(smem));
+        merge_splits<16, kD>(a, (long long)b * a.Hq + h0, GQ, warp, kWarps, lane, reinterpret_cast<float*>(smem));
 }
 
 template <int BITS, int GQ, bool CL>

@@ -38,9 +38,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
 
-// Flush, dequant and fake quantization: D in {64, 128, 256}, G in {32, 64,
-// 128} with G <= D (a value group lies within one token row), 2 or 4 bits.
-// The decode also needs D = 128.
+// Every op: D in {64, 128, 256}, G in {32, 64, 128} with G <= D (a value
+// group lies within one token row), 2 or 4 bits.
 kivi_status shape_check(int D, int G, int bits) {
     if (!head_dim_ok(D) || (G != 32 && G != 64 && G != 128) || G > D || (bits != 2 && bits != 4))
         return KIVI_ERR_UNSUPPORTED;
@@ -103,8 +102,10 @@ constexpr bool kOneWave = KIVI_DECODE_ONE_WAVE != 0;
 
 bool mma_group(int gq) { return gq == 1 || gq == 2 || gq == 4; }
 
-// pair_ok: the warp-pair kernel may run (it reads stores of group size 32 only)
-DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool pair_ok) {
+// pair_ok: the warp-pair kernel may run (it reads stores of group size 32 at
+// head dim 128 only). D: head dim; D = 256 keeps 8 warps per SM resident
+// instead of 16.
+DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool pair_ok, int D) {
     DecodePlan p;
     const int gq = Hkv > 0 && Hq >= Hkv ? Hq / Hkv : 1;
     p.q_sub = mma_group(gq) ? 1 : (gq + 3) / 4;
@@ -121,7 +122,7 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool 
         // a grid of multi-tile warps that just spills into a second wave of
         // resident CTAs (at most 1.25 waves) takes up to half again as many
         // tiles per warp instead
-        const long long slots = (long long)(16 / p.warps_per_cta) * sm_count();  // 16 warps per SM
+        const long long slots = (long long)((D == 256 ? 8 : 16) / p.warps_per_cta) * sm_count();  // resident CTAs
         auto ctas = [&](long long t) { return heads * ((p.n_tiles + p.warps_per_cta * t - 1) / (p.warps_per_cta * t)); };
         if (ctas(tpw) > slots && 4 * ctas(tpw) <= 5 * slots) {
             long long t = tpw;
@@ -149,14 +150,14 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool 
 }
 
 // Workspace: [merge counters, KIVI_DECODE_COUNTER_BYTES][part_o, 256-aligned][part_ml]
-size_t part_o_bytes(int B, int Hq, const DecodePlan& p) {
-    return (((size_t)B * Hq * p.n_split * kD * sizeof(float)) + 255) & ~(size_t)255;
+size_t part_o_bytes(int B, int Hq, int D, const DecodePlan& p) {
+    return (((size_t)B * Hq * p.n_split * D * sizeof(float)) + 255) & ~(size_t)255;
 }
 
-size_t workspace_bytes(int B, int Hq, const DecodePlan& p) {
+size_t workspace_bytes(int B, int Hq, int D, const DecodePlan& p) {
     if (p.n_split <= 1) return 0;
     const size_t ml = (size_t)B * Hq * p.n_split * 2 * sizeof(float);
-    return (size_t)KIVI_DECODE_COUNTER_BYTES + part_o_bytes(B, Hq, p) + ml;
+    return (size_t)KIVI_DECODE_COUNTER_BYTES + part_o_bytes(B, Hq, D, p) + ml;
 }
 
 kivi_status flush_check(const void* x, int BH, int S, int x_bh_stride, int D, int G, int bits,
@@ -445,14 +446,14 @@ kivi_status kivi_residual_compact_kv(void* k_res_f16, void* v_res_f16, int BH, i
 }
 
 size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S_q < 0 || n_res < 0 || D != kD || S_q + n_res == 0)
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S_q < 0 || n_res < 0 || !head_dim_ok(D) || S_q + n_res == 0)
         return 0;
     // the plan depends on the bit width and, through the choice of kernel, on
     // the group size; the size covers every plan
     size_t w = 0;
     for (int bits : {2, 4})
         for (bool pair_ok : {false, true}) {
-            const size_t wb = workspace_bytes(B, Hq, make_plan(B, Hkv, Hq, S_q, n_res, bits, pair_ok));
+            const size_t wb = workspace_bytes(B, Hq, D, make_plan(B, Hkv, Hq, S_q, n_res, bits, pair_ok && D == kD, D));
             if (wb > w) w = wb;
         }
     return w;
@@ -465,7 +466,6 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
                                int D, int group_size, int bits, float sm_scale, float* out_f32,
                                void* workspace, size_t workspace_bytes_, kivi_stream_t stream) {
     kivi_status st = shape_check(D, group_size, bits);
-    if (st == KIVI_OK && D != kD) st = KIVI_ERR_UNSUPPORTED;  // the decode's fragments span 128 channels
     if (st != KIVI_OK) return st;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S_q < 0 || n_res < 0 ||
         S_q + n_res == 0 || S_q > s_cap || n_res > res_cap || s_cap < 0 || res_cap < 0 ||
@@ -482,8 +482,8 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
         !aligned16(vzero_f16) || !aligned16(k_res_f16) || !aligned16(v_res_f16) ||
         !aligned16(workspace))
         return KIVI_ERR_ALIGNMENT;
-    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res, bits, group_size == kG);
-    const size_t need = workspace_bytes(B, Hq, p);
+    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res, bits, group_size == kG && D == kD, D);
+    const size_t need = workspace_bytes(B, Hq, D, p);
     if (need > 0 && (!workspace || workspace_bytes_ < need)) return KIVI_ERR_WORKSPACE;
 
     DecodeArgs a;
@@ -497,6 +497,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
     a.S_q = S_q;
     a.s_cap = s_cap;
     a.g_shift = group_size == 128 ? 2 : (group_size == 64 ? 1 : 0);
+    a.D = D;
     a.k_res = static_cast<const __half*>(k_res_f16);
     a.v_res = static_cast<const __half*>(v_res_f16);
     a.n_res = n_res;
@@ -515,7 +516,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
     char* ws = static_cast<char*>(workspace);
     a.counters = need > 0 ? reinterpret_cast<unsigned int*>(ws) : nullptr;
     a.part_o = need > 0 ? reinterpret_cast<float*>(ws + KIVI_DECODE_COUNTER_BYTES) : nullptr;
-    a.part_ml = need > 0 ? reinterpret_cast<float*>(ws + KIVI_DECODE_COUNTER_BYTES + part_o_bytes(B, Hq, p))
+    a.part_ml = need > 0 ? reinterpret_cast<float*>(ws + KIVI_DECODE_COUNTER_BYTES + part_o_bytes(B, Hq, D, p))
                          : nullptr;
     a.out = out_f32;
     const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);

@@ -51,6 +51,7 @@ struct DecodeArgs {
     int S_q;
     int s_cap;
     int g_shift;          // log2(G / 32): the store's group size is 32, 64 or 128
+    int D = kD;           // head dim: 64, 128 or 256 (the warp-pair kernel: 128)
     const __half* k_res;  // [B*Hkv, res_cap, D]
     const __half* v_res;
     int n_res;
@@ -150,8 +151,11 @@ cudaError_t launch_residual_compact(__half* res0, __half* res1, int BH, int res_
                                     cudaStream_t stream);
 // Fused decodes; each merges its own splits in the same launch.
 // One warp per tile: gq in {1, 2, 4}, or any other gq in a.q_sub sub-groups of
-// up to 4 query heads; stores of group size 32, 64 or 128.
+// up to 4 query heads; stores of group size 32, 64 or 128; head dim a.D of 64,
+// 128 or 256 (the _d64 / _d256 forms serve one head dim each).
 cudaError_t launch_decode_mma(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
+cudaError_t launch_decode_mma_d64(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
+cudaError_t launch_decode_mma_d256(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 // gq in {1, 2, 4}: two warps per tile, 4 warp pairs per CTA (small batches);
 // stores of group size 32 only.
 cudaError_t launch_decode_pair(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);

@@ -133,8 +133,9 @@ def decode(L, q=FAKE, S_q=2080, s_cap=2080, n_res=158, res_cap=160, B=1, Hq=32, 
 def test_decode_rejects_bad_arguments(L):
     assert decode(L, Hq=12) == INVALID               # 12 / 8 is not an integer
     assert decode(L, G=16) == UNSUPPORTED            # group sizes 32, 64, 128
-    assert decode(L, D=64) == UNSUPPORTED            # the decode takes D = 128 only
-    assert decode(L, D=256) == UNSUPPORTED
+    assert decode(L, D=96) == UNSUPPORTED            # head dims 64, 128, 256
+    assert decode(L, D=64, G=128, S_q=2048, s_cap=2048) == UNSUPPORTED  # G > D
+    assert decode(L, D=256, ws=None) == WORKSPACE    # D = 256 passes the checks
     assert decode(L, G=64) == INVALID                # s_cap 2080 is not a multiple of 64
     assert decode(L, G=128, S_q=2048, s_cap=2048, ws=None) == WORKSPACE  # G = 128 passes the checks
     assert decode(L, Hq=520) == UNSUPPORTED          # 65 query heads per KV head
@@ -178,7 +179,10 @@ def test_workspace_init_rejects_null(L):
 
 def test_workspace_size(L):
     assert L.kivi_decode_workspace_size(1, 32, 8, 0, 0, 128) == 0
-    assert L.kivi_decode_workspace_size(1, 32, 8, 64, 0, 64) == 0
+    assert L.kivi_decode_workspace_size(1, 32, 8, 64, 0, 96) == 0      # unsupported head dim
+    # the partials hold D floats per split: a wider head needs a larger workspace
+    w64, w128, w256 = (L.kivi_decode_workspace_size(1, 32, 8, 4096, 64, d) for d in (64, 128, 256))
+    assert 32768 < w64 < w128 < w256
     small = L.kivi_decode_workspace_size(1, 32, 8, 2080, 158, 128)
     big = L.kivi_decode_workspace_size(1, 32, 8, 32640, 128, 128)
     assert 0 < small <= big

@@ -1,8 +1,8 @@
-"""GPU parity of the flush, dequant, fake quantization and residual window at
-head dims 64 and 256 (the kernels are templated on D; D = 128 is covered by
-the other parity files). Codes, packed bytes, scales, zeros and fp16 outputs
-must equal the oracle's bit for bit. The fused decode takes D = 128 only and
-rejects other head dims on the host, before any launch."""
+"""GPU parity of the flush, dequant, fake quantization, residual window and
+fused decode at head dims 64 and 256 (the kernels are templated on D; D = 128
+is covered by the other parity files). Codes, packed bytes, scales, zeros and
+fp16 outputs must equal the oracle's bit for bit; the decode must lie within
+2e-3 of the float64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -175,16 +175,76 @@ def test_residual_head_dims(D):
     assert same(host(kres), rk) and same(host(vres), rv)
 
 
+TOL = 2e-3  # decode max-abs error against the float64 oracle
+
+
+def decode_both(D, G, bits, B, hq, hkv, S_q, n_res, seed, noalloc=False):
+    """Flush K and V of S_q tokens on both sides, then decode one query per
+    head over the store plus n_res fp16 tokens; returns (gpu, oracle)."""
+    rng = np.random.default_rng(seed)
+    BH = B * hkv
+    k = synth.keys(rng, (BH, S_q + n_res), D, outliers(D), 8.0)
+    v = synth.normal(rng, (BH, S_q + n_res, D))
+    q = synth.normal(rng, (B, hq, D))
+    sm_scale = 1.0 / np.sqrt(D)
+    s_cap = max(G, -(-S_q // G) * G)
+    gk = kv.KiviStore(0, BH, s_cap, D, G, bits, device=DEV)
+    gv = kv.KiviStore(1, BH, s_cap, D, G, bits, device=DEV)
+    rk = oracle.Store(0, BH, s_cap, D, G, bits)
+    rv = oracle.Store(1, BH, s_cap, D, G, bits)
+    if S_q:
+        kv.kivi_flush_kv(dev(k), dev(v), 0, gk, gv, n_tokens=S_q)
+        oracle.flush(0, k, S_q, rk)
+        oracle.flush(1, v, S_q, rv)
+    kr = np.ascontiguousarray(k[:, S_q:])
+    vr = np.ascontiguousarray(v[:, S_q:])
+    fn = kv.kivi_decode_attend_noalloc if noalloc else kv.kivi_decode_attend
+    out = fn(dev(q), gk, gv, S_q, dev(kr), dev(vr), n_res, hkv, sm_scale)
+    ref = oracle.decode_attend(q, rk, rv, S_q, kr, vr, n_res, hkv, sm_scale)
+    return host(out).astype(np.float64), ref
+
+
+DECODE_SHAPES = [
+    (2, 8, 8, 70, 9),        # ragged last key group; a tile of 6 valid tokens
+    (2, 32, 8, 4096, 37),    # 4 heads per KV head, several splits per head
+    (1, 24, 8, 1000, 200),   # 3 heads per KV head (sub-groups), ragged store
+    (1, 16, 2, 16384, 100),  # sub-groups of a long cache: more splits than a cluster holds
+    (3, 4, 4, 64, 0),        # store only
+    (1, 8, 8, 0, 37),        # fp16 residual only
+]
+
+
 @pytest.mark.parametrize("D", [64, 256])
-def test_decode_rejects_other_head_dims(D):
-    """Checked on the host: UNSUPPORTED, nothing launched, out untouched."""
-    G = 32
-    ks = kv.KiviStore(0, 8, 64, D, G, 4, device=DEV)
-    vs = kv.KiviStore(1, 8, 64, D, G, 4, device=DEV)
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("big_g", [False, True])
+@pytest.mark.parametrize("B,hq,hkv,S_q,n_res", DECODE_SHAPES)
+def test_decode_head_dims(D, bits, big_g, B, hq, hkv, S_q, n_res):
+    """The fused decode at head dims 64 and 256 (group size 32, and 64 at
+    D = 64 or 128 at D = 256) against the float64 oracle."""
+    G = (64 if D == 64 else 128) if big_g else 32
+    out, ref = decode_both(D, G, bits, B, hq, hkv, S_q, n_res, seed=900 + D + G + bits + S_q + hq)
+    err = np.max(np.abs(out - ref))
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("D", [64, 256])
+def test_decode_head_dims_batched_and_noalloc(D):
+    """A batch of 8 sequences x 2048 tokens (4 query heads per KV head), and
+    the no-alloc entry point on a split plan."""
+    out, ref = decode_both(D, 32, 4, 8, 32, 8, 2016, 32, seed=950 + D)
+    assert np.max(np.abs(out - ref)) <= TOL
+    out, ref = decode_both(D, 32, 4, 1, 32, 8, 4032, 64, seed=960 + D, noalloc=True)
+    assert np.max(np.abs(out - ref)) <= TOL
+
+
+def test_decode_rejects_unsupported_head_dim_pairs():
+    """G > D is refused on the host: UNSUPPORTED, nothing launched."""
+    D, G = 64, 128
+    ks = kv.KiviStore(0, 8, 128, D, G, 4, device=DEV)
+    vs = kv.KiviStore(1, 8, 128, D, G, 4, device=DEV)
     q = torch.zeros((1, 32, D), dtype=torch.float16, device=DEV)
     res = torch.zeros((8, 16, D), dtype=torch.float16, device=DEV)
     out = torch.full((1, 32, D), 7.0, dtype=torch.float32, device=DEV)
-    assert kv.kivi_decode_workspace_size(1, 32, 8, 64, 16, D) == 0
     with pytest.raises(kv.KiviError) as e:
         kv.kivi_decode_attend(q, ks, vs, 64, res, res, 16, 8, 0.1, out=out)
     assert e.value.status == 2
