@@ -121,7 +121,8 @@ def flush_count(n_res: int, residual_length: int, group_size: int) -> int:
 
 
 def quantize_group(v, bits: int):
-    """One group of fp32 values -> (codes uint8[n], scale f32, zero f32)."""
+    """One group of fp32 values -> (codes uint8[n], scale f32, zero f32).
+    bits may carry SCALE_F16 (the returned scale is then the binary16 one)."""
     v = np.ascontiguousarray(v, dtype=np.float32)
     codes = np.empty(v.size, np.uint8)
     s = np.zeros(1, np.float32)
@@ -148,21 +149,32 @@ def unpack_codes(packed, n: int, bits: int) -> np.ndarray:
 # store
 # --------------------------------------------------------------------------
 
+# Option bit of the C oracle's `bits` arguments: scales stored as binary16.
+SCALE_F16 = 0x100
+
+
 class Store:
     """Quantized store for one tensor (keys or values), host numpy arrays.
 
     codes  uint8   [BH, s_cap, D*bits/8]
-    scale  float32 [BH, s_cap/G, D] (keys)  or [BH, s_cap, D/G] (values)
+    scale  float32 (or float16 with scale_f16) [BH, s_cap/G, D] (keys) or
+           [BH, s_cap, D/G] (values)
     zero   float16 same shape as scale
     """
 
-    def __init__(self, axis: int, BH: int, s_cap: int, D: int, G: int, bits: int):
+    def __init__(self, axis: int, BH: int, s_cap: int, D: int, G: int, bits: int, scale_f16: bool = False):
         assert s_cap % G == 0
         self.axis, self.BH, self.s_cap, self.D, self.G, self.bits = axis, BH, s_cap, D, G, bits
+        self.scale_f16 = scale_f16
         self.codes = np.zeros((BH, s_cap, D * bits // 8), np.uint8)
         meta = (BH, s_cap // G, D) if axis == 0 else (BH, s_cap, D // G)
-        self.scale = np.zeros(meta, np.float32)
+        self.scale = np.zeros(meta, np.float16 if scale_f16 else np.float32)
         self.zero = np.zeros(meta, np.float16)
+
+    @property
+    def c_bits(self) -> int:
+        """The `bits` argument of the C oracle: width plus the scale option."""
+        return self.bits | (SCALE_F16 if self.scale_f16 else 0)
 
 
 def flush(axis: int, x, n_flush: int, store: Store, s_off: int = 0, t0: int = 0):
@@ -173,7 +185,7 @@ def flush(axis: int, x, n_flush: int, store: Store, s_off: int = 0, t0: int = 0)
     assert 0 <= t0 and t0 + n_flush <= S
     fn = _load().orc_flush_keys if axis == 0 else _load().orc_flush_values
     ptr = ctypes.c_void_p(x.ctypes.data + t0 * D * 2)
-    fn(ptr, BH, S, n_flush, D, store.G, store.bits, _p(store.codes),
+    fn(ptr, BH, S, n_flush, D, store.G, store.c_bits, _p(store.codes),
        _p(store.scale), _p(store.zero.view(np.uint16)), s_off, store.s_cap)
     return store
 
@@ -182,7 +194,7 @@ def recon_f32(store: Store, S: int) -> np.ndarray:
     out = np.empty((store.BH, S, store.D), np.float32)
     _load().orc_recon_f32(store.axis, _p(store.codes), _p(store.scale),
                           _p(store.zero.view(np.uint16)), store.BH, S, store.D,
-                          store.G, store.bits, store.s_cap, _p(out))
+                          store.G, store.c_bits, store.s_cap, _p(out))
     return out
 
 
@@ -190,7 +202,7 @@ def dequant(store: Store, S: int) -> np.ndarray:
     out = np.empty((store.BH, S, store.D), np.uint16)
     _load().orc_dequant(store.axis, _p(store.codes), _p(store.scale),
                         _p(store.zero.view(np.uint16)), store.BH, S, store.D,
-                        store.G, store.bits, store.s_cap, _p(out))
+                        store.G, store.c_bits, store.s_cap, _p(out))
     return out.view(np.float16)
 
 
@@ -214,6 +226,7 @@ def residual_compact(res, n_res: int, n_drop: int):
 def decode_attend(q, kstore: Store, vstore: Store, S_q: int, k_res, v_res, n_res: int,
                   Hkv: int, sm_scale: float) -> np.ndarray:
     """q [B, Hq, D] fp16; residual [B*Hkv, res_cap, D] fp16 -> out [B, Hq, D] float64."""
+    assert kstore.scale_f16 == vstore.scale_f16, "one scale storage for both stores"
     q = _f16(q)
     k_res = _f16(k_res)
     v_res = _f16(v_res)
@@ -226,5 +239,5 @@ def decode_attend(q, kstore: Store, vstore: Store, S_q: int, k_res, v_res, n_res
         _p(vstore.codes), _p(vstore.scale), _p(vstore.zero.view(np.uint16)),
         S_q, kstore.s_cap,
         _p(k_res.view(np.uint16)), _p(v_res.view(np.uint16)), n_res, res_cap,
-        B, Hq, Hkv, D, kstore.G, kstore.bits, float(sm_scale), _p(out))
+        B, Hq, Hkv, D, kstore.G, kstore.c_bits, float(sm_scale), _p(out))
     return out

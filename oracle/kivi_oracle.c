@@ -19,6 +19,9 @@
  * Readings where the pages are silent (all listed in the design notes):
  *  - quantizer arithmetic is fp32 after widening the fp16 inputs;
  *  - scale is stored as fp32, zero as fp16 (lossless: zero is an fp16 input);
+ *    with the ORC_SCALE_F16 option bit set in `bits`, scale is stored as
+ *    binary16 (round to nearest even) and the codes are computed with that
+ *    stored scale, so a dequant reproduces exactly what the flush used;
  *  - min and max of -0.0 are taken as +0.0, so the stored zero and scale
  *    never carry a negative sign whatever order equal values are met in;
  *  - max == min gives scale 0, every code 0, recon == min;
@@ -129,10 +132,17 @@ int orc_flush_count(int n_res, int residual_length, int group_size)
  *     scale = (max(group) - min(group)) / (2^bits - 1)
  *     q     = round((x - zero) / scale)          then clip to [0, 2^bits-1]
  * and [F] "Three ways to be off by one bit" #2 fixes the rounding to
- * half-to-even (rint). Each line is one fp32 operation. */
+ * half-to-even (rint). Each line is one fp32 operation.
+ * `bits` is the bit width, optionally ORed with ORC_SCALE_F16: the scale is
+ * then rounded to binary16 before any code is computed (the stored scale is
+ * the one the codes use). The fp16 scale can be 0 for a range far below the
+ * fp16 grid (every code 0), and a subnormal fp16 scale can leave a quotient
+ * past 2^bits - 1, which the clip catches. *scale receives the scale used. */
 void orc_quantize_group(const float* v, int n, int bits,
                         uint8_t* codes, float* scale, float* zero)
 {
+    int f16_scale = (bits & ORC_SCALE_F16) != 0;
+    bits &= ORC_BITS_MASK;
     float mn = v[0];
     float mx = v[0];
     for (int i = 1; i < n; ++i) {
@@ -144,6 +154,8 @@ void orc_quantize_group(const float* v, int n, int bits,
     float levels = (float)((1 << bits) - 1); /* 2^bits - 1 */
     float range = mx - mn;
     float s = range / levels;
+    if (f16_scale)
+        s = orc_half_to_float(orc_float_to_half(s)); /* the stored binary16 scale */
     for (int i = 0; i < n; ++i) {
         int q = 0;
         if (s != 0.0f) {                     /* max == min: every code 0 */
@@ -158,6 +170,23 @@ void orc_quantize_group(const float* v, int n, int bits,
     }
     *scale = s;
     *zero = mn;
+}
+
+/* A stored scale: fp32, or binary16 under ORC_SCALE_F16 (element m of the
+ * array either way). */
+static void store_scale(void* scale, long m, float s, int bits)
+{
+    if (bits & ORC_SCALE_F16)
+        ((uint16_t*)scale)[m] = orc_float_to_half(s);
+    else
+        ((float*)scale)[m] = s;
+}
+
+static float load_scale(const void* scale, long m, int bits)
+{
+    if (bits & ORC_SCALE_F16)
+        return orc_half_to_float(((const uint16_t*)scale)[m]);
+    return ((const float*)scale)[m];
 }
 
 /* [F] "Three ways to be off by one bit" #1: the reconstruction is a multiply
@@ -215,10 +244,11 @@ static int fill_group(float* buf, int G, const float* real, int n_real)
  * (head, group, channel). */
 void orc_flush_keys(const uint16_t* x, int BH, int x_bh_stride, int n_flush,
                     int D, int G, int bits,
-                    uint8_t* codes, float* kscale, uint16_t* kzero,
+                    uint8_t* codes, void* kscale, uint16_t* kzero,
                     int s_off, int s_cap)
 {
-    int row_bytes = D * bits / 8;
+    int width = bits & ORC_BITS_MASK;
+    int row_bytes = D * width / 8;
     int ng_cap = s_cap / G;
     int ng = (n_flush + G - 1) / G;
     float* real = (float*)malloc(sizeof(float) * (size_t)G);
@@ -239,12 +269,12 @@ void orc_flush_keys(const uint16_t* x, int BH, int x_bh_stride, int n_flush,
                 for (int t = t0; t < t1; ++t)
                     rows[(long)t * D + d] = q[t - t0];
                 long m = ((long)bh * ng_cap + (s_off / G + g)) * D + d;
-                kscale[m] = s;
+                store_scale(kscale, m, s, bits);
                 kzero[m] = orc_float_to_half(z);
             }
         }
         for (int t = 0; t < n_flush; ++t)
-            orc_pack_codes(rows + (long)t * D, D, bits,
+            orc_pack_codes(rows + (long)t * D, D, width,
                            codes + ((long)bh * s_cap + s_off + t) * row_bytes);
     }
     free(real);
@@ -258,10 +288,11 @@ void orc_flush_keys(const uint16_t* x, int BH, int x_bh_stride, int n_flush,
  * (head, token, group). */
 void orc_flush_values(const uint16_t* x, int BH, int x_bh_stride, int n_flush,
                       int D, int G, int bits,
-                      uint8_t* codes, float* vscale, uint16_t* vzero,
+                      uint8_t* codes, void* vscale, uint16_t* vzero,
                       int s_off, int s_cap)
 {
-    int row_bytes = D * bits / 8;
+    int width = bits & ORC_BITS_MASK;
+    int row_bytes = D * width / 8;
     int ngd = (D + G - 1) / G;
     float* real = (float*)malloc(sizeof(float) * (size_t)G);
     float* buf = (float*)malloc(sizeof(float) * (size_t)G);
@@ -281,10 +312,10 @@ void orc_flush_values(const uint16_t* x, int BH, int x_bh_stride, int n_flush,
                 for (int d = d0; d < d1; ++d)
                     row[d] = q[d - d0];
                 long m = ((long)bh * s_cap + s_off + t) * ngd + j;
-                vscale[m] = s;
+                store_scale(vscale, m, s, bits);
                 vzero[m] = orc_float_to_half(z);
             }
-            orc_pack_codes(row, D, bits,
+            orc_pack_codes(row, D, width,
                            codes + ((long)bh * s_cap + s_off + t) * row_bytes);
         }
     }
@@ -301,17 +332,18 @@ void orc_flush_values(const uint16_t* x, int BH, int x_bh_stride, int n_flush,
 /* recon = q * scale + zero (two roundings), per element, with the scale and
  * zero of the element's group: keys by (token group, channel), values by
  * (token, channel group). */
-void orc_recon_f32(int axis, const uint8_t* codes, const float* scale,
+void orc_recon_f32(int axis, const uint8_t* codes, const void* scale,
                    const uint16_t* zero, int BH, int S, int D, int G, int bits,
                    int s_cap, float* out)
 {
-    int row_bytes = D * bits / 8;
+    int width = bits & ORC_BITS_MASK;
+    int row_bytes = D * width / 8;
     int ng_cap = s_cap / G;
     int ngd = (D + G - 1) / G;
     uint8_t* row = (uint8_t*)malloc((size_t)D);
     for (int bh = 0; bh < BH; ++bh) {
         for (int t = 0; t < S; ++t) {
-            orc_unpack_codes(codes + ((long)bh * s_cap + t) * row_bytes, D, bits, row);
+            orc_unpack_codes(codes + ((long)bh * s_cap + t) * row_bytes, D, width, row);
             for (int d = 0; d < D; ++d) {
                 long m;
                 if (axis == 0)
@@ -319,14 +351,14 @@ void orc_recon_f32(int axis, const uint8_t* codes, const float* scale,
                 else
                     m = ((long)bh * s_cap + t) * ngd + d / G;
                 float z = orc_half_to_float(zero[m]);
-                out[((long)bh * S + t) * D + d] = recon_one(row[d], scale[m], z);
+                out[((long)bh * S + t) * D + d] = recon_one(row[d], load_scale(scale, m, bits), z);
             }
         }
     }
     free(row);
 }
 
-void orc_dequant(int axis, const uint8_t* codes, const float* scale,
+void orc_dequant(int axis, const uint8_t* codes, const void* scale,
                  const uint16_t* zero, int BH, int S, int D, int G, int bits,
                  int s_cap, uint16_t* out)
 {
@@ -375,8 +407,8 @@ void orc_residual_compact(uint16_t* res, int BH, int res_cap, int D, int n_res,
  * h / (Hq / Hkv) (grouped-query attention, [Q] "Picking a model"). No mask:
  * the single query sees every cached token. Computed in float64. */
 void orc_decode_attend(const uint16_t* q,
-                       const uint8_t* kcodes, const float* kscale, const uint16_t* kzero,
-                       const uint8_t* vcodes, const float* vscale, const uint16_t* vzero,
+                       const uint8_t* kcodes, const void* kscale, const uint16_t* kzero,
+                       const uint8_t* vcodes, const void* vscale, const uint16_t* vzero,
                        int S_q, int s_cap,
                        const uint16_t* k_res, const uint16_t* v_res, int n_res, int res_cap,
                        int B, int Hq, int Hkv, int D, int G, int bits, double sm_scale,
@@ -389,18 +421,19 @@ void orc_decode_attend(const uint16_t* q,
     double* K = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * D);
     double* V = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * D);
     double* score = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
-    int row_bytes = D * bits / 8;
+    int row_bytes = D * (bits & ORC_BITS_MASK) / 8;
     int ng_cap = s_cap / G;
     int ngd = (D + G - 1) / G;
+    long esz = (bits & ORC_SCALE_F16) ? 2 : 4; /* bytes per stored scale */
     for (int b = 0; b < B; ++b) {
         for (int hk = 0; hk < Hkv; ++hk) {
             int bh = b * Hkv + hk;
             /* Gather this KV head's rows: store (fp32 recon) then residual. */
             if (S_q > 0) {
                 long off_codes = (long)bh * s_cap * row_bytes;
-                orc_recon_f32(0, kcodes + off_codes, kscale + (long)bh * ng_cap * D,
+                orc_recon_f32(0, kcodes + off_codes, (const char*)kscale + (long)bh * ng_cap * D * esz,
                               kzero + (long)bh * ng_cap * D, 1, S_q, D, G, bits, s_cap, kf);
-                orc_recon_f32(1, vcodes + off_codes, vscale + (long)bh * s_cap * ngd,
+                orc_recon_f32(1, vcodes + off_codes, (const char*)vscale + (long)bh * s_cap * ngd * esz,
                               vzero + (long)bh * s_cap * ngd, 1, S_q, D, G, bits, s_cap, vf);
             }
             for (int t = 0; t < S_q; ++t)

@@ -24,6 +24,13 @@
 
 #include <stdint.h>
 
+/* `bits` arguments: the bit width (2 or 4) in the low byte, optionally ORed
+ * with ORC_SCALE_F16 to store every scale as binary16 instead of fp32 (the
+ * codes are then computed with the stored binary16 scale). Scale arrays are
+ * float32 or uint16 (binary16 bit patterns) accordingly. */
+#define ORC_SCALE_F16 0x100
+#define ORC_BITS_MASK 0xff
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -52,22 +59,22 @@ void orc_unpack_codes(const uint8_t* packed, int n, int bits, uint8_t* codes);
  * written at store token offset s_off of a store with capacity s_cap. */
 void orc_flush_keys(const uint16_t* x, int BH, int x_bh_stride, int n_flush,
                     int D, int G, int bits,
-                    uint8_t* codes, float* kscale, uint16_t* kzero,
+                    uint8_t* codes, void* kscale, uint16_t* kzero,
                     int s_off, int s_cap);
 
 /* Value flush: per-token groups of G channels. Same arguments as above;
  * vscale / vzero are [BH, s_cap, D/G]. */
 void orc_flush_values(const uint16_t* x, int BH, int x_bh_stride, int n_flush,
                       int D, int G, int bits,
-                      uint8_t* codes, float* vscale, uint16_t* vzero,
+                      uint8_t* codes, void* vscale, uint16_t* vzero,
                       int s_off, int s_cap);
 
 /* Reconstruction of tokens [0, S) of the store, in fp32 (before the final
  * fp16 rounding) and in fp16. axis 0 = keys, 1 = values. out is [BH, S, D]. */
-void orc_recon_f32(int axis, const uint8_t* codes, const float* scale,
+void orc_recon_f32(int axis, const uint8_t* codes, const void* scale,
                    const uint16_t* zero, int BH, int S, int D, int G, int bits,
                    int s_cap, float* out);
-void orc_dequant(int axis, const uint8_t* codes, const float* scale,
+void orc_dequant(int axis, const uint8_t* codes, const void* scale,
                  const uint16_t* zero, int BH, int S, int D, int G, int bits,
                  int s_cap, uint16_t* out);
 
@@ -82,8 +89,8 @@ void orc_residual_compact(uint16_t* res, int BH, int res_cap, int D, int n_res,
 /* Single-token decode over S_q store tokens followed by n_res residual
  * tokens, in float64. q [B, Hq, D] fp16; out [B, Hq, D] float64. */
 void orc_decode_attend(const uint16_t* q,
-                       const uint8_t* kcodes, const float* kscale, const uint16_t* kzero,
-                       const uint8_t* vcodes, const float* vscale, const uint16_t* vzero,
+                       const uint8_t* kcodes, const void* kscale, const uint16_t* kzero,
+                       const uint8_t* vcodes, const void* vscale, const uint16_t* vzero,
                        int S_q, int s_cap,
                        const uint16_t* k_res, const uint16_t* v_res, int n_res, int res_cap,
                        int B, int Hq, int Hkv, int D, int G, int bits, double sm_scale,

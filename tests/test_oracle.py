@@ -80,6 +80,81 @@ def test_golden_group(line):
     assert r.tolist() == _floats(recon), name
 
 
+@pytest.mark.parametrize("line", read_golden("quant_groups_scale_f16.txt"))
+def test_golden_group_scale_f16(line):
+    """The fp16-scale storage option on hand-worked groups: the rounding of
+    the scale to fp16 changes codes (one_fifteenth, one_third), can zero the
+    scale (underflow) and can engage the clip (clamp)."""
+    name, bits, x, codes, scale, zero, recon = [p.strip() for p in line.split(";")]
+    bits = int(bits)
+    x = np.array(_floats(x), np.float32)
+    c, s, z = oracle.quantize_group(x, bits | oracle.SCALE_F16)
+    assert c.tolist() == [int(v) for v in codes.split()], name
+    assert s == np.float32(float(scale)) and z == np.float32(float(zero)), name
+    # through the key store: the stored scale is the fp16 value, and the
+    # reconstruction uses it
+    G = x.size
+    store = oracle.Store(0, 1, G, 4 if bits == 2 else 2, G, bits, scale_f16=True)
+    xs = np.repeat(x.astype(np.float16)[None, :, None], store.D, axis=2)
+    oracle.flush(0, xs, G, store)
+    assert store.scale.dtype == np.float16
+    assert float(store.scale[0, 0, 0]) == float(scale), name
+    assert oracle.recon_f32(store, G)[0, :, 0].tolist() == _floats(recon), name
+    # and through the value store (one group per token row)
+    vstore = oracle.Store(1, 1, G, G, G, bits, scale_f16=True)
+    oracle.flush(1, x.astype(np.float16)[None, None, :], 1, vstore)
+    assert float(vstore.scale[0, 0, 0]) == float(scale), name
+    assert oracle.recon_f32(vstore, 1)[0, 0].tolist() == _floats(recon), name
+
+
+def test_scale_f16_store_matches_rounded_fp32_scale():
+    """On random data the fp16-scale store holds exactly the fp16 rounding of
+    the fp32-scale store's scales (numpy's binary16 conversion), every code is
+    within [0, 2^bits - 1], and codes differ from the fp32-scale codes only
+    where the rounded scale moved a quotient across a rounding boundary."""
+    rng = np.random.default_rng(71)
+    for axis in (0, 1):
+        for bits in (2, 4):
+            x = synth.normal(rng, (3, 96, 64)) * np.float16(3)
+            a = oracle.flush(axis, x, 96, oracle.Store(axis, 3, 96, 64, 32, bits))
+            b = oracle.flush(axis, x, 96, oracle.Store(axis, 3, 96, 64, 32, bits, scale_f16=True))
+            assert np.array_equal(b.scale.view(np.uint16), a.scale.astype(np.float16).view(np.uint16))
+            assert np.array_equal(b.zero.view(np.uint16), a.zero.view(np.uint16))
+            ca = np.stack([oracle.unpack_codes(r, 64, bits) for r in a.codes.reshape(-1, 64 * bits // 8)])
+            cb = np.stack([oracle.unpack_codes(r, 64, bits) for r in b.codes.reshape(-1, 64 * bits // 8)])
+            assert cb.max() <= 2 ** bits - 1
+            assert 0 < np.count_nonzero(ca != cb) < ca.size // 20  # some, never many, codes move
+            assert np.max(np.abs(ca.astype(int) - cb.astype(int))) == 1
+            # the reconstruction error stays within half a stored step (plus rounding)
+            r = oracle.recon_f32(b, 96)
+            s = b.scale.astype(np.float32)
+            step = np.repeat(s, 32, axis=1) if axis == 0 else np.repeat(s, 32, axis=2)
+            assert np.all(np.abs(r - x.astype(np.float32)) <= step * 0.5 * (1 + 2 ** -9) + 1e-6)
+
+
+def test_scale_f16_decode_matches_brute_force():
+    """Attention over fp16-scale stores of 2 KV heads equals float64 softmax
+    attention written out here over the stores' fp32 reconstructions (each
+    head's scales must be read at its own offset)."""
+    rng = np.random.default_rng(72)
+    B, Hkv, Hq, D, S_q, n_res = 1, 2, 4, 64, 64, 5
+    k = synth.normal(rng, (B * Hkv, S_q + n_res, D))
+    v = synth.normal(rng, (B * Hkv, S_q + n_res, D))
+    q = synth.normal(rng, (B, Hq, D))
+    rk = oracle.flush(0, k, S_q, oracle.Store(0, B * Hkv, S_q, D, 32, 4, scale_f16=True))
+    rv = oracle.flush(1, v, S_q, oracle.Store(1, B * Hkv, S_q, D, 32, 4, scale_f16=True))
+    kr, vr = np.ascontiguousarray(k[:, S_q:]), np.ascontiguousarray(v[:, S_q:])
+    out = oracle.decode_attend(q, rk, rv, S_q, kr, vr, n_res, Hkv, 0.125)
+    K = np.concatenate([oracle.recon_f32(rk, S_q), kr.astype(np.float32)], axis=1).astype(np.float64)
+    V = np.concatenate([oracle.recon_f32(rv, S_q), vr.astype(np.float32)], axis=1).astype(np.float64)
+    for h in range(Hq):
+        hk = h // (Hq // Hkv)
+        sc = 0.125 * (K[hk] @ q[0, h].astype(np.float64))
+        p = np.exp(sc - sc.max())
+        ref = (p / p.sum()) @ V[hk]
+        assert np.max(np.abs(out[0, h] - ref)) < 1e-12
+
+
 def _parse_table(name):
     rows = {}
     for ln in read_golden(name):

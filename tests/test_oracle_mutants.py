@@ -41,6 +41,11 @@ MUTANTS = {
     "values_read_as_keys": ("V[(long)t * D + d] = (double)vf[(long)t * D + d];",
                             "V[(long)t * D + d] = (double)kf[(long)t * D + d];"),
     "missing_normalisation": ("oh[d] = T > 0 ? acc / denom : 0.0;", "oh[d] = acc;"),
+    "f16_scale_codes_use_fp32_scale": ("        s = orc_half_to_float(orc_float_to_half(s)); /* the stored binary16 scale */",
+                                       "        ;"),
+    "f16_scale_read_as_fp32": ("        return orc_half_to_float(((const uint16_t*)scale)[m]);",
+                               "        return ((const float*)scale)[m];"),
+    "f16_scale_head_stride_of_fp32": ("long esz = (bits & ORC_SCALE_F16) ? 2 : 4;", "long esz = 4;"),
     "gqa_modulo_mapping": ("const uint16_t* qh = q + ((long)b * Hq + h) * D;",
                            "const uint16_t* qh = q + ((long)b * Hq + (h % group) * Hkv + hk) * D;"),
 }
