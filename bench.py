@@ -80,16 +80,17 @@ def parse_args():
 # workload accounting
 # ---------------------------------------------------------------------------
 
-def op_bytes(w, n_flush: int, n_res: int) -> dict:
-    """Algorithmic HBM bytes per step, per op (each tensor read or written once)."""
+def op_bytes(w, n_flush: int, n_res: int, meta_bytes: int = 6) -> dict:
+    """Algorithmic HBM bytes per step, per op (each tensor read or written once).
+    meta_bytes: scale + zero per group (6 with fp32 scales, 4 with fp16)."""
     el = w.BH * n_flush * w.D                     # flushed elements per tensor
-    packed = w.bits / 8 + 6 / w.G                 # code bits + 4 B scale + 2 B zero per group
+    packed = w.bits / 8 + meta_bytes / w.G        # code bits + scale + zero per group
     flush = 2 * el * (2 + packed)                 # K and V: read fp16, write codes + metadata
     dequant = 2 * el * (packed + 2)               # read codes + metadata, write fp16
     append = 2 * 2 * w.BH * n_res * w.D * 2       # K and V tail rows: read + write
     # decode: per (kv head, store token) K+V codes + key metadata (6 B per channel
     # per 32 tokens) + value metadata (6 B per 32-channel group)
-    per_tok = 2 * w.D * w.bits / 8 + w.D * 6 / w.G + (w.D // w.G) * 6
+    per_tok = 2 * w.D * w.bits / 8 + w.D * meta_bytes / w.G + (w.D // w.G) * meta_bytes
     decode = (w.BH * n_flush * per_tok + w.BH * n_res * w.D * 2 * 2
               + w.B * w.Hq * w.D * 2 + w.B * w.Hq * w.D * 4)
     return {"flush_kv": flush, "residual_append": append, "dequant_kv": dequant, "decode_attend": decode}
@@ -617,33 +618,38 @@ def run_sweep(args):
 
     # flush / dequant at the long-context 2-bit and qwen8b sizes; head dims 64
     # and 256 at the long 2-bit size with the same element count (16 or 4 KV heads)
-    shapes = (("qwen8b", 32, 128), ("long2bit", 32, 128), ("long2bit", 64, 128), ("long2bit", 128, 128),
-              ("long2bit", 32, 64), ("long2bit", 64, 64), ("long2bit", 32, 256), ("long2bit", 128, 256))
-    for name, G, D in (shapes if args.sweep in ("all", "flush") else ()):
+    # (workload, G, D, fp16 scales)
+    shapes = (("qwen8b", 32, 128, False), ("long2bit", 32, 128, False), ("long2bit", 64, 128, False),
+              ("long2bit", 128, 128, False), ("long2bit", 32, 64, False), ("long2bit", 64, 64, False),
+              ("long2bit", 32, 256, False), ("long2bit", 128, 256, False), ("long2bit", 32, 128, True))
+    for name, G, D, hs in (shapes if args.sweep in ("all", "flush") else ()):
         w = dataclasses.replace(synth.WORKLOADS[name], G=G, D=D, Hkv=synth.WORKLOADS[name].Hkv * 128 // D,
                                 Hq=synth.WORKLOADS[name].Hq * 128 // D)
         n = kv.kivi_flush_count(w.S, w.R, w.G)
-        per = w.BH * w.S * w.D * 2 * 2 + 2 * w.BH * n * (w.D * w.bits // 8 + w.D * 6 // w.G) + w.BH * n * w.D * 4
+        meta = 4 if hs else 6  # bytes of scale + zero per group
+        per = w.BH * w.S * w.D * 2 * 2 + 2 * w.BH * n * (w.D * w.bits // 8 + w.D * meta // w.G) + w.BH * n * w.D * 4
         P = pool_count(per)
         ks, vs, kd, vd, xs = [], [], [], [], []
         for i in range(P):
             k, v, _ = synth.prefill_inputs_torch(w, 7000 + i, dev)
             xs.append((k, v))
-            ks.append(kv.KiviStore(0, w.BH, n, w.D, w.G, w.bits, device=dev))
-            vs.append(kv.KiviStore(1, w.BH, n, w.D, w.G, w.bits, device=dev))
+            ks.append(kv.KiviStore(0, w.BH, n, w.D, w.G, w.bits, device=dev, scale_f16=hs))
+            vs.append(kv.KiviStore(1, w.BH, n, w.D, w.G, w.bits, device=dev, scale_f16=hs))
             kd.append(torch.empty((w.BH, n, w.D), dtype=torch.float16, device=dev))
             vd.append(torch.empty_like(kd[-1]))
-        ob = op_bytes(w, n, w.S - n)
+        ob = op_bytes(w, n, w.S - n, meta_bytes=4 if hs else 6)
         timed([lambda i=i: kv.kivi_flush_kv(xs[i][0], xs[i][1], w.R, ks[i], vs[i]) for i in range(P)],
-              ob["flush_kv"], "flush_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "D": D, "pool": P})
+              ob["flush_kv"], "flush_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "D": D, "scale_f16": hs,
+                                                   "pool": P})
         timed([lambda i=i: kv.kivi_dequant_kv(ks[i], vs[i], n, kout=kd[i], vout=vd[i]) for i in range(P)],
-              ob["dequant_kv"], "dequant_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "D": D, "pool": P})
+              ob["dequant_kv"], "dequant_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "D": D, "scale_f16": hs,
+                                                     "pool": P})
         # fake quantization of the same tokens: read 2 B and write 2 B per element of K and V (the kd/vd
         # buffers hold the n flushed tokens, so the S - n fp16 tokens are not part of this launch)
         timed([lambda i=i: kv.kivi_fake_quant_kv(xs[i][0][:, :n], xs[i][1][:, :n], 0, kout=kd[i], vout=vd[i],
-                                                 G=G, bits=w.bits) for i in range(P)],
+                                                 G=G, bits=w.bits, scale_f16=hs) for i in range(P)],
               2 * w.BH * n * w.D * 4, "fake_quant_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G,
-                                                        "D": D, "pool": P})
+                                                        "D": D, "scale_f16": hs, "pool": P})
         del ks, vs, kd, vd, xs
         torch.cuda.empty_cache()
     if args.sweep == "flush":
@@ -665,22 +671,27 @@ def run_sweep(args):
     # head dims 64 and 256
     cases += [(1, 16384 - 128, 128, 4, 32, 32, 64), (32, 4032, 64, 4, 32, 32, 64),
               (1, 16384 - 128, 128, 4, 32, 32, 256), (32, 4032, 64, 4, 32, 32, 256)]
+    # fp16 scale storage (160 bytes per 4-bit token instead of 176)
+    cases += [(1, 2080, 158, 4, 32, 32, 128, True), (1, 16384 - 128, 128, 4, 32, 32, 128, True),
+              (32, 4032, 64, 4, 32, 32, 128, True)]
     for case in cases:
         B, S_q, n_res, bits = case[:4]
         Hq = case[4] if len(case) > 4 else 32
         G = case[5] if len(case) > 5 else 32
         D = case[6] if len(case) > 6 else 128
+        hs = case[7] if len(case) > 7 else False
         w = synth.Workload("decode", B=B, Hkv=8, Hq=Hq, D=D, S=S_q + n_res, bits=bits, G=G, R=0,
                            n_outlier=4, outlier_scale=8.0, seed=11)
         s_cap = max(1, -(-S_q // G)) * G
-        per_tok = 2 * w.D * bits / 8 + w.D * 6 / w.G + (w.D // w.G) * 6
+        meta = 4 if hs else 6  # bytes of scale + zero per group
+        per_tok = 2 * w.D * bits / 8 + w.D * meta / w.G + (w.D // w.G) * meta
         nbytes = w.BH * S_q * per_tok + w.BH * n_res * w.D * 4 + B * w.Hq * w.D * 6
         P = pool_count(nbytes)
         entries = []
         for i in range(P):
             k, v, q = synth.prefill_inputs_torch(w, 9000 + i, dev)
-            gk = kv.KiviStore(0, w.BH, s_cap, w.D, w.G, bits, device=dev)
-            gv = kv.KiviStore(1, w.BH, s_cap, w.D, w.G, bits, device=dev)
+            gk = kv.KiviStore(0, w.BH, s_cap, w.D, w.G, bits, device=dev, scale_f16=hs)
+            gv = kv.KiviStore(1, w.BH, s_cap, w.D, w.G, bits, device=dev, scale_f16=hs)
             if S_q > 0:
                 kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
             kr = k[:, S_q:].contiguous()
@@ -694,7 +705,7 @@ def run_sweep(args):
         fns = [lambda e=e: kv.kivi_decode_attend(e[0], e[1], e[2], S_q, e[3], e[4], n_res, w.Hkv, w.sm_scale,
                                                  out=e[5], workspace=e[6]) for e in entries]
         timed(fns, nbytes, "decode_attend", {"B": B, "Hkv": 8, "Hq": Hq, "S_kv": S_q + n_res, "bits": bits,
-                                             "G": G, "D": D, "pool": P, "tokens_per_s": None})
+                                             "G": G, "D": D, "scale_f16": hs, "pool": P, "tokens_per_s": None})
         del entries, fns
         torch.cuda.empty_cache()
 

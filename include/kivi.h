@@ -48,11 +48,27 @@
  * with s_cap (the store's token capacity) a multiple of G. zero is the group
  * minimum (an fp16 input, so fp16 storage is lossless); scale is the fp32
  * value the codes were computed with.
+ *
+ * fp16 scale storage (KIVI_SCALE_F16): every `bits` argument may be ORed
+ * with KIVI_SCALE_F16. The scale arrays then hold fp16 values (same shapes,
+ * 2 bytes per element; pass them through the float* parameters by a pointer
+ * cast). The flush rounds each fp32 scale (max - min) / (2^bits - 1) to the
+ * nearest fp16 and computes the codes with that stored scale, so dequant and
+ * decode reproduce exactly what the flush used: 4 instead of 6 bytes of
+ * metadata per group. Consequences of the rounding: a group whose range is
+ * below about 2^-25 * (2^bits - 1) stores scale 0 (every code 0, recon = min);
+ * a subnormal fp16 scale can clip the largest codes at 2^bits - 1; and a
+ * scale rounded up can reconstruct the group maximum past 65504 (fp16 inf in
+ * a dequant) for inputs within one step of the fp16 range. A store is read
+ * with the same option it was flushed with.
  */
 #ifndef KIVI_GB300_H
 #define KIVI_GB300_H
 
 #include <stddef.h>
+
+/* Option bit of every `bits` argument: scales stored as fp16 (see above). */
+#define KIVI_SCALE_F16 0x100
 
 #ifdef __cplusplus
 extern "C" {

@@ -126,22 +126,31 @@ def kivi_flush_count(n_res: int, residual_length: int, group_size: int = 32) -> 
     return lib().kivi_flush_count(n_res, residual_length, group_size)
 
 
+KIVI_SCALE_F16 = 0x100  # option bit of every `bits` argument: scales stored as fp16
+
+
 class KiviStore:
     """Device buffers of one packed store (keys or values), allocated by torch.
 
-    codes uint8 [BH, s_cap, D*bits/8]; keys: scale f32 / zero f16
-    [BH, s_cap/G, D]; values: scale f32 / zero f16 [BH, s_cap, D/G].
+    codes uint8 [BH, s_cap, D*bits/8]; keys: scale f32 (f16 with scale_f16) /
+    zero f16 [BH, s_cap/G, D]; values: the same dtypes, [BH, s_cap, D/G].
     """
 
     def __init__(self, axis: int, BH: int, s_cap: int, D: int = 128, group_size: int = 32,
-                 bits: int = 4, device="cuda"):
+                 bits: int = 4, device="cuda", scale_f16: bool = False):
         import torch
         assert s_cap % group_size == 0
         self.axis, self.BH, self.s_cap, self.D, self.G, self.bits = axis, BH, s_cap, D, group_size, bits
+        self.scale_f16 = scale_f16
         self.codes = torch.zeros((BH, s_cap, D * bits // 8), dtype=torch.uint8, device=device)
         meta = (BH, s_cap // group_size, D) if axis == KIVI_AXIS_KEYS else (BH, s_cap, D // group_size)
-        self.scale = torch.zeros(meta, dtype=torch.float32, device=device)
+        self.scale = torch.zeros(meta, dtype=torch.float16 if scale_f16 else torch.float32, device=device)
         self.zero = torch.zeros(meta, dtype=torch.float16, device=device)
+
+    @property
+    def abi_bits(self) -> int:
+        """The `bits` argument of the C ABI: the width plus the scale option."""
+        return self.bits | (KIVI_SCALE_F16 if self.scale_f16 else 0)
 
     def nbytes_per_token(self) -> float:
         return (self.codes[0, 0].numel() + (self.scale.numel() * 4 + self.zero.numel() * 2)
@@ -155,7 +164,7 @@ class KiviStore:
 def _flush(name: str, x, residual_length: int, store: KiviStore, s_off: int, n_tokens, stream):
     S = x.shape[1] if n_tokens is None else n_tokens
     n = ctypes.c_int(0)
-    st = getattr(lib(), name)(_ptr(x), x.shape[0], S, _rows(x, store.D), store.D, store.G, store.bits,
+    st = getattr(lib(), name)(_ptr(x), x.shape[0], S, _rows(x, store.D), store.D, store.G, store.abi_bits,
                               residual_length, _ptr(store.codes), _ptr(store.scale), _ptr(store.zero),
                               s_off, store.s_cap, ctypes.byref(n), _stream(stream))
     _check(name, st)
@@ -181,7 +190,8 @@ def kivi_flush_kv(k, v, residual_length: int, kstore: KiviStore, vstore: KiviSto
     stride = _rows(k, kstore.D)
     assert _rows(v, vstore.D) == stride and v.shape[0] == k.shape[0]
     n = ctypes.c_int(0)
-    st = lib().kivi_flush_kv(_ptr(k), _ptr(v), k.shape[0], S, stride, kstore.D, kstore.G, kstore.bits,
+    assert kstore.scale_f16 == vstore.scale_f16
+    st = lib().kivi_flush_kv(_ptr(k), _ptr(v), k.shape[0], S, stride, kstore.D, kstore.G, kstore.abi_bits,
                              residual_length, _ptr(kstore.codes), _ptr(kstore.scale), _ptr(kstore.zero),
                              _ptr(vstore.codes), _ptr(vstore.scale), _ptr(vstore.zero), s_off,
                              kstore.s_cap, ctypes.byref(n), _stream(stream))
@@ -195,13 +205,14 @@ def kivi_dequant(store: KiviStore, S: int, out=None, stream=None):
     if out is None:
         out = torch.empty((store.BH, S, store.D), dtype=torch.float16, device=store.codes.device)
     st = lib().kivi_dequant(store.axis, _ptr(store.codes), _ptr(store.scale), _ptr(store.zero), store.BH,
-                            S, store.D, store.G, store.bits, store.s_cap, _ptr(out), _stream(stream))
+                            S, store.D, store.G, store.abi_bits, store.s_cap, _ptr(out), _stream(stream))
     _check("kivi_dequant", st)
     return out
 
 
 def kivi_dequant_kv(kstore: KiviStore, vstore: KiviStore, S: int, kout=None, vout=None, stream=None):
     """Key and value fp16 reconstructions of tokens [0, S) in one launch."""
+    assert kstore.scale_f16 == vstore.scale_f16, "one scale storage for both stores"
     import torch
     if kout is None:
         kout = torch.empty((kstore.BH, S, kstore.D), dtype=torch.float16, device=kstore.codes.device)
@@ -209,7 +220,7 @@ def kivi_dequant_kv(kstore: KiviStore, vstore: KiviStore, S: int, kout=None, vou
         vout = torch.empty((vstore.BH, S, vstore.D), dtype=torch.float16, device=vstore.codes.device)
     st = lib().kivi_dequant_kv(_ptr(kstore.codes), _ptr(kstore.scale), _ptr(kstore.zero), _ptr(vstore.codes),
                                _ptr(vstore.scale), _ptr(vstore.zero), kstore.BH, S, kstore.D, kstore.G,
-                               kstore.bits, kstore.s_cap, _ptr(kout), _ptr(vout), _stream(stream))
+                               kstore.abi_bits, kstore.s_cap, _ptr(kout), _ptr(vout), _stream(stream))
     _check("kivi_dequant_kv", st)
     return kout, vout
 
@@ -261,18 +272,22 @@ def _fake_quant(fn: str, x, residual_length: int, out, G: int, bits: int, stream
     return out, n.value
 
 
-def kivi_fake_quant_keys(x, residual_length: int, out=None, G: int = 32, bits: int = 4, stream=None):
+def kivi_fake_quant_keys(x, residual_length: int, out=None, G: int = 32, bits: int = 4, stream=None,
+                         scale_f16: bool = False):
     """Fake-quantized keys x [BH, S, D] fp16 -> (out, n_quantized); out may be x (in place)."""
-    return _fake_quant("kivi_fake_quant_keys", x, residual_length, out, G, bits, stream)
+    return _fake_quant("kivi_fake_quant_keys", x, residual_length, out, G,
+                       bits | (KIVI_SCALE_F16 if scale_f16 else 0), stream)
 
 
-def kivi_fake_quant_values(x, residual_length: int, out=None, G: int = 32, bits: int = 4, stream=None):
+def kivi_fake_quant_values(x, residual_length: int, out=None, G: int = 32, bits: int = 4, stream=None,
+                           scale_f16: bool = False):
     """Fake-quantized values x [BH, S, D] fp16 -> (out, n_quantized); out may be x (in place)."""
-    return _fake_quant("kivi_fake_quant_values", x, residual_length, out, G, bits, stream)
+    return _fake_quant("kivi_fake_quant_values", x, residual_length, out, G,
+                       bits | (KIVI_SCALE_F16 if scale_f16 else 0), stream)
 
 
 def kivi_fake_quant_kv(k, v, residual_length: int, kout=None, vout=None, G: int = 32, bits: int = 4,
-                       stream=None):
+                       stream=None, scale_f16: bool = False):
     """Fake quantization of keys and values of equal geometry -> (kout, vout, n_quantized)."""
     import torch
     BH, S, D = k.shape
@@ -283,6 +298,7 @@ def kivi_fake_quant_kv(k, v, residual_length: int, kout=None, vout=None, G: int 
     stride = _rows(k, D)
     assert _rows(v, D) == stride and _rows(kout, D) == _rows(vout, D)
     n = ctypes.c_int(-1)
+    bits = bits | (KIVI_SCALE_F16 if scale_f16 else 0)
     st = lib().kivi_fake_quant_kv(_ptr(k), _ptr(v), BH, S, stride, D, G, bits, residual_length, _ptr(kout), _ptr(vout),
                                   _rows(kout, D), ctypes.byref(n), _stream(stream))
     _check("kivi_fake_quant_kv", st)
@@ -311,6 +327,7 @@ def kivi_decode_attend(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res,
                        Hkv: int, sm_scale: float, out=None, workspace=None, stream=None):
     """Single-token decode: q [B, Hq, D] fp16 -> out [B, Hq, D] fp32."""
     import torch
+    assert kstore.scale_f16 == vstore.scale_f16, "one scale storage for both stores"
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
@@ -325,7 +342,7 @@ def kivi_decode_attend(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res,
     st = lib().kivi_decode_attend(
         _ptr(q), _ptr(kstore.codes), _ptr(kstore.scale), _ptr(kstore.zero),
         _ptr(vstore.codes), _ptr(vstore.scale), _ptr(vstore.zero), S_q, kstore.s_cap,
-        _ptr(k_res), _ptr(v_res), n_res, res_cap, B, Hq, Hkv, D, kstore.G, kstore.bits,
+        _ptr(k_res), _ptr(v_res), n_res, res_cap, B, Hq, Hkv, D, kstore.G, kstore.abi_bits,
         float(sm_scale), _ptr(out), _ptr(workspace), wbytes, _stream(stream))
     _check("kivi_decode_attend", st)
     return out
@@ -341,6 +358,7 @@ def kivi_decode_attend_noalloc(q, kstore: KiviStore, vstore: KiviStore, S_q: int
     not allocate device memory when they decode). Calls that overlap on the GPU
     race on that array; make the first call on a device before any stream
     capture."""
+    assert kstore.scale_f16 == vstore.scale_f16, "one scale storage for both stores"
     global _noalloc_fn
     import torch
     if _noalloc_fn is None:
@@ -359,7 +377,7 @@ def kivi_decode_attend_noalloc(q, kstore: KiviStore, vstore: KiviStore, S_q: int
     st = _noalloc_fn(
         _ptr(q), _ptr(kstore.codes), _ptr(kstore.scale), _ptr(kstore.zero),
         _ptr(vstore.codes), _ptr(vstore.scale), _ptr(vstore.zero), S_q, kstore.s_cap,
-        _ptr(k_res), _ptr(v_res), n_res, res_cap, B, Hq, Hkv, D, kstore.G, kstore.bits,
+        _ptr(k_res), _ptr(v_res), n_res, res_cap, B, Hq, Hkv, D, kstore.G, kstore.abi_bits,
         float(sm_scale), _ptr(out), _stream(stream))
     _check("kivi_decode_attend_noalloc", st)
     return out

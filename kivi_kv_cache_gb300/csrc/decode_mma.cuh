@@ -2,8 +2,10 @@
 // tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation), one warp
 // per tile, for groups of up to 4 query heads per KV head; larger groups run
 // in sub-groups of up to 4 heads (one CTA group each, reading the same tiles).
-// Templated on the head dim D (64, 128, 256); decode_mma.cu, decode_mma_d64.cu
-// and decode_mma_d256.cu each instantiate one D, so they compile in parallel.
+// Templated on the head dim D (64, 128, 256) and on the scale storage (fp32
+// or fp16); decode_mma.cu, decode_mma_f16s.cu, decode_mma_d64.cu,
+// decode_mma_d256.cu and decode_mma_d256_f16s.cu split the instantiations so
+// that they compile in parallel.
 //
 // Method: VeloxQuant-MLX blog, "A 5.65x Metal Kernel That Made My LLM Exactly
 // 0% Faster", "So why does the kernel ship?" (attention reads the packed
@@ -144,7 +146,7 @@ __device__ __forceinline__ int swz(int row, int col) {
 // tile staging
 // ---------------------------------------------------------------------------
 
-template <int BITS, int D>
+template <int BITS, int D, bool HS>
 __device__ __forceinline__ void fetch_store_tile(const DecodeArgs& a, int bh, int tile, uint8_t* st, int lane) {
     using GE = Geo<D>;
     constexpr int ROWB = D * BITS / 8;       // bytes per code row
@@ -160,33 +162,56 @@ __device__ __forceinline__ void fetch_store_tile(const DecodeArgs& a, int bh, in
     }
     // the key group (32 << g_shift tokens) holding this tile, and the value
     // metadata of its 32 tokens: (D / 32) >> g_shift entries per token, packed
-    // at the front of VS and VZ (widen_value_meta spreads them for G > 32)
+    // at the front of VS and VZ. fp16 scales (scale_f16) land raw at the front
+    // of KS and VS (HS). expand_meta turns both forms into the layout the tile
+    // code reads.
     const int sh = a.g_shift;
     const long long krow = (long long)bh * (a.s_cap >> (5 + sh)) + (tile >> sh);
+    const long long vrow = ((long long)bh * a.s_cap + tok0) * ((D / 32) >> sh);
+    const int nvz = (D / 8) >> sh;  // 16-byte chunks of the 32 tokens' zeros (and fp16 scales)
+    if (HS) {
+        const __half* ks = reinterpret_cast<const __half*>(a.kscale) + krow * D;
+        const __half* vs = reinterpret_cast<const __half*>(a.vscale) + vrow;
+        if (lane < D / 8) cp_async16(st + GE::kKS + lane * 16, ks + lane * 8, true);
+        if (lane < nvz) cp_async16(st + GE::kVS + lane * 16, vs + lane * 8, true);
+    }
     const float* ks = a.kscale + krow * D;
     const __half* kz = a.kzero + krow * D;
+    if (!HS) {
 #pragma unroll
-    for (int i = lane; i < D / 4; i += 32) cp_async16(st + GE::kKS + padc(i * 4) * 4, ks + i * 4, true);
+        for (int i = lane; i < D / 4; i += 32) cp_async16(st + GE::kKS + padc(i * 4) * 4, ks + i * 4, true);
+    }
     if (lane < D / 8) cp_async16(st + GE::kKZ + lane * 16, kz + lane * 8, true);
-    const long long vrow = ((long long)bh * a.s_cap + tok0) * ((D / 32) >> sh);
     const float* vs = a.vscale + vrow;
     const __half* vz = a.vzero + vrow;
-    const int nvs = (D / 4) >> sh, nvz = (D / 8) >> sh;  // 16-byte chunks of the 32 tokens' entries
+    const int nvs = (D / 4) >> sh;  // 16-byte chunks of the 32 tokens' fp32 scales
+    if (!HS) {
 #pragma unroll
-    for (int i = lane; i < D / 4; i += 32)
-        if (i < nvs) cp_async16(st + GE::kVS + i * 16, vs + i * 4, true);
+        for (int i = lane; i < D / 4; i += 32)
+            if (i < nvs) cp_async16(st + GE::kVS + i * 16, vs + i * 4, true);
+    }
     if (lane < nvz) cp_async16(st + GE::kVZ + lane * 16, vz + lane * 8, true);
 }
 
-// A store of group size 64 (g_shift 1) or 128 (g_shift 2) has 2 or 4 times
-// fewer value scales and zeros per token than one per 32 channels, the layout
-// the tile code reads (VS and VZ [32 tokens][D / 32]). Each lane takes its
-// token's entries, then, once the warp has read them all, writes them back
-// with each repeated 2 or 4 times.
+// Metadata that does not arrive in the layout the tile code reads (VS and VZ
+// [32 tokens][D / 32], one entry per 32 channels; KS fp32 in padded channel
+// order):
+//   * a store of group size 64 (g_shift 1) or 128 (g_shift 2) has 2 or 4
+//     times fewer value scales and zeros per token: each is repeated;
+//   * fp16 scales (f16) arrive raw at the front of KS and VS: widened to fp32.
+// Each lane reads its token's value entries and D / 32 key scales, then, once
+// the warp has read them all, writes them back in place.
 template <int D>
-__device__ __forceinline__ void widen_value_meta(uint8_t* st, int sh, int lane) {
+__device__ __forceinline__ void expand_meta(uint8_t* st, int sh, bool f16, int lane) {
     using GE = Geo<D>;
     constexpr int NE = GE::kNE;
+    constexpr int KPL = D / 32;  // key scales per lane
+    float ksv[KPL];
+    if (f16) {
+        const __half* kraw = reinterpret_cast<const __half*>(st + GE::kKS);
+#pragma unroll
+        for (int k = 0; k < KPL; ++k) ksv[k] = __half2float(kraw[lane * KPL + k]);
+    }
     float* vs = reinterpret_cast<float*>(st + GE::kVS);
     unsigned short* vz = reinterpret_cast<unsigned short*>(st + GE::kVZ);
     const int nr = NE >> sh;  // entries per token in the store
@@ -194,10 +219,16 @@ __device__ __forceinline__ void widen_value_meta(uint8_t* st, int sh, int lane) 
     unsigned short z[NE];
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
-        s[e] = vs[lane * nr + (e >> sh)];
-        z[e] = vz[lane * nr + (e >> sh)];
+        const int idx = lane * nr + (e >> sh);
+        s[e] = f16 ? __half2float(reinterpret_cast<const __half*>(vs)[idx]) : vs[idx];
+        z[e] = vz[idx];
     }
     __syncwarp();
+    if (f16) {
+        float* ks = reinterpret_cast<float*>(st + GE::kKS);
+#pragma unroll
+        for (int k = 0; k < KPL; ++k) ks[padc(lane * KPL + k)] = ksv[k];
+    }
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
         vs[lane * NE + e] = s[e];
@@ -258,7 +289,7 @@ __device__ __forceinline__ void cta_heads(const DecodeArgs& a, int& h0, int& nh)
 // D: head dim. A lane's share of a code row is D / 4 contiguous channels; the
 // score operands are built and applied in chunks of at most 128 channels so
 // that D = 256 holds no more of them at a time than D = 128.
-template <int BITS, int GQ, int NW, bool CL, int D>
+template <int BITS, int GQ, int NW, bool CL, int D, bool HS>
 __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_kernel(DecodeArgs a) {
     constexpr int kWarps = NW;
     constexpr int kThreads = 32 * NW;
@@ -287,9 +318,9 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
 
     pdl_wait();
     // start the first two store tiles' copies, then stage q while they fly
-    if (ns > 0) fetch_store_tile<BITS, D>(a, bh, w0, st0, lane);
+    if (ns > 0) fetch_store_tile<BITS, D, HS>(a, bh, w0, st0, lane);
     cp_async_commit();
-    if (ns > 1) fetch_store_tile<BITS, D>(a, bh, w0 + 1, st0 + kStage, lane);
+    if (ns > 1) fetch_store_tile<BITS, D, HS>(a, bh, w0 + 1, st0 + kStage, lane);
     cp_async_commit();
 
     // q * score_scale for the nh heads of this CTA (heads >= nh are zero)
@@ -337,7 +368,7 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
         uint8_t* S = st0 + (it & 1) * kStage;
         cp_async_wait<1>();
         __syncwarp();
-        if (a.g_shift != 0) widen_value_meta<D>(S, a.g_shift, lane);
+        if (HS || a.g_shift != 0) expand_meta<D>(S, a.g_shift, HS, lane);
         const int nvalid = min(32, a.S_q - tile * 32);
         if (nvalid < 32) {  // zero the value metadata of rows past S_q
             float* vsz = reinterpret_cast<float*>(S + GE::kVS);
@@ -673,7 +704,7 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
             }
         }
         __syncwarp();
-        if (it + 2 < ns) fetch_store_tile<BITS, D>(a, bh, tile + 2, S, lane);
+        if (it + 2 < ns) fetch_store_tile<BITS, D, HS>(a, bh, tile + 2, S, lane);
         cp_async_commit();
     }
     cp_async_wait<0>();
@@ -895,14 +926,14 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
         merge_splits<16, D>(a, (long long)b * a.Hq + h0, nh, warp, kWarps, lane, reinterpret_cast<float*>(smem));
 }
 
-template <int BITS, int GQ, int NW, bool CL, int D>
+template <int BITS, int GQ, int NW, bool CL, int D, bool HS>
 cudaError_t configure_mma() {
     static cudaError_t status = cudaErrorNotReady;  // benign race: every caller sets the same values
     if (status == cudaErrorNotReady) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ, NW, CL, D>,
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ, NW, CL, D, HS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<NW, D>::kSmemBytes);
         if (e == cudaSuccess && CL)
-            e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ, NW, CL, D>,
+            e = cudaFuncSetAttribute(decode_mma_kernel<BITS, GQ, NW, CL, D, HS>,
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         status = e;
     }
@@ -912,7 +943,7 @@ cudaError_t configure_mma() {
 // Resident CTAs of this kernel on the device: without clusters (n = 1) or in
 // clusters of n CTAs (0 if such clusters cannot be resident). Computed once
 // per device and n with the occupancy calculator.
-template <int BITS, int GQ, int NW, int D>
+template <int BITS, int GQ, int NW, int D, bool HS>
 int resident_ctas(int n, cudaStream_t stream) {
     constexpr int kDevs = 16;
     static int cache[kDevs][kMaxClusterSplits + 1];  // 0 unknown, -1 none, else CTAs + 1
@@ -925,12 +956,12 @@ int resident_ctas(int n, cudaStream_t stream) {
         int ctas = 0;
         if (n == 1) {
             int per_sm = 0, sms = 0;
-            if (configure_mma<BITS, GQ, NW, false, D>() == cudaSuccess &&
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<BITS, GQ, NW, false, D>,
+            if (configure_mma<BITS, GQ, NW, false, D, HS>() == cudaSuccess &&
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<BITS, GQ, NW, false, D, HS>,
                                                               32 * NW, Layout<NW, D>::kSmemBytes) == cudaSuccess &&
                 cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
                 ctas = per_sm * sms;
-        } else if (configure_mma<BITS, GQ, NW, true, D>() == cudaSuccess) {
+        } else if (configure_mma<BITS, GQ, NW, true, D, HS>() == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(n, 1, 1);
             cfg.blockDim = dim3(32 * NW);
@@ -944,7 +975,7 @@ int resident_ctas(int n, cudaStream_t stream) {
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, decode_mma_kernel<BITS, GQ, NW, true, D>, &cfg) ==
+            if (cudaOccupancyMaxActiveClusters(&clusters, decode_mma_kernel<BITS, GQ, NW, true, D, HS>, &cfg) ==
                 cudaSuccess)
                 ctas = clusters * n;
         }
@@ -958,54 +989,55 @@ int resident_ctas(int n, cudaStream_t stream) {
 // whole grid fits in one wave of clusters (the latency case) or clusters keep
 // at least 95 % of the resident CTAs (otherwise a cluster size that packs the
 // GPU's processor clusters badly costs more than the merge saves).
-template <int BITS, int GQ, int NW, int D>
+template <int BITS, int GQ, int NW, int D, bool HS>
 bool use_cluster(const DecodeArgs& a, cudaStream_t stream) {
     const int n = a.n_split;
     if (n < 2 || n > kMaxClusterSplits) return false;
-    const long long with = resident_ctas<BITS, GQ, NW, D>(n, stream);
+    const long long with = resident_ctas<BITS, GQ, NW, D, HS>(n, stream);
     if (with <= 0) return false;
     const long long ctas = (long long)n * a.Hkv * a.q_sub * a.B;
-    return ctas <= with || 20 * with >= 19LL * resident_ctas<BITS, GQ, NW, D>(1, stream);
+    return ctas <= with || 20 * with >= 19LL * resident_ctas<BITS, GQ, NW, D, HS>(1, stream);
 }
 
-template <int BITS, int GQ, int NW, int D>
+template <int BITS, int GQ, int NW, int D, bool HS>
 cudaError_t launch_mma_typed(const DecodeArgs& a, cudaStream_t stream) {
     const dim3 grid(a.n_split, a.Hkv * a.q_sub, a.B);
     constexpr int kSmem = Layout<NW, D>::kSmemBytes;
-    if (use_cluster<BITS, GQ, NW, D>(a, stream)) {
-        cudaError_t e = configure_mma<BITS, GQ, NW, true, D>();
+    if (use_cluster<BITS, GQ, NW, D, HS>(a, stream)) {
+        cudaError_t e = configure_mma<BITS, GQ, NW, true, D, HS>();
         if (e != cudaSuccess) return e;
-        return launch_pdl_cluster(decode_mma_kernel<BITS, GQ, NW, true, D>, grid, 32 * NW, kSmem, stream,
+        return launch_pdl_cluster(decode_mma_kernel<BITS, GQ, NW, true, D, HS>, grid, 32 * NW, kSmem, stream,
                                   a.n_split, a);
     }
-    cudaError_t e = configure_mma<BITS, GQ, NW, false, D>();
+    cudaError_t e = configure_mma<BITS, GQ, NW, false, D, HS>();
     if (e != cudaSuccess) return e;
-    return launch_pdl(decode_mma_kernel<BITS, GQ, NW, false, D>, grid, 32 * NW, kSmem, stream, a);
+    return launch_pdl(decode_mma_kernel<BITS, GQ, NW, false, D, HS>, grid, 32 * NW, kSmem, stream, a);
 }
 
-template <int BITS, int GQ, int D>
+template <int BITS, int GQ, int D, bool HS>
 cudaError_t launch_mma_warps(const DecodeArgs& a, cudaStream_t stream) {
-    return a.warps_per_cta == 8 ? launch_mma_typed<BITS, GQ, 8, D>(a, stream)
-                                : launch_mma_typed<BITS, GQ, 4, D>(a, stream);
+    return a.warps_per_cta == 8 ? launch_mma_typed<BITS, GQ, 8, D, HS>(a, stream)
+                                : launch_mma_typed<BITS, GQ, 4, D, HS>(a, stream);
 }
 
-// The one-warp-per-tile decode of head dim D: groups of 1, 2 or 4 heads run
-// their own width; other groups run in sub-groups of 4 heads (a.q_sub of them
-// per KV head, the last possibly partial).
-template <int D>
+// The one-warp-per-tile decode of head dim D, with fp32 (HS false) or fp16
+// (HS true) scales: groups of 1, 2 or 4 heads run their own width; other
+// groups run in sub-groups of 4 heads (a.q_sub of them per KV head, the last
+// possibly partial).
+template <int D, bool HS>
 cudaError_t launch_decode_mma_impl(const DecodeArgs& a, int bits, int gq, cudaStream_t stream) {
     cudaError_t e = cudaErrorInvalidValue;
     if (gq < 1 || (gq > 2 && (gq + 3) / 4 != a.q_sub) || (gq <= 2 && a.q_sub != 1)) return e;
     if (bits == 4) {
-        if (gq == 1) e = launch_mma_warps<4, 1, D>(a, stream);
-        else if (gq == 2) e = launch_mma_warps<4, 2, D>(a, stream);
-        else if (gq == 4) e = launch_mma_warps<4, 4, D>(a, stream);
-        else e = launch_mma_warps<4, kSubGroupGQ, D>(a, stream);
+        if (gq == 1) e = launch_mma_warps<4, 1, D, HS>(a, stream);
+        else if (gq == 2) e = launch_mma_warps<4, 2, D, HS>(a, stream);
+        else if (gq == 4) e = launch_mma_warps<4, 4, D, HS>(a, stream);
+        else e = launch_mma_warps<4, kSubGroupGQ, D, HS>(a, stream);
     } else {
-        if (gq == 1) e = launch_mma_warps<2, 1, D>(a, stream);
-        else if (gq == 2) e = launch_mma_warps<2, 2, D>(a, stream);
-        else if (gq == 4) e = launch_mma_warps<2, 4, D>(a, stream);
-        else e = launch_mma_warps<2, kSubGroupGQ, D>(a, stream);
+        if (gq == 1) e = launch_mma_warps<2, 1, D, HS>(a, stream);
+        else if (gq == 2) e = launch_mma_warps<2, 2, D, HS>(a, stream);
+        else if (gq == 4) e = launch_mma_warps<2, 4, D, HS>(a, stream);
+        else e = launch_mma_warps<2, kSubGroupGQ, D, HS>(a, stream);
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -77,7 +77,7 @@ __device__ __forceinline__ uint32_t load_word(const uint8_t* p) {
 // keys: one warp per (head, 32-token block, 64-channel slice); lane =
 // part*8 + oc, part owns 8 tokens of the block. Scale and zero are per (key
 // group of G tokens, channel): the block's group is block * 32 / G.
-template <int BITS, int G, int D>
+template <int BITS, int G, int D, bool HS>
 __device__ __forceinline__ void dequant_keys_warp(const DequantArgs& a, int warp_id, int bh) {
     constexpr int ROWB = D * BITS / 8;
     constexpr int NSL = D / 64;  // 64-channel slices per row
@@ -95,11 +95,23 @@ __device__ __forceinline__ void dequant_keys_warp(const DequantArgs& a, int warp
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = (t0 + i < a.S) ? load_word<BITS>(crow + i * ROWB) : 0u;
     const long long m = ((long long)bh * (a.s_cap / G) + g) * D + octet * 8;
-    const float4 sa = __ldg(reinterpret_cast<const float4*>(a.scale + m));
-    const float4 sb = __ldg(reinterpret_cast<const float4*>(a.scale + m) + 1);
+    float s[8];
+    if (HS) {  // 8 fp16 scales
+        const uint4 hw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(a.scale) + m));
+        const uint32_t hv[4] = {hw.x, hw.y, hw.z, hw.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(u32_as_h2(hv[k]));
+            s[2 * k] = f.x;
+            s[2 * k + 1] = f.y;
+        }
+    } else {
+        const float4 sa = __ldg(reinterpret_cast<const float4*>(a.scale + m));
+        const float4 sb = __ldg(reinterpret_cast<const float4*>(a.scale + m) + 1);
+        s[0] = sa.x, s[1] = sa.y, s[2] = sa.z, s[3] = sa.w, s[4] = sb.x, s[5] = sb.y, s[6] = sb.z, s[7] = sb.w;
+    }
     const uint4 zw = __ldg(reinterpret_cast<const uint4*>(a.zero + m));
     pdl_trigger();
-    const float s[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
     const uint32_t zz[4] = {zw.x, zw.y, zw.z, zw.w};
     f32x2 s2[4], ns2[4], z2[4];
 #pragma unroll
@@ -118,7 +130,7 @@ __device__ __forceinline__ void dequant_keys_warp(const DequantArgs& a, int warp
 // values: one warp per NR * RPT consecutive tokens of one head (NR = 32 / (D /
 // 8) rows per pass); lane = sub * (D / 8) + octet, iteration i handles token
 // NR * i + sub. Scale and zero are per (token, G-channel group).
-template <int BITS, int G, int D>
+template <int BITS, int G, int D, bool HS>
 __device__ __forceinline__ void dequant_values_warp(const DequantArgs& a, int warp_id, int bh) {
     constexpr int ROWB = D * BITS / 8;
     constexpr int RPT = 4;
@@ -137,7 +149,8 @@ __device__ __forceinline__ void dequant_values_warp(const DequantArgs& a, int wa
         const long long row = row0 + NR * i;
         if (tw + NR * i + sub < a.S) {
             w[i] = load_word<BITS>(a.codes + row * ROWB + octet * BITS);
-            s[i] = __ldg(a.scale + row * (D / G) + octet / (G / 8));
+            const long long mi = row * (D / G) + octet / (G / 8);
+            s[i] = HS ? __half2float(reinterpret_cast<const __half*>(a.scale)[mi]) : __ldg(a.scale + mi);
             z[i] = __half2float(a.zero[row * (D / G) + octet / (G / 8)]);
         } else {
             w[i] = 0u;
@@ -165,25 +178,25 @@ int value_blocks_x(int S, int D) {
     return (S + tokens_per_block - 1) / tokens_per_block;
 }
 
-template <int BITS, int G, int D>
+template <int BITS, int G, int D, bool HS>
 __global__ void __launch_bounds__(kThreads) dequant_keys_kernel(DequantArgs a) {
     pdl_wait();
-    dequant_keys_warp<BITS, G, D>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+    dequant_keys_warp<BITS, G, D, HS>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
 
-template <int BITS, int G, int D>
+template <int BITS, int G, int D, bool HS>
 __global__ void __launch_bounds__(kThreads) dequant_values_kernel(DequantArgs a) {
     pdl_wait();
-    dequant_values_warp<BITS, G, D>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+    dequant_values_warp<BITS, G, D, HS>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
 
-template <int BITS, int G, int D>
+template <int BITS, int G, int D, bool HS>
 __global__ void __launch_bounds__(kThreads) dequant_kv_kernel(DequantArgs k, DequantArgs v, int kbx) {
     pdl_wait();
     if ((int)blockIdx.x < kbx)
-        dequant_keys_warp<BITS, G, D>(k, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
+        dequant_keys_warp<BITS, G, D, HS>(k, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y);
     else
-        dequant_values_warp<BITS, G, D>(v, (blockIdx.x - kbx) * 4 + (threadIdx.x >> 5), blockIdx.y);
+        dequant_values_warp<BITS, G, D, HS>(v, (blockIdx.x - kbx) * 4 + (threadIdx.x >> 5), blockIdx.y);
 }
 
 
@@ -192,34 +205,35 @@ DequantArgs head_slice(const DequantArgs& a, int h0, int nh, int bits, int axis)
     s.BH = nh;
     s.codes += (long long)h0 * a.s_cap * (a.D * bits / 8);
     const long long meta = axis == 0 ? (long long)(a.s_cap / a.G) * a.D : (long long)a.s_cap * (a.D / a.G);
-    s.scale += h0 * meta;
+    s.scale = a.scale_f16 ? reinterpret_cast<const float*>(reinterpret_cast<const __half*>(a.scale) + h0 * meta)
+                          : a.scale + h0 * meta;
     s.zero += h0 * meta;
     s.out += (long long)h0 * a.S * a.D;
     return s;
 }
 
-template <int BITS, int G, int D>
+template <int BITS, int G, int D, bool HS>
 cudaError_t launch_dequant_typed(int axis, const DequantArgs& a, cudaStream_t stream) {
     const int bx = axis == 0 ? key_blocks_x(a.S, D) : value_blocks_x(a.S, D);
     for (int h0 = 0; h0 < a.BH; h0 += 65535) {
         const int nh = a.BH - h0 < 65535 ? a.BH - h0 : 65535;
         const DequantArgs s = head_slice(a, h0, nh, BITS, axis);
         const dim3 grid(bx, nh);
-        const cudaError_t e = axis == 0 ? launch_pdl(dequant_keys_kernel<BITS, G, D>, grid, kThreads, 0, stream, s)
-                                        : launch_pdl(dequant_values_kernel<BITS, G, D>, grid, kThreads, 0, stream, s);
+        const cudaError_t e = axis == 0 ? launch_pdl(dequant_keys_kernel<BITS, G, D, HS>, grid, kThreads, 0, stream, s)
+                                        : launch_pdl(dequant_values_kernel<BITS, G, D, HS>, grid, kThreads, 0, stream, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
 
-template <int BITS, int G, int D>
+template <int BITS, int G, int D, bool HS>
 cudaError_t launch_dequant_kv_typed(const DequantArgs& k, const DequantArgs& v, cudaStream_t stream) {
     const int kbx = key_blocks_x(k.S, D), vbx = value_blocks_x(v.S, D);
     for (int h0 = 0; h0 < k.BH; h0 += 65535) {
         const int nh = k.BH - h0 < 65535 ? k.BH - h0 : 65535;
         const DequantArgs ks = head_slice(k, h0, nh, BITS, 0), vs = head_slice(v, h0, nh, BITS, 1);
         const dim3 grid(kbx + vbx, nh);
-        const cudaError_t e = launch_pdl(dequant_kv_kernel<BITS, G, D>, grid, kThreads, 0, stream, ks, vs, kbx);
+        const cudaError_t e = launch_pdl(dequant_kv_kernel<BITS, G, D, HS>, grid, kThreads, 0, stream, ks, vs, kbx);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
@@ -253,14 +267,16 @@ cudaError_t by_shape(int bits, int G, int D, A&&... args) {
 template <int BITS, int G, int D>
 struct DequantOne {
     static cudaError_t run(int axis, const DequantArgs& a, cudaStream_t stream) {
-        return launch_dequant_typed<BITS, G, D>(axis, a, stream);
+        return a.scale_f16 ? launch_dequant_typed<BITS, G, D, true>(axis, a, stream)
+                           : launch_dequant_typed<BITS, G, D, false>(axis, a, stream);
     }
 };
 
 template <int BITS, int G, int D>
 struct DequantKV {
     static cudaError_t run(const DequantArgs& k, const DequantArgs& v, cudaStream_t stream) {
-        return launch_dequant_kv_typed<BITS, G, D>(k, v, stream);
+        return k.scale_f16 ? launch_dequant_kv_typed<BITS, G, D, true>(k, v, stream)
+                           : launch_dequant_kv_typed<BITS, G, D, false>(k, v, stream);
     }
 };
 

@@ -122,12 +122,24 @@ __device__ __forceinline__ void quant8_codes(const uint4 xv, const f32x2 (&z2)[4
     }
 }
 
+// With an fp16 scale (HS) a subnormal stored scale can leave a quotient past
+// 2^BITS - 1 (up to about 1.5 (2^BITS - 1)): clip the codes, whose fp32
+// patterns 2^23 + q order like q.
+template <int BITS, bool HS>
+__device__ __forceinline__ void clip8(uint32_t (&tb)[8]) {
+    if (HS) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tb[i] = min(tb[i], 0x4B000000u + (uint32_t)Levels<BITS>::value);
+    }
+}
+
 // The codes of quant8_codes packed into BITS*8 bits.
-template <int BITS>
+template <int BITS, bool HS>
 __device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
                                            const float (&s)[8]) {
     uint32_t tb[8];
     quant8_codes(xv, z2, r2, s, tb);
+    clip8<BITS, HS>(tb);
     return pack8<BITS>(tb);
 }
 
@@ -136,10 +148,12 @@ __device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4],
 // That Made My LLM Exactly 0% Faster", "What we're actually optimizing";
 // multiply, then a separate add: "Three ways to be off by one bit" #1).
 // With tb = bits of 2^23 + q, fma(2^23 + q, s, -2^23 s) is q * s rounded once.
+template <int BITS, bool HS>
 __device__ __forceinline__ uint4 fake8(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
                                        const float (&s)[8]) {
     uint32_t tb[8];
     quant8_codes(xv, z2, r2, s, tb);
+    clip8<BITS, HS>(tb);
     uint32_t h[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -154,6 +168,29 @@ __device__ __forceinline__ uint4 fake8(const uint4 xv, const f32x2 (&z2)[4], con
 
 // -0 -> +0 (applied to min and max, so zero and scale carry no negative sign)
 __device__ __forceinline__ float canon(float v) { return __fadd_rn(v, 0.0f); }
+
+// Scale stores: fp32, or fp16 (HS; the scale is already an fp16 value, so the
+// conversion is exact) at element index m of the scale array.
+template <bool HS>
+__device__ __forceinline__ void store_scale(float* scale, long long m, float s) {
+    if (HS) reinterpret_cast<__half*>(scale)[m] = __float2half_rn(s);
+    else scale[m] = s;
+}
+template <bool HS>
+__device__ __forceinline__ void store_scales8(float* scale, long long m, const float (&s)[8]) {
+    if (HS) {
+        uint4 h;
+        h.x = h2_as_u32(__floats2half2_rn(s[0], s[1]));
+        h.y = h2_as_u32(__floats2half2_rn(s[2], s[3]));
+        h.z = h2_as_u32(__floats2half2_rn(s[4], s[5]));
+        h.w = h2_as_u32(__floats2half2_rn(s[6], s[7]));
+        *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(scale) + m) = h;
+    } else {
+        float4* sp = reinterpret_cast<float4*>(scale + m);
+        sp[0] = make_float4(s[0], s[1], s[2], s[3]);
+        sp[1] = make_float4(s[4], s[5], s[6], s[7]);
+    }
+}
 
 // ---------------------------------------------------------------------------
 // work items, staged per warp through shared memory
@@ -255,8 +292,9 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
 // keys: lane = part * kNOc + oc; part owns tokens [8 part, 8 part + 8) of the
 // group, oc owns 8 channels of this item's channel slice. FAKE: write the
 // fake-quantized fp16 rows to a.fq instead of codes, scales and zeros.
-template <int BITS, bool FAKE, int G, int D>
+template <int BITS, int MODE, int G, int D>
 __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st, int lane) {
+    constexpr bool FAKE = (MODE & 1) != 0, HS = (MODE & 2) != 0;  // fake quantization; fp16 scales
     using KS = KeyShape<G, D>;
     const unsigned u = item;
     const int qs = u % KS::kQ, g = (u / KS::kQ) % it.ng, bh = (u / KS::kQ) / it.ng;
@@ -316,6 +354,7 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         for (int c = 0; c < CPP; ++c) {
             const bool odd = ((ch0 + c) & 1) != 0;
             my_s[c] = __fdiv_rn(__fsub_rn(canon(odd ? hi.y : hi.x), canon(odd ? lo.y : lo.x)), L);
+            if (HS) my_s[c] = __half2float(__float2half_rn(my_s[c]));  // the stored fp16 scale
             my_r[c] = my_s[c] == 0.0f ? 0.0f : __frcp_rn(my_s[c]);
         }
     }
@@ -335,14 +374,12 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     if (FAKE) {
         uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * D) + octet;
 #pragma unroll 1
-        for (int i = 0; i < nv; ++i) frow[i * (D / 8)] = fake8(xs[i * KS::kNOc], z2, r2, s);
+        for (int i = 0; i < nv; ++i) frow[i * (D / 8)] = fake8<BITS, HS>(xs[i * KS::kNOc], z2, r2, s);
         return;
     }
     if (part == 0) {
         const long long m = ((long long)bh * (a.s_cap / G) + a.s_off / G + g) * D + octet * 8;
-        float4* sp = reinterpret_cast<float4*>(a.scale + m);
-        sp[0] = make_float4(s[0], s[1], s[2], s[3]);
-        sp[1] = make_float4(s[4], s[5], s[6], s[7]);
+        store_scales8<HS>(a.scale, m, s);
         uint4 zp;
         zp.x = h2_as_u32(__floats2half2_rn(z[0], z[1]));
         zp.y = h2_as_u32(__floats2half2_rn(z[2], z[3]));
@@ -357,7 +394,7 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
     };
 #pragma unroll (kKeyUnroll)
-    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS>(xs[i * KS::kNOc], z2, r2, s));
+    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, HS>(xs[i * KS::kNOc], z2, r2, s));
 }
 
 // min and max of the 8 fp16 of each vector of x, as half2 (min and max of fp16
@@ -387,9 +424,10 @@ __device__ __forceinline__ void minmax_tree(const uint4 (&x)[N], __half2& m2, __
 // one, whose min/max it shares with its partner lane (lane ^ kRows, the other
 // half of the same row's group) (G = 128). Min/max, scale and codes of a
 // group stay in its lane(s); one code store per group or half group.
-template <int BITS, bool FAKE, int G, int D>
+template <int BITS, int MODE, int G, int D>
 __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
                                            int lane) {
+    constexpr bool FAKE = (MODE & 1) != 0, HS = (MODE & 2) != 0;  // fake quantization; fp16 scales
     using VS = ValueShape<D>;
     static_assert(G <= D, "a value group lies within one token row");
     const unsigned vi = item - it.key_items;
@@ -416,7 +454,8 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
             if (!valid) return;
         }
         const float z = canon(__half2float(__hmin(__low2half(m2), __high2half(m2))));
-        const float sc = __fdiv_rn(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z), L);
+        float sc = __fdiv_rn(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z), L);
+        if (HS) sc = __half2float(__float2half_rn(sc));  // the stored fp16 scale
         const float rc = sc == 0.0f ? 0.0f : __frcp_rn(sc);
         const f32x2 z1 = pk(z, z), r1 = pk(rc, rc);
         const f32x2 z2[4] = {z1, z1, z1, z1}, r2[4] = {r1, r1, r1, r1};
@@ -425,11 +464,11 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
         if (FAKE) {
             uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * D) + cv;
 #pragma unroll
-            for (int k = 0; k < NVEC; ++k) frow[k] = fake8(x[k], z2, r2, sv);
+            for (int k = 0; k < NVEC; ++k) frow[k] = fake8<BITS, HS>(x[k], z2, r2, sv);
         } else {
             uint32_t pq[NVEC];
 #pragma unroll
-            for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS>(x[k], z2, r2, sv);
+            for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS, HS>(x[k], z2, r2, sv);
             uint8_t* cdst = a.codes + grow * (D * BITS / 8) + cv * BITS;  // 8 channels per vector
             if (BITS == 4) {
 #pragma unroll
@@ -442,7 +481,7 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
                         make_uint2(pq[k] | (pq[k + 1] << 16), pq[k + 2] | (pq[k + 3] << 16));
             }
             if (G != 128 || (jp & 1) == 0) {
-                a.scale[grow * (D / G) + j] = sc;
+                store_scale<HS>(a.scale, grow * (D / G) + j, sc);
                 a.zero[grow * (D / G) + j] = __float2half_rn(z);
             }
         }
@@ -453,8 +492,9 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
 // lane = part * 8 + oc; part owns tokens [8 part, 8 part + 8) of the
 // group, oc owns 8 channels of this 64-channel half. FAKE: write the fake-
 // quantized fp16 rows to a.fq instead of codes, scales and zeros.
-template <int BITS, bool FAKE>
+template <int BITS, int MODE>
 __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it, int item, const uint8_t* st, int lane) {
+    constexpr bool FAKE = (MODE & 1) != 0, HS = (MODE & 2) != 0;  // fake quantization; fp16 scales
     const int half = item & 1, g = (item >> 1) % it.ng, bh = (item >> 1) / it.ng;
     const int oc = lane & 7, part = lane >> 3;
     const int octet = half * 8 + oc;
@@ -506,6 +546,10 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
         const float2 hi = __half22float2(hx), lo = __half22float2(hn);
         my_s[0] = __fdiv_rn(__fsub_rn(canon(hi.x), canon(lo.x)), L);
         my_s[1] = __fdiv_rn(__fsub_rn(canon(hi.y), canon(lo.y)), L);
+        if (HS) {  // the stored fp16 scales
+            my_s[0] = __half2float(__float2half_rn(my_s[0]));
+            my_s[1] = __half2float(__float2half_rn(my_s[1]));
+        }
         my_r[0] = my_s[0] == 0.0f ? 0.0f : __frcp_rn(my_s[0]);
         my_r[1] = my_s[1] == 0.0f ? 0.0f : __frcp_rn(my_s[1]);
     }
@@ -525,14 +569,12 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
     if (FAKE) {
         uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * kD) + octet;
 #pragma unroll 1
-        for (int i = 0; i < nv; ++i) frow[i * (kD / 8)] = fake8(xs[i * 8], z2, r2, s);
+        for (int i = 0; i < nv; ++i) frow[i * (kD / 8)] = fake8<BITS, HS>(xs[i * 8], z2, r2, s);
         return;
     }
     if (part == 0) {
         const long long m = ((long long)bh * (a.s_cap / kG) + a.s_off / kG + g) * kD + octet * 8;
-        float4* sp = reinterpret_cast<float4*>(a.scale + m);
-        sp[0] = make_float4(s[0], s[1], s[2], s[3]);
-        sp[1] = make_float4(s[4], s[5], s[6], s[7]);
+        store_scales8<HS>(a.scale, m, s);
         uint4 zp;
         zp.x = h2_as_u32(__floats2half2_rn(z[0], z[1]));
         zp.y = h2_as_u32(__floats2half2_rn(z[2], z[3]));
@@ -547,16 +589,17 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
         else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
     };
 #pragma unroll (kKeyUnroll)
-    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS>(xs[i * 8], z2, r2, s));
+    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, HS>(xs[i * 8], z2, r2, s));
 }
 
 // G = 32 values: lane = 16 jp + row; the lane quantizes the groups j = 2 jp and
 // 2 jp + 1 (32 channels each) of row `row` of the item: min/max, scale and
 // codes of a whole group in one lane, no shuffles, one 16-byte code store
 // (4-bit) per group.
-template <int BITS, bool FAKE>
+template <int BITS, int MODE>
 __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
                                            int lane) {
+    constexpr bool FAKE = (MODE & 1) != 0, HS = (MODE & 2) != 0;  // fake quantization; fp16 scales
     const int vi = item - it.key_items;
     const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
     const int row = lane & 15, jp = lane >> 4;
@@ -582,7 +625,8 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
         const __half2 m2 = __hmin2(__hmin2(mk[0], mk[1]), __hmin2(mk[2], mk[3]));
         const __half2 x2 = __hmax2(__hmax2(xk[0], xk[1]), __hmax2(xk[2], xk[3]));
         const float z = canon(__half2float(__hmin(__low2half(m2), __high2half(m2))));
-        const float sc = __fdiv_rn(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z), L);
+        float sc = __fdiv_rn(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z), L);
+        if (HS) sc = __half2float(__float2half_rn(sc));  // the stored fp16 scale
         const float rc = sc == 0.0f ? 0.0f : __frcp_rn(sc);
         const f32x2 z1 = pk(z, z), r1 = pk(rc, rc);
         const f32x2 z2[4] = {z1, z1, z1, z1}, r2[4] = {r1, r1, r1, r1};
@@ -590,7 +634,7 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
         if (FAKE) {
             uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * kD + 32 * j);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) frow[k] = fake8(x[k], z2, r2, sv);
+            for (int k = 0; k < 4; ++k) frow[k] = fake8<BITS, HS>(x[k], z2, r2, sv);
         } else {
             auto store_group = [&](const uint32_t (&pq)[4]) {
                 if (BITS == 4) {
@@ -602,9 +646,9 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
             };
             uint32_t pq[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS>(x[k], z2, r2, sv);
+            for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS, HS>(x[k], z2, r2, sv);
             store_group(pq);
-            a.scale[grow * (kD / kG) + j] = sc;
+            store_scale<HS>(a.scale, grow * (kD / kG) + j, sc);
             a.zero[grow * (kD / kG) + j] = __float2half_rn(z);
         }
     }
@@ -612,7 +656,7 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
 
 // Keys, values, or both: warp w of the grid handles items w, w + W, ... of the
 // list [key items | value items] (W = total warps).
-template <int BITS, bool FAKE, int G, int D>
+template <int BITS, int MODE, int G, int D>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -632,11 +676,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs
         cp_async_wait1();
         __syncwarp();
         if (G == 32 && D == kD) {  // the generic item code at G = 32 measured 0.7 % slower than this form
-            if (item < it.key_items) key_item_g32<BITS, FAKE>(k, it, item, S, lane);
-            else value_item_g32<BITS, FAKE>(v, it, item, S, lane);
+            if (item < it.key_items) key_item_g32<BITS, MODE>(k, it, item, S, lane);
+            else value_item_g32<BITS, MODE>(v, it, item, S, lane);
         } else {
-            if (item < it.key_items) key_item<BITS, FAKE, G, D>(k, it, item, S, lane);
-            else value_item<BITS, FAKE, G, D>(v, it, item, S, lane);
+            if (item < it.key_items) key_item<BITS, MODE, G, D>(k, it, item, S, lane);
+            else value_item<BITS, MODE, G, D>(v, it, item, S, lane);
         }
         __syncwarp();
         if (item + 2 * stride < total) fetch_item<G, D>(k, v, it, item + 2 * stride, S, lane);
@@ -644,13 +688,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs
     }
 }
 
-template <int BITS, bool FAKE, int G, int D>
+template <int BITS, int MODE, int G, int D>
 cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
     static int grid_cap = 0;
     static bool configured = false;  // benign race: every caller sets the same values
     const int smem = (kThreads / 32) * 2 * Stage<G>::kBytes;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, FAKE, G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, MODE, G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -662,7 +706,7 @@ cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it
     if (total <= 0) return cudaSuccess;
     long long blocks = (total + 3) / 4;
     if (blocks > grid_cap) blocks = grid_cap;
-    return launch_pdl(flush_kernel<BITS, FAKE, G, D>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
+    return launch_pdl(flush_kernel<BITS, MODE, G, D>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
 }
 
 // Pointers of heads [h0, h0 + nh) of a flush.
@@ -676,24 +720,25 @@ FlushArgs head_slice(const FlushArgs& a, int h0, int nh, int bits, int axis) {
     }
     s.codes += (long long)h0 * a.s_cap * (a.D * bits / 8);
     const long long meta = axis == 0 ? (long long)(a.s_cap / a.G) * a.D : (long long)a.s_cap * (a.D / a.G);
-    s.scale += h0 * meta;
+    s.scale = a.scale_f16 ? reinterpret_cast<float*>(reinterpret_cast<__half*>(a.scale) + h0 * meta)
+                          : a.scale + h0 * meta;
     s.zero += h0 * meta;
     return s;
 }
 
 // (G, D) pairs: G in {32, 64, 128}, D in {64, 128, 256}, G <= D
-template <int BITS, bool FAKE>
+template <int BITS, int MODE>
 cudaError_t launch_items_g(const FlushArgs& k, const FlushArgs& v, const Items& it, int G, int D,
                            cudaStream_t stream) {
     switch (G * 1000 + D) {
-        case 32064: return launch_items<BITS, FAKE, 32, 64>(k, v, it, stream);
-        case 32128: return launch_items<BITS, FAKE, 32, 128>(k, v, it, stream);
-        case 32256: return launch_items<BITS, FAKE, 32, 256>(k, v, it, stream);
-        case 64064: return launch_items<BITS, FAKE, 64, 64>(k, v, it, stream);
-        case 64128: return launch_items<BITS, FAKE, 64, 128>(k, v, it, stream);
-        case 64256: return launch_items<BITS, FAKE, 64, 256>(k, v, it, stream);
-        case 128128: return launch_items<BITS, FAKE, 128, 128>(k, v, it, stream);
-        case 128256: return launch_items<BITS, FAKE, 128, 256>(k, v, it, stream);
+        case 32064: return launch_items<BITS, MODE, 32, 64>(k, v, it, stream);
+        case 32128: return launch_items<BITS, MODE, 32, 128>(k, v, it, stream);
+        case 32256: return launch_items<BITS, MODE, 32, 256>(k, v, it, stream);
+        case 64064: return launch_items<BITS, MODE, 64, 64>(k, v, it, stream);
+        case 64128: return launch_items<BITS, MODE, 64, 128>(k, v, it, stream);
+        case 64256: return launch_items<BITS, MODE, 64, 256>(k, v, it, stream);
+        case 128128: return launch_items<BITS, MODE, 128, 128>(k, v, it, stream);
+        case 128256: return launch_items<BITS, MODE, 128, 256>(k, v, it, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -721,11 +766,20 @@ cudaError_t launch_flush_impl(const FlushArgs& k, const FlushArgs& v, bool do_k,
         it.nv = nv;
         it.key_items = do_k ? nh * kq * ng : 0;
         it.val_items = do_v ? nh * nv : 0;
-        const bool fake = a.fq != nullptr;
-        cudaError_t e = bits == 4 ? (fake ? launch_items_g<4, true>(ks, vs, it, G, D, stream)
-                                          : launch_items_g<4, false>(ks, vs, it, G, D, stream))
-                                  : (fake ? launch_items_g<2, true>(ks, vs, it, G, D, stream)
-                                          : launch_items_g<2, false>(ks, vs, it, G, D, stream));
+        // MODE bit 0: fake quantization; bit 1: fp16 scales
+        const int mode = (a.fq != nullptr ? 1 : 0) | (a.scale_f16 ? 2 : 0);
+        cudaError_t e = cudaErrorInvalidValue;
+        switch (bits * 10 + mode) {
+            case 40: e = launch_items_g<4, 0>(ks, vs, it, G, D, stream); break;
+            case 41: e = launch_items_g<4, 1>(ks, vs, it, G, D, stream); break;
+            case 42: e = launch_items_g<4, 2>(ks, vs, it, G, D, stream); break;
+            case 43: e = launch_items_g<4, 3>(ks, vs, it, G, D, stream); break;
+            case 20: e = launch_items_g<2, 0>(ks, vs, it, G, D, stream); break;
+            case 21: e = launch_items_g<2, 1>(ks, vs, it, G, D, stream); break;
+            case 22: e = launch_items_g<2, 2>(ks, vs, it, G, D, stream); break;
+            case 23: e = launch_items_g<2, 3>(ks, vs, it, G, D, stream); break;
+            default: break;
+        }
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

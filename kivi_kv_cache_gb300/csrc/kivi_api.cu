@@ -36,6 +36,12 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The `bits` argument of every entry point: the bit width, optionally ORed
+// with KIVI_SCALE_F16 (scales stored as fp16). Any other high bit leaves a
+// width outside {2, 4}, which the shape check refuses.
+bool scale_f16_of(int bits) { return (bits & KIVI_SCALE_F16) != 0; }
+int width_of(int bits) { return bits & ~KIVI_SCALE_F16; }
+
 bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
 
 // Every op: D in {64, 128, 256}, G in {32, 64, 128} with G <= D (a value
@@ -178,10 +184,11 @@ kivi_status flush_check(const void* x, int BH, int S, int x_bh_stride, int D, in
 }
 
 FlushArgs flush_args(const void* x, int BH, int x_bh_stride, int n, void* codes, float* scale,
-                     void* zero, int s_off, int s_cap, int G, int D) {
+                     void* zero, int s_off, int s_cap, int G, int D, bool hs) {
     FlushArgs a;
     a.G = G;
     a.D = D;
+    a.scale_f16 = hs;
     a.x = static_cast<const __half*>(x);
     a.x_bh_stride = x_bh_stride;
     a.BH = BH;
@@ -197,13 +204,15 @@ FlushArgs flush_args(const void* x, int BH, int x_bh_stride, int n, void* codes,
 kivi_status flush_one(int axis, const void* x, int BH, int S, int x_bh_stride, int D, int G,
                       int bits, int R, void* codes, float* scale, void* zero, int s_off,
                       int s_cap, int* n_flushed, kivi_stream_t stream) {
+    const bool hs = scale_f16_of(bits);
+    bits = width_of(bits);
     int n = 0;
     kivi_status st = flush_check(x, BH, S, x_bh_stride, D, G, bits, R, codes, scale, zero, s_off,
                                  s_cap, axis == 0, &n);
     if (st != KIVI_OK) return st;
     if (n_flushed) *n_flushed = n;
     if (n == 0) return KIVI_OK;
-    return from_cuda(launch_flush(axis, flush_args(x, BH, x_bh_stride, n, codes, scale, zero, s_off, s_cap, G, D),
+    return from_cuda(launch_flush(axis, flush_args(x, BH, x_bh_stride, n, codes, scale, zero, s_off, s_cap, G, D, hs),
                                   bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -214,6 +223,8 @@ kivi_status flush_one(int axis, const void* x, int BH, int S, int x_bh_stride, i
 kivi_status fake_quant(const void* k, const void* v, bool do_k, bool do_v, int BH, int S, int x_bh_stride,
                        int D, int G, int bits, int R, void* k_out, void* v_out, int out_bh_stride,
                        int* n_quantized, kivi_stream_t stream) {
+    const bool hs = scale_f16_of(bits);
+    bits = width_of(bits);
     kivi_status st = shape_check(D, G, bits);
     if (st != KIVI_OK) return st;
     if (BH <= 0 || S < 0 || R < 0 || x_bh_stride < S || out_bh_stride < S) return KIVI_ERR_INVALID_ARG;
@@ -229,8 +240,8 @@ kivi_status fake_quant(const void* k, const void* v, bool do_k, bool do_v, int B
         return KIVI_ERR_ALIGNMENT;
     const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
     if (n > 0) {
-        FlushArgs ka = flush_args(do_k ? k : v, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G, D);
-        FlushArgs va = flush_args(do_v ? v : k, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G, D);
+        FlushArgs ka = flush_args(do_k ? k : v, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G, D, hs);
+        FlushArgs va = flush_args(do_v ? v : k, BH, x_bh_stride, n, nullptr, nullptr, nullptr, 0, G, G, D, hs);
         ka.fq = static_cast<__half*>(do_k ? k_out : v_out);
         va.fq = static_cast<__half*>(do_v ? v_out : k_out);
         ka.fq_bh_stride = va.fq_bh_stride = out_bh_stride;
@@ -320,6 +331,8 @@ kivi_status kivi_flush_kv(const void* k_f16, const void* v_f16, int BH, int S, i
                           float* kscale, void* kzero_f16, void* vcodes_u8, float* vscale,
                           void* vzero_f16, int s_off, int s_cap, int* n_flushed,
                           kivi_stream_t stream) {
+    const bool hs = scale_f16_of(bits);
+    bits = width_of(bits);
     int nk = 0, nv = 0;
     kivi_status st = flush_check(k_f16, BH, S, x_bh_stride, D, group_size, bits, residual_length,
                                  kcodes_u8, kscale, kzero_f16, s_off, s_cap, true, &nk);
@@ -330,14 +343,16 @@ kivi_status kivi_flush_kv(const void* k_f16, const void* v_f16, int BH, int S, i
     if (n_flushed) *n_flushed = nk;
     if (nk == 0) return KIVI_OK;
     return from_cuda(launch_flush_kv(
-        flush_args(k_f16, BH, x_bh_stride, nk, kcodes_u8, kscale, kzero_f16, s_off, s_cap, group_size, D),
-        flush_args(v_f16, BH, x_bh_stride, nv, vcodes_u8, vscale, vzero_f16, s_off, s_cap, group_size, D), bits,
+        flush_args(k_f16, BH, x_bh_stride, nk, kcodes_u8, kscale, kzero_f16, s_off, s_cap, group_size, D, hs),
+        flush_args(v_f16, BH, x_bh_stride, nv, vcodes_u8, vscale, vzero_f16, s_off, s_cap, group_size, D, hs), bits,
         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kivi_status kivi_dequant(kivi_axis axis, const void* codes_u8, const float* scale,
                          const void* zero_f16, int BH, int S, int D, int group_size, int bits,
                          int s_cap, void* out_f16, kivi_stream_t stream) {
+    const bool hs = scale_f16_of(bits);
+    bits = width_of(bits);
     kivi_status st = shape_check(D, group_size, bits);
     if (st != KIVI_OK) return st;
     if ((axis != KIVI_AXIS_KEYS && axis != KIVI_AXIS_VALUES) || BH <= 0 || S < 0 || s_cap <= 0 ||
@@ -357,6 +372,7 @@ kivi_status kivi_dequant(kivi_axis axis, const void* codes_u8, const float* scal
     a.out = static_cast<__half*>(out_f16);
     a.G = group_size;
     a.D = D;
+    a.scale_f16 = hs;
     return from_cuda(launch_dequant((int)axis, a, bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -364,6 +380,8 @@ kivi_status kivi_dequant_kv(const void* kcodes_u8, const float* kscale, const vo
                             const void* vcodes_u8, const float* vscale, const void* vzero_f16, int BH, int S,
                             int D, int group_size, int bits, int s_cap, void* kout_f16, void* vout_f16,
                             kivi_stream_t stream) {
+    const bool hs = scale_f16_of(bits);
+    bits = width_of(bits);
     kivi_status st = shape_check(D, group_size, bits);
     if (st != KIVI_OK) return st;
     if (BH <= 0 || S < 0 || s_cap <= 0 || s_cap % group_size != 0 || S > s_cap) return KIVI_ERR_INVALID_ARG;
@@ -387,6 +405,7 @@ kivi_status kivi_dequant_kv(const void* kcodes_u8, const float* kscale, const vo
     k.s_cap = v.s_cap = s_cap;
     k.G = v.G = group_size;
     k.D = v.D = D;
+    k.scale_f16 = v.scale_f16 = hs;
     return from_cuda(launch_dequant_kv(k, v, bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -465,6 +484,8 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
                                const void* v_res_f16, int n_res, int res_cap, int B, int Hq, int Hkv,
                                int D, int group_size, int bits, float sm_scale, float* out_f32,
                                void* workspace, size_t workspace_bytes_, kivi_stream_t stream) {
+    const bool hs = scale_f16_of(bits);
+    bits = width_of(bits);
     kivi_status st = shape_check(D, group_size, bits);
     if (st != KIVI_OK) return st;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S_q < 0 || n_res < 0 ||
@@ -482,7 +503,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
         !aligned16(vzero_f16) || !aligned16(k_res_f16) || !aligned16(v_res_f16) ||
         !aligned16(workspace))
         return KIVI_ERR_ALIGNMENT;
-    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res, bits, group_size == kG && D == kD, D);
+    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res, bits, group_size == kG && D == kD && !hs, D);
     const size_t need = workspace_bytes(B, Hq, D, p);
     if (need > 0 && (!workspace || workspace_bytes_ < need)) return KIVI_ERR_WORKSPACE;
 
@@ -498,6 +519,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
     a.s_cap = s_cap;
     a.g_shift = group_size == 128 ? 2 : (group_size == 64 ? 1 : 0);
     a.D = D;
+    a.scale_f16 = hs ? 1 : 0;
     a.k_res = static_cast<const __half*>(k_res_f16);
     a.v_res = static_cast<const __half*>(v_res_f16);
     a.n_res = n_res;

@@ -18,7 +18,7 @@ struct FlushArgs {
     int BH;
     int n_flush;
     uint8_t* codes;       // [BH, s_cap, D*bits/8]
-    float* scale;         // keys [BH, s_cap/G, D]; values [BH, s_cap, D/G]
+    float* scale;         // keys [BH, s_cap/G, D]; values [BH, s_cap, D/G]; __half elements if scale_f16
     __half* zero;
     int s_off;
     int s_cap;
@@ -26,6 +26,7 @@ struct FlushArgs {
     long long fq_bh_stride = 0;
     int G = kG;                // group size: 32, 64 or 128
     int D = kD;                // head dim: 64, 128 or 256 (G <= D)
+    bool scale_f16 = false;    // scales stored as fp16 (codes computed with the stored scale)
 };
 
 struct DequantArgs {
@@ -38,6 +39,7 @@ struct DequantArgs {
     __half* out;          // [BH, S, D]
     int G = kG;           // group size: 32, 64 or 128
     int D = kD;           // head dim: 64, 128 or 256 (G <= D)
+    bool scale_f16 = false;  // scales stored as fp16
 };
 
 struct DecodeArgs {
@@ -52,6 +54,7 @@ struct DecodeArgs {
     int s_cap;
     int g_shift;          // log2(G / 32): the store's group size is 32, 64 or 128
     int D = kD;           // head dim: 64, 128 or 256 (the warp-pair kernel: 128)
+    int scale_f16 = 0;    // 1: scales stored as fp16 (the warp-pair kernel: fp32 only)
     const __half* k_res;  // [B*Hkv, res_cap, D]
     const __half* v_res;
     int n_res;
@@ -152,10 +155,13 @@ cudaError_t launch_residual_compact(__half* res0, __half* res1, int BH, int res_
 // Fused decodes; each merges its own splits in the same launch.
 // One warp per tile: gq in {1, 2, 4}, or any other gq in a.q_sub sub-groups of
 // up to 4 query heads; stores of group size 32, 64 or 128; head dim a.D of 64,
-// 128 or 256 (the _d64 / _d256 forms serve one head dim each).
+// 128 or 256, fp32 or fp16 scales (the suffixed forms serve one head dim and
+// scale storage each).
 cudaError_t launch_decode_mma(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
+cudaError_t launch_decode_mma_d128_f16s(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 cudaError_t launch_decode_mma_d64(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 cudaError_t launch_decode_mma_d256(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
+cudaError_t launch_decode_mma_d256_f16s(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);
 // gq in {1, 2, 4}: two warps per tile, 4 warp pairs per CTA (small batches);
 // stores of group size 32 only.
 cudaError_t launch_decode_pair(const DecodeArgs& a, int bits, int gq, cudaStream_t stream);

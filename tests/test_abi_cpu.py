@@ -75,6 +75,9 @@ def flush(L, name="kivi_flush_keys", x=FAKE, BH=8, S=256, stride=256, D=128, G=3
 @pytest.mark.parametrize("name", ["kivi_flush_keys", "kivi_flush_values"])
 def test_flush_rejects_bad_arguments_without_launching(L, name):
     assert flush(L, name, bits=3)[0] == UNSUPPORTED
+    assert flush(L, name, bits=3 | 0x100)[0] == UNSUPPORTED   # KIVI_SCALE_F16 with a bad width
+    assert flush(L, name, bits=4 | 0x200)[0] == UNSUPPORTED   # an unknown option bit
+    assert flush(L, name, bits=4 | 0x100, zero=FAKE + 2)[0] == ALIGN  # the option passes the checks
     assert flush(L, name, D=96)[0] == UNSUPPORTED
     assert flush(L, name, D=512)[0] == UNSUPPORTED
     assert flush(L, name, D=64, G=128)[0] == UNSUPPORTED  # a value group would outgrow the row
@@ -136,6 +139,8 @@ def test_decode_rejects_bad_arguments(L):
     assert decode(L, D=96) == UNSUPPORTED            # head dims 64, 128, 256
     assert decode(L, D=64, G=128, S_q=2048, s_cap=2048) == UNSUPPORTED  # G > D
     assert decode(L, D=256, ws=None) == WORKSPACE    # D = 256 passes the checks
+    assert decode(L, bits=4 | 0x100, ws=None) == WORKSPACE  # fp16 scales pass the checks
+    assert decode(L, bits=4 | 0x400) == UNSUPPORTED
     assert decode(L, G=64) == INVALID                # s_cap 2080 is not a multiple of 64
     assert decode(L, G=128, S_q=2048, s_cap=2048, ws=None) == WORKSPACE  # G = 128 passes the checks
     assert decode(L, Hq=520) == UNSUPPORTED          # 65 query heads per KV head
