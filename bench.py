@@ -44,8 +44,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 # --profile-case NAME: (op kind, B, S_q, n_res, bits); flush cases use the named workload
+# (with the group size a _gNN suffix names)
 PROFILE_CASES = {
     "flush_long2bit": ("flush", 0, 0, 0, 2),
+    "flush_long2bit_g128": ("flush", 0, 0, 0, 2),
     "decode_b1_16k": ("decode", 1, 16384 - 128, 128, 4),
     "decode_b32_4k": ("decode", 32, 4032, 64, 4),
 }
@@ -935,7 +937,10 @@ def run_profile_case(name: str, reps: int = 3):
     torch.cuda.set_device(dev)
     kind, B, S_q, n_res, bits = PROFILE_CASES[name]
     if kind == "flush":
-        w = synth.WORKLOADS[name.split("_")[1]]
+        parts = name.split("_")
+        w = synth.WORKLOADS[parts[1]]
+        if len(parts) > 2 and parts[2].startswith("g"):
+            w = dataclasses.replace(w, G=int(parts[2][1:]))
         n = kv.kivi_flush_count(w.S, w.R, w.G)
         k, v, _ = synth.prefill_inputs_torch(w, 1, dev)
         ks = kv.KiviStore(0, w.BH, n, w.D, w.G, w.bits, device=dev)
