@@ -56,6 +56,8 @@
 
 #include <math.h>
 
+#include <type_traits>
+
 #include "decode_common.cuh"
 #include "decode_merge.cuh"
 #include "kivi_device.cuh"
@@ -162,9 +164,9 @@ __device__ __forceinline__ void fetch_store_tile(const DecodeArgs& a, int bh, in
     }
     // the key group (32 << g_shift tokens) holding this tile, and the value
     // metadata of its 32 tokens: (D / 32) >> g_shift entries per token, packed
-    // at the front of VS and VZ. fp16 scales (scale_f16) land raw at the front
-    // of KS and VS (HS). expand_meta turns both forms into the layout the tile
-    // code reads.
+    // at the front of VS and VZ (widen_value_meta spreads them for G > 32).
+    // fp16 scales (HS) land in plain channel order at the front of KS and VS
+    // and are read as fp16 by the tile code.
     const int sh = a.g_shift;
     const long long krow = (long long)bh * (a.s_cap >> (5 + sh)) + (tile >> sh);
     const long long vrow = ((long long)bh * a.s_cap + tok0) * ((D / 32) >> sh);
@@ -193,48 +195,63 @@ __device__ __forceinline__ void fetch_store_tile(const DecodeArgs& a, int bh, in
     if (lane < nvz) cp_async16(st + GE::kVZ + lane * 16, vz + lane * 8, true);
 }
 
-// Metadata that does not arrive in the layout the tile code reads (VS and VZ
-// [32 tokens][D / 32], one entry per 32 channels; KS fp32 in padded channel
-// order):
-//   * a store of group size 64 (g_shift 1) or 128 (g_shift 2) has 2 or 4
-//     times fewer value scales and zeros per token: each is repeated;
-//   * fp16 scales (f16) arrive raw at the front of KS and VS: widened to fp32.
-// Each lane reads its token's value entries and D / 32 key scales, then, once
-// the warp has read them all, writes them back in place.
-template <int D>
-__device__ __forceinline__ void expand_meta(uint8_t* st, int sh, bool f16, int lane) {
+// A store of group size 64 (g_shift 1) or 128 (g_shift 2) has 2 or 4 times
+// fewer value scales and zeros per token than the tile code reads (VS and VZ
+// [32 tokens][D / 32], one entry per 32 channels). Each lane takes its
+// token's entries, then, once the warp has read them all, writes them back
+// with each repeated 2 or 4 times. Value scales are fp32, or fp16 (HS); key
+// scales need no change (fp32 in padded channel order, or fp16 in plain
+// channel order, which the tile code reads as such).
+template <int D, bool HS>
+__device__ __forceinline__ void widen_value_meta(uint8_t* st, int sh, int lane) {
     using GE = Geo<D>;
     constexpr int NE = GE::kNE;
-    constexpr int KPL = D / 32;  // key scales per lane
-    float ksv[KPL];
-    if (f16) {
-        const __half* kraw = reinterpret_cast<const __half*>(st + GE::kKS);
-#pragma unroll
-        for (int k = 0; k < KPL; ++k) ksv[k] = __half2float(kraw[lane * KPL + k]);
-    }
-    float* vs = reinterpret_cast<float*>(st + GE::kVS);
+    using ST = typename std::conditional<HS, unsigned short, float>::type;  // one stored scale
+    ST* vs = reinterpret_cast<ST*>(st + GE::kVS);
     unsigned short* vz = reinterpret_cast<unsigned short*>(st + GE::kVZ);
     const int nr = NE >> sh;  // entries per token in the store
-    float s[NE];
+    ST s[NE];
     unsigned short z[NE];
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
         const int idx = lane * nr + (e >> sh);
-        s[e] = f16 ? __half2float(reinterpret_cast<const __half*>(vs)[idx]) : vs[idx];
+        s[e] = vs[idx];
         z[e] = vz[idx];
     }
     __syncwarp();
-    if (f16) {
-        float* ks = reinterpret_cast<float*>(st + GE::kKS);
-#pragma unroll
-        for (int k = 0; k < KPL; ++k) ks[padc(lane * KPL + k)] = ksv[k];
-    }
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
         vs[lane * NE + e] = s[e];
         vz[lane * NE + e] = z[e];
     }
     __syncwarp();
+}
+
+// fp16 scales of the staged tile (HS) as fp32: key scales of channels cb ..
+// cb + 7 (cb a multiple of 8) or cb .. cb + 3 (a multiple of 4), in plain
+// channel order at ks; the NE value scales of token t at vs ([32][NE]).
+__device__ __forceinline__ void key_scales8_h(const uint8_t* ks, int cb, float4& a, float4& b) {
+    const uint4 h = *reinterpret_cast<const uint4*>(ks + 2 * cb);
+    const float2 f0 = __half22float2(u32_as_h2(h.x)), f1 = __half22float2(u32_as_h2(h.y));
+    const float2 f2 = __half22float2(u32_as_h2(h.z)), f3 = __half22float2(u32_as_h2(h.w));
+    a = make_float4(f0.x, f0.y, f1.x, f1.y);
+    b = make_float4(f2.x, f2.y, f3.x, f3.y);
+}
+__device__ __forceinline__ float4 key_scales4_h(const uint8_t* ks, int cb) {
+    const uint2 h = *reinterpret_cast<const uint2*>(ks + 2 * cb);
+    const float2 f0 = __half22float2(u32_as_h2(h.x)), f1 = __half22float2(u32_as_h2(h.y));
+    return make_float4(f0.x, f0.y, f1.x, f1.y);
+}
+template <int NE>
+__device__ __forceinline__ void value_scales_h(const uint8_t* vs, int t, float (&x)[NE]) {
+    uint32_t w[NE / 2];
+    load_words<NE / 2>(vs + 2 * NE * t, w);
+#pragma unroll
+    for (int e = 0; e < NE / 2; ++e) {
+        const float2 f = __half22float2(u32_as_h2(w[e]));
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
 }
 
 // kResTok fp16 rows of K into st0 and of V into st1, 16-byte chunk c of row r
@@ -368,15 +385,16 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
         uint8_t* S = st0 + (it & 1) * kStage;
         cp_async_wait<1>();
         __syncwarp();
-        if (HS || a.g_shift != 0) expand_meta<D>(S, a.g_shift, HS, lane);
+        if (a.g_shift != 0) widen_value_meta<D, HS>(S, a.g_shift, lane);
         const int nvalid = min(32, a.S_q - tile * 32);
         if (nvalid < 32) {  // zero the value metadata of rows past S_q
-            float* vsz = reinterpret_cast<float*>(S + GE::kVS);
+            using ST = typename std::conditional<HS, unsigned short, float>::type;
+            ST* vsz = reinterpret_cast<ST*>(S + GE::kVS);
             unsigned short* vzz = reinterpret_cast<unsigned short*>(S + GE::kVZ);
             if (lane >= nvalid) {
 #pragma unroll
                 for (int j = 0; j < NE; ++j) {
-                    vsz[lane * NE + j] = 0.f;
+                    vsz[lane * NE + j] = 0;
                     vzz[lane * NE + j] = 0;
                 }
             }
@@ -391,7 +409,9 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
         float smax = 0.f;
 #pragma unroll
         for (int i = lane; i < D / 4; i += 32) {
-            const float4 s4 = *reinterpret_cast<const float4*>(KS + padc(4 * i));  // scales are >= 0
+            float4 s4;  // scales are >= 0
+            if constexpr (HS) s4 = key_scales4_h(S + GE::kKS, 4 * i);
+            else s4 = *reinterpret_cast<const float4*>(KS + padc(4 * i));
             smax = fmaxf(smax, fmaxf(fmaxf(s4.x, s4.y), fmaxf(s4.z, s4.w)));
         }
         smax = warp_max(smax);
@@ -447,8 +467,13 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
 #pragma unroll
                 for (int mm = 0; mm < WPC; ++mm) {
                     const int cb = (D / 4) * c + 8 * (WPC * ch + mm);
-                    const float4 sa = *reinterpret_cast<const float4*>(KS + padc(cb));
-                    const float4 sb = *reinterpret_cast<const float4*>(KS + padc(cb + 4));
+                    float4 sa, sb;
+                    if constexpr (HS) {
+                        key_scales8_h(S + GE::kKS, cb, sa, sb);
+                    } else {
+                        sa = *reinterpret_cast<const float4*>(KS + padc(cb));
+                        sb = *reinterpret_cast<const float4*>(KS + padc(cb + 4));
+                    }
                     const float4 qa = *reinterpret_cast<const float4*>(qrow + padc(cb));
                     const float4 qb = *reinterpret_cast<const float4*>(qrow + padc(cb + 4));
                     const float2 v01 = upk(mul2(mul2(pk(qa.x, qa.y), pk(sa.x, sa.y)), fB2));
@@ -493,7 +518,9 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int cb = (D / 4) * c + 16 * (WPC * ch + mm) + 4 * i;
-                        const float4 s4 = *reinterpret_cast<const float4*>(KS + padc(cb));
+                        float4 s4;
+                        if constexpr (HS) s4 = key_scales4_h(S + GE::kKS, cb);
+                        else s4 = *reinterpret_cast<const float4*>(KS + padc(cb));
                         const float4 q4 = *reinterpret_cast<const float4*>(qrow + padc(cb));
                         const float2 lo2 = upk(mul2(mul2(pk(q4.x, q4.y), pk(s4.x, s4.y)), fB2));
                         const float2 hi2 = upk(mul2(mul2(pk(q4.z, q4.w), pk(s4.z, s4.w)), fB2h));
@@ -604,8 +631,16 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
                 const int ta = 16 * ks + 2 * c, tb = ta + 8;
-                dst[ks][0] = split_pair(pp[ks][0] * VS[ta * NE + j], pp[ks][1] * VS[(ta + 1) * NE + j], lo_part);
-                dst[ks][1] = split_pair(pp[ks][2] * VS[tb * NE + j], pp[ks][3] * VS[(tb + 1) * NE + j], lo_part);
+                if constexpr (HS) {
+                    const __half* VH = reinterpret_cast<const __half*>(VS);
+                    dst[ks][0] = split_pair(pp[ks][0] * __half2float(VH[ta * NE + j]),
+                                            pp[ks][1] * __half2float(VH[(ta + 1) * NE + j]), lo_part);
+                    dst[ks][1] = split_pair(pp[ks][2] * __half2float(VH[tb * NE + j]),
+                                            pp[ks][3] * __half2float(VH[(tb + 1) * NE + j]), lo_part);
+                } else {
+                    dst[ks][0] = split_pair(pp[ks][0] * VS[ta * NE + j], pp[ks][1] * VS[(ta + 1) * NE + j], lo_part);
+                    dst[ks][1] = split_pair(pp[ks][2] * VS[tb * NE + j], pp[ks][3] * VS[(tb + 1) * NE + j], lo_part);
+                }
             }
         };
         if (D <= 128) {
@@ -625,10 +660,28 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
                         x[e + 1] = r.y;
                     }
                 };
-                prodN(pp[ks][0], VS + ta * NE, xa0);
-                prodN(pp[ks][1], VS + (ta + 1) * NE, xa1);
-                prodN(pp[ks][2], VS + tb * NE, xb0);
-                prodN(pp[ks][3], VS + (tb + 1) * NE, xb1);
+                if constexpr (HS) {
+                    auto prodH = [&](float pt, int t, float (&x)[NE]) {
+                        const f32x2 p2 = pk(pt, pt);
+                        float v[NE];
+                        value_scales_h<NE>(S + GE::kVS, t, v);
+#pragma unroll
+                        for (int e = 0; e < NE; e += 2) {
+                            const float2 r = upk(mul2(p2, pk(v[e], v[e + 1])));
+                            x[e] = r.x;
+                            x[e + 1] = r.y;
+                        }
+                    };
+                    prodH(pp[ks][0], ta, xa0);
+                    prodH(pp[ks][1], ta + 1, xa1);
+                    prodH(pp[ks][2], tb, xb0);
+                    prodH(pp[ks][3], tb + 1, xb1);
+                } else {
+                    prodN(pp[ks][0], VS + ta * NE, xa0);
+                    prodN(pp[ks][1], VS + (ta + 1) * NE, xa1);
+                    prodN(pp[ks][2], VS + tb * NE, xb0);
+                    prodN(pp[ks][3], VS + (tb + 1) * NE, xb1);
+                }
 #pragma unroll
                 for (int j = 0; j < NBP; ++j) {
                     bp[j][ks][0] = split_pair(xa0[j], xa1[j], lo_part);
