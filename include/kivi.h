@@ -299,7 +299,7 @@ kivi_status kivi_decode_attend(const void* q_f16,
  * interface addition of this library.
  *
  * Instead of a workspace argument it uses one library-owned device array of
- * KIVI_NOALLOC_SCRATCH_BYTES (4 MiB) per device, reserved when the library's
+ * KIVI_NOALLOC_SCRATCH_BYTES (8 MiB) per device, reserved when the library's
  * device code is loaded and kept until the process exits. It allocates
  * nothing itself.
  *   - Size limit: if kivi_decode_workspace_size(...) for these sizes exceeds
@@ -318,7 +318,7 @@ kivi_status kivi_decode_attend(const void* q_f16,
  * Every other argument, check, status and result is that of
  * kivi_decode_attend.
  */
-#define KIVI_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+#define KIVI_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 kivi_status kivi_decode_attend_noalloc(const void* q_f16,
                                        const void* kcodes_u8, const float* kscale, const void* kzero_f16,
                                        const void* vcodes_u8, const float* vscale, const void* vzero_f16,

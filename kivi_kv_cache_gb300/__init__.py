@@ -354,7 +354,7 @@ _noalloc_fn = None
 def kivi_decode_attend_noalloc(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res, v_res, n_res: int,
                                Hkv: int, sm_scale: float, out=None, stream=None):
     """The decode of kivi_decode_attend without a workspace argument: the split
-    scratch lives in a library-owned 4 MiB device array (for callers that may
+    scratch lives in a library-owned 8 MiB device array (for callers that may
     not allocate device memory when they decode). Calls that overlap on the GPU
     race on that array; make the first call on a device before any stream
     capture."""

@@ -204,12 +204,16 @@ def test_every_plan_fits_the_noalloc_scratch(L):
     """Without a device the planner sizes for 152 SMs (a GB300). Its split
     count keeps the partials near one per planned warp, so over a wide grid of
     shapes (group sizes 1 to 64, sub-groups included) no workspace exceeds
-    the 4 MiB library-owned scratch of kivi_decode_attend_noalloc."""
-    worst = 0
+    the 8 MiB library-owned scratch of kivi_decode_attend_noalloc, at any
+    supported head dim (the partials hold D floats per split)."""
+    worst = {64: 0, 128: 0, 256: 0}
     for hkv in (1, 2, 8, 32):
         for gq in (1, 2, 3, 4, 6, 8, 12, 32, 64):
             for B in (1, 3, 16, 64, 256):
                 for S in (32, 100, 1024, 4096, 32768, 131072):
                     for n_res in (0, 37):
-                        worst = max(worst, L.kivi_decode_workspace_size(B, hkv * gq, hkv, S, n_res, 128))
-    assert 3 << 20 < worst <= 4 * 1024 * 1024
+                        for D in worst:
+                            worst[D] = max(worst[D], L.kivi_decode_workspace_size(B, hkv * gq, hkv, S, n_res, D))
+    assert 3 << 20 < worst[128] <= 4 * 1024 * 1024
+    assert worst[64] < worst[128] < worst[256]
+    assert 6 << 20 < worst[256] <= 8 * 1024 * 1024
