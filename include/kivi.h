@@ -122,8 +122,9 @@ int kivi_flush_count(int n_res, int residual_length, int group_size);
  *     q = clamp(rint(RN32(RN32(x - zero) / scale)), 0, 2^bits - 1)
  * (IEEE fp32 division, round half to even; scale == 0 gives q = 0), and
  * written at store token offset s_off (a multiple of G) of a key store of
- * capacity s_cap: codes[BH, s_cap, D*bits/8], scale f32 / zero fp16
- * [BH, s_cap/G, D]. Bit-exact with the CPU oracle.
+ * capacity s_cap: codes[BH, s_cap, D*bits/8], scale f32 (fp16 with
+ * KIVI_SCALE_F16) / zero fp16 [BH, s_cap/G, D]. Bit-exact with the CPU
+ * oracle.
  * *n_flushed (host pointer, may be NULL) receives n_flush.
  * Errors: INVALID_ARG if S < 0, BH <= 0, x_bh_stride < S, s_cap % G != 0,
  * s_off % G != 0 or s_off + n_flush > s_cap; ALIGNMENT if a pointer is not
@@ -136,9 +137,9 @@ kivi_status kivi_flush_keys(const void* x_f16, int BH, int S, int x_bh_stride, i
 
 /*
  * Value flush ([F] "The layout problem", "Kernel B"): as kivi_flush_keys,
- * but each group is G consecutive channels of one token; scale f32 and zero
- * fp16 are [BH, s_cap, D/G]. s_off need not be a multiple of G here, but must
- * satisfy s_off + n_flush <= s_cap.
+ * but each group is G consecutive channels of one token; scale f32 (fp16
+ * with KIVI_SCALE_F16) and zero fp16 are [BH, s_cap, D/G]. s_off need not be
+ * a multiple of G here, but must satisfy s_off + n_flush <= s_cap.
  */
 kivi_status kivi_flush_values(const void* x_f16, int BH, int S, int x_bh_stride, int D,
                               int group_size, int bits, int residual_length,
@@ -160,7 +161,8 @@ kivi_status kivi_flush_kv(const void* k_f16, const void* v_f16, int BH, int S, i
  * "Three ways to be off by one bit" #1: a multiply then a separate add, two
  * roundings, no FMA): tokens [0, S) of a store of capacity s_cap to fp16
  * out[BH, S, D]:  out = fp16_rn(RN32(RN32(q * scale) + zero)).
- * axis selects the key or value metadata layout. Bit-exact with the oracle.
+ * axis selects the key or value metadata layout; bits carries
+ * KIVI_SCALE_F16 when the store holds fp16 scales. Bit-exact with the oracle.
  * Errors: INVALID_ARG if S < 0, S > s_cap or s_cap % G != 0.
  */
 kivi_status kivi_dequant(kivi_axis axis, const void* codes_u8, const float* scale,
@@ -231,8 +233,9 @@ kivi_status kivi_fake_quant_kv(const void* k_f16, const void* v_f16, int BH, int
 
 /*
  * Bytes of device workspace kivi_decode_attend needs for these sizes on the
- * current device, for any bit width and group size (the split count depends
- * on the device's SM count, the bit width and the group size). Returns
+ * current device, for any bit width, group size and scale storage (the
+ * split count depends on the device's SM count, the bit width and the kernel
+ * these select; the partials hold D floats per split). Returns
  * 0 when the decode runs as a single split per (batch, KV head) and needs no
  * workspace, and 0 for invalid sizes. Host only (reads the device's SM count
  * once).
