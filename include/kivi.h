@@ -253,6 +253,23 @@ kivi_status kivi_fake_quant_kv(const void* k_f16, const void* v_f16, int BH, int
 size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, int D);
 
 /*
+ * The split plan kivi_decode_attend takes for these arguments (bits may carry
+ * KIVI_SCALE_F16), for inspection and capacity planning. Host only; reads the
+ * device's SM count once. info (host, 7 ints) receives:
+ *   [0] kernel: 0 one warp per tile, 1 warp pairs (small batches; group size
+ *       32, head dim 128, fp32 scales, 1, 2 or 4 query heads per KV head)
+ *   [1] n_split: CTAs per head group, merged in the same launch
+ *   [2] tiles per warp (per warp pair for the pair kernel)
+ *   [3] warps per CTA
+ *   [4] query sub-groups per KV head (1, or ceil(Hq/Hkv / 4))
+ *   [5] tiles per head group: ceil(S_q / 32) store + ceil(n_res / 16) residual
+ *   [6] tiles per split
+ * Errors: as kivi_decode_attend's argument checks (no pointers but info).
+ */
+kivi_status kivi_decode_plan_info(int B, int Hq, int Hkv, int S_q, int n_res, int D, int group_size, int bits,
+                                  int* info);
+
+/*
  * Zero the merge counters of a fresh decode workspace: the first
  * min(workspace_bytes, KIVI_DECODE_COUNTER_BYTES) bytes, by an asynchronous
  * memset on `stream`. Needed once per workspace, before its first decode.

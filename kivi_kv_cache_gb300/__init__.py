@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
             "kivi_fake_quant_values": ([P, I, I, I, I, I, I, I, P, I, IP, P], I),
             "kivi_fake_quant_kv": ([P, P, I, I, I, I, I, I, I, P, P, I, IP, P], I),
             "kivi_decode_workspace_size": ([I, I, I, I, I, I], Z),
+            "kivi_decode_plan_info": ([I, I, I, I, I, I, I, I, IP], I),
             "kivi_decode_workspace_init": ([P, Z, P], I),
             "kivi_decode_attend": ([P, P, P, P, P, P, P, I, I, P, P, I, I, I, I, I, I, I, I, F, P, P, Z, P], I),
         }
@@ -307,6 +308,17 @@ def kivi_fake_quant_kv(k, v, residual_length: int, kout=None, vout=None, G: int 
 
 def kivi_decode_workspace_size(B: int, Hq: int, Hkv: int, S_q: int, n_res: int, D: int = 128) -> int:
     return lib().kivi_decode_workspace_size(B, Hq, Hkv, S_q, n_res, D)
+
+
+def kivi_decode_plan_info(B: int, Hq: int, Hkv: int, S_q: int, n_res: int, D: int = 128, G: int = 32,
+                          bits: int = 4, scale_f16: bool = False) -> dict:
+    """The split plan kivi_decode_attend takes for these arguments (host only)."""
+    info = (ctypes.c_int * 7)()
+    st = lib().kivi_decode_plan_info(B, Hq, Hkv, S_q, n_res, D, G, bits | (KIVI_SCALE_F16 if scale_f16 else 0),
+                                     ctypes.cast(info, ctypes.POINTER(ctypes.c_int)))
+    _check("kivi_decode_plan_info", st)
+    keys = ("pair_kernel", "n_split", "tiles_per_warp", "warps_per_cta", "q_sub", "n_tiles", "tiles_per_split")
+    return dict(zip(keys, list(info)))
 
 
 def kivi_decode_workspace_init(workspace, stream=None) -> None:

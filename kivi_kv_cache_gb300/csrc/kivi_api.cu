@@ -478,6 +478,28 @@ size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, in
     return w;
 }
 
+kivi_status kivi_decode_plan_info(int B, int Hq, int Hkv, int S_q, int n_res, int D, int group_size, int bits,
+                                  int* info) {
+    const bool hs = scale_f16_of(bits);
+    bits = width_of(bits);
+    kivi_status st = shape_check(D, group_size, bits);
+    if (st != KIVI_OK) return st;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S_q < 0 || n_res < 0 || S_q + n_res == 0)
+        return KIVI_ERR_INVALID_ARG;
+    if (Hq / Hkv > 64) return KIVI_ERR_UNSUPPORTED;
+    if (!info) return KIVI_ERR_INVALID_ARG;
+    // the plan kivi_decode_attend takes for these arguments
+    const DecodePlan p = make_plan(B, Hkv, Hq, S_q, n_res, bits, group_size == kG && D == kD && !hs, D);
+    info[0] = p.pair_kernel;
+    info[1] = p.n_split;
+    info[2] = p.tiles_per_warp;
+    info[3] = p.pair_kernel ? 2 * kPairsPerCta : p.warps_per_cta;
+    info[4] = p.q_sub;
+    info[5] = p.n_tiles;
+    info[6] = p.tiles_per_split;
+    return KIVI_OK;
+}
+
 kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const float* kscale,
                                const void* kzero_f16, const void* vcodes_u8, const float* vscale,
                                const void* vzero_f16, int S_q, int s_cap, const void* k_res_f16,

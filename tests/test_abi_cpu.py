@@ -217,3 +217,46 @@ def test_every_plan_fits_the_noalloc_scratch(L):
     assert 3 << 20 < worst[128] <= 4 * 1024 * 1024
     assert worst[64] < worst[128] < worst[256]
     assert 6 << 20 < worst[256] <= 8 * 1024 * 1024
+
+
+def test_decode_plan_rules(L):
+    """The decode's split plan (kivi_decode_plan_info; planned for 152 SMs
+    without a device) follows its rules on a grid of shapes: splits cover the
+    tiles without an empty split, the warp-pair kernel only for group size 32,
+    head dim 128, fp32 scales and 1, 2 or 4 heads per KV head, query
+    sub-groups of 4, one split per head group beyond the merge counters, and
+    a workspace at least as large as the plan's partials."""
+    seen_pair = seen_mma = seen_one_split = 0
+    for B in (1, 4, 32, 256, 2048):
+        for hkv, gq in ((8, 4), (8, 1), (2, 8), (8, 3), (1, 12)):
+            for S_q, n_res in ((0, 37), (2080, 158), (4032, 64), (16256, 128)):
+                for D, G, hs in ((128, 32, False), (128, 64, False), (64, 32, False), (256, 128, False),
+                                 (128, 32, True)):
+                    p = kv.kivi_decode_plan_info(B, hkv * gq, hkv, S_q, n_res, D, G, 4, hs)
+                    assert p["n_tiles"] == -(-S_q // 32) + -(-n_res // 16)
+                    assert p["n_split"] * p["tiles_per_split"] >= p["n_tiles"]
+                    assert (p["n_split"] - 1) * p["tiles_per_split"] < p["n_tiles"]
+                    assert p["q_sub"] == (1 if gq in (1, 2, 4) else -(-gq // 4))
+                    if p["pair_kernel"]:
+                        seen_pair += 1
+                        assert (D, G, hs) == (128, 32, False) and gq in (1, 2, 4)
+                        assert p["warps_per_cta"] == 8
+                    else:
+                        seen_mma += 1
+                        assert p["warps_per_cta"] in (4, 8)
+                    if B * hkv * p["q_sub"] > 8192:
+                        seen_one_split += 1
+                        assert p["n_split"] == 1  # more head groups than merge counters: one split each
+                    ws = L.kivi_decode_workspace_size(B, hkv * gq, hkv, S_q, n_res, D)
+                    if p["n_split"] > 1:
+                        assert ws >= 32768 + B * hkv * gq * p["n_split"] * (D + 2) * 4
+    assert seen_pair and seen_mma and seen_one_split
+    # the qwen8b decode takes the warp-pair kernel; stores of another group
+    # size or head dim, or with fp16 scales, the one-warp-per-tile kernel
+    assert kv.kivi_decode_plan_info(1, 32, 8, 2080, 158)["pair_kernel"] == 1
+    for kw in ({"G": 64}, {"D": 64}, {"scale_f16": True}):
+        assert kv.kivi_decode_plan_info(1, 32, 8, 2080, 158, **kw)["pair_kernel"] == 0
+    with pytest.raises(kv.KiviError):
+        kv.kivi_decode_plan_info(1, 12, 8, 2080, 158)          # 12 / 8 heads
+    with pytest.raises(kv.KiviError):
+        kv.kivi_decode_plan_info(1, 32, 8, 2080, 158, D=64, G=128)
