@@ -54,5 +54,10 @@ int main(void)
            (int)kivi_decode_attend(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 2080, 2080, NULL, NULL, 158,
                                    160, 1, 8 * 65, 8, 128, 32, 4, 0.088f, NULL, NULL, 0, NULL));
     printf("workspace_init_null %d\n", (int)kivi_decode_workspace_init(NULL, 1024, NULL));
+    int info[7] = {0};
+    st = kivi_decode_plan_info(1, 32, 8, 2080, 158, 128, 32, 4, info);
+    printf("plan_qwen8b %d %d %d %d\n", (int)st, info[0], info[1], info[5]); /* status, pair kernel, splits, tiles */
+    st = kivi_decode_plan_info(1, 32, 8, 2080, 158, 128, 32, 4 | KIVI_SCALE_F16, info);
+    printf("plan_qwen8b_f16s %d %d\n", (int)st, info[0]);
     return 0;
 }

@@ -50,3 +50,12 @@ def test_c_client_argument_checks(client):
     assert int(client["decode_bad_group"]) == INVALID
     assert int(client["decode_too_many_heads"]) == UNSUPPORTED
     assert int(client["workspace_init_null"]) == INVALID
+
+
+def test_c_client_plan_info(client):
+    # the qwen8b decode (2080 packed + 158 fp16 tokens = 65 + 10 tiles per KV
+    # head) takes the warp-pair kernel, planned for 152 SMs without a device;
+    # with fp16 scales it takes the one-warp-per-tile kernel
+    st, pair, n_split, n_tiles = (int(x) for x in client["plan_qwen8b"].split())
+    assert (st, pair, n_tiles) == (OK, 1, 75) and n_split > 1
+    assert client["plan_qwen8b_f16s"] == "%d 0" % OK
