@@ -375,6 +375,35 @@ def test_quantizer_invariants(bits):
             assert s == 0 and np.all(c == 0)
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quantizer_invariants_scale_f16(bits):
+    """The fp16-scale option on random groups over six decades of magnitude:
+    the scale is numpy's binary16 rounding of the fp32-scale quantizer's scale;
+    codes stay in [0, 2^bits - 1]; whenever that scale is a normal fp16 number
+    the minimum codes to 0, the maximum to 2^bits - 1, and every
+    reconstruction lies within half a stored step (plus rounding)."""
+    rng = np.random.default_rng(17 + bits)
+    L = (1 << bits) - 1
+    normal = 0
+    for trial in range(300):
+        n = int(rng.integers(1, 65))
+        x = (rng.standard_normal(n) * 10 ** rng.uniform(-6, 3)).astype(np.float16).astype(np.float32)
+        c32, s32, _ = oracle.quantize_group(x, bits)
+        c, s, z = oracle.quantize_group(x, bits | oracle.SCALE_F16)
+        assert s == np.float32(np.float16(s32))
+        assert c.min() >= 0 and c.max() <= L and z == x.min()
+        if s >= 2.0 ** -14:
+            normal += 1
+            assert c[np.argmin(x)] == 0 and c[np.argmax(x)] == L
+            recon = c.astype(np.float32) * np.float32(s) + np.float32(z)
+            ulp32 = np.spacing(np.abs(x).max().astype(np.float32))
+            assert np.all(np.abs(recon - x) <= s / 2 + 4 * ulp32)
+            assert np.max(np.abs(c.astype(int) - c32.astype(int))) <= 1
+        elif s == 0:
+            assert np.all(c == 0)
+    assert normal > 150
+
+
 def test_grid_values_round_trip():
     # values on min + k*scale with dyadic scale are reproduced exactly
     rng = np.random.default_rng(3)
