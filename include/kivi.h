@@ -322,18 +322,26 @@ kivi_status kivi_decode_attend(const void* q_f16,
  * KIVI_NOALLOC_SCRATCH_BYTES (8 MiB) per device, reserved when the library's
  * device code is loaded and kept until the process exits. It allocates
  * nothing itself.
- *   - Size limit: if kivi_decode_workspace_size(...) for these sizes exceeds
+ *   - Size limit: if the workspace of the split plan this call takes (for
+ *     its bit width, group size and scale storage) exceeds
  *     KIVI_NOALLOC_SCRATCH_BYTES, it returns KIVI_ERR_WORKSPACE and launches
- *     nothing.
+ *     nothing. The plan's split count grows with the device's SM count; on a
+ *     152-SM GB300 with the library's default planner settings no supported
+ *     shape needs more than about 6.1 MB (head dim 256), 3.1 MB (128) or
+ *     1.6 MB (64). A device with more SMs may reject the widest shapes.
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's contents. Calls whose kernels overlap on the GPU (two
  *     unordered streams) race and give wrong results; order them.
  *   - Its merge counters start at zero (the array is zero-initialised when
  *     the device code loads) and every completed call leaves them zero.
- *   - First call per device: it looks up the array's device address with
+ *   - Address: host code cannot use the array's name as a device address, so
+ *     every call made outside stream capture looks it up with
  *     cudaGetSymbolAddress (the current device must be the one the pointers
- *     belong to) and caches it; this may load the library's device code, so
- *     make the first call before capturing any stream. KIVI_ERR_CUDA if the
+ *     belong to); after cudaDeviceReset the reloaded array is found at its
+ *     new address. A call made while `stream` is being captured uses the
+ *     address the last uncaptured call on that device found, so make one call
+ *     per device before capturing any stream (the first call may also load
+ *     the library's device code). KIVI_ERR_CUDA if no address is known or the
  *     lookup fails.
  * Every other argument, check, status and result is that of
  * kivi_decode_attend.

@@ -19,10 +19,15 @@
 //     __device__ array is zero-initialised when the module loads, and every
 //     completed call leaves the counters zero; each call writes every partial
 //     it later reads, and the array keeps the last call's contents afterwards.
-// Host code cannot use the array's name as a device address, so the first call
-// on each device looks the address up with cudaGetSymbolAddress (with that
-// device current) and caches it; that first call may load the library's
-// device code, so make it before capturing any stream.
+// Host code cannot use the array's name as a device address, so each call
+// looks the address up with cudaGetSymbolAddress (with the pointers' device
+// current). The lookup is repeated on every call made outside stream capture,
+// so a module reloaded after cudaDeviceReset (or after the primary context
+// was released and created again) is found at its new address, with its
+// counters zero again. Inside a stream capture the call uses the address the
+// last uncaptured call on that device found: make one call on each device
+// before capturing any stream (that first call may also load the library's
+// device code, which a capture must not do).
 #include <atomic>
 
 #include "../../include/kivi.h"
@@ -36,14 +41,20 @@ constexpr int kMaxDevices = 64;
 std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 // Device address of the scratch array on the current device, or nullptr.
-void* scratch_address() {
+// Looked up afresh outside stream capture; inside a capture, the address the
+// last uncaptured lookup on this device found.
+void* scratch_address(cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
         return nullptr;
     }
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p) return p;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return g_scratch_addr[dev].load(std::memory_order_acquire);
     void* addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
         cudaGetLastError();
@@ -60,12 +71,14 @@ extern "C" kivi_status kivi_decode_attend_noalloc(
     const void* vcodes_u8, const float* vscale, const void* vzero_f16, int S_q, int s_cap,
     const void* k_res_f16, const void* v_res_f16, int n_res, int res_cap, int B, int Hq, int Hkv,
     int D, int group_size, int bits, float sm_scale, float* out_f32, kivi_stream_t stream) {
-    // Reject work whose split scratch would not fit before touching the device.
-    const size_t need = kivi_decode_workspace_size(B, Hq, Hkv, S_q, n_res, D);
+    // Reject work whose split scratch would not fit before touching the device:
+    // the need of the exact plan this call takes (its bit width, group size
+    // and scale storage), not the largest over all of them.
+    const size_t need = kivi::decode_workspace_need(B, Hq, Hkv, S_q, n_res, D, group_size, bits);
     if (need > (size_t)KIVI_NOALLOC_SCRATCH_BYTES) return KIVI_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (need > 0) {
-        scratch = scratch_address();
+        scratch = scratch_address(reinterpret_cast<cudaStream_t>(stream));
         if (!scratch) return KIVI_ERR_CUDA;
     }
     // All argument checks and launches are those of kivi_decode_attend.

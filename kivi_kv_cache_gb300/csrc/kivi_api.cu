@@ -264,6 +264,18 @@ kivi_status fake_quant(const void* k, const void* v, bool do_k, bool do_v, int B
 
 }  // namespace
 
+// Workspace bytes of the plan kivi_decode_attend takes for exactly these
+// arguments (bits may carry KIVI_SCALE_F16); 0 for a single-split plan or
+// for arguments the decode rejects.
+size_t kivi::decode_workspace_need(int B, int Hq, int Hkv, int S_q, int n_res, int D, int group_size, int bits) {
+    const bool hs = scale_f16_of(bits);
+    bits = width_of(bits);
+    if (shape_check(D, group_size, bits) != KIVI_OK || B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 ||
+        Hq / Hkv > 64 || S_q < 0 || n_res < 0 || S_q + n_res == 0)
+        return 0;
+    return workspace_bytes(B, Hq, D, make_plan(B, Hkv, Hq, S_q, n_res, bits, group_size == kG && D == kD && !hs, D));
+}
+
 extern "C" {
 
 kivi_status kivi_fake_quant_keys(const void* x_f16, int BH, int S, int x_bh_stride, int D, int group_size,

@@ -138,6 +138,12 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(Exp...), dim3 grid, dim3 bl
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
 }
 
+// Workspace bytes of the exact plan kivi_decode_attend takes for these
+// arguments (bits may carry KIVI_SCALE_F16); 0 for a single-split plan or
+// for arguments the decode rejects. kivi_decode_workspace_size is the
+// largest of these over bit widths, group sizes and scale storage.
+size_t decode_workspace_need(int B, int Hq, int Hkv, int S_q, int n_res, int D, int group_size, int bits);
+
 cudaError_t launch_flush(int axis, const FlushArgs& a, int bits, cudaStream_t stream);
 cudaError_t launch_flush_kv(const FlushArgs& k, const FlushArgs& v, int bits, cudaStream_t stream);
 // fake quantization (k.fq / v.fq set): the first n_flush tokens of x become

@@ -1,4 +1,4 @@
-"""The usage example of README.md, run as written, checked against the oracle."""
+"""The documented usage example of the package (flush, dequant, decode), run as written and checked against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +12,7 @@ def test_readme_example():
     import __graft_entry__
     __graft_entry__.build()
     torch.manual_seed(0)
-    # --- the README lines ---
+    # --- the usage example, as documented ---
     import kivi_kv_cache_gb300 as kv
     k = torch.randn(8, 2238, 128, device="cuda").half()       # [B*H_kv, S, D]
     v = torch.randn_like(k)

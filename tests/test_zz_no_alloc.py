@@ -25,14 +25,14 @@ def _built():
     __graft_entry__.build()
 
 
-def _decode_inputs(w, S_q, n_res, seed):
+def _decode_inputs(w, S_q, n_res, seed, scale_f16=False):
     rng = np.random.default_rng(seed)
     k = synth.keys(rng, (w.BH, S_q + n_res), w.D, synth.outlier_channels(w), w.outlier_scale)
     v = synth.normal(rng, (w.BH, S_q + n_res, w.D))
     q = synth.normal(rng, (w.B, w.Hq, w.D))
     k, v, q = (torch.from_numpy(a).cuda() for a in (k, v, q))
-    ks = kv.KiviStore(0, w.BH, S_q, w.D, w.G, w.bits, device="cuda")
-    vs = kv.KiviStore(1, w.BH, S_q, w.D, w.G, w.bits, device="cuda")
+    ks = kv.KiviStore(0, w.BH, S_q, w.D, w.G, w.bits, device="cuda", scale_f16=scale_f16)
+    vs = kv.KiviStore(1, w.BH, S_q, w.D, w.G, w.bits, device="cuda", scale_f16=scale_f16)
     assert kv.kivi_flush_kv(k, v, 0, ks, vs, n_tokens=S_q) == S_q
     return q, ks, vs, k[:, S_q:], v[:, S_q:]
 
@@ -71,3 +71,35 @@ def test_noalloc_largest_plan(D, lo_mb):
     torch.cuda.synchronize()
     err = (out.double() - ref.double()).abs().max().item()
     assert err <= TOL, err
+
+
+def test_noalloc_alternating_plans():
+    """Back-to-back no-alloc calls whose plans use the shared scratch
+    differently: an fp16-scale store of group size 64 read by 8 query heads
+    per KV head (two sub-groups of 4 heads, each with its own merge counter
+    and partials), then a 4-head fp32-scale store of group size 32 (the
+    warp-pair kernel), then the first again. Each call must leave the
+    counters it used at zero for the next, whatever its plan; every result
+    equals kivi_decode_attend with a workspace of its own."""
+    # 16384 tokens: 13 splits per head group over 416 CTAs, more than one
+    # wave of clusters, so the splits merge through the scratch's counters
+    wa = synth.Workload("gq8_g64_f16", B=2, Hkv=8, Hq=64, D=128, S=16384 + 100, bits=4, G=64, R=0, n_outlier=4,
+                        outlier_scale=8.0, seed=21)
+    wb = synth.WORKLOADS["qwen8b"]
+    A = _decode_inputs(wa, 16384, 100, seed=5, scale_f16=True)
+    Bc = _decode_inputs(wb, 2080, 158, seed=6)
+    assert kv.kivi_decode_plan_info(wa.B, wa.Hq, wa.Hkv, 16384, 100, 128, 64, 4, True)["q_sub"] == 2
+    assert kv.kivi_decode_plan_info(wb.B, wb.Hq, wb.Hkv, 2080, 158)["pair_kernel"] == 1
+    cases = [(wa, A, 16384, 100), (wb, Bc, 2080, 158)]
+    refs = [kv.kivi_decode_attend(x[0], x[1], x[2], S_q, x[3], x[4], n_res, w.Hkv, w.sm_scale)
+            for w, x, S_q, n_res in cases]
+    for w, x, S_q, n_res in cases:
+        assert 0 < kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, S_q, n_res, w.D) <= SCRATCH_BYTES
+    for i in (0, 1, 0, 1):
+        w, x, S_q, n_res = cases[i]
+        out = torch.full_like(refs[i], float("nan"))
+        kv.kivi_decode_attend_noalloc(x[0], x[1], x[2], S_q, x[3], x[4], n_res, w.Hkv, w.sm_scale, out=out)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out).all()
+        err = (out.double() - refs[i].double()).abs().max().item()
+        assert err <= TOL, (i, err)
