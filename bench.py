@@ -1,11 +1,12 @@
 #!/usr/bin/env python3
 """KIVI hot-path benchmark on GB300.
 
-One step = one pass of the whole hot path over one batch of the Qwen3-8B-like
-single-layer workload (B=1, H_kv=8, 32 query heads, D=128, 2238-token prompt,
-4-bit, G=32, residual_length=128):
-  1. flush the oldest 2080 tokens of K and V into the packed store (one launch),
-  2. append the 158-token fp16 tail to the K and V residual windows (one launch),
+One step = one pass of the whole hot path over one batch of the long-context
+2-bit workload (B=1, H_kv=8, 32 query heads, D=128, S=32768, 2-bit, G=32,
+residual_length=128), the single-sequence point (B=1, H_kv=8, S_kv >= 4096)
+that the throughput targets are stated at:
+  1. flush the oldest 32640 tokens of K and V into the packed store (one launch),
+  2. append the 128-token fp16 tail to the K and V residual windows (one launch),
   3. dequantize the packed K and V stores back to fp16 (one launch),
   4. fused dequantize-and-attend decode of one query token per head (split over
      the cached tokens; the last CTA of each head merges the splits).
@@ -17,7 +18,15 @@ several times the L2 cache, so no step finds its inputs in L2. Steps are
 captured in CUDA graphs of 8 consecutive steps on 8 distinct instances; the
 timed region replays them (K steps in all) between two CUDA events. Each op's
 average launch duration is timed the same way on graphs of 8 launches of that
-op alone.
+op alone, over at least 256 launches and 50 ms of device time.
+
+On one GPU the same JSON line also carries, each timed on its own:
+  * "qwen8b": the Qwen3-8B-like single-layer step (2238-token prompt, 4-bit);
+  * "batched_decode": 32 sequences of 4096 cached tokens, 30 steps that each
+    append one token per sequence and decode (tokens/s);
+  * "stream": 36 layers, B=16, context 1024 -> 4096, an incremental flush
+    whenever a window fills, a decode every layer-step (tokens/s);
+  * "decode_b1": single-sequence decodes at 4096, 8192 and 16384 tokens.
 
 --impl reference times the plain CPU oracle on the same workload and metric.
 """
@@ -29,6 +38,7 @@ import dataclasses
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -41,6 +51,9 @@ if ROOT not in sys.path:
 
 METRIC = "KIVI flush/dequant/decode-attend HBM GB/s (% of peak); decode tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+GRAPH_STEPS = 8
+MIN_OP_LAUNCHES = 256
+MIN_OP_MS = 50.0
 
 
 # --profile-case NAME: (op kind, B, S_q, n_res, bits); flush cases use the named workload
@@ -48,7 +61,10 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE_CASES = {
     "flush_long2bit": ("flush", 0, 0, 0, 2),
     "flush_long2bit_g128": ("flush", 0, 0, 0, 2),
+    "flush_qwen8b": ("flush", 0, 0, 0, 4),
+    "decode_b1_4k": ("decode", 1, 4096 - 128, 128, 4),
     "decode_b1_16k": ("decode", 1, 16384 - 128, 128, 4),
+    "decode_b1_32k_2bit": ("decode", 1, 32768 - 128, 128, 2),
     "decode_b32_4k": ("decode", 32, 4032, 64, 4),
 }
 
@@ -56,31 +72,44 @@ PROFILE_CASES = {
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20000)
-    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=16)
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    p.add_argument("--workload", default="qwen8b", choices=["tiny", "qwen8b", "long2bit"])
+    p.add_argument("--workload", default="long2bit", choices=["tiny", "qwen8b", "long2bit"])
     p.add_argument("--pool", type=int, default=0, help="instances in the rotating pool (0 = auto)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--e2e-streams", type=int, default=2,
                    help="streams the end-to-end instances alternate between (copies of one overlap the others)")
-    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the qwen8b, batched, stream and B=1 decode sub-objects of the line")
     p.add_argument("--hashes", action="store_true", help="print the source hash of each op and exit")
     p.add_argument("--stream", action="store_true",
                    help="instead of the step line: the 36-layer streaming serving simulation (tokens/s)")
-    p.add_argument("--stream-steps", type=int, default=3072, help="decode steps of --stream (multiple of 32)")
+    p.add_argument("--stream-steps", type=int, default=3072, help="decode steps of the stream simulation "
+                                                                   "(multiple of 32)")
     p.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
                    help="run one op on one case a few times, untimed (a target for ncu captures)")
-    p.add_argument("--sweep", nargs="?", const="all", choices=["all", "decode", "flush"],
+    p.add_argument("--sweep", nargs="?", const="all", choices=["all", "decode", "flush", "twopass"],
                    help="instead of the step line: per-op GB/s at larger sizes and a decode S_kv sweep "
-                        "('decode': the decode cases only; 'flush': flush, dequant and fake quantization only)")
+                        "('decode': the decode cases only; 'flush': flush, dequant and fake quantization only; "
+                        "'twopass': the fused decode against dequantize-once + fp16 attend over S_kv x B)")
     return p.parse_args()
 
 
 # ---------------------------------------------------------------------------
 # workload accounting
 # ---------------------------------------------------------------------------
+
+def decode_bytes(B, Hkv, Hq, D, G, bits, S_q, n_res, meta_bytes=6) -> float:
+    """Algorithmic bytes of one decode: per (KV head, store token) the K and V
+    codes plus the key metadata (meta_bytes per channel per G tokens) and the
+    value metadata (meta_bytes per G-channel group); 4 D bytes per (KV head,
+    residual token); q (fp16) and out (fp32) once."""
+    per_tok = 2 * D * bits / 8 + D * meta_bytes / G + (D // G) * meta_bytes
+    return B * Hkv * S_q * per_tok + B * Hkv * n_res * D * 4 + B * Hq * D * 6
+
 
 def op_bytes(w, n_flush: int, n_res: int, meta_bytes: int = 6) -> dict:
     """Algorithmic HBM bytes per step, per op (each tensor read or written once).
@@ -90,12 +119,17 @@ def op_bytes(w, n_flush: int, n_res: int, meta_bytes: int = 6) -> dict:
     flush = 2 * el * (2 + packed)                 # K and V: read fp16, write codes + metadata
     dequant = 2 * el * (packed + 2)               # read codes + metadata, write fp16
     append = 2 * 2 * w.BH * n_res * w.D * 2       # K and V tail rows: read + write
-    # decode: per (kv head, store token) K+V codes + key metadata (6 B per channel
-    # per 32 tokens) + value metadata (6 B per 32-channel group)
-    per_tok = 2 * w.D * w.bits / 8 + w.D * meta_bytes / w.G + (w.D // w.G) * meta_bytes
-    decode = (w.BH * n_flush * per_tok + w.BH * n_res * w.D * 2 * 2
-              + w.B * w.Hq * w.D * 2 + w.B * w.Hq * w.D * 4)
+    decode = decode_bytes(w.B, w.Hkv, w.Hq, w.D, w.G, w.bits, n_flush, n_res, meta_bytes)
     return {"flush_kv": flush, "residual_append": append, "dequant_kv": dequant, "decode_attend": decode}
+
+
+def op_read_bytes(w, n_flush: int, n_res: int, meta_bytes: int = 6) -> dict:
+    """The read share of op_bytes (what a DRAM read counter should see)."""
+    el = w.BH * n_flush * w.D
+    packed = w.bits / 8 + meta_bytes / w.G
+    dec = decode_bytes(w.B, w.Hkv, w.Hq, w.D, w.G, w.bits, n_flush, n_res, meta_bytes) - w.B * w.Hq * w.D * 4
+    return {"flush_kv": 2 * el * 2, "residual_append": 2 * w.BH * n_res * w.D * 2, "dequant_kv": 2 * el * packed,
+            "decode_attend": dec}
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -134,15 +168,18 @@ def source_hash(files) -> str:
     return h.hexdigest()[:16]
 
 
-def read_traffic(files, op: str):
-    """DRAM bytes per launch of an op from an ncu capture (profiles/traffic.txt
-    lines 'op sha bytes'), or None if the op's sources changed since."""
+def read_traffic(files, op: str, workload: str):
+    """DRAM bytes per launch of an op at a workload from an ncu capture
+    (profiles/traffic.txt lines 'op workload sha read_bytes write_bytes'), as
+    {"read": r, "write": w}, or None if there is no capture of the op's
+    current sources at that workload."""
     try:
         sha = source_hash(files)
         for ln in open(os.path.join(ROOT, "profiles", "traffic.txt")):
             parts = ln.split()
-            if len(parts) >= 3 and not ln.startswith("#") and parts[0] == op and parts[1] == sha:
-                return float(parts[2])
+            if (len(parts) >= 5 and not ln.startswith("#") and parts[0] == op and parts[1] == workload
+                    and parts[2] == sha):
+                return {"read": float(parts[3]), "write": float(parts[4])}
     except Exception:
         pass
     return None
@@ -207,7 +244,54 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# the GB300 arm
+# device timing helpers
+# ---------------------------------------------------------------------------
+
+def capture(fn):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def time_graphs(graphs, launches_per_graph: int, min_launches: int = MIN_OP_LAUNCHES, min_ms: float = MIN_OP_MS):
+    """Mean device time (ms) per launch over replays of `graphs` in turn (each
+    graph holds launches_per_graph launches on distinct pool entries): at
+    least min_launches launches and min_ms of device time, CUDA events on the
+    current stream around the replays."""
+    import torch
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for g in graphs:
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    per_graph = max(e0.elapsed_time(e1) / len(graphs), 1e-4)
+    reps = max(len(graphs), math.ceil(min_launches / launches_per_graph), math.ceil(min_ms / per_graph))
+    e0.record()
+    for i in range(reps):
+        graphs[i % len(graphs)].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * launches_per_graph)
+
+
+def pool_count(bytes_each: float, l2: int, lo: int = 8, hi: int = 64) -> int:
+    """Independent pool entries (a multiple of 8) totalling more than 4x L2."""
+    return max(lo, min(hi, int(math.ceil(4 * l2 / max(bytes_each, 1) / 8)) * 8))
+
+
+def l2_bytes(dev) -> int:
+    import torch
+    return getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20)
+
+
+# ---------------------------------------------------------------------------
+# the single-layer step (flush, append, dequant, decode)
 # ---------------------------------------------------------------------------
 
 class Instance:
@@ -233,6 +317,19 @@ class Instance:
         self.side = torch.cuda.Stream(device=device)
         self.flushed = torch.cuda.Event()
 
+    def op(self, name):
+        kv, w = self.kv, self.w
+        if name == "flush_kv":
+            kv.kivi_flush_kv(self.k, self.v, w.R, self.kst, self.vst)
+        elif name == "residual_append":
+            kv.kivi_residual_append_kv(self.k[:, self.n_flush:], self.v[:, self.n_flush:], self.kres, self.vres, 0,
+                                       self.n_res)
+        elif name == "dequant_kv":
+            kv.kivi_dequant_kv(self.kst, self.vst, self.n_flush, kout=self.kdq, vout=self.vdq)
+        else:
+            kv.kivi_decode_attend(self.q, self.kst, self.vst, self.n_flush, self.kres, self.vres, self.n_res, w.Hkv,
+                                  w.sm_scale, out=self.out, workspace=self.ws)
+
     def step(self, join=True):
         """One pass of the hot path. The flush and the dequant run on the
         current stream; the residual append and the decode (which needs the
@@ -240,19 +337,16 @@ class Instance:
         stream joins the current one at the end (or, with join=False, when the
         caller joins it, so independent steps may overlap)."""
         import torch
-        kv, w = self.kv, self.w
         main = torch.cuda.current_stream()
         self.side.wait_stream(main)
         with torch.cuda.stream(self.side):
-            kv.kivi_residual_append_kv(self.k[:, self.n_flush:], self.v[:, self.n_flush:], self.kres, self.vres,
-                                       0, self.n_res)
-        kv.kivi_flush_kv(self.k, self.v, w.R, self.kst, self.vst)
+            self.op("residual_append")
+        self.op("flush_kv")
         self.flushed.record(main)
-        kv.kivi_dequant_kv(self.kst, self.vst, self.n_flush, kout=self.kdq, vout=self.vdq)
+        self.op("dequant_kv")
         with torch.cuda.stream(self.side):
             self.side.wait_event(self.flushed)
-            kv.kivi_decode_attend(self.q, self.kst, self.vst, self.n_flush, self.kres, self.vres, self.n_res,
-                                  w.Hkv, w.sm_scale, out=self.out, workspace=self.ws)
+            self.op("decode_attend")
         if join:
             main.wait_stream(self.side)
 
@@ -263,9 +357,8 @@ class Instance:
 
 
 OPS = ["flush_kv", "residual_append", "dequant_kv", "decode_attend"]
-GRAPH_STEPS = 8
 OP_KERNEL_FILES = {"flush_kv": ["flush.cu"], "residual_append": ["residual.cu"], "dequant_kv": ["dequant.cu"],
-                   "decode_attend": ["decode_pair.cu", "decode_merge.cuh", "decode_common.cuh"]}
+                   "decode_attend": ["decode_pair.cu", "decode_mma.cuh", "decode_merge.cuh", "decode_common.cuh"]}
 LAUNCHES = {"flush_kv": 1, "residual_append": 1, "dequant_kv": 1, "decode_attend": 1}
 
 
@@ -275,6 +368,285 @@ def workload_label(w) -> str:
             "(B=%d, H_kv=%d, Hq=%d, D=%d, S=%d, bits=%d, G=%d, residual_length=%d)"
             % (w.name, w.B, w.Hkv, w.Hq, w.D, w.S, w.bits, w.G, w.R))
 
+
+class StepBench:
+    """A rotating pool of instances of one workload, with CUDA graphs of
+    GRAPH_STEPS steps (and of GRAPH_STEPS launches of each op) over distinct
+    instances."""
+
+    def __init__(self, kv, synth, w, dev, rank, pool_arg=0):
+        self.kv, self.w, self.dev = kv, w, dev
+        probe = Instance(w, 1000 * rank + 0, dev, kv, synth)
+        self.inst_bytes = probe.nbytes()
+        l2 = l2_bytes(dev)
+        self.l2 = l2
+        pool = pool_arg or int(min(64, max(2, math.ceil(4 * l2 / self.inst_bytes))))
+        self.pool = max(GRAPH_STEPS, (pool + GRAPH_STEPS - 1) // GRAPH_STEPS * GRAPH_STEPS)
+        self.insts = [probe] + [Instance(w, 1000 * rank + i, dev, kv, synth) for i in range(1, self.pool)]
+        self.n_flush, self.n_res = probe.n_flush, probe.n_res
+
+    def warm_and_capture(self, warmup):
+        import torch
+        for i in range(max(1, warmup)):
+            self.insts[i % self.pool].step()
+        torch.cuda.synchronize()
+
+        def steps(j):
+            group = self.insts[j * GRAPH_STEPS:(j + 1) * GRAPH_STEPS]
+            for inst in group:
+                inst.step(join=False)
+            for inst in group:
+                torch.cuda.current_stream().wait_stream(inst.side)
+
+        self.multi = [capture(lambda j=j: steps(j)) for j in range(self.pool // GRAPH_STEPS)]
+        self.single = [capture(lambda I=I: I.step()) for I in self.insts]
+        for i in range(max(1, warmup // GRAPH_STEPS)):
+            self.multi[i % len(self.multi)].replay()
+        torch.cuda.synchronize()
+
+    def time_steps(self, steps, before=None):
+        """Device ms of exactly `steps` steps between two CUDA events."""
+        import torch
+        if before:
+            before()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        n_multi, n_rest = divmod(steps, GRAPH_STEPS)
+        start.record()
+        for i in range(n_multi):
+            self.multi[i % len(self.multi)].replay()
+        for i in range(n_rest):
+            self.single[i % self.pool].replay()
+        end.record()
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
+
+    def op_times(self):
+        """Mean device ms per launch of each op: graphs of GRAPH_STEPS
+        launches of the op alone on consecutive instances of the pool, with
+        the step's launch configuration."""
+        op_ms = {}
+        for op in OPS:
+            gs = [capture(lambda j=j, op=op: [self.insts[j * GRAPH_STEPS + t].op(op) for t in range(GRAPH_STEPS)])
+                  for j in range(self.pool // GRAPH_STEPS)]
+            op_ms[op] = time_graphs(gs, GRAPH_STEPS)
+            del gs
+        return op_ms
+
+    def summary(self, op_ms, peak, steps=None, elapsed_ms=None, world=1):
+        w = self.w
+        ob = op_bytes(w, self.n_flush, self.n_res)
+        ops = {}
+        for op in OPS:
+            gbs = ob[op] / (op_ms[op] * 1e-3) / 1e9
+            ops[op] = {"us": round(op_ms[op] * 1e3, 3), "bytes": int(ob[op]), "GB/s": round(gbs, 1),
+                       "frac_of_peak": round(gbs / peak, 4)}
+        d = {"workload": workload_label(w), "n_flush": self.n_flush, "n_res": self.n_res, "ops": ops,
+             "step_bytes": int(sum(ob.values())),
+             "decode_tokens_per_s": round(w.B / (op_ms["decode_attend"] * 1e-3), 1),
+             "pool": "rotating pool of %d independent instances, %.0f MB total (L2 %d MB)"
+                     % (self.pool, self.pool * self.inst_bytes / 2 ** 20, self.l2 >> 20)}
+        if steps:
+            d["steps"] = steps
+            d["ms_per_step"] = round(elapsed_ms / steps, 6)
+            d["GB/s"] = round(job_gbs(world, sum(ob.values()), steps, elapsed_ms), 2)
+        return d
+
+
+# ---------------------------------------------------------------------------
+# decode cases, the batched decode and the streaming simulation
+# ---------------------------------------------------------------------------
+
+def time_decode_case(kv, synth, dev, B, S_q, n_res, bits, Hq=32, G=32, D=128, hs=False, Hkv=8, peak=None):
+    """Mean device time of one decode over a rotating pool of independent
+    stores (more than 4x L2 in total): graphs of 8 launches on distinct
+    entries, at least 256 launches and 50 ms."""
+    import torch
+    w = synth.Workload("decode", B=B, Hkv=Hkv, Hq=Hq, D=D, S=S_q + n_res, bits=bits, G=G, R=0,
+                       n_outlier=4, outlier_scale=8.0, seed=11)
+    s_cap = max(1, -(-S_q // G)) * G
+    meta = 4 if hs else 6
+    nbytes = decode_bytes(B, Hkv, w.Hq, D, G, bits, S_q, n_res, meta)
+    P = pool_count(nbytes, l2_bytes(dev))
+    entries = []
+    for i in range(P):
+        k, v, q = synth.prefill_inputs_torch(w, 9000 + i, dev)
+        gk = kv.KiviStore(0, w.BH, s_cap, D, G, bits, device=dev, scale_f16=hs)
+        gv = kv.KiviStore(1, w.BH, s_cap, D, G, bits, device=dev, scale_f16=hs)
+        if S_q > 0:
+            kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
+        kr = k[:, S_q:].contiguous()
+        vr = v[:, S_q:].contiguous()
+        out = torch.empty((B, w.Hq, D), dtype=torch.float32, device=dev)
+        need = kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, S_q, n_res, D)
+        entries.append((q, gk, gv, kr, vr, out, kv.kivi_decode_workspace(need, dev)))
+        del k, v
+    torch.cuda.synchronize()
+
+    def fn(e):
+        kv.kivi_decode_attend(e[0], e[1], e[2], S_q, e[3], e[4], n_res, w.Hkv, w.sm_scale, out=e[5], workspace=e[6])
+
+    for e in entries:
+        fn(e)
+    gs = [capture(lambda j=j: [fn(entries[8 * j + t]) for t in range(8)]) for j in range(P // 8)]
+    ms = time_graphs(gs, 8)
+    us = ms * 1e3
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    plan = kv.kivi_decode_plan_info(B, w.Hq, w.Hkv, S_q, n_res, D, G, bits, hs)
+    d = {"B": B, "Hkv": Hkv, "Hq": w.Hq, "S_kv": S_q + n_res, "S_q": S_q, "n_res": n_res, "bits": bits, "G": G,
+         "D": D, "scale_f16": hs, "us": round(us, 3), "bytes": int(nbytes), "GB/s": round(gbs, 1), "pool": P,
+         "tokens_per_s": round(B / (ms * 1e-3), 1), "plan": plan}
+    if peak:
+        d["frac_of_peak"] = round(gbs / peak, 4)
+    del entries, gs
+    torch.cuda.empty_cache()
+    return d
+
+
+def run_batched(kv, synth, dev, peak, instances=2):
+    """The batched decode workload: B=32 sequences, H_kv=8, 32 query heads,
+    4096 cached tokens each (4032 packed + 64 fp16: a layer cache with
+    residual_length 64 prefilled with 4096 tokens), then 30 steps that each
+    append one token per sequence (kivi_cache_append) and decode one query
+    token per head (kivi_cache_decode). Independent caches alternate step by
+    step (their stores total more than L2, as the layers of a model would),
+    so no step finds its store in L2. tokens/s = sequences * steps / time."""
+    import torch
+    w = synth.WORKLOADS["batched"]
+    R, steps = 64, w.steps
+    caches, toks, wss = [], [], []
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(32)
+    for i in range(instances):
+        k, v, _ = synth.prefill_inputs_torch(w, 31 + i, dev)
+        c = kv.KiviCache(w.BH, w.S_q, w.D, w.G, w.bits, R, device=dev)
+        assert c.prefill(k, v) == w.S_q and c.n_res == w.n_res
+        del k, v
+        nk = torch.randn((steps, w.BH, 1, w.D), generator=gen, device=dev).half()
+        nv = torch.randn((steps, w.BH, 1, w.D), generator=gen, device=dev).half()
+        qs = torch.randn((steps, w.B, w.Hq, w.D), generator=gen, device=dev).half()
+        out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+        need = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, w.S_q, w.n_res + steps, w.D)
+        caches.append(c)
+        toks.append((nk, nv, qs, out))
+        wss.append(kv.kivi_decode_workspace(need, dev))
+    states = [c.state() for c in caches]
+
+    def run_steps():
+        for s in range(steps):
+            for c, (nk, nv, qs, out), ws in zip(caches, toks, wss):
+                c.append(nk[s], nv[s])
+                c.decode(qs[s], w.Hkv, w.sm_scale, out=out, workspace=ws)
+
+    run_steps()  # eager warm-up (loads the kernels, sets attributes)
+    torch.cuda.synchronize()
+    for c, st in zip(caches, states):
+        c.set_state(*st)
+    g = capture(run_steps)  # every replay appends the same tokens at the same rows
+    for c, st in zip(caches, states):
+        c.set_state(*st)
+    ms = time_graphs([g], instances * steps, min_launches=1, min_ms=200.0)  # per (cache, step)
+    us = ms * 1e3
+    per_step = sum(decode_bytes(w.B, w.Hkv, w.Hq, w.D, w.G, w.bits, w.S_q, w.n_res + i + 1)
+                   + w.BH * w.D * 2 * 2 * 2 for i in range(steps)) / steps
+    gbs = per_step / (ms * 1e-3) / 1e9
+    return {"workload": "batched: B=32, H_kv=8, Hq=32, D=128, 4-bit, G=32, 4032 packed + 64 fp16 tokens, "
+                        "30 steps of append 1 token + decode",
+            "us_per_step": round(us, 3), "tokens_per_s": round(w.B / (ms * 1e-3), 1),
+            "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "bytes_per_step": int(per_step),
+            "l2": "%d independent caches alternate step by step (%.0f MB of stores)"
+                  % (instances, instances * w.BH * w.S_q * 176 / 2 ** 20)}
+
+
+def run_stream_sim(kv, synth, dev, peak, steps=3072, L=36):
+    """The streaming serving simulation of the KV-cache work: L layers, B=16,
+    H_kv=8, Hq=32, D=128, 4-bit, G=32, R=128, context growing from 1024
+    tokens by one token per step. Each layer-step is kivi_cache_append of the
+    new token's K and V (which flushes G tokens into the store and compacts
+    the window whenever it reaches R + G tokens) and kivi_cache_decode of one
+    query token per head. The launches of each 32-step flush cycle (all
+    layers) are captured in a CUDA graph beforehand; the timed region replays
+    them all. tokens/s = B * steps / time (KV-cache work only: no projections
+    or MLP)."""
+    import torch
+    B, Hkv, Hq, D, G, R, bits = 16, 8, 32, 128, 32, 128, 4
+    ctx0 = 1024
+    steps = (steps // G) * G
+    BH = B * Hkv
+    s_cap = ctx0 + steps
+    w = synth.Workload("stream", B=B, Hkv=Hkv, Hq=Hq, D=D, S=ctx0, bits=bits, G=G, R=R, n_outlier=4,
+                       outlier_scale=8.0, seed=5)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    new_k = torch.randn((BH, G, D), generator=gen, device=dev).to(torch.float16)  # tokens appended, cyclically
+    new_v = torch.randn((BH, G, D), generator=gen, device=dev).to(torch.float16)
+    qs = torch.randn((G, B, Hq, D), generator=gen, device=dev).to(torch.float16)
+    caches, outs = [], []
+    for layer in range(L):
+        k, v, _ = synth.prefill_inputs_torch(w, 100 + layer, dev)
+        c = kv.KiviCache(BH, s_cap, D, G, bits, R, device=dev)
+        c.prefill(k, v)
+        caches.append(c)
+        outs.append(torch.empty((B, Hq, D), dtype=torch.float32, device=dev))
+        del k, v
+    S_q0, n_res0 = caches[0].state()
+    need = max(kv.kivi_decode_workspace_size(B, Hq, Hkv, sq, nr, D)  # the largest plan of any step
+               for sq in range(S_q0, s_cap + 1, G) for nr in range(R, R + G + 1))
+    ws = kv.kivi_decode_workspace(need, dev)
+
+    def layer_step(c, out, i):
+        c.append(new_k[:, i % G:i % G + 1], new_v[:, i % G:i % G + 1])
+        c.decode(qs[i % G], Hkv, w.sm_scale, out=out, workspace=ws)
+
+    # one eager layer-step per layer loads the kernels; the counters are then
+    # restored (the graphs rewrite the appended rows)
+    snapshot = [c.state() for c in caches]
+    for c, out in zip(caches, outs):
+        layer_step(c, out, 0)
+    torch.cuda.synchronize()
+    for c, st in zip(caches, snapshot):
+        c.set_state(*st)
+    graphs = []
+    for cyc in range(steps // G):
+        graphs.append(capture(lambda cyc=cyc: [layer_step(c, out, cyc * G + j)
+                                               for j in range(G) for c, out in zip(caches, outs)]))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for g in graphs:
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    # algorithmic bytes: the decodes, the appends and the flushes (the window
+    # compaction moves are not counted)
+    total = 0.0
+    S_q, n_res = S_q0, n_res0
+    flush_b = 2 * BH * G * D * (2 + bits / 8 + 6 / G)
+    for i in range(steps):
+        n_res += 1
+        total += BH * D * 2 * 2 * 2
+        if n_res >= R + G:
+            S_q += G
+            n_res -= G
+            total += flush_b
+        total += decode_bytes(B, Hkv, Hq, D, G, bits, S_q, n_res)
+    total *= L
+    assert (S_q, n_res) == caches[0].state()
+    gbs = total / (ms * 1e-3) / 1e9
+    return {"workload": "stream: %d layers, B=16, H_kv=8, Hq=32, D=128, 4-bit, G=32, R=128, context %d -> %d"
+                        % (L, ctx0, ctx0 + steps),
+            "steps": steps, "ms": round(ms, 3), "tokens_per_s": round(B * steps / (ms * 1e-3), 1),
+            "us_per_layer_step": round(ms * 1e3 / (steps * L), 3), "flushes_per_layer": steps // G,
+            "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "note": "KV-cache work only (append, flush + compact every 32 steps, decode per layer-step); "
+                    "no projections or MLP; bytes exclude the window compaction"}
+
+
+# ---------------------------------------------------------------------------
+# the GB300 arm
+# ---------------------------------------------------------------------------
 
 def run_gb300(args, rank, world, local_rank):
     import torch
@@ -288,121 +660,55 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     w = synth.WORKLOADS[args.workload]
     props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    peak, peak_kind = measured_peaks()
 
-    probe = Instance(w, 1000 * rank + 0, dev, kv, synth)
-    inst_bytes = probe.nbytes()
-    # pool: a multiple of GRAPH_STEPS independent instances, >= 4x L2 in total
-    pool = args.pool or int(min(64, max(2, math.ceil(4 * l2 / inst_bytes))))
-    pool = max(GRAPH_STEPS, (pool + GRAPH_STEPS - 1) // GRAPH_STEPS * GRAPH_STEPS)
-    insts = [probe] + [Instance(w, 1000 * rank + i, dev, kv, synth) for i in range(1, pool)]
-    launches_per_step = sum(LAUNCHES.values())
-
-    # eager warm-up; then CUDA graphs of GRAPH_STEPS consecutive steps, each on
-    # its own instance (a graph launch costs microseconds; steps inside a graph
-    # follow each other with programmatic dependent launch), plus one-step
-    # graphs for a remainder of K that is not a multiple of GRAPH_STEPS
-    for i in range(max(1, args.warmup)):
-        insts[i % pool].step()
-    torch.cuda.synchronize()
-
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        return g
-
-    def steps(j):
-        group = insts[j * GRAPH_STEPS:(j + 1) * GRAPH_STEPS]
-        for inst in group:
-            inst.step(join=False)
-        for inst in group:
-            torch.cuda.current_stream().wait_stream(inst.side)
-
-    multi = [capture(lambda j=j: steps(j)) for j in range(pool // GRAPH_STEPS)]
-    single = [capture(lambda I=I: I.step()) for I in insts]
-    for i in range(max(1, args.warmup // GRAPH_STEPS)):
-        multi[i % len(multi)].replay()
-    torch.cuda.synchronize()
+    sb = StepBench(kv, synth, w, dev, rank, args.pool)
+    sb.warm_and_capture(args.warmup)
 
     gpu_id = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local_rank)
     clocks = ClockSampler(gpu_id)
     clocks.start()
     time.sleep(0.2)
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else None
+    elapsed_ms = sb.time_steps(args.steps, before=barrier)
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    n_multi, n_rest = divmod(args.steps, GRAPH_STEPS)
-    start.record()
-    for i in range(n_multi):
-        multi[i % len(multi)].replay()
-    for i in range(n_rest):
-        single[i % pool].replay()
-    end.record()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    # per-op average launch duration (CUDA events on the launching stream,
+    # graphs of GRAPH_STEPS launches of the op alone), in the same clock window
+    op_ms = sb.op_times()
     clock = clocks.stop()
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
 
-    # per-op average launch duration: CUDA events on the launching stream
-    # around replays of a graph of GRAPH_STEPS launches of that op alone, on
-    # consecutive instances of the same rotating pool and with the step's
-    # launch configuration
-    op_fns = {
-        "flush_kv": lambda I: kv.kivi_flush_kv(I.k, I.v, w.R, I.kst, I.vst),
-        "residual_append": lambda I: kv.kivi_residual_append_kv(I.k[:, I.n_flush:], I.v[:, I.n_flush:], I.kres,
-                                                                 I.vres, 0, I.n_res),
-        "dequant_kv": lambda I: kv.kivi_dequant_kv(I.kst, I.vst, I.n_flush, kout=I.kdq, vout=I.vdq),
-        "decode_attend": lambda I: kv.kivi_decode_attend(I.q, I.kst, I.vst, I.n_flush, I.kres, I.vres, I.n_res,
-                                                         w.Hkv, w.sm_scale, out=I.out, workspace=I.ws),
-    }
-    op_ms = {}
-    reps = max(4, min(200, args.steps // GRAPH_STEPS))
-    for op, fn in op_fns.items():
-        gs = [capture(lambda j=j, fn=fn: [fn(insts[j * GRAPH_STEPS + t]) for t in range(GRAPH_STEPS)])
-              for j in range(pool // GRAPH_STEPS)]
-        for g in gs:
-            g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(reps):
-            gs[i % len(gs)].replay()
-        e1.record()
-        torch.cuda.synchronize()
-        op_ms[op] = e0.elapsed_time(e1) / (reps * GRAPH_STEPS)
-        del gs
-
-    ob = op_bytes(w, probe.n_flush, probe.n_res)
+    summ = sb.summary(op_ms, peak)
+    ob = op_bytes(w, sb.n_flush, sb.n_res)
     step_bytes = sum(ob.values())
     ms_per_step = elapsed_ms / args.steps
     value = job_gbs(world, step_bytes, args.steps, elapsed_ms)
-    peak, peak_kind = measured_peaks()
-    ops = {}
-    for op in OPS:
-        gbs = ob[op] / (op_ms[op] * 1e-3) / 1e9
-        ops[op] = {"us": round(op_ms[op] * 1e3, 3), "bytes": int(ob[op]), "GB/s": round(gbs, 1),
-                   "frac_of_peak": round(gbs / peak, 4)}
     dom = max(OPS, key=lambda o: op_ms[o])
     achieved = ob[dom] / (op_ms[dom] * 1e-3) / 1e9
+    traffic = read_traffic(OP_KERNEL_FILES[dom], dom, w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                 "peak_kind": peak_kind + " hbm_gbs (copy, burst)", "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": read_traffic(OP_KERNEL_FILES[dom], dom)}
+                "frac": round(achieved / peak, 4),
+                "traffic": None if traffic is None else traffic["read"] + traffic["write"],
+                "traffic_read": None if traffic is None else traffic["read"],
+                "algorithmic_bytes": int(ob[dom]),
+                "algorithmic_read_bytes": int(op_read_bytes(w, sb.n_flush, sb.n_res)[dom]),
+                "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch at this workload; "
+                                "writes a launch leaves in L2 are not counted"}
 
     # end to end: host inputs (pinned) -> device, the step, result -> host.
     # Each instance's public-API calls (the copies of its K, V and q from
     # pinned host buffers, the step, the copy of its output back) are
     # captured once as a CUDA graph, as a serving loop would; graphs of
-    # independent instances alternate between two streams, so the copies of
-    # one step overlap the kernels of the other. Every step moves its inputs
+    # independent instances alternate between streams, so the copies of
+    # one step overlap the kernels of another. Every step moves its inputs
     # and its result through the copy engines inside the timed region.
     e2e = None
+    insts = sb.insts
     if args.e2e_steps > 0:
         nl = max(1, args.e2e_streams)
-        ne = min(pool, max(2 * nl, 4))  # instances: two per stream, at least 4
+        ne = min(sb.pool, max(2 * nl, 4))  # instances: two per stream, at least 4
         hk = [insts[i].k.cpu().pin_memory() for i in range(ne)]
         hv = [insts[i].v.cpu().pin_memory() for i in range(ne)]
         hq = [insts[i].q.cpu().pin_memory() for i in range(ne)]
@@ -450,39 +756,82 @@ def run_gb300(args, rank, world, local_rank):
                "ms_per_step": round(e2e_ms / args.e2e_steps, 5),
                "how": "per-instance CUDA graphs of the public-API calls: pinned H2D copies of K, V, q, the step, "
                       "D2H of the output; %d streams alternate instances so copies overlap kernels" % nl}
+        del e2e_graphs, hk, hv, hq
+    del sb, insts
+    torch.cuda.empty_cache()
+
+    # the other workloads (one GPU only; each timed on its own)
+    extra = {}
+    if world == 1 and not args.no_extra:
+        if w.name != "qwen8b":
+            sq = StepBench(kv, synth, synth.WORKLOADS["qwen8b"], dev, rank)
+            sq.warm_and_capture(16)
+            q_steps = 2000
+            q_ms = sq.time_steps(q_steps)
+            extra["qwen8b"] = sq.summary(sq.op_times(), peak, q_steps, q_ms)
+            del sq
+            torch.cuda.empty_cache()
+        extra["batched_decode"] = run_batched(kv, synth, dev, peak)
+        torch.cuda.empty_cache()
+        extra["stream"] = run_stream_sim(kv, synth, dev, peak, args.stream_steps)
+        torch.cuda.empty_cache()
+        extra["decode_b1"] = [time_decode_case(kv, synth, dev, 1, S - 128, 128, 4, peak=peak)
+                              for S in (4096, 8192, 16384)]
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle(w, args.cpu_seconds)
 
-    decode_s = op_ms["decode_attend"] * 1e-3
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": workload_label(w),
-                   "n_flush": probe.n_flush, "n_res": probe.n_res,
-                   "l2": "rotating pool of %d independent instances, %.0f MB total (L2 %d MB)"
-                         % (pool, pool * inst_bytes / 2 ** 20, l2 >> 20),
+                   "n_flush": summ["n_flush"], "n_res": summ["n_res"],
+                   "l2": summ["pool"],
                    "timing": "graphs of %d steps on distinct instances, K steps between CUDA events" % GRAPH_STEPS,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "ops": ops,
-        "decode_tokens_per_s": round(w.B / decode_s, 1),
+        "ops": summ["ops"],
+        "decode_tokens_per_s": summ["decode_tokens_per_s"],
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": sum(LAUNCHES.values()) * args.steps,
         "clocks": clock,
         "peak_hbm_gbs": peak,
-        "per_op_timing": "CUDA events around graphs of %d back-to-back launches of the op" % GRAPH_STEPS,
+        "per_op_timing": "CUDA events around graphs of %d back-to-back launches of the op on distinct instances, "
+                         "at least %d launches and %.0f ms per op" % (GRAPH_STEPS, MIN_OP_LAUNCHES, MIN_OP_MS),
     }
+    line.update(extra)
     return line
 
 
 # ---------------------------------------------------------------------------
 # the CPU oracle (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
+
+def cpu_model() -> str:
+    """The host CPU's model name from /proc/cpuinfo (implementer and part on
+    Arm, whose cpuinfo has no model name)."""
+    impl = part = None
+    try:
+        for ln in open("/proc/cpuinfo"):
+            key, _, val = ln.partition(":")
+            key, val = key.strip().lower(), val.strip()
+            if key == "model name":
+                return val
+            if key == "cpu implementer" and impl is None:
+                impl = val
+            if key == "cpu part" and part is None:
+                part = val
+    except OSError:
+        pass
+    if impl or part:
+        return "%s implementer %s part %s" % (platform.machine(), impl, part)
+    return platform.processor() or platform.machine()
+
 
 def cpu_oracle_step(w, k, v, q, threads):
     """One step of the workload on the CPU oracle, one KV head per thread."""
@@ -508,12 +857,30 @@ def cpu_oracle_step(w, k, v, q, threads):
         qh = np.ascontiguousarray(q[b:b + 1, hk * gq:(hk + 1) * gq])
         return oracle.decode_attend(qh, ks, vs, n, kres, vres, n_res, 1, w.sm_scale)
 
+    if threads == 1:
+        for bh in range(w.BH):
+            head(bh)
+        return
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(head, range(w.BH)))
 
 
-def cpu_oracle(w, seconds, steps=None):
-    """Time the oracle on host cores: whole steps until `seconds` (or `steps`)."""
+def _time_oracle(w, k, v, q, threads, seconds, min_steps=1):
+    done, times, t0 = 0, [], time.perf_counter()
+    while True:
+        t = time.perf_counter()
+        cpu_oracle_step(w, k, v, q, threads)
+        times.append(time.perf_counter() - t)
+        done += 1
+        if done >= min_steps and time.perf_counter() - t0 >= seconds:
+            break
+    return done, sum(times)
+
+
+def cpu_oracle(w, seconds):
+    """Time the oracle on the host cores: whole steps for about seconds / 2
+    with one KV head per thread on up to BH threads, then whole steps for
+    about seconds / 2 on one thread."""
     from kivi_kv_cache_gb300 import synth
     import oracle
     oracle.build()
@@ -522,21 +889,17 @@ def cpu_oracle(w, seconds, steps=None):
     cpu_oracle_step(w, k, v, q, threads)  # warm (page in, build)
     n = oracle.flush_count(w.S, w.R, w.G)
     step_bytes = sum(op_bytes(w, n, w.S - n).values())
-    done, t0 = 0, time.perf_counter()
-    times = []
-    while True:
-        t = time.perf_counter()
-        cpu_oracle_step(w, k, v, q, threads)
-        times.append(time.perf_counter() - t)
-        done += 1
-        if (steps is not None and done >= steps) or (steps is None and time.perf_counter() - t0 >= seconds):
-            break
-    total = sum(times)
+    done, total = _time_oracle(w, k, v, q, threads, seconds / 2)
+    done1, total1 = _time_oracle(w, k, v, q, 1, seconds / 2)
     return {"value": round(step_bytes * done / total / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
             "sample": "%d whole steps of the %s workload (C oracle, one KV head per thread), %.1f s"
                       % (done, w.name, total),
-            "ms_per_step": round(1e3 * total / done, 3)}
+            "ms_per_step": round(1e3 * total / done, 3),
+            "single_thread": {"value": round(step_bytes * done1 / total1 / 1e9, 4), "unit": "GB/s",
+                              "ms_per_step": round(1e3 * total1 / done1, 3),
+                              "sample": "%d whole steps on one thread, %.1f s" % (done1, total1)},
+            "cpu_model": cpu_model(), "host_cores": os.cpu_count()}
 
 
 def run_reference(args, rank, world):
@@ -546,14 +909,13 @@ def run_reference(args, rank, world):
     oracle.build()
     k, v, q = synth.prefill_inputs(w)
     threads = max(1, min(os.cpu_count() or 1, w.BH))
-    for _ in range(max(0, args.warmup)):
-        cpu_oracle_step(w, k, v, q, threads)
-    steps = max(1, args.steps)
-    # keep the reference arm to a bounded number of whole steps
     t = time.perf_counter()
-    cpu_oracle_step(w, k, v, q, threads)
+    cpu_oracle_step(w, k, v, q, threads)  # one warm-up step, also the size of a step
     one = time.perf_counter() - t
-    steps = max(1, min(steps, int(120.0 / max(one, 1e-3))))
+    for _ in range(max(0, min(args.warmup, 2) - 1)):
+        cpu_oracle_step(w, k, v, q, threads)
+    # a bounded sample of whole steps (about a minute at most)
+    steps = max(1, min(args.steps, int(60.0 / max(one, 1e-3))))
     t0 = time.perf_counter()
     for _ in range(steps):
         cpu_oracle_step(w, k, v, q, threads)
@@ -568,16 +930,21 @@ def run_reference(args, rank, world):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": workload_label(w), "note": "plain C CPU oracle as the reference arm"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
+
+# ---------------------------------------------------------------------------
+# sweeps
+# ---------------------------------------------------------------------------
 
 def run_sweep(args):
     """Per-op throughput at larger sizes (one JSON line per measurement).
 
     Each measurement: a rotating pool of independent inputs totalling more than
     4x L2, CUDA graphs of 8 launches of the op on distinct pool entries, CUDA
-    events around R graph replays; GB/s = algorithmic bytes / mean duration."""
+    events around at least 256 launches and 50 ms; GB/s = algorithmic bytes /
+    mean duration."""
     import torch
 
     import __graft_entry__
@@ -587,36 +954,20 @@ def run_sweep(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20)
+    l2 = l2_bytes(dev)
     peak, kind = measured_peaks()
 
-    def timed(fns, nbytes, label, extra):
-        gs = []
-        for j in range(len(fns) // 8):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                for f in fns[8 * j:8 * j + 8]:
-                    f()
-            gs.append(g)
-        for g in gs:
-            g.replay()
-        torch.cuda.synchronize()
-        reps = max(8, 400 // len(gs))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(reps):
-            gs[i % len(gs)].replay()
-        e1.record()
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * 8)
-        gbs = nbytes / (us * 1e-6) / 1e9
-        line = {"op": label, "us": round(us, 3), "bytes": int(nbytes), "GB/s": round(gbs, 1),
+    def emit(label, nbytes, ms, extra):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        line = {"op": label, "us": round(ms * 1e3, 3), "bytes": int(nbytes), "GB/s": round(gbs, 1),
                 "frac_of_peak": round(gbs / peak, 4), "peak": peak, "peak_kind": kind}
         line.update(extra)
         print(json.dumps(line), flush=True)
 
-    def pool_count(bytes_each):
-        return max(8, min(64, int(math.ceil(4 * l2 / max(bytes_each, 1) / 8)) * 8))
+    def timed(fns, nbytes, label, extra):
+        gs = [capture(lambda j=j: [f() for f in fns[8 * j:8 * j + 8]]) for j in range(len(fns) // 8)]
+        emit(label, nbytes, time_graphs(gs, 8), extra)
+        del gs
 
     # flush / dequant at the long-context 2-bit and qwen8b sizes; head dims 64
     # and 256 at the long 2-bit size with the same element count (16 or 4 KV heads)
@@ -630,7 +981,7 @@ def run_sweep(args):
         n = kv.kivi_flush_count(w.S, w.R, w.G)
         meta = 4 if hs else 6  # bytes of scale + zero per group
         per = w.BH * w.S * w.D * 2 * 2 + 2 * w.BH * n * (w.D * w.bits // 8 + w.D * meta // w.G) + w.BH * n * w.D * 4
-        P = pool_count(per)
+        P = pool_count(per, l2)
         ks, vs, kd, vd, xs = [], [], [], [], []
         for i in range(P):
             k, v, _ = synth.prefill_inputs_torch(w, 7000 + i, dev)
@@ -639,206 +990,101 @@ def run_sweep(args):
             vs.append(kv.KiviStore(1, w.BH, n, w.D, w.G, w.bits, device=dev, scale_f16=hs))
             kd.append(torch.empty((w.BH, n, w.D), dtype=torch.float16, device=dev))
             vd.append(torch.empty_like(kd[-1]))
-        ob = op_bytes(w, n, w.S - n, meta_bytes=4 if hs else 6)
+        ob = op_bytes(w, n, w.S - n, meta_bytes=meta)
+        ex = {"workload": name, "tokens": n, "bits": w.bits, "G": G, "D": D, "scale_f16": hs, "pool": P}
         timed([lambda i=i: kv.kivi_flush_kv(xs[i][0], xs[i][1], w.R, ks[i], vs[i]) for i in range(P)],
-              ob["flush_kv"], "flush_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "D": D, "scale_f16": hs,
-                                                   "pool": P})
+              ob["flush_kv"], "flush_kv", ex)
         timed([lambda i=i: kv.kivi_dequant_kv(ks[i], vs[i], n, kout=kd[i], vout=vd[i]) for i in range(P)],
-              ob["dequant_kv"], "dequant_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G, "D": D, "scale_f16": hs,
-                                                     "pool": P})
+              ob["dequant_kv"], "dequant_kv", ex)
         # fake quantization of the same tokens: read 2 B and write 2 B per element of K and V (the kd/vd
         # buffers hold the n flushed tokens, so the S - n fp16 tokens are not part of this launch)
         timed([lambda i=i: kv.kivi_fake_quant_kv(xs[i][0][:, :n], xs[i][1][:, :n], 0, kout=kd[i], vout=vd[i],
                                                  G=G, bits=w.bits, scale_f16=hs) for i in range(P)],
-              2 * w.BH * n * w.D * 4, "fake_quant_kv", {"workload": name, "tokens": n, "bits": w.bits, "G": G,
-                                                        "D": D, "scale_f16": hs, "pool": P})
+              2 * w.BH * n * w.D * 4, "fake_quant_kv", ex)
         del ks, vs, kd, vd, xs
         torch.cuda.empty_cache()
-    if args.sweep == "flush":
-        return
 
-    # decode over a packed store + fp16 residual
-    # (B, packed tokens, fp16 residual tokens, bits): the qwen8b decode, the long-context and batched
-    # decodes, and the streaming workload's S_kv sweep (128 / 512 / 2048 / 8192 / 16384 at B=1 and B=16)
-    cases = [(1, 2080, 158, 4), (1, 4096 - 128, 128, 4), (1, 8192 - 128, 128, 4), (1, 16384 - 128, 128, 4),
-             (1, 32768 - 128, 128, 2), (32, 4032, 64, 4), (16, 2048 - 128, 128, 4), (16, 16384 - 128, 128, 4),
-             (1, 0, 128, 4), (1, 512 - 128, 128, 4), (1, 2048 - 128, 128, 4),
-             (16, 0, 128, 4), (16, 512 - 128, 128, 4), (16, 8192 - 128, 128, 4)]
-    # 8, 6 and 3 query heads per KV head (sub-groups of up to 4 heads)
-    cases += [(1, 16384 - 128, 128, 4, 64), (32, 4032, 64, 4, 64), (1, 4096 - 128, 128, 4, 64),
-              (32, 4032, 64, 4, 48), (32, 4032, 64, 4, 24)]
-    # stores of group size 64 and 128
-    cases += [(1, 2080, 158, 4, 32, 64), (1, 16384 - 128, 128, 4, 32, 64), (1, 16384 - 128, 128, 4, 32, 128),
-              (32, 4032, 64, 4, 32, 64), (32, 4032, 64, 4, 32, 128), (1, 32768 - 128, 128, 2, 32, 128)]
-    # head dims 64 and 256
-    cases += [(1, 16384 - 128, 128, 4, 32, 32, 64), (32, 4032, 64, 4, 32, 32, 64),
-              (1, 16384 - 128, 128, 4, 32, 32, 256), (32, 4032, 64, 4, 32, 32, 256)]
-    # fp16 scale storage (160 bytes per 4-bit token instead of 176)
-    cases += [(1, 2080, 158, 4, 32, 32, 128, True), (1, 16384 - 128, 128, 4, 32, 32, 128, True),
-              (32, 4032, 64, 4, 32, 32, 128, True)]
-    for case in cases:
-        B, S_q, n_res, bits = case[:4]
-        Hq = case[4] if len(case) > 4 else 32
-        G = case[5] if len(case) > 5 else 32
-        D = case[6] if len(case) > 6 else 128
-        hs = case[7] if len(case) > 7 else False
-        w = synth.Workload("decode", B=B, Hkv=8, Hq=Hq, D=D, S=S_q + n_res, bits=bits, G=G, R=0,
-                           n_outlier=4, outlier_scale=8.0, seed=11)
-        s_cap = max(1, -(-S_q // G)) * G
-        meta = 4 if hs else 6  # bytes of scale + zero per group
-        per_tok = 2 * w.D * bits / 8 + w.D * meta / w.G + (w.D // w.G) * meta
-        nbytes = w.BH * S_q * per_tok + w.BH * n_res * w.D * 4 + B * w.Hq * w.D * 6
-        P = pool_count(nbytes)
-        entries = []
-        for i in range(P):
-            k, v, q = synth.prefill_inputs_torch(w, 9000 + i, dev)
-            gk = kv.KiviStore(0, w.BH, s_cap, w.D, w.G, bits, device=dev, scale_f16=hs)
-            gv = kv.KiviStore(1, w.BH, s_cap, w.D, w.G, bits, device=dev, scale_f16=hs)
-            if S_q > 0:
-                kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
-            kr = k[:, S_q:].contiguous()
-            vr = v[:, S_q:].contiguous()
-            out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device=dev)
-            need = kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, S_q, n_res, w.D)
-            ws = kv.kivi_decode_workspace(need, dev)
-            entries.append((q, gk, gv, kr, vr, out, ws))
-            del k, v
-        torch.cuda.synchronize()
-        fns = [lambda e=e: kv.kivi_decode_attend(e[0], e[1], e[2], S_q, e[3], e[4], n_res, w.Hkv, w.sm_scale,
-                                                 out=e[5], workspace=e[6]) for e in entries]
-        timed(fns, nbytes, "decode_attend", {"B": B, "Hkv": 8, "Hq": Hq, "S_kv": S_q + n_res, "bits": bits,
-                                             "G": G, "D": D, "scale_f16": hs, "pool": P, "tokens_per_s": None})
-        del entries, fns
-        torch.cuda.empty_cache()
+    if args.sweep in ("all", "decode"):
+        # decode over a packed store + fp16 residual
+        # (B, packed tokens, fp16 residual tokens, bits[, Hq, G, D, fp16 scales]): the qwen8b decode, the
+        # long-context and batched decodes, and the streaming workload's S_kv sweep (128 / 512 / 2048 /
+        # 8192 / 16384 at B=1 and B=16)
+        cases = [(1, 2080, 158, 4), (1, 4096 - 128, 128, 4), (1, 8192 - 128, 128, 4), (1, 16384 - 128, 128, 4),
+                 (1, 32768 - 128, 128, 2), (32, 4032, 64, 4), (16, 2048 - 128, 128, 4), (16, 16384 - 128, 128, 4),
+                 (1, 0, 128, 4), (1, 512 - 128, 128, 4), (1, 2048 - 128, 128, 4),
+                 (16, 0, 128, 4), (16, 512 - 128, 128, 4), (16, 8192 - 128, 128, 4)]
+        # 8, 6 and 3 query heads per KV head (sub-groups of up to 4 heads)
+        cases += [(1, 16384 - 128, 128, 4, 64), (32, 4032, 64, 4, 64), (1, 4096 - 128, 128, 4, 64),
+                  (32, 4032, 64, 4, 48), (32, 4032, 64, 4, 24)]
+        # stores of group size 64 and 128
+        cases += [(1, 2080, 158, 4, 32, 64), (1, 16384 - 128, 128, 4, 32, 64), (1, 16384 - 128, 128, 4, 32, 128),
+                  (32, 4032, 64, 4, 32, 64), (32, 4032, 64, 4, 32, 128), (1, 32768 - 128, 128, 2, 32, 128)]
+        # head dims 64 and 256
+        cases += [(1, 16384 - 128, 128, 4, 32, 32, 64), (32, 4032, 64, 4, 32, 32, 64),
+                  (1, 16384 - 128, 128, 4, 32, 32, 256), (32, 4032, 64, 4, 32, 32, 256)]
+        # fp16 scale storage (160 bytes per 4-bit token instead of 176)
+        cases += [(1, 2080, 158, 4, 32, 32, 128, True), (1, 16384 - 128, 128, 4, 32, 32, 128, True),
+                  (32, 4032, 64, 4, 32, 32, 128, True)]
+        for case in cases:
+            B, S_q, n_res, bits = case[:4]
+            d = time_decode_case(kv, synth, dev, B, S_q, n_res, bits, Hq=case[4] if len(case) > 4 else 32,
+                                 G=case[5] if len(case) > 5 else 32, D=case[6] if len(case) > 6 else 128,
+                                 hs=case[7] if len(case) > 7 else False, peak=peak)
+            d.update({"op": "decode_attend", "peak": peak, "peak_kind": kind})
+            print(json.dumps(d), flush=True)
+        print(json.dumps(dict(op="batched_decode_steps", **run_batched(kv, synth, dev, peak))), flush=True)
 
-    # two-pass "decode-once" against the fused decode (B=1 and B=32, 4032
-    # packed + 64 fp16 tokens): the store changes only when a flush folds G
-    # tokens in, so a two-pass decoder dequantizes it once per G steps and
-    # attends over an all-fp16 cache every step. Reported: the fused decode,
-    # the dequant, the fp16 attend (the same decode kernels over S_q = 0 and
-    # S_kv fp16 tokens) and the two-pass cost per step, attend + dequant / G.
-    for B in (1, 32):
-        S_q, n_res = 4032, 64
-        S = S_q + n_res
-        w = synth.Workload("twopass", B=B, Hkv=8, Hq=32, D=128, S=S, bits=4, G=32, R=0, n_outlier=4,
-                           outlier_scale=8.0, seed=12)
-        k, v, q = synth.prefill_inputs_torch(w, 41, dev)
-        gk = kv.KiviStore(0, w.BH, S_q, w.D, w.G, 4, device=dev)
-        gv = kv.KiviStore(1, w.BH, S_q, w.D, w.G, 4, device=dev)
-        kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
-        kr, vr = k[:, S_q:].contiguous(), v[:, S_q:].contiguous()
-        kd = torch.empty((w.BH, S_q, w.D), dtype=torch.float16, device=dev)
-        vd = torch.empty_like(kd)
-        kfull = torch.cat([kd, kr], dim=1)  # the fp16 cache the attend reads (contents: any fp16)
-        vfull = torch.cat([vd, vr], dim=1)
-        del k, v
-        out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device=dev)
-        ws = kv.kivi_decode_workspace(max(kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, S_q, n_res, w.D),
-                                          kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, 0, S, w.D)), dev)
-        per_tok = 2 * w.D * 4 / 8 + w.D * 6 / w.G + (w.D // w.G) * 6
-        fused_b = w.BH * S_q * per_tok + w.BH * n_res * w.D * 4 + B * w.Hq * w.D * 6
-        deq_b = 2 * w.BH * S_q * w.D * (2 + 4 / 8 + 6 / w.G)
-        att_b = w.BH * S * w.D * 4 + B * w.Hq * w.D * 6
-        res = {}
-        for label, fn, nbytes in (
-                ("fused", lambda: kv.kivi_decode_attend(q, gk, gv, S_q, kr, vr, n_res, w.Hkv, w.sm_scale, out=out,
-                                                        workspace=ws), fused_b),
-                ("dequant", lambda: kv.kivi_dequant_kv(gk, gv, S_q, kout=kd, vout=vd), deq_b),
-                ("fp16_attend", lambda: kv.kivi_decode_attend(q, gk, gv, 0, kfull, vfull, S, w.Hkv, w.sm_scale,
-                                                              out=out, workspace=ws), att_b)):
-            g = torch.cuda.CUDAGraph()
-            fn()
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g):
-                for _ in range(8):
-                    fn()
-            g.replay()
-            torch.cuda.synchronize()
-            reps = 25
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(reps):
-                g.replay()
-            e1.record()
-            torch.cuda.synchronize()
-            res[label] = e0.elapsed_time(e1) * 1e3 / (reps * 8)
-            res[label + "_GB/s"] = round(nbytes / (res[label] * 1e-6) / 1e9, 1)
-        two_pass = res["fp16_attend"] + res["dequant"] / w.G
-        print(json.dumps({"op": "decode_two_pass_vs_fused", "B": B, "S_kv": S, "bits": 4,
-                          "fused_us": round(res["fused"], 3), "dequant_us": round(res["dequant"], 3),
-                          "fp16_attend_us": round(res["fp16_attend"], 3),
-                          "two_pass_us_per_step": round(two_pass, 3),
-                          "fused_over_two_pass": round(two_pass / res["fused"], 3),
-                          "GB/s": {k2: v2 for k2, v2 in res.items() if k2.endswith("GB/s")},
-                          "note": "two-pass per step = fp16 attend + dequant / G (one dequant per G steps); "
-                                  "L2 not flushed between launches: one instance, 8 launches per graph"}),
-              flush=True)
-        del gk, gv, kr, vr, kd, vd, kfull, vfull, ws
-        torch.cuda.empty_cache()
+    if args.sweep in ("all", "twopass"):
+        run_twopass_sweep(kv, synth, dev, peak, kind)
 
-    # batched decode, 30 consecutive steps: B=32 sequences of 4032 packed + 64
-    # fp16 tokens; each step appends one token per sequence to the residual
-    # window (n_res 64 -> 93, no flush) and decodes one query token per head
-    B, S_q, n0, steps = 32, 4032, 64, 30
-    w = synth.Workload("batched", B=B, Hkv=8, Hq=32, D=128, S=S_q + n0 + steps, bits=4, G=32, R=0,
-                       n_outlier=4, outlier_scale=8.0, seed=4)
-    k, v, _ = synth.prefill_inputs_torch(w, 31, dev)
-    gk = kv.KiviStore(0, w.BH, S_q, w.D, w.G, 4, device=dev)
-    gv = kv.KiviStore(1, w.BH, S_q, w.D, w.G, 4, device=dev)
-    kv.kivi_flush_kv(k, v, 0, gk, gv, n_tokens=S_q)
-    res_cap = 128
-    kres = torch.zeros((w.BH, res_cap, w.D), dtype=torch.float16, device=dev)
-    vres = torch.zeros_like(kres)
-    kv.kivi_residual_append_kv(k[:, S_q:S_q + n0], v[:, S_q:S_q + n0], kres, vres, 0)
-    new_k = k[:, S_q + n0:].contiguous()
-    new_v = v[:, S_q + n0:].contiguous()
-    del k, v
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(32)
-    qs = torch.randn((steps, B, w.Hq, w.D), generator=gen, device=dev).to(torch.float16)
-    out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device=dev)
-    ws = kv.kivi_decode_workspace(kv.kivi_decode_workspace_size(B, w.Hq, w.Hkv, S_q, n0 + steps, w.D), dev)
 
-    def run_steps():
-        for i in range(steps):
-            kv.kivi_residual_append_kv(new_k[:, i:i + 1], new_v[:, i:i + 1], kres, vres, n0 + i)
-            kv.kivi_decode_attend(qs[i], gk, gv, S_q, kres[:, :n0 + i + 1], vres[:, :n0 + i + 1], n0 + i + 1,
-                                  w.Hkv, w.sm_scale, out=out, workspace=ws)
-
-    run_steps()  # eager warm-up (loads the kernels, sets attributes)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        run_steps()
-    g.replay()
-    torch.cuda.synchronize()
-    reps = 20
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / (reps * steps)
-    per_step = sum(B * w.Hkv * S_q * (2 * w.D * 4 / 8 + w.D * 6 / w.G + (w.D // w.G) * 6) +
-                   B * w.Hkv * (n0 + i + 1) * w.D * 4 + B * w.Hq * w.D * 6 + B * w.Hkv * w.D * 2 * 2 * 2
-                   for i in range(steps)) / steps
-    gbs = per_step / (us * 1e-6) / 1e9
-    print(json.dumps({"op": "batched_decode_steps", "B": B, "S_kv": S_q + n0, "steps": steps,
-                      "us_per_step": round(us, 3), "tokens_per_s": round(B / (us * 1e-6), 1),
-                      "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "peak": peak,
-                      "peak_kind": kind, "step": "append 1 token (K, V) + decode"}), flush=True)
+def run_twopass_sweep(kv, synth, dev, peak, kind):
+    """Two-pass "decode-once" against the fused decode over S_kv x B, every
+    arm over its own rotating pool of independent inputs (L2-cold). The
+    store changes only when a flush folds G tokens in, so a two-pass decoder
+    dequantizes it once per G steps and attends over an all-fp16 cache every
+    step: its cost per step is attend + dequant / G. The fp16 attend arm runs
+    the decode kernels over S_q = 0 and S_kv fp16 tokens. Also reported: the
+    two-pass cost at the HBM bound (its bytes at the measured peak), a lower
+    bound for any fp16 attend kernel."""
+    import torch
+    l2 = l2_bytes(dev)
+    G, bits, D, Hkv, Hq, n_res = 32, 4, 128, 8, 32, 64
+    for B in (1, 16, 32):
+        for S in (512, 1024, 2048, 3072, 4096, 8192):
+            S_q = S - n_res
+            fused = time_decode_case(kv, synth, dev, B, S_q, n_res, bits, peak=peak)
+            att = time_decode_case(kv, synth, dev, B, 0, S, bits, peak=peak)
+            # dequant of the S_q store tokens, rotating pool
+            w = synth.Workload("twopass", B=B, Hkv=Hkv, Hq=Hq, D=D, S=S, bits=bits, G=G, R=0, n_outlier=4,
+                               outlier_scale=8.0, seed=12)
+            deq_b = 2 * w.BH * S_q * D * (2 + bits / 8 + 6 / G)
+            P = pool_count(deq_b, l2)
+            ent = []
+            for i in range(P):
+                k, v, _ = synth.prefill_inputs_torch(w, 500 + i, dev, S=S_q)
+                gk = kv.KiviStore(0, w.BH, S_q, D, G, bits, device=dev)
+                gv = kv.KiviStore(1, w.BH, S_q, D, G, bits, device=dev)
+                kv.kivi_flush_kv(k, v, 0, gk, gv)
+                ent.append((gk, gv, k, v))  # the inputs' buffers take the fp16 output
+            gs = [capture(lambda j=j: [kv.kivi_dequant_kv(e[0], e[1], S_q, kout=e[2], vout=e[3])
+                                       for e in ent[8 * j:8 * j + 8]]) for j in range(P // 8)]
+            deq_ms = time_graphs(gs, 8)
+            del gs, ent
+            torch.cuda.empty_cache()
+            two = att["us"] + deq_ms * 1e3 / G
+            bound = (att["bytes"] + deq_b / G) / (peak * 1e9) * 1e6
+            print(json.dumps({"op": "decode_two_pass_vs_fused", "B": B, "S_kv": S, "S_q": S_q, "n_res": n_res,
+                              "bits": bits, "fused_us": fused["us"], "fp16_attend_us": att["us"],
+                              "dequant_us": round(deq_ms * 1e3, 3), "two_pass_us_per_step": round(two, 3),
+                              "two_pass_at_hbm_bound_us": round(bound, 3),
+                              "fused_over_two_pass": round(two / fused["us"], 3),
+                              "fused_over_two_pass_bound": round(bound / fused["us"], 3),
+                              "fused_GB/s": fused["GB/s"], "fp16_attend_GB/s": att["GB/s"], "peak": peak,
+                              "peak_kind": kind, "note": "every arm over a rotating pool (L2-cold)"}), flush=True)
 
 
 def run_stream(args):
-    """Streaming serving simulation of the KV-cache work: 36 layers, B=16,
-    H_kv=8, Hq=32, D=128, 4-bit, G=32, R=128, context growing from 1024 tokens
-    by one token per step. Every layer-step appends the new token's K and V to
-    the fp16 residual window, flushes G tokens into the packed store and
-    compacts the window when it reaches R + G tokens, and decodes one query
-    token per head. The launches of each 32-step flush cycle (all layers) are
-    captured in a CUDA graph beforehand; the timed region replays them all.
-    tokens/s = B * steps / time (KV-cache work only: no projections or MLP)."""
     import torch
 
     import __graft_entry__
@@ -849,78 +1095,9 @@ def run_stream(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peak, kind = measured_peaks()
-    L, B, Hkv, Hq, D, G, R, bits = 36, 16, 8, 32, 128, 32, 128, 4
-    ctx0 = 1024
-    steps = (args.stream_steps // G) * G
-    BH = B * Hkv
-    s_cap = ctx0 + steps
-    res_cap = R + G
-    w = synth.Workload("stream", B=B, Hkv=Hkv, Hq=Hq, D=D, S=ctx0, bits=bits, G=G, R=R, n_outlier=4,
-                       outlier_scale=8.0, seed=5)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(5)
-    new_k = torch.randn((BH, G, D), generator=gen, device=dev).to(torch.float16)  # tokens appended, cyclically
-    new_v = torch.randn((BH, G, D), generator=gen, device=dev).to(torch.float16)
-    qs = torch.randn((G, B, Hq, D), generator=gen, device=dev).to(torch.float16)
-    layers = []
-    for l in range(L):
-        k, v, _ = synth.prefill_inputs_torch(w, 100 + l, dev)
-        ks = kv.KiviStore(0, BH, s_cap, D, G, bits, device=dev)
-        vs = kv.KiviStore(1, BH, s_cap, D, G, bits, device=dev)
-        S_q = kv.kivi_flush_kv(k, v, R, ks, vs)
-        kres = torch.zeros((BH, res_cap, D), dtype=torch.float16, device=dev)
-        vres = torch.zeros_like(kres)
-        n_res = kv.kivi_residual_append_kv(k[:, S_q:], v[:, S_q:], kres, vres, 0)
-        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
-        layers.append({"ks": ks, "vs": vs, "kres": kres, "vres": vres, "S_q": S_q, "n_res": n_res, "out": out})
-        del k, v
-    need = max(kv.kivi_decode_workspace_size(B, Hq, Hkv, sq, nr, D)  # the largest plan of any step
-               for sq in range(ctx0 - R, s_cap + 1, G) for nr in range(R, R + G + 1))
-    ws = kv.kivi_decode_workspace(need, dev)
-
-    def layer_step(st, i):
-        st["n_res"] = kv.kivi_residual_append_kv(new_k[:, i % G:i % G + 1], new_v[:, i % G:i % G + 1], st["kres"],
-                                                 st["vres"], st["n_res"])
-        if st["n_res"] >= R + G:
-            n = kv.kivi_flush_kv(st["kres"], st["vres"], R, st["ks"], st["vs"], s_off=st["S_q"],
-                                 n_tokens=st["n_res"])
-            st["S_q"] += n
-            st["n_res"] = kv.kivi_residual_compact_kv(st["kres"], st["vres"], st["n_res"], n)
-        nr = st["n_res"]
-        kv.kivi_decode_attend(qs[i % G], st["ks"], st["vs"], st["S_q"], st["kres"][:, :nr], st["vres"][:, :nr],
-                              nr, Hkv, w.sm_scale, out=st["out"], workspace=ws)
-
-    # warm-up on a copy of nothing: one eager cycle would change the state, so
-    # run the first cycle eagerly only to load the kernels, then restart it
-    snapshot = [(st["S_q"], st["n_res"]) for st in layers]
-    for st in layers:
-        layer_step(st, 0)
-    torch.cuda.synchronize()
-    for st, (sq, nr) in zip(layers, snapshot):  # the appended token is overwritten by the replay
-        st["S_q"], st["n_res"] = sq, nr
-    graphs = []
-    for c in range(steps // G):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for j in range(G):
-                for st in layers:
-                    layer_step(st, c * G + j)
-        graphs.append(g)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for g in graphs:
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    print(json.dumps({"op": "stream_simulation", "layers": L, "B": B, "Hkv": Hkv, "Hq": Hq, "D": D, "bits": bits,
-                      "G": G, "R": R, "context": [ctx0, ctx0 + steps], "steps": steps,
-                      "ms": round(ms, 3), "tokens_per_s": round(B * steps / (ms * 1e-3), 1),
-                      "us_per_layer_step": round(ms * 1e3 / (steps * L), 3),
-                      "flushes_per_layer": steps // G, "peak": peak, "peak_kind": kind,
-                      "note": "KV-cache work only (append, flush, compact, decode per layer-step); "
-                              "no projections or MLP"}), flush=True)
+    d = run_stream_sim(kv, synth, dev, peak, args.stream_steps)
+    d.update({"op": "stream_simulation", "peak": peak, "peak_kind": kind})
+    print(json.dumps(d), flush=True)
 
 
 def run_profile_case(name: str, reps: int = 3):

@@ -310,6 +310,90 @@ kivi_status kivi_decode_attend(const void* q_f16,
                                void* workspace, size_t workspace_bytes, kivi_stream_t stream);
 
 /*
+ * One attention layer's KIVI cache ([F] "What we're actually optimizing":
+ * the newest residual_length tokens stay fp16, and the oldest whole groups
+ * are quantized into the packed store once enough accumulate; [F] "Four
+ * benchmarks that lied", Lie #2, counts those flushes per decode run). The
+ * struct holds the geometry, the caller-owned device buffers and two host
+ * counters; the calls below sequence the library's kernels and update the
+ * counters. The caller owns the struct and every buffer.
+ *   stores:  as kivi_flush_keys / kivi_flush_values, BH heads, capacity s_cap
+ *            (a multiple of group_size) tokens;
+ *   windows: fp16 [BH, res_cap, D] for keys and for values, with
+ *            res_cap >= residual_length + group_size;
+ *   S_q:     tokens in the stores (set 0 for an empty cache);
+ *   n_res:   tokens in the windows, oldest first (set 0 for an empty cache).
+ * Invariant kept by the calls: after each call, n_res < residual_length +
+ * group_size (a window that reaches R + G tokens flushes its oldest
+ * floor((n_res - R) / G) * G tokens into the stores at offset S_q and moves
+ * the rest to the front).
+ * Errors: every argument check (geometry, counters, pointers and alignment,
+ * store capacity for every flush the call will make) runs before the call's
+ * first launch; a failed check returns its status, launches nothing and
+ * leaves the counters unchanged. After a KIVI_ERR_CUDA the counters describe
+ * the launches that succeeded.
+ */
+typedef struct {
+    int BH;               /* sequences times KV heads */
+    int D;                /* head dim: 64, 128 or 256 */
+    int group_size;       /* 32, 64 or 128 (<= D) */
+    int bits;             /* 2 or 4, optionally ORed with KIVI_SCALE_F16 */
+    int residual_length;  /* R: fp16 tokens kept after a flush */
+    int s_cap;            /* store capacity in tokens */
+    int res_cap;          /* window capacity in tokens */
+    void* kcodes;         /* key store */
+    float* kscale;
+    void* kzero;
+    void* vcodes;         /* value store */
+    float* vscale;
+    void* vzero;
+    void* k_res;          /* fp16 windows */
+    void* v_res;
+    int S_q;              /* tokens in the stores */
+    int n_res;            /* tokens in the windows */
+} kivi_cache;
+
+/*
+ * Prefill into a cache whose windows are empty (n_res == 0): of the S tokens
+ * of k and v ([BH, S, D] fp16, x_bh_stride tokens between heads), the oldest
+ * n = kivi_flush_count(S, residual_length, group_size) are flushed straight
+ * from k and v into the stores at offset S_q (one launch), and the other
+ * S - n are copied into the windows. S_q += n, n_res = S - n; *n_flushed
+ * (may be NULL) receives n. With residual_length 0 and S not a multiple of
+ * group_size the last key group is ragged and the cache takes no further
+ * flushes (their store offset would not be a multiple of group_size).
+ * Errors: INVALID_ARG if n_res != 0, S < 0, x_bh_stride < S, the stores
+ * lack room, or a flush would start at an offset that is not a multiple of
+ * group_size.
+ */
+kivi_status kivi_cache_prefill(kivi_cache* cache, const void* k_f16, const void* v_f16, int x_bh_stride, int S,
+                               int* n_flushed, kivi_stream_t stream);
+
+/*
+ * Append n_new tokens (k, v: [BH, n_new, D] fp16, src_bh_stride tokens
+ * between heads) to the windows, oldest first, flushing as the rule above
+ * says. The tokens enter in pieces that fit the windows, each followed by
+ * the flush it triggers (one piece when res_cap >= residual_length +
+ * group_size + n_new). *n_flushed (may be NULL) receives the tokens flushed.
+ * One decode step of a serving loop is kivi_cache_append of one token
+ * followed by kivi_cache_decode.
+ * Errors: INVALID_ARG if n_new < 0, src_bh_stride < n_new, or a flush would
+ * overrun the stores or start at an offset that is not a multiple of
+ * group_size.
+ */
+kivi_status kivi_cache_append(kivi_cache* cache, const void* k_f16, const void* v_f16, int src_bh_stride,
+                              int n_new, int* n_flushed, kivi_stream_t stream);
+
+/*
+ * kivi_decode_attend over the cache's S_q store tokens and n_res window
+ * tokens, for B sequences with Hkv KV heads (B * Hkv == BH) and Hq query
+ * heads; every other argument, check and result is that of
+ * kivi_decode_attend. The counters are not changed.
+ */
+kivi_status kivi_cache_decode(const kivi_cache* cache, const void* q_f16, int B, int Hq, int Hkv, float sm_scale,
+                              float* out_f32, void* workspace, size_t workspace_bytes, kivi_stream_t stream);
+
+/*
  * kivi_decode_attend_noalloc -- the same decode as kivi_decode_attend, for
  * callers that cannot allocate device memory when they decode: serving
  * runtimes that hand out all of HBM to weights and KV-cache pages at start-up

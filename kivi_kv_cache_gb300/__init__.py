@@ -23,7 +23,7 @@ __all__ = [
     "kivi_residual_append", "kivi_residual_compact", "kivi_residual_append_kv", "kivi_residual_compact_kv",
     "kivi_fake_quant_keys", "kivi_fake_quant_values", "kivi_fake_quant_kv",
     "kivi_decode_workspace_size", "kivi_decode_workspace", "kivi_decode_workspace_init",
-    "kivi_decode_attend", "kivi_decode_attend_noalloc",
+    "kivi_decode_attend", "kivi_decode_attend_noalloc", "KiviCache",
 ]
 
 # KIVI_GB300_LIB: load the library from another path (e.g. a build with other
@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
             "kivi_decode_plan_info": ([I, I, I, I, I, I, I, I, IP], I),
             "kivi_decode_workspace_init": ([P, Z, P], I),
             "kivi_decode_attend": ([P, P, P, P, P, P, P, I, I, P, P, I, I, I, I, I, I, I, I, F, P, P, Z, P], I),
+            "kivi_cache_prefill": ([P, P, P, I, I, IP, P], I),
+            "kivi_cache_append": ([P, P, P, I, I, IP, P], I),
+            "kivi_cache_decode": ([P, P, I, I, I, F, P, P, Z, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -393,3 +396,83 @@ def kivi_decode_attend_noalloc(q, kstore: KiviStore, vstore: KiviStore, S_q: int
         float(sm_scale), _ptr(out), _stream(stream))
     _check("kivi_decode_attend_noalloc", st)
     return out
+
+
+class _CacheStruct(ctypes.Structure):
+    """The C struct kivi_cache (include/kivi.h), field for field."""
+    _fields_ = [("BH", ctypes.c_int), ("D", ctypes.c_int), ("group_size", ctypes.c_int), ("bits", ctypes.c_int),
+                ("residual_length", ctypes.c_int), ("s_cap", ctypes.c_int), ("res_cap", ctypes.c_int),
+                ("kcodes", ctypes.c_void_p), ("kscale", ctypes.c_void_p), ("kzero", ctypes.c_void_p),
+                ("vcodes", ctypes.c_void_p), ("vscale", ctypes.c_void_p), ("vzero", ctypes.c_void_p),
+                ("k_res", ctypes.c_void_p), ("v_res", ctypes.c_void_p), ("S_q", ctypes.c_int), ("n_res", ctypes.c_int)]
+
+
+class KiviCache:
+    """One attention layer's KIVI cache (C struct kivi_cache): packed key and
+    value stores of s_cap tokens, fp16 key and value windows of res_cap
+    tokens (default residual_length + group_size), and the counters S_q and
+    n_res, which the C calls update. torch allocates the buffers."""
+
+    def __init__(self, BH: int, s_cap: int, D: int = 128, group_size: int = 32, bits: int = 4,
+                 residual_length: int = 128, res_cap=None, device="cuda", scale_f16: bool = False):
+        import torch
+        res_cap = residual_length + group_size if res_cap is None else res_cap
+        self.kstore = KiviStore(0, BH, s_cap, D, group_size, bits, device=device, scale_f16=scale_f16)
+        self.vstore = KiviStore(1, BH, s_cap, D, group_size, bits, device=device, scale_f16=scale_f16)
+        self.k_res = torch.zeros((BH, res_cap, D), dtype=torch.float16, device=device)
+        self.v_res = torch.zeros_like(self.k_res)
+        ks, vs = self.kstore, self.vstore
+        self.c = _CacheStruct(BH, D, group_size, ks.abi_bits, residual_length, s_cap, res_cap,
+                              ks.codes.data_ptr(), ks.scale.data_ptr(), ks.zero.data_ptr(),
+                              vs.codes.data_ptr(), vs.scale.data_ptr(), vs.zero.data_ptr(),
+                              self.k_res.data_ptr(), self.v_res.data_ptr(), 0, 0)
+
+    @property
+    def S_q(self) -> int:
+        return self.c.S_q
+
+    @property
+    def n_res(self) -> int:
+        return self.c.n_res
+
+    def state(self):
+        """The counters (S_q, n_res), e.g. to restore them after a graph capture."""
+        return self.c.S_q, self.c.n_res
+
+    def set_state(self, S_q: int, n_res: int) -> None:
+        self.c.S_q, self.c.n_res = S_q, n_res
+
+    def prefill(self, k, v, n_tokens=None, stream=None) -> int:
+        """kivi_cache_prefill of k, v [BH, S, D] fp16; returns the tokens flushed."""
+        S = k.shape[1] if n_tokens is None else n_tokens
+        stride = _rows(k, self.c.D)
+        assert _rows(v, self.c.D) == stride
+        n = ctypes.c_int(0)
+        _check("kivi_cache_prefill", lib().kivi_cache_prefill(ctypes.byref(self.c), _ptr(k), _ptr(v), stride, S,
+                                                             ctypes.byref(n), _stream(stream)))
+        return n.value
+
+    def append(self, k, v, n_new=None, stream=None) -> int:
+        """kivi_cache_append of k, v [BH, n, D] fp16; returns the tokens flushed."""
+        n_new = k.shape[1] if n_new is None else n_new
+        stride = _rows(k, self.c.D)
+        assert _rows(v, self.c.D) == stride
+        n = ctypes.c_int(0)
+        _check("kivi_cache_append", lib().kivi_cache_append(ctypes.byref(self.c), _ptr(k), _ptr(v), stride, n_new,
+                                                           ctypes.byref(n), _stream(stream)))
+        return n.value
+
+    def decode(self, q, Hkv: int, sm_scale: float, out=None, workspace=None, stream=None):
+        """kivi_cache_decode: q [B, Hq, D] fp16 -> out [B, Hq, D] fp32."""
+        import torch
+        B, Hq, D = q.shape
+        if out is None:
+            out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+        if workspace is None:
+            need = kivi_decode_workspace_size(B, Hq, Hkv, self.c.S_q, self.c.n_res, D)
+            workspace = kivi_decode_workspace(need, q.device) if need > 0 else None
+        wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _check("kivi_cache_decode", lib().kivi_cache_decode(ctypes.byref(self.c), _ptr(q), B, Hq, Hkv,
+                                                           float(sm_scale), _ptr(out), _ptr(workspace), wbytes,
+                                                           _stream(stream)))
+        return out

@@ -21,7 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkivi_gb300.so")
 SOURCES = ["kivi_api.cu", "flush.cu", "dequant.cu", "decode_mma.cu", "decode_mma_f16s.cu", "decode_mma_d64.cu",
-           "decode_mma_d256.cu", "decode_mma_d256_f16s.cu", "decode_pair.cu", "residual.cu", "decode_noalloc.cu"]
+           "decode_mma_d256.cu", "decode_mma_d256_f16s.cu", "decode_pair.cu", "residual.cu", "decode_noalloc.cu",
+           "kivi_cache.cu"]
 HEADERS = ["kivi_device.cuh", "kivi_launch.h", "decode_merge.cuh", "decode_common.cuh", "decode_mma.cuh"]
 
 NVCC_FLAGS = [

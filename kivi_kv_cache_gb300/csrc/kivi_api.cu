@@ -264,6 +264,12 @@ kivi_status fake_quant(const void* k, const void* v, bool do_k, bool do_v, int B
 
 }  // namespace
 
+// KIVI_OK, or KIVI_ERR_UNSUPPORTED for a head dim, group size or bit width
+// (bits may carry KIVI_SCALE_F16) outside the compiled set.
+int kivi::shape_status(int D, int group_size, int bits) {
+    return (int)shape_check(D, group_size, width_of(bits));
+}
+
 // Workspace bytes of the plan kivi_decode_attend takes for exactly these
 // arguments (bits may carry KIVI_SCALE_F16); 0 for a single-split plan or
 // for arguments the decode rejects.

@@ -138,6 +138,10 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(Exp...), dim3 grid, dim3 bl
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
 }
 
+// KIVI_OK (0), or KIVI_ERR_UNSUPPORTED for a head dim, group size or bit
+// width (bits may carry KIVI_SCALE_F16) outside the compiled set.
+int shape_status(int D, int group_size, int bits);
+
 // Workspace bytes of the exact plan kivi_decode_attend takes for these
 // arguments (bits may carry KIVI_SCALE_F16); 0 for a single-split plan or
 // for arguments the decode rejects. kivi_decode_workspace_size is the

@@ -260,3 +260,61 @@ def test_decode_plan_rules(L):
         kv.kivi_decode_plan_info(1, 12, 8, 2080, 158)          # 12 / 8 heads
     with pytest.raises(kv.KiviError):
         kv.kivi_decode_plan_info(1, 32, 8, 2080, 158, D=64, G=128)
+
+
+def fake_cache(**kw):
+    """A kivi_cache struct over never-dereferenced 16-byte aligned addresses."""
+    c = kv._CacheStruct(8, 128, 32, 4, 128, 256, 160, *([FAKE] * 8), 0, 0)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@no_gpu
+def test_cache_rejects_bad_arguments_without_launching(L):
+    """Every check of kivi_cache_prefill / _append / _decode runs before the
+    first launch and leaves the counters unchanged: geometry, buffers,
+    counters, and room in the stores for every flush the call would make."""
+    n = ctypes.c_int(-7)
+
+    def prefill(c, S=200, stride=None, k=FAKE, v=FAKE):
+        return L.kivi_cache_prefill(ctypes.byref(c), k, v, S if stride is None else stride, S, ctypes.byref(n), None)
+
+    def append(c, n_new=1, k=FAKE, v=FAKE, stride=None):
+        return L.kivi_cache_append(ctypes.byref(c), k, v, n_new if stride is None else stride, n_new,
+                                   ctypes.byref(n), None)
+
+    assert prefill(fake_cache(res_cap=159)) == INVALID            # window < R + G
+    assert prefill(fake_cache(D=96)) == UNSUPPORTED
+    assert prefill(fake_cache(bits=3)) == UNSUPPORTED
+    assert prefill(fake_cache(group_size=0)) == INVALID
+    assert prefill(fake_cache(s_cap=250)) == INVALID              # not a multiple of G
+    assert prefill(fake_cache(S_q=288)) == INVALID                # S_q > s_cap
+    assert prefill(fake_cache(n_res=161)) == INVALID              # n_res > res_cap
+    assert prefill(fake_cache(k_res=None)) == INVALID
+    assert prefill(fake_cache(vzero=FAKE + 2)) == ALIGN
+    assert prefill(fake_cache(), k=FAKE + 8) == ALIGN
+    assert prefill(fake_cache(), k=None) == INVALID
+    assert prefill(fake_cache(), stride=100) == INVALID           # head stride < S
+    c = fake_cache(n_res=5)
+    assert prefill(c) == INVALID and (c.S_q, c.n_res) == (0, 5)   # windows not empty
+    c = fake_cache(S_q=224)
+    assert prefill(c, S=300) == INVALID and c.S_q == 224          # flush of 160 overruns the store
+    assert prefill(fake_cache(), S=0) == OK                       # nothing to do
+    # append: a full store cannot take the flush the 160th window token triggers
+    c = fake_cache(S_q=256, n_res=159)
+    assert append(c) == INVALID and (c.S_q, c.n_res) == (256, 159)
+    c = fake_cache(S_q=250, s_cap=512, n_res=159)                 # ragged store end: no further key flush
+    assert append(c) == INVALID and (c.S_q, c.n_res) == (250, 159)
+    # pieces: 340 tokens through a 160-token window would flush 288 tokens into a 256-token store
+    c = fake_cache(S_q=0, n_res=100)
+    assert append(c, n_new=340) == INVALID and (c.S_q, c.n_res) == (0, 100)
+    assert append(fake_cache(), n_new=2, stride=1) == INVALID     # head stride < n_new
+    assert append(fake_cache(), v=None) == INVALID
+    assert append(fake_cache(), k=FAKE + 4) == ALIGN
+    assert append(fake_cache(), n_new=0, k=None, v=None) == OK
+    # decode: B * Hkv must be the cache's BH
+    c = fake_cache(S_q=256, n_res=150)
+    assert L.kivi_cache_decode(ctypes.byref(c), FAKE, 2, 32, 8, 0.088, FAKE, FAKE, 1 << 30, None) == INVALID
+    assert L.kivi_cache_decode(ctypes.byref(c), FAKE, 1, 32, 8, 0.088, FAKE, None, 0, None) == WORKSPACE
+    assert L.kivi_cache_decode(None, FAKE, 1, 32, 8, 0.088, FAKE, FAKE, 1 << 30, None) == INVALID
