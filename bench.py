@@ -26,7 +26,9 @@ On one GPU the same JSON line also carries, each timed on its own:
     append one token per sequence and decode (tokens/s);
   * "stream": 36 layers, B=16, context 1024 -> 4096, an incremental flush
     whenever a window fills, a decode every layer-step (tokens/s);
-  * "decode_b1": single-sequence decodes at 4096, 8192 and 16384 tokens.
+  * "decode_b1": single-sequence decodes at 4096, 8192 and 16384 tokens
+    (4-bit) and 32768 (2-bit), plain and with KIVI_DECODE_STORE_READY (a
+    sequence of decodes: the preceding kernel never writes the store).
 
 --impl reference times the plain CPU oracle on the same workload and metric.
 """
@@ -458,10 +460,13 @@ class StepBench:
 # decode cases, the batched decode and the streaming simulation
 # ---------------------------------------------------------------------------
 
-def time_decode_case(kv, synth, dev, B, S_q, n_res, bits, Hq=32, G=32, D=128, hs=False, Hkv=8, peak=None):
+def time_decode_case(kv, synth, dev, B, S_q, n_res, bits, Hq=32, G=32, D=128, hs=False, Hkv=8, peak=None,
+                     store_ready=False):
     """Mean device time of one decode over a rotating pool of independent
     stores (more than 4x L2 in total): graphs of 8 launches on distinct
-    entries, at least 256 launches and 50 ms."""
+    entries, at least 256 launches and 50 ms. store_ready: the decodes take
+    KIVI_DECODE_STORE_READY (the preceding kernel is another decode, which
+    does not write their stores)."""
     import torch
     w = synth.Workload("decode", B=B, Hkv=Hkv, Hq=Hq, D=D, S=S_q + n_res, bits=bits, G=G, R=0,
                        n_outlier=4, outlier_scale=8.0, seed=11)
@@ -485,7 +490,8 @@ def time_decode_case(kv, synth, dev, B, S_q, n_res, bits, Hq=32, G=32, D=128, hs
     torch.cuda.synchronize()
 
     def fn(e):
-        kv.kivi_decode_attend(e[0], e[1], e[2], S_q, e[3], e[4], n_res, w.Hkv, w.sm_scale, out=e[5], workspace=e[6])
+        kv.kivi_decode_attend(e[0], e[1], e[2], S_q, e[3], e[4], n_res, w.Hkv, w.sm_scale, out=e[5], workspace=e[6],
+                              store_ready=store_ready)
 
     for e in entries:
         fn(e)
@@ -495,7 +501,8 @@ def time_decode_case(kv, synth, dev, B, S_q, n_res, bits, Hq=32, G=32, D=128, hs
     gbs = nbytes / (ms * 1e-3) / 1e9
     plan = kv.kivi_decode_plan_info(B, w.Hq, w.Hkv, S_q, n_res, D, G, bits, hs)
     d = {"B": B, "Hkv": Hkv, "Hq": w.Hq, "S_kv": S_q + n_res, "S_q": S_q, "n_res": n_res, "bits": bits, "G": G,
-         "D": D, "scale_f16": hs, "us": round(us, 3), "bytes": int(nbytes), "GB/s": round(gbs, 1), "pool": P,
+         "D": D, "scale_f16": hs, "store_ready": store_ready, "us": round(us, 3), "bytes": int(nbytes),
+         "GB/s": round(gbs, 1), "pool": P,
          "tokens_per_s": round(B / (ms * 1e-3), 1), "plan": plan}
     if peak:
         d["frac_of_peak"] = round(gbs / peak, 4)
@@ -775,8 +782,8 @@ def run_gb300(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         extra["stream"] = run_stream_sim(kv, synth, dev, peak, args.stream_steps)
         torch.cuda.empty_cache()
-        extra["decode_b1"] = [time_decode_case(kv, synth, dev, 1, S - 128, 128, 4, peak=peak)
-                              for S in (4096, 8192, 16384)]
+        extra["decode_b1"] = [time_decode_case(kv, synth, dev, 1, S - 128, 128, bits, peak=peak, store_ready=sr)
+                              for S, bits in ((4096, 4), (8192, 4), (16384, 4), (32768, 2)) for sr in (False, True)]
         torch.cuda.empty_cache()
 
     cpu = None

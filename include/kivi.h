@@ -69,6 +69,20 @@
 
 /* Option bit of every `bits` argument: scales stored as fp16 (see above). */
 #define KIVI_SCALE_F16 0x100
+/* Option bit of the decode's `bits` argument (kivi_decode_attend and
+ * kivi_decode_attend_noalloc): the caller states that the kernel preceding
+ * this call on `stream` does not write the store (codes, scales, zeros) the
+ * decode reads -- e.g. the store was last flushed before that kernel, or
+ * that kernel is an append to the residual window, a projection or another
+ * layer's decode. The decode then requests its first store tiles before
+ * waiting for that kernel to finish (the library launches every kernel with
+ * programmatic dependent launch), so its first DRAM round trip overlaps the
+ * preceding kernel's tail. q, the residual window and the workspace are
+ * still read only after the wait. Results are identical with and without the
+ * option; setting it when the preceding kernel does write the store (a flush
+ * launched directly before the decode on the same stream) gives undefined
+ * results. */
+#define KIVI_DECODE_STORE_READY 0x200
 
 #ifdef __cplusplus
 extern "C" {
@@ -351,6 +365,7 @@ typedef struct {
     void* v_res;
     int S_q;              /* tokens in the stores */
     int n_res;            /* tokens in the windows */
+    int store_written;    /* 1 when the cache's latest launch wrote the stores (set 0 for an empty cache) */
 } kivi_cache;
 
 /*
@@ -388,7 +403,11 @@ kivi_status kivi_cache_append(kivi_cache* cache, const void* k_f16, const void* 
  * kivi_decode_attend over the cache's S_q store tokens and n_res window
  * tokens, for B sequences with Hkv KV heads (B * Hkv == BH) and Hq query
  * heads; every other argument, check and result is that of
- * kivi_decode_attend. The counters are not changed.
+ * kivi_decode_attend. The counters are not changed. Unless the cache's
+ * latest launch wrote the stores (store_written: a flush that no window
+ * compaction followed), the decode takes KIVI_DECODE_STORE_READY: the calls
+ * on one cache are meant to be issued on one stream, and a flush followed by
+ * any other kernel has finished before the decode's first loads.
  */
 kivi_status kivi_cache_decode(const kivi_cache* cache, const void* q_f16, int B, int Hq, int Hkv, float sm_scale,
                               float* out_f32, void* workspace, size_t workspace_bytes, kivi_stream_t stream);

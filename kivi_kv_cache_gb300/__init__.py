@@ -131,6 +131,7 @@ def kivi_flush_count(n_res: int, residual_length: int, group_size: int = 32) -> 
 
 
 KIVI_SCALE_F16 = 0x100  # option bit of every `bits` argument: scales stored as fp16
+KIVI_DECODE_STORE_READY = 0x200  # decode option: the preceding kernel on the stream does not write the store
 
 
 class KiviStore:
@@ -339,8 +340,10 @@ def kivi_decode_workspace(nbytes: int, device):
 
 
 def kivi_decode_attend(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res, v_res, n_res: int,
-                       Hkv: int, sm_scale: float, out=None, workspace=None, stream=None):
-    """Single-token decode: q [B, Hq, D] fp16 -> out [B, Hq, D] fp32."""
+                       Hkv: int, sm_scale: float, out=None, workspace=None, stream=None, store_ready: bool = False):
+    """Single-token decode: q [B, Hq, D] fp16 -> out [B, Hq, D] fp32.
+    store_ready: KIVI_DECODE_STORE_READY (the kernel before this call on the
+    stream does not write the stores)."""
     import torch
     assert kstore.scale_f16 == vstore.scale_f16, "one scale storage for both stores"
     B, Hq, D = q.shape
@@ -357,7 +360,8 @@ def kivi_decode_attend(q, kstore: KiviStore, vstore: KiviStore, S_q: int, k_res,
     st = lib().kivi_decode_attend(
         _ptr(q), _ptr(kstore.codes), _ptr(kstore.scale), _ptr(kstore.zero),
         _ptr(vstore.codes), _ptr(vstore.scale), _ptr(vstore.zero), S_q, kstore.s_cap,
-        _ptr(k_res), _ptr(v_res), n_res, res_cap, B, Hq, Hkv, D, kstore.G, kstore.abi_bits,
+        _ptr(k_res), _ptr(v_res), n_res, res_cap, B, Hq, Hkv, D, kstore.G,
+        kstore.abi_bits | (KIVI_DECODE_STORE_READY if store_ready else 0),
         float(sm_scale), _ptr(out), _ptr(workspace), wbytes, _stream(stream))
     _check("kivi_decode_attend", st)
     return out
@@ -404,7 +408,8 @@ class _CacheStruct(ctypes.Structure):
                 ("residual_length", ctypes.c_int), ("s_cap", ctypes.c_int), ("res_cap", ctypes.c_int),
                 ("kcodes", ctypes.c_void_p), ("kscale", ctypes.c_void_p), ("kzero", ctypes.c_void_p),
                 ("vcodes", ctypes.c_void_p), ("vscale", ctypes.c_void_p), ("vzero", ctypes.c_void_p),
-                ("k_res", ctypes.c_void_p), ("v_res", ctypes.c_void_p), ("S_q", ctypes.c_int), ("n_res", ctypes.c_int)]
+                ("k_res", ctypes.c_void_p), ("v_res", ctypes.c_void_p), ("S_q", ctypes.c_int), ("n_res", ctypes.c_int),
+                ("store_written", ctypes.c_int)]
 
 
 class KiviCache:

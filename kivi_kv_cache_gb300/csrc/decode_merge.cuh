@@ -41,140 +41,87 @@ __device__ __forceinline__ bool take_last_ticket(const DecodeArgs& a, int bh, in
     return *flag != 0;
 }
 
-// Float4 vectors of a head-dim-D row per lane: lane l holds channels
-// 4 (l + 32 v) .. + 3 for v < kMergeVec; at D = 64 only lanes 0..15 hold one.
-template <int D>
-struct MergeShape {
-    static constexpr int kVec = D >= 128 ? D / 128 : 1;
-    __device__ static bool active(int lane) { return D >= 128 || lane < D / 4; }
-};
+// VW consecutive floats (1, 2, 4 or 8; 4 VW-byte aligned) read through L2
+// (ld.global.cg: other CTAs of this launch wrote them), or zeros.
+template <int VW>
+__device__ __forceinline__ void ldcg_vec(float (&v)[VW], const float* p, bool on) {
+    if constexpr (VW == 1) {
+        v[0] = on ? __ldcg(p) : 0.f;
+    } else if constexpr (VW == 2) {
+        const float2 x = on ? __ldcg(reinterpret_cast<const float2*>(p)) : make_float2(0.f, 0.f);
+        v[0] = x.x, v[1] = x.y;
+    } else {
+#pragma unroll
+        for (int e = 0; e < VW / 4; ++e) {
+            const float4 x = on ? __ldcg(reinterpret_cast<const float4*>(p) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[4 * e] = x.x, v[4 * e + 1] = x.y, v[4 * e + 2] = x.z, v[4 * e + 3] = x.w;
+        }
+    }
+}
 
-// Log-sum-exp sum of the partials lo .. hi-1 of one query head: *M = their
-// largest running max, *L = sum_s l_s 2^(m_s - M), and acc = sum_s o_s
-// 2^(m_s - M) for this lane's channels (M = -inf, L = 0, 0 for an empty
-// range). Partials are read through L2 (ld.global.cg): other CTAs of this
-// launch wrote them. The first CHUNK partial rows are requested together with
-// the (m, l) pairs, so up to CHUNK splits cost one L2 round trip.
-template <int CHUNK, int D>
-__device__ __forceinline__ void merge_range(const float2* ml, const float4* po, int lo, int hi, int lane,
-                                            float* M_out, float* L_out, float4 (&acc)[MergeShape<D>::kVec]) {
-    static_assert(CHUNK == 4 || CHUNK == 8 || CHUNK == 16, "chunk of partial rows");
-    constexpr int NV = MergeShape<D>::kVec;
-    const bool on = MergeShape<D>::active(lane);
-    const int n = hi - lo;
-    ml += lo;
-    po += (long long)lo * (D / 4);
-    float4 v[CHUNK][NV];
+// Merge of the n_split partials of query heads bq0 .. bq0 + nheads - 1
+// (nheads <= 4) by the NW warps (4 or 8) of the CTA holding the last ticket:
+// warp w takes head w % 4 and channel slice w / 4 of the NW / 4 slices of a
+// row, over every split. A lane holds VW consecutive channels of the slice;
+// the first CHUNK partial rows (up to 64 registers' worth) are requested
+// together with the (m, l) pairs, so up to CHUNK splits cost one L2 round
+// trip. The (m, l) of split s sit in lane s % 32, and each row's weight
+// 2^(m_s - M) reaches the other lanes by shuffle. No barrier inside.
+template <int NW, int D>
+__device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0, int nheads, int warp, int lane) {
+    static_assert(NW == 4 || NW == 8, "4 or 8 warps");
+    constexpr int SL = NW / 4;       // channel slices per row
+    constexpr int CW = D / SL;       // channels per slice
+    constexpr int VW = CW / 32;      // channels per lane
+    static_assert(VW >= 1 && VW <= 8 && CW % 32 == 0, "a slice is 32 to 256 channels");
+    constexpr int CHUNK = VW <= 2 ? 32 : (VW == 4 ? 16 : 8);  // rows per round trip
+    const int h = warp & 3, sl = warp >> 2;
+    if (h >= nheads) return;
+    const long long bq = bq0 + h;
+    const int n = a.n_split;
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + bq * n;
+    const float* po = a.part_o + bq * n * D + sl * CW + lane * VW;
+    float v[CHUNK][VW];
 #pragma unroll
-    for (int k = 0; k < CHUNK; ++k)
-#pragma unroll
-        for (int e = 0; e < NV; ++e)
-            v[k][e] = on && k < n ? __ldcg(po + (long long)k * (D / 4) + 32 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float2 x0 = lane < n ? __ldcg(&ml[lane]) : make_float2(-INFINITY, 0.f);
+    for (int k = 0; k < CHUNK; ++k) ldcg_vec<VW>(v[k], po + (long long)k * D, k < n);
+    const float2 x0 = lane < n ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
     float M = x0.x;
-    for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, __ldcg(&ml[s]).x);
+    for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, __ldcg(ml + s).x);
     M = warp_max(M);
-    float L = 0.f;
+    float acc[VW], L = 0.f;
 #pragma unroll
-    for (int e = 0; e < NV; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = 0; e < VW; ++e) acc[e] = 0.f;
     for (int s0 = 0; s0 < n; s0 += 32) {
         float2 x = x0;
-        if (s0 > 0) x = s0 + lane < n ? __ldcg(&ml[s0 + lane]) : make_float2(-INFINITY, 0.f);
-        const float wt = x.x == -INFINITY ? 0.f : exp2f(x.x - M);
+        if (s0 > 0) x = s0 + lane < n ? __ldcg(ml + s0 + lane) : make_float2(-INFINITY, 0.f);
+        const float wt = x.x == -INFINITY ? 0.f : exp2f(x.x - M);  // 0 past the last split
         L = fmaf(x.y, wt, L);
         for (int k0 = 0; k0 < 32 && s0 + k0 < n; k0 += CHUNK) {
             if (s0 + k0 > 0) {
 #pragma unroll
                 for (int k = 0; k < CHUNK; ++k)
-#pragma unroll
-                    for (int e = 0; e < NV; ++e)
-                        v[k][e] = on && s0 + k0 + k < n ? __ldcg(po + (long long)(s0 + k0 + k) * (D / 4) + 32 * e)
-                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                    ldcg_vec<VW>(v[k], po + (long long)(s0 + k0 + k) * D, s0 + k0 + k < n);
             }
 #pragma unroll
             for (int k = 0; k < CHUNK; ++k) {
-                const float wk = __shfl_sync(0xffffffffu, wt, k0 + k);  // 0 past the last split
+                const float wk = __shfl_sync(0xffffffffu, wt, k0 + k);
 #pragma unroll
-                for (int e = 0; e < NV; ++e) {
-                    acc[e].x = fmaf(v[k][e].x, wk, acc[e].x);
-                    acc[e].y = fmaf(v[k][e].y, wk, acc[e].y);
-                    acc[e].z = fmaf(v[k][e].z, wk, acc[e].z);
-                    acc[e].w = fmaf(v[k][e].w, wk, acc[e].w);
-                }
+                for (int e = 0; e < VW; ++e) acc[e] = fmaf(v[k][e], wk, acc[e]);
             }
         }
     }
-    *M_out = M;
-    *L_out = warp_sum(L);
-}
-
-// Shared-memory row of one head's share in the multi-warp merge: o[D], m, l,
-// padded to a multiple of 4 floats so float4 rows stay aligned.
-template <int D>
-__host__ __device__ constexpr int scratch_row() { return D + 4; }
-
-// Merge of the partials of query heads bq0 .. bq0 + nheads - 1 (nheads <= 4)
-// by a CTA of nwarps (4, 8 or 16) warps: warp w takes head w % 4 and the w / 4-th
-// of the splits, so more warps cut the L2 round trips; the shares meet in
-// `scratch` (16-byte aligned shared memory, nwarps * scratch_row<D>() floats).
-// Every thread of the CTA must call it (it holds a CTA barrier when nwarps > 4).
-// CHUNK partial rows per L2 round trip: CHUNK / kVec of them at D = 256.
-template <int CHUNK, int D>
-__device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0, int nheads, int warp,
-                                             int nwarps, int lane, float* scratch) {
-    constexpr int NV = MergeShape<D>::kVec;
-    constexpr int RC = CHUNK / NV;  // rows per request at this width
-    constexpr int kRow = scratch_row<D>();
-    const bool on = MergeShape<D>::active(lane);
-    const int n = a.n_split;
-    const int h = warp & 3, sub = warp >> 2, nsub = nwarps >> 2;
-    const int per = (n + nsub - 1) / nsub;
-    const int lo = min(n, sub * per), hi = min(n, lo + per);
-    const long long bq = bq0 + h;
-    float M = -INFINITY, L = 0.f;
-    float4 acc[NV];
+    L = warp_sum(L);
+    const float r = 1.0f / L;
+    float* out = a.out + bq * D + sl * CW + lane * VW;
+    if constexpr (VW == 1) {
+        out[0] = acc[0] * r;
+    } else if constexpr (VW == 2) {
+        *reinterpret_cast<float2*>(out) = make_float2(acc[0] * r, acc[1] * r);
+    } else {
 #pragma unroll
-    for (int e = 0; e < NV; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (h < nheads)
-        merge_range<RC, D>(reinterpret_cast<const float2*>(a.part_ml) + bq * n,
-                           reinterpret_cast<const float4*>(a.part_o + bq * n * D) + lane, lo, hi, lane, &M, &L, acc);
-    if (nsub > 1) {
-        float* mine = scratch + (sub * 4 + h) * kRow;
-        if (sub > 0 && h < nheads) {
-            if (on) {
-#pragma unroll
-                for (int e = 0; e < NV; ++e) reinterpret_cast<float4*>(mine)[lane + 32 * e] = acc[e];
-            }
-            if (lane == 0) {
-                mine[D] = M;
-                mine[D + 1] = L;
-            }
-        }
-        __syncthreads();
-        if (sub > 0 || h >= nheads) return;
-        for (int t = 1; t < nsub; ++t) {
-            const float* other = scratch + (t * 4 + h) * kRow;
-            const float Mo = other[D];
-            if (Mo == -INFINITY) continue;  // an empty share of the splits
-            const float Mn = fmaxf(M, Mo);
-            const float fa = M == -INFINITY ? 0.f : exp2f(M - Mn), fb = exp2f(Mo - Mn);
-            if (on) {
-#pragma unroll
-                for (int e = 0; e < NV; ++e) {
-                    const float4 ob = reinterpret_cast<const float4*>(other)[lane + 32 * e];
-                    acc[e] = make_float4(fmaf(acc[e].x, fa, ob.x * fb), fmaf(acc[e].y, fa, ob.y * fb),
-                                         fmaf(acc[e].z, fa, ob.z * fb), fmaf(acc[e].w, fa, ob.w * fb));
-                }
-            }
-            L = fmaf(L, fa, other[D + 1] * fb);
-            M = Mn;
-        }
-    }
-    if (h < nheads && on) {
-#pragma unroll
-        for (int e = 0; e < NV; ++e)
-            reinterpret_cast<float4*>(a.out + bq * D)[lane + 32 * e] =
-                make_float4(acc[e].x / L, acc[e].y / L, acc[e].z / L, acc[e].w / L);
+        for (int e = 0; e < VW / 4; ++e)
+            reinterpret_cast<float4*>(out)[e] =
+                make_float4(acc[4 * e] * r, acc[4 * e + 1] * r, acc[4 * e + 2] * r, acc[4 * e + 3] * r);
     }
 }
 

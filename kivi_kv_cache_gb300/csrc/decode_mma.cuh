@@ -333,12 +333,16 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
     const int r_begin = max(w0, a.n_store_tiles);         // residual tiles [r_begin, w1)
     const int ns = s_end - w0;
 
-    pdl_wait();
-    // start the first two store tiles' copies, then stage q while they fly
+    // start the first two store tiles' copies, then stage q while they fly;
+    // with store_ready (the store is not written by the preceding kernel on
+    // the stream) the copies start before waiting for that kernel, and q and
+    // the residual window are read only after the wait
+    if (!a.store_ready) pdl_wait();
     if (ns > 0) fetch_store_tile<BITS, D, HS>(a, bh, w0, st0, lane);
     cp_async_commit();
     if (ns > 1) fetch_store_tile<BITS, D, HS>(a, bh, w0 + 1, st0 + kStage, lane);
     cp_async_commit();
+    if (a.store_ready) pdl_wait();
 
     // q * score_scale for the nh heads of this CTA (heads >= nh are zero)
     float qm = 0.f;
@@ -870,77 +874,85 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
     }
 
     // ---------------------------- merge the warps ----------------------------
-    __syncthreads();  // every warp is done with its stages
-    float* Ow = reinterpret_cast<float*>(st0);          // [4 heads][D] of this warp
-    float* ml = misc + 16;                                 // [warp][head][2]
+    // Each warp rescales its own accumulators by 2^(m_w - M) (M: the CTA's
+    // largest running max of the head) before they meet in shared memory, so
+    // the cross-warp combine is a plain sum.
+    __syncthreads();  // every warp is done with its stages (they now take its share of the output)
+    float* Ow = reinterpret_cast<float*>(st0);  // [4 heads][D] of this warp
+    float* ml = misc + 16;                       // [warp][head][2]: m, then l * 2^(m - M)
+    float* Mh = misc + 8;                        // [head]: M
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {  // l and sum_t p_t z_tj of head c: the lanes of equal c hold disjoint tokens
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, x);
+#pragma unroll
+        for (int j = 0; j < NE; ++j) pzl[j] += __shfl_xor_sync(0xffffffffu, pzl[j], x);
+    }
+    if (g == 0) ml[(warp * 4 + c) * 2] = m_run;
+    __syncthreads();
     {
-        // l and sum_t p_t z_tj of head c: the lanes of equal c hold disjoint tokens
+        float Mc = -INFINITY;
 #pragma unroll
-        for (int x = 4; x < 32; x <<= 1) {
-            l_run += __shfl_xor_sync(0xffffffffu, l_run, x);
-#pragma unroll
-            for (int j = 0; j < NE; ++j) pzl[j] += __shfl_xor_sync(0xffffffffu, pzl[j], x);
-        }
+        for (int w = 0; w < kWarps; ++w) Mc = fmaxf(Mc, ml[(w * 4 + c) * 2]);
+        const float f = m_run == -INFINITY ? 0.f : exp2f(m_run - Mc);  // a warp without tiles adds nothing
         // o holds sum p s c in units of kOUnit4 / kOUnit2; the z term adds per value group
         if (BITS == 4) {
 #pragma unroll
             for (int j = 0; j < NE; ++j)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const float sc = 1.0f / kOUnit4[u];
-                    Ow[c * D + 32 * j + 4 * g + u] = fmaf(o[2 * j + u][0] + o[2 * j + u][1], sc, pzl[j]);
-                    Ow[c * D + 32 * j + 4 * g + 2 + u] = fmaf(o[2 * j + u][2] + o[2 * j + u][3], sc, pzl[j]);
+                    const float sc = f / kOUnit4[u], zf = pzl[j] * f;
+                    Ow[c * D + 32 * j + 4 * g + u] = fmaf(o[2 * j + u][0] + o[2 * j + u][1], sc, zf);
+                    Ow[c * D + 32 * j + 4 * g + 2 + u] = fmaf(o[2 * j + u][2] + o[2 * j + u][3], sc, zf);
                 }
         } else {
 #pragma unroll
             for (int hc = 0; hc < D / 64; ++hc) {
-                const float pzj = g < 4 ? pzl[2 * hc] : pzl[2 * hc + 1];
+                const float zf = (g < 4 ? pzl[2 * hc] : pzl[2 * hc + 1]) * f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float sc = 1.0f / kOUnit2[k];
-                    Ow[c * D + 64 * hc + 8 * g + k] = fmaf(o[4 * hc + k][0] + o[4 * hc + k][1], sc, pzj);
-                    Ow[c * D + 64 * hc + 8 * g + 4 + k] = fmaf(o[4 * hc + k][2] + o[4 * hc + k][3], sc, pzj);
+                    const float sc = f / kOUnit2[k];
+                    Ow[c * D + 64 * hc + 8 * g + k] = fmaf(o[4 * hc + k][0] + o[4 * hc + k][1], sc, zf);
+                    Ow[c * D + 64 * hc + 8 * g + 4 + k] = fmaf(o[4 * hc + k][2] + o[4 * hc + k][3], sc, zf);
                 }
             }
         }
         if (g == 0) {
-            ml[(warp * 4 + c) * 2 + 0] = m_run;
-            ml[(warp * 4 + c) * 2 + 1] = l_run;
+            ml[(warp * 4 + c) * 2 + 1] = l_run * f;
+            if (warp == 0) Mh[c] = Mc;
         }
     }
     pdl_trigger();
     __syncthreads();
     int h0, nh;  // recomputed here rather than held through the tile loop
     cta_heads<GQ>(a, h0, nh);
-    for (int idx = tid; idx < nh * D; idx += kThreads) {
-        const int h = idx / D, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 4 + h) * 2]);
-        float L = 0.f, acc = 0.f;
+    for (int i4 = tid; i4 < nh * (D / 4); i4 += kThreads) {
+        const int h = i4 / (D / 4), d = 4 * (i4 % (D / 4));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float mw = ml[(w * 4 + h) * 2];
-            if (mw == -INFINITY) continue;  // a warp without tiles
-            const float f = exp2f(mw - M);
-            L = fmaf(ml[(w * 4 + h) * 2 + 1], f, L);
-            acc = fmaf(reinterpret_cast<const float*>(smem + w * GE::kWarpSmem)[h * D + d], f, acc);
+            const float4 v = *reinterpret_cast<const float4*>(
+                reinterpret_cast<const float*>(smem + w * GE::kWarpSmem) + h * D + d);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+            L += ml[(w * 4 + h) * 2 + 1];
         }
+        const float M = Mh[h];
         const long long bq = (long long)b * a.Hq + h0 + h;
         if (a.n_split == 1) {
-            a.out[bq * D + d] = acc / L;
+            const float r = 1.0f / L;
+            *reinterpret_cast<float4*>(a.out + bq * D + d) = make_float4(acc.x * r, acc.y * r, acc.z * r, acc.w * r);
         } else if (CL) {  // the partial stays in this CTA's shared memory (the q area is free now)
-            q_s[h * D + d] = acc;
+            *reinterpret_cast<float4*>(q_s + h * D + d) = acc;
             if (d == 0) {
                 misc[100 + 2 * h] = M;
                 misc[101 + 2 * h] = L;
             }
         } else {
-            a.part_o[(bq * a.n_split + split) * D + d] = acc;
-            if (d == 0) {
-                a.part_ml[(bq * a.n_split + split) * 2 + 0] = M;
-                a.part_ml[(bq * a.n_split + split) * 2 + 1] = L;
-            }
+            __stcg(reinterpret_cast<float4*>(a.part_o + (bq * a.n_split + split) * D + d), acc);
+            if (d == 0) __stcg(reinterpret_cast<float2*>(a.part_ml + (bq * a.n_split + split) * 2), make_float2(M, L));
         }
     }
     if (a.n_split == 1) return;
@@ -976,7 +988,7 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
     }
     // one ticket counter per (batch, KV head, sub-group)
     if (take_last_ticket(a, b * (int)gridDim.y + (int)blockIdx.y, reinterpret_cast<int*>(misc + 96)))
-        merge_splits<16, D>(a, (long long)b * a.Hq + h0, nh, warp, kWarps, lane, reinterpret_cast<float*>(smem));
+        merge_splits<kWarps, D>(a, (long long)b * a.Hq + h0, nh, warp, lane);
 }
 
 template <int BITS, int GQ, int NW, bool CL, int D, bool HS>

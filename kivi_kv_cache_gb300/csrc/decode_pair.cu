@@ -148,12 +148,18 @@ __global__ void __launch_bounds__(kThreads, kPairs <= 4 ? 2 : 1) decode_pair_ker
     const int t0 = (int)(gp * a.n_tiles / np_head);
     const int nt = (int)((gp + 1) * a.n_tiles / np_head) - t0;
 
-    pdl_wait();
+    // with store_ready (the store is not written by the preceding kernel on
+    // the stream) a pair whose first stages are all store tiles requests them
+    // before waiting for that kernel; q and the residual window are read only
+    // after the wait
+    const bool early = a.store_ready && t0 + (kStages - 1) <= a.n_store_tiles;
+    if (!early) pdl_wait();
 #pragma unroll
     for (int k = 0; k < kStages - 1; ++k) {
         if (k < nt) fetch_tile<BITS>(a, bh, t0 + k, ring + k * kStage, pt);
         cp_async_commit();
     }
+    if (early) pdl_wait();
 
     // q * score_scale for the GQ heads of this KV head (heads >= GQ are zero)
     float qm = 0.f;
@@ -497,17 +503,27 @@ __global__ void __launch_bounds__(kThreads, kPairs <= 4 ? 2 : 1) decode_pair_ker
     cp_async_wait<0>();
 
     // ---------------------------- merge the pairs ----------------------------
+    // Each warp rescales its accumulators by 2^(m_pair - M) (M: the CTA's
+    // largest running max of the head) before they meet in shared memory, so
+    // the cross-pair combine is a plain sum.
     __syncthreads();  // every pair is done with its ring
     float* Ow = reinterpret_cast<float*>(ring);  // [4 heads][128] of this pair (each warp its 64 channels)
-    float* ml = misc + 16;                        // [pair][head][2]
-    {
-        // l and sum_t p_t z_tj of head c: the lanes of equal c hold disjoint tokens
+    float* ml = misc + 16;                        // [pair][head][2]: m, then l * 2^(m - M)
+    float* Mh = misc + 8;                         // [head]: M
+    // l and sum_t p_t z_tj of head c: the lanes of equal c hold disjoint tokens
 #pragma unroll
-        for (int x = 4; x < 32; x <<= 1) {
-            l_run += __shfl_xor_sync(0xffffffffu, l_run, x);
-            pzl[0] += __shfl_xor_sync(0xffffffffu, pzl[0], x);
-            pzl[1] += __shfl_xor_sync(0xffffffffu, pzl[1], x);
-        }
+    for (int x = 4; x < 32; x <<= 1) {
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, x);
+        pzl[0] += __shfl_xor_sync(0xffffffffu, pzl[0], x);
+        pzl[1] += __shfl_xor_sync(0xffffffffu, pzl[1], x);
+    }
+    if (hf == 0 && g == 0) ml[(pair * 4 + c) * 2] = m_run;
+    __syncthreads();
+    {
+        float Mc = -INFINITY;
+#pragma unroll
+        for (int pp = 0; pp < kPairs; ++pp) Mc = fmaxf(Mc, ml[(pp * 4 + c) * 2]);
+        const float f = m_run == -INFINITY ? 0.f : exp2f(m_run - Mc);  // a pair without tiles adds nothing
         // o holds sum p s c in units of kOUnit4 / kOUnit2; the z term adds per value group
         if (BITS == 4) {
 #pragma unroll
@@ -515,55 +531,55 @@ __global__ void __launch_bounds__(kThreads, kPairs <= 4 ? 2 : 1) decode_pair_ker
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int j = 2 * hf + jj;
-                    const float sc = 1.0f / kOUnit4[u];
-                    Ow[c * kD + 32 * j + 4 * g + u] = fmaf(o[2 * jj + u][0] + o[2 * jj + u][1], sc, pzl[jj]);
-                    Ow[c * kD + 32 * j + 4 * g + 2 + u] = fmaf(o[2 * jj + u][2] + o[2 * jj + u][3], sc, pzl[jj]);
+                    const float sc = f / kOUnit4[u], zf = pzl[jj] * f;
+                    Ow[c * kD + 32 * j + 4 * g + u] = fmaf(o[2 * jj + u][0] + o[2 * jj + u][1], sc, zf);
+                    Ow[c * kD + 32 * j + 4 * g + 2 + u] = fmaf(o[2 * jj + u][2] + o[2 * jj + u][3], sc, zf);
                 }
         } else {
-            const float pzj = g < 4 ? pzl[0] : pzl[1];  // rows of lanes g < 4 lie in group 2hf
+            const float zf = (g < 4 ? pzl[0] : pzl[1]) * f;  // rows of lanes g < 4 lie in group 2hf
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float sc = 1.0f / kOUnit2[k];
-                Ow[c * kD + 64 * hf + 8 * g + k] = fmaf(o[k][0] + o[k][1], sc, pzj);
-                Ow[c * kD + 64 * hf + 8 * g + 4 + k] = fmaf(o[k][2] + o[k][3], sc, pzj);
+                const float sc = f / kOUnit2[k];
+                Ow[c * kD + 64 * hf + 8 * g + k] = fmaf(o[k][0] + o[k][1], sc, zf);
+                Ow[c * kD + 64 * hf + 8 * g + 4 + k] = fmaf(o[k][2] + o[k][3], sc, zf);
             }
         }
         if (hf == 0 && g == 0) {
-            ml[(pair * 4 + c) * 2 + 0] = m_run;
-            ml[(pair * 4 + c) * 2 + 1] = l_run;
+            ml[(pair * 4 + c) * 2 + 1] = l_run * f;
+            if (pair == 0) Mh[c] = Mc;
         }
     }
     pdl_trigger();
     __syncthreads();
-    const int d = tid & (kD - 1);
-    for (int h = tid / kD; h < GQ; h += kThreads / kD) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int pp = 0; pp < kPairs; ++pp) M = fmaxf(M, ml[(pp * 4 + h) * 2]);
-        float L = 0.f, acc = 0.f;
+    for (int i4 = tid; i4 < GQ * (kD / 4); i4 += kThreads) {
+        const int h = i4 / (kD / 4), d = 4 * (i4 % (kD / 4));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = 0.f;
 #pragma unroll
         for (int pp = 0; pp < kPairs; ++pp) {
-            const float mp = ml[(pp * 4 + h) * 2];
-            if (mp == -INFINITY) continue;  // a pair without tiles
-            const float f = exp2f(mp - M);
-            L = fmaf(ml[(pp * 4 + h) * 2 + 1], f, L);
-            acc = fmaf(reinterpret_cast<const float*>(smem + pp * kStages * kStage)[h * kD + d], f, acc);
+            const float4 v =
+                *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(smem + pp * kStages * kStage) + h * kD + d);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+            L += ml[(pp * 4 + h) * 2 + 1];
         }
+        const float M = Mh[h];
         const long long bq = (long long)b * a.Hq + h0 + h;
         if (a.n_split == 1) {
-            a.out[bq * kD + d] = acc / L;
+            const float r = 1.0f / L;
+            *reinterpret_cast<float4*>(a.out + bq * kD + d) = make_float4(acc.x * r, acc.y * r, acc.z * r, acc.w * r);
         } else if (CL) {  // the partial stays in this CTA's shared memory (the q area is free now)
-            q_s[h * kD + d] = acc;
+            *reinterpret_cast<float4*>(q_s + h * kD + d) = acc;
             if (d == 0) {
                 misc[100 + 2 * h] = M;
                 misc[101 + 2 * h] = L;
             }
         } else {
-            a.part_o[(bq * a.n_split + split) * kD + d] = acc;
-            if (d == 0) {
-                a.part_ml[(bq * a.n_split + split) * 2 + 0] = M;
-                a.part_ml[(bq * a.n_split + split) * 2 + 1] = L;
-            }
+            __stcg(reinterpret_cast<float4*>(a.part_o + (bq * a.n_split + split) * kD + d), acc);
+            if (d == 0)
+                __stcg(reinterpret_cast<float2*>(a.part_ml + (bq * a.n_split + split) * 2), make_float2(M, L));
         }
     }
     if (a.n_split == 1) return;
@@ -595,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, kPairs <= 4 ? 2 : 1) decode_pair_ker
         return;
     }
     if (take_last_ticket(a, bh, reinterpret_cast<int*>(misc + 96)))
-        merge_splits<16, kD>(a, (long long)b * a.Hq + h0, GQ, warp, kWarps, lane, reinterpret_cast<float*>(smem));
+        merge_splits<kWarps, kD>(a, (long long)b * a.Hq + h0, GQ, warp, lane);
 }
 
 template <int BITS, int GQ, bool CL>

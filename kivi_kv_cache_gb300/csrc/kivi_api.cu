@@ -41,6 +41,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // width outside {2, 4}, which the shape check refuses.
 bool scale_f16_of(int bits) { return (bits & KIVI_SCALE_F16) != 0; }
 int width_of(int bits) { return bits & ~KIVI_SCALE_F16; }
+// The decode's `bits` may also carry KIVI_DECODE_STORE_READY (the store is
+// not written by the kernel that precedes the call on its stream).
+bool store_ready_of(int bits) { return (bits & KIVI_DECODE_STORE_READY) != 0; }
+int decode_bits(int bits) { return bits & ~KIVI_DECODE_STORE_READY; }
 
 bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
 
@@ -105,6 +109,10 @@ constexpr int kMmaMaxSplits4 = KIVI_DECODE_MMA_MAX_SPLITS4;
 #define KIVI_DECODE_ONE_WAVE 1
 #endif
 constexpr bool kOneWave = KIVI_DECODE_ONE_WAVE != 0;
+#ifndef KIVI_DECODE_BALANCE
+#define KIVI_DECODE_BALANCE 1
+#endif
+constexpr bool kBalance = KIVI_DECODE_BALANCE != 0;
 
 bool mma_group(int gq) { return gq == 1 || gq == 2 || gq == 4; }
 
@@ -152,6 +160,26 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool 
         }
     }
     p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    if (kBalance && !p.pair_kernel && heads <= kMergeCounters) {
+        // A one-warp-per-tile grid of more than one CTA per SM but less than
+        // one wave leaves some SMs one CTA more than others, and those set the
+        // pace. When more splits fill every SM's resident slots (at least 95 %
+        // of them), take them: each split gets fewer tiles and every SM the
+        // same load. Plans that merge inside a cluster (at most 16 splits)
+        // keep that merge.
+        const long long S = sm_count(), cps = (D == 256 ? 8 : 16) / p.warps_per_cta;
+        const long long ctas = heads * p.n_split;
+        if (ctas > S && ctas < cps * S) {
+            long long n2 = cps * S / heads;
+            if (n2 > p.n_tiles) n2 = p.n_tiles;
+            const bool keeps_cluster = p.n_split <= kMaxClusterSplits && n2 > kMaxClusterSplits;
+            if (n2 > p.n_split && !keeps_cluster && 20 * heads * n2 >= 19 * cps * S) {
+                p.n_split = (int)n2;
+                p.tiles_per_split = (p.n_tiles + p.n_split - 1) / p.n_split;
+                p.tiles_per_warp = (p.tiles_per_split + p.warps_per_cta - 1) / p.warps_per_cta;
+            }
+        }
+    }
     return p;
 }
 
@@ -274,6 +302,7 @@ int kivi::shape_status(int D, int group_size, int bits) {
 // arguments (bits may carry KIVI_SCALE_F16); 0 for a single-split plan or
 // for arguments the decode rejects.
 size_t kivi::decode_workspace_need(int B, int Hq, int Hkv, int S_q, int n_res, int D, int group_size, int bits) {
+    bits = decode_bits(bits);
     const bool hs = scale_f16_of(bits);
     bits = width_of(bits);
     if (shape_check(D, group_size, bits) != KIVI_OK || B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 ||
@@ -498,6 +527,7 @@ size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, in
 
 kivi_status kivi_decode_plan_info(int B, int Hq, int Hkv, int S_q, int n_res, int D, int group_size, int bits,
                                   int* info) {
+    bits = decode_bits(bits);
     const bool hs = scale_f16_of(bits);
     bits = width_of(bits);
     kivi_status st = shape_check(D, group_size, bits);
@@ -524,6 +554,8 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
                                const void* v_res_f16, int n_res, int res_cap, int B, int Hq, int Hkv,
                                int D, int group_size, int bits, float sm_scale, float* out_f32,
                                void* workspace, size_t workspace_bytes_, kivi_stream_t stream) {
+    const bool ready = store_ready_of(bits);
+    bits = decode_bits(bits);
     const bool hs = scale_f16_of(bits);
     bits = width_of(bits);
     kivi_status st = shape_check(D, group_size, bits);
@@ -583,6 +615,7 @@ kivi_status kivi_decode_attend(const void* q_f16, const void* kcodes_u8, const f
     a.out = out_f32;
     const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
     a.q_sub = p.q_sub;
+    a.store_ready = ready ? 1 : 0;
     return from_cuda(p.pair_kernel ? launch_decode_pair(a, bits, gq, strm) : launch_decode_mma(a, bits, gq, strm));
 }
 

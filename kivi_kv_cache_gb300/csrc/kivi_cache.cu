@@ -55,8 +55,10 @@ kivi_status flush_window(kivi_cache* c, int n, kivi_stream_t stream) {
                                    c->s_cap, &done, stream);
     if (st != KIVI_OK) return st;
     c->S_q += done;
+    c->store_written = 1;
     st = kivi_residual_compact_kv(c->k_res, c->v_res, c->BH, c->res_cap, c->D, c->n_res, done, stream);
     if (st != KIVI_OK) return st;
+    if (done > 0 && done < c->n_res) c->store_written = 0;  // the compaction ran after the flush
     c->n_res -= done;
     return KIVI_OK;
 }
@@ -84,6 +86,7 @@ kivi_status kivi_cache_prefill(kivi_cache* c, const void* k_f16, const void* v_f
                            c->kscale, c->kzero, c->vcodes, c->vscale, c->vzero, c->S_q, c->s_cap, &done, stream);
         if (st != KIVI_OK) return st;
         c->S_q += done;
+        c->store_written = 1;
         if (n_flushed) *n_flushed = done;
     }
     if (tail > 0) {
@@ -93,6 +96,7 @@ kivi_status kivi_cache_prefill(kivi_cache* c, const void* k_f16, const void* v_f
                                      stream);
         if (st != KIVI_OK) return st;
         c->n_res = tail;
+        c->store_written = 0;
     }
     return KIVI_OK;
 }
@@ -137,6 +141,7 @@ kivi_status kivi_cache_append(kivi_cache* c, const void* k_f16, const void* v_f1
                                      stream);
         if (st != KIVI_OK) return st;
         c->n_res += m;
+        c->store_written = 0;
         off += m;
         const int f = window_flush(c->n_res, R, G);
         if (f > 0) {
@@ -154,9 +159,10 @@ kivi_status kivi_cache_decode(const kivi_cache* c, const void* q_f16, int B, int
     kivi_status st = cache_check(c);
     if (st != KIVI_OK) return st;
     if (B <= 0 || Hkv <= 0 || (long long)B * Hkv != c->BH) return KIVI_ERR_INVALID_ARG;
+    const int bits = c->bits | (c->store_written ? 0 : KIVI_DECODE_STORE_READY);
     return kivi_decode_attend(q_f16, c->kcodes, c->kscale, c->kzero, c->vcodes, c->vscale, c->vzero, c->S_q,
                               c->s_cap, c->k_res, c->v_res, c->n_res, c->res_cap, B, Hq, Hkv, c->D, c->group_size,
-                              c->bits, sm_scale, out_f32, workspace, workspace_bytes, stream);
+                              bits, sm_scale, out_f32, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -71,6 +71,8 @@ struct DecodeArgs {
     int n_store_tiles;
     int n_tiles;
     int q_sub;            // one-warp-per-tile kernel: query sub-groups of up to 4 heads per KV head
+    int store_ready = 0;  // 1: the store is not written by the preceding kernel on the stream, so its first
+                          // tiles may be requested before griddepcontrol.wait
     unsigned int* counters;  // [B*Hkv*q_sub] merge tickets, zero between calls (n_split > 1)
     float* part_o;        // [B, Hq, n_split, D]
     float* part_ml;       // [B, Hq, n_split, 2]  (running max, running sum)

@@ -234,8 +234,9 @@ def test_decode_plan_rules(L):
                                  (128, 32, True)):
                     p = kv.kivi_decode_plan_info(B, hkv * gq, hkv, S_q, n_res, D, G, 4, hs)
                     assert p["n_tiles"] == -(-S_q // 32) + -(-n_res // 16)
+                    # the kernels spread a head group's tiles evenly over its splits: none is empty
                     assert p["n_split"] * p["tiles_per_split"] >= p["n_tiles"]
-                    assert (p["n_split"] - 1) * p["tiles_per_split"] < p["n_tiles"]
+                    assert 1 <= p["n_split"] <= p["n_tiles"]
                     assert p["q_sub"] == (1 if gq in (1, 2, 4) else -(-gq // 4))
                     if p["pair_kernel"]:
                         seen_pair += 1
@@ -251,6 +252,12 @@ def test_decode_plan_rules(L):
                     if p["n_split"] > 1:
                         assert ws >= 32768 + B * hkv * gq * p["n_split"] * (D + 2) * 4
     assert seen_pair and seen_mma and seen_one_split
+    # balance: a one-warp-per-tile grid between one CTA per SM and one wave
+    # (8-warp CTAs, two per SM on 152 SMs) fills every SM's slots
+    for S_q, bits in ((16256, 4), (32640, 2), (8064, 4)):
+        p = kv.kivi_decode_plan_info(1, 32, 8, S_q, 128, bits=bits)
+        assert p["pair_kernel"] == 0 and p["warps_per_cta"] == 8
+        assert 8 * p["n_split"] == 2 * 152, (S_q, p)
     # the qwen8b decode takes the warp-pair kernel; stores of another group
     # size or head dim, or with fp16 scales, the one-warp-per-tile kernel
     assert kv.kivi_decode_plan_info(1, 32, 8, 2080, 158)["pair_kernel"] == 1
