@@ -68,6 +68,8 @@ PROFILE_CASES = {
     "decode_b1_16k": ("decode", 1, 16384 - 128, 128, 4),
     "decode_b1_32k_2bit": ("decode", 1, 32768 - 128, 128, 2),
     "decode_b32_4k": ("decode", 32, 4032, 64, 4),
+    "step_long2bit": ("step", 0, 0, 0, 2),
+    "step_qwen8b": ("step", 0, 0, 0, 4),
 }
 
 
@@ -1120,7 +1122,11 @@ def run_profile_case(name: str, reps: int = 3):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     kind, B, S_q, n_res, bits = PROFILE_CASES[name]
-    if kind == "flush":
+    if kind == "step":  # one instance of the bench's step, eagerly (flush, append, dequant, decode)
+        inst = Instance(synth.WORKLOADS[name.split("_")[1]], 1, dev, kv, synth)
+        for _ in range(reps):
+            inst.step()
+    elif kind == "flush":
         parts = name.split("_")
         w = synth.WORKLOADS[parts[1]]
         if len(parts) > 2 and parts[2].startswith("g"):

@@ -724,9 +724,17 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
                                  bj[ks][0], bj[ks][1]);
             }
         } else {
-            // o[4h + k]: rows g -> channel 64h + 8g + k, g+8 -> 64h + 8g + 4 + k;
-            // rows of lanes g < 4 lie in group 2h, of lanes g >= 4 in group 2h+1
+            // A 16-byte chunk of a 2-bit row holds value groups 2hc and 2hc + 1
+            // (4 halves of 8 crumbs each). The transposed ldmatrix gives lane g
+            // half g of the chunk, so lanes g < 4 hold group 2hc and lanes g >= 4
+            // group 2hc + 1; one shuffle hands every lane half (g & 3) of each
+            // group. MMA m of group grp then takes crumb 2m + (g >> 2) of the
+            // low byte (row g) and of the high byte (row g + 8), so all 16 rows
+            // share the group's B operand:
+            // o[4hc + 2grp + m]: row g -> channel 64hc + 32grp + 8(g & 3) + 2m + (g >> 2),
+            // row g + 8 -> that channel + 4, in units of 4^(2m + (g >> 2)) 2^-24
             constexpr int CPR = D / 64;  // 16-byte chunks (64 channels) per 2-bit row
+            const int gh = g >> 2;
 #pragma unroll
             for (int hc = 0; hc < CPR; ++hc) {
                 uint32_t bA[2][2], bB[2][2];
@@ -739,25 +747,25 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
                 const int row = 8 * (lane >> 3) + (lane & 7);
                 uint32_t W[4];
                 ldsm_x4_t(W, VC + row * (D / 4) + 16 * swz<CPR>(row, hc));
+                uint32_t X[2][4], Xs[2][4];  // [group][token block]: half (g & 3), its high byte shifted down
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t xl[4], xh[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t mk = 0x00030003u << (2 * k);  // channel 8g + k | 8g + 4 + k, units 4^k 2^-24
-                        xl[q] = W[q] & mk;
-                        xh[q] = (W[q] >> 8) & mk;
-                    }
-                    const bool first = g < 4;
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const uint32_t a0 = xl[2 * ks], a1 = xh[2 * ks], a2 = xl[2 * ks + 1], a3 = xh[2 * ks + 1];
-                        mma16816(o[4 * hc + k], first ? a0 : 0u, first ? a1 : 0u, first ? a2 : 0u,
-                                 first ? a3 : 0u, b0[ks][0], b0[ks][1]);
-                        mma16816(o[4 * hc + k], first ? 0u : a0, first ? 0u : a1, first ? 0u : a2,
-                                 first ? 0u : a3, b1[ks][0], b1[ks][1]);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    X[0][q] = __shfl_sync(0xffffffffu, W[q], lane & 15);  // lanes g < 4 hold group 2hc
+                    X[1][q] = __shfl_sync(0xffffffffu, W[q], lane | 16);  // lanes g >= 4 hold group 2hc + 1
+                    Xs[0][q] = X[0][q] >> 8;
+                    Xs[1][q] = X[1][q] >> 8;
                 }
+#pragma unroll
+                for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const uint32_t mk = 0x00030003u << (2 * (2 * m + gh));
+                        const uint32_t(&bg)[2][2] = grp ? b1 : b0;
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks)
+                            mma16816(o[4 * hc + 2 * grp + m], X[grp][2 * ks] & mk, Xs[grp][2 * ks] & mk,
+                                     X[grp][2 * ks + 1] & mk, Xs[grp][2 * ks + 1] & mk, bg[ks][0], bg[ks][1]);
+                    }
             }
         }
         __syncwarp();
@@ -845,30 +853,37 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
                 }
             }
         } else {
-            // o[4hc + k]: rows g -> channel 64hc + 8g + k, g+8 -> 64hc + 8g + 4 + k
+            // the store tiles' layout: o[4hc + 2grp + m]: row g -> channel 64hc + 32grp + 8(g & 3) + p,
+            // row g + 8 -> + 4, with p = 2m + (g >> 2), in units of 4^p 2^-24
+            const int gh = g >> 2;
+            const uint32_t sel = gh ? 0x7632u : 0x5410u;  // half p & 1 = g >> 2 of each word
 #pragma unroll
-            for (int hc = 0; hc < D / 64; ++hc) {
-                uint32_t rv[4][4];  // tokens 2c, 2c+1, 2c+8, 2c+9: channels 64hc + 8g .. + 7
+            for (int hc = 0; hc < D / 64; ++hc)
 #pragma unroll
-                for (int ti = 0; ti < 4; ++ti) {
-                    const int t = 2 * c + (ti & 1) + 8 * (ti >> 1);
-                    const uint4 v4 = *reinterpret_cast<const uint4*>(VR + t * (2 * D) + (((8 * hc + g) ^ (t & 7)) << 4));
-                    rv[ti][0] = v4.x;
-                    rv[ti][1] = v4.y;
-                    rv[ti][2] = v4.z;
-                    rv[ti][3] = v4.w;
+                for (int grp = 0; grp < 2; ++grp) {
+                    uint32_t rv[4][4];  // tokens 2c, 2c+1, 2c+8, 2c+9: channels 64hc + 32grp + 8(g & 3) .. + 7
+                    const int chunk = 8 * hc + 4 * grp + (g & 3);
+#pragma unroll
+                    for (int ti = 0; ti < 4; ++ti) {
+                        const int t = 2 * c + (ti & 1) + 8 * (ti >> 1);
+                        const uint4 v4 = *reinterpret_cast<const uint4*>(VR + t * (2 * D) + ((chunk ^ (t & 7)) << 4));
+                        rv[ti][0] = v4.x;
+                        rv[ti][1] = v4.y;
+                        rv[ti][2] = v4.z;
+                        rv[ti][3] = v4.w;
+                    }
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const int wa = m, wb = 2 + m;  // words of halves p and p + 4 (p = 2m + (g >> 2))
+                        float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma16816(tmp, __byte_perm(rv[0][wa], rv[1][wa], sel), __byte_perm(rv[0][wb], rv[1][wb], sel),
+                                 __byte_perm(rv[2][wa], rv[3][wa], sel), __byte_perm(rv[2][wb], rv[3][wb], sel), bp0,
+                                 bp1);
+                        const float unit = pow2i(2 * (2 * m + gh) - 24);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[4 * hc + 2 * grp + m][e] = fmaf(tmp[e], unit, o[4 * hc + 2 * grp + m][e]);
+                    }
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t sel = (k & 1) ? 0x7632u : 0x5410u;
-                    const int wa = k >> 1, wb = 2 + (k >> 1);  // words of channels k and 4 + k
-                    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma16816(tmp, __byte_perm(rv[0][wa], rv[1][wa], sel), __byte_perm(rv[0][wb], rv[1][wb], sel),
-                             __byte_perm(rv[2][wa], rv[3][wa], sel), __byte_perm(rv[2][wb], rv[3][wb], sel), bp0, bp1);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[4 * hc + k][e] = fmaf(tmp[e], kOUnit2[k], o[4 * hc + k][e]);
-                }
-            }
         }
         __syncwarp();
     }
@@ -905,16 +920,22 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
                     Ow[c * D + 32 * j + 4 * g + 2 + u] = fmaf(o[2 * j + u][2] + o[2 * j + u][3], sc, zf);
                 }
         } else {
+            const int gh = g >> 2;
 #pragma unroll
-            for (int hc = 0; hc < D / 64; ++hc) {
-                const float zf = (g < 4 ? pzl[2 * hc] : pzl[2 * hc + 1]) * f;
+            for (int hc = 0; hc < D / 64; ++hc)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float sc = f / kOUnit2[k];
-                    Ow[c * D + 64 * hc + 8 * g + k] = fmaf(o[4 * hc + k][0] + o[4 * hc + k][1], sc, zf);
-                    Ow[c * D + 64 * hc + 8 * g + 4 + k] = fmaf(o[4 * hc + k][2] + o[4 * hc + k][3], sc, zf);
+                for (int grp = 0; grp < 2; ++grp) {
+                    const float zf = pzl[2 * hc + grp] * f;
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const int p = 2 * m + gh;  // crumb position: units 4^p 2^-24
+                        const float sc = f * pow2i(24 - 2 * p);
+                        const int ch = 64 * hc + 32 * grp + 8 * (g & 3) + p;
+                        const float(&oo)[4] = o[4 * hc + 2 * grp + m];
+                        Ow[c * D + ch] = fmaf(oo[0] + oo[1], sc, zf);
+                        Ow[c * D + ch + 4] = fmaf(oo[2] + oo[3], sc, zf);
+                    }
                 }
-            }
         }
         if (g == 0) {
             ml[(warp * 4 + c) * 2 + 1] = l_run * f;

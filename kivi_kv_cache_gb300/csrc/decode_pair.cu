@@ -423,30 +423,33 @@ __global__ void __launch_bounds__(kThreads, kPairs <= 4 ? 2 : 1) decode_pair_ker
                     }
                 }
             } else {
-                // o[k]: rows g -> channel 64hf + 8g + k, g+8 -> 64hf + 8g + 4 + k; rows of lanes
-                // g < 4 lie in group 2hf, of lanes g >= 4 in group 2hf + 1
+                // groups 2hf and 2hf + 1 share this warp's 16-byte chunk; as in the
+                // one-warp-per-tile kernel, a shuffle hands every lane half (g & 3)
+                // of each group and MMA m takes crumb 2m + (g >> 2):
+                // o[2grp + m]: row g -> channel 64hf + 32grp + 8(g & 3) + 2m + (g >> 2), row g + 8 -> + 4,
+                // in units of 4^(2m + (g >> 2)) 2^-24
                 const int row = lane;
                 uint32_t W[4];
                 ldsm_x4_t(W, VC + row * 32 + 16 * (hf ^ ((row >> 2) & 1)));
-                const bool first = g < 4;
+                uint32_t X[2][4], Xs[2][4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t xl[4], xh[4];
-#pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        const uint32_t mk = 0x00030003u << (2 * k);  // channel 8g + k | 8g + 4 + k
-                        xl[qq] = W[qq] & mk;
-                        xh[qq] = (W[qq] >> 8) & mk;
-                    }
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const uint32_t a0 = xl[2 * ks], a1 = xh[2 * ks], a2 = xl[2 * ks + 1], a3 = xh[2 * ks + 1];
-                        mma16816(o[k], first ? a0 : 0u, first ? a1 : 0u, first ? a2 : 0u, first ? a3 : 0u,
-                                 bp[0][ks][0], bp[0][ks][1]);
-                        mma16816(o[k], first ? 0u : a0, first ? 0u : a1, first ? 0u : a2, first ? 0u : a3,
-                                 bp[1][ks][0], bp[1][ks][1]);
-                    }
+                for (int qq = 0; qq < 4; ++qq) {
+                    X[0][qq] = __shfl_sync(0xffffffffu, W[qq], lane & 15);
+                    X[1][qq] = __shfl_sync(0xffffffffu, W[qq], lane | 16);
+                    Xs[0][qq] = X[0][qq] >> 8;
+                    Xs[1][qq] = X[1][qq] >> 8;
                 }
+                const int gh = g >> 2;
+#pragma unroll
+                for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const uint32_t mk = 0x00030003u << (2 * (2 * m + gh));
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks)
+                            mma16816(o[2 * grp + m], X[grp][2 * ks] & mk, Xs[grp][2 * ks] & mk,
+                                     X[grp][2 * ks + 1] & mk, Xs[grp][2 * ks + 1] & mk, bp[grp][ks][0], bp[grp][ks][1]);
+                    }
             }
         } else {
             // residual tile: B = p of head hh (hi or lo), tokens {2c, 2c+1 | 2c+8, 2c+9}; the P.V of
@@ -476,25 +479,34 @@ __global__ void __launch_bounds__(kThreads, kPairs <= 4 ? 2 : 1) decode_pair_ker
                     }
                 }
             } else {
-                uint32_t rv[4][4];  // tokens 2c, 2c+1, 2c+8, 2c+9: channels 64hf + 8g .. + 7
+                // the store tiles' layout: o[2grp + m]: row g -> channel 64hf + 32grp + 8(g & 3) + p, row
+                // g + 8 -> + 4, with p = 2m + (g >> 2), in units of 4^p 2^-24
+                const int gh = g >> 2;
+                const uint32_t sel = gh ? 0x7632u : 0x5410u;  // half p & 1 = g >> 2 of each word
 #pragma unroll
-                for (int ti = 0; ti < 4; ++ti) {
-                    const int t = 2 * c + (ti & 1) + 8 * (ti >> 1);
-                    const uint4 v4 = *reinterpret_cast<const uint4*>(VR + t * 256 + (((8 * hf + g) ^ (t & 7)) << 4));
-                    rv[ti][0] = v4.x;
-                    rv[ti][1] = v4.y;
-                    rv[ti][2] = v4.z;
-                    rv[ti][3] = v4.w;
-                }
+                for (int grp = 0; grp < 2; ++grp) {
+                    uint32_t rv[4][4];  // tokens 2c, 2c+1, 2c+8, 2c+9: channels 64hf + 32grp + 8(g & 3) .. + 7
+                    const int chunk = 8 * hf + 4 * grp + (g & 3);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t sel = (k & 1) ? 0x7632u : 0x5410u;
-                    const int wa = k >> 1, wb = 2 + (k >> 1);  // words of channels k and 4 + k
-                    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma16816(tmp, __byte_perm(rv[0][wa], rv[1][wa], sel), __byte_perm(rv[0][wb], rv[1][wb], sel),
-                             __byte_perm(rv[2][wa], rv[3][wa], sel), __byte_perm(rv[2][wb], rv[3][wb], sel), bp0, bp1);
+                    for (int ti = 0; ti < 4; ++ti) {
+                        const int t = 2 * c + (ti & 1) + 8 * (ti >> 1);
+                        const uint4 v4 = *reinterpret_cast<const uint4*>(VR + t * 256 + ((chunk ^ (t & 7)) << 4));
+                        rv[ti][0] = v4.x;
+                        rv[ti][1] = v4.y;
+                        rv[ti][2] = v4.z;
+                        rv[ti][3] = v4.w;
+                    }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[k][e] = fmaf(tmp[e], kOUnit2[k], o[k][e]);
+                    for (int m = 0; m < 2; ++m) {
+                        const int wa = m, wb = 2 + m;  // words of halves p and p + 4
+                        float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma16816(tmp, __byte_perm(rv[0][wa], rv[1][wa], sel), __byte_perm(rv[0][wb], rv[1][wb], sel),
+                                 __byte_perm(rv[2][wa], rv[3][wa], sel), __byte_perm(rv[2][wb], rv[3][wb], sel), bp0,
+                                 bp1);
+                        const float unit = pow2i(2 * (2 * m + gh) - 24);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[2 * grp + m][e] = fmaf(tmp[e], unit, o[2 * grp + m][e]);
+                    }
                 }
             }
         }
@@ -536,12 +548,18 @@ __global__ void __launch_bounds__(kThreads, kPairs <= 4 ? 2 : 1) decode_pair_ker
                     Ow[c * kD + 32 * j + 4 * g + 2 + u] = fmaf(o[2 * jj + u][2] + o[2 * jj + u][3], sc, zf);
                 }
         } else {
-            const float zf = (g < 4 ? pzl[0] : pzl[1]) * f;  // rows of lanes g < 4 lie in group 2hf
+            const int gh = g >> 2;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float sc = f / kOUnit2[k];
-                Ow[c * kD + 64 * hf + 8 * g + k] = fmaf(o[k][0] + o[k][1], sc, zf);
-                Ow[c * kD + 64 * hf + 8 * g + 4 + k] = fmaf(o[k][2] + o[k][3], sc, zf);
+            for (int grp = 0; grp < 2; ++grp) {
+                const float zf = pzl[grp] * f;
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const int pc = 2 * m + gh;  // crumb position: units 4^pc 2^-24
+                    const float sc = f * pow2i(24 - 2 * pc);
+                    const int ch = 64 * hf + 32 * grp + 8 * (g & 3) + pc;
+                    Ow[c * kD + ch] = fmaf(o[2 * grp + m][0] + o[2 * grp + m][1], sc, zf);
+                    Ow[c * kD + ch + 4] = fmaf(o[2 * grp + m][2] + o[2 * grp + m][3], sc, zf);
+                }
             }
         }
         if (hf == 0 && g == 0) {
