@@ -160,16 +160,28 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool 
         }
     }
     p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-    if (kBalance && !p.pair_kernel && heads <= kMergeCounters) {
+    if (kBalance && heads <= kMergeCounters) {
         // A one-warp-per-tile grid of more than one CTA per SM but less than
         // one wave leaves some SMs one CTA more than others, and those set the
         // pace. When more splits fill every SM's resident slots (at least 95 %
         // of them), take them: each split gets fewer tiles and every SM the
         // same load. Plans that merge inside a cluster (at most 16 splits)
         // keep that merge.
-        const long long S = sm_count(), cps = (D == 256 ? 8 : 16) / p.warps_per_cta;
+        const long long S = sm_count();
+        const long long cps = p.pair_kernel ? 16 / (2 * kPairsPerCta) : (D == 256 ? 8 : 16) / p.warps_per_cta;
         const long long ctas = heads * p.n_split;
-        if (ctas > S && ctas < cps * S) {
+        const int wpc = p.pair_kernel ? kPairsPerCta : p.warps_per_cta;  // warps (pairs) sharing a split
+        if (ctas > cps * S && 3 * ctas <= 4 * cps * S && p.n_split > 1) {
+            // a grid that spills just past one wave (at most 4/3 of a wave: the
+            // multi-tile rule above did not apply) takes fewer splits and
+            // stays in one wave; its warps take a tile or so more each
+            const long long n2 = cps * S / heads;
+            if (n2 >= 1) {
+                p.n_split = (int)n2;
+                p.tiles_per_split = (p.n_tiles + p.n_split - 1) / p.n_split;
+                p.tiles_per_warp = (p.tiles_per_split + wpc - 1) / wpc;
+            }
+        } else if (!p.pair_kernel && ctas > S && ctas < cps * S) {
             long long n2 = cps * S / heads;
             if (n2 > p.n_tiles) n2 = p.n_tiles;
             const bool keeps_cluster = p.n_split <= kMaxClusterSplits && n2 > kMaxClusterSplits;
