@@ -333,14 +333,16 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
     const int r_begin = max(w0, a.n_store_tiles);         // residual tiles [r_begin, w1)
     const int ns = s_end - w0;
 
-    // start the first two store tiles' copies, then stage q while they fly;
-    // with store_ready (the store is not written by the preceding kernel on
-    // the stream) the copies start before waiting for that kernel, and q and
-    // the residual window are read only after the wait
+    // start the first store tile's copy, then stage q while it flies; with
+    // store_ready (the store is not written by the preceding kernel on the
+    // stream) the copy starts before waiting for that kernel, and q and the
+    // residual window are read only after the wait. Each warp requests one
+    // tile ahead (the next one when the current one has landed): every SM
+    // still has more bytes in flight than the HBM latency-bandwidth product
+    // needs, and a launch's first tiles arrive about twice as early as with
+    // two tiles requested up front.
     if (!a.store_ready) pdl_wait();
     if (ns > 0) fetch_store_tile<BITS, D, HS>(a, bh, w0, st0, lane);
-    cp_async_commit();
-    if (ns > 1) fetch_store_tile<BITS, D, HS>(a, bh, w0 + 1, st0 + kStage, lane);
     cp_async_commit();
     if (a.store_ready) pdl_wait();
 
@@ -387,8 +389,10 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
     for (int it = 0; it < ns; ++it) {
         const int tile = w0 + it;
         uint8_t* S = st0 + (it & 1) * kStage;
-        cp_async_wait<1>();
+        cp_async_wait<0>();  // this tile
         __syncwarp();
+        if (it + 1 < ns) fetch_store_tile<BITS, D, HS>(a, bh, tile + 1, st0 + ((it + 1) & 1) * kStage, lane);
+        cp_async_commit();
         if (a.g_shift != 0) widen_value_meta<D, HS>(S, a.g_shift, lane);
         const int nvalid = min(32, a.S_q - tile * 32);
         if (nvalid < 32) {  // zero the value metadata of rows past S_q
@@ -769,8 +773,6 @@ __global__ void __launch_bounds__(32 * NW, warps_per_sm<D>() / NW) decode_mma_ke
             }
         }
         __syncwarp();
-        if (it + 2 < ns) fetch_store_tile<BITS, D, HS>(a, bh, tile + 2, S, lane);
-        cp_async_commit();
     }
     cp_async_wait<0>();
     __syncwarp();
