@@ -62,11 +62,12 @@ __device__ __forceinline__ void ldcg_vec(float (&v)[VW], const float* p, bool on
 // Merge of the n_split partials of query heads bq0 .. bq0 + nheads - 1
 // (nheads <= 4) by the NW warps (4 or 8) of the CTA holding the last ticket:
 // warp w takes head w % 4 and channel slice w / 4 of the NW / 4 slices of a
-// row, over every split. A lane holds VW consecutive channels of the slice;
-// the first CHUNK partial rows (up to 64 registers' worth) are requested
-// together with the (m, l) pairs, so up to CHUNK splits cost one L2 round
-// trip. The (m, l) of split s sit in lane s % 32, and each row's weight
-// 2^(m_s - M) reaches the other lanes by shuffle. No barrier inside.
+// row, over every split. A lane holds VW consecutive channels of the slice.
+// The first CHUNK partial rows (up to 80 registers' worth: 40 rows at
+// VW <= 2) are requested together with the (m, l) pairs of splits lane and
+// lane + 32, so up to CHUNK splits cost one L2 round trip; row s takes its
+// weight 2^(m_s - M) from lane s % 32 by shuffle. Splits past CHUNK follow in
+// blocks of 32. No barrier inside.
 template <int NW, int D>
 __device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0, int nheads, int warp, int lane) {
     static_assert(NW == 4 || NW == 8, "4 or 8 warps");
@@ -74,7 +75,8 @@ __device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0,
     constexpr int CW = D / SL;       // channels per slice
     constexpr int VW = CW / 32;      // channels per lane
     static_assert(VW >= 1 && VW <= 8 && CW % 32 == 0, "a slice is 32 to 256 channels");
-    constexpr int CHUNK = VW <= 2 ? 32 : (VW == 4 ? 16 : 8);  // rows per round trip
+    constexpr int CHUNK = VW <= 2 ? 40 : (VW == 4 ? 16 : 8);  // rows of the first round trip
+    constexpr int BLK = VW <= 2 ? 32 : CHUNK;                  // rows per later round trip
     const int h = warp & 3, sl = warp >> 2;
     if (h >= nheads) return;
     const long long bq = bq0 + h;
@@ -85,29 +87,35 @@ __device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0,
 #pragma unroll
     for (int k = 0; k < CHUNK; ++k) ldcg_vec<VW>(v[k], po + (long long)k * D, k < n);
     const float2 x0 = lane < n ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
-    float M = x0.x;
-    for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, __ldcg(ml + s).x);
+    const float2 x1 = lane + 32 < n ? __ldcg(ml + lane + 32) : make_float2(-INFINITY, 0.f);
+    float M = fmaxf(x0.x, x1.x);
+    for (int s = lane + 64; s < n; s += 32) M = fmaxf(M, __ldcg(ml + s).x);
     M = warp_max(M);
-    float acc[VW], L = 0.f;
+    const float w0 = x0.x == -INFINITY ? 0.f : exp2f(x0.x - M);  // 0 past the last split
+    const float w1 = x1.x == -INFINITY ? 0.f : exp2f(x1.x - M);
+    float L = fmaf(x0.y, w0, x1.y * w1);
+    float acc[VW];
 #pragma unroll
     for (int e = 0; e < VW; ++e) acc[e] = 0.f;
-    for (int s0 = 0; s0 < n; s0 += 32) {
-        float2 x = x0;
-        if (s0 > 0) x = s0 + lane < n ? __ldcg(ml + s0 + lane) : make_float2(-INFINITY, 0.f);
-        const float wt = x.x == -INFINITY ? 0.f : exp2f(x.x - M);  // 0 past the last split
-        L = fmaf(x.y, wt, L);
-        for (int k0 = 0; k0 < 32 && s0 + k0 < n; k0 += CHUNK) {
-            if (s0 + k0 > 0) {
 #pragma unroll
-                for (int k = 0; k < CHUNK; ++k)
-                    ldcg_vec<VW>(v[k], po + (long long)(s0 + k0 + k) * D, s0 + k0 + k < n);
-            }
+    for (int k = 0; k < CHUNK; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, k < 32 ? w0 : w1, k & 31);
 #pragma unroll
-            for (int k = 0; k < CHUNK; ++k) {
-                const float wk = __shfl_sync(0xffffffffu, wt, k0 + k);
+        for (int e = 0; e < VW; ++e) acc[e] = fmaf(v[k][e], wk, acc[e]);
+    }
+    for (int s0 = CHUNK; s0 < n; s0 += BLK) {
+        // splits s0 .. s0 + BLK - 1: rows, and the weights in lanes 0 .. BLK - 1
+        const int s = s0 + lane;
+        float2 x = lane < BLK && s < n ? __ldcg(ml + s) : make_float2(-INFINITY, 0.f);
+        const float wt = x.x == -INFINITY ? 0.f : exp2f(x.x - M);
+        if (s >= 64) L = fmaf(x.y, wt, L);  // splits below 64 are in w0, w1 already
 #pragma unroll
-                for (int e = 0; e < VW; ++e) acc[e] = fmaf(v[k][e], wk, acc[e]);
-            }
+        for (int k = 0; k < BLK; ++k) ldcg_vec<VW>(v[k], po + (long long)(s0 + k) * D, s0 + k < n);
+#pragma unroll
+        for (int k = 0; k < BLK; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, wt, k);
+#pragma unroll
+            for (int e = 0; e < VW; ++e) acc[e] = fmaf(v[k][e], wk, acc[e]);
         }
     }
     L = warp_sum(L);
