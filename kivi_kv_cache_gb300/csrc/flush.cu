@@ -30,10 +30,11 @@
 //    sends the rare near-tie element to an exact IEEE division (out of line).
 //    Byte permutes pack 8 codes per 32-bit word.
 //  * work is cut into 4 KB items (a key group's G tokens x 2048 / G channels,
-//    or 2048 / D value rows); each warp walks the items with a grid stride, staging
-//    two at a time in shared memory with cp.async, so the copy of the next
-//    item overlaps the quantization of the current one; the key loop takes
-//    two token rows per trip.
+//    or 2048 / D value rows; at G = 128 an 8 KB key item of 128 tokens x 32
+//    channels, so its row pieces are 64 bytes, not 32); each warp walks the
+//    items with a grid stride, staging two at a time in shared memory with
+//    cp.async, so the copy of the next item overlaps the quantization of the
+//    current one; the key loop takes two token rows per trip.
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
@@ -203,17 +204,32 @@ __device__ __forceinline__ void store_scales8(float* scale, long long m, const f
 // the quantization of the current one. Rows past n_flush are zero-filled and
 // never read from global memory.
 
-// A stage holds one 4 KB item; with G > 32 a key item's 8-token parts are padded
-// by one row (kNOc 16-byte chunks) so that the parts of a quarter warp read
-// different banks. Each warp has two stages.
+// Key items are 4 KB, except at G = 128, whose 4 KB item (128 tokens x 16
+// channels) reads 32-byte row pieces: its 8 KB item (128 tokens x 32
+// channels, 64-byte pieces) halves the rows per byte fetched.
+#ifndef KIVI_FLUSH_G128_ITEM
+#define KIVI_FLUSH_G128_ITEM 8192
+#endif
+__host__ __device__ constexpr int key_item_bytes(int G) { return G == 128 ? KIVI_FLUSH_G128_ITEM : 4096; }
+__host__ __device__ constexpr int key_item_channels(int G) { return key_item_bytes(G) / (2 * G); }
+
+// A stage holds one item; with G > 32 a key item's token parts are padded by
+// one row (kNOc 16-byte chunks) so that the parts of a quarter warp read
+// different banks (32 / kNOc parts of kNOc * 16 bytes). Each warp has two
+// stages.
 template <int G>
 struct Stage {
-    static constexpr int kBytes = G > 32 ? 4096 + 512 : 4096;
+    static constexpr int kBytes = key_item_bytes(G) + (G > 32 ? 32 * 16 : 0);
 };
 #ifndef KIVI_FLUSH_BLOCKS_PER_SM
 #define KIVI_FLUSH_BLOCKS_PER_SM 4
 #endif
-constexpr int kBlocksPerSm = KIVI_FLUSH_BLOCKS_PER_SM;  // resident CTAs per SM the grid is sized for
+// resident CTAs per SM the grid is sized for (three with 8 KB items: 68 KB of
+// stages per CTA)
+template <int G>
+__host__ __device__ constexpr int blocks_per_sm() {
+    return Stage<G>::kBytes > 6144 ? 3 : KIVI_FLUSH_BLOCKS_PER_SM;
+}
 #ifndef KIVI_FLUSH_KEY_UNROLL
 #define KIVI_FLUSH_KEY_UNROLL 2
 #endif
@@ -237,15 +253,16 @@ struct Items {
     int nv;          // value items per head
 };
 
-// Key items of group size G and head dim D: G tokens x kCh channels (4 KB); a
-// lane owns 8 tokens x 8 channels, lane = part * kNOc + oc.
+// Key items of group size G and head dim D: G tokens x kCh channels; a lane
+// owns kTPP tokens x 8 channels, lane = part * kNOc + oc.
 template <int G, int D>
 struct KeyShape {
-    static constexpr int kCh = 2048 / G;      // channels of an item: 64, 32 or 16
-    static constexpr int kNOc = kCh / 8;      // 8-channel octets: 8, 4 or 2
-    static constexpr int kNPart = 32 / kNOc;  // 8-token parts: 4, 8 or 16 (= G / 8)
-    static constexpr int kQ = D / kCh;        // items per key group: 1 to 16
-    static constexpr int kPad = G > 32 ? 1 : 0;  // pad rows per 8-token part in shared memory
+    static constexpr int kCh = key_item_channels(G);  // channels of an item: 64, 32, 32 (16 with 4 KB at G = 128)
+    static constexpr int kNOc = kCh / 8;              // 8-channel octets: 8, 4 or 4
+    static constexpr int kNPart = 32 / kNOc;          // token parts: 4, 8 or 8
+    static constexpr int kTPP = G / kNPart;           // tokens per part: 8, 8 or 16
+    static constexpr int kQ = D / kCh;                // items per key group: 1 to 16
+    static constexpr int kPad = G > 32 ? 1 : 0;       // pad rows per part in shared memory
     static_assert(kQ >= 1, "a key item spans at most the head dim");
 };
 
@@ -270,10 +287,10 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
                              qs * (KS::kCh * 2);
         constexpr int CPR = KS::kNOc;  // 16-byte chunks per token row
 #pragma unroll
-        for (int i = lane; i < 256; i += 32) {  // G rows x CPR chunks
+        for (int i = lane; i < G * CPR; i += 32) {  // G rows x CPR chunks
             const int row = i / CPR, col = i % CPR;
             const bool ok = g * G + row < k.n_flush;
-            cp_async16(st + ((row + KS::kPad * (row >> 3)) * CPR + col) * 16,
+            cp_async16(st + ((row + KS::kPad * (row / KS::kTPP)) * CPR + col) * 16,
                        ok ? (const void*)(src + row * RB + col * 16) : (const void*)src, ok);
         }
     } else {
@@ -300,16 +317,16 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     const int qs = u % KS::kQ, g = (u / KS::kQ) % it.ng, bh = (u / KS::kQ) / it.ng;
     const int oc = lane % KS::kNOc, part = lane / KS::kNOc;
     const int octet = qs * KS::kNOc + oc;
-    const int t0 = g * G + part * 8;
-    const int nv = min(8, a.n_flush - t0);  // may be <= 0 in a ragged last group
-    const uint4* xs = reinterpret_cast<const uint4*>(st) + (part * (8 + KS::kPad)) * KS::kNOc + oc;  // row stride kNOc
+    const int t0 = g * G + part * KS::kTPP;
+    const int nv = min(KS::kTPP, a.n_flush - t0);  // may be <= 0 in a ragged last group
+    const uint4* xs = reinterpret_cast<const uint4*>(st) + (part * (KS::kTPP + KS::kPad)) * KS::kNOc + oc;  // row stride kNOc
 
     const __half2 pinf = __half2half2(__ushort_as_half(0x7c00));
     const __half2 ninf = __half2half2(__ushort_as_half(0xfc00));
     __half2 mn[4] = {pinf, pinf, pinf, pinf};
     __half2 mx[4] = {ninf, ninf, ninf, ninf};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < KS::kTPP; ++i) {
         if (i < nv) {
             const uint4 x = xs[i * KS::kNOc];
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -657,7 +674,7 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
 // Keys, values, or both: warp w of the grid handles items w, w + W, ... of the
 // list [key items | value items] (W = total warps).
 template <int BITS, int MODE, int G, int D>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
+__global__ void __launch_bounds__(kThreads, blocks_per_sm<G>()) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kStageBytes = Stage<G>::kBytes;
@@ -699,7 +716,7 @@ cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             sms = 152;
-        grid_cap = sms * kBlocksPerSm;
+        grid_cap = sms * blocks_per_sm<G>();
         configured = true;
     }
     const long long total = (long long)it.key_items + it.val_items;
@@ -753,7 +770,7 @@ cudaError_t launch_flush_impl(const FlushArgs& k, const FlushArgs& v, bool do_k,
     const int G = a.G, D = a.D;
     const int rows = 2048 / D;  // token rows per value item
     const int ng = (a.n_flush + G - 1) / G, nv = (a.n_flush + rows - 1) / rows;
-    const int kq = D / (2048 / G);  // key items per group
+    const int kq = D / key_item_channels(G);  // key items per group
     const int per_head = (do_k ? kq * ng : 0) + (do_v ? nv : 0);
     const int max_heads = (int)(0x3fffffff / per_head) > 0 ? (int)(0x3fffffff / per_head) : 1;
     for (int h0 = 0; h0 < a.BH; h0 += max_heads) {
