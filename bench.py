@@ -63,6 +63,7 @@ MIN_OP_MS = 50.0
 PROFILE_CASES = {
     "flush_long2bit": ("flush", 0, 0, 0, 2),
     "flush_long2bit_g128": ("flush", 0, 0, 0, 2),
+    "flush_long2bit_f16s": ("flush", 0, 0, 0, 2),
     "flush_qwen8b": ("flush", 0, 0, 0, 4),
     "decode_b1_4k": ("decode", 1, 4096 - 128, 128, 4),
     "decode_b1_16k": ("decode", 1, 16384 - 128, 128, 4),
@@ -1131,10 +1132,11 @@ def run_profile_case(name: str, reps: int = 3):
         w = synth.WORKLOADS[parts[1]]
         if len(parts) > 2 and parts[2].startswith("g"):
             w = dataclasses.replace(w, G=int(parts[2][1:]))
+        hs = parts[-1] == "f16s"  # fp16 scale storage
         n = kv.kivi_flush_count(w.S, w.R, w.G)
         k, v, _ = synth.prefill_inputs_torch(w, 1, dev)
-        ks = kv.KiviStore(0, w.BH, n, w.D, w.G, w.bits, device=dev)
-        vs = kv.KiviStore(1, w.BH, n, w.D, w.G, w.bits, device=dev)
+        ks = kv.KiviStore(0, w.BH, n, w.D, w.G, w.bits, device=dev, scale_f16=hs)
+        vs = kv.KiviStore(1, w.BH, n, w.D, w.G, w.bits, device=dev, scale_f16=hs)
         for _ in range(reps):
             kv.kivi_flush_kv(k, v, w.R, ks, vs)
     else:

@@ -35,6 +35,8 @@
 //    items with a grid stride, staging two at a time in shared memory with
 //    cp.async, so the copy of the next item overlaps the quantization of the
 //    current one; the key loop takes two token rows per trip.
+#include <type_traits>
+
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
@@ -123,24 +125,32 @@ __device__ __forceinline__ void quant8_codes(const uint4 xv, const f32x2 (&z2)[4
     }
 }
 
-// With an fp16 scale (HS) a subnormal stored scale can leave a quotient past
+// With an fp16 scale a subnormal stored scale can leave a quotient past
 // 2^BITS - 1 (up to about 1.5 (2^BITS - 1)): clip the codes, whose fp32
 // patterns 2^23 + q order like q.
-template <int BITS, bool HS>
+template <int BITS>
 __device__ __forceinline__ void clip8(uint32_t (&tb)[8]) {
-    if (HS) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) tb[i] = min(tb[i], 0x4B000000u + (uint32_t)Levels<BITS>::value);
-    }
+    for (int i = 0; i < 8; ++i) tb[i] = min(tb[i], 0x4B000000u + (uint32_t)Levels<BITS>::value);
 }
 
+// Only a scale below the smallest normal fp16 (2^-14) can push a code past
+// 2^BITS - 1 once rounded to fp16: a normal fp16 scale lies within a relative
+// 2^-11 of the fp32 one, and every a is at most max - min, so a / s stays
+// below L (1 + 2^-10) < L + 1/2. The decision is taken per warp (a vote over
+// its active lanes), so warps without such a scale run the unclipped loop.
+__device__ __forceinline__ bool warp_has_subnormal_scale(bool lane_has) {
+    return __any_sync(__activemask(), lane_has);
+}
+constexpr float kMinNormalF16 = 6.103515625e-05f;  // 2^-14
+
 // The codes of quant8_codes packed into BITS*8 bits.
-template <int BITS, bool HS>
+template <int BITS, bool CLIP>
 __device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
                                            const float (&s)[8]) {
     uint32_t tb[8];
     quant8_codes(xv, z2, r2, s, tb);
-    clip8<BITS, HS>(tb);
+    if (CLIP) clip8<BITS>(tb);
     return pack8<BITS>(tb);
 }
 
@@ -149,12 +159,12 @@ __device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4],
 // That Made My LLM Exactly 0% Faster", "What we're actually optimizing";
 // multiply, then a separate add: "Three ways to be off by one bit" #1).
 // With tb = bits of 2^23 + q, fma(2^23 + q, s, -2^23 s) is q * s rounded once.
-template <int BITS, bool HS>
+template <int BITS, bool CLIP>
 __device__ __forceinline__ uint4 fake8(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
                                        const float (&s)[8]) {
     uint32_t tb[8];
     quant8_codes(xv, z2, r2, s, tb);
-    clip8<BITS, HS>(tb);
+    if (CLIP) clip8<BITS>(tb);
     uint32_t h[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -388,10 +398,19 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         z2[k] = pk(z[2 * k], z[2 * k + 1]);
         r2[k] = pk(r[2 * k], r[2 * k + 1]);
     }
+    // every scale of the item was computed by some lane (my_s), so the vote covers them all
+    bool small = false;
+#pragma unroll
+    for (int c = 0; c < CPP; ++c) small |= my_s[c] < kMinNormalF16;
+    const bool clip = HS && warp_has_subnormal_scale(small);
     if (FAKE) {
         uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * D) + octet;
+        auto rows = [&](auto cl) {
 #pragma unroll 1
-        for (int i = 0; i < nv; ++i) frow[i * (D / 8)] = fake8<BITS, HS>(xs[i * KS::kNOc], z2, r2, s);
+            for (int i = 0; i < nv; ++i) frow[i * (D / 8)] = fake8<BITS, decltype(cl)::value>(xs[i * KS::kNOc], z2, r2, s);
+        };
+        if (clip) rows(std::true_type{});
+        else rows(std::false_type{});
         return;
     }
     if (part == 0) {
@@ -410,8 +429,12 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
         else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
     };
+    auto rows = [&](auto cl) {
 #pragma unroll (kKeyUnroll)
-    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, HS>(xs[i * KS::kNOc], z2, r2, s));
+        for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, decltype(cl)::value>(xs[i * KS::kNOc], z2, r2, s));
+    };
+    if (clip) rows(std::true_type{});
+    else rows(std::false_type{});
 }
 
 // min and max of the 8 fp16 of each vector of x, as half2 (min and max of fp16
@@ -478,14 +501,25 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
         const f32x2 z2[4] = {z1, z1, z1, z1}, r2[4] = {r1, r1, r1, r1};
         const float sv[8] = {sc, sc, sc, sc, sc, sc, sc, sc};
         const int j = (64 * jp + (G == 32 ? 32 * e : 0)) / G;  // this group's index in the row
+        const bool clip = HS && warp_has_subnormal_scale(sc < kMinNormalF16);
         if (FAKE) {
             uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * D) + cv;
+            if (clip) {
 #pragma unroll
-            for (int k = 0; k < NVEC; ++k) frow[k] = fake8<BITS, HS>(x[k], z2, r2, sv);
+                for (int k = 0; k < NVEC; ++k) frow[k] = fake8<BITS, true>(x[k], z2, r2, sv);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NVEC; ++k) frow[k] = fake8<BITS, false>(x[k], z2, r2, sv);
+            }
         } else {
             uint32_t pq[NVEC];
+            if (clip) {
 #pragma unroll
-            for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS, HS>(x[k], z2, r2, sv);
+                for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS, true>(x[k], z2, r2, sv);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS, false>(x[k], z2, r2, sv);
+            }
             uint8_t* cdst = a.codes + grow * (D * BITS / 8) + cv * BITS;  // 8 channels per vector
             if (BITS == 4) {
 #pragma unroll
@@ -583,10 +617,16 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
         z2[k] = pk(z[2 * k], z[2 * k + 1]);
         r2[k] = pk(r[2 * k], r[2 * k + 1]);
     }
+    // every scale of the item was computed by some lane (my_s), so the vote covers them all
+    const bool clip = HS && warp_has_subnormal_scale(my_s[0] < kMinNormalF16 || my_s[1] < kMinNormalF16);
     if (FAKE) {
         uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * kD) + octet;
+        auto rows = [&](auto cl) {
 #pragma unroll 1
-        for (int i = 0; i < nv; ++i) frow[i * (kD / 8)] = fake8<BITS, HS>(xs[i * 8], z2, r2, s);
+            for (int i = 0; i < nv; ++i) frow[i * (kD / 8)] = fake8<BITS, decltype(cl)::value>(xs[i * 8], z2, r2, s);
+        };
+        if (clip) rows(std::true_type{});
+        else rows(std::false_type{});
         return;
     }
     if (part == 0) {
@@ -605,8 +645,12 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
         if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
         else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
     };
+    auto rows = [&](auto cl) {
 #pragma unroll (kKeyUnroll)
-    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, HS>(xs[i * 8], z2, r2, s));
+        for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, decltype(cl)::value>(xs[i * 8], z2, r2, s));
+    };
+    if (clip) rows(std::true_type{});
+    else rows(std::false_type{});
 }
 
 // G = 32 values: lane = 16 jp + row; the lane quantizes the groups j = 2 jp and
@@ -648,10 +692,16 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
         const f32x2 z1 = pk(z, z), r1 = pk(rc, rc);
         const f32x2 z2[4] = {z1, z1, z1, z1}, r2[4] = {r1, r1, r1, r1};
         const float sv[8] = {sc, sc, sc, sc, sc, sc, sc, sc};
+        const bool clip = HS && warp_has_subnormal_scale(sc < kMinNormalF16);
         if (FAKE) {
             uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * kD + 32 * j);
+            if (clip) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) frow[k] = fake8<BITS, HS>(x[k], z2, r2, sv);
+                for (int k = 0; k < 4; ++k) frow[k] = fake8<BITS, true>(x[k], z2, r2, sv);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) frow[k] = fake8<BITS, false>(x[k], z2, r2, sv);
+            }
         } else {
             auto store_group = [&](const uint32_t (&pq)[4]) {
                 if (BITS == 4) {
@@ -662,8 +712,13 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
                 }
             };
             uint32_t pq[4];
+            if (clip) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS, HS>(x[k], z2, r2, sv);
+                for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS, true>(x[k], z2, r2, sv);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS, false>(x[k], z2, r2, sv);
+            }
             store_group(pq);
             store_scale<HS>(a.scale, grow * (kD / kG) + j, sc);
             a.zero[grow * (kD / kG) + j] = __float2half_rn(z);
