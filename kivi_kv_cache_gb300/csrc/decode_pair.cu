@@ -683,12 +683,15 @@ int pair_cluster_ctas(int n, cudaStream_t stream) {
 }
 
 // The splits of a head merge inside a cluster when the whole grid fits in one
-// wave of resident clusters (the kernel serves small batches).
+// wave of resident clusters (the kernel serves small batches) and has at
+// least as many CTAs as SMs; a smaller grid spreads one CTA per SM and merges
+// through the workspace (13 splits at B=1: 6.1 us against 6.9 in clusters).
 template <int BITS, int GQ>
 cudaError_t launch_pair_typed(const DecodeArgs& a, cudaStream_t stream) {
     const dim3 grid(a.n_split, a.Hkv, a.B);
     const int n = a.n_split;
-    if (n >= 2 && n <= kMaxClusterSplits && (long long)n * a.Hkv * a.B <= pair_cluster_ctas<BITS, GQ>(n, stream)) {
+    const long long ctas = (long long)n * a.Hkv * a.B;
+    if (n >= 2 && n <= kMaxClusterSplits && ctas >= sm_count() && ctas <= pair_cluster_ctas<BITS, GQ>(n, stream)) {
         cudaError_t e = configure_pair<BITS, GQ, true>();
         if (e != cudaSuccess) return e;
         return launch_pdl_cluster(decode_pair_kernel<BITS, GQ, true>, grid, kThreads, kSmemBytes, stream, n, a);

@@ -13,11 +13,11 @@
 using namespace kivi;
 
 namespace {
-
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
+}  // namespace
 
-int sm_count() {
+int kivi::sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
@@ -33,6 +33,8 @@ int sm_count() {
     }
     return n;
 }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

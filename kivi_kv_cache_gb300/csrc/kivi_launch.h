@@ -144,6 +144,10 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(Exp...), dim3 grid, dim3 bl
 // width (bits may carry KIVI_SCALE_F16) outside the compiled set.
 int shape_status(int D, int group_size, int bits);
 
+// Streaming multiprocessors of the current device (152 when no device is
+// visible), read once per device.
+int sm_count();
+
 // Workspace bytes of the exact plan kivi_decode_attend takes for these
 // arguments (bits may carry KIVI_SCALE_F16); 0 for a single-split plan or
 // for arguments the decode rejects. kivi_decode_workspace_size is the

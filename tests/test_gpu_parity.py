@@ -288,6 +288,29 @@ def test_decode_edge_shapes(S_q, n_res, bits, hq, hkv):
     assert err <= TOL, err
 
 
+@pytest.mark.parametrize("B,S_q,n_res,bits", [
+    (1, 1472, 64, 4),    # warp pairs, 13 splits, fewer CTAs than SMs: workspace merge
+    (4, 960, 64, 4),     # warp pairs, 9 splits over 288 CTAs: cluster merge where resident
+    (8, 960, 64, 2),     # the same, 2-bit, 576 CTAs
+    (1, 3008, 64, 4),    # one warp per tile, 13 splits, 104 CTAs: workspace merge
+    (4, 4032, 64, 4),    # one warp per tile, 9 splits over 288 CTAs: cluster merge
+    (16, 1920, 128, 2),  # one warp per tile, 4 splits over 512 CTAs: cluster merge
+])
+def test_decode_merge_paths(B, S_q, n_res, bits):
+    """Shapes on both sides of the grid-size rule that picks the split merge
+    (cluster or workspace ticket) for each decode kernel; every output is
+    checked against the oracle."""
+    w = synth.Workload("merge", B=B, Hkv=8, Hq=32, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
+                       n_outlier=4, outlier_scale=8.0, seed=B * 31 + S_q % 97)
+    rng = np.random.default_rng(w.seed)
+    k = synth.keys(rng, (w.BH, S_q + n_res), 128, synth.outlier_channels(w), 8.0)
+    v = synth.normal(rng, (w.BH, S_q + n_res, 128))
+    q = synth.normal(rng, (B, 32, 128))
+    out, ref = decode_case(w, S_q, n_res, k, v, q)
+    err = np.max(np.abs(out - ref))
+    assert err <= TOL, err
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("hq,hkv", [(16, 2), (6, 2)])
 def test_decode_subgroups_many_splits(hq, hkv, bits):
