@@ -274,7 +274,7 @@ size_t kivi_decode_workspace_size(int B, int Hq, int Hkv, int S_q, int n_res, in
  *       32, head dim 128, fp32 scales, 1, 2 or 4 query heads per KV head)
  *   [1] n_split: CTAs per head group, merged in the same launch
  *   [2] tiles per warp (per warp pair for the pair kernel)
- *   [3] warps per CTA
+ *   [3] warps per CTA (2, 4 or 8; the pair kernel: 8, four pairs)
  *   [4] query sub-groups per KV head (1, or ceil(Hq/Hkv / 4))
  *   [5] tiles per head group: ceil(S_q / 32) store + ceil(n_res / 16) residual
  *   [6] tiles per split

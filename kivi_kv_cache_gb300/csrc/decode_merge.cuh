@@ -59,27 +59,15 @@ __device__ __forceinline__ void ldcg_vec(float (&v)[VW], const float* p, bool on
     }
 }
 
-// Merge of the n_split partials of query heads bq0 .. bq0 + nheads - 1
-// (nheads <= 4) by the NW warps (4 or 8) of the CTA holding the last ticket:
-// warp w takes head w % 4 and channel slice w / 4 of the NW / 4 slices of a
-// row, over every split. A lane holds VW consecutive channels of the slice.
-// The first CHUNK partial rows (up to 80 registers' worth: 40 rows at
-// VW <= 2) are requested together with the (m, l) pairs of splits lane and
-// lane + 32, so up to CHUNK splits cost one L2 round trip; row s takes its
-// weight 2^(m_s - M) from lane s % 32 by shuffle. Splits past CHUNK follow in
-// blocks of 32. No barrier inside.
+// One head of the merge below: warp-level, channel slice sl of the row.
 template <int NW, int D>
-__device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0, int nheads, int warp, int lane) {
-    static_assert(NW == 4 || NW == 8, "4 or 8 warps");
-    constexpr int SL = NW / 4;       // channel slices per row
+__device__ __forceinline__ void merge_one(const DecodeArgs& a, long long bq, int sl, int lane) {
+    constexpr int SL = NW >= 4 ? NW / 4 : 1;  // channel slices per row
     constexpr int CW = D / SL;       // channels per slice
     constexpr int VW = CW / 32;      // channels per lane
     static_assert(VW >= 1 && VW <= 8 && CW % 32 == 0, "a slice is 32 to 256 channels");
     constexpr int CHUNK = VW <= 2 ? 40 : (VW == 4 ? 16 : 8);  // rows of the first round trip
     constexpr int BLK = VW <= 2 ? 32 : CHUNK;                  // rows per later round trip
-    const int h = warp & 3, sl = warp >> 2;
-    if (h >= nheads) return;
-    const long long bq = bq0 + h;
     const int n = a.n_split;
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + bq * n;
     const float* po = a.part_o + bq * n * D + sl * CW + lane * VW;
@@ -131,6 +119,29 @@ __device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0,
             reinterpret_cast<float4*>(out)[e] =
                 make_float4(acc[4 * e] * r, acc[4 * e + 1] * r, acc[4 * e + 2] * r, acc[4 * e + 3] * r);
     }
+}
+
+// Merge of the n_split partials of query heads bq0 .. bq0 + nheads - 1
+// (nheads <= 4) by the NW warps (2, 4 or 8) of the CTA holding the last
+// ticket: with 4 or 8 warps, warp w takes head w % 4 and channel slice w / 4
+// of the NW / 4 slices of a row; with 2 warps, warp w takes heads w and
+// w + 2 in turn, whole rows. A lane holds VW consecutive channels of the
+// slice.
+// The first CHUNK partial rows (up to 80 registers' worth: 40 rows at
+// VW <= 2) are requested together with the (m, l) pairs of splits lane and
+// lane + 32, so up to CHUNK splits cost one L2 round trip; row s takes its
+// weight 2^(m_s - M) from lane s % 32 by shuffle. Splits past CHUNK follow in
+// blocks of 32. No barrier inside.
+template <int NW, int D>
+__device__ __forceinline__ void merge_splits(const DecodeArgs& a, long long bq0, int nheads, int warp, int lane) {
+    static_assert(NW == 2 || NW == 4 || NW == 8, "2, 4 or 8 warps");
+    if (NW == 2) {  // each warp merges two heads in turn
+        for (int h = warp; h < nheads; h += 2) merge_one<NW, D>(a, bq0 + h, 0, lane);
+        return;
+    }
+    const int h = warp & 3, sl = warp >> 2;
+    if (h >= nheads) return;
+    merge_one<NW, D>(a, bq0 + h, sl, lane);
 }
 
 }  // namespace kivi

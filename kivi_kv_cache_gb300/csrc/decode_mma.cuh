@@ -35,7 +35,7 @@
 //   * a per-tile power-of-two factor keeps every hi below 2^14 (no fp16
 //     overflow for any finite input); it is divided out exactly afterwards.
 //
-// Work split: grid (n_split, Hkv * q_sub, B), 4 or 8 warps per CTA; each warp owns a
+// Work split: grid (n_split, Hkv * q_sub, B), 2, 4 or 8 warps per CTA; each warp owns a
 // contiguous run of tiles of its split (32-token store tiles, then 16-token
 // residual tiles) and keeps its own online softmax; the warps merge in shared
 // memory and the CTA writes one partial (or the output when n_split == 1; the
@@ -47,7 +47,8 @@
 // warps) of shared memory per CTA, 16 warps per SM either way; D = 64 halves
 // the stages, D = 256 doubles them and runs 8 warps per SM. 8-warp CTAs halve
 // the partials a merge reads; the plan takes them when 4-warp CTAs would leave
-// more than 16 splits.
+// more than 16 splits. 2-warp CTAs (27 KB, D = 128 only) split a head group
+// finer when short warp runs would otherwise leave a ragged wave.
 // MMA layouts (m16n8k16, row.col): lane = 4 g + c; A regs hold (row g,
 // k 2c..2c+1), (row g+8, same k), (row g, k 2c+8..9), (row g+8, k 2c+8..9);
 // B regs (k 2c..2c+1, n g), (k 2c+8..9, n g); C regs (row g, n 2c..2c+1),
@@ -299,7 +300,7 @@ __device__ __forceinline__ void cta_heads(const DecodeArgs& a, int& h0, int& nh)
     }
 }
 
-// NW warps per CTA (4 or 8): 16 warps per SM either way at 128 registers
+// NW warps per CTA (2, 4 or 8): 16 warps per SM at 128 registers
 // (D <= 128), or 8 at up to 255 registers (D = 256).
 // CL: the n_split CTAs of a (batch, KV head) form one thread-block cluster
 // (n_split <= kMaxClusterSplits) and merge through distributed shared memory.
@@ -1108,6 +1109,9 @@ cudaError_t launch_mma_typed(const DecodeArgs& a, cudaStream_t stream) {
 
 template <int BITS, int GQ, int D, bool HS>
 cudaError_t launch_mma_warps(const DecodeArgs& a, cudaStream_t stream) {
+    if constexpr (D == 128) {
+        if (a.warps_per_cta == 2) return launch_mma_typed<BITS, GQ, 2, D, HS>(a, stream);
+    }
     return a.warps_per_cta == 8 ? launch_mma_typed<BITS, GQ, 8, D, HS>(a, stream)
                                 : launch_mma_typed<BITS, GQ, 4, D, HS>(a, stream);
 }

@@ -115,6 +115,11 @@ constexpr bool kOneWave = KIVI_DECODE_ONE_WAVE != 0;
 #define KIVI_DECODE_BALANCE 1
 #endif
 constexpr bool kBalance = KIVI_DECODE_BALANCE != 0;
+#ifndef KIVI_DECODE_SHORT_RUNS
+#define KIVI_DECODE_SHORT_RUNS 1
+#endif
+constexpr bool kShortRuns = KIVI_DECODE_SHORT_RUNS != 0;
+constexpr long long kShortRunTiles = 8;  // longest warp run the 2-warp plan serves
 
 bool mma_group(int gq) { return gq == 1 || gq == 2 || gq == 4; }
 
@@ -191,6 +196,31 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool 
                 p.n_split = (int)n2;
                 p.tiles_per_split = (p.n_tiles + p.n_split - 1) / p.n_split;
                 p.tiles_per_warp = (p.tiles_per_split + p.warps_per_cta - 1) / p.warps_per_cta;
+            }
+        }
+    }
+    if (kShortRuns && !p.pair_kernel && heads <= kMergeCounters && D == 128) {
+        // Short warp runs on a grid of 4- or 8-warp CTAs that spills past
+        // one wave, or that leaves each warp a third more tiles than a finer
+        // split would: 2-warp CTAs (8 per SM) fill one wave with more splits
+        // per head group, so its warps' runs are shorter (B=16 x 3072 tokens:
+        // 27.1 -> 24.6 us). At equal or nearly equal runs the extra partials
+        // and CTA merges cost more than they save, so the plan stays.
+        const long long S = sm_count();
+        const long long slots = (long long)(16 / p.warps_per_cta) * S;
+        const long long ctas = heads * p.n_split;
+        const long long tpw = (p.tiles_per_split + p.warps_per_cta - 1) / p.warps_per_cta;
+        const long long run = ((ctas + slots - 1) / slots) * tpw;  // tiles a warp slot runs
+        long long n2 = 8 * S / heads;
+        if (n2 > p.n_tiles) n2 = p.n_tiles;
+        if (n2 >= 1) {
+            const long long tps2 = (p.n_tiles + n2 - 1) / n2;
+            const long long run2 = (tps2 + 1) / 2;
+            if (run2 <= kShortRunTiles && (ctas > slots ? run2 < run : 3 * run2 <= 2 * run)) {
+                p.warps_per_cta = 2;
+                p.n_split = (int)((p.n_tiles + tps2 - 1) / tps2);
+                p.tiles_per_split = (int)tps2;
+                p.tiles_per_warp = (int)run2;
             }
         }
     }

@@ -66,7 +66,7 @@ struct DecodeArgs {
     int n_split;
     int tiles_per_split;  // planned tiles per split (the kernels spread n_tiles evenly)
     int tiles_per_warp;   // planned tiles per warp of the one-warp-per-tile kernel
-    int warps_per_cta;    // one-warp-per-tile kernel: 4 or 8
+    int warps_per_cta;    // one-warp-per-tile kernel: 2 (head dim 128 only), 4 or 8
     int pair_kernel;      // 1: groups of 1, 2 or 4 heads run the warp-pair kernel
     int n_store_tiles;
     int n_tiles;

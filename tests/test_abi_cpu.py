@@ -244,7 +244,7 @@ def test_decode_plan_rules(L):
                         assert p["warps_per_cta"] == 8
                     else:
                         seen_mma += 1
-                        assert p["warps_per_cta"] in (4, 8)
+                        assert p["warps_per_cta"] in ((2, 4, 8) if D == 128 else (4, 8))
                     if B * hkv * p["q_sub"] > 8192:
                         seen_one_split += 1
                         assert p["n_split"] == 1  # more head groups than merge counters: one split each
@@ -258,6 +258,15 @@ def test_decode_plan_rules(L):
         p = kv.kivi_decode_plan_info(1, 32, 8, S_q, 128, bits=bits)
         assert p["pair_kernel"] == 0 and p["warps_per_cta"] == 8
         assert 8 * p["n_split"] == 2 * 152, (S_q, p)
+    # short warp runs at B=16: 2-warp CTAs, 8 per SM, one wave, shorter runs
+    # than the 4-warp plan (which spilled past one wave or left longer runs)
+    for S_q, n_res in ((1408, 128), (2944, 128), (3968, 128), (896, 128)):
+        p = kv.kivi_decode_plan_info(16, 32, 8, S_q, n_res)
+        assert p["warps_per_cta"] == 2 and 16 * 8 * p["n_split"] <= 8 * 152, (S_q, p)
+        assert p["tiles_per_warp"] <= 8
+    for S_q, n_res in ((1920, 128), (3456, 128)):  # one wave, runs nearly as short already: unchanged
+        assert kv.kivi_decode_plan_info(16, 32, 8, S_q, n_res)["warps_per_cta"] == 4
+    assert kv.kivi_decode_plan_info(32, 32, 8, 4032, 64)["warps_per_cta"] == 4  # long runs: unchanged
     # the qwen8b decode takes the warp-pair kernel; stores of another group
     # size or head dim, or with fp16 scales, the one-warp-per-tile kernel
     assert kv.kivi_decode_plan_info(1, 32, 8, 2080, 158)["pair_kernel"] == 1

@@ -295,11 +295,14 @@ def test_decode_edge_shapes(S_q, n_res, bits, hq, hkv):
     (1, 3008, 64, 4),    # one warp per tile, 13 splits, 104 CTAs: workspace merge
     (4, 4032, 64, 4),    # one warp per tile, 9 splits over 288 CTAs: cluster merge
     (16, 1920, 128, 2),  # one warp per tile, 4 splits over 512 CTAs: cluster merge
+    (16, 1408, 128, 4),  # 2-warp CTAs, 9 splits over 1152 CTAs
+    (16, 896, 128, 2),   # 2-warp CTAs, 2-bit
+    (8, 8064, 128, 4),   # 2-warp CTAs, 19 splits: workspace merge
 ])
 def test_decode_merge_paths(B, S_q, n_res, bits):
     """Shapes on both sides of the grid-size rule that picks the split merge
-    (cluster or workspace ticket) for each decode kernel; every output is
-    checked against the oracle."""
+    (cluster or workspace ticket) for each decode kernel, and plans of 2-, 4-
+    and 8-warp CTAs; every output is checked against the oracle."""
     w = synth.Workload("merge", B=B, Hkv=8, Hq=32, D=128, S=S_q + n_res, bits=bits, G=32, R=0,
                        n_outlier=4, outlier_scale=8.0, seed=B * 31 + S_q % 97)
     rng = np.random.default_rng(w.seed)
