@@ -320,6 +320,7 @@ class Instance:
         need = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, self.n_flush, self.n_res, w.D)
         self.ws = kv.kivi_decode_workspace(need, device)
         self.side = torch.cuda.Stream(device=device)
+        self.own = torch.cuda.Stream(device=device)  # this instance's branch in the timed graphs
         self.flushed = torch.cuda.Event()
 
     def op(self, name):
@@ -335,12 +336,11 @@ class Instance:
             kv.kivi_decode_attend(self.q, self.kst, self.vst, self.n_flush, self.kres, self.vres, self.n_res, w.Hkv,
                                   w.sm_scale, out=self.out, workspace=self.ws)
 
-    def step(self, join=True):
+    def step(self):
         """One pass of the hot path. The flush and the dequant run on the
         current stream; the residual append and the decode (which needs the
         flushed store) run on a side stream beside the dequant; the side
-        stream joins the current one at the end (or, with join=False, when the
-        caller joins it, so independent steps may overlap)."""
+        stream joins the current one at the end."""
         import torch
         main = torch.cuda.current_stream()
         self.side.wait_stream(main)
@@ -352,8 +352,7 @@ class Instance:
         with torch.cuda.stream(self.side):
             self.side.wait_event(self.flushed)
             self.op("decode_attend")
-        if join:
-            main.wait_stream(self.side)
+        main.wait_stream(self.side)
 
     def nbytes(self):
         ts = [self.k, self.v, self.q, self.kres, self.vres, self.kdq, self.vdq, self.out, self.ws,
@@ -397,11 +396,17 @@ class StepBench:
         torch.cuda.synchronize()
 
         def steps(j):
+            # independent steps on parallel branches: each instance's step on
+            # its own stream (flush -> dequant; append -> decode after the
+            # flush), all joined at the end of the graph
             group = self.insts[j * GRAPH_STEPS:(j + 1) * GRAPH_STEPS]
+            cur = torch.cuda.current_stream()
             for inst in group:
-                inst.step(join=False)
+                inst.own.wait_stream(cur)
+                with torch.cuda.stream(inst.own):
+                    inst.step()
             for inst in group:
-                torch.cuda.current_stream().wait_stream(inst.side)
+                cur.wait_stream(inst.own)
 
         self.multi = [capture(lambda j=j: steps(j)) for j in range(self.pool // GRAPH_STEPS)]
         self.single = [capture(lambda I=I: I.step()) for I in self.insts]
@@ -801,7 +806,8 @@ def run_gb300(args, rank, world, local_rank):
         "config": {"workload": workload_label(w),
                    "n_flush": summ["n_flush"], "n_res": summ["n_res"],
                    "l2": summ["pool"],
-                   "timing": "graphs of %d steps on distinct instances, K steps between CUDA events" % GRAPH_STEPS,
+                   "timing": "graphs of %d independent steps on distinct instances, each on its own stream branch, "
+                             "K steps between CUDA events" % GRAPH_STEPS,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "ops": summ["ops"],
         "decode_tokens_per_s": summ["decode_tokens_per_s"],
