@@ -54,6 +54,7 @@ if ROOT not in sys.path:
 METRIC = "KIVI flush/dequant/decode-attend HBM GB/s (% of peak); decode tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 GRAPH_STEPS = 8
+GRAPH_BRANCHES = 4  # parallel stream branches per timed graph (two steps each)
 MIN_OP_LAUNCHES = 256
 MIN_OP_MS = 50.0
 
@@ -320,7 +321,6 @@ class Instance:
         need = kv.kivi_decode_workspace_size(w.B, w.Hq, w.Hkv, self.n_flush, self.n_res, w.D)
         self.ws = kv.kivi_decode_workspace(need, device)
         self.side = torch.cuda.Stream(device=device)
-        self.own = torch.cuda.Stream(device=device)  # this instance's branch in the timed graphs
         self.flushed = torch.cuda.Event()
 
     def op(self, name):
@@ -395,18 +395,22 @@ class StepBench:
             self.insts[i % self.pool].step()
         torch.cuda.synchronize()
 
+        branches = [torch.cuda.Stream(device=self.dev) for _ in range(GRAPH_BRANCHES)]
+
         def steps(j):
-            # independent steps on parallel branches: each instance's step on
-            # its own stream (flush -> dequant; append -> decode after the
-            # flush), all joined at the end of the graph
+            # the graph's independent steps on GRAPH_BRANCHES parallel stream
+            # branches (step t on branch t % GRAPH_BRANCHES; within a step the
+            # flush -> dequant chain and, after the flush, the decode), all
+            # joined at the end of the graph
             group = self.insts[j * GRAPH_STEPS:(j + 1) * GRAPH_STEPS]
             cur = torch.cuda.current_stream()
-            for inst in group:
-                inst.own.wait_stream(cur)
-                with torch.cuda.stream(inst.own):
+            for b in branches:
+                b.wait_stream(cur)
+            for t, inst in enumerate(group):
+                with torch.cuda.stream(branches[t % GRAPH_BRANCHES]):
                     inst.step()
-            for inst in group:
-                cur.wait_stream(inst.own)
+            for b in branches:
+                cur.wait_stream(b)
 
         self.multi = [capture(lambda j=j: steps(j)) for j in range(self.pool // GRAPH_STEPS)]
         self.single = [capture(lambda I=I: I.step()) for I in self.insts]
@@ -806,8 +810,8 @@ def run_gb300(args, rank, world, local_rank):
         "config": {"workload": workload_label(w),
                    "n_flush": summ["n_flush"], "n_res": summ["n_res"],
                    "l2": summ["pool"],
-                   "timing": "graphs of %d independent steps on distinct instances, each on its own stream branch, "
-                             "K steps between CUDA events" % GRAPH_STEPS,
+                   "timing": "graphs of %d independent steps on distinct instances over %d stream branches, "
+                             "K steps between CUDA events" % (GRAPH_STEPS, GRAPH_BRANCHES),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "ops": summ["ops"],
         "decode_tokens_per_s": summ["decode_tokens_per_s"],
