@@ -314,6 +314,34 @@ def test_decode_merge_paths(B, S_q, n_res, bits):
     assert err <= TOL, err
 
 
+@pytest.mark.parametrize("B,Hq,S_q,n_res,hs", [
+    (16, 32, 1408, 128, True),   # 2-warp CTAs, fp16 scales
+    (8, 64, 1408, 128, False),   # 2-warp CTAs, sub-groups of 4 of 8 heads per KV head
+    (16, 8, 1408, 128, False),   # 2-warp CTAs, one head per KV head
+])
+def test_decode_two_warp_plans(B, Hq, S_q, n_res, hs):
+    """Plans of 2-warp CTAs for other scale storage and head groups, against
+    the oracle."""
+    assert kv.kivi_decode_plan_info(B, Hq, 8, S_q, n_res, 128, 32, 4, hs)["warps_per_cta"] == 2
+    w = synth.Workload("w2", B=B, Hkv=8, Hq=Hq, D=128, S=S_q + n_res, bits=4, G=32, R=0, n_outlier=4,
+                       outlier_scale=8.0, seed=B + Hq)
+    rng = np.random.default_rng(w.seed)
+    k = synth.keys(rng, (w.BH, S_q + n_res), 128, synth.outlier_channels(w), 8.0)
+    v = synth.normal(rng, (w.BH, S_q + n_res, 128))
+    q = synth.normal(rng, (B, Hq, 128))
+    gk = kv.KiviStore(0, w.BH, S_q, 128, 32, 4, device=DEV, scale_f16=hs)
+    gv = kv.KiviStore(1, w.BH, S_q, 128, 32, 4, device=DEV, scale_f16=hs)
+    kv.kivi_flush_kv(dev(k), dev(v), 0, gk, gv, n_tokens=S_q)
+    rk = oracle.Store(0, w.BH, S_q, 128, 32, 4, scale_f16=hs)
+    rv = oracle.Store(1, w.BH, S_q, 128, 32, 4, scale_f16=hs)
+    oracle.flush(0, k, S_q, rk)
+    oracle.flush(1, v, S_q, rv)
+    kr, vr = np.ascontiguousarray(k[:, S_q:]), np.ascontiguousarray(v[:, S_q:])
+    ref = oracle.decode_attend(q, rk, rv, S_q, kr, vr, n_res, 8, w.sm_scale)
+    out = host(kv.kivi_decode_attend(dev(q), gk, gv, S_q, dev(kr), dev(vr), n_res, 8, w.sm_scale))
+    assert np.max(np.abs(out - ref)) <= TOL
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("hq,hkv", [(16, 2), (6, 2)])
 def test_decode_subgroups_many_splits(hq, hkv, bits):

@@ -103,3 +103,20 @@ def test_noalloc_alternating_plans():
         assert torch.isfinite(out).all()
         err = (out.double() - refs[i].double()).abs().max().item()
         assert err <= TOL, (i, err)
+
+
+def test_noalloc_two_warp_plan():
+    """A plan of 2-warp CTAs (B=16, 1408 packed + 128 fp16 tokens: 9 splits
+    per head group, 8 CTAs per SM) through the library-owned scratch, twice,
+    equals the workspace entry point."""
+    w = synth.Workload("w2", B=16, Hkv=8, Hq=32, D=128, S=1408 + 128, bits=4, G=32, R=0, n_outlier=4,
+                       outlier_scale=8.0, seed=13)
+    assert kv.kivi_decode_plan_info(16, 32, 8, 1408, 128)["warps_per_cta"] == 2
+    q, ks, vs, kr, vr = _decode_inputs(w, 1408, 128, seed=8)
+    ref = kv.kivi_decode_attend(q, ks, vs, 1408, kr, vr, 128, w.Hkv, w.sm_scale)
+    for _ in range(2):
+        out = torch.full_like(ref, float("nan"))
+        kv.kivi_decode_attend_noalloc(q, ks, vs, 1408, kr, vr, 128, w.Hkv, w.sm_scale, out=out)
+        torch.cuda.synchronize()
+        err = (out.double() - ref.double()).abs().max().item()
+        assert err <= TOL, err
