@@ -22,13 +22,16 @@
 //    memory chunks are swizzled by row so a warp's reads are conflict-free.
 //  * min/max run on packed fp16 (exact). x - zero is one mixed-precision
 //    subtraction (fp16 operand, fp32 result: no separate conversion). The
-//    quotient: with r = RN(1/s), the exact product a * r lies within 2^-19 of
-//    RN(a/s) for quotients below 16, so one fp32x2 fma RN(a r + 2^23) rounds
-//    it half to even and leaves the code in the low byte, and a second fma
-//    measures its distance from that integer; when the distance is within
-//    0.5 - 2^-14 the code equals rint(RN(a/s)). One check per 8 elements
-//    sends the rare near-tie element to an exact IEEE division (out of line).
-//    Byte permutes pack 8 codes per 32-bit word.
+//    scale RN((max - min) / L) is one multiply and two fmas (division by the
+//    constant L = 3 or 15 with one remainder correction; checked equal to
+//    the IEEE quotient for every non-negative finite fp32). The quotient:
+//    with r = 1/s to within 1 ulp (rcp.approx.f32), the exact product a * r
+//    lies within 2^-18 of RN(a/s) for quotients below 16, so one fp32x2 fma
+//    RN(a r + 2^23) rounds it half to even and leaves the code in the low
+//    byte, and a second fma measures its distance from that integer; when
+//    the distance is within 0.5 - 2^-14 the code equals rint(RN(a/s)). One
+//    check per 8 elements sends the rare near-tie element to an exact IEEE
+//    division (out of line). Byte permutes pack 8 codes per 32-bit word.
 //  * work is cut into 4 KB items (a key group's G tokens x 2048 / G channels,
 //    or 2048 / D value rows; at G = 128 an 8 KB key item of 128 tokens x 32
 //    channels, so its row pieces are 64 bytes, not 32); each warp walks the
@@ -91,9 +94,11 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 }
 
 // Codes of 8 fp16 elements (one 16-byte vector), each as the fp32 bit
-// pattern of 2^23 + q in tb[i]. z2/r2: per-element zero and r = RN(1/scale)
-// as fp32x2 pairs; s: scales. With a = RN(x - z), the exact product a * r
-// lies within 2^-19 of RN(a / s) (quotients below 16), so t = RN(a r + 2^23)
+// pattern of 2^23 + q in tb[i]. z2/r2: per-element zero and r = 1/scale to
+// within 1 ulp, as fp32x2 pairs; s: scales. With a = RN(x - z), the exact
+// product a * r lies within (a/s) 2^-23 + 2^-21 < 2^-18 of RN(a / s)
+// (quotients below 16; below 2^-17 for the quotients below 32 that an fp16
+// scale allows), so t = RN(a r + 2^23)
 // (one fma) holds q = rint(RN(a / s)) whenever f = RN(a r - (t - 2^23)) is
 // within 0.5 - 2^-14 of zero; the rare element outside that band takes an
 // IEEE division (out of line).
@@ -175,6 +180,30 @@ __device__ __forceinline__ uint4 fake8(const uint4 xv, const f32x2 (&z2)[4], con
         h[k] = h2_as_u32(__floats2half2_rn(r.x, r.y));
     }
     return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+// The scale RN(x / L) for x = max - min >= 0 and L = 2^BITS - 1 (3 or 15):
+// q = RN(x c) with c = RN(1 / L), the remainder x - q L (exact in one fma),
+// then one fma correction q + RN(remainder) c (the division-by-a-constant
+// step with an fma-computed remainder, as in Markstein's division
+// algorithms). That this equals the IEEE quotient for L = 3 and 15 is not a
+// general theorem: tests/test_guard_band.py checks it against IEEE division
+// for every non-negative finite fp32 x.
+template <int BITS>
+__device__ __forceinline__ float div_levels(float x) {
+    constexpr float L = (float)Levels<BITS>::value;
+    constexpr float c = 1.0f / L;
+    const float q = __fmul_rn(x, c);
+    const float r = __fmaf_rn(-q, L, x);
+    return __fmaf_rn(r, c, q);
+}
+
+// 1 / s within 1 ulp (rcp.approx.f32, s a positive normal fp32): the fast
+// quotient only needs a r within a relative 2^-23 of a / s.
+__device__ __forceinline__ float rcp_1ulp(float s) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+    return r;
 }
 
 // -0 -> +0 (applied to min and max, so zero and scale carry no negative sign)
@@ -362,7 +391,6 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         z[2 * k] = canon(lo.x);
         z[2 * k + 1] = canon(lo.y);
     }
-    const float L = (float)Levels<BITS>::value;
     // the part lanes of a column compute its 8 scales: 2 each (4 parts), 1 each
     // (8 parts), or 1 each in parts 0..7 and again in parts 8..15 (16 parts)
     constexpr int CPP = KS::kNPart >= 8 ? 1 : 8 / KS::kNPart;
@@ -380,9 +408,9 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
 #pragma unroll
         for (int c = 0; c < CPP; ++c) {
             const bool odd = ((ch0 + c) & 1) != 0;
-            my_s[c] = __fdiv_rn(__fsub_rn(canon(odd ? hi.y : hi.x), canon(odd ? lo.y : lo.x)), L);
+            my_s[c] = div_levels<BITS>(__fsub_rn(canon(odd ? hi.y : hi.x), canon(odd ? lo.y : lo.x)));
             if (HS) my_s[c] = __half2float(__float2half_rn(my_s[c]));  // the stored fp16 scale
-            my_r[c] = my_s[c] == 0.0f ? 0.0f : __frcp_rn(my_s[c]);
+            my_r[c] = my_s[c] == 0.0f ? 0.0f : rcp_1ulp(my_s[c]);
         }
     }
     float s[8], r[8];
@@ -475,7 +503,6 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
     const int row = lane % VS::kRows, jp = lane / VS::kRows;
     const bool valid = t0 + row < a.n_flush;
     if (G != 128 && !valid) return;  // (G = 128: both lanes of a row leave together below)
-    const float L = (float)Levels<BITS>::value;
     const uint4* xs = reinterpret_cast<const uint4*>(st + row * (2 * D));
     const long long grow = (long long)bh * a.s_cap + a.s_off + t0 + row;
     constexpr int NG = G == 32 ? 2 : 1;      // groups (or half groups) per lane
@@ -494,9 +521,9 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
             if (!valid) return;
         }
         const float z = canon(__half2float(__hmin(__low2half(m2), __high2half(m2))));
-        float sc = __fdiv_rn(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z), L);
+        float sc = div_levels<BITS>(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z));
         if (HS) sc = __half2float(__float2half_rn(sc));  // the stored fp16 scale
-        const float rc = sc == 0.0f ? 0.0f : __frcp_rn(sc);
+        const float rc = sc == 0.0f ? 0.0f : rcp_1ulp(sc);
         const f32x2 z1 = pk(z, z), r1 = pk(rc, rc);
         const f32x2 z2[4] = {z1, z1, z1, z1}, r2[4] = {r1, r1, r1, r1};
         const float sv[8] = {sc, sc, sc, sc, sc, sc, sc, sc};
@@ -584,7 +611,6 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
         z[2 * k] = canon(lo.x);
         z[2 * k + 1] = canon(lo.y);
     }
-    const float L = (float)Levels<BITS>::value;
     float my_s[2], my_r[2];
     {
         __half2 hx = mx[0], hn = mn[0];  // channels 2*part, 2*part + 1 of this octet
@@ -595,14 +621,14 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
                 hn = mn[k];
             }
         const float2 hi = __half22float2(hx), lo = __half22float2(hn);
-        my_s[0] = __fdiv_rn(__fsub_rn(canon(hi.x), canon(lo.x)), L);
-        my_s[1] = __fdiv_rn(__fsub_rn(canon(hi.y), canon(lo.y)), L);
+        my_s[0] = div_levels<BITS>(__fsub_rn(canon(hi.x), canon(lo.x)));
+        my_s[1] = div_levels<BITS>(__fsub_rn(canon(hi.y), canon(lo.y)));
         if (HS) {  // the stored fp16 scales
             my_s[0] = __half2float(__float2half_rn(my_s[0]));
             my_s[1] = __half2float(__float2half_rn(my_s[1]));
         }
-        my_r[0] = my_s[0] == 0.0f ? 0.0f : __frcp_rn(my_s[0]);
-        my_r[1] = my_s[1] == 0.0f ? 0.0f : __frcp_rn(my_s[1]);
+        my_r[0] = my_s[0] == 0.0f ? 0.0f : rcp_1ulp(my_s[0]);
+        my_r[1] = my_s[1] == 0.0f ? 0.0f : rcp_1ulp(my_s[1]);
     }
     float s[8], r[8];
 #pragma unroll
@@ -665,7 +691,6 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
     const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
     const int row = lane & 15, jp = lane >> 4;
     if (t0 + row >= a.n_flush) return;
-    const float L = (float)Levels<BITS>::value;
     const uint4* xs = reinterpret_cast<const uint4*>(st + row * 256);
     const long long grow = (long long)bh * a.s_cap + a.s_off + t0 + row;
 #pragma unroll
@@ -686,9 +711,9 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
         const __half2 m2 = __hmin2(__hmin2(mk[0], mk[1]), __hmin2(mk[2], mk[3]));
         const __half2 x2 = __hmax2(__hmax2(xk[0], xk[1]), __hmax2(xk[2], xk[3]));
         const float z = canon(__half2float(__hmin(__low2half(m2), __high2half(m2))));
-        float sc = __fdiv_rn(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z), L);
+        float sc = div_levels<BITS>(__fsub_rn(canon(__half2float(__hmax(__low2half(x2), __high2half(x2)))), z));
         if (HS) sc = __half2float(__float2half_rn(sc));  // the stored fp16 scale
-        const float rc = sc == 0.0f ? 0.0f : __frcp_rn(sc);
+        const float rc = sc == 0.0f ? 0.0f : rcp_1ulp(sc);
         const f32x2 z1 = pk(z, z), r1 = pk(rc, rc);
         const f32x2 z2[4] = {z1, z1, z1, z1}, r2[4] = {r1, r1, r1, r1};
         const float sv[8] = {sc, sc, sc, sc, sc, sc, sc, sc};

@@ -21,40 +21,6 @@ struct Levels {
     static constexpr uint32_t value = (1u << BITS) - 1u;
 };
 
-// rint(RN(a / s)) with the quotient rounded as an IEEE fp32 division, clamped
-// to [0, 2^bits - 1]. a >= 0 and s >= 0 (a = x - min, s = scale); r is
-// RN(1/s), or 0 when s == 0 (then every code is 0).
-//
-// The fast path forms y = RN(a * r). With a/s < 16, |y - RN(a/s)| < 2^-18
-// (two relative errors of 2^-24 on the product plus half an ulp of the
-// quotient), so whenever y is farther than 2^-14 from every half-integer,
-// rint(y) == rint(RN(a/s)). Inside that guard band the exact IEEE division
-// decides, so ties (x - min exactly on a half step, common for grid-aligned
-// data) round half to even as the reference does. RN(y + 2^23) rounds y to
-// an integer, ties to even, and leaves it in the low mantissa bits.
-template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float a, float s, float r) {
-    float y = __fmul_rn(a, r);
-    float z = __fadd_rn(y, kMagic);
-    float f = __fsub_rn(y, __fsub_rn(z, kMagic));
-    if (fabsf(f) > 0.5f - 1.0f / 16384.0f) {
-        y = __fdiv_rn(a, s);
-        z = __fadd_rn(y, kMagic);
-    }
-    uint32_t q = __float_as_uint(z) - 0x4B000000u;  // wraps to huge for garbage
-    return q < Levels<BITS>::value ? q : Levels<BITS>::value;
-}
-
-// Exact fp32 value of a small unsigned integer code.
-__device__ __forceinline__ float code_to_float(uint32_t c) {
-    return __fsub_rn(__uint_as_float(0x4B000000u | c), kMagic);
-}
-
-// recon = RN(RN(q * s) + z): a multiply, then a separate add.
-__device__ __forceinline__ float recon(uint32_t q, float s, float z) {
-    return __fadd_rn(__fmul_rn(code_to_float(q), s), z);
-}
-
 // --- packed fp32x2 arithmetic (sm_100+): two IEEE round-to-nearest ops per
 // instruction, each lane rounded exactly like the scalar __f*_rn intrinsic.
 typedef unsigned long long f32x2;

@@ -1,8 +1,9 @@
 """The flush against the oracle over more than 10^9 elements, bit-exact.
 
-The flush kernel computes each code from the product a * RN(1 / s) and
-falls back to an IEEE division only for quotients within 2^-14 of a
-half-integer (the bound is restated in tests/test_guard_band.py). Ties are
+The flush kernel computes each scale by a multiply and two fmas, each code
+from the product a * r (r = 1 / s to within 1 ulp), and falls back to an
+IEEE division only for quotients within 2^-14 of a half-integer (the scale
+division and the bound are checked in tests/test_guard_band.py). Ties are
 common in real data (VeloxQuant-MLX blog, "A 5.65x Metal Kernel That Made My
 LLM Exactly 0% Faster", "Three ways to be off by one bit", #2), so both paths
 must agree with the oracle's division everywhere. Eight chunks of 16 heads x
