@@ -38,8 +38,6 @@
 //    items with a grid stride, staging two at a time in shared memory with
 //    cp.async, so the copy of the next item overlaps the quantization of the
 //    current one; the key loop takes two token rows per trip.
-#include <type_traits>
-
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
@@ -93,6 +91,15 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return d;
 }
 
+// With an fp16 scale a subnormal stored scale can leave a quotient past
+// 2^BITS - 1 (up to about 1.5 (2^BITS - 1)): clip the codes, whose fp32
+// patterns 2^23 + q order like q.
+template <int BITS>
+__device__ __forceinline__ void clip8(uint32_t (&tb)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tb[i] = min(tb[i], 0x4B000000u + (uint32_t)Levels<BITS>::value);
+}
+
 // Codes of 8 fp16 elements (one 16-byte vector), each as the fp32 bit
 // pattern of 2^23 + q in tb[i]. z2/r2: per-element zero and r = 1/scale to
 // within 1 ulp, as fp32x2 pairs; s: scales. With a = RN(x - z), the exact
@@ -101,9 +108,12 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 // scale allows), so t = RN(a r + 2^23)
 // (one fma) holds q = rint(RN(a / s)) whenever f = RN(a r - (t - 2^23)) is
 // within 0.5 - 2^-14 of zero; the rare element outside that band takes an
-// IEEE division (out of line).
+// IEEE division (out of line). With fp16 scales (HS), clip (warp-uniform,
+// set only where a subnormal scale can push a code past 2^BITS - 1) sends
+// the 8 codes down the same rare branch to be clipped.
+template <int BITS, bool HS>
 __device__ __forceinline__ void quant8_codes(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
-                                             const float (&s)[8], uint32_t (&tb)[8]) {
+                                             const float (&s)[8], uint32_t (&tb)[8], bool clip) {
     const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
     const f32x2 M2 = pk(kMagic, kMagic);
     f32x2 a[4];
@@ -120,42 +130,34 @@ __device__ __forceinline__ void quant8_codes(const uint4 xv, const f32x2 (&z2)[4
         tb[2 * k + 1] = __float_as_uint(tt.y);
     }
     const float fm = max3f(max3f(d[0], d[1], d[2]), max3f(d[3], d[4], d[5]), fmaxf(d[6], d[7]));
-    if (fm > kTieBand) {  // rare: a quotient within about 2^-14 of a half-integer
+    if (fm > kTieBand || (HS && clip)) {  // rare: a quotient within about 2^-14 of a half-integer
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const float2 aa = upk(a[k]);
             if (d[2 * k] > kTieBand) tb[2 * k] = exact_code_bits(aa.x, s[2 * k]);
             if (d[2 * k + 1] > kTieBand) tb[2 * k + 1] = exact_code_bits(aa.y, s[2 * k + 1]);
         }
+        if (HS && clip) clip8<BITS>(tb);
     }
-}
-
-// With an fp16 scale a subnormal stored scale can leave a quotient past
-// 2^BITS - 1 (up to about 1.5 (2^BITS - 1)): clip the codes, whose fp32
-// patterns 2^23 + q order like q.
-template <int BITS>
-__device__ __forceinline__ void clip8(uint32_t (&tb)[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) tb[i] = min(tb[i], 0x4B000000u + (uint32_t)Levels<BITS>::value);
 }
 
 // Only a scale below the smallest normal fp16 (2^-14) can push a code past
 // 2^BITS - 1 once rounded to fp16: a normal fp16 scale lies within a relative
 // 2^-11 of the fp32 one, and every a is at most max - min, so a / s stays
 // below L (1 + 2^-10) < L + 1/2. The decision is taken per warp (a vote over
-// its active lanes), so warps without such a scale run the unclipped loop.
+// its active lanes); warps without such a scale never take the clip, and the
+// others take it in the rare branch of quant8_codes (one copy of the loop).
 __device__ __forceinline__ bool warp_has_subnormal_scale(bool lane_has) {
     return __any_sync(__activemask(), lane_has);
 }
 constexpr float kMinNormalF16 = 6.103515625e-05f;  // 2^-14
 
 // The codes of quant8_codes packed into BITS*8 bits.
-template <int BITS, bool CLIP>
+template <int BITS, bool HS>
 __device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
-                                           const float (&s)[8]) {
+                                           const float (&s)[8], bool clip) {
     uint32_t tb[8];
-    quant8_codes(xv, z2, r2, s, tb);
-    if (CLIP) clip8<BITS>(tb);
+    quant8_codes<BITS, HS>(xv, z2, r2, s, tb, clip);
     return pack8<BITS>(tb);
 }
 
@@ -164,12 +166,11 @@ __device__ __forceinline__ uint32_t quant8(const uint4 xv, const f32x2 (&z2)[4],
 // That Made My LLM Exactly 0% Faster", "What we're actually optimizing";
 // multiply, then a separate add: "Three ways to be off by one bit" #1).
 // With tb = bits of 2^23 + q, fma(2^23 + q, s, -2^23 s) is q * s rounded once.
-template <int BITS, bool CLIP>
+template <int BITS, bool HS>
 __device__ __forceinline__ uint4 fake8(const uint4 xv, const f32x2 (&z2)[4], const f32x2 (&r2)[4],
-                                       const float (&s)[8]) {
+                                       const float (&s)[8], bool clip) {
     uint32_t tb[8];
-    quant8_codes(xv, z2, r2, s, tb);
-    if (CLIP) clip8<BITS>(tb);
+    quant8_codes<BITS, HS>(xv, z2, r2, s, tb, clip);
     uint32_t h[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -433,12 +434,8 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     const bool clip = HS && warp_has_subnormal_scale(small);
     if (FAKE) {
         uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * D) + octet;
-        auto rows = [&](auto cl) {
 #pragma unroll 1
-            for (int i = 0; i < nv; ++i) frow[i * (D / 8)] = fake8<BITS, decltype(cl)::value>(xs[i * KS::kNOc], z2, r2, s);
-        };
-        if (clip) rows(std::true_type{});
-        else rows(std::false_type{});
+        for (int i = 0; i < nv; ++i) frow[i * (D / 8)] = fake8<BITS, HS>(xs[i * KS::kNOc], z2, r2, s, clip);
         return;
     }
     if (part == 0) {
@@ -457,12 +454,8 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
         else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
     };
-    auto rows = [&](auto cl) {
 #pragma unroll (kKeyUnroll)
-        for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, decltype(cl)::value>(xs[i * KS::kNOc], z2, r2, s));
-    };
-    if (clip) rows(std::true_type{});
-    else rows(std::false_type{});
+    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, HS>(xs[i * KS::kNOc], z2, r2, s, clip));
 }
 
 // min and max of the 8 fp16 of each vector of x, as half2 (min and max of fp16
@@ -531,22 +524,12 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
         const bool clip = HS && warp_has_subnormal_scale(sc < kMinNormalF16);
         if (FAKE) {
             uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * D) + cv;
-            if (clip) {
-#pragma unroll
-                for (int k = 0; k < NVEC; ++k) frow[k] = fake8<BITS, true>(x[k], z2, r2, sv);
-            } else {
-#pragma unroll
-                for (int k = 0; k < NVEC; ++k) frow[k] = fake8<BITS, false>(x[k], z2, r2, sv);
-            }
+            #pragma unroll
+            for (int k = 0; k < NVEC; ++k) frow[k] = fake8<BITS, HS>(x[k], z2, r2, sv, clip);
         } else {
             uint32_t pq[NVEC];
-            if (clip) {
-#pragma unroll
-                for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS, true>(x[k], z2, r2, sv);
-            } else {
-#pragma unroll
-                for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS, false>(x[k], z2, r2, sv);
-            }
+            #pragma unroll
+            for (int k = 0; k < NVEC; ++k) pq[k] = quant8<BITS, HS>(x[k], z2, r2, sv, clip);
             uint8_t* cdst = a.codes + grow * (D * BITS / 8) + cv * BITS;  // 8 channels per vector
             if (BITS == 4) {
 #pragma unroll
@@ -647,12 +630,8 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
     const bool clip = HS && warp_has_subnormal_scale(my_s[0] < kMinNormalF16 || my_s[1] < kMinNormalF16);
     if (FAKE) {
         uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * kD) + octet;
-        auto rows = [&](auto cl) {
 #pragma unroll 1
-            for (int i = 0; i < nv; ++i) frow[i * (kD / 8)] = fake8<BITS, decltype(cl)::value>(xs[i * 8], z2, r2, s);
-        };
-        if (clip) rows(std::true_type{});
-        else rows(std::false_type{});
+        for (int i = 0; i < nv; ++i) frow[i * (kD / 8)] = fake8<BITS, HS>(xs[i * 8], z2, r2, s, clip);
         return;
     }
     if (part == 0) {
@@ -671,12 +650,8 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
         if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
         else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
     };
-    auto rows = [&](auto cl) {
 #pragma unroll (kKeyUnroll)
-        for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, decltype(cl)::value>(xs[i * 8], z2, r2, s));
-    };
-    if (clip) rows(std::true_type{});
-    else rows(std::false_type{});
+    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, HS>(xs[i * 8], z2, r2, s, clip));
 }
 
 // G = 32 values: lane = 16 jp + row; the lane quantizes the groups j = 2 jp and
@@ -720,13 +695,8 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
         const bool clip = HS && warp_has_subnormal_scale(sc < kMinNormalF16);
         if (FAKE) {
             uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0 + row) * kD + 32 * j);
-            if (clip) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) frow[k] = fake8<BITS, true>(x[k], z2, r2, sv);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) frow[k] = fake8<BITS, false>(x[k], z2, r2, sv);
-            }
+            #pragma unroll
+            for (int k = 0; k < 4; ++k) frow[k] = fake8<BITS, HS>(x[k], z2, r2, sv, clip);
         } else {
             auto store_group = [&](const uint32_t (&pq)[4]) {
                 if (BITS == 4) {
@@ -737,13 +707,8 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
                 }
             };
             uint32_t pq[4];
-            if (clip) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS, true>(x[k], z2, r2, sv);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS, false>(x[k], z2, r2, sv);
-            }
+            #pragma unroll
+            for (int k = 0; k < 4; ++k) pq[k] = quant8<BITS, HS>(x[k], z2, r2, sv, clip);
             store_group(pq);
             store_scale<HS>(a.scale, grow * (kD / kG) + j, sc);
             a.zero[grow * (kD / kG) + j] = __float2half_rn(z);
