@@ -336,11 +336,16 @@ kivi_status kivi_decode_attend(const void* q_f16,
  *   windows: fp16 [BH, res_cap, D] for keys and for values, with
  *            res_cap >= residual_length + group_size;
  *   S_q:     tokens in the stores (set 0 for an empty cache);
- *   n_res:   tokens in the windows, oldest first (set 0 for an empty cache).
+ *   n_res:   tokens in the windows, oldest first (set 0 for an empty cache);
+ *   res_off: the window's first row: its tokens are rows res_off ..
+ *            res_off + n_res - 1 of each head (set 0 for an empty cache).
  * Invariant kept by the calls: after each call, n_res < residual_length +
  * group_size (a window that reaches R + G tokens flushes its oldest
- * floor((n_res - R) / G) * G tokens into the stores at offset S_q and moves
- * the rest to the front).
+ * floor((n_res - R) / G) * G tokens into the stores at offset S_q; the
+ * window then starts that many rows later). The window moves back to row 0
+ * only when new tokens would not fit behind it, so with res_cap = R + kG
+ * the remaining tokens are copied once per about k - 1 flushes instead of
+ * after every flush.
  * Errors: every argument check (geometry, counters, pointers and alignment,
  * store capacity for every flush the call will make) runs before the call's
  * first launch; a failed check returns its status, launches nothing and
@@ -366,6 +371,7 @@ typedef struct {
     int S_q;              /* tokens in the stores */
     int n_res;            /* tokens in the windows */
     int store_written;    /* 1 when the cache's latest launch wrote the stores (set 0 for an empty cache) */
+    int res_off;          /* first window row in use (set 0 for an empty cache) */
 } kivi_cache;
 
 /*
@@ -373,7 +379,8 @@ typedef struct {
  * of k and v ([BH, S, D] fp16, x_bh_stride tokens between heads), the oldest
  * n = kivi_flush_count(S, residual_length, group_size) are flushed straight
  * from k and v into the stores at offset S_q (one launch), and the other
- * S - n are copied into the windows. S_q += n, n_res = S - n; *n_flushed
+ * S - n are copied into rows 0 .. S - n - 1 of the windows. S_q += n,
+ * n_res = S - n, res_off = 0; *n_flushed
  * (may be NULL) receives n. With residual_length 0 and S not a multiple of
  * group_size the last key group is ragged and the cache takes no further
  * flushes (their store offset would not be a multiple of group_size).
@@ -405,7 +412,7 @@ kivi_status kivi_cache_append(kivi_cache* cache, const void* k_f16, const void* 
  * heads; every other argument, check and result is that of
  * kivi_decode_attend. The counters are not changed. Unless the cache's
  * latest launch wrote the stores (store_written: a flush that no window
- * compaction followed), the decode takes KIVI_DECODE_STORE_READY: the calls
+ * append or move followed), the decode takes KIVI_DECODE_STORE_READY: the calls
  * on one cache are meant to be issued on one stream, and a flush followed by
  * any other kernel has finished before the decode's first loads.
  */

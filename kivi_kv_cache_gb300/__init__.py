@@ -409,14 +409,15 @@ class _CacheStruct(ctypes.Structure):
                 ("kcodes", ctypes.c_void_p), ("kscale", ctypes.c_void_p), ("kzero", ctypes.c_void_p),
                 ("vcodes", ctypes.c_void_p), ("vscale", ctypes.c_void_p), ("vzero", ctypes.c_void_p),
                 ("k_res", ctypes.c_void_p), ("v_res", ctypes.c_void_p), ("S_q", ctypes.c_int), ("n_res", ctypes.c_int),
-                ("store_written", ctypes.c_int)]
+                ("store_written", ctypes.c_int), ("res_off", ctypes.c_int)]
 
 
 class KiviCache:
     """One attention layer's KIVI cache (C struct kivi_cache): packed key and
     value stores of s_cap tokens, fp16 key and value windows of res_cap
-    tokens (default residual_length + group_size), and the counters S_q and
-    n_res, which the C calls update. torch allocates the buffers."""
+    tokens (default residual_length + group_size), and the counters S_q,
+    n_res and res_off (the window's first row), which the C calls update.
+    torch allocates the buffers."""
 
     def __init__(self, BH: int, s_cap: int, D: int = 128, group_size: int = 32, bits: int = 4,
                  residual_length: int = 128, res_cap=None, device="cuda", scale_f16: bool = False):
@@ -430,7 +431,7 @@ class KiviCache:
         self.c = _CacheStruct(BH, D, group_size, ks.abi_bits, residual_length, s_cap, res_cap,
                               ks.codes.data_ptr(), ks.scale.data_ptr(), ks.zero.data_ptr(),
                               vs.codes.data_ptr(), vs.scale.data_ptr(), vs.zero.data_ptr(),
-                              self.k_res.data_ptr(), self.v_res.data_ptr(), 0, 0)
+                              self.k_res.data_ptr(), self.v_res.data_ptr(), 0, 0, 0, 0)
 
     @property
     def S_q(self) -> int:
@@ -440,12 +441,22 @@ class KiviCache:
     def n_res(self) -> int:
         return self.c.n_res
 
-    def state(self):
-        """The counters (S_q, n_res), e.g. to restore them after a graph capture."""
-        return self.c.S_q, self.c.n_res
+    @property
+    def res_off(self) -> int:
+        return self.c.res_off
 
-    def set_state(self, S_q: int, n_res: int) -> None:
-        self.c.S_q, self.c.n_res = S_q, n_res
+    def state(self):
+        """The counters (S_q, n_res, res_off, store_written), e.g. to restore
+        them after a graph capture."""
+        return self.c.S_q, self.c.n_res, self.c.res_off, self.c.store_written
+
+    def set_state(self, S_q: int, n_res: int, res_off: int = 0, store_written: int = 0) -> None:
+        self.c.S_q, self.c.n_res, self.c.res_off, self.c.store_written = S_q, n_res, res_off, store_written
+
+    def window(self):
+        """Views of the live window rows: (k, v) [BH, n_res, D] fp16."""
+        o, n = self.c.res_off, self.c.n_res
+        return self.k_res[:, o:o + n], self.v_res[:, o:o + n]
 
     def prefill(self, k, v, n_tokens=None, stream=None) -> int:
         """kivi_cache_prefill of k, v [BH, S, D] fp16; returns the tokens flushed."""

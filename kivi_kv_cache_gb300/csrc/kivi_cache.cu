@@ -8,9 +8,10 @@
 // its oldest whole groups are quantized into the packed store; the section
 // "Four benchmarks that lied" (Lie #2) counts those flushes per decode run.
 // The rule: whenever the window holds n_res >= R + G tokens, its oldest
-// floor((n_res - R) / G) * G tokens are flushed at store offset S_q and the
-// remaining tokens move to the front of the window, so R <= n_res < R + G
-// afterwards.
+// floor((n_res - R) / G) * G tokens are flushed at store offset S_q, so
+// R <= n_res < R + G afterwards. The window is rows res_off .. res_off +
+// n_res - 1 of its buffer: a flush advances res_off, and the remaining
+// tokens move back to row 0 only when an append would not fit behind them.
 //
 // Every step runs in the library's kernels (residual append, flush, residual
 // compact, decode); this file only sequences them and keeps the counters.
@@ -31,7 +32,7 @@ kivi_status cache_check(const kivi_cache* c) {
     if (sh != KIVI_OK) return sh;
     if (c->BH <= 0 || c->residual_length < 0 || c->s_cap <= 0 || c->s_cap % c->group_size != 0 ||
         (long long)c->res_cap < (long long)c->residual_length + c->group_size || c->S_q < 0 || c->S_q > c->s_cap ||
-        c->n_res < 0 || c->n_res > c->res_cap)
+        c->n_res < 0 || c->res_off < 0 || (long long)c->res_off + c->n_res > c->res_cap)
         return KIVI_ERR_INVALID_ARG;
     const void* bufs[8] = {c->kcodes, c->kscale, c->kzero, c->vcodes, c->vscale, c->vzero, c->k_res, c->v_res};
     for (const void* p : bufs) {
@@ -45,21 +46,36 @@ kivi_status cache_check(const kivi_cache* c) {
 // n_res >= R + G, else 0.
 int window_flush(int n_res, int R, int G) { return n_res >= R + G ? (n_res - R) / G * G : 0; }
 
+// Row r of the window buffers (16-byte aligned: rows are 2 D bytes, D >= 64).
+const void* window_row(const void* base, const kivi_cache* c, int r) {
+    return static_cast<const __half*>(base) + (long long)r * c->D;
+}
+
 // Flush the oldest n tokens of the windows into the stores at S_q (exactly n:
-// the windows are passed as n tokens with residual_length 0), then move the
-// other n_res - n tokens to the front.
+// the windows are passed from row res_off as n tokens with residual_length
+// 0); the window then starts n rows later.
 kivi_status flush_window(kivi_cache* c, int n, kivi_stream_t stream) {
     int done = 0;
-    kivi_status st = kivi_flush_kv(c->k_res, c->v_res, c->BH, n, c->res_cap, c->D, c->group_size, c->bits, 0,
-                                   c->kcodes, c->kscale, c->kzero, c->vcodes, c->vscale, c->vzero, c->S_q,
-                                   c->s_cap, &done, stream);
+    kivi_status st = kivi_flush_kv(window_row(c->k_res, c, c->res_off), window_row(c->v_res, c, c->res_off), c->BH,
+                                   n, c->res_cap, c->D, c->group_size, c->bits, 0, c->kcodes, c->kscale, c->kzero,
+                                   c->vcodes, c->vscale, c->vzero, c->S_q, c->s_cap, &done, stream);
     if (st != KIVI_OK) return st;
     c->S_q += done;
     c->store_written = 1;
-    st = kivi_residual_compact_kv(c->k_res, c->v_res, c->BH, c->res_cap, c->D, c->n_res, done, stream);
-    if (st != KIVI_OK) return st;
-    if (done > 0 && done < c->n_res) c->store_written = 0;  // the compaction ran after the flush
     c->n_res -= done;
+    c->res_off = c->n_res == 0 ? 0 : c->res_off + done;
+    return KIVI_OK;
+}
+
+// Move the window's n_res tokens from row res_off to row 0 (an overlap-safe
+// copy) so that m more tokens fit behind them; nothing to do if they fit.
+kivi_status make_room(kivi_cache* c, int m, kivi_stream_t stream) {
+    if ((long long)c->res_off + c->n_res + m <= c->res_cap || c->res_off == 0) return KIVI_OK;
+    const kivi_status st = kivi_residual_compact_kv(c->k_res, c->v_res, c->BH, c->res_cap, c->D,
+                                                    c->res_off + c->n_res, c->res_off, stream);
+    if (st != KIVI_OK) return st;
+    c->res_off = 0;
+    if (c->n_res > 0) c->store_written = 0;
     return KIVI_OK;
 }
 
@@ -98,6 +114,7 @@ kivi_status kivi_cache_prefill(kivi_cache* c, const void* k_f16, const void* v_f
         c->n_res = tail;
         c->store_written = 0;
     }
+    c->res_off = 0;
     return KIVI_OK;
 }
 
@@ -135,10 +152,12 @@ kivi_status kivi_cache_append(kivi_cache* c, const void* k_f16, const void* v_f1
     while (off < n_new) {
         const int room = c->res_cap - c->n_res;
         const int m = n_new - off < room ? n_new - off : room;
+        st = make_room(c, m, stream);
+        if (st != KIVI_OK) return st;
         const __half* k = static_cast<const __half*>(k_f16) + (long long)off * c->D;
         const __half* v = static_cast<const __half*>(v_f16) + (long long)off * c->D;
-        st = kivi_residual_append_kv(k, v, src_bh_stride, m, c->k_res, c->v_res, c->BH, c->res_cap, c->D, c->n_res,
-                                     stream);
+        st = kivi_residual_append_kv(k, v, src_bh_stride, m, c->k_res, c->v_res, c->BH, c->res_cap, c->D,
+                                     c->res_off + c->n_res, stream);
         if (st != KIVI_OK) return st;
         c->n_res += m;
         c->store_written = 0;
@@ -161,8 +180,9 @@ kivi_status kivi_cache_decode(const kivi_cache* c, const void* q_f16, int B, int
     if (B <= 0 || Hkv <= 0 || (long long)B * Hkv != c->BH) return KIVI_ERR_INVALID_ARG;
     const int bits = c->bits | (c->store_written ? 0 : KIVI_DECODE_STORE_READY);
     return kivi_decode_attend(q_f16, c->kcodes, c->kscale, c->kzero, c->vcodes, c->vscale, c->vzero, c->S_q,
-                              c->s_cap, c->k_res, c->v_res, c->n_res, c->res_cap, B, Hq, Hkv, c->D, c->group_size,
-                              bits, sm_scale, out_f32, workspace, workspace_bytes, stream);
+                              c->s_cap, window_row(c->k_res, c, c->res_off), window_row(c->v_res, c, c->res_off),
+                              c->n_res, c->res_cap, B, Hq, Hkv, c->D, c->group_size, bits, sm_scale, out_f32,
+                              workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

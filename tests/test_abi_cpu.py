@@ -307,6 +307,8 @@ def test_cache_rejects_bad_arguments_without_launching(L):
     assert prefill(fake_cache(s_cap=250)) == INVALID              # not a multiple of G
     assert prefill(fake_cache(S_q=288)) == INVALID                # S_q > s_cap
     assert prefill(fake_cache(n_res=161)) == INVALID              # n_res > res_cap
+    assert prefill(fake_cache(res_off=-1)) == INVALID             # window start before the buffer
+    assert prefill(fake_cache(res_off=100, n_res=61)) == INVALID  # window past the buffer's end
     assert prefill(fake_cache(k_res=None)) == INVALID
     assert prefill(fake_cache(vzero=FAKE + 2)) == ALIGN
     assert prefill(fake_cache(), k=FAKE + 8) == ALIGN

@@ -87,19 +87,24 @@ def assert_same_state(gc: kv.KiviCache, oc: OracleCache, bh=None):
         assert np.array_equal(g.scale[sel].cpu().numpy().view(np.uint8), o.scale.view(np.uint8))
         assert np.array_equal(g.zero[sel].cpu().numpy().view(np.uint16), o.zero.view(np.uint16))
     n = oc.n_res
-    for g, o in ((gc.k_res, oc.kres), (gc.v_res, oc.vres)):
-        assert np.array_equal(g[sel, :n].cpu().numpy().view(np.uint16), o[:, :n].view(np.uint16))
+    for g, o in zip(gc.window(), (oc.kres, oc.vres)):
+        assert np.array_equal(g[sel].cpu().numpy().view(np.uint16), o[:, :n].view(np.uint16))
 
 
-@pytest.mark.parametrize("G,R,bits,scale_f16,chunk,steps", [
-    (32, 128, 4, False, 1, 100),   # config 5's rule: a flush every 32 decode steps
-    (64, 64, 2, True, 1, 140),     # group size 64, 2-bit, fp16 scales
-    (32, 32, 4, False, 45, 6),     # 45-token chunks through a 64-token window: several flushes per call
+@pytest.mark.parametrize("G,R,bits,scale_f16,chunk,steps,extra", [
+    (32, 128, 4, False, 1, 100, 0),    # config 5's rule: a flush every 32 decode steps
+    (32, 128, 4, False, 1, 140, 96),   # a 256-token window: it moves back to row 0 once per 4 flushes
+    (64, 64, 2, True, 1, 140, 0),      # group size 64, 2-bit, fp16 scales
+    (32, 32, 4, False, 45, 6, 0),      # 45-token chunks through a 64-token window: several flushes per call
+    (32, 32, 4, False, 45, 6, 40),     # the same through a 104-token window
 ])
-def test_streaming_loop_matches_oracle(G, R, bits, scale_f16, chunk, steps):
+def test_streaming_loop_matches_oracle(G, R, bits, scale_f16, chunk, steps, extra):
     """A reduced streaming serving run (2 layers, B=2, H_kv=8, 32 query
     heads, D=128, context from 1024 tokens): prefill, then per step and layer
-    append `chunk` tokens and decode one query token per head."""
+    append `chunk` tokens and decode one query token per head. The cache's
+    window holds R + G + extra tokens; the oracle's compacts after every
+    flush, the cache's moves back to row 0 only when the next tokens would
+    not fit behind it."""
     L, B, Hkv, Hq, D, ctx0 = 2, 2, 8, 32, 128, 1024
     w = synth.Workload("stream_small", B=B, Hkv=Hkv, Hq=Hq, D=D, S=ctx0, bits=bits, G=G, R=R, n_outlier=4,
                        outlier_scale=8.0, seed=5)
@@ -109,7 +114,7 @@ def test_streaming_loop_matches_oracle(G, R, bits, scale_f16, chunk, steps):
     layers = []
     for layer in range(L):
         k, v, _ = synth.prefill_inputs(w, seed=700 + layer)
-        gc = kv.KiviCache(w.BH, s_cap, D, G, bits, R, device=dev, scale_f16=scale_f16)
+        gc = kv.KiviCache(w.BH, s_cap, D, G, bits, R, res_cap=R + G + extra, device=dev, scale_f16=scale_f16)
         oc = OracleCache(w.BH, s_cap, D, G, bits, R, R + G + chunk, scale_f16=scale_f16)
         n_g = gc.prefill(torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev))
         assert n_g == oc.prefill(k, v)
@@ -117,6 +122,7 @@ def test_streaming_loop_matches_oracle(G, R, bits, scale_f16, chunk, steps):
         assert_same_state(gc, oc)
         layers.append((gc, oc))
     flushes = 0
+    offsets = set()
     for step in range(steps):
         for gc, oc in layers:
             kn, vn, q = synth.step_tokens(rng, w, chunk)
@@ -127,6 +133,7 @@ def test_streaming_loop_matches_oracle(G, R, bits, scale_f16, chunk, steps):
             torch.cuda.synchronize()
             err = float(np.max(np.abs(out.cpu().numpy().astype(np.float64) - ref)))
             assert err <= TOL, (step, err)
+            offsets.add(gc.res_off)
             if f:
                 flushes += 1
                 assert_same_state(gc, oc)
@@ -134,6 +141,8 @@ def test_streaming_loop_matches_oracle(G, R, bits, scale_f16, chunk, steps):
         assert_same_state(gc, oc)
         assert R <= gc.n_res < R + G
     assert flushes >= 2 * L
+    if extra >= G:
+        assert len(offsets) > 1  # the window started at rows other than 0
 
 
 def test_batched_thirty_steps_match_oracle_on_sampled_sequences():
