@@ -244,32 +244,30 @@ __device__ __forceinline__ void store_scales8(float* scale, long long m, const f
 // the quantization of the current one. Rows past n_flush are zero-filled and
 // never read from global memory.
 
-// Key items are 4 KB, except at G = 128, whose 4 KB item (128 tokens x 16
-// channels) reads 32-byte row pieces: its 8 KB item (128 tokens x 32
-// channels, 64-byte pieces) halves the rows per byte fetched.
-#ifndef KIVI_FLUSH_G128_ITEM
-#define KIVI_FLUSH_G128_ITEM 8192
-#endif
-__host__ __device__ constexpr int key_item_bytes(int G) { return G == 128 ? KIVI_FLUSH_G128_ITEM : 4096; }
-__host__ __device__ constexpr int key_item_channels(int G) { return key_item_bytes(G) / (2 * G); }
+// Key items are a key group's G tokens x 2048 / G channels (4 KB) at G = 32
+// and 64. At G = 128 a key item is the group's 128 tokens x 32 channels
+// (64-byte row pieces) split over a warp pair: each warp stages and
+// quantizes 64 of the tokens (4 KB) and the pair exchanges its column minima
+// and maxima once through shared memory. (A whole 8 KB item per warp fits
+// only 12 warps per SM; 128 tokens x 16 channels read 32-byte pieces.)
+__host__ __device__ constexpr int key_item_channels(int G) { return G == 128 ? 32 : 4096 / (2 * G); }
+__host__ __device__ constexpr int key_warp_tokens(int G) { return G == 128 ? 64 : G; }  // per warp
 
-// A stage holds one item; with G > 32 a key item's token parts are padded by
-// one row (kNOc 16-byte chunks) so that the parts of a quarter warp read
-// different banks (32 / kNOc parts of kNOc * 16 bytes). Each warp has two
-// stages.
+// A stage holds one warp's share of an item (4 KB); with G > 32 a key item's
+// token parts are padded by one row (kNOc 16-byte chunks) so that the parts
+// of a quarter warp read different banks (32 / kNOc parts of kNOc * 16
+// bytes). Each warp has two stages.
 template <int G>
 struct Stage {
-    static constexpr int kBytes = key_item_bytes(G) + (G > 32 ? 32 * 16 : 0);
+    static constexpr int kBytes = 4096 + (G > 32 ? 32 * 16 : 0);
 };
 #ifndef KIVI_FLUSH_BLOCKS_PER_SM
 #define KIVI_FLUSH_BLOCKS_PER_SM 4
 #endif
-// resident CTAs per SM the grid is sized for (three with 8 KB items: 68 KB of
-// stages per CTA)
-template <int G>
-__host__ __device__ constexpr int blocks_per_sm() {
-    return Stage<G>::kBytes > 6144 ? 3 : KIVI_FLUSH_BLOCKS_PER_SM;
-}
+constexpr int kBlocksPerSm = KIVI_FLUSH_BLOCKS_PER_SM;  // resident CTAs per SM the grid is sized for
+// G = 128: per CTA, the warps' minima and maxima for the pair exchange, two
+// slots (alternate items) of 32 words per warp
+constexpr int kXchgBytes = 2 * (kThreads / 32) * 32 * 4;
 #ifndef KIVI_FLUSH_KEY_UNROLL
 #define KIVI_FLUSH_KEY_UNROLL 2
 #endif
@@ -285,6 +283,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool fill
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// barrier over `threads` threads (a multiple of 32) with named barrier `id` (1..15)
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 struct Items {
     int key_items;   // BH * ng * (D / key item channels)
@@ -293,14 +295,15 @@ struct Items {
     int nv;          // value items per head
 };
 
-// Key items of group size G and head dim D: G tokens x kCh channels; a lane
-// owns kTPP tokens x 8 channels, lane = part * kNOc + oc.
+// Key items of group size G and head dim D: G tokens x kCh channels (a warp
+// takes key_warp_tokens(G) of them); a lane owns kTPP tokens x 8 channels,
+// lane = part * kNOc + oc.
 template <int G, int D>
 struct KeyShape {
-    static constexpr int kCh = key_item_channels(G);  // channels of an item: 64, 32, 32 (16 with 4 KB at G = 128)
+    static constexpr int kCh = key_item_channels(G);  // channels of an item: 64, 32, 32
     static constexpr int kNOc = kCh / 8;              // 8-channel octets: 8, 4 or 4
     static constexpr int kNPart = 32 / kNOc;          // token parts: 4, 8 or 8
-    static constexpr int kTPP = G / kNPart;           // tokens per part: 8, 8 or 16
+    static constexpr int kTPP = key_warp_tokens(G) / kNPart;  // tokens per part: 8
     static constexpr int kQ = D / kCh;                // items per key group: 1 to 16
     static constexpr int kPad = G > 32 ? 1 : 0;       // pad rows per part in shared memory
     static_assert(kQ >= 1, "a key item spans at most the head dim");
@@ -314,27 +317,32 @@ struct ValueShape {
     static constexpr int kCpr = D / 8;      // 16-byte chunks per row: 8, 16 or 32
 };
 
+// Stage this warp's share of item `item`: key item tokens half * 64 ..
+// (G = 128) or the whole key group, or value item vi (a value index, or
+// -1 for none).
 template <int G, int D>
 __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& v, const Items& it, int item,
-                                           uint8_t* st, int lane) {
+                                           int half, int vi_in, uint8_t* st, int lane) {
     using KS = KeyShape<G, D>;
     using VS = ValueShape<D>;
     constexpr int RB = 2 * D;  // bytes per fp16 token row
+    constexpr int KT = key_warp_tokens(G);
     if (item < it.key_items) {
         const unsigned u = item;  // item >= 0: unsigned division by the power of two kQ is a shift
         const int qs = u % KS::kQ, g = (u / KS::kQ) % it.ng, bh = (u / KS::kQ) / it.ng;
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(k.x) + ((long long)bh * k.x_bh_stride + g * G) * RB +
+        const int r0 = g * G + half * KT;  // first token of this warp's share
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(k.x) + ((long long)bh * k.x_bh_stride + r0) * RB +
                              qs * (KS::kCh * 2);
         constexpr int CPR = KS::kNOc;  // 16-byte chunks per token row
 #pragma unroll
-        for (int i = lane; i < G * CPR; i += 32) {  // G rows x CPR chunks
+        for (int i = lane; i < KT * CPR; i += 32) {  // KT rows x CPR chunks
             const int row = i / CPR, col = i % CPR;
-            const bool ok = g * G + row < k.n_flush;
+            const bool ok = r0 + row < k.n_flush;
             cp_async16(st + ((row + KS::kPad * (row / KS::kTPP)) * CPR + col) * 16,
                        ok ? (const void*)(src + row * RB + col * 16) : (const void*)src, ok);
         }
-    } else {
-        const unsigned vi = item - it.key_items;
+    } else if (G != 128 || vi_in >= 0) {
+        const unsigned vi = vi_in;
         const int t0 = (vi % it.nv) * VS::kRows, bh = vi / it.nv;
         const uint8_t* src = reinterpret_cast<const uint8_t*>(v.x) + ((long long)bh * v.x_bh_stride + t0) * RB;
 #pragma unroll
@@ -347,17 +355,23 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
 }
 
 // keys: lane = part * kNOc + oc; part owns tokens [8 part, 8 part + 8) of the
-// group, oc owns 8 channels of this item's channel slice. FAKE: write the
-// fake-quantized fp16 rows to a.fq instead of codes, scales and zeros.
+// warp's share of the group, oc owns 8 channels of this item's channel slice.
+// At G = 128 the warp holds tokens half * 64 .. of the group, and the two
+// warps of a pair (warp, warp ^ 1) exchange their column minima and maxima
+// through xchg (32 words per warp; named barrier bar_id over the pair's 64
+// threads) before the scales; the half-0 warp stores the scales and zeros.
+// FAKE: write the fake-quantized fp16 rows to a.fq instead of codes, scales
+// and zeros.
 template <int BITS, int MODE, int G, int D>
-__device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st, int lane) {
+__device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, int item, int half, uint32_t* xchg,
+                                         int warp, const uint8_t* st, int lane) {
     constexpr bool FAKE = (MODE & 1) != 0, HS = (MODE & 2) != 0;  // fake quantization; fp16 scales
     using KS = KeyShape<G, D>;
     const unsigned u = item;
     const int qs = u % KS::kQ, g = (u / KS::kQ) % it.ng, bh = (u / KS::kQ) / it.ng;
     const int oc = lane % KS::kNOc, part = lane / KS::kNOc;
     const int octet = qs * KS::kNOc + oc;
-    const int t0 = g * G + part * KS::kTPP;
+    const int t0 = g * G + half * key_warp_tokens(G) + part * KS::kTPP;
     const int nv = min(KS::kTPP, a.n_flush - t0);  // may be <= 0 in a ragged last group
     const uint4* xs = reinterpret_cast<const uint4*>(st) + (part * (KS::kTPP + KS::kPad)) * KS::kNOc + oc;  // row stride kNOc
 
@@ -385,6 +399,23 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
             mx[k] = __hmax2(mx[k], u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(mx[k]), o)));
         }
     }
+    if (G == 128) {  // the pair's other half of the group
+        uint32_t* mine = xchg + warp * 32 + oc * 8;
+        const uint32_t* theirs = xchg + (warp ^ 1) * 32 + oc * 8;
+        if (part == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                mine[k] = h2_as_u32(mn[k]);
+                mine[4 + k] = h2_as_u32(mx[k]);
+            }
+        }
+        named_barrier(1 + (warp >> 1), 64);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            mn[k] = __hmin2(mn[k], u32_as_h2(theirs[k]));
+            mx[k] = __hmax2(mx[k], u32_as_h2(theirs[4 + k]));
+        }
+    }
     float z[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -392,12 +423,12 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         z[2 * k] = canon(lo.x);
         z[2 * k + 1] = canon(lo.y);
     }
-    // the part lanes of a column compute its 8 scales: 2 each (4 parts), 1 each
-    // (8 parts), or 1 each in parts 0..7 and again in parts 8..15 (16 parts)
-    constexpr int CPP = KS::kNPart >= 8 ? 1 : 8 / KS::kNPart;
+    // the part lanes of a column compute its 8 scales: 2 each (4 parts) or 1
+    // each (8 parts)
+    constexpr int CPP = 8 / KS::kNPart;
     float my_s[CPP], my_r[CPP];
     {
-        const int ch0 = CPP == 1 ? (part & 7) : part * CPP;  // first channel of the octet this lane scales
+        const int ch0 = part * CPP;  // first channel of the octet this lane scales
         __half2 hx = mx[0], hn = mn[0];                      // the half2 pair holding it (and its neighbour)
 #pragma unroll
         for (int k = 1; k < 4; ++k)
@@ -438,7 +469,7 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
         for (int i = 0; i < nv; ++i) frow[i * (D / 8)] = fake8<BITS, HS>(xs[i * KS::kNOc], z2, r2, s, clip);
         return;
     }
-    if (part == 0) {
+    if (part == 0 && half == 0) {
         const long long m = ((long long)bh * (a.s_cap / G) + a.s_off / G + g) * D + octet * 8;
         store_scales8<HS>(a.scale, m, s);
         uint4 zp;
@@ -486,12 +517,12 @@ __device__ __forceinline__ void minmax_tree(const uint4 (&x)[N], __half2& m2, __
 // half of the same row's group) (G = 128). Min/max, scale and codes of a
 // group stay in its lane(s); one code store per group or half group.
 template <int BITS, int MODE, int G, int D>
-__device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
+__device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, int vi_in, const uint8_t* st,
                                            int lane) {
     constexpr bool FAKE = (MODE & 1) != 0, HS = (MODE & 2) != 0;  // fake quantization; fp16 scales
     using VS = ValueShape<D>;
     static_assert(G <= D, "a value group lies within one token row");
-    const unsigned vi = item - it.key_items;
+    const unsigned vi = vi_in;
     const int t0 = (vi % it.nv) * VS::kRows, bh = vi / it.nv;
     const int row = lane % VS::kRows, jp = lane / VS::kRows;
     const bool valid = t0 + row < a.n_flush;
@@ -717,20 +748,35 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
 }
 
 // Keys, values, or both: warp w of the grid handles items w, w + W, ... of the
-// list [key items | value items] (W = total warps).
+// list [key items | value items] (W = total warps). At G = 128 the unit is a
+// warp pair (warps 2p, 2p + 1 of a CTA): pair w of the grid handles units
+// w, w + W, ... of the list [key items | value item pairs]; both warps of a
+// pair walk the same units, so they meet at the same key-item barriers.
 template <int BITS, int MODE, int G, int D>
-__global__ void __launch_bounds__(kThreads, blocks_per_sm<G>()) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kStageBytes = Stage<G>::kBytes;
     uint8_t* const base = smem + warp * 2 * kStageBytes;
-    const int total = it.key_items + it.val_items;
-    const int stride = gridDim.x * (kThreads / 32);
-    int item = blockIdx.x * (kThreads / 32) + warp;
+    constexpr bool kPair = G == 128;
+    const int half = kPair ? warp & 1 : 0;
+    const int per_cta = kPair ? kThreads / 64 : kThreads / 32;        // units a CTA walks at a time
+    const int unit0 = blockIdx.x * per_cta + (kPair ? warp >> 1 : warp);
+    const int total = it.key_items + (kPair ? (it.val_items + 1) / 2 : it.val_items);
+    const int stride = gridDim.x * per_cta;
+    uint32_t* const xchg = reinterpret_cast<uint32_t*>(smem + (kThreads / 32) * 2 * kStageBytes);
+    // value item of unit u for this warp, or -1 (a pair's second warp past the last value item)
+    auto value_of = [&](int u) {
+        if (!kPair) return u - it.key_items;
+        const int vi = 2 * (u - it.key_items) + half;
+        return vi < it.val_items ? vi : -1;
+    };
+    int item = unit0;
     pdl_wait();
-    if (item < total) fetch_item<G, D>(k, v, it, item, base, lane);
+    if (item < total) fetch_item<G, D>(k, v, it, item, half, value_of(item), base, lane);
     cp_async_commit();
-    if (item + stride < total) fetch_item<G, D>(k, v, it, item + stride, base + kStageBytes, lane);
+    if (item + stride < total) fetch_item<G, D>(k, v, it, item + stride, half, value_of(item + stride),
+                                                base + kStageBytes, lane);
     cp_async_commit();
     pdl_trigger();
     for (int n = 0; item < total; item += stride, ++n) {
@@ -741,11 +787,16 @@ __global__ void __launch_bounds__(kThreads, blocks_per_sm<G>()) flush_kernel(Flu
             if (item < it.key_items) key_item_g32<BITS, MODE>(k, it, item, S, lane);
             else value_item_g32<BITS, MODE>(v, it, item, S, lane);
         } else {
-            if (item < it.key_items) key_item<BITS, MODE, G, D>(k, it, item, S, lane);
-            else value_item<BITS, MODE, G, D>(v, it, item, S, lane);
+            if (item < it.key_items) {
+                key_item<BITS, MODE, G, D>(k, it, item, half, xchg + (n & 1) * (kThreads / 32) * 32, warp, S, lane);
+            } else {
+                const int vi = value_of(item);
+                if (!kPair || vi >= 0) value_item<BITS, MODE, G, D>(v, it, vi, S, lane);
+            }
         }
         __syncwarp();
-        if (item + 2 * stride < total) fetch_item<G, D>(k, v, it, item + 2 * stride, S, lane);
+        if (item + 2 * stride < total)
+            fetch_item<G, D>(k, v, it, item + 2 * stride, half, value_of(item + 2 * stride), S, lane);
         cp_async_commit();
     }
 }
@@ -754,19 +805,21 @@ template <int BITS, int MODE, int G, int D>
 cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
     static int grid_cap = 0;
     static bool configured = false;  // benign race: every caller sets the same values
-    const int smem = (kThreads / 32) * 2 * Stage<G>::kBytes;
+    const int smem = (kThreads / 32) * 2 * Stage<G>::kBytes + (G == 128 ? kXchgBytes : 0);
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, MODE, G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             sms = 152;
-        grid_cap = sms * blocks_per_sm<G>();
+        grid_cap = sms * kBlocksPerSm;
         configured = true;
     }
-    const long long total = (long long)it.key_items + it.val_items;
+    // units: items, or at G = 128 key items and value item pairs, each for a warp pair
+    const long long total = (long long)it.key_items + (G == 128 ? (it.val_items + 1) / 2 : it.val_items);
     if (total <= 0) return cudaSuccess;
-    long long blocks = (total + 3) / 4;
+    const int per_cta = G == 128 ? kThreads / 64 : kThreads / 32;
+    long long blocks = (total + per_cta - 1) / per_cta;
     if (blocks > grid_cap) blocks = grid_cap;
     return launch_pdl(flush_kernel<BITS, MODE, G, D>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
 }
