@@ -33,11 +33,12 @@
 //    check per 8 elements sends the rare near-tie element to an exact IEEE
 //    division (out of line). Byte permutes pack 8 codes per 32-bit word.
 //  * work is cut into 4 KB items (a key group's G tokens x 2048 / G channels,
-//    or 2048 / D value rows; at G = 128 an 8 KB key item of 128 tokens x 32
-//    channels, so its row pieces are 64 bytes, not 32); each warp walks the
-//    items with a grid stride, staging two at a time in shared memory with
-//    cp.async, so the copy of the next item overlaps the quantization of the
-//    current one; the key loop takes two token rows per trip.
+//    or 2048 / D value rows; at G = 128 a key item of 128 tokens x 32
+//    channels, 64-byte row pieces, is split over a warp pair, 64 tokens per
+//    warp); each warp walks the items with a grid stride, staging two at a
+//    time in shared memory with cp.async, so the copy of the next item
+//    overlaps the quantization of the current one; the key loop takes two
+//    token rows per trip.
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
