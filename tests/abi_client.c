@@ -9,6 +9,7 @@
  * My LLM Exactly 0% Faster", "The full end-to-end record" (559 -> 512,
  * 2059 -> 2016, 8209 -> 8160 at residual_length = group_size = 32).
  */
+#include <stddef.h>
 #include <stdio.h>
 
 #include "kivi.h"
@@ -59,5 +60,23 @@ int main(void)
     printf("plan_qwen8b %d %d %d %d\n", (int)st, info[0], info[1], info[5]); /* status, pair kernel, splits, tiles */
     st = kivi_decode_plan_info(1, 32, 8, 2080, 158, 128, 32, 4 | KIVI_SCALE_F16, info);
     printf("plan_qwen8b_f16s %d %d\n", (int)st, info[0]);
+
+    /* the layer cache: the struct's layout as C sees it, and its checks
+       (never-dereferenced 16-byte aligned addresses) */
+    printf("cache_layout %zu %zu %zu %zu %zu\n", sizeof(kivi_cache), offsetof(kivi_cache, kcodes),
+           offsetof(kivi_cache, S_q), offsetof(kivi_cache, store_written), offsetof(kivi_cache, res_off));
+    void* a = (void*)256;
+    kivi_cache c = {8, 128, 32, 4, 128, 256, 160, a, (float*)a, a, a, (float*)a, a, a, a, 0, 0, 0, 0};
+    n = -7;
+    st = kivi_cache_prefill(&c, a, a, 0, 0, &n, NULL);
+    printf("cache_prefill_nothing %d %d\n", (int)st, n);
+    c.res_off = 100;
+    c.n_res = 61;
+    st = kivi_cache_append(&c, a, a, 1, 1, &n, NULL);
+    printf("cache_window_past_end %d %d %d\n", (int)st, c.n_res, c.res_off);
+    c.res_off = 0;
+    c.n_res = 0;
+    printf("cache_decode_bad_batch %d\n",
+           (int)kivi_cache_decode(&c, a, 2, 32, 8, 0.088f, (float*)a, a, (size_t)1 << 30, NULL));
     return 0;
 }

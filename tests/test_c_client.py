@@ -52,6 +52,19 @@ def test_c_client_argument_checks(client):
     assert int(client["workspace_init_null"]) == INVALID
 
 
+def test_c_client_cache(client):
+    """The kivi_cache struct has the same layout in C and in the Python
+    binding, and its calls check before launching."""
+    import ctypes
+    import kivi_kv_cache_gb300 as kv
+    S = kv._CacheStruct
+    assert [int(x) for x in client["cache_layout"].split()] == [
+        ctypes.sizeof(S), S.kcodes.offset, S.S_q.offset, S.store_written.offset, S.res_off.offset]
+    assert client["cache_prefill_nothing"] == "%d 0" % OK
+    assert client["cache_window_past_end"] == "%d 61 100" % INVALID  # rows 100 .. 160 past a 160-row window
+    assert int(client["cache_decode_bad_batch"]) == INVALID           # B * Hkv != BH
+
+
 def test_c_client_plan_info(client):
     # the qwen8b decode (2080 packed + 158 fp16 tokens = 65 + 10 tiles per KV
     # head) takes the warp-pair kernel, planned for 152 SMs without a device;
