@@ -119,7 +119,8 @@ constexpr bool kBalance = KIVI_DECODE_BALANCE != 0;
 #define KIVI_DECODE_SHORT_RUNS 1
 #endif
 constexpr bool kShortRuns = KIVI_DECODE_SHORT_RUNS != 0;
-constexpr long long kShortRunTiles = 8;  // longest warp run the 2-warp plan serves
+constexpr long long kShortRunTiles = 8;       // longest warp run the 2-warp plan serves
+constexpr long long kShortRunMaxSplits = 24;  // most splits per head group it takes
 
 bool mma_group(int gq) { return gq == 1 || gq == 2 || gq == 4; }
 
@@ -205,7 +206,10 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool 
         // split would: 2-warp CTAs (8 per SM) fill one wave with more splits
         // per head group, so its warps' runs are shorter (B=16 x 3072 tokens:
         // 27.1 -> 24.6 us). At equal or nearly equal runs the extra partials
-        // and CTA merges cost more than they save, so the plan stays.
+        // and CTA merges cost more than they save, so the plan stays; so do
+        // plans that would need more than 24 splits per head group, whose
+        // merges read too many partials (B=1 x 65536: 147 splits of 2 warps
+        // took 37.4 us against 31.2 us).
         const long long S = sm_count();
         const long long slots = (long long)(16 / p.warps_per_cta) * S;
         const long long ctas = heads * p.n_split;
@@ -213,6 +217,7 @@ DecodePlan make_plan(int B, int Hkv, int Hq, int S_q, int n_res, int bits, bool 
         const long long run = ((ctas + slots - 1) / slots) * tpw;  // tiles a warp slot runs
         long long n2 = 8 * S / heads;
         if (n2 > p.n_tiles) n2 = p.n_tiles;
+        if (n2 > kShortRunMaxSplits) n2 = kShortRunMaxSplits;
         if (n2 >= 1) {
             const long long tps2 = (p.n_tiles + n2 - 1) / n2;
             const long long run2 = (tps2 + 1) / 2;

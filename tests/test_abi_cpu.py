@@ -267,6 +267,9 @@ def test_decode_plan_rules(L):
     for S_q, n_res in ((1920, 128), (3456, 128)):  # one wave, runs nearly as short already: unchanged
         assert kv.kivi_decode_plan_info(16, 32, 8, S_q, n_res)["warps_per_cta"] == 4
     assert kv.kivi_decode_plan_info(32, 32, 8, 4032, 64)["warps_per_cta"] == 4  # long runs: unchanged
+    for B, S_q in ((1, 65408), (2, 32640), (6, 2944)):  # a 2-warp plan would need more than 24 splits
+        p = kv.kivi_decode_plan_info(B, 32, 8, S_q, 128)
+        assert p["warps_per_cta"] != 2 or p["n_split"] <= 24, (B, S_q, p)
     # the qwen8b decode takes the warp-pair kernel; stores of another group
     # size or head dim, or with fp16 scales, the one-warp-per-tile kernel
     assert kv.kivi_decode_plan_info(1, 32, 8, 2080, 158)["pair_kernel"] == 1
