@@ -63,6 +63,7 @@ MIN_OP_MS = 50.0
 # (with the group size a _gNN suffix names)
 PROFILE_CASES = {
     "flush_long2bit": ("flush", 0, 0, 0, 2),
+    "flush_long2bit_g64": ("flush", 0, 0, 0, 2),
     "flush_long2bit_g128": ("flush", 0, 0, 0, 2),
     "flush_long2bit_f16s": ("flush", 0, 0, 0, 2),
     "flush_qwen8b": ("flush", 0, 0, 0, 4),
