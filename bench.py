@@ -17,8 +17,9 @@ Inputs rotate through a pool of independent instances whose total size is
 several times the L2 cache, so no step finds its inputs in L2. Steps are
 captured in CUDA graphs of 8 consecutive steps on 8 distinct instances; the
 timed region replays them (K steps in all) between two CUDA events. Each op's
-average launch duration is timed the same way on graphs of 8 launches of that
-op alone, over at least 256 launches and 50 ms of device time.
+launch duration is timed on graphs of 8 launches of that op alone: the median
+of 21 samples per op, taken in turn with the other ops, at least 256 launches
+and 50 ms of device time per op in all.
 
 On one GPU the same JSON line also carries, each timed on its own:
   * "qwen8b": the Qwen3-8B-like single-layer step (2238-token prompt, 4-bit);
@@ -53,10 +54,12 @@ if ROOT not in sys.path:
 
 METRIC = "KIVI flush/dequant/decode-attend HBM GB/s (% of peak); decode tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # HBM3e nominal, quoted beside the measured peak
 GRAPH_STEPS = 8
 GRAPH_BRANCHES = 4  # parallel stream branches per timed graph (two steps each)
 MIN_OP_LAUNCHES = 256
 MIN_OP_MS = 50.0
+OP_ROUNDS = 21  # interleaved timing samples per op of the step (the median is reported)
 
 
 # --profile-case NAME: (op kind, B, S_q, n_res, bits); flush cases use the named workload
@@ -437,17 +440,35 @@ class StepBench:
         torch.cuda.synchronize()
         return start.elapsed_time(end)
 
-    def op_times(self):
-        """Mean device ms per launch of each op: graphs of GRAPH_STEPS
+    def op_times(self, rounds=OP_ROUNDS):
+        """Device ms per launch of each op: the median of `rounds` samples per
+        op, taken in turn (flush, append, dequant, decode, flush, ...). A
+        sample is CUDA events around replays of graphs of GRAPH_STEPS
         launches of the op alone on consecutive instances of the pool, with
-        the step's launch configuration."""
-        op_ms = {}
+        the step's launch configuration; each sample takes at least
+        1/rounds of MIN_OP_LAUNCHES launches and of MIN_OP_MS."""
+        import torch
+        graphs, reps = {}, {}
         for op in OPS:
             gs = [capture(lambda j=j, op=op: [self.insts[j * GRAPH_STEPS + t].op(op) for t in range(GRAPH_STEPS)])
                   for j in range(self.pool // GRAPH_STEPS)]
-            op_ms[op] = time_graphs(gs, GRAPH_STEPS)
-            del gs
-        return op_ms
+            per_graph = max(time_graphs(gs, GRAPH_STEPS, min_launches=1, min_ms=0.0) * GRAPH_STEPS, 1e-4)
+            reps[op] = max(len(gs), math.ceil(MIN_OP_LAUNCHES / (rounds * GRAPH_STEPS)),
+                           math.ceil(MIN_OP_MS / (rounds * per_graph)))
+            graphs[op] = gs
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        samples = {op: [] for op in OPS}
+        for _ in range(rounds):
+            for op in OPS:
+                gs, n = graphs[op], reps[op]
+                e0.record()
+                for i in range(n):
+                    gs[i % len(gs)].replay()
+                e1.record()
+                torch.cuda.synchronize()
+                samples[op].append(e0.elapsed_time(e1) / (n * GRAPH_STEPS))
+        del graphs
+        return {op: statistics.median(samples[op]) for op in OPS}
 
     def summary(self, op_ms, peak, steps=None, elapsed_ms=None, world=1):
         w = self.w
@@ -710,7 +731,7 @@ def run_gb300(args, rank, world, local_rank):
     achieved = ob[dom] / (op_ms[dom] * 1e-3) / 1e9
     traffic = read_traffic(OP_KERNEL_FILES[dom], dom, w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
-                "peak_kind": peak_kind + " hbm_gbs (copy, burst)", "unit": "GB/s",
+                "peak_kind": peak_kind + " hbm_gbs (copy, burst)", "unit": "GB/s", "nominal_peak": NOMINAL_HBM_GBS,
                 "frac": round(achieved / peak, 4),
                 "traffic": None if traffic is None else traffic["read"] + traffic["write"],
                 "traffic_read": None if traffic is None else traffic["read"],
@@ -824,8 +845,9 @@ def run_gb300(args, rank, world, local_rank):
         "gpu_launches": sum(LAUNCHES.values()) * args.steps,
         "clocks": clock,
         "peak_hbm_gbs": peak,
-        "per_op_timing": "CUDA events around graphs of %d back-to-back launches of the op on distinct instances, "
-                         "at least %d launches and %.0f ms per op" % (GRAPH_STEPS, MIN_OP_LAUNCHES, MIN_OP_MS),
+        "per_op_timing": "median of %d samples per op taken in turn with the other ops; a sample is CUDA events "
+                         "around graphs of %d back-to-back launches of the op on distinct instances; at least %d "
+                         "launches and %.0f ms per op" % (OP_ROUNDS, GRAPH_STEPS, MIN_OP_LAUNCHES, MIN_OP_MS),
     }
     line.update(extra)
     return line
