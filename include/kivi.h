@@ -109,6 +109,18 @@ const char* kivi_status_string(kivi_status status);
 int kivi_version(void);
 
 /*
+ * Waits that ran out. The flush stages its items of group size 32 and head
+ * dim 128 with bulk tensor copies, each completing on a shared-memory
+ * barrier that the warp polls a bounded number of times (well over a
+ * second). A poll that runs out adds one to a device-wide count, and that
+ * warp leaves its remaining items undone (their outputs are unspecified).
+ * *count (host pointer) receives the count; reset != 0 sets it back to zero.
+ * It is zero in correct operation. Synchronizes the device. Errors:
+ * INVALID_ARG if count is NULL; CUDA if the device copy fails.
+ */
+kivi_status kivi_wait_timeouts(unsigned int* count, int reset);
+
+/*
  * Flush plan ([F] "What we're actually optimizing": the newest
  * residual_length tokens stay fp16 and fresh tokens are quantized in a batch
  * once enough accumulate). Given a residual window holding n_res tokens,

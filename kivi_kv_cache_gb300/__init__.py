@@ -18,7 +18,7 @@ import threading
 
 __all__ = [
     "KiviError", "KiviStore", "lib", "library_path",
-    "kivi_status_string", "kivi_version", "kivi_flush_count",
+    "kivi_status_string", "kivi_version", "kivi_wait_timeouts", "kivi_flush_count",
     "kivi_flush_keys", "kivi_flush_values", "kivi_flush_kv", "kivi_dequant", "kivi_dequant_kv",
     "kivi_residual_append", "kivi_residual_compact", "kivi_residual_append_kv", "kivi_residual_compact_kv",
     "kivi_fake_quant_keys", "kivi_fake_quant_values", "kivi_fake_quant_kv",
@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
         sig = {
             "kivi_status_string": ([I], ctypes.c_char_p),
             "kivi_version": ([], I),
+            "kivi_wait_timeouts": ([ctypes.POINTER(ctypes.c_uint), I], I),
             "kivi_flush_count": ([I, I, I], I),
             "kivi_flush_keys": ([P, I, I, I, I, I, I, I, P, P, P, I, I, IP, P], I),
             "kivi_flush_values": ([P, I, I, I, I, I, I, I, P, P, P, I, I, IP, P], I),
@@ -124,6 +125,14 @@ def kivi_status_string(status: int) -> str:
 
 def kivi_version() -> int:
     return lib().kivi_version()
+
+
+def kivi_wait_timeouts(reset: bool = False) -> int:
+    """Bounded waits on a bulk copy that ran out since the last reset (zero in
+    correct operation); synchronizes the device."""
+    n = ctypes.c_uint(0)
+    _check("kivi_wait_timeouts", lib().kivi_wait_timeouts(ctypes.byref(n), 1 if reset else 0))
+    return n.value
 
 
 def kivi_flush_count(n_res: int, residual_length: int, group_size: int = 32) -> int:

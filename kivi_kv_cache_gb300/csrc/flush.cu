@@ -36,9 +36,14 @@
 //    or 2048 / D value rows; at G = 128 a key item of 128 tokens x 32
 //    channels, 64-byte row pieces, is split over a warp pair, 64 tokens per
 //    warp); each warp walks the items with a grid stride, staging two at a
-//    time in shared memory with cp.async, so the copy of the next item
-//    overlaps the quantization of the current one; the key loop takes two
-//    token rows per trip.
+//    time in shared memory, so the copy of the next item overlaps the
+//    quantization of the current one; the key loop takes two token rows per
+//    trip. At G = 32 and D = 128 one lane stages an item with bulk tensor
+//    copies (TMA: one 32 x 64 key box, or two 16 x 64 value boxes in the
+//    128-byte swizzle) that complete on the stage's shared-memory barrier;
+//    other shapes stage with per-lane 16-byte cp.async.
+#include <cuda.h>  // CUtensorMap (the encoder is taken from the driver at run time)
+
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
@@ -289,6 +294,59 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// --- bulk tensor copies (TMA) with shared-memory barrier completion, for the
+// G = 32, D = 128 items: one elected lane starts a 4 KB copy, the warp waits
+// on the stage's barrier. Every wait is bounded (one second of the global
+// timer): a wait that runs out counts itself in g_wait_timeouts and the warp
+// stops (the count is read through kivi_wait_timeouts; it is zero unless a
+// copy never completes).
+__device__ unsigned int g_wait_timeouts = 0;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// box of the 3-d tensor map at element coordinates (x, y, z) into shared dst
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// true once the barrier's phase of the given parity has completed (all lanes
+// agree); false if it has not within kWaitLimitNs
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    bool done = mbar_try(bar, parity);
+    if (!done) {
+        const unsigned long long t0 = global_ns();
+        while (!(done = mbar_try(bar, parity)) && global_ns() - t0 < kWaitLimitNs) {
+        }
+    }
+    return __all_sync(0xffffffffu, done);
+}
+
 struct Items {
     int key_items;   // BH * ng * (D / key item channels)
     int val_items;   // BH * ceil(n_flush / value item rows)
@@ -352,6 +410,27 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
             const bool ok = t0 + row < v.n_flush;
             cp_async16(st + row * RB + ((col ^ (row & 7)) << 4), ok ? (const void*)(src + i * 16) : (const void*)src, ok);
         }
+    }
+}
+
+// Stage item `item` of group size 32 and head dim 128 by bulk tensor copies
+// (called by one lane): a key item is the 32 x 64 box (tokens x channels) at
+// channel 64 * half of its group, stored as plain 128-byte rows; a value item
+// is the two 16 x 64 boxes of its 16 rows, channels 0-63 at st and 64-127 at
+// st + 2048, each in the 128-byte swizzle (16-byte chunk c of row r at
+// c ^ (r & 7); st is 1024-byte aligned). Rows past n_flush arrive as zeros.
+__device__ __forceinline__ void fetch_item_tma(const CUtensorMap* kmap, const CUtensorMap* vmap, const Items& it,
+                                               int item, uint8_t* st, uint32_t bar) {
+    const uint32_t dst = smem_u32(st);
+    mbar_expect_tx(bar, 4096);
+    if (item < it.key_items) {
+        const int half = item & 1, g = (item >> 1) % it.ng, bh = (item >> 1) / it.ng;
+        tma_load_3d(dst, kmap, 64 * half, g * kG, bh, bar);
+    } else {
+        const int vi = item - it.key_items;
+        const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
+        tma_load_3d(dst, vmap, 0, t0, bh, bar);
+        tma_load_3d(dst + 2048, vmap, 64, t0, bh, bar);
     }
 }
 
@@ -689,7 +768,9 @@ __device__ __forceinline__ void key_item_g32(const FlushArgs& a, const Items& it
 // G = 32 values: lane = 16 jp + row; the lane quantizes the groups j = 2 jp and
 // 2 jp + 1 (32 channels each) of row `row` of the item: min/max, scale and
 // codes of a whole group in one lane, no shuffles, one 16-byte code store
-// (4-bit) per group.
+// (4-bit) per group. The stage holds the item as fetch_item_tma leaves it
+// (channel halves 2 KB apart, swizzled rows), so the 8 lanes of a quarter
+// warp read 8 different 16-byte bank groups.
 template <int BITS, int MODE>
 __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& it, int item, const uint8_t* st,
                                            int lane) {
@@ -698,14 +779,14 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
     const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
     const int row = lane & 15, jp = lane >> 4;
     if (t0 + row >= a.n_flush) return;
-    const uint4* xs = reinterpret_cast<const uint4*>(st + row * 256);
+    const uint4* xs = reinterpret_cast<const uint4*>(st + 2048 * jp + row * 128);  // this lane's 64 channels
     const long long grow = (long long)bh * a.s_cap + a.s_off + t0 + row;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int j = 2 * jp + e;
         uint4 x[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) x[k] = xs[(4 * j + k) ^ (row & 7)];
+        for (int k = 0; k < 4; ++k) x[k] = xs[(4 * e + k) ^ (row & 7)];
         // min / max as a tree (min and max of fp16 are exact, so the order is free)
         __half2 mk[4], xk[4];
 #pragma unroll
@@ -753,12 +834,32 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
 // warp pair (warps 2p, 2p + 1 of a CTA): pair w of the grid handles units
 // w, w + W, ... of the list [key items | value item pairs]; both warps of a
 // pair walk the same units, so they meet at the same key-item barriers.
+// At G = 32 and D = 128 the stages are filled by bulk tensor copies (kmap:
+// the keys, boxes of 32 tokens x 64 channels; vmap: the values, boxes of 16
+// tokens x 64 channels, 128-byte swizzle), each completing on its stage's
+// shared-memory barrier; other shapes stage with cp.async (the maps are
+// unused).
 template <int BITS, int MODE, int G, int D>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs k, FlushArgs v, Items it) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
+    flush_kernel(FlushArgs k, FlushArgs v, Items it, const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    constexpr bool kTma = G == 32 && D == kD;
+    // the swizzled value boxes want 1024-byte aligned stages
+    uint8_t* const smem = kTma ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kStageBytes = Stage<G>::kBytes;
     uint8_t* const base = smem + warp * 2 * kStageBytes;
+    // kTma: this warp's two stage barriers (8 bytes each) after all stages
+    const uint32_t bar0 = smem_u32(smem + (kThreads / 32) * 2 * kStageBytes) + warp * 16;
+    if (kTma) {
+        if (lane == 0) {
+            mbar_init(bar0);
+            mbar_init(bar0 + 8);
+            mbar_init_fence();
+        }
+        __syncwarp();
+    }
     constexpr bool kPair = G == 128;
     const int half = kPair ? warp & 1 : 0;
     const int per_cta = kPair ? kThreads / 64 : kThreads / 32;        // units a CTA walks at a time
@@ -774,15 +875,34 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs
     };
     int item = unit0;
     pdl_wait();
-    if (item < total) fetch_item<G, D>(k, v, it, item, half, value_of(item), base, lane);
-    cp_async_commit();
-    if (item + stride < total) fetch_item<G, D>(k, v, it, item + stride, half, value_of(item + stride),
-                                                base + kStageBytes, lane);
-    cp_async_commit();
+    if (kTma) {
+        if (lane == 0) {
+            if (item < total) fetch_item_tma(&kmap, &vmap, it, item, base, bar0);
+            if (item + stride < total) fetch_item_tma(&kmap, &vmap, it, item + stride, base + kStageBytes, bar0 + 8);
+        }
+    } else {
+        if (item < total) fetch_item<G, D>(k, v, it, item, half, value_of(item), base, lane);
+        cp_async_commit();
+        if (item + stride < total) fetch_item<G, D>(k, v, it, item + stride, half, value_of(item + stride),
+                                                    base + kStageBytes, lane);
+        cp_async_commit();
+    }
     pdl_trigger();
     for (int n = 0; item < total; item += stride, ++n) {
         uint8_t* S = base + (n & 1) * kStageBytes;  // stage n mod 2
-        cp_async_wait1();
+        if (kTma) {
+            // use n >> 1 of this stage's barrier completes its phase of parity (n >> 1) & 1
+            if (!mbar_wait(bar0 + 8 * (n & 1), (n >> 1) & 1)) {
+                // gave up on this copy: count it, wait (bounded) for this and
+                // the other stage's copy, and stop
+                if (lane == 0) atomicAdd(&g_wait_timeouts, 1u);
+                mbar_wait(bar0 + 8 * (n & 1), (n >> 1) & 1);
+                if (item + stride < total) mbar_wait(bar0 + 8 * ((n + 1) & 1), ((n + 1) >> 1) & 1);
+                return;
+            }
+        } else {
+            cp_async_wait1();
+        }
         __syncwarp();
         if (G == 32 && D == kD) {  // the generic item code at G = 32 measured 0.7 % slower than this form
             if (item < it.key_items) key_item_g32<BITS, MODE>(k, it, item, S, lane);
@@ -796,17 +916,61 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) flush_kernel(FlushArgs
             }
         }
         __syncwarp();
-        if (item + 2 * stride < total)
-            fetch_item<G, D>(k, v, it, item + 2 * stride, half, value_of(item + 2 * stride), S, lane);
-        cp_async_commit();
+        if (kTma) {
+            // every lane has read stage S: refill it
+            if (lane == 0 && item + 2 * stride < total)
+                fetch_item_tma(&kmap, &vmap, it, item + 2 * stride, S, bar0 + 8 * (n & 1));
+        } else {
+            if (item + 2 * stride < total)
+                fetch_item<G, D>(k, v, it, item + 2 * stride, half, value_of(item + 2 * stride), S, lane);
+            cp_async_commit();
+        }
     }
+}
+
+// cuTensorMapEncodeTiled from the driver (looked up once; null if the driver
+// has none)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (EncodeTiledFn) nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// The tensor map of the flush input a.x ([BH, x_bh_stride, D] fp16, tokens
+// [0, n_flush) of each head; rows past n_flush read as zeros) with boxes of
+// `rows` tokens x 64 channels. a.x is 16-byte aligned and the row and head
+// strides (2D and 2D x_bh_stride bytes) are multiples of 16, as the copy needs.
+cudaError_t encode_rows_map(CUtensorMap* m, const FlushArgs& a, unsigned rows, CUtensorMapSwizzle swizzle) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.n_flush, (cuuint64_t)a.BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.D * 2, (cuuint64_t)a.x_bh_stride * a.D * 2};
+    const cuuint32_t box[3] = {64, rows, 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(a.x), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int BITS, int MODE, int G, int D>
 cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
     static int grid_cap = 0;
     static bool configured = false;  // benign race: every caller sets the same values
-    const int smem = (kThreads / 32) * 2 * Stage<G>::kBytes + (G == 128 ? kXchgBytes : 0);
+    constexpr bool kTma = G == 32 && D == kD;
+    // kTma: two stage barriers per warp and room to align the stages to 1024 bytes
+    const int smem = (kThreads / 32) * 2 * Stage<G>::kBytes + (G == 128 ? kXchgBytes : 0) +
+                     (kTma ? (kThreads / 32) * 16 + 1024 : 0);
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, MODE, G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
@@ -822,7 +986,15 @@ cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it
     const int per_cta = G == 128 ? kThreads / 64 : kThreads / 32;
     long long blocks = (total + per_cta - 1) / per_cta;
     if (blocks > grid_cap) blocks = grid_cap;
-    return launch_pdl(flush_kernel<BITS, MODE, G, D>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it);
+    CUtensorMap kmap{}, vmap{};
+    if (kTma) {
+        cudaError_t e = cudaSuccess;
+        if (it.key_items > 0) e = encode_rows_map(&kmap, k, kG, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (e == cudaSuccess && it.val_items > 0) e = encode_rows_map(&vmap, v, 16, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(flush_kernel<BITS, MODE, G, D>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it, kmap,
+                      vmap);
 }
 
 // Pointers of heads [h0, h0 + nh) of a flush.
@@ -912,6 +1084,15 @@ cudaError_t launch_flush_kv(const FlushArgs& k, const FlushArgs& v, int bits, cu
 cudaError_t launch_fake_quant(const FlushArgs& k, const FlushArgs& v, bool do_k, bool do_v, int bits,
                               cudaStream_t stream) {
     return launch_flush_impl(k, v, do_k, do_v, bits, stream);
+}
+
+cudaError_t read_wait_timeouts(unsigned int* count, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(unsigned int));
+    if (e == cudaSuccess && reset) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(unsigned int));
+    }
+    return e;
 }
 
 }  // namespace kivi

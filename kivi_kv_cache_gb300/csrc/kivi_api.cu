@@ -397,6 +397,11 @@ const char* kivi_status_string(kivi_status s) {
 
 int kivi_version(void) { return 100; }
 
+kivi_status kivi_wait_timeouts(unsigned int* count, int reset) {
+    if (count == nullptr) return KIVI_ERR_INVALID_ARG;
+    return from_cuda(kivi::read_wait_timeouts(count, reset != 0));
+}
+
 int kivi_flush_count(int n_res, int residual_length, int group_size) {
     if (n_res < 0 || residual_length < 0 || group_size <= 0) return -1;
     if (n_res == 0) return 0;

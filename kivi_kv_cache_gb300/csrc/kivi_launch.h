@@ -160,6 +160,9 @@ cudaError_t launch_flush_kv(const FlushArgs& k, const FlushArgs& v, int bits, cu
 // their KIVI reconstructions in fq; keys if do_k, values if do_v, one launch
 cudaError_t launch_fake_quant(const FlushArgs& k, const FlushArgs& v, bool do_k, bool do_v, int bits,
                               cudaStream_t stream);
+// The count of bounded waits on a bulk copy that ran out (flush.cu), and
+// optionally reset it. Synchronous.
+cudaError_t read_wait_timeouts(unsigned int* count, bool reset);
 cudaError_t launch_dequant(int axis, const DequantArgs& a, int bits, cudaStream_t stream);
 cudaError_t launch_dequant_kv(const DequantArgs& k, const DequantArgs& v, int bits, cudaStream_t stream);
 // src1/res1 may be null (one tensor); otherwise both pairs are handled in one launch

@@ -176,6 +176,10 @@ def test_fake_quant_argument_checks(L):
                                 ctypes.byref(n), None) == INVALID
 
 
+def test_wait_timeouts_rejects_null(L):
+    assert L.kivi_wait_timeouts(None, 0) == INVALID
+
+
 @no_gpu
 def test_workspace_init_rejects_null(L):
     assert L.kivi_decode_workspace_init(None, 0, None) == OK      # nothing to zero
