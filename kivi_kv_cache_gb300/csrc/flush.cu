@@ -38,10 +38,11 @@
 //    warp); each warp walks the items with a grid stride, staging two at a
 //    time in shared memory, so the copy of the next item overlaps the
 //    quantization of the current one; the key loop takes two token rows per
-//    trip. At G = 32 and D = 128 one lane stages an item with bulk tensor
-//    copies (TMA: one 32 x 64 key box, or two 16 x 64 value boxes in the
-//    128-byte swizzle) that complete on the stage's shared-memory barrier;
-//    other shapes stage with per-lane 16-byte cp.async.
+//    trip. Long flushes at G = 32 and D = 128 stage an item from one lane
+//    with bulk tensor copies (TMA: one 32 x 64 key box, or two 16 x 64 value
+//    boxes in the 128-byte swizzle) that complete on the stage's
+//    shared-memory barrier, at 6 CTAs per SM; everything else stages with
+//    per-lane 16-byte cp.async at 4 (launch_items says which and why).
 #include <cuda.h>  // CUtensorMap (the encoder is taken from the driver at run time)
 
 #include "kivi_device.cuh"
@@ -274,12 +275,12 @@ struct Stage {
 #define KIVI_FLUSH_TMA_BLOCKS_PER_SM 6
 #endif
 // resident CTAs per SM the grid is sized for (and the register bound): the
-// bulk-copy kernel (G = 32, D = 128) needs no per-lane copy addressing and
-// fits 6 CTAs in 80 registers without spills (measured: 6 faster than 5 and
-// 4); the others run 4
-template <int G, int D>
+// bulk-copy kernel needs no per-lane copy addressing and fits 6 CTAs in 80
+// registers without spills (measured: 6 faster than 5 and 4 on long
+// flushes); the cp.async kernel runs 4
+template <bool TMA>
 constexpr int blocks_per_sm() {
-    return G == 32 && D == kD ? KIVI_FLUSH_TMA_BLOCKS_PER_SM : KIVI_FLUSH_BLOCKS_PER_SM;
+    return TMA ? KIVI_FLUSH_TMA_BLOCKS_PER_SM : KIVI_FLUSH_BLOCKS_PER_SM;
 }
 // G = 128: per CTA, the warps' minima and maxima for the pair exchange, two
 // slots (alternate items) of 32 words per warp
@@ -344,6 +345,10 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     return done != 0;
+}
+// fetch a tensor map into the descriptor cache ahead of its first copy
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 // true once the barrier's phase of the given parity has completed (all lanes
 // agree); false if it has not within kWaitLimitNs
@@ -418,7 +423,10 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
         for (int i = lane; i < 256; i += 32) {  // kRows rows x kCpr chunks, chunk c of row r at c ^ (r & 7)
             const int row = i / VS::kCpr, col = i % VS::kCpr;
             const bool ok = t0 + row < v.n_flush;
-            cp_async16(st + row * RB + ((col ^ (row & 7)) << 4), ok ? (const void*)(src + i * 16) : (const void*)src, ok);
+            // G = 32, D = 128: the layout fetch_item_tma leaves (64-channel halves 2 KB apart, 128-byte rows)
+            const int off = G == 32 && D == kD ? (col >> 3) * 2048 + row * 128 + (((col & 7) ^ (row & 7)) << 4)
+                                               : row * RB + ((col ^ (row & 7)) << 4);
+            cp_async16(st + off, ok ? (const void*)(src + i * 16) : (const void*)src, ok);
         }
     }
 }
@@ -844,17 +852,18 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
 // warp pair (warps 2p, 2p + 1 of a CTA): pair w of the grid handles units
 // w, w + W, ... of the list [key items | value item pairs]; both warps of a
 // pair walk the same units, so they meet at the same key-item barriers.
-// At G = 32 and D = 128 the stages are filled by bulk tensor copies (kmap:
-// the keys, boxes of 32 tokens x 64 channels; vmap: the values, boxes of 16
-// tokens x 64 channels, 128-byte swizzle), each completing on its stage's
-// shared-memory barrier; other shapes stage with cp.async (the maps are
-// unused).
-template <int BITS, int MODE, int G, int D>
-__global__ void __launch_bounds__(kThreads, blocks_per_sm<G, D>())
+// TMA (G = 32 and D = 128 only): the stages are filled by bulk tensor copies
+// (kmap: the keys, boxes of 32 tokens x 64 channels; vmap: the values, boxes
+// of 16 tokens x 64 channels, 128-byte swizzle), each completing on its
+// stage's shared-memory barrier; otherwise they are filled with cp.async
+// (the maps are unused).
+template <int BITS, int MODE, int G, int D, bool TMA>
+__global__ void __launch_bounds__(kThreads, blocks_per_sm<TMA>())
     flush_kernel(FlushArgs k, FlushArgs v, Items it, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap) {
+    static_assert(!TMA || (G == 32 && D == kD), "bulk copies stage the G = 32, D = 128 items only");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    constexpr bool kTma = G == 32 && D == kD;
+    constexpr bool kTma = TMA;
     // the swizzled value boxes want 1024-byte aligned stages
     uint8_t* const smem = kTma ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -863,6 +872,10 @@ __global__ void __launch_bounds__(kThreads, blocks_per_sm<G, D>())
     // kTma: this warp's two stage barriers (8 bytes each) after all stages
     const uint32_t bar0 = smem_u32(smem + (kThreads / 32) * 2 * kStageBytes) + warp * 16;
     if (kTma) {
+        if (threadIdx.x == 0) {  // the maps this launch uses, while the previous kernel may still run
+            if (it.key_items > 0) prefetch_map(&kmap);
+            if (it.val_items > 0) prefetch_map(&vmap);
+        }
         if (lane == 0) {
             mbar_init(bar0);
             mbar_init(bar0 + 8);
@@ -973,21 +986,29 @@ cudaError_t encode_rows_map(CUtensorMap* m, const FlushArgs& a, unsigned rows, C
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int BITS, int MODE, int G, int D>
-cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
+int sm_count_cached() {
+    static const int sms = [] {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 152;
+        return n;
+    }();
+    return sms;
+}
+
+template <int BITS, int MODE, int G, int D, bool TMA>
+cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
     static int grid_cap = 0;
     static bool configured = false;  // benign race: every caller sets the same values
-    constexpr bool kTma = G == 32 && D == kD;
+    constexpr bool kTma = TMA;
     // kTma: two stage barriers per warp and room to align the stages to 1024 bytes
     const int smem = (kThreads / 32) * 2 * Stage<G>::kBytes + (G == 128 ? kXchgBytes : 0) +
                      (kTma ? (kThreads / 32) * 16 + 1024 : 0);
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, MODE, G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, MODE, G, D, TMA>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            sms = 152;
-        grid_cap = sms * blocks_per_sm<G, D>();
+        grid_cap = sm_count_cached() * blocks_per_sm<TMA>();
         configured = true;
     }
     // units: items, or at G = 128 key items and value item pairs, each for a warp pair
@@ -1003,8 +1024,25 @@ cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it
         if (e == cudaSuccess && it.val_items > 0) e = encode_rows_map(&vmap, v, 16, CU_TENSOR_MAP_SWIZZLE_128B);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(flush_kernel<BITS, MODE, G, D>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it, kmap,
-                      vmap);
+    return launch_pdl(flush_kernel<BITS, MODE, G, D, TMA>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it,
+                      kmap, vmap);
+}
+
+// The bulk-copy kernel takes flushes (not fake quantization) of G = 32 and
+// D = 128 with more items than one wave of the cp.async grid: measured on
+// the long 2-bit flush 29.5 us against 31.2; the cp.async kernel keeps fake
+// quantization (54.7 us against 56.1 at 4 and 60.9 at 6 CTAs per SM) and
+// launches of at most one item per warp (the qwen8b flush, 5.7 against
+// 6.1 us), whose time is one item's latency.
+template <int BITS, int MODE, int G, int D>
+cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
+    constexpr bool kCanTma = G == 32 && D == kD && (MODE & 1) == 0;
+    if constexpr (kCanTma) {
+        const long long units = (long long)it.key_items + it.val_items;
+        if (units > (long long)sm_count_cached() * blocks_per_sm<false>() * (kThreads / 32))
+            return launch_items_t<BITS, MODE, G, D, true>(k, v, it, stream);
+    }
+    return launch_items_t<BITS, MODE, G, D, false>(k, v, it, stream);
 }
 
 // Pointers of heads [h0, h0 + nh) of a flush.
