@@ -260,13 +260,10 @@ __device__ __forceinline__ void store_scales8(float* scale, long long m, const f
 __host__ __device__ constexpr int key_item_channels(int G) { return G == 128 ? 32 : 4096 / (2 * G); }
 __host__ __device__ constexpr int key_warp_tokens(int G) { return G == 128 ? 64 : G; }  // per warp
 
-// A stage holds one warp's share of an item (4 KB); with G > 32 a key item's
-// token parts are padded by one row (kNOc 16-byte chunks) so that the parts
-// of a quarter warp read different banks (32 / kNOc parts of kNOc * 16
-// bytes). Each warp has two stages.
+// A stage holds one warp's share of an item (4 KB). Each warp has two stages.
 template <int G>
 struct Stage {
-    static constexpr int kBytes = 4096 + (G > 32 ? 32 * 16 : 0);
+    static constexpr int kBytes = 4096;
 };
 #ifndef KIVI_FLUSH_BLOCKS_PER_SM
 #define KIVI_FLUSH_BLOCKS_PER_SM 4
@@ -300,9 +297,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool fill
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-// barrier over `threads` threads (a multiple of 32) with named barrier `id` (1..15)
-__device__ __forceinline__ void named_barrier(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+// barrier over `threads` threads (a multiple of 32) with named barrier ID (1..15)
+template <int ID>
+__device__ __forceinline__ void named_barrier(int threads) {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(threads) : "memory");
 }
 
 // --- bulk tensor copies (TMA) with shared-memory barrier completion, for the
@@ -370,8 +368,11 @@ struct Items {
 };
 
 // Key items of group size G and head dim D: G tokens x kCh channels (a warp
-// takes key_warp_tokens(G) of them); a lane owns kTPP tokens x 8 channels,
-// lane = part * kNOc + oc.
+// takes key_warp_tokens(G) of them, staged as plain rows of kCh channels); a
+// lane owns kTPP tokens x 8 channels, lane = part * kNOc + oc, and part p
+// the rows p, p + kNPart, p + 2 kNPart, ... of the warp's share. With
+// 64-byte rows (kNOc = 4) the two parts of a quarter warp then read rows of
+// both parities, eight different 16-byte bank groups, with no padding rows.
 template <int G, int D>
 struct KeyShape {
     static constexpr int kCh = key_item_channels(G);  // channels of an item: 64, 32, 32
@@ -379,7 +380,6 @@ struct KeyShape {
     static constexpr int kNPart = 32 / kNOc;          // token parts: 4, 8 or 8
     static constexpr int kTPP = key_warp_tokens(G) / kNPart;  // tokens per part: 8
     static constexpr int kQ = D / kCh;                // items per key group: 1 to 16
-    static constexpr int kPad = G > 32 ? 1 : 0;       // pad rows per part in shared memory
     static_assert(kQ >= 1, "a key item spans at most the head dim");
 };
 
@@ -412,8 +412,8 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
         for (int i = lane; i < KT * CPR; i += 32) {  // KT rows x CPR chunks
             const int row = i / CPR, col = i % CPR;
             const bool ok = r0 + row < k.n_flush;
-            cp_async16(st + ((row + KS::kPad * (row / KS::kTPP)) * CPR + col) * 16,
-                       ok ? (const void*)(src + row * RB + col * 16) : (const void*)src, ok);
+            cp_async16(st + (row * CPR + col) * 16, ok ? (const void*)(src + row * RB + col * 16) : (const void*)src,
+                       ok);
         }
     } else if (G != 128 || vi_in >= 0) {
         const unsigned vi = vi_in;
@@ -423,9 +423,9 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
         for (int i = lane; i < 256; i += 32) {  // kRows rows x kCpr chunks, chunk c of row r at c ^ (r & 7)
             const int row = i / VS::kCpr, col = i % VS::kCpr;
             const bool ok = t0 + row < v.n_flush;
-            // G = 32, D = 128: the layout fetch_item_tma leaves (64-channel halves 2 KB apart, 128-byte rows)
-            const int off = G == 32 && D == kD ? (col >> 3) * 2048 + row * 128 + (((col & 7) ^ (row & 7)) << 4)
-                                               : row * RB + ((col ^ (row & 7)) << 4);
+            // D = 128: the layout fetch_item_tma leaves (64-channel halves 2 KB apart, 128-byte rows)
+            const int off = D == kD ? (col >> 3) * 2048 + row * 128 + (((col & 7) ^ (row & 7)) << 4)
+                                    : row * RB + ((col ^ (row & 7)) << 4);
             cp_async16(st + off, ok ? (const void*)(src + i * 16) : (const void*)src, ok);
         }
     }
@@ -452,8 +452,9 @@ __device__ __forceinline__ void fetch_item_tma(const CUtensorMap* kmap, const CU
     }
 }
 
-// keys: lane = part * kNOc + oc; part owns tokens [8 part, 8 part + 8) of the
-// warp's share of the group, oc owns 8 channels of this item's channel slice.
+// keys: lane = part * kNOc + oc; part owns the tokens part, part + kNPart, ...
+// of the warp's share of the group (kTPP of them), oc owns 8 channels of this
+// item's channel slice.
 // At G = 128 the warp holds tokens half * 64 .. of the group, and the two
 // warps of a pair (warp, warp ^ 1) exchange their column minima and maxima
 // through xchg (32 words per warp; named barrier bar_id over the pair's 64
@@ -469,9 +470,12 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     const int qs = u % KS::kQ, g = (u / KS::kQ) % it.ng, bh = (u / KS::kQ) / it.ng;
     const int oc = lane % KS::kNOc, part = lane / KS::kNOc;
     const int octet = qs * KS::kNOc + oc;
-    const int t0 = g * G + half * key_warp_tokens(G) + part * KS::kTPP;
-    const int nv = min(KS::kTPP, a.n_flush - t0);  // may be <= 0 in a ragged last group
-    const uint4* xs = reinterpret_cast<const uint4*>(st) + (part * (KS::kTPP + KS::kPad)) * KS::kNOc + oc;  // row stride kNOc
+    const int tw = g * G + half * key_warp_tokens(G);  // first token of the warp's share
+    const int t0 = tw + part;                           // this lane's first token
+    const int nw = a.n_flush - tw;                      // valid tokens of the share (ragged last group)
+    const int nv = nw <= part ? 0 : min(KS::kTPP, (nw - part + KS::kNPart - 1) / KS::kNPart);
+    constexpr int kStep = KS::kNPart;                   // tokens between a lane's rows
+    const uint4* xs = reinterpret_cast<const uint4*>(st) + part * KS::kNOc + oc;  // row i at xs[i * kStep * kNOc]
 
     const __half2 pinf = __half2half2(__ushort_as_half(0x7c00));
     const __half2 ninf = __half2half2(__ushort_as_half(0xfc00));
@@ -480,7 +484,7 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
 #pragma unroll
     for (int i = 0; i < KS::kTPP; ++i) {
         if (i < nv) {
-            const uint4 x = xs[i * KS::kNOc];
+            const uint4 x = xs[i * kStep * KS::kNOc];
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -507,7 +511,8 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
                 mine[4 + k] = h2_as_u32(mx[k]);
             }
         }
-        named_barrier(1 + (warp >> 1), 64);
+        if (warp >> 1) named_barrier<2>(64);  // compile-time ids: 3 hardware barriers, not 16
+        else named_barrier<1>(64);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             mn[k] = __hmin2(mn[k], u32_as_h2(theirs[k]));
@@ -564,7 +569,8 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     if (FAKE) {
         uint4* frow = reinterpret_cast<uint4*>(a.fq + ((long long)bh * a.fq_bh_stride + t0) * D) + octet;
 #pragma unroll 1
-        for (int i = 0; i < nv; ++i) frow[i * (D / 8)] = fake8<BITS, HS>(xs[i * KS::kNOc], z2, r2, s, clip);
+        for (int i = 0; i < nv; ++i)
+            frow[i * kStep * (D / 8)] = fake8<BITS, HS>(xs[i * kStep * KS::kNOc], z2, r2, s, clip);
         return;
     }
     if (part == 0 && half == 0) {
@@ -580,11 +586,11 @@ __device__ __forceinline__ void key_item(const FlushArgs& a, const Items& it, in
     constexpr int ROWB = D * BITS / 8;
     uint8_t* crow = a.codes + ((long long)bh * a.s_cap + a.s_off + t0) * ROWB + octet * BITS;
     auto store_row = [&](int i, uint32_t packed) {
-        if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * ROWB) = packed;
-        else *reinterpret_cast<uint16_t*>(crow + i * ROWB) = (uint16_t)packed;
+        if (BITS == 4) *reinterpret_cast<uint32_t*>(crow + i * kStep * ROWB) = packed;
+        else *reinterpret_cast<uint16_t*>(crow + i * kStep * ROWB) = (uint16_t)packed;
     };
 #pragma unroll (kKeyUnroll)
-    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, HS>(xs[i * KS::kNOc], z2, r2, s, clip));
+    for (int i = 0; i < nv; ++i) store_row(i, quant8<BITS, HS>(xs[i * kStep * KS::kNOc], z2, r2, s, clip));
 }
 
 // min and max of the 8 fp16 of each vector of x, as half2 (min and max of fp16
@@ -625,16 +631,19 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
     const int row = lane % VS::kRows, jp = lane / VS::kRows;
     const bool valid = t0 + row < a.n_flush;
     if (G != 128 && !valid) return;  // (G = 128: both lanes of a row leave together below)
-    const uint4* xs = reinterpret_cast<const uint4*>(st + row * (2 * D));
+    // D = 128: the stage holds 64-channel halves 2 KB apart in 128-byte rows
+    // (the layout fetch_item_tma leaves); other D: whole rows
+    const uint4* xs = reinterpret_cast<const uint4*>(D == kD ? st + 2048 * jp + row * 128 : st + row * (2 * D));
     const long long grow = (long long)bh * a.s_cap + a.s_off + t0 + row;
     constexpr int NG = G == 32 ? 2 : 1;      // groups (or half groups) per lane
     constexpr int NVEC = G == 32 ? 4 : 8;    // 16-byte vectors per group (or half group) in this lane
 #pragma unroll
     for (int e = 0; e < NG; ++e) {
         const int cv = (64 * jp + (G == 32 ? 32 * e : 0)) / 8;  // first vector of this lane's channels
+        const int cl = D == kD ? cv - 8 * jp : cv;               // ... within the staged row piece
         uint4 x[NVEC];
 #pragma unroll
-        for (int k = 0; k < NVEC; ++k) x[k] = xs[(cv + k) ^ (row & 7)];
+        for (int k = 0; k < NVEC; ++k) x[k] = xs[(cl + k) ^ (row & 7)];
         __half2 m2, x2;
         minmax_tree<NVEC>(x, m2, x2);
         if (G == 128) {  // the other half of the group sits in lane ^ kRows (same row)
@@ -971,14 +980,16 @@ EncodeTiledFn encode_tiled() {
 
 // The tensor map of the flush input a.x ([BH, x_bh_stride, D] fp16, tokens
 // [0, n_flush) of each head; rows past n_flush read as zeros) with boxes of
-// `rows` tokens x 64 channels. a.x is 16-byte aligned and the row and head
-// strides (2D and 2D x_bh_stride bytes) are multiples of 16, as the copy needs.
-cudaError_t encode_rows_map(CUtensorMap* m, const FlushArgs& a, unsigned rows, CUtensorMapSwizzle swizzle) {
+// `rows` tokens x `cols` channels (cols * 2 bytes a multiple of 16). a.x is
+// 16-byte aligned and the row and head strides (2D and 2D x_bh_stride bytes)
+// are multiples of 16, as the copy needs.
+cudaError_t encode_rows_map(CUtensorMap* m, const FlushArgs& a, unsigned cols, unsigned rows,
+                            CUtensorMapSwizzle swizzle) {
     const EncodeTiledFn fn = encode_tiled();
     if (fn == nullptr) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.n_flush, (cuuint64_t)a.BH};
     const cuuint64_t strides[2] = {(cuuint64_t)a.D * 2, (cuuint64_t)a.x_bh_stride * a.D * 2};
-    const cuuint32_t box[3] = {64, rows, 1};
+    const cuuint32_t box[3] = {cols, rows, 1};
     const cuuint32_t elem[3] = {1, 1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(a.x), dims, strides, box, elem,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1020,8 +1031,8 @@ cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& 
     CUtensorMap kmap{}, vmap{};
     if (kTma) {
         cudaError_t e = cudaSuccess;
-        if (it.key_items > 0) e = encode_rows_map(&kmap, k, kG, CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (e == cudaSuccess && it.val_items > 0) e = encode_rows_map(&vmap, v, 16, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (it.key_items > 0) e = encode_rows_map(&kmap, k, 64, kG, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (e == cudaSuccess && it.val_items > 0) e = encode_rows_map(&vmap, v, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(flush_kernel<BITS, MODE, G, D, TMA>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it,
@@ -1030,16 +1041,19 @@ cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& 
 
 // The bulk-copy kernel takes flushes (not fake quantization) of G = 32 and
 // D = 128 with more items than one wave of the cp.async grid: measured on
-// the long 2-bit flush 29.5 us against 31.2; the cp.async kernel keeps fake
-// quantization (54.7 us against 56.1 at 4 and 60.9 at 6 CTAs per SM) and
+// the long 2-bit flush 29.5 us against 31.2. The cp.async kernel keeps fake
+// quantization (54.7 us against 56.1 at 4 and 60.9 at 6 CTAs per SM),
 // launches of at most one item per warp (the qwen8b flush, 5.7 against
-// 6.1 us), whose time is one item's latency.
+// 6.1 us: one item's latency) and the other group sizes (bulk copies of the
+// 64 x 32 key boxes measured 34.2 against 32.5 us at G = 64, and 36.0
+// against 36.0 at G = 128, whose warp pairs' exchange sets the pace).
 template <int BITS, int MODE, int G, int D>
 cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
-    constexpr bool kCanTma = G == 32 && D == kD && (MODE & 1) == 0;
+    constexpr bool kCanTma = D == kD && G == 32 && (MODE & 1) == 0;
     if constexpr (kCanTma) {
-        const long long units = (long long)it.key_items + it.val_items;
-        if (units > (long long)sm_count_cached() * blocks_per_sm<false>() * (kThreads / 32))
+        const long long units = (long long)it.key_items + (G == 128 ? (it.val_items + 1) / 2 : it.val_items);
+        const int per_cta = G == 128 ? kThreads / 64 : kThreads / 32;
+        if (units > (long long)sm_count_cached() * blocks_per_sm<false>() * per_cta)
             return launch_items_t<BITS, MODE, G, D, true>(k, v, it, stream);
     }
     return launch_items_t<BITS, MODE, G, D, false>(k, v, it, stream);
