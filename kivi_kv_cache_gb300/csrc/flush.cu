@@ -38,9 +38,9 @@
 //    warp); each warp walks the items with a grid stride, staging two at a
 //    time in shared memory, so the copy of the next item overlaps the
 //    quantization of the current one; the key loop takes two token rows per
-//    trip. Long flushes at G = 32 and D = 128 stage an item from one lane
-//    with bulk tensor copies (TMA: one 32 x 64 key box, or two 16 x 64 value
-//    boxes in the 128-byte swizzle) that complete on the stage's
+//    trip. Long flushes at G = 32 stage an item from one lane with bulk
+//    tensor copies (TMA: one 32 x 64 key box, or D / 64 value boxes of 64
+//    channels in the 128-byte swizzle) that complete on the stage's
 //    shared-memory barrier, at 6 CTAs per SM; everything else stages with
 //    per-lane 16-byte cp.async at 4 (launch_items says which and why).
 #include <cuda.h>  // CUtensorMap (the encoder is taken from the driver at run time)
@@ -420,35 +420,38 @@ __device__ __forceinline__ void fetch_item(const FlushArgs& k, const FlushArgs& 
         const int t0 = (vi % it.nv) * VS::kRows, bh = vi / it.nv;
         const uint8_t* src = reinterpret_cast<const uint8_t*>(v.x) + ((long long)bh * v.x_bh_stride + t0) * RB;
 #pragma unroll
-        for (int i = lane; i < 256; i += 32) {  // kRows rows x kCpr chunks, chunk c of row r at c ^ (r & 7)
+        for (int i = lane; i < 256; i += 32) {  // kRows rows x kCpr chunks
             const int row = i / VS::kCpr, col = i % VS::kCpr;
             const bool ok = t0 + row < v.n_flush;
-            // D = 128: the layout fetch_item_tma leaves (64-channel halves 2 KB apart, 128-byte rows)
-            const int off = D == kD ? (col >> 3) * 2048 + row * 128 + (((col & 7) ^ (row & 7)) << 4)
-                                    : row * RB + ((col ^ (row & 7)) << 4);
+            // the layout fetch_item_tma leaves: 64-channel pieces kRows * 128 bytes apart, 128-byte rows
+            const int off = (col >> 3) * (VS::kRows * 128) + row * 128 + (((col & 7) ^ (row & 7)) << 4);
             cp_async16(st + off, ok ? (const void*)(src + i * 16) : (const void*)src, ok);
         }
     }
 }
 
-// Stage item `item` of group size 32 and head dim 128 by bulk tensor copies
+// Stage item `item` of group size 32 and head dim D by bulk tensor copies
 // (called by one lane): a key item is the 32 x 64 box (tokens x channels) at
-// channel 64 * half of its group, stored as plain 128-byte rows; a value item
-// is the two 16 x 64 boxes of its 16 rows, channels 0-63 at st and 64-127 at
-// st + 2048, each in the 128-byte swizzle (16-byte chunk c of row r at
-// c ^ (r & 7); st is 1024-byte aligned). Rows past n_flush arrive as zeros.
+// channel 64 * (item mod D / 64) of its group, stored as plain 128-byte rows;
+// a value item is the D / 64 boxes of its kRows = 2048 / D rows, 64 channels
+// each, box j at st + j * kRows * 128 in the 128-byte swizzle (16-byte chunk
+// c of row r at c ^ (r & 7); st is 1024-byte aligned, and so is every box).
+// Rows past n_flush arrive as zeros.
+template <int D>
 __device__ __forceinline__ void fetch_item_tma(const CUtensorMap* kmap, const CUtensorMap* vmap, const Items& it,
                                                int item, uint8_t* st, uint32_t bar) {
+    constexpr int kQ = D / 64, kRows = ValueShape<D>::kRows;
     const uint32_t dst = smem_u32(st);
     mbar_expect_tx(bar, 4096);
     if (item < it.key_items) {
-        const int half = item & 1, g = (item >> 1) % it.ng, bh = (item >> 1) / it.ng;
-        tma_load_3d(dst, kmap, 64 * half, g * kG, bh, bar);
+        const unsigned u = item;
+        const int qs = u % kQ, g = (u / kQ) % it.ng, bh = (u / kQ) / it.ng;
+        tma_load_3d(dst, kmap, 64 * qs, g * kG, bh, bar);
     } else {
         const int vi = item - it.key_items;
-        const int t0 = (vi % it.nv) * 16, bh = vi / it.nv;
-        tma_load_3d(dst, vmap, 0, t0, bh, bar);
-        tma_load_3d(dst + 2048, vmap, 64, t0, bh, bar);
+        const int t0 = (vi % it.nv) * kRows, bh = vi / it.nv;
+#pragma unroll
+        for (int j = 0; j < kQ; ++j) tma_load_3d(dst + j * kRows * 128, vmap, 64 * j, t0, bh, bar);
     }
 }
 
@@ -631,16 +634,16 @@ __device__ __forceinline__ void value_item(const FlushArgs& a, const Items& it, 
     const int row = lane % VS::kRows, jp = lane / VS::kRows;
     const bool valid = t0 + row < a.n_flush;
     if (G != 128 && !valid) return;  // (G = 128: both lanes of a row leave together below)
-    // D = 128: the stage holds 64-channel halves 2 KB apart in 128-byte rows
-    // (the layout fetch_item_tma leaves); other D: whole rows
-    const uint4* xs = reinterpret_cast<const uint4*>(D == kD ? st + 2048 * jp + row * 128 : st + row * (2 * D));
+    // the stage holds 64-channel pieces kRows * 128 bytes apart in 128-byte
+    // rows (the layout fetch_item_tma leaves): this lane's piece jp
+    const uint4* xs = reinterpret_cast<const uint4*>(st + jp * (VS::kRows * 128) + row * 128);
     const long long grow = (long long)bh * a.s_cap + a.s_off + t0 + row;
     constexpr int NG = G == 32 ? 2 : 1;      // groups (or half groups) per lane
     constexpr int NVEC = G == 32 ? 4 : 8;    // 16-byte vectors per group (or half group) in this lane
 #pragma unroll
     for (int e = 0; e < NG; ++e) {
         const int cv = (64 * jp + (G == 32 ? 32 * e : 0)) / 8;  // first vector of this lane's channels
-        const int cl = D == kD ? cv - 8 * jp : cv;               // ... within the staged row piece
+        const int cl = cv - 8 * jp;                               // ... within the staged row piece
         uint4 x[NVEC];
 #pragma unroll
         for (int k = 0; k < NVEC; ++k) x[k] = xs[(cl + k) ^ (row & 7)];
@@ -861,16 +864,16 @@ __device__ __forceinline__ void value_item_g32(const FlushArgs& a, const Items& 
 // warp pair (warps 2p, 2p + 1 of a CTA): pair w of the grid handles units
 // w, w + W, ... of the list [key items | value item pairs]; both warps of a
 // pair walk the same units, so they meet at the same key-item barriers.
-// TMA (G = 32 and D = 128 only): the stages are filled by bulk tensor copies
-// (kmap: the keys, boxes of 32 tokens x 64 channels; vmap: the values, boxes
-// of 16 tokens x 64 channels, 128-byte swizzle), each completing on its
+// TMA (G = 32 only): the stages are filled by bulk tensor copies (kmap: the
+// keys, boxes of 32 tokens x 64 channels; vmap: the values, boxes of
+// 2048 / D tokens x 64 channels, 128-byte swizzle), each completing on its
 // stage's shared-memory barrier; otherwise they are filled with cp.async
 // (the maps are unused).
 template <int BITS, int MODE, int G, int D, bool TMA>
 __global__ void __launch_bounds__(kThreads, blocks_per_sm<TMA>())
     flush_kernel(FlushArgs k, FlushArgs v, Items it, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap) {
-    static_assert(!TMA || (G == 32 && D == kD), "bulk copies stage the G = 32, D = 128 items only");
+    static_assert(!TMA || G == 32, "bulk copies stage the items of group size 32 only");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     constexpr bool kTma = TMA;
     // the swizzled value boxes want 1024-byte aligned stages
@@ -909,8 +912,9 @@ __global__ void __launch_bounds__(kThreads, blocks_per_sm<TMA>())
     pdl_wait();
     if (kTma) {
         if (lane == 0) {
-            if (item < total) fetch_item_tma(&kmap, &vmap, it, item, base, bar0);
-            if (item + stride < total) fetch_item_tma(&kmap, &vmap, it, item + stride, base + kStageBytes, bar0 + 8);
+            if (item < total) fetch_item_tma<D>(&kmap, &vmap, it, item, base, bar0);
+            if (item + stride < total)
+                fetch_item_tma<D>(&kmap, &vmap, it, item + stride, base + kStageBytes, bar0 + 8);
         }
     } else {
         if (item < total) fetch_item<G, D>(k, v, it, item, half, value_of(item), base, lane);
@@ -951,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, blocks_per_sm<TMA>())
         if (kTma) {
             // every lane has read stage S: refill it
             if (lane == 0 && item + 2 * stride < total)
-                fetch_item_tma(&kmap, &vmap, it, item + 2 * stride, S, bar0 + 8 * (n & 1));
+                fetch_item_tma<D>(&kmap, &vmap, it, item + 2 * stride, S, bar0 + 8 * (n & 1));
         } else {
             if (item + 2 * stride < total)
                 fetch_item<G, D>(k, v, it, item + 2 * stride, half, value_of(item + 2 * stride), S, lane);
@@ -997,16 +1001,6 @@ cudaError_t encode_rows_map(CUtensorMap* m, const FlushArgs& a, unsigned cols, u
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int sm_count_cached() {
-    static const int sms = [] {
-        int dev = 0, n = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 152;
-        return n;
-    }();
-    return sms;
-}
-
 template <int BITS, int MODE, int G, int D, bool TMA>
 cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
     static int grid_cap = 0;
@@ -1019,7 +1013,7 @@ cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& 
         cudaError_t e = cudaFuncSetAttribute(flush_kernel<BITS, MODE, G, D, TMA>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        grid_cap = sm_count_cached() * blocks_per_sm<TMA>();
+        grid_cap = sm_count() * blocks_per_sm<TMA>();
         configured = true;
     }
     // units: items, or at G = 128 key items and value item pairs, each for a warp pair
@@ -1032,16 +1026,18 @@ cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& 
     if (kTma) {
         cudaError_t e = cudaSuccess;
         if (it.key_items > 0) e = encode_rows_map(&kmap, k, 64, kG, CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (e == cudaSuccess && it.val_items > 0) e = encode_rows_map(&vmap, v, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (e == cudaSuccess && it.val_items > 0)
+            e = encode_rows_map(&vmap, v, 64, ValueShape<D>::kRows, CU_TENSOR_MAP_SWIZZLE_128B);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(flush_kernel<BITS, MODE, G, D, TMA>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it,
                       kmap, vmap);
 }
 
-// The bulk-copy kernel takes flushes (not fake quantization) of G = 32 and
-// D = 128 with more items than one wave of the cp.async grid: measured on
-// the long 2-bit flush 29.5 us against 31.2. The cp.async kernel keeps fake
+// The bulk-copy kernel takes flushes (not fake quantization) of G = 32 with
+// more items than one wave of the cp.async grid: measured on the long 2-bit
+// flush 29.5 us against 31.2 (D = 128), 28.3 against 30.8 (D = 64) and 29.6
+// against 31.1 (D = 256). The cp.async kernel keeps fake
 // quantization (54.7 us against 56.1 at 4 and 60.9 at 6 CTAs per SM),
 // launches of at most one item per warp (the qwen8b flush, 5.7 against
 // 6.1 us: one item's latency) and the other group sizes (bulk copies of the
@@ -1049,11 +1045,11 @@ cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& 
 // against 36.0 at G = 128, whose warp pairs' exchange sets the pace).
 template <int BITS, int MODE, int G, int D>
 cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
-    constexpr bool kCanTma = D == kD && G == 32 && (MODE & 1) == 0;
+    constexpr bool kCanTma = G == 32 && (MODE & 1) == 0;
     if constexpr (kCanTma) {
         const long long units = (long long)it.key_items + (G == 128 ? (it.val_items + 1) / 2 : it.val_items);
         const int per_cta = G == 128 ? kThreads / 64 : kThreads / 32;
-        if (units > (long long)sm_count_cached() * blocks_per_sm<false>() * per_cta)
+        if (units > (long long)sm_count() * blocks_per_sm<false>() * per_cta)
             return launch_items_t<BITS, MODE, G, D, true>(k, v, it, stream);
     }
     return launch_items_t<BITS, MODE, G, D, false>(k, v, it, stream);
