@@ -1001,8 +1001,10 @@ cudaError_t encode_rows_map(CUtensorMap* m, const FlushArgs& a, unsigned cols, u
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// TMA: kmap and vmap describe k.x and v.x (encode_rows_map); otherwise unused.
 template <int BITS, int MODE, int G, int D, bool TMA>
-cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
+cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& it, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, cudaStream_t stream) {
     static int grid_cap = 0;
     static bool configured = false;  // benign race: every caller sets the same values
     constexpr bool kTma = TMA;
@@ -1022,14 +1024,6 @@ cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& 
     const int per_cta = G == 128 ? kThreads / 64 : kThreads / 32;
     long long blocks = (total + per_cta - 1) / per_cta;
     if (blocks > grid_cap) blocks = grid_cap;
-    CUtensorMap kmap{}, vmap{};
-    if (kTma) {
-        cudaError_t e = cudaSuccess;
-        if (it.key_items > 0) e = encode_rows_map(&kmap, k, 64, kG, CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (e == cudaSuccess && it.val_items > 0)
-            e = encode_rows_map(&vmap, v, 64, ValueShape<D>::kRows, CU_TENSOR_MAP_SWIZZLE_128B);
-        if (e != cudaSuccess) return e;
-    }
     return launch_pdl(flush_kernel<BITS, MODE, G, D, TMA>, dim3((unsigned)blocks), kThreads, smem, stream, k, v, it,
                       kmap, vmap);
 }
@@ -1042,17 +1036,22 @@ cudaError_t launch_items_t(const FlushArgs& k, const FlushArgs& v, const Items& 
 // launches of at most one item per warp (the qwen8b flush, 5.7 against
 // 6.1 us: one item's latency) and the other group sizes (bulk copies of the
 // 64 x 32 key boxes measured 34.2 against 32.5 us at G = 64, and 36.0
-// against 36.0 at G = 128, whose warp pairs' exchange sets the pace).
+// against 36.0 at G = 128, whose warp pairs' exchange sets the pace). The
+// bulk copies need the driver's tensor-map encoder: where it is missing, or
+// rejects a map, the cp.async kernel runs instead (the same results).
 template <int BITS, int MODE, int G, int D>
 cudaError_t launch_items(const FlushArgs& k, const FlushArgs& v, const Items& it, cudaStream_t stream) {
+    CUtensorMap kmap{}, vmap{};
     constexpr bool kCanTma = G == 32 && (MODE & 1) == 0;
     if constexpr (kCanTma) {
-        const long long units = (long long)it.key_items + (G == 128 ? (it.val_items + 1) / 2 : it.val_items);
-        const int per_cta = G == 128 ? kThreads / 64 : kThreads / 32;
-        if (units > (long long)sm_count() * blocks_per_sm<false>() * per_cta)
-            return launch_items_t<BITS, MODE, G, D, true>(k, v, it, stream);
+        const long long units = (long long)it.key_items + it.val_items;
+        if (units > (long long)sm_count() * blocks_per_sm<false>() * (kThreads / 32) &&
+            (it.key_items == 0 || encode_rows_map(&kmap, k, 64, kG, CU_TENSOR_MAP_SWIZZLE_NONE) == cudaSuccess) &&
+            (it.val_items == 0 ||
+             encode_rows_map(&vmap, v, 64, ValueShape<D>::kRows, CU_TENSOR_MAP_SWIZZLE_128B) == cudaSuccess))
+            return launch_items_t<BITS, MODE, G, D, true>(k, v, it, kmap, vmap, stream);
     }
-    return launch_items_t<BITS, MODE, G, D, false>(k, v, it, stream);
+    return launch_items_t<BITS, MODE, G, D, false>(k, v, it, kmap, vmap, stream);
 }
 
 // Pointers of heads [h0, h0 + nh) of a flush.
